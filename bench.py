@@ -1,0 +1,447 @@
+"""Benchmark of the OScaR INT2 decode path on GB300.
+
+One step = one decode step of one attention layer for the batch-48, 128K
+context workload (32 query / 8 KV heads, head_dim 128): rotate the queries,
+append the new token's key and value (flushing the full residual window to
+INT2 every 128 steps), then the fused INT2 dequant + inverse scaling +
+split-K attention and the log-sum-exp combine.  The packed cache (~4.35 GB
+read per step) is far larger than L2, so no flush between steps is needed.
+
+Prints one JSON line: value = device time per step (us, CUDA events over the
+timed steps, max over ranks); e2e = the same through the C ABI with the step's
+inputs copied from pinned host memory and the output read back every step;
+roofline = the fused decode call against the measured HBM copy bandwidth;
+cpu_baseline = the CPU oracle on a bounded sample, extrapolated.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import os
+
+# the CPU oracle leg is timed single-threaded (its BLAS calls must not fan out)
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+WORKLOAD = "batch48_128k"
+METRIC = "INT2 decode-attn µs/step & HBM GB/s (% of GB300 peak) at 128K ctx, batch 48"
+UNIT = "us/step"
+HERE = os.path.dirname(os.path.abspath(__file__))
+TRAFFIC_FILE = os.path.join(HERE, "profiles", "decode_int2_batch48_128k_traffic.json")
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1024)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-bf16", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=256)
+    return p.parse_args()
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _config(wl, S=None):
+    cfg = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": 128,
+           "context": wl.T0, "key_group": 32, "residual_window": 128,
+           "step": "rotate_q + append_kv (flush every 128) + fused INT2 decode + LSE combine",
+           "l2": "inputs larger than L2: ~4.35 GB packed cache read per step vs 129 MB L2",
+           "parallelism": "replicas (one independent layer cache per GPU)"}
+    if S is not None:
+        cfg["num_splits"] = S
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(f[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + f[0].split(".")[1]) if "." in f[0] else 0.0
+                rows.append({"t": ts, "sm": float(f[2]), "sm_max": float(f[3]),
+                             "power": float(f[4]) if f[4] not in ("[N/A]", "") else None,
+                             "hw_slowdown": f[6], "hw_thermal": f[7], "sw_thermal": f[8],
+                             "sw_power_cap": f[9]})
+            except (ValueError, IndexError):
+                continue
+        return rows
+
+
+def _clock_summary(rows, t0, t1):
+    inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05]
+    window = "timed"
+    if len(inside) < 3:
+        inside, window = rows, "benchmark run (timed region shorter than the sampling period)"
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    reasons = set()
+    for r in inside:
+        for k in ("hw_slowdown", "hw_thermal", "sw_thermal", "sw_power_cap"):
+            if r[k].lower().startswith("active"):
+                reasons.add(k)
+    return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+            "sm_max_mhz": max(r["sm_max"] for r in inside),
+            "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (bounded sample)
+# ---------------------------------------------------------------------------
+
+def _oracle_row_cache(wl, b, h, T_hist):
+    from oracle import oscar_oracle as O
+    kb = wl.k_bits([b], [h], 0, T_hist)[0, 0]
+    vb = wl.v_bits([b], [h], 0, T_hist)[0, 0]
+    return O.build_head_cache(kb[:wl.T0], vb[:wl.T0], wl.n_packed), kb, vb
+
+
+def oracle_step_time(wl, rows, n_steps, token_fraction=1.0):
+    """Seconds per (row, step) of the oracle decode step: rotate the row's
+    queries, append its new token, attend over its cache (optionally over the
+    first ``token_fraction`` of the packed tokens)."""
+    from oracle import oscar_oracle as O
+    g = wl.g
+    tau = 1.0 / math.sqrt(128)
+    times = []
+    for (b, h) in rows:
+        hc, kb, vb = _oracle_row_cache(wl, b, h, wl.T0 + n_steps)
+        if token_fraction < 1.0:
+            keep = max(32, int(hc.n_packed * token_fraction) // 32 * 32)
+            kq, vq = hc.packed_k(), hc.packed_v()
+            hc.k_codes = [O.QuantK(kq.codes[:keep], kq.step16[:keep // 32], kq.zero16[:keep // 32])]
+            hc.k_norm16 = [hc.packed_norm16()[:keep]]
+            hc.v_q = [O.QuantV(vq.codes[:keep], vq.step16[:keep], vq.zero16[:keep])]
+        qs = [wl.q_bits([b], range(h * g, (h + 1) * g), i)[0] for i in range(n_steps)]
+        t = time.perf_counter()
+        for i in range(n_steps):
+            qr = O.rotate_q(qs[i])
+            hc.append(kb[wl.T0 + i], vb[wl.T0 + i])
+            hc.decode(qr, tau)
+        times.append((time.perf_counter() - t) / n_steps)
+    return float(np.mean(times))
+
+
+def cpu_baseline(wl, budget_s=20.0):
+    rows = [(0, 0), (wl.B - 1, wl.Hkv - 1)]
+    t1 = oracle_step_time(wl, rows[:1], 1)
+    n = max(1, min(20, int(budget_s / max(t1, 1e-3) / len(rows))))
+    per = oracle_step_time(wl, rows, n)
+    total_rows = wl.B * wl.Hkv
+    return {"value": per * total_rows * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(rows)} of {total_rows} (sequence, KV head) rows x {n} decode steps "
+                      f"at full context, single thread; extrapolated x{total_rows} rows"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle as the timed program
+# ---------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    from int2_kv_cache_02_gb300 import workloads as W
+    if rank != 0:
+        return 0
+    wl = W.WORKLOADS[WORKLOAD]
+    total_rows = wl.B * wl.Hkv
+    steps = args.steps + args.warmup
+    # size each step so that the whole run stays within about two minutes
+    probe = oracle_step_time(wl, [(0, 0)], 1)
+    frac = min(1.0, (120.0 / max(steps, 1)) / max(probe, 1e-6))
+    frac = max(frac, 1.0 / 64)
+    from oracle import oscar_oracle as O
+    hc, kb, vb = _oracle_row_cache(wl, 0, 0, wl.T0 + steps)
+    keep = max(32, int(hc.n_packed * frac) // 32 * 32)
+    kq, vq = hc.packed_k(), hc.packed_v()
+    hc.k_codes = [O.QuantK(kq.codes[:keep], kq.step16[:keep // 32], kq.zero16[:keep // 32])]
+    hc.k_norm16 = [hc.packed_norm16()[:keep]]
+    hc.v_q = [O.QuantV(vq.codes[:keep], vq.step16[:keep], vq.zero16[:keep])]
+    g, tau = wl.g, 1.0 / math.sqrt(128)
+    qs = [wl.q_bits([0], range(g), i)[0] for i in range(steps)]
+    for i in range(args.warmup):
+        hc.append(kb[wl.T0 + i], vb[wl.T0 + i])
+        hc.decode(O.rotate_q(qs[i]), tau)
+    t = time.perf_counter()
+    for i in range(args.warmup, steps):
+        hc.append(kb[wl.T0 + i], vb[wl.T0 + i])
+        hc.decode(O.rotate_q(qs[i]), tau)
+    per = (time.perf_counter() - t) / max(args.steps, 1)
+    scale = total_rows * (wl.n_packed / keep)
+    value = per * scale * 1e6
+    sample = (f"1 of {total_rows} rows per step over the first {keep} of {wl.n_packed} packed "
+              f"tokens (+ residual), single thread; extrapolated x{scale:.1f}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": _config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def _algorithmic_bytes(wl, n_packed, n_res, S):
+    rows = wl.B * wl.Hkv
+    cache = rows * (n_packed * 86 + n_res * 514)
+    qo = 2 * wl.B * wl.Hq * 128 * 4                      # q' in, out
+    ws = 2 * wl.B * wl.Hq * (S + 1) * 132 * 4             # partials written and read
+    return cache + qo + ws
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sys.path.insert(0, HERE)
+    import __graft_entry__
+    __graft_entry__.build()
+    from int2_kv_cache_02_gb300 import oscar as L
+    from int2_kv_cache_02_gb300 import workloads as W
+
+    wl = W.WORKLOADS[WORKLOAD]
+    tau = 1.0 / math.sqrt(128)
+    W_, K_ = args.warmup, args.steps
+    E_ = args.e2e_steps
+    total_steps = W_ + K_ + 2 + E_
+    T_cap = wl.t_cap(total_steps - wl.steps)
+
+    # prompt: raw K, V drawn on the device, cache built through the library
+    K, V = W.draw_kv_cuda(wl, 0, wl.T0, device=dev)
+    cache = W.build_cache_cuda(wl, K, V, T_cap=T_cap, device=dev)
+    # per-step inputs, one contiguous slice per step
+    Kn, Vn = W.draw_kv_cuda(wl, wl.T0, total_steps, device=dev)
+    Kn = Kn.permute(2, 0, 1, 3).contiguous()
+    Vn = Vn.permute(2, 0, 1, 3).contiguous()
+    Q = torch.stack([W.draw_q_cuda(wl, i, device=dev) for i in range(total_steps)])
+    torch.cuda.synchronize()
+
+    S = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, wl.n_packed)
+    ws = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, T_cap, S), device=dev)
+    qr = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
+    out = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        L.rotate_q(Q[i], qr)
+        L.append_kv(cache, Kn[i], Vn[i], n_tok=1)
+        if ev is not None:
+            ev[0].record(stream)
+        L.decode_attention(cache, qr, wl.Hq, tau, out, ws, num_splits=S)
+        if ev is not None:
+            ev[1].record(stream)
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    vis = [v for v in vis.split(",") if v.strip().isdigit()]
+    sampler = ClockSampler(int(vis[local]) if local < len(vis) else local)
+    for i in range(W_):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ctx0 = (cache.n_packed, cache.n_res)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K_)]
+    flush_steps = []
+    launches0 = L.kernel_launches()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record(stream)
+    bytes_sum = 0
+    for j in range(K_):
+        if cache.n_res == 128:
+            flush_steps.append(j)
+        step(W_ + j, evs[j])
+        bytes_sum += _algorithmic_bytes(wl, cache.n_packed, cache.n_res, S)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = L.kernel_launches() - launches0
+    clock_rows = sampler.stop()
+    if L.device_status() != 0:
+        raise RuntimeError("a kernel recorded an error during the benchmark")
+
+    ms_total = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_step = ms_total / K_
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    dec_avg_ms = float(np.mean(dec_ms))
+    achieved = (bytes_sum / K_) / (dec_avg_ms * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers ----
+    pin = lambda t: t.cpu().pin_memory()
+    base = W_ + K_ + 2
+    Qh, Kh, Vh = pin(Q[base:base + E_]), pin(Kn[base:base + E_]), pin(Vn[base:base + E_])
+    outh = torch.empty((E_,) + tuple(out.shape), dtype=torch.float32).pin_memory()
+    qd, kd, vd = torch.empty_like(Q[0]), torch.empty_like(Kn[0]), torch.empty_like(Vn[0])
+    for i in range(2):  # untimed: touch the copy paths
+        qd.copy_(Qh[i], non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(E_):
+        qd.copy_(Qh[i], non_blocking=True)
+        kd.copy_(Kh[i], non_blocking=True)
+        vd.copy_(Vh[i], non_blocking=True)
+        L.rotate_q(qd, qr)
+        L.append_kv(cache, kd, vd, n_tok=1)
+        L.decode_attention(cache, qr, wl.Hq, tau, out, ws, num_splits=S)
+        outh[i].copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) / E_ * 1e3
+    h2d = (Qh[0].numel() * Qh.element_size() + Kh[0].numel() * Kh.element_size()
+           + Vh[0].numel() * Vh.element_size())
+    d2h = out.numel() * out.element_size()
+    if world > 1:
+        t = torch.tensor([e2e_us], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_us = float(t.item())
+
+    # ---- bf16 comparison kernel, same shape (context T0) ----
+    bf16 = None
+    if not args.no_bf16:
+        qb = Q[0]
+        S16 = 0
+        ws16 = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, wl.T0, 512),
+                                 device=dev)
+        o16 = torch.empty_like(out)
+        for _ in range(3):
+            L.bf16_decode_attention(qb, K, V, wl.B, wl.Hq, wl.Hkv, wl.T0, wl.T0, tau, o16, ws16,
+                                    num_splits=S16)
+        torch.cuda.synchronize()
+        reps = 20
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            L.bf16_decode_attention(qb, K, V, wl.B, wl.Hq, wl.Hkv, wl.T0, wl.T0, tau, o16, ws16,
+                                    num_splits=S16)
+        b.record(stream)
+        torch.cuda.synchronize()
+        bf_ms = a.elapsed_time(b) / reps
+        bf_bytes = wl.B * wl.Hkv * wl.T0 * 512
+        bf16 = {"us_per_call": bf_ms * 1e3, "GB/s": bf_bytes / (bf_ms * 1e-3) / 1e9,
+                "int2_decode_speedup": bf_ms / dec_avg_ms,
+                "note": "equal-shape bf16 split-K decode (B48, 32/8, 131072 tokens), "
+                        "25.8 GB of K,V per call"}
+
+    peaks = {}
+    try:
+        with open(os.path.join(HERE, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "of measured" if peak else "of fallback"
+    peak = peak or 6800.0
+    traffic = None
+    try:
+        with open(TRAFFIC_FILE) as f:
+            traffic = json.load(f).get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        traffic = None
+
+    line = {
+        "metric": METRIC, "value": ms_step * 1e3, "unit": UNIT, "n_gpus": world,
+        "steps": K_, "warmup": W_, "ms_per_step": ms_step, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "int2 codes; f16 tensor-core MMA (hi+lo split), f32 accumulate",
+        "data": "synthetic", "config": _config(wl, S),
+        "decode_tokens_per_s": world * wl.B / (ms_step * 1e-3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_src, "traffic": traffic,
+                     "kernel": "oscar_decode_attention (fused INT2 decode + LSE combine)",
+                     "decode_us": dec_avg_ms * 1e3,
+                     "algorithmic_bytes_per_launch": bytes_sum / K_},
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": E_},
+        "gpu_launches": int(launches),
+        "clocks": _clock_summary(clock_rows, wall0, wall1),
+        "context_tokens": {"start": ctx0[0] + ctx0[1],
+                           "end": cache.n_packed + cache.n_res},
+        "flushes_in_timed_region": len(flush_steps),
+    }
+    if bf16 is not None:
+        line["bf16_decode"] = bf16
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = _args()
+    world, rank, local = _dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

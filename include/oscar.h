@@ -1,0 +1,227 @@
+/*
+ * oscar.h -- C ABI of liboscar: the decode hot path of OScaR (Omni-Scaled
+ * Canalized Rotation) INT2 KV-cache quantisation, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page title and section):
+ *  [rainbus] "OScaR：面向大模型及多模态LLM极限KV缓存量化的奥卡姆剃刀" (paper.rainbus.top
+ *            summary): 方法步骤详情 (method step details), 前置知识, 论文图表 Fig. 2.
+ *  [notes]   "OScaR: The Occam's Razor for Extreme KV Cache Quantization in LLMs
+ *            and Beyond" (reading notes): II. Method -- Step One: Canalized
+ *            Rotation; Step Two: Omni-Token Scaling; End-to-End Flow.
+ *            III. Experiments -- Efficiency.
+ *  [news]    news article on arXiv 2605.19660 (animattoys.com): 二 (the two
+ *            steps), 三 (three kernels; packed cache and residual cache).
+ *
+ * Conventions (all calls)
+ *  - head_dim D = 128, key block G = 32 tokens, residual window R = 128 tokens.
+ *  - Every data pointer is DEVICE memory owned by the caller.  The library
+ *    never allocates or frees memory and keeps no state except one device
+ *    status word (read with oscar_device_status) and a host launch counter.
+ *  - Pointers must be 16-byte aligned (else OSCAR_ERR_ALIGNMENT).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default
+ *    stream).  Arguments are validated on the host before any launch; a
+ *    validation failure launches nothing and leaves the cache struct unchanged.
+ *    A launch failure returns OSCAR_ERR_CUDA.  Kernels that hit an internal
+ *    wait limit record it in the device status word instead of hanging.
+ *  - bf16 / fp16 values are passed as their 16-bit patterns.
+ *  - (b, h) rows are contiguous: "[B][Hkv][X]" means row (b*Hkv + h) of X.
+ *  - Query head j reads KV head j / g where g = Hq / Hkv (grouped-query
+ *    attention); g must be 1, 2, 4 or 8.
+ */
+#ifndef OSCAR_H
+#define OSCAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t oscar_bf16;
+typedef uint16_t oscar_f16;
+
+typedef enum {
+  OSCAR_OK = 0,
+  OSCAR_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad flag, state violation */
+  OSCAR_ERR_UNSUPPORTED = 2,   /* e.g. Hq/Hkv not in {1,2,4,8} */
+  OSCAR_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned */
+  OSCAR_ERR_CAPACITY = 4,      /* would write past T_cap */
+  OSCAR_ERR_WORKSPACE = 5,     /* workspace too small or null */
+  OSCAR_ERR_CUDA = 6,          /* a CUDA runtime call failed */
+  OSCAR_ERR_DEVICE_STATUS = 7  /* a kernel recorded an error (see oscar_device_status) */
+} oscar_status;
+
+/* Ablation flags ([notes] III, Ablations: rotation only / scaling only).
+ * 0 = the method: rotation then scaling. */
+enum { OSCAR_NO_ROTATE = 1u, OSCAR_NO_SCALE = 2u };
+
+#define OSCAR_HEAD_DIM 128
+#define OSCAR_GROUP 32
+#define OSCAR_RESIDUAL 128
+
+/*
+ * The KV cache of one attention layer for B sequences and Hkv KV heads:
+ * the "packed cache" of INT2 codes, quantisation parameters and token-norm
+ * tags plus the "residual cache" of the newest <= 128 tokens in 16 bit
+ * ([news] 三; [rainbus] Fig. 2(c)).  Plain old data; every pointer is caller
+ * device memory.  n_packed and n_res are uniform across the batch and are
+ * advanced by the calls below (host-side bookkeeping).
+ *
+ * Packed layout, per (b, h) row, T_cap tokens of capacity (multiple of 32):
+ *  k_codes  uint32 [B][Hkv][T_cap][8]   key codes, 16 per word.  Word w of a
+ *           token holds channels 16w..16w+15; channel 16w+j sits at bit
+ *           2*(j/2) + 16*(j%2) (even channels in the low half-word, odd in
+ *           the high half-word).
+ *  v_codes  uint32 [B][Hkv][T_cap/32][256] value codes, 16 per word, per
+ *           block of 32 tokens: word 128*kh + 4*(4g+t) + 2p + hh (kh, p, hh
+ *           in {0,1}, g in 0..7, t in 0..3) holds token 16kh+2t+8p in its low
+ *           half-word and the next token in its high half-word; slot k (bits
+ *           2k..2k+1 of a half) holds channel g + 8*(8hh+k).
+ *  k_scale, k_zero fp16 [B][Hkv][T_cap/32][128] per (block, channel) step and
+ *           zero of the keys ([rainbus] 方法步骤详情 (2), block size G = 32).
+ *  k_norm   fp16 [B][Hkv][T_cap]  each key's L2 norm ([notes] Step Two).
+ *  v_scale, v_zero fp16 [B][Hkv][T_cap] per-token step and zero of the values.
+ * Residual layout:
+ *  k_res    bf16 [B][Hkv][128][128] rotated, unit-norm keys (slot = age order)
+ *  v_res    bf16 [B][Hkv][128][128] values
+ *  k_res_norm fp16 [B][Hkv][128]
+ * Codes c in {0,1,2,3} dequantise to c*step + zero (x norm for keys).
+ */
+typedef struct {
+  int B, Hkv, T_cap;
+  uint32_t* k_codes;
+  uint32_t* v_codes;
+  oscar_f16* k_scale;
+  oscar_f16* k_zero;
+  oscar_f16* k_norm;
+  oscar_f16* v_scale;
+  oscar_f16* v_zero;
+  oscar_bf16* k_res;
+  oscar_bf16* v_res;
+  oscar_f16* k_res_norm;
+  int n_packed;      /* quantised tokens per row, multiple of 32 */
+  int n_res;         /* residual tokens per row, 0..128 */
+  unsigned flags;    /* OSCAR_NO_ROTATE / OSCAR_NO_SCALE, fixed for the cache's life */
+} oscar_cache;
+
+/*
+ * Canalized Rotation of the queries: q' = H q with H the 128x128 Sylvester
+ * Hadamard matrix scaled by 1/sqrt(128), applied online every decode step so
+ * that q'.k' = q.k ([notes] Step One, "Query-side symmetric processing";
+ * [rainbus] 方法步骤详情 (1)).  The softmax scale is not applied here.
+ *  q      bf16 [B][Hq][128]   input
+ *  q_rot  fp32 [B][Hq][128]   output (may not alias q)
+ *  flags  OSCAR_NO_ROTATE copies q (as fp32); OSCAR_NO_SCALE has no effect.
+ */
+oscar_status oscar_rotate_q(const oscar_bf16* q, float* q_rot, int B, int Hq,
+                            unsigned flags, void* stream);
+
+/*
+ * Canalized Rotation + Omni-Token Scaling of keys (the fused kernel (1) of
+ * [news] 三): k' = H k, s = sum(k'^2), k_hat = k' * rsqrt(s) (hardware rsqrt,
+ * [news] 三), norm = ||k|| ([notes] Step Two: divide each token by its own L2
+ * norm and keep the norm).  A zero key gives k_hat = 0, norm = 0.
+ * OSCAR_NO_ROTATE skips H; OSCAR_NO_SCALE keeps k' and writes norm = 1.
+ *  k        bf16 input,  element (b,h,t,c) at k[((b*Hkv+h)*in_T + t)*128 + c], t < n_tok
+ *  k_hat    bf16 output, element at k_hat[((b*Hkv+h)*out_T + out_t0 + t)*128 + c]
+ *  norm_out fp16 output, element at norm_out[(b*Hkv+h)*out_T + out_t0 + t]
+ * Requires n_tok >= 1, in_T >= n_tok, out_t0 + n_tok <= out_T.
+ */
+oscar_status oscar_rotate_scale_k(const oscar_bf16* k, int in_T,
+                                  oscar_bf16* k_hat, oscar_f16* norm_out, int out_T, int out_t0,
+                                  int B, int Hkv, int n_tok, unsigned flags, void* stream);
+
+/*
+ * Quantisation kernel (2) of [news] 三: keys as block-wise per-channel INT2
+ * (each channel's step and zero shared by 32 consecutive tokens), values as
+ * per-token INT2 ([rainbus] 方法步骤详情 (2)(3)).  Per group: zero = min,
+ * step = (max - min)/3 in fp32, code = round-half-even((x - zero)/step)
+ * clamped to [0,3] (0 when max == min); step and zero stored as fp16.
+ * Tokens [0, n_tok) of each (b,h) row of the sources are written to packed
+ * positions [n_packed, n_packed + n_tok); then c->n_packed += n_tok.
+ *  k_hat  bf16 [B][Hkv][src_T][128] rotated, scaled keys (from oscar_rotate_scale_k)
+ *  k_norm fp16 [B][Hkv][src_T]      their norms
+ *  v      bf16 [B][Hkv][src_T][128] values
+ * Flush mode: k_hat == k_norm == v == NULL quantises the full residual window
+ * (requires c->n_res == 128, src_T and n_tok ignored) and sets c->n_res = 0
+ * ([news] 三: batch quantisation once 128 tokens have accumulated).
+ * Requires n_tok % 32 == 0, n_tok >= 32, src_T >= n_tok, c->n_res == 0 in
+ * non-flush mode (packed tokens precede residual ones) and
+ * c->n_packed + n_tok <= c->T_cap (else OSCAR_ERR_CAPACITY).
+ */
+oscar_status oscar_quantize_kv(oscar_cache* c, const oscar_bf16* k_hat, const oscar_f16* k_norm,
+                               const oscar_bf16* v, int src_T, int n_tok, void* stream);
+
+/*
+ * Cache update for n_tok new tokens per (b,h) row, one after another: before
+ * each token, a full residual window (128 tokens) is flushed as in
+ * oscar_quantize_kv flush mode; the token's key is rotated and scaled into
+ * residual slot n_res, its value copied next to it, and c->n_res grows
+ * (flush-before-append: the newest token always stays 16-bit).  A decode
+ * step calls it with n_tok = 1.  ([notes] End-to-End Flow; [news] 三.)
+ *  k_new, v_new  bf16 [B][Hkv][n_tok][128] raw keys and values
+ * Fails with OSCAR_ERR_CAPACITY, launching nothing, if the flushes the call
+ * needs do not fit in T_cap.
+ */
+oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const oscar_bf16* v_new,
+                             int n_tok, void* stream);
+
+/*
+ * Fused dequantisation + inverse token scaling + attention (kernel (3) of
+ * [news] 三; [notes] End-to-End Flow: "Q.K^T and dequantization fused into a
+ * single kernel", III Efficiency), split-K over tokens (flash-decoding) with
+ * a log-sum-exp combine.  For query head j of sequence b, with h = j / g:
+ *   score_t = softmax_scale * q'_j . k_t,   k_t = (c*step + zero) * norm (packed)
+ *                                           k_t = k_hat_t * norm_t       (residual)
+ *   out_j   = sum_t softmax(score)_t * v_t, v_t = c*step + zero (packed) or v_res_t
+ * over the c->n_packed packed and c->n_res residual tokens of row (b, h).
+ *  q_rot      fp32 [B][Hq][128] rotated queries (oscar_rotate_q)
+ *  out        fp32 [B][Hq][128]; an empty cache gives zeros
+ *  num_splits packed-token splits per (b,h); 0 = choose for this device
+ *             (oscar_decode_num_splits); one more split handles the residual.
+ *  workspace  device scratch of at least oscar_decode_workspace_bytes(B, Hq,
+ *             splits) bytes (16-byte aligned); contents need no initialisation.
+ */
+oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, int Hq,
+                                    float softmax_scale, float* out, int num_splits,
+                                    void* workspace, size_t ws_bytes, void* stream);
+
+/* Split count oscar_decode_attention uses for num_splits = 0 on the current
+ * device (>= 1).  Returns 1 when no device can be queried. */
+int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed);
+
+/* Workspace bytes needed by oscar_decode_attention / oscar_bf16_decode_attention
+ * for `num_splits` token splits (0 = the automatic count for n_packed tokens). */
+size_t oscar_decode_workspace_bytes(int B, int Hkv, int Hq, int n_packed, int num_splits);
+
+/*
+ * Comparison kernel: unquantised bf16 split-K flash-decoding attention with
+ * the same grid, split and combine scheme (the "BF16 FlashDecoding-v2"
+ * baseline of [notes] III Efficiency).  No rotation, no scaling.
+ *  q      bf16 [B][Hq][128]
+ *  K, V   bf16 [B][Hkv][T_stride][128], tokens [0, T) of each row used
+ *  out    fp32 [B][Hq][128]
+ *  workspace as for oscar_decode_attention (use n_packed = T for sizing).
+ */
+oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* K,
+                                         const oscar_bf16* V, int B, int Hq, int Hkv, int T,
+                                         int T_stride, float softmax_scale, float* out,
+                                         int num_splits, void* workspace, size_t ws_bytes,
+                                         void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word.  OSCAR_OK if no kernel recorded an error, else OSCAR_ERR_DEVICE_STATUS. */
+oscar_status oscar_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* oscar_status_string(oscar_status s);
+
+/* Number of kernels this library has launched in this process. */
+unsigned long long oscar_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H */

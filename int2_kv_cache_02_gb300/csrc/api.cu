@@ -1,0 +1,310 @@
+// C ABI of liboscar (include/oscar.h): argument validation, split planning,
+// state bookkeeping of oscar_cache, and dispatch to the kernels.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+__device__ unsigned g_oscar_status;  // OR of kDevErr* bits since the last read
+
+namespace {
+
+using namespace oscar;
+
+std::atomic<unsigned long long> g_launches{0};
+std::mutex g_mu;
+unsigned* g_status_ptr[128] = {};
+
+unsigned* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_oscar_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+oscar_status from_cuda(cudaError_t e) { return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA; }
+
+oscar_status check_cache(const oscar_cache* c) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  if (c->B <= 0 || c->Hkv <= 0 || c->T_cap <= 0 || c->T_cap % kG != 0)
+    return OSCAR_ERR_INVALID_ARG;
+  const void* ptrs[] = {c->k_codes, c->v_codes, c->k_scale,  c->k_zero, c->k_norm,
+                        c->v_scale, c->v_zero,  c->k_res,    c->v_res,  c->k_res_norm};
+  for (const void* p : ptrs) {
+    if (!p) return OSCAR_ERR_INVALID_ARG;
+    if (!al16(p)) return OSCAR_ERR_ALIGNMENT;
+  }
+  if (c->n_packed < 0 || c->n_packed % kG != 0 || c->n_packed > c->T_cap)
+    return OSCAR_ERR_INVALID_ARG;
+  if (c->n_res < 0 || c->n_res > kR) return OSCAR_ERR_INVALID_ARG;
+  if (c->flags & ~3u) return OSCAR_ERR_INVALID_ARG;
+  return OSCAR_OK;
+}
+
+// Split planning: minimise (waves of CTAs) x (blocks per CTA) + a small
+// per-split cost, so the grid fills the SMs without long tails.
+int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  if (nblk <= 0 || rows <= 0) return 1;
+  const long long slots = (long long)sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+  int best = 1;
+  double best_cost = 1e300;
+  const int hi = (int)std::min<long long>(max_splits, nblk);
+  for (int s = 1; s <= hi; ++s) {
+    const long long waves = (rows * s + slots - 1) / slots;
+    const long long per = (nblk + s - 1) / s;
+    const double cost = (double)waves * (double)per + 0.25 * s;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+size_t ws_bytes_for(int B, int Hq, int parts) {
+  return (size_t)B * (size_t)Hq * (size_t)parts * kRecFloats * sizeof(float);
+}
+
+oscar_status flush_residual(oscar_cache* c, cudaStream_t s) {
+  if (c->n_packed + kR > c->T_cap) return OSCAR_ERR_CAPACITY;
+  cudaError_t e = launch_quantize_kv(
+      c->k_res, reinterpret_cast<const __half*>(c->k_res_norm), c->v_res, kR, kR, c->B, c->Hkv,
+      c->T_cap, c->n_packed, c->k_codes, c->v_codes, reinterpret_cast<__half*>(c->k_scale),
+      reinterpret_cast<__half*>(c->k_zero), reinterpret_cast<__half*>(c->k_norm),
+      reinterpret_cast<__half*>(c->v_scale), reinterpret_cast<__half*>(c->v_zero), s);
+  g_launches++;
+  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+  c->n_packed += kR;
+  c->n_res = 0;
+  return OSCAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+oscar_status oscar_rotate_q(const oscar_bf16* q, float* q_rot, int B, int Hq, unsigned flags,
+                            void* stream) {
+  if (!q || !q_rot || B <= 0 || Hq <= 0 || (flags & ~3u)) return OSCAR_ERR_INVALID_ARG;
+  if (!al16(q) || !al16(q_rot)) return OSCAR_ERR_ALIGNMENT;
+  const long long n = (long long)B * Hq;
+  if (n > (1LL << 30)) return OSCAR_ERR_INVALID_ARG;
+  cudaError_t e = launch_rotate_q(q, q_rot, (int)n, flags, as_stream(stream));
+  g_launches++;
+  return from_cuda(e);
+}
+
+oscar_status oscar_rotate_scale_k(const oscar_bf16* k, int in_T, oscar_bf16* k_hat,
+                                  oscar_f16* norm_out, int out_T, int out_t0, int B, int Hkv,
+                                  int n_tok, unsigned flags, void* stream) {
+  if (!k || !k_hat || !norm_out || B <= 0 || Hkv <= 0 || n_tok <= 0 || (flags & ~3u))
+    return OSCAR_ERR_INVALID_ARG;
+  if (in_T < n_tok || out_t0 < 0 || out_t0 + (long long)n_tok > out_T)
+    return OSCAR_ERR_INVALID_ARG;
+  if (!al16(k) || !al16(k_hat) || !al16(norm_out)) return OSCAR_ERR_ALIGNMENT;
+  const long long rows = (long long)B * Hkv;
+  if (rows * n_tok > (1LL << 34)) return OSCAR_ERR_INVALID_ARG;
+  cudaError_t e = launch_rotate_scale_k(k, in_T, k_hat, reinterpret_cast<__half*>(norm_out),
+                                        out_T, out_t0, (int)rows, n_tok, nullptr, nullptr, flags,
+                                        as_stream(stream));
+  g_launches++;
+  return from_cuda(e);
+}
+
+oscar_status oscar_quantize_kv(oscar_cache* c, const oscar_bf16* k_hat, const oscar_f16* k_norm,
+                               const oscar_bf16* v, int src_T, int n_tok, void* stream) {
+  oscar_status st = check_cache(c);
+  if (st != OSCAR_OK) return st;
+  if (!k_hat && !k_norm && !v) {
+    if (c->n_res != kR) return OSCAR_ERR_INVALID_ARG;
+    return flush_residual(c, as_stream(stream));
+  }
+  if (!k_hat || !k_norm || !v) return OSCAR_ERR_INVALID_ARG;
+  if (!al16(k_hat) || !al16(k_norm) || !al16(v)) return OSCAR_ERR_ALIGNMENT;
+  if (n_tok < kG || n_tok % kG != 0 || src_T < n_tok) return OSCAR_ERR_INVALID_ARG;
+  if (c->n_res != 0) return OSCAR_ERR_INVALID_ARG;  // packed tokens must precede residual ones
+  if ((long long)c->n_packed + n_tok > c->T_cap) return OSCAR_ERR_CAPACITY;
+  cudaError_t e = launch_quantize_kv(
+      k_hat, reinterpret_cast<const __half*>(k_norm), v, src_T, n_tok, c->B, c->Hkv, c->T_cap,
+      c->n_packed, c->k_codes, c->v_codes, reinterpret_cast<__half*>(c->k_scale),
+      reinterpret_cast<__half*>(c->k_zero), reinterpret_cast<__half*>(c->k_norm),
+      reinterpret_cast<__half*>(c->v_scale), reinterpret_cast<__half*>(c->v_zero),
+      as_stream(stream));
+  g_launches++;
+  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+  c->n_packed += n_tok;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const oscar_bf16* v_new,
+                             int n_tok, void* stream) {
+  oscar_status st = check_cache(c);
+  if (st != OSCAR_OK) return st;
+  if (!k_new || !v_new || n_tok <= 0) return OSCAR_ERR_INVALID_ARG;
+  if (!al16(k_new) || !al16(v_new)) return OSCAR_ERR_ALIGNMENT;
+  // capacity of the whole call, checked before anything is launched
+  {
+    long long res = c->n_res, packed = c->n_packed;
+    for (long long left = n_tok; left > 0;) {
+      if (res == kR) {
+        packed += kR;
+        res = 0;
+      }
+      const long long m = std::min<long long>(left, kR - res);
+      res += m;
+      left -= m;
+    }
+    if (packed > c->T_cap) return OSCAR_ERR_CAPACITY;
+  }
+  const cudaStream_t s = as_stream(stream);
+  const int rows = c->B * c->Hkv;
+  for (int done = 0; done < n_tok;) {
+    if (c->n_res == kR) {
+      st = flush_residual(c, s);
+      if (st != OSCAR_OK) return st;
+    }
+    const int m = std::min(n_tok - done, kR - c->n_res);
+    cudaError_t e = launch_rotate_scale_k(
+        k_new + (size_t)done * kD, n_tok, c->k_res, reinterpret_cast<__half*>(c->k_res_norm), kR,
+        c->n_res, rows, m, v_new + (size_t)done * kD, c->v_res, c->flags, s);
+    g_launches++;
+    if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+    c->n_res += m;
+    done += m;
+  }
+  return OSCAR_OK;
+}
+
+int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed) {
+  if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || !group_ok(Hq / Hkv)) return 1;
+  return plan_splits((long long)B * Hkv, n_packed / kG, decode_int2_ctas_per_sm(Hq / Hkv), 512);
+}
+
+size_t oscar_decode_workspace_bytes(int B, int Hkv, int Hq, int n_packed, int num_splits) {
+  if (B <= 0 || Hq <= 0) return 0;
+  const int s = num_splits > 0 ? num_splits : oscar_decode_num_splits(B, Hkv, Hq, n_packed);
+  return ws_bytes_for(B, Hq, s + 1);
+}
+
+oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, int Hq,
+                                    float softmax_scale, float* out, int num_splits,
+                                    void* workspace, size_t ws_bytes, void* stream) {
+  oscar_status st = check_cache(c);
+  if (st != OSCAR_OK) return st;
+  if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
+      !std::isfinite(softmax_scale))
+    return OSCAR_ERR_INVALID_ARG;
+  if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
+  if (!al16(q_rot) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
+  int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, c->n_packed);
+  if (!workspace || ws_bytes < ws_bytes_for(c->B, Hq, S + 1)) return OSCAR_ERR_WORKSPACE;
+  if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;
+  DecodeArgs a;
+  a.k_codes = c->k_codes;
+  a.v_codes = c->v_codes;
+  a.k_scale = reinterpret_cast<const __half*>(c->k_scale);
+  a.k_zero = reinterpret_cast<const __half*>(c->k_zero);
+  a.k_norm = reinterpret_cast<const __half*>(c->k_norm);
+  a.v_scale = reinterpret_cast<const __half*>(c->v_scale);
+  a.v_zero = reinterpret_cast<const __half*>(c->v_zero);
+  a.k_res = c->k_res;
+  a.v_res = c->v_res;
+  a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
+  a.q_rot = q_rot;
+  a.ws = static_cast<float*>(workspace);
+  a.out = out;
+  a.status = status_ptr();
+  a.B = c->B;
+  a.Hkv = c->Hkv;
+  a.Hq = Hq;
+  a.T_cap = c->T_cap;
+  a.n_packed = c->n_packed;
+  a.n_res = c->n_res;
+  a.num_splits = S;
+  a.flags = c->flags;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e = launch_decode_int2(a, as_stream(stream));
+  g_launches += 2;
+  return from_cuda(e);
+}
+
+oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* K,
+                                         const oscar_bf16* V, int B, int Hq, int Hkv, int T,
+                                         int T_stride, float softmax_scale, float* out,
+                                         int num_splits, void* workspace, size_t ws_bytes,
+                                         void* stream) {
+  if (!q || !K || !V || !out || B <= 0 || Hq <= 0 || Hkv <= 0 || T < 0 || T_stride < T ||
+      num_splits < 0 || num_splits > 4096 || !std::isfinite(softmax_scale))
+    return OSCAR_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !group_ok(Hq / Hkv)) return OSCAR_ERR_UNSUPPORTED;
+  if (!al16(q) || !al16(K) || !al16(V) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
+  int S = num_splits;
+  if (S == 0) {
+    const long long chunk = 16;  // tokens per warp chunk, the unit of work here
+    S = plan_splits((long long)B * Hkv, (T + chunk - 1) / chunk,
+                    decode_bf16_ctas_per_sm(Hq / Hkv), 512);
+  }
+  if (!workspace || ws_bytes < ws_bytes_for(B, Hq, S)) return OSCAR_ERR_WORKSPACE;
+  if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;
+  Bf16DecodeArgs a;
+  a.q = q;
+  a.K = K;
+  a.V = V;
+  a.ws = static_cast<float*>(workspace);
+  a.out = out;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.T = T;
+  a.T_stride = T_stride;
+  a.num_splits = S;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e = launch_decode_bf16(a, as_stream(stream));
+  g_launches += 2;
+  return from_cuda(e);
+}
+
+oscar_status oscar_device_status(void* stream) {
+  unsigned* p = status_ptr();
+  if (!p) return OSCAR_ERR_CUDA;
+  const cudaStream_t s = as_stream(stream);
+  unsigned v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, p, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return OSCAR_ERR_CUDA;
+  if (cudaMemsetAsync(p, 0, sizeof(unsigned), s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return OSCAR_ERR_CUDA;
+  return v ? OSCAR_ERR_DEVICE_STATUS : OSCAR_OK;
+}
+
+const char* oscar_status_string(oscar_status s) {
+  switch (s) {
+    case OSCAR_OK: return "ok";
+    case OSCAR_ERR_INVALID_ARG: return "invalid argument";
+    case OSCAR_ERR_UNSUPPORTED: return "unsupported configuration";
+    case OSCAR_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case OSCAR_ERR_CAPACITY: return "cache capacity exceeded";
+    case OSCAR_ERR_WORKSPACE: return "workspace missing or too small";
+    case OSCAR_ERR_CUDA: return "CUDA runtime error";
+    case OSCAR_ERR_DEVICE_STATUS: return "a kernel recorded an error";
+  }
+  return "unknown status";
+}
+
+unsigned long long oscar_kernel_launches(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,69 @@
+// Host-side launchers of the liboscar kernels (internal; the public ABI is
+// include/oscar.h).  Each returns the cudaGetLastError() after its launches.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace oscar {
+
+cudaError_t launch_rotate_q(const uint16_t* q, float* out, int n_vec, unsigned flags,
+                            cudaStream_t s);
+
+cudaError_t launch_rotate_scale_k(const uint16_t* k, int in_T, uint16_t* k_hat, __half* norm,
+                                  int out_T, int out_t0, int n_rows, int n_tok,
+                                  const uint16_t* v_in, uint16_t* v_out, unsigned flags,
+                                  cudaStream_t s);
+
+cudaError_t launch_quantize_kv(const uint16_t* k_hat, const __half* k_norm, const uint16_t* v,
+                               int src_T, int n_tok, int B, int Hkv, int T_cap, int p0,
+                               uint32_t* k_codes, uint32_t* v_codes, __half* k_scale,
+                               __half* k_zero, __half* k_norm_out, __half* v_scale,
+                               __half* v_zero, cudaStream_t s);
+
+struct DecodeArgs {
+  const uint32_t* k_codes;
+  const uint32_t* v_codes;
+  const __half* k_scale;
+  const __half* k_zero;
+  const __half* k_norm;
+  const __half* v_scale;
+  const __half* v_zero;
+  const uint16_t* k_res;
+  const uint16_t* v_res;
+  const __half* k_res_norm;
+  const float* q_rot;
+  float* ws;          // partial records [B*Hq][num_splits + 1][kRecFloats]
+  float* out;         // [B][Hq][128]
+  unsigned* status;
+  int B, Hkv, Hq, T_cap, n_packed, n_res, num_splits;
+  unsigned flags;
+  float scale_log2;   // softmax_scale * log2(e)
+};
+
+// Floats per split-K partial record: m, l, 2 pad, o[128].
+constexpr int kRecFloats = 132;
+
+// Fused INT2 decode attention + combine (two launches).
+cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t s);
+// Blocks per SM the INT2 decode kernel reaches for query group size g.
+int decode_int2_ctas_per_sm(int g);
+
+struct Bf16DecodeArgs {
+  const uint16_t* q;
+  const uint16_t* K;
+  const uint16_t* V;
+  float* ws;
+  float* out;
+  int B, Hq, Hkv, T, T_stride, num_splits;
+  float scale_log2;
+};
+
+cudaError_t launch_decode_bf16(const Bf16DecodeArgs& a, cudaStream_t s);
+int decode_bf16_ctas_per_sm(int g);
+
+// Log-sum-exp combine of n_parts partial records per (b, q-head).
+cudaError_t launch_combine(const float* ws, float* out, int n_rows, int n_parts, cudaStream_t s);
+
+}  // namespace oscar

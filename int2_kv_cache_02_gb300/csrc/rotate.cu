@@ -1,0 +1,126 @@
+// Canalized Rotation (online fast Walsh-Hadamard transform over head_dim)
+// and Omni-Token Scaling.
+//
+// "OScaR: The Occam's Razor for Extreme KV Cache Quantization in LLMs and
+// Beyond" (reading notes), II. Method, Step One (K' = K.H, H orthogonal with
+// entries +-1/sqrt(d), computed as an O(d log d) FHT; the same rotation is
+// applied to Q) and Step Two (divide each token by its own L2 norm, keep the
+// norm).  News article on arXiv 2605.19660, 三: one fused kernel does the FHT
+// and the scaling for K and only the FHT for Q, with the hardware rsqrt.
+//
+// One warp per 128-vector: lane l holds elements 4l..4l+3.  Index bits 0-1
+// are butterflied in registers, bits 2-6 across lanes with shuffles.
+#include "common.cuh"
+#include "launch.h"
+
+namespace oscar {
+
+constexpr float kInvSqrtD = 0.088388347648318440550f;  // 1/sqrt(128)
+
+// Unnormalised natural-order Walsh-Hadamard transform of the warp's vector.
+__device__ __forceinline__ void fht128(float (&x)[4], int lane) {
+  float a = x[0] + x[1], b = x[0] - x[1], c = x[2] + x[3], d = x[2] - x[3];
+  x[0] = a + c; x[2] = a - c; x[1] = b + d; x[3] = b - d;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float y = __shfl_xor_sync(0xffffffffu, x[r], m);
+      x[r] = upper ? (y - x[r]) : (x[r] + y);
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+
+__global__ void __launch_bounds__(256) rotate_q_kernel(const uint16_t* __restrict__ q,
+                                                       float* __restrict__ out, int n_vec,
+                                                       unsigned flags) {
+  const int lane = threadIdx.x & 31;
+  const long long v = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (v >= n_vec) return;
+  const uint2 raw = reinterpret_cast<const uint2*>(q + v * kD)[lane];
+  float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+  if (!(flags & OSCAR_NO_ROTATE)) {
+    fht128(x, lane);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) x[r] *= kInvSqrtD;
+  }
+  reinterpret_cast<float4*>(out + v * kD)[lane] = make_float4(x[0], x[1], x[2], x[3]);
+}
+
+// Rotates and scales n_tok keys per (b,h) row; optionally copies the value of
+// the same token (the decode append).
+__global__ void __launch_bounds__(256) rotate_scale_k_kernel(
+    const uint16_t* __restrict__ k, int in_T, uint16_t* __restrict__ k_hat,
+    __half* __restrict__ norm_out, int out_T, int out_t0, int n_rows, int n_tok,
+    const uint16_t* __restrict__ v_in, uint16_t* __restrict__ v_out, unsigned flags) {
+  const int lane = threadIdx.x & 31;
+  const long long v = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (v >= (long long)n_rows * n_tok) return;
+  const long long row = v / n_tok;
+  const int t = (int)(v - row * n_tok);
+  const long long src = (row * in_T + t) * kD;
+  const long long dst_tok = row * out_T + out_t0 + t;
+
+  const uint2 raw = reinterpret_cast<const uint2*>(k + src)[lane];
+  float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+  const bool rot = !(flags & OSCAR_NO_ROTATE);
+  if (rot) fht128(x, lane);
+
+  float norm;
+  if (flags & OSCAR_NO_SCALE) {
+    const float f = rot ? kInvSqrtD : 1.0f;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) x[r] *= f;
+    norm = 1.0f;
+  } else {
+    const float s = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+    if (s > 0.0f) {
+      const float rs = rsqrtf(s);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) x[r] *= rs;
+      norm = sqrtf(s) * (rot ? kInvSqrtD : 1.0f);
+    } else {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) x[r] = 0.0f;
+      norm = 0.0f;
+    }
+  }
+  __nv_bfloat162 p0 = __floats2bfloat162_rn(x[0], x[1]);
+  __nv_bfloat162 p1 = __floats2bfloat162_rn(x[2], x[3]);
+  uint2 o;
+  o.x = *reinterpret_cast<uint32_t*>(&p0);
+  o.y = *reinterpret_cast<uint32_t*>(&p1);
+  reinterpret_cast<uint2*>(k_hat + dst_tok * kD)[lane] = o;
+  if (lane == 0) norm_out[dst_tok] = __float2half_rn(norm);
+  if (v_in != nullptr) {
+    reinterpret_cast<uint2*>(v_out + dst_tok * kD)[lane] =
+        reinterpret_cast<const uint2*>(v_in + src)[lane];
+  }
+}
+
+cudaError_t launch_rotate_q(const uint16_t* q, float* out, int n_vec, unsigned flags,
+                            cudaStream_t s) {
+  const int grid = (n_vec + 7) / 8;
+  rotate_q_kernel<<<grid, 256, 0, s>>>(q, out, n_vec, flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rotate_scale_k(const uint16_t* k, int in_T, uint16_t* k_hat, __half* norm,
+                                  int out_T, int out_t0, int n_rows, int n_tok,
+                                  const uint16_t* v_in, uint16_t* v_out, unsigned flags,
+                                  cudaStream_t s) {
+  const long long n = (long long)n_rows * n_tok;
+  const long long grid = (n + 7) / 8;
+  rotate_scale_k_kernel<<<(unsigned)grid, 256, 0, s>>>(k, in_T, k_hat, norm, out_T, out_t0,
+                                                       n_rows, n_tok, v_in, v_out, flags);
+  return cudaGetLastError();
+}
+
+}  // namespace oscar

@@ -1,0 +1,224 @@
+"""Python binding of liboscar (include/oscar.h): argument marshalling only.
+
+Every computation runs in the CUDA kernels of liboscar.so; this module turns
+torch tensors into device pointers, keeps the oscar_cache struct, and raises
+OscarError on a non-OK status.  Importing it fails loudly if the library has
+not been built (``__graft_entry__.build()`` or ``python -m
+int2_kv_cache_02_gb300._build``): there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from ctypes import POINTER, c_float, c_int, c_size_t, c_uint, c_ulonglong, c_void_p
+
+import torch
+
+from . import _build
+
+D, G, R = 128, 32, 128
+NO_ROTATE, NO_SCALE = 1, 2
+
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CAPACITY",
+           5: "WORKSPACE", 6: "CUDA", 7: "DEVICE_STATUS"}
+
+
+class OscarError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)} "
+                         f"({_lib.oscar_status_string(status).decode()})")
+
+
+class OscarCacheStruct(ctypes.Structure):
+    _fields_ = [("B", c_int), ("Hkv", c_int), ("T_cap", c_int),
+                ("k_codes", c_void_p), ("v_codes", c_void_p),
+                ("k_scale", c_void_p), ("k_zero", c_void_p), ("k_norm", c_void_p),
+                ("v_scale", c_void_p), ("v_zero", c_void_p),
+                ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
+                ("n_packed", c_int), ("n_res", c_int), ("flags", c_uint)]
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.lib_path("liboscar.so")
+    if not os.path.exists(path):
+        raise ImportError(f"liboscar.so is not built ({path}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P = POINTER(OscarCacheStruct)
+    sig = {
+        "oscar_rotate_q": (c_int, [c_void_p, c_void_p, c_int, c_int, c_uint, c_void_p]),
+        "oscar_rotate_scale_k": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int,
+                                         c_int, c_int, c_int, c_uint, c_void_p]),
+        "oscar_quantize_kv": (c_int, [P, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p]),
+        "oscar_append_kv": (c_int, [P, c_void_p, c_void_p, c_int, c_void_p]),
+        "oscar_decode_attention": (c_int, [P, c_void_p, c_int, c_float, c_void_p, c_int,
+                                           c_void_p, c_size_t, c_void_p]),
+        "oscar_decode_num_splits": (c_int, [c_int, c_int, c_int, c_int]),
+        "oscar_decode_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+        "oscar_bf16_decode_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                                c_int, c_int, c_int, c_float, c_void_p, c_int,
+                                                c_void_p, c_size_t, c_void_p]),
+        "oscar_device_status": (c_int, [c_void_p]),
+        "oscar_status_string": (ctypes.c_char_p, [c_int]),
+        "oscar_kernel_launches": (c_ulonglong, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("liboscar takes device tensors")
+    if not t.is_contiguous():
+        raise ValueError("liboscar takes contiguous tensors")
+    return c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise OscarError(st, where)
+
+
+# ---------------------------------------------------------------------------
+# the cache
+# ---------------------------------------------------------------------------
+
+class KVCache:
+    """Caller-owned device buffers of one layer's OScaR cache plus the
+    oscar_cache struct that points at them (layouts in include/oscar.h)."""
+
+    def __init__(self, B: int, Hkv: int, T_cap: int, flags: int = 0, device=None):
+        if T_cap % G:
+            raise ValueError("T_cap must be a multiple of 32")
+        dev = torch.device(device if device is not None else "cuda")
+        nb = T_cap // G
+        e = torch.empty
+        self.k_codes = e((B, Hkv, T_cap, 8), dtype=torch.int32, device=dev)
+        self.v_codes = e((B, Hkv, nb, 256), dtype=torch.int32, device=dev)
+        self.k_scale = e((B, Hkv, nb, D), dtype=torch.float16, device=dev)
+        self.k_zero = e((B, Hkv, nb, D), dtype=torch.float16, device=dev)
+        self.k_norm = e((B, Hkv, T_cap), dtype=torch.float16, device=dev)
+        self.v_scale = e((B, Hkv, T_cap), dtype=torch.float16, device=dev)
+        self.v_zero = e((B, Hkv, T_cap), dtype=torch.float16, device=dev)
+        self.k_res = torch.zeros((B, Hkv, R, D), dtype=torch.bfloat16, device=dev)
+        self.v_res = torch.zeros((B, Hkv, R, D), dtype=torch.bfloat16, device=dev)
+        self.k_res_norm = torch.zeros((B, Hkv, R), dtype=torch.float16, device=dev)
+        s = OscarCacheStruct()
+        s.B, s.Hkv, s.T_cap = B, Hkv, T_cap
+        for name in ("k_codes", "v_codes", "k_scale", "k_zero", "k_norm", "v_scale", "v_zero",
+                     "k_res", "v_res", "k_res_norm"):
+            setattr(s, name, getattr(self, name).data_ptr())
+        s.n_packed, s.n_res, s.flags = 0, 0, flags
+        self.struct = s
+
+    B = property(lambda self: self.struct.B)
+    Hkv = property(lambda self: self.struct.Hkv)
+    T_cap = property(lambda self: self.struct.T_cap)
+    n_packed = property(lambda self: self.struct.n_packed)
+    n_res = property(lambda self: self.struct.n_res)
+    flags = property(lambda self: self.struct.flags)
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+    def bytes_packed_per_row(self) -> int:
+        return self.n_packed * 86
+
+    def nbytes(self) -> int:
+        return sum(getattr(self, n).numel() * getattr(self, n).element_size()
+                   for n in ("k_codes", "v_codes", "k_scale", "k_zero", "k_norm", "v_scale",
+                             "v_zero", "k_res", "v_res", "k_res_norm"))
+
+
+# ---------------------------------------------------------------------------
+# the calls (same names as the C ABI, without the oscar_ prefix)
+# ---------------------------------------------------------------------------
+
+def rotate_q(q: torch.Tensor, q_rot: torch.Tensor, flags: int = 0, stream=None):
+    B, Hq = q.shape[0], q.shape[1]
+    _check(_lib.oscar_rotate_q(_ptr(q), _ptr(q_rot), B, Hq, flags, _stream(stream)),
+           "oscar_rotate_q")
+
+
+def rotate_scale_k(k: torch.Tensor, k_hat: torch.Tensor, norm: torch.Tensor, B: int, Hkv: int,
+                   n_tok: int, in_T: int, out_T: int, out_t0: int = 0, flags: int = 0,
+                   stream=None):
+    _check(_lib.oscar_rotate_scale_k(_ptr(k), in_T, _ptr(k_hat), _ptr(norm), out_T, out_t0,
+                                     B, Hkv, n_tok, flags, _stream(stream)),
+           "oscar_rotate_scale_k")
+
+
+def quantize_kv(cache: KVCache, k_hat=None, k_norm=None, v=None, src_T: int = 0,
+                n_tok: int = 0, stream=None):
+    _check(_lib.oscar_quantize_kv(cache.ref(), _ptr(k_hat), _ptr(k_norm), _ptr(v), src_T, n_tok,
+                                  _stream(stream)), "oscar_quantize_kv")
+
+
+def append_kv(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, n_tok: int = 1,
+              stream=None):
+    _check(_lib.oscar_append_kv(cache.ref(), _ptr(k_new), _ptr(v_new), n_tok, _stream(stream)),
+           "oscar_append_kv")
+
+
+def decode_num_splits(B: int, Hkv: int, Hq: int, n_packed: int) -> int:
+    return int(_lib.oscar_decode_num_splits(B, Hkv, Hq, n_packed))
+
+
+def decode_workspace_bytes(B: int, Hkv: int, Hq: int, n_packed: int, num_splits: int = 0) -> int:
+    return int(_lib.oscar_decode_workspace_bytes(B, Hkv, Hq, n_packed, num_splits))
+
+
+def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
+    return torch.empty(max(16, (nbytes + 15) // 16 * 16) // 4, dtype=torch.float32,
+                       device=device if device is not None else "cuda")
+
+
+def decode_attention(cache: KVCache, q_rot: torch.Tensor, Hq: int, softmax_scale: float,
+                     out: torch.Tensor, workspace: torch.Tensor, num_splits: int = 0,
+                     stream=None):
+    _check(_lib.oscar_decode_attention(cache.ref(), _ptr(q_rot), Hq, softmax_scale, _ptr(out),
+                                       num_splits, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)), "oscar_decode_attention")
+
+
+def bf16_decode_attention(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, B: int, Hq: int,
+                          Hkv: int, T: int, T_stride: int, softmax_scale: float,
+                          out: torch.Tensor, workspace: torch.Tensor, num_splits: int = 0,
+                          stream=None):
+    _check(_lib.oscar_bf16_decode_attention(_ptr(q), _ptr(K), _ptr(V), B, Hq, Hkv, T, T_stride,
+                                            softmax_scale, _ptr(out), num_splits,
+                                            _ptr(workspace),
+                                            workspace.numel() * workspace.element_size(),
+                                            _stream(stream)), "oscar_bf16_decode_attention")
+
+
+def device_status(stream=None) -> int:
+    return int(_lib.oscar_device_status(_stream(stream)))
+
+
+def kernel_launches() -> int:
+    return int(_lib.oscar_kernel_launches())
+
+
+def default_scale() -> float:
+    return 1.0 / math.sqrt(D)

@@ -178,3 +178,48 @@ def mixed_modality_factors(seed: int, b_idx, t0: int, n_t: int, T_hint: int,
         kf[i] = (level * outl).astype(np.float32) * sink
         vf[i] = sink
     return kf, vf
+
+
+# --------------------------------------------------------------------------
+# The same generator on the GPU (liboscar_synth.so, include/oscar_synth.h).
+# --------------------------------------------------------------------------
+
+_synth_lib = None
+
+
+def _synth():
+    global _synth_lib
+    if _synth_lib is None:
+        import ctypes
+        import os
+        from . import _build
+        path = _build.lib_path("liboscar_synth.so")
+        if not os.path.exists(path):
+            raise ImportError(f"liboscar_synth.so is not built ({path})")
+        lib = ctypes.CDLL(path)
+        c = ctypes
+        lib.oscar_synth_bf16.restype = c.c_int
+        lib.oscar_synth_bf16.argtypes = [c.c_void_p, c.c_int, c.c_int, c.c_int, c.c_int, c.c_int,
+                                         c.c_int, c.c_ulonglong, c.c_void_p, c.c_void_p,
+                                         c.c_void_p]
+        _synth_lib = lib
+    return _synth_lib
+
+
+def gen_bf16_cuda(out, seed: int, H: int, b0: int, t0: int, n_t: int,
+                  chan_factor=None, tok_factor=None, stream=None):
+    """Fills the bf16 device tensor ``out`` [nB][H][out_T][128] (tokens
+    [0, n_t) of each row) with the same values as ``gen_bf16``.
+    ``chan_factor`` / ``tok_factor`` are device fp32 tensors or None."""
+    import ctypes
+    import torch
+    assert out.is_cuda and out.dtype == torch.bfloat16 and out.is_contiguous()
+    nB, Hh, out_T = out.shape[0], out.shape[1], out.shape[2]
+    assert Hh == H
+    s = stream if stream is not None else torch.cuda.current_stream()
+    cf = ctypes.c_void_p(chan_factor.data_ptr()) if chan_factor is not None else None
+    tf = ctypes.c_void_p(tok_factor.data_ptr()) if tok_factor is not None else None
+    rc = _synth().oscar_synth_bf16(ctypes.c_void_p(out.data_ptr()), nB, H, b0, out_T, t0, n_t,
+                                   seed & 0xFFFFFFFFFFFFFFFF, cf, tf, ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise RuntimeError(f"oscar_synth_bf16 failed ({rc})")

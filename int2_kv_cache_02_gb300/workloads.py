@@ -1,0 +1,182 @@
+"""The decode workloads: shapes and seeded synthetic structure.
+
+Each workload is one attention layer's KV cache for B sequences, drawn with
+the generator of ``synth.py`` (numpy on the CPU, the same numbers on the GPU).
+Structure follows the token-norm-imbalance patterns the pages describe: a few
+channel outliers in K, attention-sink tokens with low K and V norm, and for
+the mixed-modality stream norm jumps at segment boundaries plus rare
+high-norm tokens.  Shapes are Qwen3-8B-like (32 query / 8 KV heads) and
+Qwen3-Omni-30B-A3B-like (32 / 4) layers, head_dim 128.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from . import synth
+
+OUTLIER_CHANNELS = (5, 38, 77, 110)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    T0: int            # cached tokens before the first decode step
+    n_packed: int      # of which quantised (multiple of 32); T0 - n_packed <= 128 stay bf16
+    steps: int         # decode steps that append one token each
+    chan_factor_value: float
+    mixed_modality: bool
+    seed_base: int
+
+    @property
+    def g(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def n_res(self) -> int:
+        return self.T0 - self.n_packed
+
+    # seeds of the separate streams
+    @property
+    def seed_k(self) -> int:
+        return self.seed_base + 1
+
+    @property
+    def seed_v(self) -> int:
+        return self.seed_base + 2
+
+    @property
+    def seed_q(self) -> int:
+        return self.seed_base + 3
+
+    @property
+    def seed_seg(self) -> int:
+        return self.seed_base + 5
+
+    def chan_factor(self) -> np.ndarray:
+        return synth.channel_factors(OUTLIER_CHANNELS, self.chan_factor_value)
+
+    def tok_factors(self, b_idx, t0: int, n_t: int):
+        """(k_factor, v_factor) fp32 [len(b_idx)][n_t] for positions t0.."""
+        b_idx = np.atleast_1d(np.asarray(b_idx))
+        if self.mixed_modality:
+            return synth.mixed_modality_factors(self.seed_seg, b_idx, t0, n_t,
+                                                T_hint=self.T0 + self.steps)
+        f = synth.sink_token_factors(len(b_idx), t0, n_t)
+        return f, f.copy()
+
+    def t_cap(self, extra_steps: int = 0) -> int:
+        """Capacity covering the prompt and every flush of steps + extra_steps."""
+        res, packed = self.n_res, self.n_packed
+        for _ in range(self.steps + extra_steps):
+            if res == 128:
+                packed += 128
+                res = 0
+            res += 1
+        return max(packed, 32)
+
+    # -- CPU (numpy) draws of any slice -------------------------------------
+    def k_bits(self, b_idx, h_idx, t0: int, n_t: int) -> np.ndarray:
+        kf, _ = self.tok_factors(b_idx, t0, n_t)
+        return synth.gen_bf16(self.seed_k, self.Hkv, b_idx, h_idx, t0, n_t,
+                              chan_factor=self.chan_factor(), tok_factor=kf)
+
+    def v_bits(self, b_idx, h_idx, t0: int, n_t: int) -> np.ndarray:
+        _, vf = self.tok_factors(b_idx, t0, n_t)
+        return synth.gen_bf16(self.seed_v, self.Hkv, b_idx, h_idx, t0, n_t, tok_factor=vf)
+
+    def q_bits(self, b_idx, hq_idx, step: int) -> np.ndarray:
+        """Query of decode step ``step`` (position = step in the query stream)."""
+        return synth.gen_bf16(self.seed_q, self.Hq, b_idx, hq_idx, step, 1)[:, :, 0]
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tiny_1k", B=1, Hq=1, Hkv=1, T0=1024, n_packed=992, steps=0,
+                 chan_factor_value=20.0, mixed_modality=False, seed_base=1000),
+        Workload("qwen3_8b_32k", B=8, Hq=32, Hkv=8, T0=32768, n_packed=32640, steps=1,
+                 chan_factor_value=15.0, mixed_modality=False, seed_base=2000),
+        Workload("long_stream_128k", B=1, Hq=32, Hkv=8, T0=131072, n_packed=130944, steps=256,
+                 chan_factor_value=20.0, mixed_modality=False, seed_base=3000),
+        Workload("batch48_128k", B=48, Hq=32, Hkv=8, T0=131072, n_packed=130944, steps=256,
+                 chan_factor_value=20.0, mixed_modality=False, seed_base=4000),
+        Workload("omni_tni_64k", B=16, Hq=32, Hkv=4, T0=65536, n_packed=65408, steps=256,
+                 chan_factor_value=15.0, mixed_modality=True, seed_base=5000),
+    ]
+}
+
+
+# ---------------------------------------------------------------------------
+# GPU side: draw the inputs on the device and build the cache through the
+# library's own calls.
+# ---------------------------------------------------------------------------
+
+def draw_kv_cuda(wl: Workload, t0: int, n_t: int, device="cuda"):
+    """Raw bf16 K and V [B][Hkv][n_t][128] of positions t0.. on the device."""
+    import torch
+    K = torch.empty((wl.B, wl.Hkv, n_t, 128), dtype=torch.bfloat16, device=device)
+    V = torch.empty_like(K)
+    kf, vf = wl.tok_factors(np.arange(wl.B), t0, n_t)
+    cf = torch.from_numpy(wl.chan_factor()).to(device)
+    synth.gen_bf16_cuda(K, wl.seed_k, wl.Hkv, 0, t0, n_t, chan_factor=cf,
+                        tok_factor=torch.from_numpy(kf).to(device))
+    synth.gen_bf16_cuda(V, wl.seed_v, wl.Hkv, 0, t0, n_t,
+                        tok_factor=torch.from_numpy(vf).to(device))
+    return K, V
+
+
+def draw_q_cuda(wl: Workload, step: int, device="cuda"):
+    import torch
+    q = torch.empty((wl.B, wl.Hq, 1, 128), dtype=torch.bfloat16, device=device)
+    synth.gen_bf16_cuda(q, wl.seed_q, wl.Hq, 0, step, 1)
+    return q.view(wl.B, wl.Hq, 128)
+
+
+def build_cache_cuda(wl: Workload, K, V, flags: int = 0, T_cap: int | None = None,
+                     chunk: int = 8192, device="cuda"):
+    """Prompt of T0 tokens -> OScaR cache: rotate + scale + quantise the first
+    n_packed tokens (in chunks, through a bf16 staging buffer), then append
+    the remaining ones to the residual window."""
+    import torch
+    from . import oscar
+    T_cap = T_cap if T_cap is not None else wl.t_cap()
+    cache = oscar.KVCache(wl.B, wl.Hkv, T_cap, flags=flags, device=device)
+    T_stride = K.shape[2]
+    chunk = min(chunk, max(32, wl.n_packed))
+    stage = torch.empty((wl.B, wl.Hkv, chunk, 128), dtype=torch.bfloat16, device=device)
+    norm = torch.empty((wl.B, wl.Hkv, chunk), dtype=torch.float16, device=device)
+    vstage = torch.empty_like(stage)
+    for t0 in range(0, wl.n_packed, chunk):
+        n = min(chunk, wl.n_packed - t0)
+        oscar.rotate_scale_k(_offset(K, t0), stage, norm, wl.B, wl.Hkv, n, in_T=T_stride,
+                             out_T=chunk, flags=flags)
+        vstage[:, :, :n].copy_(V[:, :, t0:t0 + n])
+        oscar.quantize_kv(cache, stage, norm, vstage, src_T=chunk, n_tok=n)
+    if wl.n_res:
+        kr = K[:, :, wl.n_packed:wl.T0].contiguous()
+        vr = V[:, :, wl.n_packed:wl.T0].contiguous()
+        oscar.append_kv(cache, kr, vr, n_tok=wl.n_res)
+    return cache
+
+
+class _Offset:
+    """A device pointer into a contiguous tensor at token offset t0 (rows keep
+    their full stride, as the C ABI's in_T argument expects)."""
+
+    def __init__(self, base, t0: int):
+        self.base, self.t0 = base, t0
+        self.is_cuda = True
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return self.base.data_ptr() + self.t0 * 128 * self.base.element_size()
+
+
+def _offset(t, t0: int):
+    return _Offset(t, t0)

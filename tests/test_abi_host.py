@@ -1,0 +1,157 @@
+"""Host-side checks of the C ABI: the libraries build for sm_103a, load, export
+every symbol the headers declare, and reject bad arguments before launching
+anything.  No kernel runs here.
+
+The validation cases pass made-up device addresses that must never reach a
+kernel; they are skipped where a GPU is present so that a validation bug can
+never turn into a launch with a bad pointer.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from int2_kv_cache_02_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = {"liboscar.so": "oscar.h", "liboscar_synth.so": "oscar_synth.h"}
+
+no_gpu_only = pytest.mark.skipif(torch.cuda.is_available(),
+                                 reason="fake-pointer validation runs only without a GPU")
+
+
+@pytest.fixture(scope="module")
+def libs():
+    paths = _build.build()
+    return {k: ctypes.CDLL(v) for k, v in paths.items()}
+
+
+def _declared(header: str) -> list[str]:
+    text = open(os.path.join(ROOT, "include", header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(oscar_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_headers_declare_the_documented_calls():
+    names = _declared("oscar.h")
+    for want in ["oscar_rotate_q", "oscar_rotate_scale_k", "oscar_quantize_kv",
+                 "oscar_append_kv", "oscar_decode_attention", "oscar_bf16_decode_attention",
+                 "oscar_decode_workspace_bytes", "oscar_decode_num_splits",
+                 "oscar_device_status", "oscar_status_string", "oscar_kernel_launches"]:
+        assert want in names
+    assert _declared("oscar_synth.h") == ["oscar_synth_bf16"]
+
+
+@pytest.mark.parametrize("lib", sorted(HEADERS))
+def test_every_declared_symbol_is_exported(libs, lib):
+    for name in _declared(HEADERS[lib]):
+        assert hasattr(libs[lib], name), f"{lib} does not export {name}"
+
+
+def test_status_strings(libs):
+    f = libs["liboscar.so"].oscar_status_string
+    f.restype = ctypes.c_char_p
+    seen = {f(i) for i in range(8)}
+    assert len(seen) == 8 and f(99) == b"unknown status"
+
+
+# --------------------------------------------------------------------------
+# validation (made-up addresses, no device)
+# --------------------------------------------------------------------------
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def _cache(**kw):
+    from int2_kv_cache_02_gb300.oscar import OscarCacheStruct
+    s = OscarCacheStruct()
+    s.B, s.Hkv, s.T_cap = kw.get("B", 2), kw.get("Hkv", 2), kw.get("T_cap", 256)
+    for i, name in enumerate(["k_codes", "v_codes", "k_scale", "k_zero", "k_norm", "v_scale",
+                              "v_zero", "k_res", "v_res", "k_res_norm"]):
+        setattr(s, name, kw.get(name, FAKE + 0x100000 * i))
+    s.n_packed, s.n_res, s.flags = kw.get("n_packed", 0), kw.get("n_res", 0), kw.get("flags", 0)
+    return s
+
+
+@no_gpu_only
+def test_rotate_validation():
+    from int2_kv_cache_02_gb300 import oscar as O
+    L = O.library()
+    P = ctypes.c_void_p
+    assert L.oscar_rotate_q(None, P(FAKE), 1, 1, 0, None) == 1
+    assert L.oscar_rotate_q(P(FAKE + 8), P(FAKE), 1, 1, 0, None) == 3
+    assert L.oscar_rotate_q(P(FAKE), P(FAKE), 1, 1, 4, None) == 1          # unknown flag
+    assert L.oscar_rotate_q(P(FAKE), P(FAKE), 0, 1, 0, None) == 1
+    assert L.oscar_rotate_scale_k(P(FAKE), 4, P(FAKE), P(FAKE), 8, 6, 1, 1, 4, 0, None) == 1
+    assert L.oscar_rotate_scale_k(P(FAKE), 2, P(FAKE), P(FAKE), 8, 0, 1, 1, 4, 0, None) == 1
+    assert L.oscar_rotate_scale_k(P(FAKE), 4, P(FAKE + 2), P(FAKE), 8, 0, 1, 1, 4, 0, None) == 3
+
+
+@no_gpu_only
+def test_cache_validation_and_state_untouched():
+    from int2_kv_cache_02_gb300 import oscar as O
+    L = O.library()
+    P = ctypes.c_void_p
+    bad_cap = _cache(T_cap=100)
+    assert L.oscar_quantize_kv(ctypes.byref(bad_cap), None, None, None, 0, 0, None) == 1
+    misaligned = _cache(k_norm=FAKE + 4)
+    assert L.oscar_quantize_kv(ctypes.byref(misaligned), None, None, None, 0, 0, None) == 3
+    c = _cache()
+    # flush needs a full residual window
+    assert L.oscar_quantize_kv(ctypes.byref(c), None, None, None, 0, 0, None) == 1
+    # non-multiple of 32, and too many tokens for the capacity
+    assert L.oscar_quantize_kv(ctypes.byref(c), P(FAKE), P(FAKE), P(FAKE), 64, 48, None) == 1
+    assert L.oscar_quantize_kv(ctypes.byref(c), P(FAKE), P(FAKE), P(FAKE), 512, 512, None) == 4
+    # packed tokens must precede residual ones
+    c2 = _cache(n_res=3)
+    assert L.oscar_quantize_kv(ctypes.byref(c2), P(FAKE), P(FAKE), P(FAKE), 64, 64, None) == 1
+    # append needing a flush that does not fit: nothing launched, struct unchanged
+    full = _cache(n_packed=256, n_res=128)
+    assert L.oscar_append_kv(ctypes.byref(full), P(FAKE), P(FAKE), 1, None) == 4
+    assert full.n_packed == 256 and full.n_res == 128
+    st = _cache(n_packed=128, n_res=128)
+    assert L.oscar_append_kv(ctypes.byref(st), P(FAKE), P(FAKE), 200, None) == 4
+    assert st.n_packed == 128 and st.n_res == 128
+    assert c.n_packed == 0 and c.n_res == 0
+
+
+@no_gpu_only
+def test_decode_validation():
+    from int2_kv_cache_02_gb300 import oscar as O
+    L = O.library()
+    P = ctypes.c_void_p
+    c = _cache(Hkv=2)
+    # query group of 3 is not supported
+    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 6, 0.1, P(FAKE), 0, P(FAKE),
+                                    1 << 30, None) == 2
+    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 32, 0.1, P(FAKE), 0, P(FAKE),
+                                    1 << 30, None) == 2
+    # workspace missing / too small
+    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, P(FAKE), 4, None,
+                                    1 << 30, None) == 5
+    need = L.oscar_decode_workspace_bytes(2, 2, 8, 0, 4)
+    assert need == 2 * 8 * 5 * 132 * 4
+    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, P(FAKE), 4, P(FAKE),
+                                    need - 1, None) == 5
+    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, float("nan"), P(FAKE), 4,
+                                    P(FAKE), need, None) == 1
+    # bf16 comparison kernel
+    assert L.oscar_bf16_decode_attention(P(FAKE), P(FAKE), P(FAKE), 1, 4, 2, 100, 50, 0.1,
+                                         P(FAKE), 1, P(FAKE), 1 << 20, None) == 1
+    assert L.oscar_bf16_decode_attention(P(FAKE), P(FAKE), P(FAKE), 1, 5, 2, 100, 100, 0.1,
+                                         P(FAKE), 1, P(FAKE), 1 << 20, None) == 2
+    assert L.oscar_bf16_decode_attention(P(FAKE), P(FAKE), P(FAKE), 1, 4, 2, 100, 100, 0.1,
+                                         P(FAKE), 2, P(FAKE), 100, None) == 5
+
+
+@no_gpu_only
+def test_synth_validation(libs):
+    f = libs["liboscar_synth.so"].oscar_synth_bf16
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_ulonglong, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p]
+    assert f(None, 1, 1, 0, 4, 0, 4, 1, None, None, None) == 1
+    assert f(FAKE + 2, 1, 1, 0, 4, 0, 4, 1, None, None, None) == 1
+    assert f(FAKE, 1, 1, 0, 2, 0, 4, 1, None, None, None) == 1

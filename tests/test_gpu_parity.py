@@ -1,0 +1,391 @@
+"""GPU parity of the CUDA path against the oracle, through the C ABI.
+
+Gates (tolerances fixed by the decode-path contract):
+* rotation: k_hat within 1 bf16 ulp of the oracle's exact value, the norm
+  within 2 fp16 ulp, q' within 1e-6 relative;
+* quantisation: codes, steps, zeros and norms bit-exact when both sides
+  quantise the same bf16 inputs (the oracle's rotated keys are uploaded);
+* attention: max-abs <= 2e-3 and relative L2 <= 1e-3 per query head, both on
+  an oracle-built cache and end to end from the same raw inputs.
+Sizes span several tiles and a ragged tail; the full-size workloads are
+checked on sampled (sequence, KV head) rows in the launch configuration the
+benchmark uses.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oscar_oracle as O
+from int2_kv_cache_02_gb300 import synth
+from tests._gpu_helpers import (TAU, assert_attention_close, attn_errors, bf16_tensor_to_bits,
+                                bits_to_bf16_tensor, code_mismatches, f16_tensor_to_np,
+                                upload_oracle_cache)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    from int2_kv_cache_02_gb300 import _build
+    _build.build()
+    from int2_kv_cache_02_gb300 import oscar
+    return oscar
+
+
+def _sync_ok(L):
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+
+
+# --------------------------------------------------------------------------
+# generator
+# --------------------------------------------------------------------------
+
+def test_gpu_generator_matches_numpy(L):
+    cf = synth.channel_factors([5, 38, 77, 110], 20.0)
+    tf = synth.sink_token_factors(2, 100, 70) * np.float32(3.0)
+    out = torch.empty((2, 3, 80, 128), dtype=torch.bfloat16, device="cuda")
+    synth.gen_bf16_cuda(out, 77, 3, 5, 100, 70, chan_factor=torch.from_numpy(cf).cuda(),
+                        tok_factor=torch.from_numpy(tf).cuda())
+    got = bf16_tensor_to_bits(out)[:, :, :70]
+    want = synth.gen_bf16(77, 3, [5, 6], [0, 1, 2], 100, 70, chan_factor=cf, tok_factor=tf)
+    np.testing.assert_array_equal(got, want)
+
+
+# --------------------------------------------------------------------------
+# rotation gates
+# --------------------------------------------------------------------------
+
+def _ulp_bf16(x):
+    x = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+@pytest.mark.parametrize("flags", [0, O.NO_ROTATE, O.NO_SCALE, O.NO_ROTATE | O.NO_SCALE])
+def test_rotate_scale_k_gate(L, flags):
+    B, H, T = 2, 3, 200
+    cf = synth.channel_factors([5, 38, 77, 110], 20.0)
+    tf = synth.sink_token_factors(B, 0, T)
+    bits = synth.gen_bf16(101, H, range(B), range(H), 0, T, chan_factor=cf, tok_factor=tf)
+    bits[0, 0, 7] = 0                                   # a zero key
+    k = bits_to_bf16_tensor(bits)
+    k_hat = torch.empty((B, H, T + 5, 128), dtype=torch.bfloat16, device="cuda")
+    norm = torch.zeros((B, H, T + 5), dtype=torch.float16, device="cuda")
+    L.rotate_scale_k(k, k_hat, norm, B, H, T, in_T=T, out_T=T + 5, out_t0=5, flags=flags)
+    _sync_ok(L)
+    ref = O.rotate_scale_k(bits, flags)
+    got = O.bf16_to_f64(bf16_tensor_to_bits(k_hat)[:, :, 5:])
+    err = np.abs(got - ref.k_hat)
+    assert np.all(err <= _ulp_bf16(ref.k_hat) + 2.0 ** -133), float((err / _ulp_bf16(ref.k_hat)).max())
+    n_got = f16_tensor_to_np(norm)[:, :, 5:].astype(np.float64)
+    ulp16 = np.spacing(np.abs(ref.norm).astype(np.float16)).astype(np.float64)
+    assert np.all(np.abs(n_got - ref.norm) <= 2 * ulp16)
+    assert np.all(got[0, 0, 7] == 0) and (flags & O.NO_SCALE or n_got[0, 0, 7] == 0)
+
+
+@pytest.mark.parametrize("flags", [0, O.NO_ROTATE])
+def test_rotate_q_gate(L, flags):
+    B, Hq = 3, 8
+    bits = synth.gen_bf16(102, Hq, range(B), range(Hq), 0, 1)[:, :, 0]
+    q = bits_to_bf16_tensor(bits)
+    qr = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    L.rotate_q(q, qr, flags=flags)
+    _sync_ok(L)
+    ref = O.rotate_q(bits, flags)
+    got = qr.cpu().numpy().astype(np.float64)
+    assert np.abs(got - ref).max() <= 1e-6 * np.abs(ref).max()
+
+
+# --------------------------------------------------------------------------
+# quantisation gate: bit-exact on identical inputs
+# --------------------------------------------------------------------------
+
+def _special_blocks(k_hat_bits, v_bits):
+    """Plant degenerate groups and exact ties into the inputs."""
+    kb = k_hat_bits.copy()
+    vb = v_bits.copy()
+    kb[32:64, 3] = O.f64_to_bf16(np.full(32, 0.25))          # constant key channel in block 1
+    ties = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 2.5, 3.0] + [1.0] * 25)
+    kb[64:96, 9] = O.f64_to_bf16(ties)                        # ties 0.5/1.5/2.5 in block 2
+    vb[5, :] = O.f64_to_bf16(np.full(128, -0.75))             # constant value token
+    vb[6, :] = O.f64_to_bf16(np.resize(ties, 128))            # ties in a value token
+    return kb, vb
+
+
+def test_quantize_bit_exact(L):
+    B, H, T = 2, 2, 160
+    cf = synth.channel_factors([5, 38, 77, 110], 15.0)
+    tf = synth.sink_token_factors(B, 0, T)
+    kraw = synth.gen_bf16(201, H, range(B), range(H), 0, T, chan_factor=cf, tok_factor=tf)
+    vraw = synth.gen_bf16(202, H, range(B), range(H), 0, T, tok_factor=tf)
+    rk = O.rotate_scale_k(kraw)
+    khat = rk.k_hat_bf16.copy()
+    vb = vraw.copy()
+    khat[1, 1], vb[1, 1] = _special_blocks(khat[1, 1], vb[1, 1])
+    T_cap = 256
+    cache = L.KVCache(B, H, T_cap)
+    # quantise in two calls to exercise the packed offset
+    L.quantize_kv(cache, bits_to_bf16_tensor(khat), torch.from_numpy(rk.norm_f16).cuda(),
+                  bits_to_bf16_tensor(vb), src_T=T, n_tok=64)
+    k2 = np.ascontiguousarray(khat[:, :, 64:])
+    L.quantize_kv(cache, bits_to_bf16_tensor(k2), torch.from_numpy(np.ascontiguousarray(rk.norm_f16[:, :, 64:])).cuda(),
+                  bits_to_bf16_tensor(np.ascontiguousarray(vb[:, :, 64:])), src_T=T - 64, n_tok=96)
+    _sync_ok(L)
+    assert cache.n_packed == 160
+    for b in range(B):
+        for h in range(H):
+            kq, vq = O.quantize_k(khat[b, h]), O.quantize_v(vb[b, h])
+            np.testing.assert_array_equal(
+                cache.k_codes[b, h, :T].cpu().numpy().view(np.uint32), O.pack_k_words(kq.codes))
+            np.testing.assert_array_equal(
+                cache.v_codes[b, h, :T // 32].cpu().numpy().view(np.uint32),
+                O.pack_v_words(vq.codes))
+            for name, want in [("k_scale", kq.step16), ("k_zero", kq.zero16)]:
+                got = getattr(cache, name)[b, h, :T // 32].cpu().numpy()
+                np.testing.assert_array_equal(got.view(np.uint16), want.view(np.uint16))
+            for name, want in [("v_scale", vq.step16), ("v_zero", vq.zero16),
+                               ("k_norm", rk.norm_f16[b, h])]:
+                got = getattr(cache, name)[b, h, :T].cpu().numpy()
+                np.testing.assert_array_equal(got.view(np.uint16), want.view(np.uint16))
+
+
+# --------------------------------------------------------------------------
+# attention gate on an oracle-built cache
+# --------------------------------------------------------------------------
+
+def _oracle_heads(seed, B, Hkv, T, P, flags=0, chan=20.0, sinks=True):
+    cf = synth.channel_factors([5, 38, 77, 110], chan)
+    tf = synth.sink_token_factors(B, 0, T) if sinks else None
+    k = synth.gen_bf16(seed, Hkv, range(B), range(Hkv), 0, T, chan_factor=cf, tok_factor=tf)
+    v = synth.gen_bf16(seed + 1, Hkv, range(B), range(Hkv), 0, T, tok_factor=tf)
+    return {(b, h): O.build_head_cache(k[b, h], v[b, h], P, flags)
+            for b in range(B) for h in range(Hkv)}, k, v
+
+
+def _decode_vs_oracle(L, heads, B, Hq, Hkv, T_cap, seed_q, flags=0, splits=(0,)):
+    g = Hq // Hkv
+    cache = upload_oracle_cache(L.KVCache(B, Hkv, T_cap, flags), heads, flags)
+    qbits = synth.gen_bf16(seed_q, Hq, range(B), range(Hq), 0, 1)[:, :, 0]
+    qrot = O.rotate_q(qbits, flags)
+    ref = np.stack([np.concatenate([heads[(b, h)].decode(qrot[b, h * g:(h + 1) * g], TAU)
+                                    for h in range(Hkv)]) for b in range(B)])
+    qr = torch.from_numpy(qrot.astype(np.float32)).cuda()
+    outs = []
+    for S in splits:
+        ws = L.alloc_workspace(L.decode_workspace_bytes(B, Hkv, Hq, cache.n_packed, S))
+        out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+        L.decode_attention(cache, qr, Hq, TAU, out, ws, num_splits=S)
+        _sync_ok(L)
+        got = out.cpu().numpy()
+        assert_attention_close(got, ref, f"splits={S}")
+        outs.append(got)
+    return outs, ref
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_decode_on_oracle_cache_all_groups(L, g):
+    B, Hkv, T, P = 2, 2, 2048 + 77, 2048
+    heads, _, _ = _oracle_heads(300 + g, B, Hkv, T, P)
+    _decode_vs_oracle(L, heads, B, g * Hkv, Hkv, 2112, 310 + g, splits=(1, 2, 7, 0))
+
+
+def test_split_invariance(L):
+    B, Hkv, Hq, T, P = 1, 2, 8, 4096 + 128, 4096
+    heads, _, _ = _oracle_heads(320, B, Hkv, T, P)
+    outs, ref = _decode_vs_oracle(L, heads, B, Hq, Hkv, 4096, 321, splits=(1, 2, 7, 13, 0))
+    for o in outs[1:]:
+        d = np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0])
+        assert d <= 1e-5
+
+
+@pytest.mark.parametrize("T,P", [(96, 0), (1024, 1024), (32, 32), (33, 32), (1, 0)])
+def test_decode_edge_sizes(L, T, P):
+    B, Hkv, Hq = 1, 2, 8
+    heads, _, _ = _oracle_heads(330 + T, B, Hkv, T, P)
+    _decode_vs_oracle(L, heads, B, Hq, Hkv, max(32, P), 331, splits=(0, 3))
+
+
+def test_decode_empty_cache_gives_zeros(L):
+    cache = L.KVCache(1, 2, 64)
+    qr = torch.randn((1, 8, 128), device="cuda")
+    ws = L.alloc_workspace(L.decode_workspace_bytes(1, 2, 8, 0, 2))
+    out = torch.full((1, 8, 128), float("nan"), device="cuda")
+    L.decode_attention(cache, qr, 8, TAU, out, ws, num_splits=2)
+    _sync_ok(L)
+    assert torch.all(out == 0)
+
+
+@pytest.mark.parametrize("flags", [O.NO_ROTATE, O.NO_SCALE, O.NO_ROTATE | O.NO_SCALE])
+def test_decode_ablation_flags(L, flags):
+    B, Hkv, Hq, T, P = 1, 2, 8, 1024 + 40, 1024
+    heads, _, _ = _oracle_heads(340 + flags, B, Hkv, T, P, flags=flags)
+    _decode_vs_oracle(L, heads, B, Hq, Hkv, 1024, 341, flags=flags, splits=(0,))
+
+
+def test_decode_lossless_case_equals_plain_attention(L):
+    """INT2 storage is exact here, so the kernel must match bf16 attention."""
+    flags = O.NO_ROTATE | O.NO_SCALE
+    lv = np.array([-1.5, -0.5, 0.5, 1.5])
+    T, P, Hq = 1024 + 60, 1024, 4
+    r = synth.splitmix64(350, np.arange(2 * T * 128)).reshape(2, T, 128)
+    k = lv[(r[0] % np.uint64(4)).astype(np.int64)]
+    v = lv[(r[1] % np.uint64(4)).astype(np.int64)]
+    k[0::32], k[1::32] = -1.5, 1.5
+    v[:, 0], v[:, 1] = -1.5, 1.5
+    kb, vb = O.f64_to_bf16(k), O.f64_to_bf16(v)
+    heads = {(0, 0): O.build_head_cache(kb, vb, P, flags)}
+    outs, ref = _decode_vs_oracle(L, heads, 1, Hq, 1, 1024, 351, flags=flags, splits=(0,))
+    q = synth.gen_bf16(351, Hq, [0], range(Hq), 0, 1)[0, :, 0]
+    plain = O.bf16_attention(q, kb, vb, TAU)
+    assert_attention_close(outs[0][0], plain, "lossless")
+
+
+# --------------------------------------------------------------------------
+# end to end: GPU pipeline vs oracle pipeline from the same raw inputs
+# --------------------------------------------------------------------------
+
+def _pipeline(L, wl_name, rows, flags=0, steps=None, check_codes=True):
+    from int2_kv_cache_02_gb300 import workloads as W
+    wl = W.WORKLOADS[wl_name]
+    steps = wl.steps if steps is None else steps
+    K, V = W.draw_kv_cuda(wl, 0, wl.T0)
+    cache = W.build_cache_cuda(wl, K, V, flags=flags, T_cap=wl.t_cap(steps - wl.steps))
+    del K, V
+    if steps:
+        Kn, Vn = W.draw_kv_cuda(wl, wl.T0, steps)
+        for i in range(steps):
+            L.append_kv(cache, Kn[:, :, i].contiguous(), Vn[:, :, i].contiguous(), n_tok=1)
+        del Kn, Vn
+    step = max(steps - 1, 0)
+    q = W.draw_q_cuda(wl, step)
+    qr = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device="cuda")
+    L.rotate_q(q, qr, flags=flags)
+    S = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, cache.n_packed)
+    ws = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, cache.n_packed, S))
+    out = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device="cuda")
+    L.decode_attention(cache, qr, wl.Hq, TAU, out, ws, num_splits=S)
+    _sync_ok(L)
+    out = out.cpu().numpy()
+    g = wl.g
+    worst = (0.0, 0.0)
+    for (b, h) in rows:
+        T_all = wl.T0 + steps
+        kb = wl.k_bits([b], [h], 0, T_all)[0, 0]
+        vb = wl.v_bits([b], [h], 0, T_all)[0, 0]
+        hc = O.build_head_cache(kb[:wl.T0], vb[:wl.T0], wl.n_packed, flags)
+        for t in range(wl.T0, T_all):
+            hc.append(kb[t], vb[t])
+        assert hc.n_packed == cache.n_packed and hc.n_res == cache.n_res
+        qbits = wl.q_bits([b], range(h * g, (h + 1) * g), step)[0]
+        ref = hc.decode(O.rotate_q(qbits, flags), TAU)
+        ma, rl = assert_attention_close(out[b, h * g:(h + 1) * g], ref, f"{wl_name} row {(b, h)}")
+        worst = (max(worst[0], ma), max(worst[1], rl))
+        if check_codes:
+            kq = hc.packed_k()
+            got = cache.k_codes[b, h, :cache.n_packed].cpu().numpy().view(np.uint32)
+            n_bad = code_mismatches(got, O.pack_k_words(kq.codes))
+            # codes differ only where the GPU's rsqrt-based k_hat rounds to the
+            # neighbouring bf16 value; that must stay rare
+            assert n_bad <= max(4, 2e-5 * kq.codes.size), n_bad
+            vq = hc.packed_v()
+            gotv = cache.v_codes[b, h, :cache.n_packed // 32].cpu().numpy().view(np.uint32)
+            assert code_mismatches(gotv, O.pack_v_words(vq.codes)) == 0
+    return worst
+
+
+def test_pipeline_tiny(L):
+    _pipeline(L, "tiny_1k", [(0, 0)])
+
+
+@pytest.mark.parametrize("flags", [O.NO_ROTATE, O.NO_SCALE])
+def test_pipeline_tiny_ablations(L, flags):
+    _pipeline(L, "tiny_1k", [(0, 0)], flags=flags)
+
+
+def test_pipeline_qwen3_8b_32k_sampled(L):
+    _pipeline(L, "qwen3_8b_32k", [(0, 0), (7, 5)])
+
+
+def test_pipeline_long_stream_128k_sampled(L):
+    _pipeline(L, "long_stream_128k", [(0, 3)])
+
+
+def test_pipeline_batch48_128k_sampled(L):
+    _pipeline(L, "batch48_128k", [(0, 0), (47, 7)], steps=1)
+
+
+def test_pipeline_omni_tni_64k_sampled(L):
+    _pipeline(L, "omni_tni_64k", [(0, 0), (15, 3)])
+
+
+def test_streaming_flush_equals_one_shot_on_gpu(L):
+    """Appending tokens one by one (with flushes) and quantising the same
+    prefix in one call give identical packed words."""
+    from int2_kv_cache_02_gb300 import workloads as W
+    B, Hkv, T = 2, 2, 3 * 128 + 9
+    cf = synth.channel_factors([5], 20.0)
+    kb = synth.gen_bf16(360, Hkv, range(B), range(Hkv), 0, T, chan_factor=cf)
+    vb = synth.gen_bf16(361, Hkv, range(B), range(Hkv), 0, T)
+    K, V = bits_to_bf16_tensor(kb), bits_to_bf16_tensor(vb)
+    a = L.KVCache(B, Hkv, 512)
+    for t in range(T):
+        L.append_kv(a, K[:, :, t].contiguous(), V[:, :, t].contiguous())
+    b_ = L.KVCache(B, Hkv, 512)
+    L.append_kv(b_, K, V, n_tok=T)
+    _sync_ok(L)
+    P = 128 * ((T - 1) // 128)
+    assert a.n_packed == b_.n_packed == P and a.n_res == b_.n_res == T - P
+    stage = torch.empty((B, Hkv, P, 128), dtype=torch.bfloat16, device="cuda")
+    norm = torch.empty((B, Hkv, P), dtype=torch.float16, device="cuda")
+    L.rotate_scale_k(K, stage, norm, B, Hkv, P, in_T=T, out_T=P)
+    c = L.KVCache(B, Hkv, 512)
+    L.quantize_kv(c, stage, norm, V[:, :, :P].contiguous(), src_T=P, n_tok=P)
+    _sync_ok(L)
+    lens = {"k_codes": P, "k_norm": P, "v_scale": P, "v_zero": P,
+            "k_scale": P // 32, "k_zero": P // 32, "v_codes": P // 32}
+    for x in (a, b_):
+        for name, n in lens.items():
+            assert torch.equal(getattr(x, name)[:, :, :n], getattr(c, name)[:, :, :n]), name
+    assert torch.equal(a.k_res[:, :, :T - P], b_.k_res[:, :, :T - P])
+    assert torch.equal(a.v_res[:, :, :T - P], b_.v_res[:, :, :T - P])
+
+
+# --------------------------------------------------------------------------
+# the bf16 comparison kernel
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("g,T,S", [(1, 1000, 0), (4, 4097, 0), (4, 4097, 3), (8, 777, 2),
+                                   (2, 64, 1), (4, 1, 1)])
+def test_bf16_decode_parity(L, g, T, S):
+    B, Hkv = 2, 2
+    Hq = g * Hkv
+    kb = synth.gen_bf16(400 + g, Hkv, range(B), range(Hkv), 0, T,
+                        chan_factor=synth.channel_factors([5, 38], 20.0))
+    vb = synth.gen_bf16(401 + g, Hkv, range(B), range(Hkv), 0, T)
+    qb = synth.gen_bf16(402 + g, Hq, range(B), range(Hq), 0, 1)[:, :, 0]
+    Ts = T + 3
+    K = torch.zeros((B, Hkv, Ts, 128), dtype=torch.bfloat16, device="cuda")
+    V = torch.zeros_like(K)
+    K[:, :, :T] = bits_to_bf16_tensor(kb)
+    V[:, :, :T] = bits_to_bf16_tensor(vb)
+    q = bits_to_bf16_tensor(qb)
+    Sx = S if S else 64
+    ws = L.alloc_workspace(L.decode_workspace_bytes(B, Hkv, Hq, T, Sx))
+    out = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    L.bf16_decode_attention(q, K, V, B, Hq, Hkv, T, Ts, TAU, out, ws, num_splits=S)
+    _sync_ok(L)
+    ref = np.stack([np.concatenate([O.bf16_attention(qb[b, h * g:(h + 1) * g], kb[b, h], vb[b, h], TAU)
+                                    for h in range(Hkv)]) for b in range(B)])
+    assert_attention_close(out.cpu().numpy(), ref, f"bf16 g={g} T={T}")
+
+
+def test_kernel_launch_counter_moves(L):
+    n0 = L.kernel_launches()
+    q = torch.zeros((1, 1, 128), dtype=torch.bfloat16, device="cuda")
+    qr = torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
+    L.rotate_q(q, qr)
+    _sync_ok(L)
+    assert L.kernel_launches() == n0 + 1
