@@ -49,6 +49,9 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-bf16", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=256)
+    p.add_argument("--workload", default=WORKLOAD,
+                   help="workload name (the headline line uses the default; others are "
+                        "for profiling small cases)")
     return p.parse_args()
 
 
@@ -143,37 +146,39 @@ def _oracle_row_cache(wl, b, h, T_hist):
     return O.build_head_cache(kb[:wl.T0], vb[:wl.T0], wl.n_packed), kb, vb
 
 
-def oracle_step_time(wl, rows, n_steps, token_fraction=1.0):
-    """Seconds per (row, step) of the oracle decode step: rotate the row's
-    queries, append its new token, attend over its cache (optionally over the
-    first ``token_fraction`` of the packed tokens)."""
+def _truncate_packed(hc, keep):
+    """Keep only the first ``keep`` packed tokens of an oracle HeadCache."""
     from oracle import oscar_oracle as O
-    g = wl.g
-    tau = 1.0 / math.sqrt(128)
-    times = []
-    for (b, h) in rows:
-        hc, kb, vb = _oracle_row_cache(wl, b, h, wl.T0 + n_steps)
-        if token_fraction < 1.0:
-            keep = max(32, int(hc.n_packed * token_fraction) // 32 * 32)
-            kq, vq = hc.packed_k(), hc.packed_v()
-            hc.k_codes = [O.QuantK(kq.codes[:keep], kq.step16[:keep // 32], kq.zero16[:keep // 32])]
-            hc.k_norm16 = [hc.packed_norm16()[:keep]]
-            hc.v_q = [O.QuantV(vq.codes[:keep], vq.step16[:keep], vq.zero16[:keep])]
-        qs = [wl.q_bits([b], range(h * g, (h + 1) * g), i)[0] for i in range(n_steps)]
-        t = time.perf_counter()
-        for i in range(n_steps):
-            qr = O.rotate_q(qs[i])
-            hc.append(kb[wl.T0 + i], vb[wl.T0 + i])
-            hc.decode(qr, tau)
-        times.append((time.perf_counter() - t) / n_steps)
-    return float(np.mean(times))
+    kq, vq = hc.packed_k(), hc.packed_v()
+    hc.k_codes = [O.QuantK(kq.codes[:keep], kq.step16[:keep // 32], kq.zero16[:keep // 32])]
+    hc.k_norm16 = [hc.packed_norm16()[:keep]]
+    hc.v_q = [O.QuantV(vq.codes[:keep], vq.step16[:keep], vq.zero16[:keep])]
+
+
+def _oracle_steps(wl, hc, kb, vb, b, h, i0, n):
+    """n oracle decode steps of one row: rotate its queries, append the new
+    token (flush-before-append), attend over the row's cache.  Returns seconds."""
+    from oracle import oscar_oracle as O
+    g, tau = wl.g, 1.0 / math.sqrt(128)
+    qs = [wl.q_bits([b], range(h * g, (h + 1) * g), i)[0] for i in range(i0, i0 + n)]
+    t = time.perf_counter()
+    for j in range(n):
+        hc.append(kb[wl.T0 + i0 + j], vb[wl.T0 + i0 + j])
+        hc.decode(O.rotate_q(qs[j]), tau)
+    return time.perf_counter() - t
 
 
 def cpu_baseline(wl, budget_s=20.0):
     rows = [(0, 0), (wl.B - 1, wl.Hkv - 1)]
-    t1 = oracle_step_time(wl, rows[:1], 1)
-    n = max(1, min(20, int(budget_s / max(t1, 1e-3) / len(rows))))
-    per = oracle_step_time(wl, rows, n)
+    max_steps = 20
+    built = [(b, h) + _oracle_row_cache(wl, b, h, wl.T0 + max_steps + 1) for (b, h) in rows]
+    b, h, hc, kb, vb = built[0]
+    t1 = _oracle_steps(wl, hc, kb, vb, b, h, 0, 1)           # calibration step (untimed)
+    n = max(1, min(max_steps, int(budget_s / max(t1, 1e-3) / len(rows))))
+    tot = 0.0
+    for k, (b, h, hc, kb, vb) in enumerate(built):
+        tot += _oracle_steps(wl, hc, kb, vb, b, h, 1 if k == 0 else 0, n)
+    per = tot / (n * len(rows))
     total_rows = wl.B * wl.Hkv
     return {"value": per * total_rows * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{len(rows)} of {total_rows} (sequence, KV head) rows x {n} decode steps "
@@ -188,30 +193,18 @@ def run_reference(args, world, rank):
     from int2_kv_cache_02_gb300 import workloads as W
     if rank != 0:
         return 0
-    wl = W.WORKLOADS[WORKLOAD]
+    wl = W.WORKLOADS[args.workload]
     total_rows = wl.B * wl.Hkv
     steps = args.steps + args.warmup
+    hc, kb, vb = _oracle_row_cache(wl, 0, 0, wl.T0 + steps + 1)
+    probe = _oracle_steps(wl, hc, kb, vb, 0, 0, 0, 1)       # untimed size probe
     # size each step so that the whole run stays within about two minutes
-    probe = oracle_step_time(wl, [(0, 0)], 1)
-    frac = min(1.0, (120.0 / max(steps, 1)) / max(probe, 1e-6))
-    frac = max(frac, 1.0 / 64)
-    from oracle import oscar_oracle as O
-    hc, kb, vb = _oracle_row_cache(wl, 0, 0, wl.T0 + steps)
+    frac = min(1.0, max(1.0 / 64, (120.0 / max(steps, 1)) / max(probe, 1e-6)))
     keep = max(32, int(hc.n_packed * frac) // 32 * 32)
-    kq, vq = hc.packed_k(), hc.packed_v()
-    hc.k_codes = [O.QuantK(kq.codes[:keep], kq.step16[:keep // 32], kq.zero16[:keep // 32])]
-    hc.k_norm16 = [hc.packed_norm16()[:keep]]
-    hc.v_q = [O.QuantV(vq.codes[:keep], vq.step16[:keep], vq.zero16[:keep])]
-    g, tau = wl.g, 1.0 / math.sqrt(128)
-    qs = [wl.q_bits([0], range(g), i)[0] for i in range(steps)]
-    for i in range(args.warmup):
-        hc.append(kb[wl.T0 + i], vb[wl.T0 + i])
-        hc.decode(O.rotate_q(qs[i]), tau)
-    t = time.perf_counter()
-    for i in range(args.warmup, steps):
-        hc.append(kb[wl.T0 + i], vb[wl.T0 + i])
-        hc.decode(O.rotate_q(qs[i]), tau)
-    per = (time.perf_counter() - t) / max(args.steps, 1)
+    _truncate_packed(hc, keep)
+    _oracle_steps(wl, hc, kb, vb, 0, 0, 1, args.warmup)
+    t = _oracle_steps(wl, hc, kb, vb, 0, 0, 1 + args.warmup, args.steps)
+    per = t / max(args.steps, 1)
     scale = total_rows * (wl.n_packed / keep)
     value = per * scale * 1e6
     sample = (f"1 of {total_rows} rows per step over the first {keep} of {wl.n_packed} packed "
@@ -227,6 +220,17 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity for one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 # ---------------------------------------------------------------------------
@@ -254,7 +258,7 @@ def run_ours(args, world, rank, local):
     from int2_kv_cache_02_gb300 import oscar as L
     from int2_kv_cache_02_gb300 import workloads as W
 
-    wl = W.WORKLOADS[WORKLOAD]
+    wl = W.WORKLOADS[args.workload]
     tau = 1.0 / math.sqrt(128)
     W_, K_ = args.warmup, args.steps
     E_ = args.e2e_steps
@@ -321,11 +325,7 @@ def run_ours(args, world, rank, local):
 
     ms_total = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(b) for a, b in evs]
-    ms_step = ms_total / K_
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_total / K_, world, dev)
     dec_avg_ms = float(np.mean(dec_ms))
     achieved = (bytes_sum / K_) / (dec_avg_ms * 1e-3) / 1e9
 
@@ -355,10 +355,7 @@ def run_ours(args, world, rank, local):
     h2d = (Qh[0].numel() * Qh.element_size() + Kh[0].numel() * Kh.element_size()
            + Vh[0].numel() * Vh.element_size())
     d2h = out.numel() * out.element_size()
-    if world > 1:
-        t = torch.tensor([e2e_us], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_us = float(t.item())
+    e2e_us = max_over_ranks(e2e_us, world, dev)
 
     # ---- bf16 comparison kernel, same shape (context T0) ----
     bf16 = None
@@ -426,7 +423,7 @@ def run_ours(args, world, rank, local):
     }
     if bf16 is not None:
         line["bf16_decode"] = bf16
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)
