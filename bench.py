@@ -78,12 +78,18 @@ def _config(wl, S=None):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi polled every 100 ms in a child process; a reader thread
+    collects the lines.  ``start`` returns once the first sample arrived, so
+    the tool's own start-up never overlaps the timed region."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
+        import threading
+        self.lines = []
         self.proc = None
+        self.first = threading.Event()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -91,18 +97,31 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            self.first.set()
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line)
+            self.first.set()
+        self.first.set()
+
+    def wait_first(self, timeout=20.0):
+        self.first.wait(timeout)
 
     def stop(self):
         if self.proc is None:
             return []
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        self.reader.join(timeout=5)
         rows = []
-        for line in out.splitlines():
+        for line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 10:
                 continue
@@ -293,6 +312,7 @@ def run_ours(args, world, rank, local):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     vis = [v for v in vis.split(",") if v.strip().isdigit()]
     sampler = ClockSampler(int(vis[local]) if local < len(vis) else local)
+    sampler.wait_first()
     for i in range(W_):
         step(i)
     torch.cuda.synchronize()
@@ -396,8 +416,15 @@ def run_ours(args, world, rank, local):
     peak = peak or 6800.0
     traffic = None
     try:
+        import hashlib
         with open(TRAFFIC_FILE) as f:
-            traffic = json.load(f).get("dram_bytes_per_launch")
+            rec = json.load(f)
+        with open(os.path.join(HERE, "int2_kv_cache_02_gb300", "csrc", "decode_int2.cu"),
+                  "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+        # counters taken on another version of the kernel do not describe this one
+        if rec.get("kernel_source_sha256") == sha and wl.name == WORKLOAD:
+            traffic = rec.get("dram_bytes_per_launch")
     except (OSError, ValueError):
         traffic = None
 
