@@ -210,6 +210,34 @@ oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* 
                                          int num_splits, void* workspace, size_t ws_bytes,
                                          void* stream);
 
+/* Size of the static device array behind oscar_decode_attention_static_ws. */
+#define OSCAR_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * oscar_decode_attention without a workspace argument, for callers that
+ * cannot allocate device memory: for example a serving loop that allows no
+ * cudaMalloc after start-up (it can stall the device and fragment memory),
+ * or a plug-in whose host runtime owns all device memory and lends it no
+ * allocator.  The pages have no counterpart: this is an integration aid.
+ * Same arguments, results and checks as oscar_decode_attention, except that
+ * the split-K partial records live in a 16 MiB array inside the library
+ * (OSCAR_STATIC_SCRATCH_BYTES), which every GPU that loads the library keeps
+ * until the process exits.  The call allocates nothing.
+ *  - B * Hq * (splits + 1) * 528 bytes must fit in that array; larger
+ *    requests return OSCAR_ERR_WORKSPACE and launch nothing (the automatic
+ *    split count of a batch-48, 32-query-head layer needs about 16.2 MB).
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make it before any stream
+ *    capture.  A failed lookup returns OSCAR_ERR_CUDA.
+ *  - Every call shares the one array and it keeps the last call's contents;
+ *    calls whose kernels overlap on the GPU (e.g. on two streams) race on it.
+ *    No part of it needs to start at zero: each call writes every record it
+ *    reads.
+ */
+oscar_status oscar_decode_attention_static_ws(const oscar_cache* c, const float* q_rot, int Hq,
+                                              float softmax_scale, float* out, int num_splits,
+                                              void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  OSCAR_OK if no kernel recorded an error, else OSCAR_ERR_DEVICE_STATUS. */
 oscar_status oscar_device_status(void* stream);

@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build")
 
 LIBS = {
     "liboscar.so": ["rotate.cu", "quantize.cu", "decode_int2.cu", "decode_bf16.cu",
-                    "combine.cu", "api.cu"],
+                    "combine.cu", "api.cu", "decode_static.cu"],
     "liboscar_synth.so": ["synth.cu"],
 }
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -95,6 +95,12 @@ oscar_status flush_residual(oscar_cache* c, cudaStream_t s) {
 
 }  // namespace
 
+namespace oscar {
+// Internal accessors for other translation units of the library.
+unsigned* device_status_word() { return status_ptr(); }
+void count_launches(int n) { g_launches += (unsigned long long)n; }
+}  // namespace oscar
+
 extern "C" {
 
 oscar_status oscar_rotate_q(const oscar_bf16* q, float* q_rot, int B, int Hq, unsigned flags,

@@ -1,0 +1,115 @@
+// oscar_decode_attention_static_ws: the fused INT2 decode attention for
+// callers that cannot allocate device memory.
+//
+// oscar_decode_attention needs a caller-provided workspace for its split-K
+// partial records.  Some callers have no way to provide one: code that runs
+// where every device allocation must happen once at start-up (a serving loop
+// that forbids cudaMalloc after warm-up because it can block the device and
+// fragment memory), or a plug-in inside a runtime that owns all device memory
+// and exposes no allocator to it.  This entry point keeps the partials in a
+// fixed array in the library's own device memory instead, so the caller
+// passes only the cache, the queries and the output.
+//
+// The array is a file-scope static __device__ variable: every GPU that loads
+// the library holds OSCAR_STATIC_SCRATCH_BYTES of it until the process exits.
+// Host code only sees a stand-in for it, so its device address is looked up
+// with cudaGetSymbolAddress, once per device, on the first call made while
+// that device is current; make that first call before any stream capture.
+// All calls share the one array: calls whose kernels overlap on the GPU (two
+// streams, say) race on it and give wrong results.  Nothing in it has to
+// start at zero: every call writes each partial record before reading it, and
+// the array keeps whatever the last call left there.
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+using namespace oscar;
+
+constexpr size_t kScratchFloats = OSCAR_STATIC_SCRATCH_BYTES / sizeof(float);
+static __device__ __align__(256) float g_decode_scratch[kScratchFloats];
+
+std::mutex g_scratch_mu;
+float* g_scratch_addr[128] = {};
+
+// Device address of g_decode_scratch on the current device (set up on first use).
+float* scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  return g_scratch_addr[dev];
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
+                                                         const float* q_rot, int Hq,
+                                                         float softmax_scale, float* out,
+                                                         int num_splits, void* stream) {
+  // the same argument checks as oscar_decode_attention
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  if (c->B <= 0 || c->Hkv <= 0 || c->T_cap <= 0 || c->T_cap % kG != 0)
+    return OSCAR_ERR_INVALID_ARG;
+  const void* ptrs[] = {c->k_codes, c->v_codes, c->k_scale,  c->k_zero, c->k_norm,
+                        c->v_scale, c->v_zero,  c->k_res,    c->v_res,  c->k_res_norm};
+  for (const void* p : ptrs) {
+    if (!p) return OSCAR_ERR_INVALID_ARG;
+    if (!aligned16(p)) return OSCAR_ERR_ALIGNMENT;
+  }
+  if (c->n_packed < 0 || c->n_packed % kG != 0 || c->n_packed > c->T_cap || c->n_res < 0 ||
+      c->n_res > kR || (c->flags & ~3u))
+    return OSCAR_ERR_INVALID_ARG;
+  if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
+      !std::isfinite(softmax_scale))
+    return OSCAR_ERR_INVALID_ARG;
+  const int g = (Hq % c->Hkv == 0) ? Hq / c->Hkv : 0;
+  if (!(g == 1 || g == 2 || g == 4 || g == 8)) return OSCAR_ERR_UNSUPPORTED;
+  if (!aligned16(q_rot) || !aligned16(out)) return OSCAR_ERR_ALIGNMENT;
+
+  const int S = num_splits > 0 ? num_splits
+                               : oscar_decode_num_splits(c->B, c->Hkv, Hq, c->n_packed);
+  // the partial records must fit in the static array
+  const size_t need = (size_t)c->B * (size_t)Hq * (size_t)(S + 1) * kRecFloats;
+  if (need > kScratchFloats) return OSCAR_ERR_WORKSPACE;
+
+  float* ws = scratch_address();
+  if (!ws) return OSCAR_ERR_CUDA;
+
+  DecodeArgs a;
+  a.k_codes = c->k_codes;
+  a.v_codes = c->v_codes;
+  a.k_scale = reinterpret_cast<const __half*>(c->k_scale);
+  a.k_zero = reinterpret_cast<const __half*>(c->k_zero);
+  a.k_norm = reinterpret_cast<const __half*>(c->k_norm);
+  a.v_scale = reinterpret_cast<const __half*>(c->v_scale);
+  a.v_zero = reinterpret_cast<const __half*>(c->v_zero);
+  a.k_res = c->k_res;
+  a.v_res = c->v_res;
+  a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
+  a.q_rot = q_rot;
+  a.ws = ws;
+  a.out = out;
+  a.status = device_status_word();
+  a.B = c->B;
+  a.Hkv = c->Hkv;
+  a.Hq = Hq;
+  a.T_cap = c->T_cap;
+  a.n_packed = c->n_packed;
+  a.n_res = c->n_res;
+  a.num_splits = S;
+  a.flags = c->flags;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e = launch_decode_int2(a, static_cast<cudaStream_t>(stream));
+  count_launches(2);
+  return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
+}

@@ -63,6 +63,11 @@ struct Bf16DecodeArgs {
 cudaError_t launch_decode_bf16(const Bf16DecodeArgs& a, cudaStream_t s);
 int decode_bf16_ctas_per_sm(int g);
 
+// Device address of the current device's status word (nullptr if unavailable),
+// and the host launch counter behind oscar_kernel_launches().
+unsigned* device_status_word();
+void count_launches(int n);
+
 // Log-sum-exp combine of n_parts partial records per (b, q-head).
 cudaError_t launch_combine(const float* ws, float* out, int n_rows, int n_parts, cudaStream_t s);
 

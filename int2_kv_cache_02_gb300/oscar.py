@@ -54,6 +54,8 @@ def _load() -> ctypes.CDLL:
         "oscar_append_kv": (c_int, [P, c_void_p, c_void_p, c_int, c_void_p]),
         "oscar_decode_attention": (c_int, [P, c_void_p, c_int, c_float, c_void_p, c_int,
                                            c_void_p, c_size_t, c_void_p]),
+        "oscar_decode_attention_static_ws": (c_int, [P, c_void_p, c_int, c_float, c_void_p,
+                                                     c_int, c_void_p]),
         "oscar_decode_num_splits": (c_int, [c_int, c_int, c_int, c_int]),
         "oscar_decode_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
         "oscar_bf16_decode_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int,
@@ -199,6 +201,16 @@ def decode_attention(cache: KVCache, q_rot: torch.Tensor, Hq: int, softmax_scale
                                        num_splits, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream)), "oscar_decode_attention")
+
+
+def decode_attention_static_ws(cache: KVCache, q_rot: torch.Tensor, Hq: int,
+                               softmax_scale: float, out: torch.Tensor, num_splits: int = 0,
+                               stream=None):
+    """decode_attention for callers that cannot allocate: the split-K partials
+    use the library's own static device array (no workspace argument)."""
+    _check(_lib.oscar_decode_attention_static_ws(cache.ref(), _ptr(q_rot), Hq, softmax_scale,
+                                                 _ptr(out), num_splits, _stream(stream)),
+           "oscar_decode_attention_static_ws")
 
 
 def bf16_decode_attention(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, B: int, Hq: int,
