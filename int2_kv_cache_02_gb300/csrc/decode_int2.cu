@@ -15,15 +15,22 @@
 //    product keeps ~22 bits), the key zero z_c becomes one dot product
 //    Z = q'.z per block (itself an MMA), and the norm multiplies the score:
 //      score_t = tau * n_t * (sum_c q~_c code_tc + Z);
+//    Q.K^T runs with the query group as the M rows (hi parts in rows 0-7,
+//    lo parts in rows 8-15) and 8 tokens as the N columns;
 //  * values: p~_t = p_t s_t (hi + lo fp16) multiplies the centred codes
 //    code - 1.5 on the tensor cores; the per-token constant z_t + 1.5 s_t is
 //    accumulated as sum_t p_t (z_t + 1.5 s_t) and added per channel at the end;
 //  * 2-bit codes become fp16 operands in registers: a masked OR with the fp16
 //    bit pattern of 1024 places a code in the mantissa, one fp16 FMA removes
-//    the bias (exact), so the codes never travel through shared memory twice.
-// Stage ring: thread 0 issues seven 1-D bulk copies (TMA, cp.async.bulk) per
-// stage of NW blocks into a NSTAGE-deep shared-memory ring; mbarrier waits are
-// bounded and record kDevErrWaitTimeout instead of hanging.
+//    the bias (exact), so the codes never travel through shared memory twice;
+//  * for groups of 4 or fewer query heads the MMA rows repeat; the two lane
+//    halves that hold the same rows split the softmax work by token and swap
+//    one fp16 limb of p~ with a shuffle.
+// Each warp streams its own contiguous range of blocks through its own
+// NSTAGE-deep shared-memory ring: lanes 0-6 issue one 1-D bulk copy (TMA,
+// cp.async.bulk) each per block, completing on the warp's mbarrier.  Waits are
+// bounded and record kDevErrWaitTimeout instead of hanging; no CTA-wide
+// barrier runs inside the main loop.
 #include "common.cuh"
 #include "cta_merge.cuh"
 #include "launch.h"
@@ -31,51 +38,61 @@
 namespace oscar {
 namespace {
 
-constexpr int NW = 4;       // warps per CTA = blocks per stage
-constexpr int NSTAGE = 4;   // ring depth
-constexpr int kBlkBytes = 1024 + 1024 + 256 + 256 + 64 + 64 + 64;
-constexpr int kStageBytes = NW * kBlkBytes;
-constexpr int KC_OFF = 0;
-constexpr int VC_OFF = NW * 1024;
-constexpr int KS_OFF = NW * 2048;
-constexpr int KZ_OFF = NW * 2304;
-constexpr int KN_OFF = NW * 2560;
-constexpr int VS_OFF = NW * 2624;
-constexpr int VZ_OFF = NW * 2688;
-constexpr int kSmemBytes = NSTAGE * kStageBytes + NSTAGE * 8;
-static_assert(VZ_OFF + NW * 64 == kStageBytes, "stage layout");
+constexpr int NW = 4;       // warps per CTA
+constexpr int NSTAGE = 4;   // ring depth per warp (blocks in flight)
+// one 32-token block: key codes, value codes, key step, key zero, norms,
+// value step, value zero
+constexpr int KC_OFF = 0, VC_OFF = 1024, KS_OFF = 2048, KZ_OFF = 2304, KN_OFF = 2560,
+              VS_OFF = 2624, VZ_OFF = 2688, kBlkBytes = 2752;
+constexpr int kSmemBytes = NW * NSTAGE * kBlkBytes + NW * NSTAGE * 8;
 
 constexpr uint32_t kMagic = 0x64006400u;  // fp16x2 {1024, 1024}
 
 __device__ __forceinline__ uint32_t hfma2_u(uint32_t x, uint32_t s, uint32_t b) {
   return half2_as_u32(__hfma2(u32_as_half2(x), u32_as_half2(s), u32_as_half2(b)));
 }
-
-// Key word -> 8 fp16x2 code pairs (slot k: low/high half-word codes), values 0..3.
-__device__ __forceinline__ void unpack_k8(uint32_t w, uint32_t (&o)[8]) {
-  const uint32_t S[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
-  const uint32_t B[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u, 0xC400C400u};
-#pragma unroll
-  for (int k = 0; k < 5; ++k) o[k] = hfma2_u((w & (0x00030003u << (2 * k))) | kMagic, S[k], B[k]);
-  const uint32_t w2 = w >> 10;
-#pragma unroll
-  for (int k = 5; k < 8; ++k)
-    o[k] = hfma2_u((w2 & (0x00030003u << (2 * (k - 5)))) | kMagic, S[k - 5], B[k - 5]);
+// (a & MASK) | c in one LOP3 (truth table 0xEA), MASK an immediate.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t neg2_u(uint32_t x) {
+  return half2_as_u32(__hneg2(u32_as_half2(x)));
+}
+__device__ __forceinline__ uint32_t hmul2_u(uint32_t x, uint32_t y) {
+  return half2_as_u32(__hmul2(u32_as_half2(x), u32_as_half2(y)));
 }
 
-// Value word -> 8 fp16x2 centred code pairs (code - 1.5).
-__device__ __forceinline__ void unpack_v8(uint32_t w, uint32_t (&o)[8]) {
-  // index k-1 for k = 1..4: scale 4^-k, bias -(1024*4^-k + 1.5)
-  const uint32_t S[4] = {0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
-  const uint32_t B[4] = {0xDC06DC06u, 0xD418D418u, 0xCC60CC60u, 0xC580C580u};
-  o[0] = hfma2_u(((w << 2) & 0x000C000Cu) | kMagic, S[0], B[0]);
-#pragma unroll
-  for (int k = 1; k < 5; ++k)
-    o[k] = hfma2_u((w & (0x00030003u << (2 * k))) | kMagic, S[k - 1], B[k - 1]);
-  const uint32_t w8 = w >> 8;
-#pragma unroll
-  for (int k = 5; k < 8; ++k)
-    o[k] = hfma2_u((w8 & (0x00030003u << (2 * (k - 4)))) | kMagic, S[k - 5], B[k - 5]);
+// Key code pair at slot k (low/high half-word), as fp16x2 values 0..3.
+// w10 = w >> 10 carries slots 5..7 down to 0..2.
+template <int K>
+__device__ __forceinline__ uint32_t key_pair(uint32_t w, uint32_t w10, uint32_t magic) {
+  constexpr uint32_t S[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
+  constexpr uint32_t B[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u, 0xC400C400u};
+  if constexpr (K < 5) {
+    return hfma2_u(and_or<(0x00030003u << (2 * K))>(w, magic), S[K], B[K]);
+  } else {
+    return hfma2_u(and_or<(0x00030003u << (2 * (K - 5)))>(w10, magic), S[K - 5], B[K - 5]);
+  }
+}
+
+// Value code pair at slot k as fp16x2 centred values code - 1.5.
+// w2 = w << 2 carries slot 0 to position 1, w8 = w >> 8 slots 5..7 to 1..3.
+template <int K>
+__device__ __forceinline__ uint32_t value_pair(uint32_t w, uint32_t w2, uint32_t w8,
+                                                  uint32_t magic) {
+  // position p = 1..4: scale 4^-p, bias -(1024 * 4^-p + 1.5)
+  constexpr uint32_t S[4] = {0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
+  constexpr uint32_t B[4] = {0xDC06DC06u, 0xD418D418u, 0xCC60CC60u, 0xC580C580u};
+  if constexpr (K == 0) {
+    return hfma2_u(and_or<0x000C000Cu>(w2, magic), S[0], B[0]);
+  } else if constexpr (K < 5) {
+    return hfma2_u(and_or<(0x00030003u << (2 * K))>(w, magic), S[K - 1], B[K - 1]);
+  } else {
+    return hfma2_u(and_or<(0x00030003u << (2 * (K - 4)))>(w8, magic), S[K - 5], B[K - 5]);
+  }
 }
 
 __device__ __forceinline__ float warp_allsum(float v) {
@@ -85,11 +102,11 @@ __device__ __forceinline__ float warp_allsum(float v) {
 }
 
 template <int GQ>
-__global__ void __launch_bounds__(NW * 32) decode_int2_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(NW * 32, 3) decode_int2_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + NSTAGE * kStageBytes);
+  uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + NW * NSTAGE * kBlkBytes);
   auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
-  static_assert(sizeof(MergeSmem<GQ, NW>) <= NSTAGE * kStageBytes, "merge area");
+  static_assert(sizeof(MergeSmem<GQ, NW>) <= NW * NSTAGE * kBlkBytes, "merge area");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -99,24 +116,34 @@ __global__ void __launch_bounds__(NW * 32) decode_int2_kernel(const DecodeArgs a
 
   if (split < a.num_splits) {
     // ------------------------------------------------------------ packed
-    constexpr int NT = (GQ == 8) ? 2 : 1;        // PV n-tiles (hi / lo limbs for GQ = 8)
-    const int head = (GQ == 8) ? gid : (gid % GQ);
+    constexpr bool kSplitHalves = GQ <= 4;         // rows repeat: halves share the softmax
+    constexpr int NT = kSplitHalves ? 1 : 2;       // P.V n-tiles (GQ = 8: hi, lo limbs)
+    constexpr int NTOK = kSplitHalves ? 4 : 8;     // softmax tokens per thread per block
+    const int head = kSplitHalves ? (gid % GQ) : gid;
+    const int hf = kSplitHalves ? (gid >> 2) : 0;  // which n-tile pair this lane scores
     const int nblk = a.n_packed / kG;
     const int b0 = (int)((long long)nblk * split / a.num_splits);
     const int b1 = (int)((long long)nblk * (split + 1) / a.num_splits);
-    const int n_iter = (b1 - b0 + NW - 1) / NW;
+    const int wb0 = b0 + (int)((long long)(b1 - b0) * warp / NW);
+    const int wb1 = b0 + (int)((long long)(b1 - b0) * (warp + 1) / NW);
+    const int n = wb1 - wb0;
+    uint8_t* ring = smem + warp * NSTAGE * kBlkBytes;
+    uint64_t* bars = bars_all + warp * NSTAGE;
 
-    // Query fragments: this thread's head, channels 32*tig .. 32*tig+31,
-    // scaled by a power of two sigma so that fp16 hi/lo parts keep range.
-    uint32_t qh[8][2], ql[8][2];
-    float cst;
+    // Query fragments of this thread's head, channels c0 = 32*tig + 4*k8 ..+3,
+    // as {hi(c0,c0+1), lo(c0,c0+1), hi(c0+2,c0+3), lo(c0+2,c0+3)} (the MMA A
+    // layout of rows g and g+8).  The query carries softmax_scale * log2(e)
+    // and a power of two sigma that keeps the fp16 parts in range.
+    uint32_t aq[8][4];
+    float inv_sigma;
     {
       const float4* qp = reinterpret_cast<const float4*>(a.q_rot + (qrow0 + head) * kD + 32 * tig);
       float qf[32];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float4 v = qp[i];
-        qf[4 * i] = v.x; qf[4 * i + 1] = v.y; qf[4 * i + 2] = v.z; qf[4 * i + 3] = v.w;
+        qf[4 * i] = v.x * a.scale_log2; qf[4 * i + 1] = v.y * a.scale_log2;
+        qf[4 * i + 2] = v.z * a.scale_log2; qf[4 * i + 3] = v.w * a.scale_log2;
       }
       float amax = 0.0f;
 #pragma unroll
@@ -128,224 +155,274 @@ __global__ void __launch_bounds__(NW * 32) decode_int2_kernel(const DecodeArgs a
       int sh = (amax > 0.0f) ? (((a.flags & OSCAR_NO_SCALE) ? 1 : 14) - e) : 0;
       sh = max(-100, min(100, sh));
       const float sigma = ldexpf(1.0f, sh);
-      cst = ldexpf(a.scale_log2, -sh);
+      inv_sigma = ldexpf(1.0f, -sh);
 #pragma unroll
       for (int k8 = 0; k8 < 8; ++k8) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           const float x0 = qf[4 * k8 + 2 * j] * sigma, x1 = qf[4 * k8 + 2 * j + 1] * sigma;
           const __half2 hh = __floats2half2_rn(x0, x1);
-          const float2 hf = __half22float2(hh);
-          qh[k8][j] = half2_as_u32(hh);
-          ql[k8][j] = half2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+          const float2 hv = __half22float2(hh);
+          aq[k8][2 * j] = half2_as_u32(hh);
+          aq[k8][2 * j + 1] = half2_as_u32(__floats2half2_rn(x0 - hv.x, x1 - hv.y));
         }
       }
     }
 
     float O[NT][8][4];
 #pragma unroll
-    for (int n = 0; n < NT; ++n)
+    for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) O[n][mt][e] = 0.0f;
+        for (int e = 0; e < 4; ++e) O[t][mt][e] = 0.0f;
     float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
+    // The fp16x2 bit pattern of {1024, 1024}, kept in a register so that each
+    // code extraction is one LOP3 (mask immediate, this register).
+    uint32_t magic = kMagic;
+    asm volatile("" : "+r"(magic));
 
-    if (tid == 0) {
+    if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
       mbar_fence_init();
     }
-    __syncthreads();
+    __syncwarp();
 
-    auto issue = [&](int it, int slot) {
-      const int blk = b0 + it * NW;
-      const int nb = min(NW, b1 - blk);
-      uint8_t* st = smem + slot * kStageBytes;
-      uint64_t* bar = &bars[slot];
-      mbar_arrive_expect_tx(bar, nb * kBlkBytes);
-      const long long kb = row * (a.T_cap / kG) + blk;
-      const long long kt = row * (long long)a.T_cap + (long long)blk * kG;
-      bulk_g2s(st + KC_OFF, a.k_codes + kt * 8, nb * 1024, bar);
-      bulk_g2s(st + VC_OFF, a.v_codes + kb * 256, nb * 1024, bar);
-      bulk_g2s(st + KS_OFF, a.k_scale + kb * kD, nb * 256, bar);
-      bulk_g2s(st + KZ_OFF, a.k_zero + kb * kD, nb * 256, bar);
-      bulk_g2s(st + KN_OFF, a.k_norm + kt, nb * 64, bar);
-      bulk_g2s(st + VS_OFF, a.v_scale + kt, nb * 64, bar);
-      bulk_g2s(st + VZ_OFF, a.v_zero + kt, nb * 64, bar);
+    // Block i of this warp into ring slot `slot`: lane 0 issues the seven
+    // copies; every address is warp-uniform.
+    const long long nbr = a.T_cap / kG;             // blocks per row
+    auto issue = [&](int i, int slot) {
+      if (lane == 0) {
+        const long long kb = row * nbr + (wb0 + i);  // block index in the packed arrays
+        const long long kt = kb * kG;                // its first token
+        uint8_t* st = ring + slot * kBlkBytes;
+        uint64_t* bar = &bars[slot];
+        mbar_arrive_expect_tx(bar, kBlkBytes);
+        bulk_g2s(st + KC_OFF, a.k_codes + kt * 8, 1024, bar);
+        bulk_g2s(st + VC_OFF, a.v_codes + kb * 256, 1024, bar);
+        bulk_g2s(st + KS_OFF, a.k_scale + kb * kD, 256, bar);
+        bulk_g2s(st + KZ_OFF, a.k_zero + kb * kD, 256, bar);
+        bulk_g2s(st + KN_OFF, a.k_norm + kt, 64, bar);
+        bulk_g2s(st + VS_OFF, a.v_scale + kt, 64, bar);
+        bulk_g2s(st + VZ_OFF, a.v_zero + kt, 64, bar);
+      }
     };
 
-    int issued = 0;
-    if (tid == 0) {
-      issued = min(NSTAGE, n_iter);
-      for (int s = 0; s < issued; ++s) issue(s, s);
-    }
+    int issued = min(NSTAGE, n);
+    for (int s = 0; s < issued; ++s) issue(s, s);
 
-    bool bad = false;
+    bool ok = true;
     int it = 0;
-    for (; it < n_iter; ++it) {
+    for (; it < n; ++it) {
       const int slot = it % NSTAGE;
-      bool ok = mbar_wait_bounded(&bars[slot], (unsigned)((it / NSTAGE) & 1), kWaitLimit);
-      ok = __all_sync(0xffffffffu, ok);
-      const int blk = b0 + it * NW + warp;
-      if (ok && blk < b1) {
-        const uint8_t* st = smem + slot * kStageBytes;
-        const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + KC_OFF) + warp * 256;
-        const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + VC_OFF) + warp * 256;
-        const uint4* ks4 = reinterpret_cast<const uint4*>(st + KS_OFF + warp * 256) + tig * 4;
-        const uint4* kz4 = reinterpret_cast<const uint4*>(st + KZ_OFF + warp * 256) + tig * 4;
-        const uint32_t* kn2 = reinterpret_cast<const uint32_t*>(st + KN_OFF + warp * 64);
-        const uint32_t* vs2 = reinterpret_cast<const uint32_t*>(st + VS_OFF + warp * 64);
-        const uint32_t* vz2 = reinterpret_cast<const uint32_t*>(st + VZ_OFF + warp * 64);
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait_bounded(&bars[slot], (unsigned)((it / NSTAGE) & 1), kWaitLimit));
+      if (!ok) break;
+      const uint8_t* st = ring + slot * kBlkBytes;
+      const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + KC_OFF);
+      const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + VC_OFF);
+      const uint4* ks4 = reinterpret_cast<const uint4*>(st + KS_OFF) + tig * 4;
+      const uint4* kz4 = reinterpret_cast<const uint4*>(st + KZ_OFF) + tig * 4;
+      const uint32_t* kn2 = reinterpret_cast<const uint32_t*>(st + KN_OFF);
+      const uint32_t* vs2 = reinterpret_cast<const uint32_t*>(st + VS_OFF);
+      const uint32_t* vz2 = reinterpret_cast<const uint32_t*>(st + VZ_OFF);
 
-        // Z = q'.z_block (hi row g, lo row g+8), broadcast to all 8 columns.
-        float dz[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t at[8][4];
+      // Z = q'.z of the block: rows g (hi) and g+8 (lo), every column alike.
+      float dz[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 sv = ks4[i];
-          const uint4 zv = kz4[i];
-          const uint32_t sr[4] = {sv.x, sv.y, sv.z, sv.w};
-          const uint32_t zr[4] = {zv.x, zv.y, zv.z, zv.w};
+      for (int i = 0; i < 4; ++i) {
+        const uint4 zv = kz4[i];
+        mma_16816_acc(dz, aq[2 * i], zv.x, zv.y);
+        mma_16816_acc(dz, aq[2 * i + 1], zv.z, zv.w);
+      }
+
+      // Q.K^T, k-step outer: q~ fragment for k-step k8, then the 4 n-tiles.
+      uint32_t kw[4][2], kw10[4][2];
 #pragma unroll
-          for (int hk = 0; hk < 2; ++hk) {
-            const int k8 = 2 * i + hk;
-            const uint32_t aq[4] = {qh[k8][0], ql[k8][0], qh[k8][1], ql[k8][1]};
-            mma_16816(dz, aq, zr[2 * hk], zr[2 * hk + 1], dz);
-            // q~ = q' * s as fp16 hi + lo (exact product error via FMA).
+      for (int nt = 0; nt < 4; ++nt) {
+        const uint2 v = *reinterpret_cast<const uint2*>(kc + (8 * nt + gid) * 8 + 2 * tig);
+        kw[nt][0] = v.x; kw[nt][1] = v.y;
+        kw10[nt][0] = v.x >> 10; kw10[nt][1] = v.y >> 10;
+      }
+      float acc[4][4];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const __half2 s = u32_as_half2(sr[2 * hk + j]);
-              const __half2 q1 = u32_as_half2(qh[k8][j]);
-              const __half2 hi = __hmul2(q1, s);
-              const __half2 lo =
-                  __hadd2(__hfma2(q1, s, __hneg2(hi)), __hmul2(u32_as_half2(ql[k8][j]), s));
-              at[k8][2 * j] = half2_as_u32(hi);
-              at[k8][2 * j + 1] = half2_as_u32(lo);
+      for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = dz[e];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 sv = ks4[i];
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk) {
+          const int k8 = 2 * i + hk;
+          const uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
+          uint32_t at[4];
+          at[0] = hmul2_u(aq[k8][0], s01);
+          at[1] = hfma2_u(aq[k8][1], s01, hfma2_u(aq[k8][0], s01, neg2_u(at[0])));
+          at[2] = hmul2_u(aq[k8][2], s23);
+          at[3] = hfma2_u(aq[k8][3], s23, hfma2_u(aq[k8][2], s23, neg2_u(at[2])));
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) {
+            const uint32_t w = kw[nt][k8 >> 2], w10 = kw10[nt][k8 >> 2];
+            uint32_t b0v, b1v;
+            switch (k8 & 3) {
+              case 0: b0v = key_pair<0>(w, w10, magic); b1v = key_pair<1>(w, w10, magic); break;
+              case 1: b0v = key_pair<2>(w, w10, magic); b1v = key_pair<3>(w, w10, magic); break;
+              case 2: b0v = key_pair<4>(w, w10, magic); b1v = key_pair<5>(w, w10, magic); break;
+              default: b0v = key_pair<6>(w, w10, magic); b1v = key_pair<7>(w, w10, magic); break;
             }
+            mma_16816_acc(acc[nt], at, b0v, b1v);
           }
         }
+      }
 
-        // Scores for 4 n-tiles of 8 tokens: thread holds tokens 8nt+2tig, +1.
-        float sc[8];
+      // Scores of this thread's tokens (log2 domain): hi row + lo row, times
+      // the token norm.  Token j of the thread: n-tile nt(j), tokens 2tig, +1.
+      float sc[NTOK];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const uint2 kw = *reinterpret_cast<const uint2*>(kc + (8 * nt + gid) * 8 + 2 * tig);
-          uint32_t bk0[8], bk1[8];
-          unpack_k8(kw.x, bk0);
-          unpack_k8(kw.y, bk1);
-          float acc[4] = {dz[0], dz[1], dz[2], dz[3]};
-#pragma unroll
-          for (int k8 = 0; k8 < 4; ++k8) mma_16816(acc, at[k8], bk0[2 * k8], bk0[2 * k8 + 1], acc);
-#pragma unroll
-          for (int k8 = 0; k8 < 4; ++k8)
-            mma_16816(acc, at[4 + k8], bk1[2 * k8], bk1[2 * k8 + 1], acc);
-          const float2 nf = __half22float2(u32_as_half2(kn2[4 * nt + tig]));
-          sc[2 * nt] = (acc[0] + acc[2]) * (nf.x * cst);
-          sc[2 * nt + 1] = (acc[1] + acc[3]) * (nf.y * cst);
+      for (int j = 0; j < NTOK / 2; ++j) {
+        const int nt = kSplitHalves ? (2 * hf + j) : j;
+        float c0, c1, c2, c3;
+        if (kSplitHalves) {
+          c0 = hf ? acc[2 + j][0] : acc[j][0]; c1 = hf ? acc[2 + j][1] : acc[j][1];
+          c2 = hf ? acc[2 + j][2] : acc[j][2]; c3 = hf ? acc[2 + j][3] : acc[j][3];
+        } else {
+          c0 = acc[j][0]; c1 = acc[j][1]; c2 = acc[j][2]; c3 = acc[j][3];
         }
+        const float2 nf = __half22float2(u32_as_half2(kn2[4 * nt + tig]));
+        sc[2 * j] = (c0 + c2) * (nf.x * inv_sigma);
+        sc[2 * j + 1] = (c1 + c3) * (nf.y * inv_sigma);
+      }
 
-        // Online softmax (log2 domain) for this thread's head.
-        float mb = sc[0];
+      // Online softmax for this thread's head.
+      float mb = sc[0];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) mb = fmaxf(mb, sc[i]);
-        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-        const float m_new = fmaxf(m_run, mb);
-        if (__any_sync(0xffffffffu, m_new > m_run)) {
-          const float alpha = fast_exp2(m_run - m_new);
-          l_run *= alpha;
-          z_run *= alpha;
-          const int ha = (GQ == 8) ? 2 * tig : (2 * tig) % GQ;
-          const int hb = (GQ == 8) ? 2 * tig + 1 : (2 * tig + 1) % GQ;
-          const float al_a = __shfl_sync(0xffffffffu, alpha, 4 * ha);
-          const float al_b = __shfl_sync(0xffffffffu, alpha, 4 * hb);
+      for (int i = 1; i < NTOK; ++i) mb = fmaxf(mb, sc[i]);
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      if (kSplitHalves) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+      const float m_new = fmaxf(m_run, mb);
+      if (__any_sync(0xffffffffu, m_new > m_run)) {
+        const float alpha = fast_exp2(m_run - m_new);
+        l_run *= alpha;
+        z_run *= alpha;
+        const int ha = kSplitHalves ? (2 * tig) % GQ : 2 * tig;
+        const int hb = kSplitHalves ? (2 * tig + 1) % GQ : 2 * tig + 1;
+        const float al_a = __shfl_sync(0xffffffffu, alpha, 4 * ha);
+        const float al_b = __shfl_sync(0xffffffffu, alpha, 4 * hb);
 #pragma unroll
-          for (int n = 0; n < NT; ++n)
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              O[n][mt][0] *= al_a; O[n][mt][1] *= al_b;
-              O[n][mt][2] *= al_a; O[n][mt][3] *= al_b;
-            }
-          m_run = m_new;
+          for (int mt = 0; mt < 8; ++mt) {
+            O[t][mt][0] *= al_a; O[t][mt][1] *= al_b;
+            O[t][mt][2] *= al_a; O[t][mt][3] *= al_b;
+          }
+        m_run = m_new;
+      }
+
+      float pt[NTOK];
+#pragma unroll
+      for (int j = 0; j < NTOK / 2; ++j) {
+        const int nt = kSplitHalves ? (2 * hf + j) : j;
+        const float2 sv = __half22float2(u32_as_half2(vs2[4 * nt + tig]));
+        const float2 zv = __half22float2(u32_as_half2(vz2[4 * nt + tig]));
+        const float p0 = fast_exp2(sc[2 * j] - m_run);
+        const float p1 = fast_exp2(sc[2 * j + 1] - m_run);
+        l_run += p0 + p1;
+        z_run = fmaf(p0, fmaf(1.5f, sv.x, zv.x), z_run);
+        z_run = fmaf(p1, fmaf(1.5f, sv.y, zv.y), z_run);
+        pt[2 * j] = p0 * sv.x;
+        pt[2 * j + 1] = p1 * sv.y;
+      }
+
+      // P~ as the B operand of P.V: k-half kh uses n-tiles 2kh (tokens 2tig,
+      // 2tig+1) and 2kh+1 (2tig+8, 2tig+9); column gid is limb gid/4 (GQ <= 4).
+      uint32_t bp[2][2], bq[2][2];  // bp: limb for n-tile 0 of P.V; bq: lo limb (GQ = 8)
+      if (kSplitHalves) {
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const __half2 hv = __floats2half2_rn(pt[2 * r], pt[2 * r + 1]);
+          const float2 hf2 = __half22float2(hv);
+          hi[r] = half2_as_u32(hv);
+          lo[r] = half2_as_u32(__floats2half2_rn(pt[2 * r] - hf2.x, pt[2 * r + 1] - hf2.y));
         }
-
-        float pt[8];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const float2 sv = __half22float2(u32_as_half2(vs2[4 * nt + tig]));
-          const float2 zv = __half22float2(u32_as_half2(vz2[4 * nt + tig]));
-          const float p0 = fast_exp2(sc[2 * nt] - m_run);
-          const float p1 = fast_exp2(sc[2 * nt + 1] - m_run);
-          l_run += p0 + p1;
-          z_run = fmaf(p0, fmaf(1.5f, sv.x, zv.x), z_run);
-          z_run = fmaf(p1, fmaf(1.5f, sv.y, zv.y), z_run);
-          pt[2 * nt] = p0 * sv.x;
-          pt[2 * nt + 1] = p1 * sv.y;
-        }
-
-        // P~ as the B operand of P.V (tokens 2tig,2tig+1 | 2tig+8,2tig+9 per k-half).
-        uint32_t bh[2][2], bl[2][2];
+        // own limb for k-half hf; the partner lane (other half) needs my other limb
+        const uint32_t mine0 = hf ? lo[0] : hi[0], mine1 = hf ? lo[1] : hi[1];
+        const uint32_t give0 = hf ? hi[0] : lo[0], give1 = hf ? hi[1] : lo[1];
+        const uint32_t got0 = __shfl_xor_sync(0xffffffffu, give0, 16);
+        const uint32_t got1 = __shfl_xor_sync(0xffffffffu, give1, 16);
+        bp[0][0] = hf ? got0 : mine0; bp[0][1] = hf ? got1 : mine1;
+        bp[1][0] = hf ? mine0 : got0; bp[1][1] = hf ? mine1 : got1;
+      } else {
 #pragma unroll
         for (int kh = 0; kh < 2; ++kh)
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const float x0 = pt[4 * kh + 2 * r], x1 = pt[4 * kh + 2 * r + 1];
-            const __half2 hi = __floats2half2_rn(x0, x1);
-            const float2 hf = __half22float2(hi);
-            bh[kh][r] = half2_as_u32(hi);
-            bl[kh][r] = half2_as_u32(__floats2half2_rn(x0 - hf.x, x1 - hf.y));
+            const __half2 hv = __floats2half2_rn(x0, x1);
+            const float2 hf2 = __half22float2(hv);
+            bp[kh][r] = half2_as_u32(hv);
+            bq[kh][r] = half2_as_u32(__floats2half2_rn(x0 - hf2.x, x1 - hf2.y));
           }
+      }
 
 #pragma unroll
-        for (int kh = 0; kh < 2; ++kh) {
-          const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
-          uint32_t b0v, b1v;
-          if (GQ == 8) {
-            b0v = bh[kh][0]; b1v = bh[kh][1];
-          } else {
-            const bool lo_limb = gid >= 4;
-            b0v = lo_limb ? bl[kh][0] : bh[kh][0];
-            b1v = lo_limb ? bl[kh][1] : bh[kh][1];
-          }
+      for (int kh = 0; kh < 2; ++kh) {
+        const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
+        const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
+        uint32_t w2[4], w8[4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t va[8], vb[8];
-            unpack_v8(hh ? vw.y : vw.x, va);   // p = 0 (tokens 2tig, 2tig+1)
-            unpack_v8(hh ? vw.w : vw.z, vb);   // p = 1 (tokens 2tig+8, 2tig+9)
+        for (int q = 0; q < 4; ++q) { w2[q] = wv[q] << 2; w8[q] = wv[q] >> 8; }
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const int mt = 4 * hh + q4;
-              const uint32_t av[4] = {va[2 * q4], va[2 * q4 + 1], vb[2 * q4], vb[2 * q4 + 1]};
-              mma_16816(O[0][mt], av, b0v, b1v, O[0][mt]);
-              if (GQ == 8) mma_16816(O[NT - 1][mt], av, bl[kh][0], bl[kh][1], O[NT - 1][mt]);
-            }
+        for (int mt = 0; mt < 8; ++mt) {
+          const int hh = mt >> 2;
+          const int p0 = hh, p1 = 2 + hh;  // words of tokens (2tig,2tig+1) and (2tig+8,2tig+9)
+          uint32_t av[4];
+          switch (mt & 3) {
+            case 0:
+              av[0] = value_pair<0>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<1>(wv[p0], w2[p0], w8[p0], magic);
+              av[2] = value_pair<0>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<1>(wv[p1], w2[p1], w8[p1], magic);
+              break;
+            case 1:
+              av[0] = value_pair<2>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<3>(wv[p0], w2[p0], w8[p0], magic);
+              av[2] = value_pair<2>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<3>(wv[p1], w2[p1], w8[p1], magic);
+              break;
+            case 2:
+              av[0] = value_pair<4>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<5>(wv[p0], w2[p0], w8[p0], magic);
+              av[2] = value_pair<4>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<5>(wv[p1], w2[p1], w8[p1], magic);
+              break;
+            default:
+              av[0] = value_pair<6>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<7>(wv[p0], w2[p0], w8[p0], magic);
+              av[2] = value_pair<6>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<7>(wv[p1], w2[p1], w8[p1], magic);
+              break;
           }
+          mma_16816_acc(O[0][mt], av, bp[kh][0], bp[kh][1]);
+          if (!kSplitHalves) mma_16816_acc(O[NT - 1][mt], av, bq[kh][0], bq[kh][1]);
         }
       }
-      bad = __syncthreads_or(!ok);
-      if (bad) break;
-      if (tid == 0 && it + NSTAGE < n_iter) {
-        issue(it + NSTAGE, slot);
-        ++issued;
-      }
+      __syncwarp();
+      if (it + NSTAGE < n) issue(it + NSTAGE, slot);
     }
-    if (bad) {
-      if (tid == 0) {
+    if (!ok) {
+      if (lane == 0) {
         record_error(a.status, kDevErrWaitTimeout);
-        for (int s = it; s < issued; ++s)
+        for (int s = it; s < issued && s < n; ++s)
           if (!mbar_wait_bounded(&bars[s % NSTAGE], (unsigned)((s / NSTAGE) & 1), kDrainLimit))
             record_error(a.status, kDevErrDrainTimeout);
       }
-      return;
+      m_run = -INFINITY;   // this warp's result is void; the status word says so
     }
 
-    // Warp results: sums over the four lanes of a head, limbs folded.
+    // Warp results: sums over the lanes of a head, limbs folded.
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     z_run += __shfl_xor_sync(0xffffffffu, z_run, 1);
     z_run += __shfl_xor_sync(0xffffffffu, z_run, 2);
-    if (GQ != 8) {
+    if (kSplitHalves) {
+      l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
+      z_run += __shfl_xor_sync(0xffffffffu, z_run, 16);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -356,7 +433,7 @@ __global__ void __launch_bounds__(NW * 32) decode_int2_kernel(const DecodeArgs a
 #pragma unroll
         for (int e = 0; e < 4; ++e) O[0][mt][e] += O[NT - 1][mt][e];
     }
-    __syncthreads();   // the stage ring is dead: reuse it for the merge
+    __syncthreads();   // every warp is done with its ring: reuse it for the merge
     if (tig == 0 && gid < GQ) {
       E.m[warp][gid] = m_run;
       E.l[warp][gid] = l_run;
@@ -364,12 +441,12 @@ __global__ void __launch_bounds__(NW * 32) decode_int2_kernel(const DecodeArgs a
     }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int n = 2 * tig + e;
-      if (n < GQ) {
+      const int nc = 2 * tig + e;
+      if (nc < GQ) {
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-          E.o[warp][n][16 * mt + gid] = O[0][mt][e];
-          E.o[warp][n][16 * mt + gid + 8] = O[0][mt][2 + e];
+          E.o[warp][nc][16 * mt + gid] = O[0][mt][e];
+          E.o[warp][nc][16 * mt + gid + 8] = O[0][mt][2 + e];
         }
       }
     }
