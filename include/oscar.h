@@ -68,35 +68,34 @@ enum { OSCAR_NO_ROTATE = 1u, OSCAR_NO_SCALE = 2u };
  * device memory.  n_packed and n_res are uniform across the batch and are
  * advanced by the calls below (host-side bookkeeping).
  *
- * Packed layout, per (b, h) row, T_cap tokens of capacity (multiple of 32):
- *  k_codes  uint32 [B][Hkv][T_cap][8]   key codes, 16 per word.  Word w of a
- *           token holds channels 16w..16w+15; channel 16w+j sits at bit
- *           2*(j/2) + 16*(j%2) (even channels in the low half-word, odd in
- *           the high half-word).
- *  v_codes  uint32 [B][Hkv][T_cap/32][256] value codes, 16 per word, per
- *           block of 32 tokens: word 128*kh + 4*(4g+t) + 2p + hh (kh, p, hh
- *           in {0,1}, g in 0..7, t in 0..3) holds token 16kh+2t+8p in its low
- *           half-word and the next token in its high half-word; slot k (bits
- *           2k..2k+1 of a half) holds channel g + 8*(8hh+k).
- *  k_scale, k_zero fp16 [B][Hkv][T_cap/32][128] per (block, channel) step and
- *           zero of the keys ([rainbus] 方法步骤详情 (2), block size G = 32).
- *  k_norm   fp16 [B][Hkv][T_cap]  each key's L2 norm ([notes] Step Two).
- *  v_scale, v_zero fp16 [B][Hkv][T_cap] per-token step and zero of the values.
+ * Packed layout: one record of OSCAR_BLOCK_BYTES per block of 32 tokens,
+ * records [B][Hkv][T_cap/32] contiguous (T_cap a multiple of 32).  Byte
+ * offsets inside a record:
+ *     0  key codes    uint32 [32 tokens][8]: 16 codes per word; word w of a
+ *                     token holds channels 16w..16w+15, channel 16w+j at bit
+ *                     2*(j/2) + 16*(j%2) (even channels in the low half-word,
+ *                     odd channels in the high half-word)
+ *  1024  value codes  uint32 [256]: word 128*kh + 4*(4g+t) + 2p + hh (kh, p, hh
+ *                     in {0,1}, g in 0..7, t in 0..3) holds token 16kh+2t+8p
+ *                     in its low half-word and the next token in its high
+ *                     half-word; slot k (bits 2k..2k+1 of a half) holds channel
+ *                     g + 8*(8hh+k)
+ *  2048  key step     fp16 [128] per channel ([rainbus] 方法步骤详情 (2), G = 32)
+ *  2304  key zero     fp16 [128] per channel
+ *  2560  key norms    fp16 [32] per token ([notes] Step Two)
+ *  2624  value step   fp16 [32] per token
+ *  2688  value zero   fp16 [32] per token
  * Residual layout:
  *  k_res    bf16 [B][Hkv][128][128] rotated, unit-norm keys (slot = age order)
  *  v_res    bf16 [B][Hkv][128][128] values
  *  k_res_norm fp16 [B][Hkv][128]
  * Codes c in {0,1,2,3} dequantise to c*step + zero (x norm for keys).
  */
+#define OSCAR_BLOCK_BYTES 2752
+
 typedef struct {
   int B, Hkv, T_cap;
-  uint32_t* k_codes;
-  uint32_t* v_codes;
-  oscar_f16* k_scale;
-  oscar_f16* k_zero;
-  oscar_f16* k_norm;
-  oscar_f16* v_scale;
-  oscar_f16* v_zero;
+  uint8_t* packed;       /* [B][Hkv][T_cap/32] records of OSCAR_BLOCK_BYTES */
   oscar_bf16* k_res;
   oscar_bf16* v_res;
   oscar_f16* k_res_norm;

@@ -39,8 +39,7 @@ oscar_status check_cache(const oscar_cache* c) {
   if (!c) return OSCAR_ERR_INVALID_ARG;
   if (c->B <= 0 || c->Hkv <= 0 || c->T_cap <= 0 || c->T_cap % kG != 0)
     return OSCAR_ERR_INVALID_ARG;
-  const void* ptrs[] = {c->k_codes, c->v_codes, c->k_scale,  c->k_zero, c->k_norm,
-                        c->v_scale, c->v_zero,  c->k_res,    c->v_res,  c->k_res_norm};
+  const void* ptrs[] = {c->packed, c->k_res, c->v_res, c->k_res_norm};
   for (const void* p : ptrs) {
     if (!p) return OSCAR_ERR_INVALID_ARG;
     if (!al16(p)) return OSCAR_ERR_ALIGNMENT;
@@ -83,9 +82,7 @@ oscar_status flush_residual(oscar_cache* c, cudaStream_t s) {
   if (c->n_packed + kR > c->T_cap) return OSCAR_ERR_CAPACITY;
   cudaError_t e = launch_quantize_kv(
       c->k_res, reinterpret_cast<const __half*>(c->k_res_norm), c->v_res, kR, kR, c->B, c->Hkv,
-      c->T_cap, c->n_packed, c->k_codes, c->v_codes, reinterpret_cast<__half*>(c->k_scale),
-      reinterpret_cast<__half*>(c->k_zero), reinterpret_cast<__half*>(c->k_norm),
-      reinterpret_cast<__half*>(c->v_scale), reinterpret_cast<__half*>(c->v_zero), s);
+      c->T_cap, c->n_packed, c->packed, s);
   g_launches++;
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   c->n_packed += kR;
@@ -146,10 +143,7 @@ oscar_status oscar_quantize_kv(oscar_cache* c, const oscar_bf16* k_hat, const os
   if ((long long)c->n_packed + n_tok > c->T_cap) return OSCAR_ERR_CAPACITY;
   cudaError_t e = launch_quantize_kv(
       k_hat, reinterpret_cast<const __half*>(k_norm), v, src_T, n_tok, c->B, c->Hkv, c->T_cap,
-      c->n_packed, c->k_codes, c->v_codes, reinterpret_cast<__half*>(c->k_scale),
-      reinterpret_cast<__half*>(c->k_zero), reinterpret_cast<__half*>(c->k_norm),
-      reinterpret_cast<__half*>(c->v_scale), reinterpret_cast<__half*>(c->v_zero),
-      as_stream(stream));
+      c->n_packed, c->packed, as_stream(stream));
   g_launches++;
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   c->n_packed += n_tok;
@@ -220,13 +214,7 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   if (!workspace || ws_bytes < ws_bytes_for(c->B, Hq, S + 1)) return OSCAR_ERR_WORKSPACE;
   if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;
   DecodeArgs a;
-  a.k_codes = c->k_codes;
-  a.v_codes = c->v_codes;
-  a.k_scale = reinterpret_cast<const __half*>(c->k_scale);
-  a.k_zero = reinterpret_cast<const __half*>(c->k_zero);
-  a.k_norm = reinterpret_cast<const __half*>(c->k_norm);
-  a.v_scale = reinterpret_cast<const __half*>(c->v_scale);
-  a.v_zero = reinterpret_cast<const __half*>(c->v_zero);
+  a.packed = c->packed;
   a.k_res = c->k_res;
   a.v_res = c->v_res;
   a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);

@@ -14,6 +14,12 @@ constexpr int kD = OSCAR_HEAD_DIM;
 constexpr int kG = OSCAR_GROUP;
 constexpr int kR = OSCAR_RESIDUAL;
 
+// Byte offsets inside one packed 32-token block record (include/oscar.h).
+constexpr int kBlkBytes = OSCAR_BLOCK_BYTES;
+constexpr int kRecKC = 0, kRecVC = 1024, kRecKS = 2048, kRecKZ = 2304, kRecKN = 2560,
+              kRecVS = 2624, kRecVZ = 2688;
+static_assert(kRecVZ + 64 == kBlkBytes, "record layout");
+
 // Bits a kernel may OR into the device status word.
 enum : unsigned {
   kDevErrWaitTimeout = 1u,   // an mbarrier wait hit its iteration limit

@@ -27,8 +27,8 @@
 //    halves that hold the same rows split the softmax work by token and swap
 //    one fp16 limb of p~ with a shuffle.
 // Each warp streams its own contiguous range of blocks through its own
-// NSTAGE-deep shared-memory ring: lanes 0-6 issue one 1-D bulk copy (TMA,
-// cp.async.bulk) each per block, completing on the warp's mbarrier.  Waits are
+// NSTAGE-deep shared-memory ring: one 1-D bulk copy (TMA, cp.async.bulk) of
+// the block's 2752-byte record per block, completing on the warp's mbarrier.  Waits are
 // bounded and record kDevErrWaitTimeout instead of hanging; no CTA-wide
 // barrier runs inside the main loop.
 #include "common.cuh"
@@ -40,10 +40,10 @@ namespace {
 
 constexpr int NW = 4;       // warps per CTA
 constexpr int NSTAGE = 4;   // ring depth per warp (blocks in flight)
-// one 32-token block: key codes, value codes, key step, key zero, norms,
-// value step, value zero
-constexpr int KC_OFF = 0, VC_OFF = 1024, KS_OFF = 2048, KZ_OFF = 2304, KN_OFF = 2560,
-              VS_OFF = 2624, VZ_OFF = 2688, kBlkBytes = 2752;
+// one 32-token block record: key codes, value codes, key step, key zero,
+// norms, value step, value zero
+constexpr int KC_OFF = kRecKC, VC_OFF = kRecVC, KS_OFF = kRecKS, KZ_OFF = kRecKZ,
+              KN_OFF = kRecKN, VS_OFF = kRecVS, VZ_OFF = kRecVZ;
 constexpr int kSmemBytes = NW * NSTAGE * kBlkBytes + NW * NSTAGE * 8;
 
 constexpr uint32_t kMagic = 0x64006400u;  // fp16x2 {1024, 1024}
@@ -189,23 +189,15 @@ __global__ void __launch_bounds__(NW * 32, 3) decode_int2_kernel(const DecodeArg
     }
     __syncwarp();
 
-    // Block i of this warp into ring slot `slot`: lane 0 issues the seven
-    // copies; every address is warp-uniform.
-    const long long nbr = a.T_cap / kG;             // blocks per row
+    // Block i of this warp into ring slot `slot`: lane 0 copies its record
+    // (one 1-D bulk copy; the shared-memory slot has the record's layout).
+    const uint8_t* rows_rec = a.packed + row * (long long)(a.T_cap / kG) * kBlkBytes;
     auto issue = [&](int i, int slot) {
       if (lane == 0) {
-        const long long kb = row * nbr + (wb0 + i);  // block index in the packed arrays
-        const long long kt = kb * kG;                // its first token
-        uint8_t* st = ring + slot * kBlkBytes;
         uint64_t* bar = &bars[slot];
         mbar_arrive_expect_tx(bar, kBlkBytes);
-        bulk_g2s(st + KC_OFF, a.k_codes + kt * 8, 1024, bar);
-        bulk_g2s(st + VC_OFF, a.v_codes + kb * 256, 1024, bar);
-        bulk_g2s(st + KS_OFF, a.k_scale + kb * kD, 256, bar);
-        bulk_g2s(st + KZ_OFF, a.k_zero + kb * kD, 256, bar);
-        bulk_g2s(st + KN_OFF, a.k_norm + kt, 64, bar);
-        bulk_g2s(st + VS_OFF, a.v_scale + kt, 64, bar);
-        bulk_g2s(st + VZ_OFF, a.v_zero + kt, 64, bar);
+        bulk_g2s(ring + slot * kBlkBytes, rows_rec + (long long)(wb0 + i) * kBlkBytes, kBlkBytes,
+                 bar);
       }
     };
 

@@ -60,8 +60,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   if (!c) return OSCAR_ERR_INVALID_ARG;
   if (c->B <= 0 || c->Hkv <= 0 || c->T_cap <= 0 || c->T_cap % kG != 0)
     return OSCAR_ERR_INVALID_ARG;
-  const void* ptrs[] = {c->k_codes, c->v_codes, c->k_scale,  c->k_zero, c->k_norm,
-                        c->v_scale, c->v_zero,  c->k_res,    c->v_res,  c->k_res_norm};
+  const void* ptrs[] = {c->packed, c->k_res, c->v_res, c->k_res_norm};
   for (const void* p : ptrs) {
     if (!p) return OSCAR_ERR_INVALID_ARG;
     if (!aligned16(p)) return OSCAR_ERR_ALIGNMENT;
@@ -86,13 +85,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   if (!ws) return OSCAR_ERR_CUDA;
 
   DecodeArgs a;
-  a.k_codes = c->k_codes;
-  a.v_codes = c->v_codes;
-  a.k_scale = reinterpret_cast<const __half*>(c->k_scale);
-  a.k_zero = reinterpret_cast<const __half*>(c->k_zero);
-  a.k_norm = reinterpret_cast<const __half*>(c->k_norm);
-  a.v_scale = reinterpret_cast<const __half*>(c->v_scale);
-  a.v_zero = reinterpret_cast<const __half*>(c->v_zero);
+  a.packed = c->packed;
   a.k_res = c->k_res;
   a.v_res = c->v_res;
   a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);

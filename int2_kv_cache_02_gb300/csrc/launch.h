@@ -16,20 +16,14 @@ cudaError_t launch_rotate_scale_k(const uint16_t* k, int in_T, uint16_t* k_hat, 
                                   const uint16_t* v_in, uint16_t* v_out, unsigned flags,
                                   cudaStream_t s);
 
+// Quantises tokens [0, n_tok) of each source row into the block records of
+// packed positions [p0, p0 + n_tok).
 cudaError_t launch_quantize_kv(const uint16_t* k_hat, const __half* k_norm, const uint16_t* v,
                                int src_T, int n_tok, int B, int Hkv, int T_cap, int p0,
-                               uint32_t* k_codes, uint32_t* v_codes, __half* k_scale,
-                               __half* k_zero, __half* k_norm_out, __half* v_scale,
-                               __half* v_zero, cudaStream_t s);
+                               uint8_t* packed, cudaStream_t s);
 
 struct DecodeArgs {
-  const uint32_t* k_codes;
-  const uint32_t* v_codes;
-  const __half* k_scale;
-  const __half* k_zero;
-  const __half* k_norm;
-  const __half* v_scale;
-  const __half* v_zero;
+  const uint8_t* packed;   // block records [B][Hkv][T_cap/32]
   const uint16_t* k_res;
   const uint16_t* v_res;
   const __half* k_res_norm;

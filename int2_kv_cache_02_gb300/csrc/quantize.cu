@@ -11,7 +11,7 @@
 //
 // One CTA of 128 threads per (b, h, block of 32 tokens): the 32x128 key and
 // value tiles are staged in shared memory, codes computed one byte each, then
-// packed 16 per word into the cache layouts declared in oscar.h.
+// packed 16 per word into the block record declared in oscar.h.
 #include "common.cuh"
 #include "launch.h"
 
@@ -32,9 +32,7 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
 __global__ void __launch_bounds__(128) quantize_kv_kernel(
     const uint16_t* __restrict__ k_hat, const __half* __restrict__ k_norm,
     const uint16_t* __restrict__ v, int src_T, int Hkv, int T_cap, int p0,
-    uint32_t* __restrict__ k_codes, uint32_t* __restrict__ v_codes,
-    __half* __restrict__ k_scale, __half* __restrict__ k_zero, __half* __restrict__ k_norm_out,
-    __half* __restrict__ v_scale, __half* __restrict__ v_zero) {
+    uint8_t* __restrict__ packed) {
   __shared__ __align__(16) uint16_t kt[kG][kD];
   __shared__ __align__(16) uint16_t vt[kG][kD];
   __shared__ __align__(16) uint8_t kc[kG][kD];
@@ -60,7 +58,14 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
   __syncthreads();
 
   const long long pblk = (long long)p0 / kG + blk;   // packed block index in the row
-  const long long ptok = (long long)p0 + (long long)blk * kG;
+  uint8_t* rec = packed + (row * (T_cap / kG) + pblk) * kBlkBytes;
+  uint32_t* k_codes = reinterpret_cast<uint32_t*>(rec + kRecKC);
+  uint32_t* v_codes = reinterpret_cast<uint32_t*>(rec + kRecVC);
+  __half* k_scale = reinterpret_cast<__half*>(rec + kRecKS);
+  __half* k_zero = reinterpret_cast<__half*>(rec + kRecKZ);
+  __half* k_norm_out = reinterpret_cast<__half*>(rec + kRecKN);
+  __half* v_scale = reinterpret_cast<__half*>(rec + kRecVS);
+  __half* v_zero = reinterpret_cast<__half*>(rec + kRecVZ);
 
   // Keys: thread = channel, group = the 32 tokens of the block.
   {
@@ -76,9 +81,8 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
     const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), 3.0f) : 0.0f;
 #pragma unroll 8
     for (int t = 0; t < kG; ++t) kc[t][c] = quant_code(bf16_bits_to_float(kt[t][c]), mn, step, live);
-    const long long pi = (row * (T_cap / kG) + pblk) * kD + c;
-    k_scale[pi] = __float2half_rn(step);
-    k_zero[pi] = __float2half_rn(mn);
+    k_scale[c] = __float2half_rn(step);
+    k_zero[c] = __float2half_rn(mn);
   }
 
   // Values: warp w handles tokens 8w..8w+7, lane holds channels 4l..4l+3.
@@ -102,12 +106,12 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
 #pragma unroll
       for (int j = 0; j < 4; ++j) vc[t][4 * lane + j] = quant_code(x[j], mn, step, live);
       if (lane == 0) {
-        v_scale[row * T_cap + ptok + t] = __float2half_rn(step);
-        v_zero[row * T_cap + ptok + t] = __float2half_rn(mn);
+        v_scale[t] = __float2half_rn(step);
+        v_zero[t] = __float2half_rn(mn);
       }
     }
   }
-  if (tid < kG) k_norm_out[row * T_cap + ptok + tid] = k_norm[src_tok + tid];
+  if (tid < kG) k_norm_out[tid] = k_norm[src_tok + tid];
   __syncthreads();
 
   // Pack keys: word (t, w) = channels 16w..16w+15 of token t; channel 16w+j at
@@ -120,7 +124,7 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
     uint32_t word = 0;
 #pragma unroll
     for (int j = 0; j < 16; ++j) word |= (uint32_t)src[j] << (2 * (j >> 1) + 16 * (j & 1));
-    k_codes[(row * T_cap + ptok + t) * 8 + w] = word;
+    k_codes[t * 8 + w] = word;
   }
   // Pack values: word 128*kh + 4*lane + 2p + hh, lane = 4g + t4; low half token
   // 16kh + 2*t4 + 8p, high half the next token; slot k = channel g + 8*(8hh+k).
@@ -137,18 +141,15 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
       word |= (uint32_t)vc[tok][ch] << (2 * k);
       word |= (uint32_t)vc[tok + 1][ch] << (16 + 2 * k);
     }
-    v_codes[(row * (T_cap / kG) + pblk) * 256 + wi] = word;
+    v_codes[wi] = word;
   }
 }
 
 cudaError_t launch_quantize_kv(const uint16_t* k_hat, const __half* k_norm, const uint16_t* v,
                                int src_T, int n_tok, int B, int Hkv, int T_cap, int p0,
-                               uint32_t* k_codes, uint32_t* v_codes, __half* k_scale,
-                               __half* k_zero, __half* k_norm_out, __half* v_scale,
-                               __half* v_zero, cudaStream_t s) {
+                               uint8_t* packed, cudaStream_t s) {
   dim3 grid(n_tok / kG, Hkv, B);
-  quantize_kv_kernel<<<grid, 128, 0, s>>>(k_hat, k_norm, v, src_T, Hkv, T_cap, p0, k_codes,
-                                          v_codes, k_scale, k_zero, k_norm_out, v_scale, v_zero);
+  quantize_kv_kernel<<<grid, 128, 0, s>>>(k_hat, k_norm, v, src_T, Hkv, T_cap, p0, packed);
   return cudaGetLastError();
 }
 

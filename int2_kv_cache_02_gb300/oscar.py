@@ -33,11 +33,16 @@ class OscarError(RuntimeError):
 
 class OscarCacheStruct(ctypes.Structure):
     _fields_ = [("B", c_int), ("Hkv", c_int), ("T_cap", c_int),
-                ("k_codes", c_void_p), ("v_codes", c_void_p),
-                ("k_scale", c_void_p), ("k_zero", c_void_p), ("k_norm", c_void_p),
-                ("v_scale", c_void_p), ("v_zero", c_void_p),
+                ("packed", c_void_p),
                 ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
                 ("n_packed", c_int), ("n_res", c_int), ("flags", c_uint)]
+
+
+BLOCK_BYTES = 2752
+# byte ranges of the fields of one 32-token block record (include/oscar.h)
+RECORD_FIELDS = {"k_codes": (0, 1024), "v_codes": (1024, 2048), "k_scale": (2048, 2304),
+                 "k_zero": (2304, 2560), "k_norm": (2560, 2624), "v_scale": (2624, 2688),
+                 "v_zero": (2688, 2752)}
 
 
 def _load() -> ctypes.CDLL:
@@ -112,22 +117,14 @@ class KVCache:
         if T_cap % G:
             raise ValueError("T_cap must be a multiple of 32")
         dev = torch.device(device if device is not None else "cuda")
-        nb = T_cap // G
-        e = torch.empty
-        self.k_codes = e((B, Hkv, T_cap, 8), dtype=torch.int32, device=dev)
-        self.v_codes = e((B, Hkv, nb, 256), dtype=torch.int32, device=dev)
-        self.k_scale = e((B, Hkv, nb, D), dtype=torch.float16, device=dev)
-        self.k_zero = e((B, Hkv, nb, D), dtype=torch.float16, device=dev)
-        self.k_norm = e((B, Hkv, T_cap), dtype=torch.float16, device=dev)
-        self.v_scale = e((B, Hkv, T_cap), dtype=torch.float16, device=dev)
-        self.v_zero = e((B, Hkv, T_cap), dtype=torch.float16, device=dev)
+        self.packed = torch.zeros((B, Hkv, T_cap // G, BLOCK_BYTES), dtype=torch.uint8,
+                                  device=dev)
         self.k_res = torch.zeros((B, Hkv, R, D), dtype=torch.bfloat16, device=dev)
         self.v_res = torch.zeros((B, Hkv, R, D), dtype=torch.bfloat16, device=dev)
         self.k_res_norm = torch.zeros((B, Hkv, R), dtype=torch.float16, device=dev)
         s = OscarCacheStruct()
         s.B, s.Hkv, s.T_cap = B, Hkv, T_cap
-        for name in ("k_codes", "v_codes", "k_scale", "k_zero", "k_norm", "v_scale", "v_zero",
-                     "k_res", "v_res", "k_res_norm"):
+        for name in ("packed", "k_res", "v_res", "k_res_norm"):
             setattr(s, name, getattr(self, name).data_ptr())
         s.n_packed, s.n_res, s.flags = 0, 0, flags
         self.struct = s
@@ -142,13 +139,27 @@ class KVCache:
     def ref(self):
         return ctypes.byref(self.struct)
 
-    def bytes_packed_per_row(self) -> int:
-        return self.n_packed * 86
+    def field(self, name: str) -> torch.Tensor:
+        """Writable view of one record field for every block:
+        [B][Hkv][T_cap/32][n] with n = 256 words (codes) or 128 / 32 halves."""
+        lo, hi = RECORD_FIELDS[name]
+        raw = self.packed[..., lo:hi]
+        return raw.view(torch.int32) if name.endswith("codes") else raw.view(torch.float16)
+
+    def tokens(self, name: str) -> torch.Tensor:
+        """A copy of a field in token order: key codes [B][Hkv][T_cap][8];
+        norms and value step / zero [B][Hkv][T_cap]; value codes and key
+        step / zero stay per block ([B][Hkv][T_cap/32][n])."""
+        f = self.field(name)
+        if name == "k_codes":
+            return f.reshape(self.B, self.Hkv, self.T_cap, 8)
+        if name in ("k_norm", "v_scale", "v_zero"):
+            return f.reshape(self.B, self.Hkv, self.T_cap)
+        return f.clone()
 
     def nbytes(self) -> int:
         return sum(getattr(self, n).numel() * getattr(self, n).element_size()
-                   for n in ("k_codes", "v_codes", "k_scale", "k_zero", "k_norm", "v_scale",
-                             "v_zero", "k_res", "v_res", "k_res_norm"))
+                   for n in ("packed", "k_res", "v_res", "k_res_norm"))
 
 
 # ---------------------------------------------------------------------------

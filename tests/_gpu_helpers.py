@@ -54,13 +54,16 @@ def upload_oracle_cache(cache, heads: dict, flags: int = 0):
         assert (P is None or P == p) and (R is None or R == r)
         P, R = p, r
         if p:
-            cache.k_codes[b, h, :p] = torch.from_numpy(O.pack_k_words(kq.codes).view(np.int32))
-            cache.v_codes[b, h, :p // 32] = torch.from_numpy(O.pack_v_words(vq.codes).view(np.int32))
-            cache.k_scale[b, h, :p // 32] = torch.from_numpy(kq.step16)
-            cache.k_zero[b, h, :p // 32] = torch.from_numpy(kq.zero16)
-            cache.k_norm[b, h, :p] = torch.from_numpy(hc.packed_norm16())
-            cache.v_scale[b, h, :p] = torch.from_numpy(vq.step16)
-            cache.v_zero[b, h, :p] = torch.from_numpy(vq.zero16)
+            nb = p // 32
+            put = lambda name, arr: cache.field(name)[b, h, :nb].copy_(
+                torch.from_numpy(np.ascontiguousarray(arr)))
+            put("k_codes", O.pack_k_words(kq.codes).reshape(nb, 256).view(np.int32))
+            put("v_codes", O.pack_v_words(vq.codes).view(np.int32))
+            put("k_scale", kq.step16)
+            put("k_zero", kq.zero16)
+            put("k_norm", hc.packed_norm16().reshape(nb, 32))
+            put("v_scale", vq.step16.reshape(nb, 32))
+            put("v_zero", vq.zero16.reshape(nb, 32))
         if r:
             cache.k_res[b, h, :r] = bits_to_bf16_tensor(np.stack(hc.res_k_bf16))
             cache.v_res[b, h, :r] = bits_to_bf16_tensor(np.stack(hc.res_v_bf16))

@@ -68,8 +68,7 @@ def _cache(**kw):
     from int2_kv_cache_02_gb300.oscar import OscarCacheStruct
     s = OscarCacheStruct()
     s.B, s.Hkv, s.T_cap = kw.get("B", 2), kw.get("Hkv", 2), kw.get("T_cap", 256)
-    for i, name in enumerate(["k_codes", "v_codes", "k_scale", "k_zero", "k_norm", "v_scale",
-                              "v_zero", "k_res", "v_res", "k_res_norm"]):
+    for i, name in enumerate(["packed", "k_res", "v_res", "k_res_norm"]):
         setattr(s, name, kw.get(name, FAKE + 0x100000 * i))
     s.n_packed, s.n_res, s.flags = kw.get("n_packed", 0), kw.get("n_res", 0), kw.get("flags", 0)
     return s
@@ -96,7 +95,7 @@ def test_cache_validation_and_state_untouched():
     P = ctypes.c_void_p
     bad_cap = _cache(T_cap=100)
     assert L.oscar_quantize_kv(ctypes.byref(bad_cap), None, None, None, 0, 0, None) == 1
-    misaligned = _cache(k_norm=FAKE + 4)
+    misaligned = _cache(packed=FAKE + 4)
     assert L.oscar_quantize_kv(ctypes.byref(misaligned), None, None, None, 0, 0, None) == 3
     c = _cache()
     # flush needs a full residual window

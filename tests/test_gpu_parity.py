@@ -139,17 +139,20 @@ def test_quantize_bit_exact(L):
         for h in range(H):
             kq, vq = O.quantize_k(khat[b, h]), O.quantize_v(vb[b, h])
             np.testing.assert_array_equal(
-                cache.k_codes[b, h, :T].cpu().numpy().view(np.uint32), O.pack_k_words(kq.codes))
+                cache.tokens("k_codes")[b, h, :T].cpu().numpy().view(np.uint32),
+                O.pack_k_words(kq.codes))
             np.testing.assert_array_equal(
-                cache.v_codes[b, h, :T // 32].cpu().numpy().view(np.uint32),
+                cache.field("v_codes")[b, h, :T // 32].cpu().numpy().view(np.uint32),
                 O.pack_v_words(vq.codes))
             for name, want in [("k_scale", kq.step16), ("k_zero", kq.zero16)]:
-                got = getattr(cache, name)[b, h, :T // 32].cpu().numpy()
+                got = cache.field(name)[b, h, :T // 32].cpu().numpy()
                 np.testing.assert_array_equal(got.view(np.uint16), want.view(np.uint16))
             for name, want in [("v_scale", vq.step16), ("v_zero", vq.zero16),
                                ("k_norm", rk.norm_f16[b, h])]:
-                got = getattr(cache, name)[b, h, :T].cpu().numpy()
+                got = cache.tokens(name)[b, h, :T].cpu().numpy()
                 np.testing.assert_array_equal(got.view(np.uint16), want.view(np.uint16))
+            # the untouched tail of the capacity stays zero
+            assert torch.all(cache.packed[b, h, T // 32:] == 0)
 
 
 # --------------------------------------------------------------------------
@@ -285,13 +288,13 @@ def _pipeline(L, wl_name, rows, flags=0, steps=None, check_codes=True):
         worst = (max(worst[0], ma), max(worst[1], rl))
         if check_codes:
             kq = hc.packed_k()
-            got = cache.k_codes[b, h, :cache.n_packed].cpu().numpy().view(np.uint32)
+            got = cache.tokens("k_codes")[b, h, :cache.n_packed].cpu().numpy().view(np.uint32)
             n_bad = code_mismatches(got, O.pack_k_words(kq.codes))
             # codes differ only where the GPU's rsqrt-based k_hat rounds to the
             # neighbouring bf16 value; that must stay rare
             assert n_bad <= max(4, 2e-5 * kq.codes.size), n_bad
             vq = hc.packed_v()
-            gotv = cache.v_codes[b, h, :cache.n_packed // 32].cpu().numpy().view(np.uint32)
+            gotv = cache.field("v_codes")[b, h, :cache.n_packed // 32].cpu().numpy().view(np.uint32)
             assert code_mismatches(gotv, O.pack_v_words(vq.codes)) == 0
     return worst
 
@@ -344,11 +347,8 @@ def test_streaming_flush_equals_one_shot_on_gpu(L):
     c = L.KVCache(B, Hkv, 512)
     L.quantize_kv(c, stage, norm, V[:, :, :P].contiguous(), src_T=P, n_tok=P)
     _sync_ok(L)
-    lens = {"k_codes": P, "k_norm": P, "v_scale": P, "v_zero": P,
-            "k_scale": P // 32, "k_zero": P // 32, "v_codes": P // 32}
     for x in (a, b_):
-        for name, n in lens.items():
-            assert torch.equal(getattr(x, name)[:, :, :n], getattr(c, name)[:, :, :n]), name
+        assert torch.equal(x.packed[:, :, :P // 32], c.packed[:, :, :P // 32])
     assert torch.equal(a.k_res[:, :, :T - P], b_.k_res[:, :, :T - P])
     assert torch.equal(a.v_res[:, :, :T - P], b_.v_res[:, :, :T - P])
 
