@@ -47,6 +47,7 @@ constexpr int KC_OFF = kRecKC, VC_OFF = kRecVC, KS_OFF = kRecKS, KZ_OFF = kRecKZ
 constexpr int kSmemBytes = NW * NSTAGE * kBlkBytes + NW * NSTAGE * 8;
 
 constexpr uint32_t kMagic = 0x64006400u;  // fp16x2 {1024, 1024}
+constexpr float kLazyLog2 = 8.0f;         // lazy softmax rescale threshold (log2 units)
 
 __device__ __forceinline__ uint32_t hfma2_u(uint32_t x, uint32_t s, uint32_t b) {
   return half2_as_u32(__hfma2(u32_as_half2(x), u32_as_half2(s), u32_as_half2(b)));
@@ -65,17 +66,26 @@ __device__ __forceinline__ uint32_t hmul2_u(uint32_t x, uint32_t y) {
   return half2_as_u32(__hmul2(u32_as_half2(x), u32_as_half2(y)));
 }
 
-// Key code pair at slot k (low/high half-word), as fp16x2 values 0..3.
-// w10 = w >> 10 carries slots 5..7 down to 0..2.
+// Key code pair at slot k (low/high half-word) as fp16x2 subnormals: masking
+// a code into an otherwise empty half-word gives exactly c * 4^p * 2^-24,
+// where p is the code's 2-bit position (slots 0..4 sit at positions 0..4 of
+// w, slots 5..7 at positions 0..2 of w10 = w >> 10).  The fp16 MMA
+// multiplies subnormals exactly; 4^-p is folded into the query side and 2^24
+// into the score, so no per-code arithmetic is left.
 template <int K>
-__device__ __forceinline__ uint32_t key_pair(uint32_t w, uint32_t w10, uint32_t magic) {
-  constexpr uint32_t S[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
-  constexpr uint32_t B[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u, 0xC400C400u};
+__device__ __forceinline__ uint32_t key_pair(uint32_t w, uint32_t w10) {
   if constexpr (K < 5) {
-    return hfma2_u(and_or<(0x00030003u << (2 * K))>(w, magic), S[K], B[K]);
+    return w & (0x00030003u << (2 * K));
   } else {
-    return hfma2_u(and_or<(0x00030003u << (2 * (K - 5)))>(w10, magic), S[K - 5], B[K - 5]);
+    return w10 & (0x00030003u << (2 * (K - 5)));
   }
+}
+// 2-bit position of key slot K inside the word it is extracted from.
+constexpr int key_pos(int K) { return K < 5 ? K : K - 5; }
+// fp16x2 {4^-p, 4^-p}
+constexpr uint32_t pow4_inv_h2(int p) {
+  return p == 0 ? 0x3C003C00u : p == 1 ? 0x34003400u : p == 2 ? 0x2C002C00u
+       : p == 3 ? 0x24002400u : 0x1C001C00u;
 }
 
 // Value code pair at slot k as fp16x2 centred values code - 1.5.
@@ -237,18 +247,23 @@ __global__ void __launch_bounds__(NW * 32, 3) decode_int2_kernel(const DecodeArg
         kw[nt][0] = v.x; kw[nt][1] = v.y;
         kw10[nt][0] = v.x >> 10; kw10[nt][1] = v.y >> 10;
       }
+      // The Q.K accumulators start from zero (not from Z) so their MMA chains
+      // do not wait for the Z chain; Z joins each score below.
+      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
       float acc[4][4];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = dz[e];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint4 sv = ks4[i];
 #pragma unroll
         for (int hk = 0; hk < 2; ++hk) {
           const int k8 = 2 * i + hk;
-          const uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
+          // key step of the pair's channels times 4^-p of the pair's code
+          // position (exact: a power of two)
+          constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
+          constexpr int P23[4] = {key_pos(1), key_pos(3), key_pos(5), key_pos(7)};
+          uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
+          if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
+          if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
           uint32_t at[4];
           at[0] = hmul2_u(aq[k8][0], s01);
           at[1] = hfma2_u(aq[k8][1], s01, hfma2_u(aq[k8][0], s01, neg2_u(at[0])));
@@ -259,18 +274,24 @@ __global__ void __launch_bounds__(NW * 32, 3) decode_int2_kernel(const DecodeArg
             const uint32_t w = kw[nt][k8 >> 2], w10 = kw10[nt][k8 >> 2];
             uint32_t b0v, b1v;
             switch (k8 & 3) {
-              case 0: b0v = key_pair<0>(w, w10, magic); b1v = key_pair<1>(w, w10, magic); break;
-              case 1: b0v = key_pair<2>(w, w10, magic); b1v = key_pair<3>(w, w10, magic); break;
-              case 2: b0v = key_pair<4>(w, w10, magic); b1v = key_pair<5>(w, w10, magic); break;
-              default: b0v = key_pair<6>(w, w10, magic); b1v = key_pair<7>(w, w10, magic); break;
+              case 0: b0v = key_pair<0>(w, w10); b1v = key_pair<1>(w, w10); break;
+              case 1: b0v = key_pair<2>(w, w10); b1v = key_pair<3>(w, w10); break;
+              case 2: b0v = key_pair<4>(w, w10); b1v = key_pair<5>(w, w10); break;
+              default: b0v = key_pair<6>(w, w10); b1v = key_pair<7>(w, w10); break;
             }
-            mma_16816_acc(acc[nt], at, b0v, b1v);
+            if (k8 == 0) {
+              mma_16816(acc[nt], at, b0v, b1v, zero4);
+            } else {
+              mma_16816_acc(acc[nt], at, b0v, b1v);
+            }
           }
         }
       }
 
       // Scores of this thread's tokens (log2 domain): hi row + lo row, times
       // the token norm.  Token j of the thread: n-tile nt(j), tokens 2tig, +1.
+      // Z of this thread's head (hi row + lo row); the Q.K sums carry 2^-24
+      const float zsum = dz[0] + dz[2];
       float sc[NTOK];
 #pragma unroll
       for (int j = 0; j < NTOK / 2; ++j) {
@@ -283,8 +304,8 @@ __global__ void __launch_bounds__(NW * 32, 3) decode_int2_kernel(const DecodeArg
           c0 = acc[j][0]; c1 = acc[j][1]; c2 = acc[j][2]; c3 = acc[j][3];
         }
         const float2 nf = __half22float2(u32_as_half2(kn2[4 * nt + tig]));
-        sc[2 * j] = (c0 + c2) * (nf.x * inv_sigma);
-        sc[2 * j + 1] = (c1 + c3) * (nf.y * inv_sigma);
+        sc[2 * j] = fmaf(c0 + c2, 16777216.0f, zsum) * (nf.x * inv_sigma);
+        sc[2 * j + 1] = fmaf(c1 + c3, 16777216.0f, zsum) * (nf.y * inv_sigma);
       }
 
       // Online softmax for this thread's head.
@@ -294,8 +315,11 @@ __global__ void __launch_bounds__(NW * 32, 3) decode_int2_kernel(const DecodeArg
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
       mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
       if (kSplitHalves) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+      // Lazy rescaling: the running max moves only when a score exceeds it by
+      // more than 2^kLazyLog2, so p = 2^(score - m_run) stays below 2^kLazyLog2
+      // (well inside fp16 and fp32) and the accumulators are rescaled rarely.
       const float m_new = fmaxf(m_run, mb);
-      if (__any_sync(0xffffffffu, m_new > m_run)) {
+      if (__any_sync(0xffffffffu, m_new > m_run + kLazyLog2)) {
         const float alpha = fast_exp2(m_run - m_new);
         l_run *= alpha;
         z_run *= alpha;
