@@ -85,6 +85,8 @@ enum { OSCAR_NO_ROTATE = 1u, OSCAR_NO_SCALE = 2u };
  *  2560  key norms    fp16 [32] per token ([notes] Step Two)
  *  2624  value step   fp16 [32] per token
  *  2688  value zero   fp16 [32] per token
+ *        (the three per-token arrays hold token t of the block at position
+ *        4*(t%8) + t/8, so that tokens i, i+8, i+16, i+24 sit together)
  * Residual layout:
  *  k_res    bf16 [B][Hkv][128][128] rotated, unit-norm keys (slot = age order)
  *  v_res    bf16 [B][Hkv][128][128] values

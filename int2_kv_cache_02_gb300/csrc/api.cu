@@ -53,18 +53,52 @@ oscar_status check_cache(const oscar_cache* c) {
 
 // Split planning: minimise (waves of CTAs) x (blocks per CTA) + a small
 // per-split cost, so the grid fills the SMs without long tails.
+// Split count for `rows` (sequence, KV head) rows of `nblk` 32-token blocks.
+// A launch runs rows * (s + 1) CTAs (s packed splits and one residual split
+// per row) in waves of sms * ctas_per_sm; a packed CTA costs its blocks plus
+// a fixed start/merge overhead worth kSplitOverheadBlocks blocks.  Each warp
+// keeps at least kMinBlocksPerWarp blocks: shorter ranges measured slower.
+// The cost is waves(s) * (blocks per split + overhead); ties keep fewer
+// splits.
+constexpr long long kSplitOverheadBlocks = 32;
+constexpr long long kMinBlocksPerWarp = 16;
+
 int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
   if (nblk <= 0 || rows <= 0) return 1;
   const long long slots = (long long)sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
+  const long long most = std::max<long long>(1, nblk / (4 * kMinBlocksPerWarp));
+  const int hi = (int)std::min<long long>(max_splits, most);
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= hi; ++s) {
+    const long long waves = (rows * (s + 1) + slots - 1) / slots;
+    const long long per = (nblk + s - 1) / s;
+    const long long cost = waves * (per + kSplitOverheadBlocks);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// Split count of the bf16 comparison kernel (no residual split): waves of
+// sms * ctas_per_sm CTAs times the chunks per split, plus 0.25 per split.
+int plan_splits_bf16(long long rows, long long nchunk, int ctas_per_sm, int max_splits) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  if (nchunk <= 0 || rows <= 0) return 1;
+  const long long slots = (long long)sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
   int best = 1;
   double best_cost = 1e300;
-  const int hi = (int)std::min<long long>(max_splits, nblk);
+  const int hi = (int)std::min<long long>(max_splits, nchunk);
   for (int s = 1; s <= hi; ++s) {
     const long long waves = (rows * s + slots - 1) / slots;
-    const long long per = (nblk + s - 1) / s;
+    const long long per = (nchunk + s - 1) / s;
     const double cost = (double)waves * (double)per + 0.25 * s;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
@@ -249,8 +283,8 @@ oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* 
   int S = num_splits;
   if (S == 0) {
     const long long chunk = 16;  // tokens per warp chunk, the unit of work here
-    S = plan_splits((long long)B * Hkv, (T + chunk - 1) / chunk,
-                    decode_bf16_ctas_per_sm(Hq / Hkv), 512);
+    S = plan_splits_bf16((long long)B * Hkv, (T + chunk - 1) / chunk,
+                         decode_bf16_ctas_per_sm(Hq / Hkv), 512);
   }
   if (!workspace || ws_bytes < ws_bytes_for(B, Hq, S)) return OSCAR_ERR_WORKSPACE;
   if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;

@@ -19,6 +19,9 @@ constexpr int kBlkBytes = OSCAR_BLOCK_BYTES;
 constexpr int kRecKC = 0, kRecVC = 1024, kRecKS = 2048, kRecKZ = 2304, kRecKN = 2560,
               kRecVS = 2624, kRecVZ = 2688;
 static_assert(kRecVZ + 64 == kBlkBytes, "record layout");
+// Position of token t (0..31) of a block in the record's per-token arrays
+// (norms, value step, value zero): tokens i, i+8, i+16, i+24 are adjacent.
+__host__ __device__ constexpr int tok_slot(int t) { return 4 * (t & 7) + (t >> 3); }
 
 // Bits a kernel may OR into the device status word.
 enum : unsigned {

@@ -15,17 +15,21 @@
 //    product keeps ~22 bits), the key zero z_c becomes one dot product
 //    Z = q'.z per block (itself an MMA), and the norm multiplies the score:
 //      score_t = tau * n_t * (sum_c q~_c code_tc + Z);
-//    Q.K^T runs with the query group as the M rows (hi parts in rows 0-7,
-//    lo parts in rows 8-15) and 8 tokens as the N columns;
+//  * key codes enter Q.K as exact fp16 subnormals (a masked code is
+//    c * 4^p * 2^-24; 4^-p goes into the step, 2^24 into the score);
 //  * values: p~_t = p_t s_t (hi + lo fp16) multiplies the centred codes
 //    code - 1.5 on the tensor cores; the per-token constant z_t + 1.5 s_t is
 //    accumulated as sum_t p_t (z_t + 1.5 s_t) and added per channel at the end;
-//  * 2-bit codes become fp16 operands in registers: a masked OR with the fp16
-//    bit pattern of 1024 places a code in the mantissa, one fp16 FMA removes
-//    the bias (exact), so the codes never travel through shared memory twice;
-//  * for groups of 4 or fewer query heads the MMA rows repeat; the two lane
-//    halves that hold the same rows split the softmax work by token and swap
-//    one fp16 limb of p~ with a shuffle.
+//    a masked OR with the fp16 bit pattern of 1024 places a value code in the
+//    mantissa and one fp16 FMA removes the bias (exact);
+//  * groups of up to 4 query heads ("column" layout): Q.K runs with 16 tokens
+//    as the M rows and the (head, limb) pairs of q~ as the 8 N columns, so no
+//    row is wasted; each lane then holds whole scores of one head, and the
+//    8x8 tiles of (hi, lo) probabilities become the P.V operand with one
+//    movmatrix transpose each;
+//  * groups of 8 ("row" layout): Q.K runs with the 16 (head, limb) rows of q~
+//    as M and 8 tokens as N; its accumulator layout is already the P.V
+//    operand layout.
 // Each warp streams its own contiguous range of blocks through its own
 // NSTAGE-deep shared-memory ring: one 1-D bulk copy (TMA, cp.async.bulk) of
 // the block's 2752-byte record per block, completing on the warp's mbarrier.  Waits are
@@ -105,412 +109,693 @@ __device__ __forceinline__ uint32_t value_pair(uint32_t w, uint32_t w2, uint32_t
   }
 }
 
+// A operand of P.V m-tile mt (channels 16 mt + gid, + 8 on the row halves)
+// from the lane's four value words (tokens 2 tig.. and 2 tig + 8..): row gid
+// takes slot 2 (mt % 4), row gid + 8 slot 2 (mt % 4) + 1, of the words for
+// channel half mt / 4.
+__device__ __forceinline__ void value_frag(uint32_t (&av)[4], int mt, const uint32_t (&wv)[4],
+                                           const uint32_t (&w2)[4], const uint32_t (&w8)[4],
+                                           uint32_t magic) {
+  const int hh = mt >> 2;
+  const int p0 = hh, p1 = 2 + hh;  // words of tokens (2tig,2tig+1) and (2tig+8,2tig+9)
+  switch (mt & 3) {
+    case 0:
+      av[0] = value_pair<0>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<1>(wv[p0], w2[p0], w8[p0], magic);
+      av[2] = value_pair<0>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<1>(wv[p1], w2[p1], w8[p1], magic);
+      break;
+    case 1:
+      av[0] = value_pair<2>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<3>(wv[p0], w2[p0], w8[p0], magic);
+      av[2] = value_pair<2>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<3>(wv[p1], w2[p1], w8[p1], magic);
+      break;
+    case 2:
+      av[0] = value_pair<4>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<5>(wv[p0], w2[p0], w8[p0], magic);
+      av[2] = value_pair<4>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<5>(wv[p1], w2[p1], w8[p1], magic);
+      break;
+    default:
+      av[0] = value_pair<6>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<7>(wv[p0], w2[p0], w8[p0], magic);
+      av[2] = value_pair<6>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<7>(wv[p1], w2[p1], w8[p1], magic);
+      break;
+  }
+}
+
+// Four fp16 values (two packed pairs) as floats.
+__device__ __forceinline__ void unpack_h4(float (&f)[4], uint32_t ab, uint32_t cd) {
+  const float2 x = __half22float2(u32_as_half2(ab)), y = __half22float2(u32_as_half2(cd));
+  f[0] = x.x; f[1] = x.y; f[2] = y.x; f[3] = y.y;
+}
+
 __device__ __forceinline__ float warp_allsum(float v) {
 #pragma unroll
   for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
   return v;
 }
 
-template <int GQ>
-__global__ void __launch_bounds__(NW * 32, 3) decode_int2_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + NW * NSTAGE * kBlkBytes);
-  auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
-  static_assert(sizeof(MergeSmem<GQ, NW>) <= NW * NSTAGE * kBlkBytes, "merge area");
+// One warp's contiguous range of a row's 32-token blocks, streamed through
+// the warp's own NSTAGE-deep ring: lane 0 copies block i's record into slot
+// i % NSTAGE with one 1-D bulk copy completing on that slot's mbarrier.
+struct WarpRing {
+  uint8_t* ring;
+  uint64_t* bars;
+  const uint8_t* src;   // record of the range's first block
+  int n;                // blocks in the range
+  int lane;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const long long row = (long long)b * a.Hkv + h;
-  const long long qrow0 = (long long)b * a.Hq + (long long)h * GQ;  // first query head
-
-  if (split < a.num_splits) {
-    // ------------------------------------------------------------ packed
-    constexpr bool kSplitHalves = GQ <= 4;         // rows repeat: halves share the softmax
-    constexpr int NT = kSplitHalves ? 1 : 2;       // P.V n-tiles (GQ = 8: hi, lo limbs)
-    constexpr int NTOK = kSplitHalves ? 4 : 8;     // softmax tokens per thread per block
-    const int head = kSplitHalves ? (gid % GQ) : gid;
-    const int hf = kSplitHalves ? (gid >> 2) : 0;  // which n-tile pair this lane scores
-    const int nblk = a.n_packed / kG;
-    const int b0 = (int)((long long)nblk * split / a.num_splits);
-    const int b1 = (int)((long long)nblk * (split + 1) / a.num_splits);
-    const int wb0 = b0 + (int)((long long)(b1 - b0) * warp / NW);
-    const int wb1 = b0 + (int)((long long)(b1 - b0) * (warp + 1) / NW);
-    const int n = wb1 - wb0;
-    uint8_t* ring = smem + warp * NSTAGE * kBlkBytes;
-    uint64_t* bars = bars_all + warp * NSTAGE;
-
-    // Query fragments of this thread's head, channels c0 = 32*tig + 4*k8 ..+3,
-    // as {hi(c0,c0+1), lo(c0,c0+1), hi(c0+2,c0+3), lo(c0+2,c0+3)} (the MMA A
-    // layout of rows g and g+8).  The query carries softmax_scale * log2(e)
-    // and a power of two sigma that keeps the fp16 parts in range.
-    uint32_t aq[8][4];
-    float inv_sigma;
-    {
-      const float4* qp = reinterpret_cast<const float4*>(a.q_rot + (qrow0 + head) * kD + 32 * tig);
-      float qf[32];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 v = qp[i];
-        qf[4 * i] = v.x * a.scale_log2; qf[4 * i + 1] = v.y * a.scale_log2;
-        qf[4 * i + 2] = v.z * a.scale_log2; qf[4 * i + 3] = v.w * a.scale_log2;
-      }
-      float amax = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qf[i]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      int e = 0;
-      if (amax > 0.0f) frexpf(amax, &e);
-      int sh = (amax > 0.0f) ? (((a.flags & OSCAR_NO_SCALE) ? 1 : 14) - e) : 0;
-      sh = max(-100, min(100, sh));
-      const float sigma = ldexpf(1.0f, sh);
-      inv_sigma = ldexpf(1.0f, -sh);
-#pragma unroll
-      for (int k8 = 0; k8 < 8; ++k8) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float x0 = qf[4 * k8 + 2 * j] * sigma, x1 = qf[4 * k8 + 2 * j + 1] * sigma;
-          const __half2 hh = __floats2half2_rn(x0, x1);
-          const float2 hv = __half22float2(hh);
-          aq[k8][2 * j] = half2_as_u32(hh);
-          aq[k8][2 * j + 1] = half2_as_u32(__floats2half2_rn(x0 - hv.x, x1 - hv.y));
-        }
-      }
-    }
-
-    float O[NT][8][4];
-#pragma unroll
-    for (int t = 0; t < NT; ++t)
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) O[t][mt][e] = 0.0f;
-    float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
-    // The fp16x2 bit pattern of {1024, 1024}, kept in a register so that each
-    // code extraction is one LOP3 (mask immediate, this register).
-    uint32_t magic = kMagic;
-    asm volatile("" : "+r"(magic));
-
+  __device__ __forceinline__ void start() const {
     if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
       mbar_fence_init();
     }
     __syncwarp();
-
-    // Block i of this warp into ring slot `slot`: lane 0 copies its record
-    // (one 1-D bulk copy; the shared-memory slot has the record's layout).
-    const uint8_t* rows_rec = a.packed + row * (long long)(a.T_cap / kG) * kBlkBytes;
-    auto issue = [&](int i, int slot) {
-      if (lane == 0) {
-        uint64_t* bar = &bars[slot];
-        mbar_arrive_expect_tx(bar, kBlkBytes);
-        bulk_g2s(ring + slot * kBlkBytes, rows_rec + (long long)(wb0 + i) * kBlkBytes, kBlkBytes,
-                 bar);
-      }
-    };
-
-    int issued = min(NSTAGE, n);
-    for (int s = 0; s < issued; ++s) issue(s, s);
-
-    bool ok = true;
-    int it = 0;
-    for (; it < n; ++it) {
-      const int slot = it % NSTAGE;
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait_bounded(&bars[slot], (unsigned)((it / NSTAGE) & 1), kWaitLimit));
-      if (!ok) break;
-      const uint8_t* st = ring + slot * kBlkBytes;
-      const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + KC_OFF);
-      const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + VC_OFF);
-      const uint4* ks4 = reinterpret_cast<const uint4*>(st + KS_OFF) + tig * 4;
-      const uint4* kz4 = reinterpret_cast<const uint4*>(st + KZ_OFF) + tig * 4;
-      const uint32_t* kn2 = reinterpret_cast<const uint32_t*>(st + KN_OFF);
-      const uint32_t* vs2 = reinterpret_cast<const uint32_t*>(st + VS_OFF);
-      const uint32_t* vz2 = reinterpret_cast<const uint32_t*>(st + VZ_OFF);
-
-      // Z = q'.z of the block: rows g (hi) and g+8 (lo), every column alike.
-      float dz[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 zv = kz4[i];
-        mma_16816_acc(dz, aq[2 * i], zv.x, zv.y);
-        mma_16816_acc(dz, aq[2 * i + 1], zv.z, zv.w);
-      }
-
-      // Q.K^T, k-step outer: q~ fragment for k-step k8, then the 4 n-tiles.
-      uint32_t kw[4][2], kw10[4][2];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const uint2 v = *reinterpret_cast<const uint2*>(kc + (8 * nt + gid) * 8 + 2 * tig);
-        kw[nt][0] = v.x; kw[nt][1] = v.y;
-        kw10[nt][0] = v.x >> 10; kw10[nt][1] = v.y >> 10;
-      }
-      // The Q.K accumulators start from zero (not from Z) so their MMA chains
-      // do not wait for the Z chain; Z joins each score below.
-      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-      float acc[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 sv = ks4[i];
-#pragma unroll
-        for (int hk = 0; hk < 2; ++hk) {
-          const int k8 = 2 * i + hk;
-          // key step of the pair's channels times 4^-p of the pair's code
-          // position (exact: a power of two)
-          constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
-          constexpr int P23[4] = {key_pos(1), key_pos(3), key_pos(5), key_pos(7)};
-          uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
-          if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
-          if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
-          uint32_t at[4];
-          at[0] = hmul2_u(aq[k8][0], s01);
-          at[1] = hfma2_u(aq[k8][1], s01, hfma2_u(aq[k8][0], s01, neg2_u(at[0])));
-          at[2] = hmul2_u(aq[k8][2], s23);
-          at[3] = hfma2_u(aq[k8][3], s23, hfma2_u(aq[k8][2], s23, neg2_u(at[2])));
-#pragma unroll
-          for (int nt = 0; nt < 4; ++nt) {
-            const uint32_t w = kw[nt][k8 >> 2], w10 = kw10[nt][k8 >> 2];
-            uint32_t b0v, b1v;
-            switch (k8 & 3) {
-              case 0: b0v = key_pair<0>(w, w10); b1v = key_pair<1>(w, w10); break;
-              case 1: b0v = key_pair<2>(w, w10); b1v = key_pair<3>(w, w10); break;
-              case 2: b0v = key_pair<4>(w, w10); b1v = key_pair<5>(w, w10); break;
-              default: b0v = key_pair<6>(w, w10); b1v = key_pair<7>(w, w10); break;
-            }
-            if (k8 == 0) {
-              mma_16816(acc[nt], at, b0v, b1v, zero4);
-            } else {
-              mma_16816_acc(acc[nt], at, b0v, b1v);
-            }
-          }
-        }
-      }
-
-      // Scores of this thread's tokens (log2 domain): hi row + lo row, times
-      // the token norm.  Token j of the thread: n-tile nt(j), tokens 2tig, +1.
-      // Z of this thread's head (hi row + lo row); the Q.K sums carry 2^-24
-      const float zsum = dz[0] + dz[2];
-      float sc[NTOK];
-#pragma unroll
-      for (int j = 0; j < NTOK / 2; ++j) {
-        const int nt = kSplitHalves ? (2 * hf + j) : j;
-        float c0, c1, c2, c3;
-        if (kSplitHalves) {
-          c0 = hf ? acc[2 + j][0] : acc[j][0]; c1 = hf ? acc[2 + j][1] : acc[j][1];
-          c2 = hf ? acc[2 + j][2] : acc[j][2]; c3 = hf ? acc[2 + j][3] : acc[j][3];
-        } else {
-          c0 = acc[j][0]; c1 = acc[j][1]; c2 = acc[j][2]; c3 = acc[j][3];
-        }
-        const float2 nf = __half22float2(u32_as_half2(kn2[4 * nt + tig]));
-        sc[2 * j] = fmaf(c0 + c2, 16777216.0f, zsum) * (nf.x * inv_sigma);
-        sc[2 * j + 1] = fmaf(c1 + c3, 16777216.0f, zsum) * (nf.y * inv_sigma);
-      }
-
-      // Online softmax for this thread's head.
-      float mb = sc[0];
-#pragma unroll
-      for (int i = 1; i < NTOK; ++i) mb = fmaxf(mb, sc[i]);
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
-      if (kSplitHalves) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-      // Lazy rescaling: the running max moves only when a score exceeds it by
-      // more than 2^kLazyLog2, so p = 2^(score - m_run) stays below 2^kLazyLog2
-      // (well inside fp16 and fp32) and the accumulators are rescaled rarely.
-      const float m_new = fmaxf(m_run, mb);
-      if (__any_sync(0xffffffffu, m_new > m_run + kLazyLog2)) {
-        const float alpha = fast_exp2(m_run - m_new);
-        l_run *= alpha;
-        z_run *= alpha;
-        const int ha = kSplitHalves ? (2 * tig) % GQ : 2 * tig;
-        const int hb = kSplitHalves ? (2 * tig + 1) % GQ : 2 * tig + 1;
-        const float al_a = __shfl_sync(0xffffffffu, alpha, 4 * ha);
-        const float al_b = __shfl_sync(0xffffffffu, alpha, 4 * hb);
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            O[t][mt][0] *= al_a; O[t][mt][1] *= al_b;
-            O[t][mt][2] *= al_a; O[t][mt][3] *= al_b;
-          }
-        m_run = m_new;
-      }
-
-      float pt[NTOK];
-#pragma unroll
-      for (int j = 0; j < NTOK / 2; ++j) {
-        const int nt = kSplitHalves ? (2 * hf + j) : j;
-        const float2 sv = __half22float2(u32_as_half2(vs2[4 * nt + tig]));
-        const float2 zv = __half22float2(u32_as_half2(vz2[4 * nt + tig]));
-        const float p0 = fast_exp2(sc[2 * j] - m_run);
-        const float p1 = fast_exp2(sc[2 * j + 1] - m_run);
-        l_run += p0 + p1;
-        z_run = fmaf(p0, fmaf(1.5f, sv.x, zv.x), z_run);
-        z_run = fmaf(p1, fmaf(1.5f, sv.y, zv.y), z_run);
-        pt[2 * j] = p0 * sv.x;
-        pt[2 * j + 1] = p1 * sv.y;
-      }
-
-      // P~ as the B operand of P.V: k-half kh uses n-tiles 2kh (tokens 2tig,
-      // 2tig+1) and 2kh+1 (2tig+8, 2tig+9); column gid is limb gid/4 (GQ <= 4).
-      uint32_t bp[2][2], bq[2][2];  // bp: limb for n-tile 0 of P.V; bq: lo limb (GQ = 8)
-      if (kSplitHalves) {
-        uint32_t hi[2], lo[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const __half2 hv = __floats2half2_rn(pt[2 * r], pt[2 * r + 1]);
-          const float2 hf2 = __half22float2(hv);
-          hi[r] = half2_as_u32(hv);
-          lo[r] = half2_as_u32(__floats2half2_rn(pt[2 * r] - hf2.x, pt[2 * r + 1] - hf2.y));
-        }
-        // own limb for k-half hf; the partner lane (other half) needs my other limb
-        const uint32_t mine0 = hf ? lo[0] : hi[0], mine1 = hf ? lo[1] : hi[1];
-        const uint32_t give0 = hf ? hi[0] : lo[0], give1 = hf ? hi[1] : lo[1];
-        const uint32_t got0 = __shfl_xor_sync(0xffffffffu, give0, 16);
-        const uint32_t got1 = __shfl_xor_sync(0xffffffffu, give1, 16);
-        bp[0][0] = hf ? got0 : mine0; bp[0][1] = hf ? got1 : mine1;
-        bp[1][0] = hf ? mine0 : got0; bp[1][1] = hf ? mine1 : got1;
-      } else {
-#pragma unroll
-        for (int kh = 0; kh < 2; ++kh)
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float x0 = pt[4 * kh + 2 * r], x1 = pt[4 * kh + 2 * r + 1];
-            const __half2 hv = __floats2half2_rn(x0, x1);
-            const float2 hf2 = __half22float2(hv);
-            bp[kh][r] = half2_as_u32(hv);
-            bq[kh][r] = half2_as_u32(__floats2half2_rn(x0 - hf2.x, x1 - hf2.y));
-          }
-      }
-
-#pragma unroll
-      for (int kh = 0; kh < 2; ++kh) {
-        const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
-        const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
-        uint32_t w2[4], w8[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) { w2[q] = wv[q] << 2; w8[q] = wv[q] >> 8; }
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int hh = mt >> 2;
-          const int p0 = hh, p1 = 2 + hh;  // words of tokens (2tig,2tig+1) and (2tig+8,2tig+9)
-          uint32_t av[4];
-          switch (mt & 3) {
-            case 0:
-              av[0] = value_pair<0>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<1>(wv[p0], w2[p0], w8[p0], magic);
-              av[2] = value_pair<0>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<1>(wv[p1], w2[p1], w8[p1], magic);
-              break;
-            case 1:
-              av[0] = value_pair<2>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<3>(wv[p0], w2[p0], w8[p0], magic);
-              av[2] = value_pair<2>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<3>(wv[p1], w2[p1], w8[p1], magic);
-              break;
-            case 2:
-              av[0] = value_pair<4>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<5>(wv[p0], w2[p0], w8[p0], magic);
-              av[2] = value_pair<4>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<5>(wv[p1], w2[p1], w8[p1], magic);
-              break;
-            default:
-              av[0] = value_pair<6>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<7>(wv[p0], w2[p0], w8[p0], magic);
-              av[2] = value_pair<6>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<7>(wv[p1], w2[p1], w8[p1], magic);
-              break;
-          }
-          mma_16816_acc(O[0][mt], av, bp[kh][0], bp[kh][1]);
-          if (!kSplitHalves) mma_16816_acc(O[NT - 1][mt], av, bq[kh][0], bq[kh][1]);
-        }
-      }
-      __syncwarp();
-      if (it + NSTAGE < n) issue(it + NSTAGE, slot);
+    for (int i = 0; i < NSTAGE && i < n; ++i) issue(i);
+  }
+  __device__ __forceinline__ void issue(int i) const {
+    if (lane == 0) {
+      uint64_t* bar = &bars[i % NSTAGE];
+      mbar_arrive_expect_tx(bar, kBlkBytes);
+      bulk_g2s(ring + (i % NSTAGE) * kBlkBytes, src + (long long)i * kBlkBytes, kBlkBytes, bar);
     }
-    if (!ok) {
-      if (lane == 0) {
-        record_error(a.status, kDevErrWaitTimeout);
-        for (int s = it; s < issued && s < n; ++s)
-          if (!mbar_wait_bounded(&bars[s % NSTAGE], (unsigned)((s / NSTAGE) & 1), kDrainLimit))
-            record_error(a.status, kDevErrDrainTimeout);
+  }
+  // true on every lane once block i has landed; false if the wait gave up
+  __device__ __forceinline__ bool wait(int i) const {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(&bars[i % NSTAGE],
+                                                     (unsigned)((i / NSTAGE) & 1), kWaitLimit));
+  }
+  __device__ __forceinline__ const uint8_t* slot(int i) const {
+    return ring + (i % NSTAGE) * kBlkBytes;
+  }
+  // After consuming block i: refill its slot with block i + NSTAGE.
+  __device__ __forceinline__ void release(int i) const {
+    __syncwarp();
+    if (i + NSTAGE < n) issue(i + NSTAGE);
+  }
+  // The wait for block `it` gave up: record it and wait (bounded) for the
+  // copies still in flight, blocks it .. min(it + NSTAGE, n) - 1, so that no
+  // copy lands in shared memory after the warp has moved on.
+  __device__ __forceinline__ void fail(int it, unsigned* status) const {
+    if (lane == 0) {
+      record_error(status, kDevErrWaitTimeout);
+      for (int s = it; s < it + NSTAGE && s < n; ++s)
+        if (!mbar_wait_bounded(&bars[s % NSTAGE], (unsigned)((s / NSTAGE) & 1), kDrainLimit))
+          record_error(status, kDevErrDrainTimeout);
+    }
+    __syncwarp();
+  }
+};
+
+__device__ __forceinline__ WarpRing make_ring(const DecodeArgs& a, uint8_t* smem, long long row,
+                                              int split) {
+  const int warp = threadIdx.x >> 5;
+  const int nblk = a.n_packed / kG;
+  const int b0 = (int)((long long)nblk * split / a.num_splits);
+  const int b1 = (int)((long long)nblk * (split + 1) / a.num_splits);
+  const int wb0 = b0 + (int)((long long)(b1 - b0) * warp / NW);
+  const int wb1 = b0 + (int)((long long)(b1 - b0) * (warp + 1) / NW);
+  WarpRing r;
+  r.ring = smem + warp * NSTAGE * kBlkBytes;
+  r.bars = reinterpret_cast<uint64_t*>(smem + NW * NSTAGE * kBlkBytes) + warp * NSTAGE;
+  r.src = a.packed + (row * (long long)(a.T_cap / kG) + wb0) * kBlkBytes;
+  r.n = wb1 - wb0;
+  r.lane = threadIdx.x & 31;
+  return r;
+}
+
+// 8x8 fp16 tile transpose across the warp: the lane holding row r, columns
+// 2c and 2c+1 receives row r, columns 2c and 2c+1 of the transpose.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t d;
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(x));
+  return d;
+}
+
+// Query scaling shared by both layouts: q' times softmax_scale * log2(e) and
+// a power of two sigma chosen per head so that the fp16 parts stay in range.
+// qf holds channels 32*tig .. 32*tig+31 of the head; the lanes xor 1 and xor 2
+// hold the rest of it.  Returns sigma; qf is scaled in place.
+__device__ __forceinline__ float scale_query(float (&qf)[32], const float* qrow, int tig,
+                                            const DecodeArgs& a) {
+  const float4* qp = reinterpret_cast<const float4*>(qrow + 32 * tig);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 v = qp[i];
+    qf[4 * i] = v.x * a.scale_log2; qf[4 * i + 1] = v.y * a.scale_log2;
+    qf[4 * i + 2] = v.z * a.scale_log2; qf[4 * i + 3] = v.w * a.scale_log2;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qf[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  int e = 0;
+  if (amax > 0.0f) frexpf(amax, &e);
+  int sh = (amax > 0.0f) ? (((a.flags & OSCAR_NO_SCALE) ? 1 : 14) - e) : 0;
+  sh = max(-100, min(100, sh));
+  const float sigma = ldexpf(1.0f, sh);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) qf[i] *= sigma;
+  return sigma;
+}
+
+// ---------------------------------------------------------------- columns
+// Groups of up to 4 query heads.  Lane (gid, tig):
+//  * Q.K B operand: column gid = (head (gid/2) mod GQ, limb gid%2) of q~;
+//  * Q.K A operand: key codes of tokens 16 mt + gid and 16 mt + gid + 8;
+//  * scores, softmax and outputs: head tig mod GQ (columns 2 tig, 2 tig + 1
+//    are its hi and lo limbs), tokens gid + 8 j, j = 0..3;
+//  * P.V: channels on M as in the row layout, (head, limb of p~) on N.
+template <int GQ>
+__device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing& R,
+                                            MergeSmem<GQ, NW>& E, long long qrow0) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int hq = (gid >> 1) % GQ;   // head of this lane's q~ column
+  const int limb = gid & 1;         // 0: hi part, 1: lo part
+  const int hs = tig % GQ;          // head of this lane's scores and outputs
+  R.start();   // the first copies travel while the query is prepared
+
+  // This lane's column of q' for channels 32 tig + 4 k8 + {0,1} (pair 0) and
+  // + {2,3} (pair 1): qz = the column's own limb (the Z operand), qhm = the hi
+  // limb on lo columns and 0 on hi columns.  Per block, with step s,
+  //   r = qz s + (qhm s - fp16(qhm s))
+  // is fp16(q' s) on hi columns and the exact remainder's fp16 on lo columns.
+  uint32_t qz[8][2], qhm[8][2];
+  float inv_sigma;
+  {
+    float qf[32];
+    const float sigma = scale_query(qf, a.q_rot + (qrow0 + hq) * kD, tig, a);
+#pragma unroll
+    for (int k8 = 0; k8 < 8; ++k8)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float x0 = qf[4 * k8 + 2 * j], x1 = qf[4 * k8 + 2 * j + 1];
+        const __half2 hh = __floats2half2_rn(x0, x1);
+        const float2 hv = __half22float2(hh);
+        const __half2 ll = __floats2half2_rn(x0 - hv.x, x1 - hv.y);
+        qz[k8][j] = half2_as_u32(limb ? ll : hh);
+        qhm[k8][j] = limb ? half2_as_u32(hh) : 0u;
       }
-      m_run = -INFINITY;   // this warp's result is void; the status word says so
+    // the score head's 1/sigma lives on the lanes whose column head is hs
+    inv_sigma = __shfl_sync(0xffffffffu, ldexpf(1.0f, -ilogbf(sigma)), 8 * hs);
+  }
+  // the Q.K sums carry 2^-24 (subnormal key codes) and sigma
+  const float qk_scale = 16777216.0f * inv_sigma;
+
+  float O[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) O[mt][e] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
+  uint32_t magic = kMagic;
+  asm volatile("" : "+r"(magic));
+
+  int it = 0;
+  for (; it < R.n; ++it) {
+    if (!R.wait(it)) break;
+    const uint8_t* st = R.slot(it);
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + KC_OFF);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + VC_OFF);
+    const uint4* ks4 = reinterpret_cast<const uint4*>(st + KS_OFF) + tig * 4;
+    const uint4* kz4 = reinterpret_cast<const uint4*>(st + KZ_OFF) + tig * 4;
+    // norms, value steps and zeros of tokens gid + 8 j, j = 0..3 (adjacent
+    // in the record)
+    const uint2 kn4 = *reinterpret_cast<const uint2*>(st + KN_OFF + 8 * gid);
+    const uint2 vs4 = *reinterpret_cast<const uint2*>(st + VS_OFF + 8 * gid);
+    const uint2 vz4 = *reinterpret_cast<const uint2*>(st + VZ_OFF + 8 * gid);
+
+    // Z = q'.z.  The A operand is the loaded z quad {x, y, z, w} (pairs 0
+    // and 1 of k-steps 2i and 2i+1) as it is: with the pair-0 columns of q'
+    // for both k-steps, row gid of dza sums the pair-0 terms; with the pair-1
+    // columns, row gid + 8 of dzb sums the pair-1 terms (the other rows are
+    // unused).  Columns 2 tig, 2 tig + 1 give the hi, lo parts for head hs.
+    float dza[4] = {0.f, 0.f, 0.f, 0.f}, dzb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 zv = kz4[i];
+      const uint32_t za[4] = {zv.x, zv.y, zv.z, zv.w};
+      mma_16816_acc(dza, za, qz[2 * i][0], qz[2 * i + 1][0]);
+      mma_16816_acc(dzb, za, qz[2 * i][1], qz[2 * i + 1][1]);
     }
 
-    // Warp results: sums over the lanes of a head, limbs folded.
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-    l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-    z_run += __shfl_xor_sync(0xffffffffu, z_run, 1);
-    z_run += __shfl_xor_sync(0xffffffffu, z_run, 2);
-    if (kSplitHalves) {
-      l_run += __shfl_xor_sync(0xffffffffu, l_run, 16);
-      z_run += __shfl_xor_sync(0xffffffffu, z_run, 16);
+    // key words 2 tig, 2 tig + 1 of tokens 16 mt + gid + 8 r
+    uint32_t kw[2][2][2], kw10[2][2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint2 v = *reinterpret_cast<const uint2*>(kc + (16 * mt + gid + 8 * r) * 8 + 2 * tig);
+        kw[mt][r][0] = v.x; kw[mt][r][1] = v.y;
+        kw10[mt][r][0] = v.x >> 10; kw10[mt][r][1] = v.y >> 10;
+      }
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[2][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 sv = ks4[i];
+#pragma unroll
+      for (int hk = 0; hk < 2; ++hk) {
+        const int k8 = 2 * i + hk;
+        constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
+        constexpr int P23[4] = {key_pos(1), key_pos(3), key_pos(5), key_pos(7)};
+        uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
+        if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
+        if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+        const uint32_t r01 =
+            hfma2_u(qz[k8][0], s01, hfma2_u(qhm[k8][0], s01, neg2_u(hmul2_u(qhm[k8][0], s01))));
+        const uint32_t r23 =
+            hfma2_u(qz[k8][1], s23, hfma2_u(qhm[k8][1], s23, neg2_u(hmul2_u(qhm[k8][1], s23))));
+        const int wd = k8 >> 2;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const uint32_t wa = kw[mt][0][wd], wa10 = kw10[mt][0][wd];
+          const uint32_t wb = kw[mt][1][wd], wb10 = kw10[mt][1][wd];
+          uint32_t ak[4];
+          switch (k8 & 3) {
+            case 0: ak[0] = key_pair<0>(wa, wa10); ak[1] = key_pair<0>(wb, wb10);
+                    ak[2] = key_pair<1>(wa, wa10); ak[3] = key_pair<1>(wb, wb10); break;
+            case 1: ak[0] = key_pair<2>(wa, wa10); ak[1] = key_pair<2>(wb, wb10);
+                    ak[2] = key_pair<3>(wa, wa10); ak[3] = key_pair<3>(wb, wb10); break;
+            case 2: ak[0] = key_pair<4>(wa, wa10); ak[1] = key_pair<4>(wb, wb10);
+                    ak[2] = key_pair<5>(wa, wa10); ak[3] = key_pair<5>(wb, wb10); break;
+            default: ak[0] = key_pair<6>(wa, wa10); ak[1] = key_pair<6>(wb, wb10);
+                     ak[2] = key_pair<7>(wa, wa10); ak[3] = key_pair<7>(wb, wb10); break;
+          }
+          if (k8 == 0) {
+            mma_16816(acc[mt], ak, r01, r23, zero4);
+          } else {
+            mma_16816_acc(acc[mt], ak, r01, r23);
+          }
+        }
+      }
+    }
+
+    // Scores of head hs, token gid + 8 j (j = 2 mt + r), log2 domain.
+    const float zs = ((dza[0] + dza[1]) + (dzb[2] + dzb[3])) * inv_sigma;
+    const float2 n01 = __half22float2(u32_as_half2(kn4.x)), n23 = __half22float2(u32_as_half2(kn4.y));
+    const float nf[4] = {n01.x, n01.y, n23.x, n23.y};
+    float sc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int mt = j >> 1, r = j & 1;
+      const float qk = r ? acc[mt][2] + acc[mt][3] : acc[mt][0] + acc[mt][1];
+      sc[j] = fmaf(qk, qk_scale, zs) * nf[j];
+    }
+    float mb = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+    // Lazy rescaling (see the row layout): every value of this lane belongs
+    // to head hs, so the lane rescales with its own alpha.
+    const float m_new = fmaxf(m_run, mb);
+    if (__any_sync(0xffffffffu, m_new > m_run + kLazyLog2)) {
+      const float alpha = fast_exp2(m_run - m_new);
+      l_run *= alpha;
+      z_run *= alpha;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) O[0][mt][e] += __shfl_xor_sync(0xffffffffu, O[0][mt][e], 2);
-    } else {
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) O[0][mt][e] += O[NT - 1][mt][e];
+        for (int e = 0; e < 4; ++e) O[mt][e] *= alpha;
+      m_run = m_new;
     }
-    __syncthreads();   // every warp is done with its ring: reuse it for the merge
-    if (tig == 0 && gid < GQ) {
-      E.m[warp][gid] = m_run;
-      E.l[warp][gid] = l_run;
-      E.z[warp][gid] = z_run;
+
+    // p~ = p s_V as (hi, lo) fp16 pairs: the 8x8 tile of token rows gid (+8)
+    // and columns (head, limb); transposed, it is the P.V B operand.
+    const float2 s01 = __half22float2(u32_as_half2(vs4.x)), s23 = __half22float2(u32_as_half2(vs4.y));
+    const float2 z01 = __half22float2(u32_as_half2(vz4.x)), z23 = __half22float2(u32_as_half2(vz4.y));
+    const float svj[4] = {s01.x, s01.y, s23.x, s23.y}, zvj[4] = {z01.x, z01.y, z23.x, z23.y};
+    uint32_t bp[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      float pt[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float sv = svj[2 * mt + r], zv = zvj[2 * mt + r];
+        const float p = fast_exp2(sc[2 * mt + r] - m_run);
+        l_run += p;
+        z_run = fmaf(p, fmaf(1.5f, sv, zv), z_run);
+        pt[r] = p * sv;
+      }
+      const __half2 hh = __floats2half2_rn(pt[0], pt[1]);
+      const float2 hv = __half22float2(hh);
+      const __half2 ll = __floats2half2_rn(pt[0] - hv.x, pt[1] - hv.y);
+      bp[mt][0] = movmatrix_t(half2_as_u32(__lows2half2(hh, ll)));
+      bp[mt][1] = movmatrix_t(half2_as_u32(__highs2half2(hh, ll)));
+    }
+
+#pragma unroll
+    for (int kh = 0; kh < 2; ++kh) {
+      const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
+      const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
+      uint32_t w2[4], w8[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) { w2[q] = wv[q] << 2; w8[q] = wv[q] >> 8; }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t av[4];
+        value_frag(av, mt, wv, w2, w8, magic);
+        mma_16816_acc(O[mt], av, bp[kh][0], bp[kh][1]);
+      }
+    }
+    R.release(it);
+  }
+  if (it < R.n) {
+    R.fail(it, a.status);
+    m_run = -INFINITY;   // this warp's result is void; the status word says so
+  }
+
+  // Warp results: sums over the 8 lanes of a head (lanes xor 4, 8, 16).
+#pragma unroll
+  for (int m = 4; m < 32; m <<= 1) {
+    l_run += __shfl_xor_sync(0xffffffffu, l_run, m);
+    z_run += __shfl_xor_sync(0xffffffffu, z_run, m);
+  }
+  __syncthreads();   // every warp is done with its ring: reuse it for the merge
+  if (tig < GQ) {
+    if (gid == 0) {
+      E.m[warp][tig] = m_run;
+      E.l[warp][tig] = l_run;
+      E.z[warp][tig] = z_run;
     }
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int nc = 2 * tig + e;
-      if (nc < GQ) {
+    for (int mt = 0; mt < 8; ++mt) {
+      E.o[warp][tig][16 * mt + gid] = O[mt][0] + O[mt][1];
+      E.o[warp][tig][16 * mt + gid + 8] = O[mt][2] + O[mt][3];
+    }
+  }
+}
+
+// ------------------------------------------------------------------- rows
+// Groups of 8 query heads.  Lane (gid, tig):
+//  * Q.K A operand: rows gid (hi part) and gid + 8 (lo part) of q~ for head
+//    gid; B operand: key codes of token 8 nt + gid, n-tiles nt = 0..3;
+//  * scores and softmax: head gid, tokens 8 nt + 2 tig and + 1;
+//  * P.V: channels on M, the 8 heads on N, one n-tile per limb of p~.
+template <int GQ>
+__device__ __forceinline__ void packed_rows(const DecodeArgs& a, const WarpRing& R,
+                                            MergeSmem<GQ, NW>& E, long long qrow0) {
+  static_assert(GQ == 8, "the row layout serves groups of 8 query heads");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int head = gid;
+  R.start();   // the first copies travel while the query is prepared
+
+  // Query fragments of this thread's head, channels c0 = 32*tig + 4*k8 ..+3,
+  // as {hi(c0,c0+1), lo(c0,c0+1), hi(c0+2,c0+3), lo(c0+2,c0+3)} (the MMA A
+  // layout of rows g and g+8).  The query carries softmax_scale * log2(e)
+  // and a power of two sigma that keeps the fp16 parts in range.
+  uint32_t aq[8][4];
+  float inv_sigma;
+  {
+    float qf[32];
+    const float sigma = scale_query(qf, a.q_rot + (qrow0 + head) * kD, tig, a);
+    inv_sigma = ldexpf(1.0f, -ilogbf(sigma));
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          E.o[warp][nc][16 * mt + gid] = O[0][mt][e];
-          E.o[warp][nc][16 * mt + gid + 8] = O[0][mt][2 + e];
+    for (int k8 = 0; k8 < 8; ++k8) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float x0 = qf[4 * k8 + 2 * j], x1 = qf[4 * k8 + 2 * j + 1];
+        const __half2 hh = __floats2half2_rn(x0, x1);
+        const float2 hv = __half22float2(hh);
+        aq[k8][2 * j] = half2_as_u32(hh);
+        aq[k8][2 * j + 1] = half2_as_u32(__floats2half2_rn(x0 - hv.x, x1 - hv.y));
+      }
+    }
+  }
+  // the Q.K sums carry 2^-24 (subnormal key codes) and sigma
+  const float qk_scale = 16777216.0f * inv_sigma;
+
+  float O[2][8][4];   // P.V accumulators of the hi and lo limbs of p~
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) O[t][mt][e] = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
+  uint32_t magic = kMagic;
+  asm volatile("" : "+r"(magic));
+
+  int it = 0;
+  for (; it < R.n; ++it) {
+    if (!R.wait(it)) break;
+    const uint8_t* st = R.slot(it);
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + KC_OFF);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + VC_OFF);
+    const uint4* ks4 = reinterpret_cast<const uint4*>(st + KS_OFF) + tig * 4;
+    const uint4* kz4 = reinterpret_cast<const uint4*>(st + KZ_OFF) + tig * 4;
+    // norms, value steps and zeros: halves 0..3 are tokens 2 tig + 8 nt,
+    // halves 4..7 tokens 2 tig + 1 + 8 nt (nt = 0..3)
+    const uint4 kn8 = *reinterpret_cast<const uint4*>(st + KN_OFF + 16 * tig);
+    const uint4 vs8 = *reinterpret_cast<const uint4*>(st + VS_OFF + 16 * tig);
+    const uint4 vz8 = *reinterpret_cast<const uint4*>(st + VZ_OFF + 16 * tig);
+
+    // Z = q'.z of the block: rows g (hi) and g+8 (lo), every column alike.
+    float dz[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 zv = kz4[i];
+      mma_16816_acc(dz, aq[2 * i], zv.x, zv.y);
+      mma_16816_acc(dz, aq[2 * i + 1], zv.z, zv.w);
+    }
+
+    // Q.K^T, k-step outer: q~ fragment for k-step k8, then the 4 n-tiles.
+    uint32_t kw[4][2], kw10[4][2];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const uint2 v = *reinterpret_cast<const uint2*>(kc + (8 * nt + gid) * 8 + 2 * tig);
+      kw[nt][0] = v.x; kw[nt][1] = v.y;
+      kw10[nt][0] = v.x >> 10; kw10[nt][1] = v.y >> 10;
+    }
+    // The Q.K accumulators start from zero (not from Z) so their MMA chains
+    // do not wait for the Z chain; Z joins each score below.
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 sv = ks4[i];
+#pragma unroll
+      for (int hk = 0; hk < 2; ++hk) {
+        const int k8 = 2 * i + hk;
+        // key step of the pair's channels times 4^-p of the pair's code
+        // position (exact: a power of two)
+        constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
+        constexpr int P23[4] = {key_pos(1), key_pos(3), key_pos(5), key_pos(7)};
+        uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
+        if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
+        if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+        uint32_t at[4];
+        at[0] = hmul2_u(aq[k8][0], s01);
+        at[1] = hfma2_u(aq[k8][1], s01, hfma2_u(aq[k8][0], s01, neg2_u(at[0])));
+        at[2] = hmul2_u(aq[k8][2], s23);
+        at[3] = hfma2_u(aq[k8][3], s23, hfma2_u(aq[k8][2], s23, neg2_u(at[2])));
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const uint32_t w = kw[nt][k8 >> 2], w10 = kw10[nt][k8 >> 2];
+          uint32_t b0v, b1v;
+          switch (k8 & 3) {
+            case 0: b0v = key_pair<0>(w, w10); b1v = key_pair<1>(w, w10); break;
+            case 1: b0v = key_pair<2>(w, w10); b1v = key_pair<3>(w, w10); break;
+            case 2: b0v = key_pair<4>(w, w10); b1v = key_pair<5>(w, w10); break;
+            default: b0v = key_pair<6>(w, w10); b1v = key_pair<7>(w, w10); break;
+          }
+          if (k8 == 0) {
+            mma_16816(acc[nt], at, b0v, b1v, zero4);
+          } else {
+            mma_16816_acc(acc[nt], at, b0v, b1v);
+          }
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------ residual
-    // Unit-norm bf16 keys times their fp16 norms, bf16 values; CUDA cores.
-    float qv[GQ][4], mr[GQ], lr[GQ], orr[GQ][4];
+
+    // Scores of this thread's tokens (log2 domain): hi row + lo row, times
+    // the token norm.  Token j of the thread: n-tile nt(j), tokens 2tig, +1.
+    // Z of this thread's head (hi row + lo row); the Q.K sums carry 2^-24
+    const float zs = (dz[0] + dz[2]) * inv_sigma;
+    float ne[4], no[4];
+    unpack_h4(ne, kn8.x, kn8.y);
+    unpack_h4(no, kn8.z, kn8.w);
+    float sc[8];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      sc[2 * nt] = fmaf(acc[nt][0] + acc[nt][2], qk_scale, zs) * ne[nt];
+      sc[2 * nt + 1] = fmaf(acc[nt][1] + acc[nt][3], qk_scale, zs) * no[nt];
+    }
+
+    // Online softmax for this thread's head.
+    float mb = sc[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) mb = fmaxf(mb, sc[i]);
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    // Lazy rescaling: the running max moves only when a score exceeds it by
+    // more than 2^kLazyLog2, so p = 2^(score - m_run) stays below 2^kLazyLog2
+    // (well inside fp16 and fp32) and the accumulators are rescaled rarely.
+    const float m_new = fmaxf(m_run, mb);
+    if (__any_sync(0xffffffffu, m_new > m_run + kLazyLog2)) {
+      const float alpha = fast_exp2(m_run - m_new);
+      l_run *= alpha;
+      z_run *= alpha;
+      // the P.V columns 2 tig, 2 tig + 1 of this lane are heads 2 tig, 2 tig + 1
+      const float al_a = __shfl_sync(0xffffffffu, alpha, 8 * tig);
+      const float al_b = __shfl_sync(0xffffffffu, alpha, 8 * tig + 4);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          O[t][mt][0] *= al_a; O[t][mt][1] *= al_b;
+          O[t][mt][2] *= al_a; O[t][mt][3] *= al_b;
+        }
+      m_run = m_new;
+    }
+
+    float se[4], so[4], ze[4], zo[4];
+    unpack_h4(se, vs8.x, vs8.y);
+    unpack_h4(so, vs8.z, vs8.w);
+    unpack_h4(ze, vz8.x, vz8.y);
+    unpack_h4(zo, vz8.z, vz8.w);
+    float pt[8];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float p0 = fast_exp2(sc[2 * nt] - m_run);
+      const float p1 = fast_exp2(sc[2 * nt + 1] - m_run);
+      l_run += p0 + p1;
+      z_run = fmaf(p0, fmaf(1.5f, se[nt], ze[nt]), z_run);
+      z_run = fmaf(p1, fmaf(1.5f, so[nt], zo[nt]), z_run);
+      pt[2 * nt] = p0 * se[nt];
+      pt[2 * nt + 1] = p1 * so[nt];
+    }
+
+    // P~ as the B operand of P.V: k-half kh uses n-tiles 2kh (tokens 2tig,
+    // 2tig+1) and 2kh+1 (2tig+8, 2tig+9); bp holds the hi limb, bq the lo.
+    uint32_t bp[2][2], bq[2][2];
+#pragma unroll
+    for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float x0 = pt[4 * kh + 2 * r], x1 = pt[4 * kh + 2 * r + 1];
+        const __half2 hv = __floats2half2_rn(x0, x1);
+        const float2 hf2 = __half22float2(hv);
+        bp[kh][r] = half2_as_u32(hv);
+        bq[kh][r] = half2_as_u32(__floats2half2_rn(x0 - hf2.x, x1 - hf2.y));
+      }
+
+#pragma unroll
+    for (int kh = 0; kh < 2; ++kh) {
+      const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
+      const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
+      uint32_t w2[4], w8[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) { w2[q] = wv[q] << 2; w8[q] = wv[q] >> 8; }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t av[4];
+        value_frag(av, mt, wv, w2, w8, magic);
+        mma_16816_acc(O[0][mt], av, bp[kh][0], bp[kh][1]);
+        mma_16816_acc(O[1][mt], av, bq[kh][0], bq[kh][1]);
+      }
+    }
+    R.release(it);
+  }
+  if (it < R.n) {
+    R.fail(it, a.status);
+    m_run = -INFINITY;   // this warp's result is void; the status word says so
+  }
+
+  // Warp results: sums over the lanes of a head, limbs folded.
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  z_run += __shfl_xor_sync(0xffffffffu, z_run, 1);
+  z_run += __shfl_xor_sync(0xffffffffu, z_run, 2);
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) O[0][mt][e] += O[1][mt][e];
+  __syncthreads();   // every warp is done with its ring: reuse it for the merge
+  if (tig == 0) {
+    E.m[warp][gid] = m_run;
+    E.l[warp][gid] = l_run;
+    E.z[warp][gid] = z_run;
+  }
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int nc = 2 * tig + e;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      E.o[warp][nc][16 * mt + gid] = O[0][mt][e];
+      E.o[warp][nc][16 * mt + gid + 8] = O[0][mt][2 + e];
+    }
+  }
+}
+
+// --------------------------------------------------------------- residual
+template <int GQ>
+__device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ, NW>& E,
+                                               long long row, long long qrow0) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Unit-norm bf16 keys times their fp16 norms, bf16 values; CUDA cores.
+  float qv[GQ][4], mr[GQ], lr[GQ], orr[GQ][4];
+#pragma unroll
+  for (int j = 0; j < GQ; ++j) {
+    const float4 v = reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
+    qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
+    mr[j] = -INFINITY; lr[j] = 0.0f;
+    orr[j][0] = orr[j][1] = orr[j][2] = orr[j][3] = 0.0f;
+  }
+  for (int t = warp; t < a.n_res; t += NW) {
+    const long long tok = row * kR + t;
+    const uint2 kr = reinterpret_cast<const uint2*>(a.k_res + tok * kD)[lane];
+    const uint2 vr = reinterpret_cast<const uint2*>(a.v_res + tok * kD)[lane];
+    const float k4[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
+    const float v4[4] = {bf16_lo(vr.x), bf16_hi(vr.x), bf16_lo(vr.y), bf16_hi(vr.y)};
+    const float nrm = __half2float(a.k_res_norm[tok]);
 #pragma unroll
     for (int j = 0; j < GQ; ++j) {
-      const float4 v = reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
-      qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
-      mr[j] = -INFINITY; lr[j] = 0.0f;
-      orr[j][0] = orr[j][1] = orr[j][2] = orr[j][3] = 0.0f;
+      float d = qv[j][0] * k4[0] + qv[j][1] * k4[1] + qv[j][2] * k4[2] + qv[j][3] * k4[3];
+      d = warp_allsum(d);
+      const float s = d * nrm * a.scale_log2;
+      const float m_new = fmaxf(mr[j], s);
+      const float al = fast_exp2(mr[j] - m_new);
+      const float p = fast_exp2(s - m_new);
+      lr[j] = lr[j] * al + p;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) orr[j][i] = orr[j][i] * al + p * v4[i];
+      mr[j] = m_new;
     }
-    for (int t = warp; t < a.n_res; t += NW) {
-      const long long tok = row * kR + t;
-      const uint2 kr = reinterpret_cast<const uint2*>(a.k_res + tok * kD)[lane];
-      const uint2 vr = reinterpret_cast<const uint2*>(a.v_res + tok * kD)[lane];
-      const float k4[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
-      const float v4[4] = {bf16_lo(vr.x), bf16_hi(vr.x), bf16_lo(vr.y), bf16_hi(vr.y)};
-      const float nrm = __half2float(a.k_res_norm[tok]);
+  }
+  __syncthreads();
+  if (lane == 0) {
 #pragma unroll
-      for (int j = 0; j < GQ; ++j) {
-        float d = qv[j][0] * k4[0] + qv[j][1] * k4[1] + qv[j][2] * k4[2] + qv[j][3] * k4[3];
-        d = warp_allsum(d);
-        const float s = d * nrm * a.scale_log2;
-        const float m_new = fmaxf(mr[j], s);
-        const float al = fast_exp2(mr[j] - m_new);
-        const float p = fast_exp2(s - m_new);
-        lr[j] = lr[j] * al + p;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) orr[j][i] = orr[j][i] * al + p * v4[i];
-        mr[j] = m_new;
-      }
+    for (int j = 0; j < GQ; ++j) {
+      E.m[warp][j] = mr[j];
+      E.l[warp][j] = lr[j];
+      E.z[warp][j] = 0.0f;
     }
-    __syncthreads();
-    if (lane == 0) {
+  }
 #pragma unroll
-      for (int j = 0; j < GQ; ++j) {
-        E.m[warp][j] = mr[j];
-        E.l[warp][j] = lr[j];
-        E.z[warp][j] = 0.0f;
-      }
+  for (int j = 0; j < GQ; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) E.o[warp][j][4 * lane + i] = orr[j][i];
+}
+
+// Up to 4 CTAs per SM in the column layout (128 registers), 3 in the row layout.
+template <int GQ>
+__global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
+  static_assert(sizeof(MergeSmem<GQ, NW>) <= NW * NSTAGE * kBlkBytes, "merge area");
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const long long row = (long long)b * a.Hkv + h;
+  const long long qrow0 = (long long)b * a.Hq + (long long)h * GQ;  // first query head
+
+  if (split < a.num_splits) {
+    const WarpRing R = make_ring(a, smem, row, split);
+    if constexpr (GQ <= 4) {
+      packed_cols<GQ>(a, R, E, qrow0);
+    } else {
+      packed_rows<GQ>(a, R, E, qrow0);
     }
-#pragma unroll
-    for (int j = 0; j < GQ; ++j)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) E.o[warp][j][4 * lane + i] = orr[j][i];
+  } else {
+    residual_split<GQ>(a, E, row, qrow0);
   }
   __syncthreads();
   cta_merge_write<GQ, NW>(E, a.ws + (qrow0 * (a.num_splits + 1) + split) * kRecFloats,

@@ -106,12 +106,12 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
 #pragma unroll
       for (int j = 0; j < 4; ++j) vc[t][4 * lane + j] = quant_code(x[j], mn, step, live);
       if (lane == 0) {
-        v_scale[t] = __float2half_rn(step);
-        v_zero[t] = __float2half_rn(mn);
+        v_scale[tok_slot(t)] = __float2half_rn(step);
+        v_zero[tok_slot(t)] = __float2half_rn(mn);
       }
     }
   }
-  if (tid < kG) k_norm_out[tid] = k_norm[src_tok + tid];
+  if (tid < kG) k_norm_out[tok_slot(tid)] = k_norm[src_tok + tid];
   __syncthreads();
 
   // Pack keys: word (t, w) = channels 16w..16w+15 of token t; channel 16w+j at

@@ -43,6 +43,7 @@ BLOCK_BYTES = 2752
 RECORD_FIELDS = {"k_codes": (0, 1024), "v_codes": (1024, 2048), "k_scale": (2048, 2304),
                  "k_zero": (2304, 2560), "k_norm": (2560, 2624), "v_scale": (2624, 2688),
                  "v_zero": (2688, 2752)}
+PER_TOKEN_FIELDS = ("k_norm", "v_scale", "v_zero")
 
 
 def _load() -> ctypes.CDLL:
@@ -141,10 +142,18 @@ class KVCache:
 
     def field(self, name: str) -> torch.Tensor:
         """Writable view of one record field for every block:
-        [B][Hkv][T_cap/32][n] with n = 256 words (codes) or 128 / 32 halves."""
+        [B][Hkv][T_cap/32][n] with n = 256 words (codes) or 128 halves (key
+        step / zero); the per-token arrays (k_norm, v_scale, v_zero) as
+        [B][Hkv][T_cap/32][4][8], element [j][i] = token 8j + i of the block."""
         lo, hi = RECORD_FIELDS[name]
         raw = self.packed[..., lo:hi]
-        return raw.view(torch.int32) if name.endswith("codes") else raw.view(torch.float16)
+        if name.endswith("codes"):
+            return raw.view(torch.int32)
+        f = raw.view(torch.float16)
+        if name in PER_TOKEN_FIELDS:
+            # stored at 4 (t % 8) + t // 8: an [8][4] array, read transposed
+            return f.unflatten(-1, (8, 4)).transpose(-1, -2)
+        return f
 
     def tokens(self, name: str) -> torch.Tensor:
         """A copy of a field in token order: key codes [B][Hkv][T_cap][8];
@@ -153,7 +162,7 @@ class KVCache:
         f = self.field(name)
         if name == "k_codes":
             return f.reshape(self.B, self.Hkv, self.T_cap, 8)
-        if name in ("k_norm", "v_scale", "v_zero"):
+        if name in PER_TOKEN_FIELDS:
             return f.reshape(self.B, self.Hkv, self.T_cap)
         return f.clone()
 

@@ -61,9 +61,9 @@ def upload_oracle_cache(cache, heads: dict, flags: int = 0):
             put("v_codes", O.pack_v_words(vq.codes).view(np.int32))
             put("k_scale", kq.step16)
             put("k_zero", kq.zero16)
-            put("k_norm", hc.packed_norm16().reshape(nb, 32))
-            put("v_scale", vq.step16.reshape(nb, 32))
-            put("v_zero", vq.zero16.reshape(nb, 32))
+            put("k_norm", hc.packed_norm16().reshape(nb, 4, 8))
+            put("v_scale", vq.step16.reshape(nb, 4, 8))
+            put("v_zero", vq.zero16.reshape(nb, 4, 8))
         if r:
             cache.k_res[b, h, :r] = bits_to_bf16_tensor(np.stack(hc.res_k_bf16))
             cache.v_res[b, h, :r] = bits_to_bf16_tensor(np.stack(hc.res_v_bf16))
