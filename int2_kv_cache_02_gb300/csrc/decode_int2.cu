@@ -400,14 +400,16 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing&
       const float qk = r ? acc[mt][2] + acc[mt][3] : acc[mt][0] + acc[mt][1];
       sc[j] = fmaf(qk, qk_scale, zs) * nf[j];
     }
-    float mb = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 4));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
-    // Lazy rescaling (see the row layout): every value of this lane belongs
-    // to head hs, so the lane rescales with its own alpha.
-    const float m_new = fmaxf(m_run, mb);
-    if (__any_sync(0xffffffffu, m_new > m_run + kLazyLog2)) {
+    // Lazy rescaling (see the row layout).  Each lane tests its own scores;
+    // only when some lane is past the threshold does the warp form the
+    // block maximum of each head (lanes xor 4, 8, 16) and rescale.  Every
+    // value of this lane belongs to head hs: the lane uses its own alpha.
+    const float ml = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+    if (__any_sync(0xffffffffu, ml > m_run + kLazyLog2)) {
+      float mb = fmaxf(ml, __shfl_xor_sync(0xffffffffu, ml, 4));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 8));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 16));
+      const float m_new = fmaxf(m_run, mb);
       const float alpha = fast_exp2(m_run - m_new);
       l_run *= alpha;
       z_run *= alpha;
@@ -622,16 +624,18 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const WarpRing&
     }
 
     // Online softmax for this thread's head.
-    float mb = sc[0];
+    float ml = sc[0];
 #pragma unroll
-    for (int i = 1; i < 8; ++i) mb = fmaxf(mb, sc[i]);
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
-    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    for (int i = 1; i < 8; ++i) ml = fmaxf(ml, sc[i]);
     // Lazy rescaling: the running max moves only when a score exceeds it by
     // more than 2^kLazyLog2, so p = 2^(score - m_run) stays below 2^kLazyLog2
     // (well inside fp16 and fp32) and the accumulators are rescaled rarely.
-    const float m_new = fmaxf(m_run, mb);
-    if (__any_sync(0xffffffffu, m_new > m_run + kLazyLog2)) {
+    // Each lane tests its own scores; only then are the heads' block maxima
+    // formed (lanes xor 1, 2).
+    if (__any_sync(0xffffffffu, ml > m_run + kLazyLog2)) {
+      float mb = fmaxf(ml, __shfl_xor_sync(0xffffffffu, ml, 1));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      const float m_new = fmaxf(m_run, mb);
       const float alpha = fast_exp2(m_run - m_new);
       l_run *= alpha;
       z_run *= alpha;
