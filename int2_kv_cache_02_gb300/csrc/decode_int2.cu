@@ -806,8 +806,25 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
                           (long long)(a.num_splits + 1) * kRecFloats);
 }
 
+// Opt in to kSmemBytes of dynamic shared memory (needed above 48 KB), once
+// per instantiation and device.
+template <int GQ>
+cudaError_t allow_smem() {
+  static int done[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(decode_int2_kernel<GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 128) done[dev] = 1;
+  return e;
+}
+
 template <int GQ>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
+  cudaError_t e0 = allow_smem<GQ>();
+  if (e0 != cudaSuccess) return e0;
   dim3 grid(a.num_splits + 1, a.Hkv, a.B);
   decode_int2_kernel<GQ><<<grid, NW * 32, kSmemBytes, s>>>(a);
   cudaError_t e = cudaGetLastError();
@@ -817,6 +834,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
 
 template <int GQ>
 int occupancy_g() {
+  if (allow_smem<GQ>() != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ>, NW * 32,
                                                     kSmemBytes) != cudaSuccess)
