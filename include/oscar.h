@@ -243,6 +243,15 @@ oscar_status oscar_decode_attention_static_ws(const oscar_cache* c, const float*
  * word.  OSCAR_OK if no kernel recorded an error, else OSCAR_ERR_DEVICE_STATUS. */
 oscar_status oscar_device_status(void* stream);
 
+/* Self-test of the bounded waits (failure detection; the pages have no
+ * counterpart).  One CTA waits on an mbarrier that nothing arrives at,
+ * gives up after `iterations` polls, records the wait-timeout bit in the
+ * device status word exactly as a decode whose copies never landed would,
+ * and returns: no fault, no hang, the context stays usable.  Afterwards
+ * oscar_device_status reports OSCAR_ERR_DEVICE_STATUS (and clears the word).
+ * iterations: 1 .. 1<<20, else OSCAR_ERR_INVALID_ARG (nothing launched). */
+oscar_status oscar_selftest_wait_timeout(unsigned iterations, void* stream);
+
 /* Static description of a status code. */
 const char* oscar_status_string(oscar_status s);
 

@@ -306,6 +306,15 @@ oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* 
   return from_cuda(e);
 }
 
+oscar_status oscar_selftest_wait_timeout(unsigned iterations, void* stream) {
+  if (iterations == 0 || iterations > (1u << 20)) return OSCAR_ERR_INVALID_ARG;
+  unsigned* p = status_ptr();
+  if (!p) return OSCAR_ERR_CUDA;
+  cudaError_t e = launch_wait_timeout_selftest(p, iterations, as_stream(stream));
+  g_launches++;
+  return from_cuda(e);
+}
+
 oscar_status oscar_device_status(void* stream) {
   unsigned* p = status_ptr();
   if (!p) return OSCAR_ERR_CUDA;

@@ -75,6 +75,24 @@ static_assert(kCW * 32 == kD, "one combine thread per channel");
 
 }  // namespace
 
+// Self-test of the bounded waits: the same wait loop as the decode rings, on
+// a barrier whose phase never completes.
+__global__ void wait_timeout_selftest_kernel(unsigned* status, unsigned iterations) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const bool landed = mbar_wait_bounded(&bar, 0u, iterations);
+  if (!landed && threadIdx.x == 0) record_error(status, kDevErrWaitTimeout);
+}
+
+cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned iterations, cudaStream_t s) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(status, iterations);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_combine(const float* ws, float* out, int n_rows, int n_parts, cudaStream_t s) {
   combine_kernel<<<n_rows, kCW * 32, 0, s>>>(ws, out, n_parts);
   return cudaGetLastError();

@@ -62,6 +62,10 @@ int decode_bf16_ctas_per_sm(int g);
 unsigned* device_status_word();
 void count_launches(int n);
 
+// One CTA polls an mbarrier nothing arrives at, `iterations` times, then
+// records kDevErrWaitTimeout in *status (self-test of the bounded waits).
+cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned iterations, cudaStream_t s);
+
 // Log-sum-exp combine of n_parts partial records per (b, q-head).
 cudaError_t launch_combine(const float* ws, float* out, int n_rows, int n_parts, cudaStream_t s);
 

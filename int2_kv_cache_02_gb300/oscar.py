@@ -68,6 +68,7 @@ def _load() -> ctypes.CDLL:
                                                 c_int, c_int, c_int, c_float, c_void_p, c_int,
                                                 c_void_p, c_size_t, c_void_p]),
         "oscar_device_status": (c_int, [c_void_p]),
+        "oscar_selftest_wait_timeout": (c_int, [c_uint, c_void_p]),
         "oscar_status_string": (ctypes.c_char_p, [c_int]),
         "oscar_kernel_launches": (c_ulonglong, []),
     }
@@ -242,6 +243,13 @@ def bf16_decode_attention(q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, B: 
                                             _ptr(workspace),
                                             workspace.numel() * workspace.element_size(),
                                             _stream(stream)), "oscar_bf16_decode_attention")
+
+
+def selftest_wait_timeout(iterations: int = 256, stream=None):
+    """Launches the bounded-wait self-test: a wait that can never complete
+    gives up after `iterations` polls and sets the device status word."""
+    _check(_lib.oscar_selftest_wait_timeout(iterations, _stream(stream)),
+           "oscar_selftest_wait_timeout")
 
 
 def device_status(stream=None) -> int:

@@ -39,7 +39,8 @@ def test_headers_declare_the_documented_calls():
     for want in ["oscar_rotate_q", "oscar_rotate_scale_k", "oscar_quantize_kv",
                  "oscar_append_kv", "oscar_decode_attention", "oscar_bf16_decode_attention",
                  "oscar_decode_workspace_bytes", "oscar_decode_num_splits",
-                 "oscar_device_status", "oscar_status_string", "oscar_kernel_launches"]:
+                 "oscar_device_status", "oscar_status_string", "oscar_kernel_launches",
+                 "oscar_selftest_wait_timeout"]:
         assert want in names
     assert _declared("oscar_synth.h") == ["oscar_synth_bf16"]
 
@@ -143,6 +144,14 @@ def test_decode_validation():
                                          P(FAKE), 1, P(FAKE), 1 << 20, None) == 2
     assert L.oscar_bf16_decode_attention(P(FAKE), P(FAKE), P(FAKE), 1, 4, 2, 100, 100, 0.1,
                                          P(FAKE), 2, P(FAKE), 100, None) == 5
+
+
+def test_selftest_validation(libs):
+    # rejected on the host before any device call: safe with or without a GPU
+    f = libs["liboscar.so"].oscar_selftest_wait_timeout
+    f.argtypes = [ctypes.c_uint, ctypes.c_void_p]
+    assert f(0, None) == 1
+    assert f((1 << 20) + 1, None) == 1
 
 
 @no_gpu_only
