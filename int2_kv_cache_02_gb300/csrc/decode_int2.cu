@@ -20,8 +20,8 @@
 //  * values: p~_t = p_t s_t (hi + lo fp16) multiplies the centred codes
 //    code - 1.5 on the tensor cores; the per-token constant z_t + 1.5 s_t is
 //    accumulated as sum_t p_t (z_t + 1.5 s_t) and added per channel at the end;
-//    a masked OR with the fp16 bit pattern of 1024 places a value code in the
-//    mantissa and one fp16 FMA removes the bias (exact);
+//    a masked value code pair is an fp16 subnormal like the keys, and one
+//    exact fp16 FMA turns it into (c - 1.5) times a per-row power of two;
 //  * groups of up to 4 query heads ("column" layout): Q.K runs with 16 tokens
 //    as the M rows and the (head, limb) pairs of q~ as the 8 N columns, so no
 //    row is wasted; each lane then holds whole scores of one head, and the
@@ -50,18 +50,10 @@ constexpr int KC_OFF = kRecKC, VC_OFF = kRecVC, KS_OFF = kRecKS, KZ_OFF = kRecKZ
               KN_OFF = kRecKN, VS_OFF = kRecVS, VZ_OFF = kRecVZ;
 constexpr int kSmemBytes = NW * NSTAGE * kBlkBytes + NW * NSTAGE * 8;
 
-constexpr uint32_t kMagic = 0x64006400u;  // fp16x2 {1024, 1024}
 constexpr float kLazyLog2 = 8.0f;         // lazy softmax rescale threshold (log2 units)
 
 __device__ __forceinline__ uint32_t hfma2_u(uint32_t x, uint32_t s, uint32_t b) {
   return half2_as_u32(__hfma2(u32_as_half2(x), u32_as_half2(s), u32_as_half2(b)));
-}
-// (a & MASK) | c in one LOP3 (truth table 0xEA), MASK an immediate.
-template <uint32_t MASK>
-__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(c));
-  return d;
 }
 __device__ __forceinline__ uint32_t neg2_u(uint32_t x) {
   return half2_as_u32(__hneg2(u32_as_half2(x)));
@@ -92,48 +84,48 @@ constexpr uint32_t pow4_inv_h2(int p) {
        : p == 3 ? 0x24002400u : 0x1C001C00u;
 }
 
-// Value code pair at slot k as fp16x2 centred values code - 1.5.
-// w2 = w << 2 carries slot 0 to position 1, w8 = w >> 8 slots 5..7 to 1..3.
+// Value code pair at slot k as centred fp16 values (c - 1.5) * 2^(2p - 9):
+// the masked pair is the subnormal c * 4^p * 2^-24 (as for the keys), and
+// one exact HFMA2 scales it by 2^15 and subtracts 1.5 * 2^(2p - 9).  p is
+// the code's 2-bit position (slots 0..4 in w, 5..7 in w10 = w >> 10); the
+// row factor 2^(2p - 9) is undone once per split (value_unscale).  Unlike a
+// subnormal MMA operand (whose products with subnormal probabilities were
+// lost), the operand is a normal, centred number.
 template <int K>
-__device__ __forceinline__ uint32_t value_pair(uint32_t w, uint32_t w2, uint32_t w8,
-                                                  uint32_t magic) {
-  // position p = 1..4: scale 4^-p, bias -(1024 * 4^-p + 1.5)
-  constexpr uint32_t S[4] = {0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
-  constexpr uint32_t B[4] = {0xDC06DC06u, 0xD418D418u, 0xCC60CC60u, 0xC580C580u};
-  if constexpr (K == 0) {
-    return hfma2_u(and_or<0x000C000Cu>(w2, magic), S[0], B[0]);
-  } else if constexpr (K < 5) {
-    return hfma2_u(and_or<(0x00030003u << (2 * K))>(w, magic), S[K - 1], B[K - 1]);
-  } else {
-    return hfma2_u(and_or<(0x00030003u << (2 * (K - 4)))>(w8, magic), S[K - 5], B[K - 5]);
-  }
+__device__ __forceinline__ uint32_t value_pair(uint32_t w, uint32_t w10) {
+  constexpr uint32_t B[5] = {0x9A009A00u, 0xA200A200u, 0xAA00AA00u, 0xB200B200u, 0xBA00BA00u};
+  return hfma2_u(key_pair<K>(w, w10), 0x78007800u /* 2^15 */, B[key_pos(K)]);
+}
+// 2^(9 - 2p) for value slot k: undoes the row factor of value_pair
+__host__ __device__ constexpr float value_unscale(int k) {
+  return key_pos(k) == 0 ? 512.0f : key_pos(k) == 1 ? 128.0f : key_pos(k) == 2 ? 32.0f
+       : key_pos(k) == 3 ? 8.0f : 2.0f;
 }
 
 // A operand of P.V m-tile mt (channels 16 mt + gid, + 8 on the row halves)
-// from the lane's four value words (tokens 2 tig.. and 2 tig + 8..): row gid
-// takes slot 2 (mt % 4), row gid + 8 slot 2 (mt % 4) + 1, of the words for
-// channel half mt / 4.
+// from the lane's four value words (tokens 2 tig.. and 2 tig + 8..) and
+// their copies shifted right by 10: row gid takes slot 2 (mt % 4), row
+// gid + 8 slot 2 (mt % 4) + 1, of the words for channel half mt / 4.
 __device__ __forceinline__ void value_frag(uint32_t (&av)[4], int mt, const uint32_t (&wv)[4],
-                                           const uint32_t (&w2)[4], const uint32_t (&w8)[4],
-                                           uint32_t magic) {
+                                           const uint32_t (&w10)[4]) {
   const int hh = mt >> 2;
   const int p0 = hh, p1 = 2 + hh;  // words of tokens (2tig,2tig+1) and (2tig+8,2tig+9)
   switch (mt & 3) {
     case 0:
-      av[0] = value_pair<0>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<1>(wv[p0], w2[p0], w8[p0], magic);
-      av[2] = value_pair<0>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<1>(wv[p1], w2[p1], w8[p1], magic);
+      av[0] = value_pair<0>(wv[p0], w10[p0]); av[1] = value_pair<1>(wv[p0], w10[p0]);
+      av[2] = value_pair<0>(wv[p1], w10[p1]); av[3] = value_pair<1>(wv[p1], w10[p1]);
       break;
     case 1:
-      av[0] = value_pair<2>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<3>(wv[p0], w2[p0], w8[p0], magic);
-      av[2] = value_pair<2>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<3>(wv[p1], w2[p1], w8[p1], magic);
+      av[0] = value_pair<2>(wv[p0], w10[p0]); av[1] = value_pair<3>(wv[p0], w10[p0]);
+      av[2] = value_pair<2>(wv[p1], w10[p1]); av[3] = value_pair<3>(wv[p1], w10[p1]);
       break;
     case 2:
-      av[0] = value_pair<4>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<5>(wv[p0], w2[p0], w8[p0], magic);
-      av[2] = value_pair<4>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<5>(wv[p1], w2[p1], w8[p1], magic);
+      av[0] = value_pair<4>(wv[p0], w10[p0]); av[1] = value_pair<5>(wv[p0], w10[p0]);
+      av[2] = value_pair<4>(wv[p1], w10[p1]); av[3] = value_pair<5>(wv[p1], w10[p1]);
       break;
     default:
-      av[0] = value_pair<6>(wv[p0], w2[p0], w8[p0], magic); av[1] = value_pair<7>(wv[p0], w2[p0], w8[p0], magic);
-      av[2] = value_pair<6>(wv[p1], w2[p1], w8[p1], magic); av[3] = value_pair<7>(wv[p1], w2[p1], w8[p1], magic);
+      av[0] = value_pair<6>(wv[p0], w10[p0]); av[1] = value_pair<7>(wv[p0], w10[p0]);
+      av[2] = value_pair<6>(wv[p1], w10[p1]); av[3] = value_pair<7>(wv[p1], w10[p1]);
       break;
   }
 }
@@ -306,8 +298,6 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing&
 #pragma unroll
     for (int e = 0; e < 4; ++e) O[mt][e] = 0.0f;
   float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
-  uint32_t magic = kMagic;
-  asm volatile("" : "+r"(magic));
 
   int it = 0;
   for (; it < R.n; ++it) {
@@ -322,20 +312,6 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing&
     const uint2 kn4 = *reinterpret_cast<const uint2*>(st + KN_OFF + 8 * gid);
     const uint2 vs4 = *reinterpret_cast<const uint2*>(st + VS_OFF + 8 * gid);
     const uint2 vz4 = *reinterpret_cast<const uint2*>(st + VZ_OFF + 8 * gid);
-
-    // Z = q'.z.  The A operand is the loaded z quad {x, y, z, w} (pairs 0
-    // and 1 of k-steps 2i and 2i+1) as it is: with the pair-0 columns of q'
-    // for both k-steps, row gid of dza sums the pair-0 terms; with the pair-1
-    // columns, row gid + 8 of dzb sums the pair-1 terms (the other rows are
-    // unused).  Columns 2 tig, 2 tig + 1 give the hi, lo parts for head hs.
-    float dza[4] = {0.f, 0.f, 0.f, 0.f}, dzb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 zv = kz4[i];
-      const uint32_t za[4] = {zv.x, zv.y, zv.z, zv.w};
-      mma_16816_acc(dza, za, qz[2 * i][0], qz[2 * i + 1][0]);
-      mma_16816_acc(dzb, za, qz[2 * i][1], qz[2 * i + 1][1]);
-    }
 
     // key words 2 tig, 2 tig + 1 of tokens 16 mt + gid + 8 r
     uint32_t kw[2][2][2], kw10[2][2][2];
@@ -387,6 +363,20 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing&
           }
         }
       }
+    }
+
+    // Z = q'.z (issued after the Q.K MMAs, whose chains are longer).  The A operand is the loaded z quad {x, y, z, w} (pairs 0
+    // and 1 of k-steps 2i and 2i+1) as it is: with the pair-0 columns of q'
+    // for both k-steps, row gid of dza sums the pair-0 terms; with the pair-1
+    // columns, row gid + 8 of dzb sums the pair-1 terms (the other rows are
+    // unused).  Columns 2 tig, 2 tig + 1 give the hi, lo parts for head hs.
+    float dza[4] = {0.f, 0.f, 0.f, 0.f}, dzb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 zv = kz4[i];
+      const uint32_t za[4] = {zv.x, zv.y, zv.z, zv.w};
+      mma_16816_acc(dza, za, qz[2 * i][0], qz[2 * i + 1][0]);
+      mma_16816_acc(dzb, za, qz[2 * i][1], qz[2 * i + 1][1]);
     }
 
     // Scores of head hs, token gid + 8 j (j = 2 mt + r), log2 domain.
@@ -448,13 +438,13 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing&
     for (int kh = 0; kh < 2; ++kh) {
       const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
       const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
-      uint32_t w2[4], w8[4];
+      uint32_t w10[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) { w2[q] = wv[q] << 2; w8[q] = wv[q] >> 8; }
+      for (int q = 0; q < 4; ++q) w10[q] = wv[q] >> 10;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t av[4];
-        value_frag(av, mt, wv, w2, w8, magic);
+        value_frag(av, mt, wv, w10);
         mma_16816_acc(O[mt], av, bp[kh][0], bp[kh][1]);
       }
     }
@@ -479,9 +469,9 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing&
       E.z[warp][tig] = z_run;
     }
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      E.o[warp][tig][16 * mt + gid] = O[mt][0] + O[mt][1];
-      E.o[warp][tig][16 * mt + gid + 8] = O[mt][2] + O[mt][3];
+    for (int mt = 0; mt < 8; ++mt) {   // undo the value rows' 2^(2p - 9)
+      E.o[warp][tig][16 * mt + gid] = (O[mt][0] + O[mt][1]) * value_unscale(2 * (mt & 3));
+      E.o[warp][tig][16 * mt + gid + 8] = (O[mt][2] + O[mt][3]) * value_unscale(2 * (mt & 3) + 1);
     }
   }
 }
@@ -534,8 +524,6 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const WarpRing&
 #pragma unroll
       for (int e = 0; e < 4; ++e) O[t][mt][e] = 0.0f;
   float m_run = -INFINITY, l_run = 0.0f, z_run = 0.0f;
-  uint32_t magic = kMagic;
-  asm volatile("" : "+r"(magic));
 
   int it = 0;
   for (; it < R.n; ++it) {
@@ -687,13 +675,13 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const WarpRing&
     for (int kh = 0; kh < 2; ++kh) {
       const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
       const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
-      uint32_t w2[4], w8[4];
+      uint32_t w10[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) { w2[q] = wv[q] << 2; w8[q] = wv[q] >> 8; }
+      for (int q = 0; q < 4; ++q) w10[q] = wv[q] >> 10;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t av[4];
-        value_frag(av, mt, wv, w2, w8, magic);
+        value_frag(av, mt, wv, w10);
         mma_16816_acc(O[0][mt], av, bp[kh][0], bp[kh][1]);
         mma_16816_acc(O[1][mt], av, bq[kh][0], bq[kh][1]);
       }
@@ -724,9 +712,9 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const WarpRing&
   for (int e = 0; e < 2; ++e) {
     const int nc = 2 * tig + e;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      E.o[warp][nc][16 * mt + gid] = O[0][mt][e];
-      E.o[warp][nc][16 * mt + gid + 8] = O[0][mt][2 + e];
+    for (int mt = 0; mt < 8; ++mt) {   // undo the value rows' 2^(2p - 9)
+      E.o[warp][nc][16 * mt + gid] = O[0][mt][e] * value_unscale(2 * (mt & 3));
+      E.o[warp][nc][16 * mt + gid + 8] = O[0][mt][2 + e] * value_unscale(2 * (mt & 3) + 1);
     }
   }
 }
