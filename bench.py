@@ -49,6 +49,8 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-bf16", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=256)
+    p.add_argument("--num-splits", type=int, default=0,
+                   help="split-K count of the INT2 decode (0: the library's planner)")
     p.add_argument("--workload", default=WORKLOAD,
                    help="workload name (the headline line uses the default; others are "
                         "for profiling small cases)")
@@ -294,7 +296,7 @@ def run_ours(args, world, rank, local):
     Q = torch.stack([W.draw_q_cuda(wl, i, device=dev) for i in range(total_steps)])
     torch.cuda.synchronize()
 
-    S = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, wl.n_packed)
+    S = args.num_splits or L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, wl.n_packed)
     ws = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, T_cap, S), device=dev)
     qr = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
     out = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)

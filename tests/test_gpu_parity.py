@@ -201,7 +201,7 @@ def test_split_invariance(L):
     outs, ref = _decode_vs_oracle(L, heads, B, Hq, Hkv, 4096, 321, splits=(1, 2, 7, 13, 0))
     for o in outs[1:]:
         d = np.linalg.norm(o - outs[0]) / np.linalg.norm(outs[0])
-        assert d <= 1e-5
+        assert d <= 1e-6
 
 
 @pytest.mark.parametrize("T,P", [(96, 0), (1024, 1024), (32, 32), (33, 32), (1, 0)])
@@ -317,7 +317,7 @@ def test_pipeline_long_stream_128k_sampled(L):
 
 
 def test_pipeline_batch48_128k_sampled(L):
-    _pipeline(L, "batch48_128k", [(0, 0), (47, 7)], steps=1)
+    _pipeline(L, "batch48_128k", [(0, 0), (17, 3), (31, 5), (47, 7)], steps=1)
 
 
 def test_pipeline_omni_tni_64k_sampled(L):
