@@ -356,21 +356,52 @@ def run_ours(args, world, rank, local):
     base = W_ + K_ + 2
     Qh, Kh, Vh = pin(Q[base:base + E_]), pin(Kn[base:base + E_]), pin(Vn[base:base + E_])
     outh = torch.empty((E_,) + tuple(out.shape), dtype=torch.float32).pin_memory()
-    qd, kd, vd = torch.empty_like(Q[0]), torch.empty_like(Kn[0]), torch.empty_like(Vn[0])
+    # Copies run on their own stream, double-buffered, so that step i + 1's
+    # inputs travel and step i - 1's output returns while step i computes;
+    # every copy is still inside the timed region.
+    cs = torch.cuda.Stream(device=dev)
+    qd = [torch.empty_like(Q[0]) for _ in range(2)]
+    kd = [torch.empty_like(Kn[0]) for _ in range(2)]
+    vd = [torch.empty_like(Vn[0]) for _ in range(2)]
+    outs = [torch.empty_like(out) for _ in range(2)]
+    filled = [torch.cuda.Event() for _ in range(2)]   # inputs of buffer b on the device
+    used = [torch.cuda.Event() for _ in range(2)]     # step done with buffer b
+    back = [torch.cuda.Event() for _ in range(2)]     # output of buffer b on the host
     for i in range(2):  # untimed: touch the copy paths
-        qd.copy_(Qh[i], non_blocking=True)
+        qd[i].copy_(Qh[i], non_blocking=True)
     torch.cuda.synchronize()
+
+    def h2d_(i):
+        b = i % 2
+        with torch.cuda.stream(cs):
+            if i >= 2:
+                cs.wait_event(used[b])
+            qd[b].copy_(Qh[i], non_blocking=True)
+            kd[b].copy_(Kh[i], non_blocking=True)
+            vd[b].copy_(Vh[i], non_blocking=True)
+            filled[b].record(cs)
+
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    cs.wait_event(e0)
+    h2d_(0)
     for i in range(E_):
-        qd.copy_(Qh[i], non_blocking=True)
-        kd.copy_(Kh[i], non_blocking=True)
-        vd.copy_(Vh[i], non_blocking=True)
-        L.rotate_q(qd, qr)
-        L.append_kv(cache, kd, vd, n_tok=1)
-        L.decode_attention(cache, qr, wl.Hq, tau, out, ws, num_splits=S)
-        outh[i].copy_(out, non_blocking=True)
+        b = i % 2
+        if i + 1 < E_:
+            h2d_(i + 1)
+        stream.wait_event(filled[b])
+        if i >= 2:
+            stream.wait_event(back[b])
+        L.rotate_q(qd[b], qr)
+        L.append_kv(cache, kd[b], vd[b], n_tok=1)
+        L.decode_attention(cache, qr, wl.Hq, tau, outs[b], ws, num_splits=S)
+        used[b].record(stream)
+        with torch.cuda.stream(cs):
+            cs.wait_event(used[b])
+            outh[i].copy_(outs[b], non_blocking=True)
+            back[b].record(cs)
+    stream.wait_event(back[(E_ - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_us = e0.elapsed_time(e1) / E_ * 1e3
