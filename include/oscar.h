@@ -155,6 +155,24 @@ oscar_status oscar_quantize_kv(oscar_cache* c, const oscar_bf16* k_hat, const os
                                const oscar_bf16* v, int src_T, int n_tok, void* stream);
 
 /*
+ * Fused prefill: kernels (1) and (2) of [news] 三 in one pass over a prefix.
+ * Each key is rotated and scaled exactly as oscar_rotate_scale_k does (same
+ * k_hat bits, same norm), then keys and values are quantised and packed
+ * exactly as oscar_quantize_kv does, without k_hat or a value copy ever
+ * going through global memory (598 B of HBM traffic per token-head instead
+ * of the ~1.6 KB of the two-call path).  Tokens [0, n_tok) of each (b,h) row
+ * are written to packed positions [n_packed, n_packed + n_tok); then
+ * c->n_packed += n_tok; the rotation and scaling flags are c->flags.
+ *  k  bf16 [B][Hkv][in_T][128] raw keys (row stride in_T tokens)
+ *  v  bf16 [B][Hkv][in_T][128] values
+ * Requires n_tok % 32 == 0, n_tok >= 32, in_T >= n_tok, c->n_res == 0 and
+ * c->n_packed + n_tok <= c->T_cap (else OSCAR_ERR_CAPACITY); pointers
+ * 16-byte aligned.
+ */
+oscar_status oscar_prefill_kv(oscar_cache* c, const oscar_bf16* k, const oscar_bf16* v, int in_T,
+                              int n_tok, void* stream);
+
+/*
  * Cache update for n_tok new tokens per (b,h) row, one after another: before
  * each token, a full residual window (128 tokens) is flushed as in
  * oscar_quantize_kv flush mode; the token's key is rotated and scaled into

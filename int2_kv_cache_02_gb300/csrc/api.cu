@@ -184,6 +184,23 @@ oscar_status oscar_quantize_kv(oscar_cache* c, const oscar_bf16* k_hat, const os
   return OSCAR_OK;
 }
 
+oscar_status oscar_prefill_kv(oscar_cache* c, const oscar_bf16* k, const oscar_bf16* v, int in_T,
+                              int n_tok, void* stream) {
+  oscar_status st = check_cache(c);
+  if (st != OSCAR_OK) return st;
+  if (!k || !v) return OSCAR_ERR_INVALID_ARG;
+  if (!al16(k) || !al16(v)) return OSCAR_ERR_ALIGNMENT;
+  if (n_tok < kG || n_tok % kG != 0 || in_T < n_tok) return OSCAR_ERR_INVALID_ARG;
+  if (c->n_res != 0) return OSCAR_ERR_INVALID_ARG;  // packed tokens must precede residual ones
+  if ((long long)c->n_packed + n_tok > c->T_cap) return OSCAR_ERR_CAPACITY;
+  cudaError_t e = launch_prefill_kv(k, v, in_T, n_tok, c->B, c->Hkv, c->T_cap, c->n_packed,
+                                    c->flags, c->packed, as_stream(stream));
+  g_launches++;
+  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+  c->n_packed += n_tok;
+  return OSCAR_OK;
+}
+
 oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const oscar_bf16* v_new,
                              int n_tok, void* stream) {
   oscar_status st = check_cache(c);

@@ -62,6 +62,11 @@ int decode_bf16_ctas_per_sm(int g);
 unsigned* device_status_word();
 void count_launches(int n);
 
+// Fused rotate + scale + quantise of n_tok tokens of raw keys and values.
+cudaError_t launch_prefill_kv(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,
+                              int Hkv, int T_cap, int p0, unsigned flags, uint8_t* packed,
+                              cudaStream_t s);
+
 // One CTA polls an mbarrier nothing arrives at, `iterations` times, then
 // records kDevErrWaitTimeout in *status (self-test of the bounded waits).
 cudaError_t launch_wait_timeout_selftest(unsigned* status, unsigned iterations, cudaStream_t s);

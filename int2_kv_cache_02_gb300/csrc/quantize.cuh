@@ -1,0 +1,140 @@
+// INT2 quantisation and packing of one 32-token block of keys and values,
+// shared by quantize_kv_kernel and the fused prefill kernel (kernel (2) of the
+// news article on arXiv 2605.19660, 三).
+//
+// Keys: block-wise per-channel asymmetric INT2 -- every channel of every
+// block of G = 32 consecutive tokens has its own step and zero; values:
+// per-token INT2 ("OScaR：面向大模型及多模态LLM极限KV缓存量化的奥卡姆剃刀",
+// 方法步骤详情 (2)(3); 前置知识, step Δ and zero z per block).  Per group:
+// z = min, Δ = (max - min)/3, code = round-half-even((x - z)/Δ) clamped to
+// [0, 3], every operation one IEEE fp32 rounding; Δ = 0 and codes 0 for a
+// constant group; Δ and z stored as fp16 (round to nearest even).
+#pragma once
+
+#include "common.cuh"
+
+namespace oscar {
+
+__device__ __forceinline__ uint8_t quant_code(float x, float mn, float step, bool live) {
+  if (!live) return 0;
+  const float t = __fdiv_rn(__fsub_rn(x, mn), step);
+  float r = rintf(t);
+  r = fminf(fmaxf(r, 0.0f), 3.0f);
+  return (uint8_t)r;
+}
+
+// The same code with the quotient formed as a * (1/step): the correctly
+// rounded reciprocal times a is within ~2^-21 of the rounded quotient for
+// quotients up to 4, so both round to the same integer unless the quotient
+// lies within 1e-5 of a half-integer, where the exact division decides.
+__device__ __forceinline__ uint8_t quant_code_fast(float x, float mn, float step, float rstep,
+                                                   bool live) {
+  if (!live) return 0;
+  const float q = __fsub_rn(x, mn) * rstep;
+  if (fabsf(q - floorf(q) - 0.5f) < 1e-5f) return quant_code(x, mn, step, live);
+  return (uint8_t)fminf(fmaxf(rintf(q), 0.0f), 3.0f);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
+  return __uint_as_float(((uint32_t)u) << 16);
+}
+
+// Called by all 128 threads of the CTA after a __syncthreads that follows
+// the staging of kt (rotated, scaled keys as bf16) and vt (values as bf16)
+// for the 32 tokens of one block; norms: the block's 32 key norms (global or
+// shared memory).  Writes the block record at rec (layout in oscar.h).
+__device__ __forceinline__ void quantize_block(const uint16_t (&kt)[kG][kD],
+                                               const uint16_t (&vt)[kG][kD],
+                                               uint8_t (&kc)[kG][kD], uint8_t (&vc)[kG][kD],
+                                               const __half* norms, uint8_t* rec) {
+  const int tid = threadIdx.x;
+  uint32_t* k_codes = reinterpret_cast<uint32_t*>(rec + kRecKC);
+  uint32_t* v_codes = reinterpret_cast<uint32_t*>(rec + kRecVC);
+  __half* k_scale = reinterpret_cast<__half*>(rec + kRecKS);
+  __half* k_zero = reinterpret_cast<__half*>(rec + kRecKZ);
+  __half* k_norm_out = reinterpret_cast<__half*>(rec + kRecKN);
+  __half* v_scale = reinterpret_cast<__half*>(rec + kRecVS);
+  __half* v_zero = reinterpret_cast<__half*>(rec + kRecVZ);
+
+  // Keys: thread = channel, group = the 32 tokens of the block.
+  {
+    const int c = tid;
+    float mn = bf16_bits_to_float(kt[0][c]), mx = mn;
+#pragma unroll 8
+    for (int t = 1; t < kG; ++t) {
+      const float x = bf16_bits_to_float(kt[t][c]);
+      mn = fminf(mn, x);
+      mx = fmaxf(mx, x);
+    }
+    const bool live = mx > mn;
+    const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), 3.0f) : 0.0f;
+    const float rstep = live ? __frcp_rn(step) : 0.0f;
+#pragma unroll 8
+    for (int t = 0; t < kG; ++t)
+      kc[t][c] = quant_code_fast(bf16_bits_to_float(kt[t][c]), mn, step, rstep, live);
+    k_scale[c] = __float2half_rn(step);
+    k_zero[c] = __float2half_rn(mn);
+  }
+
+  // Values: warp w handles tokens 8w..8w+7, lane holds channels 4l..4l+3.
+  {
+    const int w = tid >> 5, lane = tid & 31;
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      const int t = 8 * w + i;
+      float x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) x[j] = bf16_bits_to_float(vt[t][4 * lane + j]);
+      float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+#pragma unroll
+      for (int m = 16; m > 0; m >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+      }
+      const bool live = mx > mn;
+      const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), 3.0f) : 0.0f;
+      const float rstep = live ? __frcp_rn(step) : 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vc[t][4 * lane + j] = quant_code_fast(x[j], mn, step, rstep, live);
+      if (lane == 0) {
+        v_scale[tok_slot(t)] = __float2half_rn(step);
+        v_zero[tok_slot(t)] = __float2half_rn(mn);
+      }
+    }
+  }
+  if (tid < kG) k_norm_out[tok_slot(tid)] = norms[tid];
+  __syncthreads();
+
+  // Pack keys: word (t, w) = channels 16w..16w+15 of token t; channel 16w+j at
+  // bit 2*(j/2) + 16*(j%2).
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int wi = tid + 128 * r;
+    const int t = wi >> 3, w = wi & 7;
+    const uint8_t* src = &kc[t][16 * w];
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) word |= (uint32_t)src[j] << (2 * (j >> 1) + 16 * (j & 1));
+    k_codes[t * 8 + w] = word;
+  }
+  // Pack values: word 128*kh + 4*lane + 2p + hh, lane = 4g + t4; low half token
+  // 16kh + 2*t4 + 8p, high half the next token; slot k = channel g + 8*(8hh+k).
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int wi = tid + 128 * r;
+    const int kh = wi >> 7, lane = (wi >> 2) & 31, p = (wi >> 1) & 1, hh = wi & 1;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int tok = 16 * kh + 2 * t4 + 8 * p;
+    uint32_t word = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int ch = g + 8 * (8 * hh + k);
+      word |= (uint32_t)vc[tok][ch] << (2 * k);
+      word |= (uint32_t)vc[tok + 1][ch] << (16 + 2 * k);
+    }
+    v_codes[wi] = word;
+  }
+}
+
+}  // namespace oscar

@@ -10,33 +10,10 @@
 //
 // One warp per 128-vector: lane l holds elements 4l..4l+3.  Index bits 0-1
 // are butterflied in registers, bits 2-6 across lanes with shuffles.
-#include "common.cuh"
 #include "launch.h"
+#include "rotate.cuh"
 
 namespace oscar {
-
-constexpr float kInvSqrtD = 0.088388347648318440550f;  // 1/sqrt(128)
-
-// Unnormalised natural-order Walsh-Hadamard transform of the warp's vector.
-__device__ __forceinline__ void fht128(float (&x)[4], int lane) {
-  float a = x[0] + x[1], b = x[0] - x[1], c = x[2] + x[3], d = x[2] - x[3];
-  x[0] = a + c; x[2] = a - c; x[1] = b + d; x[3] = b - d;
-#pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float y = __shfl_xor_sync(0xffffffffu, x[r], m);
-      x[r] = upper ? (y - x[r]) : (x[r] + y);
-    }
-  }
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-  return v;
-}
 
 __global__ void __launch_bounds__(256) rotate_q_kernel(const uint16_t* __restrict__ q,
                                                        float* __restrict__ out, int n_vec,
@@ -70,34 +47,8 @@ __global__ void __launch_bounds__(256) rotate_scale_k_kernel(
 
   const uint2 raw = reinterpret_cast<const uint2*>(k + src)[lane];
   float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-  const bool rot = !(flags & OSCAR_NO_ROTATE);
-  if (rot) fht128(x, lane);
-
-  float norm;
-  if (flags & OSCAR_NO_SCALE) {
-    const float f = rot ? kInvSqrtD : 1.0f;
-#pragma unroll
-    for (int r = 0; r < 4; ++r) x[r] *= f;
-    norm = 1.0f;
-  } else {
-    const float s = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
-    if (s > 0.0f) {
-      const float rs = rsqrtf(s);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) x[r] *= rs;
-      norm = sqrtf(s) * (rot ? kInvSqrtD : 1.0f);
-    } else {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) x[r] = 0.0f;
-      norm = 0.0f;
-    }
-  }
-  __nv_bfloat162 p0 = __floats2bfloat162_rn(x[0], x[1]);
-  __nv_bfloat162 p1 = __floats2bfloat162_rn(x[2], x[3]);
-  uint2 o;
-  o.x = *reinterpret_cast<uint32_t*>(&p0);
-  o.y = *reinterpret_cast<uint32_t*>(&p1);
-  reinterpret_cast<uint2*>(k_hat + dst_tok * kD)[lane] = o;
+  const float norm = rotate_scale_key(x, lane, flags);
+  reinterpret_cast<uint2*>(k_hat + dst_tok * kD)[lane] = pack_bf16x4(x);
   if (lane == 0) norm_out[dst_tok] = __float2half_rn(norm);
   if (v_in != nullptr) {
     reinterpret_cast<uint2*>(v_out + dst_tok * kD)[lane] =

@@ -58,6 +58,7 @@ def _load() -> ctypes.CDLL:
                                          c_int, c_int, c_int, c_uint, c_void_p]),
         "oscar_quantize_kv": (c_int, [P, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p]),
         "oscar_append_kv": (c_int, [P, c_void_p, c_void_p, c_int, c_void_p]),
+        "oscar_prefill_kv": (c_int, [P, c_void_p, c_void_p, c_int, c_int, c_void_p]),
         "oscar_decode_attention": (c_int, [P, c_void_p, c_int, c_float, c_void_p, c_int,
                                            c_void_p, c_size_t, c_void_p]),
         "oscar_decode_attention_static_ws": (c_int, [P, c_void_p, c_int, c_float, c_void_p,
@@ -188,6 +189,15 @@ def rotate_scale_k(k: torch.Tensor, k_hat: torch.Tensor, norm: torch.Tensor, B: 
     _check(_lib.oscar_rotate_scale_k(_ptr(k), in_T, _ptr(k_hat), _ptr(norm), out_T, out_t0,
                                      B, Hkv, n_tok, flags, _stream(stream)),
            "oscar_rotate_scale_k")
+
+
+def prefill_kv(cache: KVCache, k: torch.Tensor, v: torch.Tensor, n_tok: int, in_T: int = 0,
+               stream=None):
+    """Fused rotate + scale + quantise of tokens [0, n_tok) of raw bf16 keys
+    and values [B][Hkv][in_T][128] into the packed cache (advances n_packed)."""
+    in_T = in_T or k.shape[2]
+    _check(_lib.oscar_prefill_kv(cache.ref(), _ptr(k), _ptr(v), in_T, n_tok, _stream(stream)),
+           "oscar_prefill_kv")
 
 
 def quantize_kv(cache: KVCache, k_hat=None, k_norm=None, v=None, src_T: int = 0,

@@ -137,30 +137,46 @@ def draw_q_cuda(wl: Workload, step: int, device="cuda"):
 
 
 def build_cache_cuda(wl: Workload, K, V, flags: int = 0, T_cap: int | None = None,
-                     chunk: int = 8192, device="cuda"):
+                     chunk: int = 8192, device="cuda", fused: bool = True):
     """Prompt of T0 tokens -> OScaR cache: rotate + scale + quantise the first
-    n_packed tokens (in chunks, through a bf16 staging buffer), then append
-    the remaining ones to the residual window."""
+    n_packed tokens, then append the remaining ones to the residual window.
+    fused=True does the first part in one oscar_prefill_kv call; fused=False
+    takes the two-call path (oscar_rotate_scale_k into a bf16 staging buffer,
+    then oscar_quantize_kv), in chunks."""
     import torch
     from . import oscar
     T_cap = T_cap if T_cap is not None else wl.t_cap()
     cache = oscar.KVCache(wl.B, wl.Hkv, T_cap, flags=flags, device=device)
     T_stride = K.shape[2]
-    chunk = min(chunk, max(32, wl.n_packed))
-    stage = torch.empty((wl.B, wl.Hkv, chunk, 128), dtype=torch.bfloat16, device=device)
-    norm = torch.empty((wl.B, wl.Hkv, chunk), dtype=torch.float16, device=device)
-    vstage = torch.empty_like(stage)
-    for t0 in range(0, wl.n_packed, chunk):
-        n = min(chunk, wl.n_packed - t0)
-        oscar.rotate_scale_k(_offset(K, t0), stage, norm, wl.B, wl.Hkv, n, in_T=T_stride,
-                             out_T=chunk, flags=flags)
-        vstage[:, :, :n].copy_(V[:, :, t0:t0 + n])
-        oscar.quantize_kv(cache, stage, norm, vstage, src_T=chunk, n_tok=n)
+    if fused:
+        if wl.n_packed:
+            oscar.prefill_kv(cache, K, V, n_tok=wl.n_packed, in_T=T_stride)
+    else:
+        prefill_two_call(cache, K, V, wl.n_packed, chunk=chunk, device=device)
     if wl.n_res:
         kr = K[:, :, wl.n_packed:wl.T0].contiguous()
         vr = V[:, :, wl.n_packed:wl.T0].contiguous()
         oscar.append_kv(cache, kr, vr, n_tok=wl.n_res)
     return cache
+
+
+def prefill_two_call(cache, K, V, n_tok: int, chunk: int = 8192, device="cuda"):
+    """Tokens [0, n_tok) of raw K, V [B][Hkv][T][128] into the packed cache
+    through the two-call path: oscar_rotate_scale_k into a bf16 staging
+    buffer, then oscar_quantize_kv, in chunks (the cache's flags apply)."""
+    import torch
+    from . import oscar
+    B, Hkv, T_stride = K.shape[0], K.shape[1], K.shape[2]
+    chunk = min(chunk, max(32, n_tok))
+    stage = torch.empty((B, Hkv, chunk, 128), dtype=torch.bfloat16, device=device)
+    norm = torch.empty((B, Hkv, chunk), dtype=torch.float16, device=device)
+    vstage = torch.empty_like(stage)
+    for t0 in range(0, n_tok, chunk):
+        n = min(chunk, n_tok - t0)
+        oscar.rotate_scale_k(_offset(K, t0), stage, norm, B, Hkv, n, in_T=T_stride,
+                             out_T=chunk, flags=cache.flags)
+        vstage[:, :, :n].copy_(V[:, :, t0:t0 + n])
+        oscar.quantize_kv(cache, stage, norm, vstage, src_T=chunk, n_tok=n)
 
 
 class _Offset:

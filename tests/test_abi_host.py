@@ -40,7 +40,7 @@ def test_headers_declare_the_documented_calls():
                  "oscar_append_kv", "oscar_decode_attention", "oscar_bf16_decode_attention",
                  "oscar_decode_workspace_bytes", "oscar_decode_num_splits",
                  "oscar_device_status", "oscar_status_string", "oscar_kernel_launches",
-                 "oscar_selftest_wait_timeout"]:
+                 "oscar_selftest_wait_timeout", "oscar_prefill_kv"]:
         assert want in names
     assert _declared("oscar_synth.h") == ["oscar_synth_bf16"]
 
@@ -115,6 +115,22 @@ def test_cache_validation_and_state_untouched():
     assert L.oscar_append_kv(ctypes.byref(st), P(FAKE), P(FAKE), 200, None) == 4
     assert st.n_packed == 128 and st.n_res == 128
     assert c.n_packed == 0 and c.n_res == 0
+
+
+@no_gpu_only
+def test_prefill_validation():
+    from int2_kv_cache_02_gb300 import oscar as O
+    L = O.library()
+    P = ctypes.c_void_p
+    c = _cache()
+    assert L.oscar_prefill_kv(ctypes.byref(c), None, P(FAKE), 64, 64, None) == 1
+    assert L.oscar_prefill_kv(ctypes.byref(c), P(FAKE + 8), P(FAKE), 64, 64, None) == 3
+    assert L.oscar_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 64, 48, None) == 1   # not x32
+    assert L.oscar_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 32, 64, None) == 1   # in_T < n_tok
+    assert L.oscar_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 512, 512, None) == 4 # capacity
+    c2 = _cache(n_res=5)
+    assert L.oscar_prefill_kv(ctypes.byref(c2), P(FAKE), P(FAKE), 64, 64, None) == 1
+    assert c.n_packed == 0 and c2.n_packed == 0
 
 
 @no_gpu_only
