@@ -107,6 +107,34 @@ typedef struct {
 } oscar_cache;
 
 /*
+ * Paged variant for batches whose sequences have different lengths (a
+ * serving engine's layout; the pages have no counterpart in the method,
+ * which is unchanged).  The packed cache lives in pages of 32 tokens: page p
+ * holds one record (layout above) per KV head, record h at
+ * pages + (p*Hkv + h)*OSCAR_BLOCK_BYTES.  Logical block j of sequence b
+ * (its tokens 32j..32j+31) is page block_table[b*max_blocks + j]; the
+ * caller owns the page pool and the table and must map a block before a
+ * call writes it.  Lengths are per sequence and live in device memory, so a
+ * step needs no host round trip:
+ *  n_packed[b]  quantised tokens of sequence b (multiple of 32)
+ *  n_res[b]     its residual tokens, 0..128
+ * The residual window stays per (b, h) as in oscar_cache.
+ */
+typedef struct {
+  int B, Hkv;
+  int max_blocks;           /* row length of block_table */
+  int n_pages;              /* pages in the pool (page ids 0..n_pages-1) */
+  uint8_t* pages;           /* [n_pages][Hkv] records of OSCAR_BLOCK_BYTES */
+  int32_t* block_table;     /* device [B][max_blocks] page ids */
+  int32_t* n_packed;        /* device [B] */
+  int32_t* n_res;           /* device [B] */
+  oscar_bf16* k_res;        /* [B][Hkv][128][128] */
+  oscar_bf16* v_res;        /* [B][Hkv][128][128] */
+  oscar_f16* k_res_norm;    /* [B][Hkv][128] */
+  unsigned flags;
+} oscar_paged_cache;
+
+/*
  * Canalized Rotation of the queries: q' = H q with H the 128x128 Sylvester
  * Hadamard matrix scaled by 1/sqrt(128), applied online every decode step so
  * that q'.k' = q.k ([notes] Step One, "Query-side symmetric processing";
@@ -260,6 +288,44 @@ oscar_status oscar_decode_attention_static_ws(const oscar_cache* c, const float*
 /* Synchronises `stream`, then reads and clears the current device's status
  * word.  OSCAR_OK if no kernel recorded an error, else OSCAR_ERR_DEVICE_STATUS. */
 oscar_status oscar_device_status(void* stream);
+
+/*
+ * Paged cache calls (oscar_paged_cache).  Each does, per sequence, what the
+ * contiguous call of the same name does for the whole batch; lengths are
+ * read from and written to the device arrays by the kernels.
+ *
+ * oscar_paged_prefill_kv: the fused prefill of raw keys and values
+ * k, v bf16 [B][Hkv][in_T][128]: sequence b's tokens [0, n_tok[b]) are
+ * rotated, scaled, quantised and written to its logical blocks
+ * n_packed[b]/32 .. onwards; then n_packed[b] += n_tok[b].  n_tok: device
+ * int32 [B], each a multiple of 32 and <= max_tok (a host bound sizing the
+ * launch, <= in_T); requires n_res[b] == 0 for sequences with n_tok[b] > 0.
+ *
+ * oscar_paged_append_kv: one new token (k_new, v_new bf16 [B][Hkv][128])
+ * for every sequence b with active[b] != 0 (active NULL: all): a full
+ * residual window is flushed first into the sequence's next 4 logical
+ * blocks, then the token is rotated, scaled and stored at residual slot
+ * n_res[b] (flush-before-append, as oscar_append_kv).
+ *
+ * oscar_paged_decode_attention: oscar_decode_attention over every
+ * sequence's own n_packed[b] + n_res[b] tokens.  max_packed (host) bounds
+ * the n_packed[b] and plans the splits (num_splits 0: planned from it); the
+ * workspace is oscar_decode_workspace_bytes(B, Hkv, Hq, max_packed, splits).
+ * A sequence with no tokens gives zeros.
+ *
+ * The device-side checks of a page id outside [0, n_pages) or a length
+ * outside its range skip the access and record an error in the status word
+ * (oscar_device_status).
+ */
+oscar_status oscar_paged_prefill_kv(oscar_paged_cache* c, const oscar_bf16* k,
+                                    const oscar_bf16* v, int in_T, const int32_t* n_tok,
+                                    int max_tok, void* stream);
+oscar_status oscar_paged_append_kv(oscar_paged_cache* c, const oscar_bf16* k_new,
+                                   const oscar_bf16* v_new, const int32_t* active, void* stream);
+oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const float* q_rot, int Hq,
+                                          float softmax_scale, int max_packed, float* out,
+                                          int num_splits, void* workspace, size_t ws_bytes,
+                                          void* stream);
 
 /* Self-test of the bounded waits (failure detection; the pages have no
  * counterpart).  One CTA waits on an mbarrier that nothing arrives at,

@@ -287,6 +287,127 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   return from_cuda(e);
 }
 
+// ------------------------------------------------------------------ paged
+
+}  // extern "C"
+
+namespace {
+
+inline bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+oscar_status check_paged(const oscar_paged_cache* c) {
+  if (!c) return OSCAR_ERR_INVALID_ARG;
+  if (c->B <= 0 || c->Hkv <= 0 || c->max_blocks <= 0 || c->n_pages <= 0)
+    return OSCAR_ERR_INVALID_ARG;
+  const void* p16[] = {c->pages, c->k_res, c->v_res, c->k_res_norm};
+  for (const void* p : p16) {
+    if (!p) return OSCAR_ERR_INVALID_ARG;
+    if (!al16(p)) return OSCAR_ERR_ALIGNMENT;
+  }
+  const void* p4[] = {c->block_table, c->n_packed, c->n_res};
+  for (const void* p : p4) {
+    if (!p) return OSCAR_ERR_INVALID_ARG;
+    if (!al4(p)) return OSCAR_ERR_ALIGNMENT;
+  }
+  if (c->flags & ~3u) return OSCAR_ERR_INVALID_ARG;
+  return OSCAR_OK;
+}
+
+PagedArgs paged_args(const oscar_paged_cache* c) {
+  PagedArgs p;
+  p.pages = c->pages;
+  p.block_table = c->block_table;
+  p.seq_packed = c->n_packed;
+  p.seq_res = c->n_res;
+  p.k_res = c->k_res;
+  p.v_res = c->v_res;
+  p.k_res_norm = reinterpret_cast<__half*>(c->k_res_norm);
+  p.status = status_ptr();
+  p.B = c->B;
+  p.Hkv = c->Hkv;
+  p.max_blocks = c->max_blocks;
+  p.n_pages = c->n_pages;
+  p.flags = c->flags;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+oscar_status oscar_paged_prefill_kv(oscar_paged_cache* c, const oscar_bf16* k,
+                                    const oscar_bf16* v, int in_T, const int32_t* n_tok,
+                                    int max_tok, void* stream) {
+  oscar_status st = check_paged(c);
+  if (st != OSCAR_OK) return st;
+  if (!k || !v || !n_tok) return OSCAR_ERR_INVALID_ARG;
+  if (!al16(k) || !al16(v) || !al4(n_tok)) return OSCAR_ERR_ALIGNMENT;
+  if (max_tok < kG || max_tok % kG != 0 || in_T < max_tok) return OSCAR_ERR_INVALID_ARG;
+  if (max_tok / kG > c->max_blocks) return OSCAR_ERR_CAPACITY;
+  const PagedArgs p = paged_args(c);
+  if (!p.status) return OSCAR_ERR_CUDA;
+  cudaError_t e = launch_paged_prefill(p, k, v, in_T, n_tok, max_tok, as_stream(stream));
+  g_launches += 2;
+  return from_cuda(e);
+}
+
+oscar_status oscar_paged_append_kv(oscar_paged_cache* c, const oscar_bf16* k_new,
+                                   const oscar_bf16* v_new, const int32_t* active, void* stream) {
+  oscar_status st = check_paged(c);
+  if (st != OSCAR_OK) return st;
+  if (!k_new || !v_new) return OSCAR_ERR_INVALID_ARG;
+  if (!al16(k_new) || !al16(v_new) || (active && !al4(active))) return OSCAR_ERR_ALIGNMENT;
+  const PagedArgs p = paged_args(c);
+  if (!p.status) return OSCAR_ERR_CUDA;
+  cudaError_t e = launch_paged_append(p, k_new, v_new, active, as_stream(stream));
+  g_launches += 3;
+  return from_cuda(e);
+}
+
+oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const float* q_rot, int Hq,
+                                          float softmax_scale, int max_packed, float* out,
+                                          int num_splits, void* workspace, size_t ws_bytes,
+                                          void* stream) {
+  oscar_status st = check_paged(c);
+  if (st != OSCAR_OK) return st;
+  if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
+      !std::isfinite(softmax_scale) || max_packed < 0 || max_packed % kG != 0 ||
+      max_packed / kG > c->max_blocks)
+    return OSCAR_ERR_INVALID_ARG;
+  if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
+  if (!al16(q_rot) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
+  int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, max_packed);
+  if (!workspace || ws_bytes < ws_bytes_for(c->B, Hq, S + 1)) return OSCAR_ERR_WORKSPACE;
+  if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;
+  DecodeArgs a;
+  a.packed = c->pages;
+  a.k_res = c->k_res;
+  a.v_res = c->v_res;
+  a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
+  a.q_rot = q_rot;
+  a.ws = static_cast<float*>(workspace);
+  a.out = out;
+  a.status = status_ptr();
+  if (!a.status) return OSCAR_ERR_CUDA;
+  a.B = c->B;
+  a.Hkv = c->Hkv;
+  a.Hq = Hq;
+  a.T_cap = 0;
+  a.n_packed = 0;
+  a.n_res = 0;
+  a.num_splits = S;
+  a.flags = c->flags;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.block_table = c->block_table;
+  a.seq_packed = c->n_packed;
+  a.seq_res = c->n_res;
+  a.max_blocks = c->max_blocks;
+  a.n_pages = c->n_pages;
+  cudaError_t e = launch_decode_int2(a, as_stream(stream));
+  g_launches += 2;
+  return from_cuda(e);
+}
+
 oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* K,
                                          const oscar_bf16* V, int B, int Hq, int Hkv, int T,
                                          int T_stride, float softmax_scale, float* out,

@@ -27,6 +27,7 @@ __host__ __device__ constexpr int tok_slot(int t) { return 4 * (t & 7) + (t >> 3
 enum : unsigned {
   kDevErrWaitTimeout = 1u,   // an mbarrier wait hit its iteration limit
   kDevErrDrainTimeout = 2u,  // copies still in flight after the drain limit
+  kDevErrBadPaged = 4u,      // a page id or a per-sequence length out of range
 };
 
 // Iteration limits of the bounded spin-waits.  One try_wait may itself

@@ -145,12 +145,34 @@ __device__ __forceinline__ float warp_allsum(float v) {
 // One warp's contiguous range of a row's 32-token blocks, streamed through
 // the warp's own NSTAGE-deep ring: lane 0 copies block i's record into slot
 // i % NSTAGE with one 1-D bulk copy completing on that slot's mbarrier.
+template <bool PAGED>
 struct WarpRing {
   uint8_t* ring;
   uint64_t* bars;
-  const uint8_t* src;   // record of the range's first block
+  const uint8_t* src;   // record of the range's first block (contiguous cache)
   int n;                // blocks in the range
   int lane;
+  // paged cache: the range's block-table entries, the page pool, the row's
+  // KV head, and where to report a page id out of range
+  const int32_t* tab;
+  const uint8_t* pages;
+  int Hkv, h, n_pages;
+  unsigned* status;
+
+  // Record of block i of the range.  A page id out of range is reported and
+  // replaced by page 0 (the result is void; nothing outside the pool is read).
+  __device__ __forceinline__ const uint8_t* record(int i) const {
+    if constexpr (PAGED) {
+      int page = __ldg(tab + i);
+      if (page < 0 || page >= n_pages) {
+        record_error(status, kDevErrBadPaged);
+        page = 0;
+      }
+      return pages + ((long long)page * Hkv + h) * kBlkBytes;
+    } else {
+      return src + (long long)i * kBlkBytes;
+    }
+  }
 
   __device__ __forceinline__ void start() const {
     if (lane == 0) {
@@ -164,8 +186,9 @@ struct WarpRing {
   __device__ __forceinline__ void issue(int i) const {
     if (lane == 0) {
       uint64_t* bar = &bars[i % NSTAGE];
+      const uint8_t* rec = record(i);
       mbar_arrive_expect_tx(bar, kBlkBytes);
-      bulk_g2s(ring + (i % NSTAGE) * kBlkBytes, src + (long long)i * kBlkBytes, kBlkBytes, bar);
+      bulk_g2s(ring + (i % NSTAGE) * kBlkBytes, rec, kBlkBytes, bar);
     }
   }
   // true on every lane once block i has landed; false if the wait gave up
@@ -195,20 +218,44 @@ struct WarpRing {
   }
 };
 
-__device__ __forceinline__ WarpRing make_ring(const DecodeArgs& a, uint8_t* smem, long long row,
-                                              int split) {
+// Blocks of row (b, h): the cache's n_packed, or for a paged cache the
+// sequence's own length (checked: a bad length is reported and gives none).
+template <bool PAGED>
+__device__ __forceinline__ int row_blocks(const DecodeArgs& a, int b) {
+  if constexpr (PAGED) {
+    const int n = __ldg(a.seq_packed + b);
+    if (n < 0 || n % kG != 0 || n / kG > a.max_blocks) {
+      record_error(a.status, kDevErrBadPaged);
+      return 0;
+    }
+    return n / kG;
+  } else {
+    return a.n_packed / kG;
+  }
+}
+
+template <bool PAGED>
+__device__ __forceinline__ WarpRing<PAGED> make_ring(const DecodeArgs& a, uint8_t* smem, int b,
+                                                     int h, int split) {
   const int warp = threadIdx.x >> 5;
-  const int nblk = a.n_packed / kG;
+  const int nblk = row_blocks<PAGED>(a, b);
   const int b0 = (int)((long long)nblk * split / a.num_splits);
   const int b1 = (int)((long long)nblk * (split + 1) / a.num_splits);
   const int wb0 = b0 + (int)((long long)(b1 - b0) * warp / NW);
   const int wb1 = b0 + (int)((long long)(b1 - b0) * (warp + 1) / NW);
-  WarpRing r;
+  const long long row = (long long)b * a.Hkv + h;
+  WarpRing<PAGED> r;
   r.ring = smem + warp * NSTAGE * kBlkBytes;
   r.bars = reinterpret_cast<uint64_t*>(smem + NW * NSTAGE * kBlkBytes) + warp * NSTAGE;
   r.src = a.packed + (row * (long long)(a.T_cap / kG) + wb0) * kBlkBytes;
   r.n = wb1 - wb0;
   r.lane = threadIdx.x & 31;
+  r.tab = PAGED ? a.block_table + (long long)b * a.max_blocks + wb0 : nullptr;
+  r.pages = a.packed;
+  r.Hkv = a.Hkv;
+  r.h = h;
+  r.n_pages = a.n_pages;
+  r.status = a.status;
   return r;
 }
 
@@ -255,8 +302,8 @@ __device__ __forceinline__ float scale_query(float (&qf)[32], const float* qrow,
 //  * scores, softmax and outputs: head tig mod GQ (columns 2 tig, 2 tig + 1
 //    are its hi and lo limbs), tokens gid + 8 j, j = 0..3;
 //  * P.V: channels on M as in the row layout, (head, limb of p~) on N.
-template <int GQ>
-__device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing& R,
+template <int GQ, class Ring>
+__device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
                                             MergeSmem<GQ, NW>& E, long long qrow0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -482,8 +529,8 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const WarpRing&
 //    gid; B operand: key codes of token 8 nt + gid, n-tiles nt = 0..3;
 //  * scores and softmax: head gid, tokens 8 nt + 2 tig and + 1;
 //  * P.V: channels on M, the 8 heads on N, one n-tile per limb of p~.
-template <int GQ>
-__device__ __forceinline__ void packed_rows(const DecodeArgs& a, const WarpRing& R,
+template <int GQ, class Ring>
+__device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
                                             MergeSmem<GQ, NW>& E, long long qrow0) {
   static_assert(GQ == 8, "the row layout serves groups of 8 query heads");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -720,10 +767,18 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const WarpRing&
 }
 
 // --------------------------------------------------------------- residual
-template <int GQ>
+template <int GQ, bool PAGED>
 __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ, NW>& E,
-                                               long long row, long long qrow0) {
+                                               long long row, long long qrow0, int b) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int n_res = a.n_res;
+  if constexpr (PAGED) {
+    n_res = __ldg(a.seq_res + b);
+    if (n_res < 0 || n_res > kR) {
+      if (threadIdx.x == 0) record_error(a.status, kDevErrBadPaged);
+      n_res = 0;
+    }
+  }
   // Unit-norm bf16 keys times their fp16 norms, bf16 values; CUDA cores.
   float qv[GQ][4], mr[GQ], lr[GQ], orr[GQ][4];
 #pragma unroll
@@ -733,7 +788,7 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
     mr[j] = -INFINITY; lr[j] = 0.0f;
     orr[j][0] = orr[j][1] = orr[j][2] = orr[j][3] = 0.0f;
   }
-  for (int t = warp; t < a.n_res; t += NW) {
+  for (int t = warp; t < n_res; t += NW) {
     const long long tok = row * kR + t;
     const uint2 kr = reinterpret_cast<const uint2*>(a.k_res + tok * kD)[lane];
     const uint2 vr = reinterpret_cast<const uint2*>(a.v_res + tok * kD)[lane];
@@ -770,7 +825,7 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
 }
 
 // Up to 4 CTAs per SM in the column layout (128 registers), 3 in the row layout.
-template <int GQ>
+template <int GQ, bool PAGED>
 __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
@@ -780,14 +835,14 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
   const long long qrow0 = (long long)b * a.Hq + (long long)h * GQ;  // first query head
 
   if (split < a.num_splits) {
-    const WarpRing R = make_ring(a, smem, row, split);
+    const WarpRing<PAGED> R = make_ring<PAGED>(a, smem, b, h, split);
     if constexpr (GQ <= 4) {
       packed_cols<GQ>(a, R, E, qrow0);
     } else {
       packed_rows<GQ>(a, R, E, qrow0);
     }
   } else {
-    residual_split<GQ>(a, E, row, qrow0);
+    residual_split<GQ, PAGED>(a, E, row, qrow0, b);
   }
   __syncthreads();
   cta_merge_write<GQ, NW>(E, a.ws + (qrow0 * (a.num_splits + 1) + split) * kRecFloats,
@@ -796,35 +851,46 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
 
 // Opt in to kSmemBytes of dynamic shared memory (needed above 48 KB), once
 // per instantiation and device.
-template <int GQ>
+template <int GQ, bool PAGED>
 cudaError_t allow_smem() {
   static int done[128] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_int2_kernel<GQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
+  e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 128) done[dev] = 1;
   return e;
 }
 
-template <int GQ>
+template <int GQ, bool PAGED>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e0 = allow_smem<GQ>();
+  cudaError_t e0 = allow_smem<GQ, PAGED>();
   if (e0 != cudaSuccess) return e0;
   dim3 grid(a.num_splits + 1, a.Hkv, a.B);
-  decode_int2_kernel<GQ><<<grid, NW * 32, kSmemBytes, s>>>(a);
+  decode_int2_kernel<GQ, PAGED><<<grid, NW * 32, kSmemBytes, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_combine(a.ws, a.out, a.B * a.Hq, a.num_splits + 1, s);
 }
 
+template <bool PAGED>
+cudaError_t launch_p(const DecodeArgs& a, cudaStream_t s) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_g<1, PAGED>(a, s);
+    case 2: return launch_g<2, PAGED>(a, s);
+    case 4: return launch_g<4, PAGED>(a, s);
+    case 8: return launch_g<8, PAGED>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <int GQ>
 int occupancy_g() {
-  if (allow_smem<GQ>() != cudaSuccess) return 0;
+  if (allow_smem<GQ, false>() != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ>, NW * 32,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ, false>, NW * 32,
                                                     kSmemBytes) != cudaSuccess)
     return 0;
   return n;
@@ -833,13 +899,7 @@ int occupancy_g() {
 }  // namespace
 
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t s) {
-  switch (a.Hq / a.Hkv) {
-    case 1: return launch_g<1>(a, s);
-    case 2: return launch_g<2>(a, s);
-    case 4: return launch_g<4>(a, s);
-    case 8: return launch_g<8>(a, s);
-    default: return cudaErrorInvalidValue;
-  }
+  return a.block_table ? launch_p<true>(a, s) : launch_p<false>(a, s);
 }
 
 int decode_int2_ctas_per_sm(int g) {

@@ -34,6 +34,13 @@ struct DecodeArgs {
   int B, Hkv, Hq, T_cap, n_packed, n_res, num_splits;
   unsigned flags;
   float scale_log2;   // softmax_scale * log2(e)
+  // paged cache (block_table != nullptr): records at packed + (page*Hkv + h)
+  // * block bytes, page = block_table[b*max_blocks + block]; per-sequence
+  // lengths seq_packed[b], seq_res[b] replace n_packed, n_res
+  const int32_t* block_table = nullptr;
+  const int32_t* seq_packed = nullptr;
+  const int32_t* seq_res = nullptr;
+  int max_blocks = 0, n_pages = 0;
 };
 
 // Floats per split-K partial record: m, l, 2 pad, o[128].
@@ -61,6 +68,26 @@ int decode_bf16_ctas_per_sm(int g);
 // and the host launch counter behind oscar_kernel_launches().
 unsigned* device_status_word();
 void count_launches(int n);
+
+// Paged cache: fused prefill of n_tok[b] tokens per sequence (then n_packed
+// += n_tok), flush of full residual windows, residual append of one token,
+// and the length updates of an append.
+struct PagedArgs {
+  uint8_t* pages;
+  int32_t* block_table;
+  int32_t* seq_packed;
+  int32_t* seq_res;
+  uint16_t* k_res;
+  uint16_t* v_res;
+  __half* k_res_norm;
+  unsigned* status;
+  int B, Hkv, max_blocks, n_pages;
+  unsigned flags;
+};
+cudaError_t launch_paged_prefill(const PagedArgs& p, const uint16_t* k, const uint16_t* v,
+                                 int in_T, const int32_t* n_tok, int max_tok, cudaStream_t s);
+cudaError_t launch_paged_append(const PagedArgs& p, const uint16_t* k_new, const uint16_t* v_new,
+                                const int32_t* active, cudaStream_t s);
 
 // Fused rotate + scale + quantise of n_tok tokens of raw keys and values.
 cudaError_t launch_prefill_kv(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,

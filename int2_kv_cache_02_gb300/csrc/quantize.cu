@@ -89,6 +89,138 @@ __global__ void __launch_bounds__(128) prefill_kv_kernel(
   quantize_block(kt, vt, kc, vc, ns, packed + (row * (T_cap / kG) + pblk) * kBlkBytes);
 }
 
+// ------------------------------------------------------------------ paged
+// Record of logical block lb of sequence b, head h, in the page pool; an
+// unmapped block (or a page id out of range) is reported and yields nullptr.
+__device__ __forceinline__ uint8_t* paged_record(const PagedArgs& p, int b, int lb, int h) {
+  if (lb < 0 || lb >= p.max_blocks) return nullptr;
+  const int page = p.block_table[(long long)b * p.max_blocks + lb];
+  if (page < 0 || page >= p.n_pages) return nullptr;
+  return p.pages + ((long long)page * p.Hkv + h) * kBlkBytes;
+}
+
+// Fused prefill into pages: CTA (j, h, b) handles tokens 32j..32j+31 of
+// sequence b when 32j < n_tok[b]; they become logical block
+// seq_packed[b]/32 + j.  Lengths are updated by paged_lengths_kernel after.
+__global__ void __launch_bounds__(128) paged_prefill_kernel(PagedArgs p,
+                                                            const uint16_t* __restrict__ k,
+                                                            const uint16_t* __restrict__ v,
+                                                            int in_T, const int32_t* n_tok,
+                                                            int max_tok) {
+  __shared__ __align__(16) uint16_t kt[kG][kD];
+  __shared__ __align__(16) uint16_t vt[kG][kD];
+  __shared__ __align__(16) uint8_t kc[kG][kD];
+  __shared__ __align__(16) uint8_t vc[kG][kD];
+  __shared__ __half ns[kG];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int n = n_tok[b], p0 = p.seq_packed[b];
+  if (n == 0) return;
+  if (n < 0 || n % kG != 0 || n > max_tok || p0 < 0 || p0 % kG != 0 || p.seq_res[b] != 0) {
+    if (j == 0 && h == 0 && tid == 0) record_error(p.status, kDevErrBadPaged);
+    return;
+  }
+  if (kG * j >= n) return;
+  uint8_t* rec = paged_record(p, b, p0 / kG + j, h);
+  if (rec == nullptr) {
+    if (tid == 0) record_error(p.status, kDevErrBadPaged);
+    return;
+  }
+  const long long src_tok = ((long long)b * p.Hkv + h) * in_T + (long long)j * kG;
+  {
+    const uint4* vs = reinterpret_cast<const uint4*>(v + src_tok * kD);
+    uint4* vd = reinterpret_cast<uint4*>(&vt[0][0]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vd[tid + 128 * i] = vs[tid + 128 * i];
+  }
+#pragma unroll 2
+  for (int i = 0; i < 8; ++i) {
+    const int t = 8 * warp + i;
+    const uint2 raw = reinterpret_cast<const uint2*>(k + (src_tok + t) * kD)[lane];
+    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+    const float norm = rotate_scale_key(x, lane, p.flags);
+    reinterpret_cast<uint2*>(&kt[t][0])[lane] = pack_bf16x4(x);
+    if (lane == 0) ns[t] = __float2half_rn(norm);
+  }
+  __syncthreads();
+  quantize_block(kt, vt, kc, vc, ns, rec);
+}
+
+// Flush of full residual windows: CTA (j, h, b) quantises residual tokens
+// 32j..32j+31 of (b, h) into logical block seq_packed[b]/32 + j when sequence
+// b is active and its window is full.
+__global__ void __launch_bounds__(128) paged_flush_kernel(PagedArgs p, const int32_t* active) {
+  __shared__ __align__(16) uint16_t kt[kG][kD];
+  __shared__ __align__(16) uint16_t vt[kG][kD];
+  __shared__ __align__(16) uint8_t kc[kG][kD];
+  __shared__ __align__(16) uint8_t vc[kG][kD];
+  const int tid = threadIdx.x;
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (active && active[b] == 0) return;
+  if (p.seq_res[b] != kR) return;
+  const int p0 = p.seq_packed[b];
+  uint8_t* rec = (p0 >= 0 && p0 % kG == 0) ? paged_record(p, b, p0 / kG + j, h) : nullptr;
+  if (rec == nullptr) {
+    if (tid == 0) record_error(p.status, kDevErrBadPaged);
+    return;
+  }
+  const long long row = (long long)b * p.Hkv + h;
+  const long long src_tok = row * kR + (long long)j * kG;
+  {
+    const uint4* ks = reinterpret_cast<const uint4*>(p.k_res + src_tok * kD);
+    const uint4* vs = reinterpret_cast<const uint4*>(p.v_res + src_tok * kD);
+    uint4* kd = reinterpret_cast<uint4*>(&kt[0][0]);
+    uint4* vd = reinterpret_cast<uint4*>(&vt[0][0]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      kd[tid + 128 * i] = ks[tid + 128 * i];
+      vd[tid + 128 * i] = vs[tid + 128 * i];
+    }
+  }
+  __syncthreads();
+  quantize_block(kt, vt, kc, vc, p.k_res_norm + src_tok, rec);
+}
+
+// Length updates after a paged prefill (n_tok != nullptr) or append.
+__global__ void paged_lengths_kernel(PagedArgs p, const int32_t* n_tok, int max_tok,
+                                     const int32_t* active) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= p.B) return;
+  if (n_tok) {
+    const int n = n_tok[b];
+    if (n > 0 && n % kG == 0 && n <= max_tok && p.seq_res[b] == 0) p.seq_packed[b] += n;
+    return;
+  }
+  if (active && active[b] == 0) return;
+  if (p.seq_res[b] == kR) {
+    p.seq_packed[b] += kR;
+    p.seq_res[b] = 1;
+  } else {
+    p.seq_res[b] += 1;
+  }
+}
+
+cudaError_t launch_paged_prefill(const PagedArgs& p, const uint16_t* k, const uint16_t* v,
+                                 int in_T, const int32_t* n_tok, int max_tok, cudaStream_t s) {
+  dim3 grid(max_tok / kG, p.Hkv, p.B);
+  paged_prefill_kernel<<<grid, 128, 0, s>>>(p, k, v, in_T, n_tok, max_tok);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  paged_lengths_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p, n_tok, max_tok, nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_paged_flush(const PagedArgs& p, const int32_t* active, cudaStream_t s) {
+  dim3 grid(kR / kG, p.Hkv, p.B);
+  paged_flush_kernel<<<grid, 128, 0, s>>>(p, active);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_paged_lengths(const PagedArgs& p, const int32_t* active, cudaStream_t s) {
+  paged_lengths_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p, nullptr, 0, active);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_kv(const uint16_t* k_hat, const __half* k_norm, const uint16_t* v,
                                int src_T, int n_tok, int B, int Hkv, int T_cap, int p0,
                                uint8_t* packed, cudaStream_t s) {

@@ -56,6 +56,48 @@ __global__ void __launch_bounds__(256) rotate_scale_k_kernel(
   }
 }
 
+// Paged residual append: one warp per (b, h) of an active sequence writes
+// its new token at residual slot n_res[b] (slot 0 after a flush of a full
+// window, which paged_flush_kernel has done before this launch).
+__global__ void __launch_bounds__(256) paged_append_kernel(PagedArgs p,
+                                                           const uint16_t* __restrict__ k_new,
+                                                           const uint16_t* __restrict__ v_new,
+                                                           const int32_t* active) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= (long long)p.B * p.Hkv) return;
+  const int b = (int)(row / p.Hkv);
+  if (active && active[b] == 0) return;
+  const int r = p.seq_res[b];
+  if (r < 0 || r > kR) {
+    if (lane == 0) record_error(p.status, kDevErrBadPaged);
+    return;
+  }
+  const int slot = (r == kR) ? 0 : r;
+  const long long dst = row * kR + slot;
+  const uint2 raw = reinterpret_cast<const uint2*>(k_new + row * kD)[lane];
+  float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+  const float norm = rotate_scale_key(x, lane, p.flags);
+  reinterpret_cast<uint2*>(p.k_res + dst * kD)[lane] = pack_bf16x4(x);
+  if (lane == 0) p.k_res_norm[dst] = __float2half_rn(norm);
+  reinterpret_cast<uint2*>(p.v_res + dst * kD)[lane] =
+      reinterpret_cast<const uint2*>(v_new + row * kD)[lane];
+}
+
+cudaError_t launch_paged_flush(const PagedArgs& p, const int32_t* active, cudaStream_t s);
+cudaError_t launch_paged_lengths(const PagedArgs& p, const int32_t* active, cudaStream_t s);
+
+cudaError_t launch_paged_append(const PagedArgs& p, const uint16_t* k_new, const uint16_t* v_new,
+                                const int32_t* active, cudaStream_t s) {
+  cudaError_t e = launch_paged_flush(p, active, s);
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)p.B * p.Hkv;
+  paged_append_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p, k_new, v_new, active);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_paged_lengths(p, active, s);
+}
+
 cudaError_t launch_rotate_q(const uint16_t* q, float* out, int n_vec, unsigned flags,
                             cudaStream_t s) {
   const int grid = (n_vec + 7) / 8;

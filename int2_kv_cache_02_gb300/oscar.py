@@ -38,6 +38,14 @@ class OscarCacheStruct(ctypes.Structure):
                 ("n_packed", c_int), ("n_res", c_int), ("flags", c_uint)]
 
 
+class OscarPagedCacheStruct(ctypes.Structure):
+    _fields_ = [("B", c_int), ("Hkv", c_int), ("max_blocks", c_int), ("n_pages", c_int),
+                ("pages", c_void_p), ("block_table", c_void_p),
+                ("n_packed", c_void_p), ("n_res", c_void_p),
+                ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
+                ("flags", c_uint)]
+
+
 BLOCK_BYTES = 2752
 # byte ranges of the fields of one 32-token block record (include/oscar.h)
 RECORD_FIELDS = {"k_codes": (0, 1024), "v_codes": (1024, 2048), "k_scale": (2048, 2304),
@@ -52,6 +60,7 @@ def _load() -> ctypes.CDLL:
         raise ImportError(f"liboscar.so is not built ({path}); run __graft_entry__.build()")
     lib = ctypes.CDLL(path)
     P = POINTER(OscarCacheStruct)
+    PP = POINTER(OscarPagedCacheStruct)
     sig = {
         "oscar_rotate_q": (c_int, [c_void_p, c_void_p, c_int, c_int, c_uint, c_void_p]),
         "oscar_rotate_scale_k": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int,
@@ -59,6 +68,11 @@ def _load() -> ctypes.CDLL:
         "oscar_quantize_kv": (c_int, [P, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p]),
         "oscar_append_kv": (c_int, [P, c_void_p, c_void_p, c_int, c_void_p]),
         "oscar_prefill_kv": (c_int, [P, c_void_p, c_void_p, c_int, c_int, c_void_p]),
+        "oscar_paged_prefill_kv": (c_int, [PP, c_void_p, c_void_p, c_int, c_void_p, c_int,
+                                           c_void_p]),
+        "oscar_paged_append_kv": (c_int, [PP, c_void_p, c_void_p, c_void_p, c_void_p]),
+        "oscar_paged_decode_attention": (c_int, [PP, c_void_p, c_int, c_float, c_int, c_void_p,
+                                                 c_int, c_void_p, c_size_t, c_void_p]),
         "oscar_decode_attention": (c_int, [P, c_void_p, c_int, c_float, c_void_p, c_int,
                                            c_void_p, c_size_t, c_void_p]),
         "oscar_decode_attention_static_ws": (c_int, [P, c_void_p, c_int, c_float, c_void_p,
@@ -173,6 +187,72 @@ class KVCache:
                    for n in ("packed", "k_res", "v_res", "k_res_norm"))
 
 
+class PagedKVCache:
+    """Caller-owned device buffers of a paged cache (oscar_paged_cache):
+    a pool of n_pages pages (each one 2752-byte record per KV head for 32
+    tokens), the block table [B][max_blocks] (page ids, -1 = unmapped),
+    per-sequence lengths n_packed[B], n_res[B] on the device, and the
+    per-(b, h) residual windows.  Pages are handed out by the host-side
+    allocator below; the device kernels only follow the table."""
+
+    def __init__(self, B: int, Hkv: int, max_blocks: int, n_pages: int, flags: int = 0,
+                 device=None):
+        dev = torch.device(device if device is not None else "cuda")
+        self.pages = torch.zeros((n_pages, Hkv, BLOCK_BYTES), dtype=torch.uint8, device=dev)
+        self.block_table = torch.full((B, max_blocks), -1, dtype=torch.int32, device=dev)
+        self.n_packed_d = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.n_res_d = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.k_res = torch.zeros((B, Hkv, R, D), dtype=torch.bfloat16, device=dev)
+        self.v_res = torch.zeros((B, Hkv, R, D), dtype=torch.bfloat16, device=dev)
+        self.k_res_norm = torch.zeros((B, Hkv, R), dtype=torch.float16, device=dev)
+        s = OscarPagedCacheStruct()
+        s.B, s.Hkv, s.max_blocks, s.n_pages, s.flags = B, Hkv, max_blocks, n_pages, flags
+        s.pages = self.pages.data_ptr()
+        s.block_table = self.block_table.data_ptr()
+        s.n_packed = self.n_packed_d.data_ptr()
+        s.n_res = self.n_res_d.data_ptr()
+        for name in ("k_res", "v_res", "k_res_norm"):
+            setattr(s, name, getattr(self, name).data_ptr())
+        self.struct = s
+        self._free = list(range(n_pages))
+        self._table_host = [[-1] * max_blocks for _ in range(B)]
+
+    B = property(lambda self: self.struct.B)
+    Hkv = property(lambda self: self.struct.Hkv)
+    max_blocks = property(lambda self: self.struct.max_blocks)
+    n_pages = property(lambda self: self.struct.n_pages)
+    flags = property(lambda self: self.struct.flags)
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+    def map_blocks(self, b: int, n_blocks: int, order=None):
+        """Gives sequence b pages for its logical blocks 0..n_blocks-1 (those
+        not mapped yet), taking free pages in `order` (a permutation of page
+        ids, for tests) or in pool order."""
+        if order is not None:
+            free = set(self._free)
+            self._free = [p for p in order if p in free]
+        row = self._table_host[b]
+        for j in range(n_blocks):
+            if row[j] < 0:
+                if not self._free:
+                    raise OscarError(4, "PagedKVCache.map_blocks: page pool exhausted")
+                row[j] = self._free.pop(0)
+        self.block_table[b].copy_(torch.tensor(row, dtype=torch.int32))
+
+    def page_of(self, b: int, block: int) -> int:
+        return self._table_host[b][block]
+
+    def record(self, b: int, h: int, block: int) -> torch.Tensor:
+        """View of the 2752-byte record of (b, h, logical block)."""
+        return self.pages[self.page_of(b, block), h]
+
+    def lengths(self):
+        """(n_packed, n_res) per sequence, read back from the device."""
+        return self.n_packed_d.cpu().tolist(), self.n_res_d.cpu().tolist()
+
+
 # ---------------------------------------------------------------------------
 # the calls (same names as the C ABI, without the oscar_ prefix)
 # ---------------------------------------------------------------------------
@@ -198,6 +278,31 @@ def prefill_kv(cache: KVCache, k: torch.Tensor, v: torch.Tensor, n_tok: int, in_
     in_T = in_T or k.shape[2]
     _check(_lib.oscar_prefill_kv(cache.ref(), _ptr(k), _ptr(v), in_T, n_tok, _stream(stream)),
            "oscar_prefill_kv")
+
+
+def paged_prefill_kv(cache: PagedKVCache, k: torch.Tensor, v: torch.Tensor,
+                     n_tok: torch.Tensor, max_tok: int, in_T: int = 0, stream=None):
+    """Fused prefill of sequence b's tokens [0, n_tok[b]) (device int32 [B],
+    multiples of 32, <= max_tok) into its next logical blocks."""
+    in_T = in_T or k.shape[2]
+    _check(_lib.oscar_paged_prefill_kv(cache.ref(), _ptr(k), _ptr(v), in_T, _ptr(n_tok),
+                                       max_tok, _stream(stream)), "oscar_paged_prefill_kv")
+
+
+def paged_append_kv(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                    active: torch.Tensor | None = None, stream=None):
+    """One new token [B][Hkv][128] for every sequence with active[b] != 0."""
+    _check(_lib.oscar_paged_append_kv(cache.ref(), _ptr(k_new), _ptr(v_new), _ptr(active),
+                                      _stream(stream)), "oscar_paged_append_kv")
+
+
+def paged_decode_attention(cache: PagedKVCache, q_rot: torch.Tensor, Hq: int,
+                           softmax_scale: float, max_packed: int, out: torch.Tensor,
+                           workspace: torch.Tensor, num_splits: int = 0, stream=None):
+    _check(_lib.oscar_paged_decode_attention(cache.ref(), _ptr(q_rot), Hq, softmax_scale,
+                                             max_packed, _ptr(out), num_splits, _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(),
+                                             _stream(stream)), "oscar_paged_decode_attention")
 
 
 def quantize_kv(cache: KVCache, k_hat=None, k_norm=None, v=None, src_T: int = 0,

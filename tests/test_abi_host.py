@@ -40,7 +40,8 @@ def test_headers_declare_the_documented_calls():
                  "oscar_append_kv", "oscar_decode_attention", "oscar_bf16_decode_attention",
                  "oscar_decode_workspace_bytes", "oscar_decode_num_splits",
                  "oscar_device_status", "oscar_status_string", "oscar_kernel_launches",
-                 "oscar_selftest_wait_timeout", "oscar_prefill_kv"]:
+                 "oscar_selftest_wait_timeout", "oscar_prefill_kv", "oscar_paged_prefill_kv",
+                 "oscar_paged_append_kv", "oscar_paged_decode_attention"]:
         assert want in names
     assert _declared("oscar_synth.h") == ["oscar_synth_bf16"]
 
@@ -131,6 +132,39 @@ def test_prefill_validation():
     c2 = _cache(n_res=5)
     assert L.oscar_prefill_kv(ctypes.byref(c2), P(FAKE), P(FAKE), 64, 64, None) == 1
     assert c.n_packed == 0 and c2.n_packed == 0
+
+
+def _paged(**kw):
+    from int2_kv_cache_02_gb300.oscar import OscarPagedCacheStruct
+    s = OscarPagedCacheStruct()
+    s.B, s.Hkv = kw.get("B", 2), kw.get("Hkv", 2)
+    s.max_blocks, s.n_pages = kw.get("max_blocks", 8), kw.get("n_pages", 16)
+    for i, name in enumerate(["pages", "block_table", "n_packed", "n_res", "k_res", "v_res",
+                              "k_res_norm"]):
+        setattr(s, name, kw.get(name, FAKE + 0x100000 * i))
+    s.flags = kw.get("flags", 0)
+    return s
+
+
+@no_gpu_only
+def test_paged_validation():
+    from int2_kv_cache_02_gb300 import oscar as O
+    L = O.library()
+    P = ctypes.c_void_p
+    bad = _paged(n_pages=0)
+    assert L.oscar_paged_append_kv(ctypes.byref(bad), P(FAKE), P(FAKE), None, None) == 1
+    mis = _paged(pages=FAKE + 8)
+    assert L.oscar_paged_append_kv(ctypes.byref(mis), P(FAKE), P(FAKE), None, None) == 3
+    c = _paged()
+    assert L.oscar_paged_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 64, P(FAKE), 48, None) == 1
+    assert L.oscar_paged_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 512, P(FAKE), 512,
+                                    None) == 4          # more blocks than a table row
+    assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 6, 0.1, 64, P(FAKE), 0,
+                                          P(FAKE), 1 << 20, None) == 2
+    assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, 33, P(FAKE), 0,
+                                          P(FAKE), 1 << 20, None) == 1
+    assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, 64, P(FAKE), 2,
+                                          P(FAKE), 10, None) == 5
 
 
 @no_gpu_only
