@@ -393,7 +393,7 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
   a.Hkv = c->Hkv;
   a.Hq = Hq;
   a.T_cap = 0;
-  a.n_packed = 0;
+  a.n_packed = max_packed;  // sizes the equal chunks of the splits
   a.n_res = 0;
   a.num_splits = S;
   a.flags = c->flags;

@@ -155,8 +155,9 @@ struct WarpRing {
   // paged cache: the range's block-table entries, the page pool, the row's
   // KV head, and where to report a page id out of range
   const int32_t* tab;
-  const uint8_t* pages;
-  int Hkv, h, n_pages;
+  const uint8_t* pages;   // record of head h in page 0
+  long long page_bytes;   // Hkv records
+  int n_pages;
   unsigned* status;
 
   // Record of block i of the range.  A page id out of range is reported and
@@ -164,11 +165,11 @@ struct WarpRing {
   __device__ __forceinline__ const uint8_t* record(int i) const {
     if constexpr (PAGED) {
       int page = __ldg(tab + i);
-      if (page < 0 || page >= n_pages) {
+      if ((unsigned)page >= (unsigned)n_pages) {
         record_error(status, kDevErrBadPaged);
         page = 0;
       }
-      return pages + ((long long)page * Hkv + h) * kBlkBytes;
+      return pages + page * page_bytes;
     } else {
       return src + (long long)i * kBlkBytes;
     }
@@ -239,8 +240,19 @@ __device__ __forceinline__ WarpRing<PAGED> make_ring(const DecodeArgs& a, uint8_
                                                      int h, int split) {
   const int warp = threadIdx.x >> 5;
   const int nblk = row_blocks<PAGED>(a, b);
-  const int b0 = (int)((long long)nblk * split / a.num_splits);
-  const int b1 = (int)((long long)nblk * (split + 1) / a.num_splits);
+  int b0, b1;
+  if constexpr (PAGED) {
+    // Equal chunks sized by the batch's longest sequence (n_packed carries
+    // that bound): a short sequence fills fewer splits, each as long as a
+    // long sequence's, so the per-CTA setup is paid per chunk of work and
+    // not per split.  The last split takes whatever is left.
+    const int per = (a.n_packed / kG + a.num_splits - 1) / a.num_splits;
+    b0 = (int)min((long long)nblk, (long long)split * per);
+    b1 = split == a.num_splits - 1 ? nblk : min(nblk, b0 + per);
+  } else {
+    b0 = (int)((long long)nblk * split / a.num_splits);
+    b1 = (int)((long long)nblk * (split + 1) / a.num_splits);
+  }
   const int wb0 = b0 + (int)((long long)(b1 - b0) * warp / NW);
   const int wb1 = b0 + (int)((long long)(b1 - b0) * (warp + 1) / NW);
   const long long row = (long long)b * a.Hkv + h;
@@ -251,9 +263,8 @@ __device__ __forceinline__ WarpRing<PAGED> make_ring(const DecodeArgs& a, uint8_
   r.n = wb1 - wb0;
   r.lane = threadIdx.x & 31;
   r.tab = PAGED ? a.block_table + (long long)b * a.max_blocks + wb0 : nullptr;
-  r.pages = a.packed;
-  r.Hkv = a.Hkv;
-  r.h = h;
+  r.pages = a.packed + (long long)h * kBlkBytes;
+  r.page_bytes = (long long)a.Hkv * kBlkBytes;
   r.n_pages = a.n_pages;
   r.status = a.status;
   return r;

@@ -36,7 +36,8 @@ struct DecodeArgs {
   float scale_log2;   // softmax_scale * log2(e)
   // paged cache (block_table != nullptr): records at packed + (page*Hkv + h)
   // * block bytes, page = block_table[b*max_blocks + block]; per-sequence
-  // lengths seq_packed[b], seq_res[b] replace n_packed, n_res
+  // lengths seq_packed[b], seq_res[b] replace n_packed, n_res; n_packed
+  // then holds the host bound on the seq_packed[b], which sizes the splits
   const int32_t* block_table = nullptr;
   const int32_t* seq_packed = nullptr;
   const int32_t* seq_res = nullptr;

@@ -50,8 +50,9 @@ def _write_record(rec, kq, vq, norm16, j):
     rec.copy_(torch.from_numpy(np.concatenate(parts)))
 
 
-def test_paged_decode_matches_oracle(L):
-    Hkv, g = 2, 4
+@pytest.mark.parametrize("g", [1, 4, 8])
+def test_paged_decode_matches_oracle(L, g):
+    Hkv = 2
     Hq = Hkv * g
     lens = [(1024 + 40, 1024), (2336 + 128, 2336), (100, 0), (0, 0), (320 + 1, 320)]
     B = len(lens)
