@@ -23,7 +23,9 @@ Sources (page title and section):
 
 Readings where the pages are silent or ambiguous are listed in the design doc; the
 ones that shape arithmetic here are: Sylvester (natural order) Hadamard of size
-128 with entries +-1/sqrt(128); the norm is per (token, KV head); asymmetric
+128 with entries +-1/sqrt(128); the norm is per (token, KV head) unless
+NORM_ALL_HEADS asks for the norm over all heads; keys are scaled to a target
+norm (1 unless given) and the stored norm is n / target; asymmetric
 min-max INT2 with step (max-min)/3, zero = min, round half to even, codes from
 the fp32 parameters before their fp16 rounding; a constant group stores step 0
 and codes 0; a zero key keeps k_hat = 0 and norm 0; flush-before-append.
@@ -40,6 +42,7 @@ G = 32           # key quantisation block (tokens sharing a channel's step/zero)
 R = 128          # residual window
 NO_ROTATE = 1    # ablation: skip Canalized Rotation
 NO_SCALE = 2     # ablation: skip Omni-Token Scaling
+NORM_ALL_HEADS = 4   # norm-scope variant: one norm per token over all KV heads
 
 
 # --------------------------------------------------------------------------
@@ -112,7 +115,7 @@ class RotatedKeys:
     norm_f16: np.ndarray     # float16 [...]
 
 
-def rotate_scale_k(k_bits: np.ndarray, flags: int = 0) -> RotatedKeys:
+def rotate_scale_k(k_bits: np.ndarray, flags: int = 0, target: float = 1.0) -> RotatedKeys:
     """Canalized Rotation then Omni-Token Scaling of raw keys [..., 128].
 
     k' = H k ([notes] Step One, K' = K.H with H symmetric); s = sum k'^2,
@@ -120,18 +123,29 @@ def rotate_scale_k(k_bits: np.ndarray, flags: int = 0) -> RotatedKeys:
     to be multiplied back at dequantisation ([notes] Step Two; [news] 二, the
     norm is stored as a tag and restored at decode).  A zero key keeps
     k_hat = 0 and n = 0.  With NO_SCALE, k_hat = k' and n = 1.
+
+    NORM_ALL_HEADS: k_bits is [Hkv, ..., 128], heads first, and n of a token
+    is the norm of its rotated keys over all heads together ([notes] II,
+    Notation: k_i in R^{H d_h}, n_i = ||k_i||; Step Two: the norm across all
+    heads); every head's key is divided by it and stores it.
+
+    target: the keys are scaled to norm `target` instead of 1 and the stored
+    norm is n / target, so stored norm x k_hat = k' either way (the scaling
+    target that [rainbus] 独立分析的弱点 (1) says an appendix ablates).
     """
     k = bf16_to_f64(k_bits)
     kr = k if flags & NO_ROTATE else k @ _H.T
     if flags & NO_SCALE:
         n = np.ones(kr.shape[:-1])
-        kh = kr
-    else:
-        s = np.sum(kr * kr, axis=-1)
-        n = np.sqrt(s)
-        safe = np.where(n > 0, n, 1.0)
-        kh = np.where((n > 0)[..., None], kr / safe[..., None], 0.0)
-    return RotatedKeys(kh, f64_to_bf16(kh), n, f_to_f16(n))
+        return RotatedKeys(kr, f64_to_bf16(kr), n, f_to_f16(n))
+    s = np.sum(kr * kr, axis=-1)
+    if flags & NORM_ALL_HEADS:
+        s = np.broadcast_to(np.sum(s, axis=0, keepdims=True), s.shape)
+    n = np.sqrt(s)
+    safe = np.where(n > 0, n, 1.0)
+    kh = np.where((n > 0)[..., None], kr * (target / safe)[..., None], 0.0)
+    stored = n / target
+    return RotatedKeys(kh, f64_to_bf16(kh), stored, f_to_f16(stored))
 
 
 # --------------------------------------------------------------------------
@@ -288,6 +302,7 @@ def bf16_attention(q_bits, k_bits, v_bits, tau: float) -> np.ndarray:
 @dataclass
 class HeadCache:
     flags: int = 0
+    target: float = 1.0
     k_codes: list = field(default_factory=list)   # QuantK per quantised chunk
     k_norm16: list = field(default_factory=list)
     v_q: list = field(default_factory=list)
@@ -306,8 +321,13 @@ class HeadCache:
     def quantize_prefix(self, k_raw_bits: np.ndarray, v_bits: np.ndarray):
         """Rotate, scale and quantise a block-aligned run of tokens."""
         assert k_raw_bits.shape[0] % G == 0
-        rk = rotate_scale_k(k_raw_bits, self.flags)
+        rk = self._rotate(k_raw_bits)
         self._pack(rk.k_hat_bf16, rk.norm_f16, v_bits)
+
+    def _rotate(self, k_raw_bits):
+        # a per-head norm; the all-heads norm needs every head (build_row_caches)
+        assert not self.flags & NORM_ALL_HEADS
+        return rotate_scale_k(k_raw_bits, self.flags, self.target)
 
     def _pack(self, k_hat_bits, norm16, v_bits):
         self.k_codes.append(quantize_k(k_hat_bits))
@@ -318,18 +338,25 @@ class HeadCache:
         """One decode token.  Flush-before-append: a full residual (128
         tokens) is quantised as four blocks first, so the newest token always
         stays 16-bit."""
+        rk = self._rotate(k_raw_bits[None, :])
+        self.append_scaled(rk.k_hat_bf16[0], rk.norm_f16[0], v_bits)
+
+    def append_scaled(self, k_hat_bf16, norm16, v_bits):
+        """append() of a key already rotated and scaled (flush first if full)."""
         if self.n_res == R:
             self.flush()
-        rk = rotate_scale_k(k_raw_bits[None, :], self.flags)
-        self.res_k_bf16.append(rk.k_hat_bf16[0])
-        self.res_norm16.append(rk.norm_f16[0])
+        self.res_k_bf16.append(np.asarray(k_hat_bf16, dtype=np.uint16))
+        self.res_norm16.append(np.float16(norm16))
         self.res_v_bf16.append(np.asarray(v_bits, dtype=np.uint16))
 
     def push_residual(self, k_raw_bits: np.ndarray, v_bits: np.ndarray):
         """Place up to 128 prompt tokens in the residual window (no flush)."""
         assert self.n_res + k_raw_bits.shape[0] <= R
-        rk = rotate_scale_k(k_raw_bits, self.flags)
-        for i in range(k_raw_bits.shape[0]):
+        rk = self._rotate(k_raw_bits)
+        self._push_scaled(rk, v_bits)
+
+    def _push_scaled(self, rk, v_bits):
+        for i in range(rk.k_hat_bf16.shape[0]):
             self.res_k_bf16.append(rk.k_hat_bf16[i])
             self.res_norm16.append(rk.norm_f16[i])
             self.res_v_bf16.append(np.asarray(v_bits[i], dtype=np.uint16))
@@ -379,14 +406,47 @@ class HeadCache:
         return attention(np.atleast_2d(q_rot), keys, vals, tau)
 
 
-def build_head_cache(k_raw_bits, v_bits, n_packed: int, flags: int = 0) -> HeadCache:
+def build_head_cache(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
+                     target: float = 1.0) -> HeadCache:
     """Prompt of T tokens: the first ``n_packed`` (a multiple of 32) are
     quantised, the remaining T - n_packed (at most 128) stay in the residual."""
     T = k_raw_bits.shape[0]
     assert n_packed % G == 0 and 0 <= T - n_packed <= R
-    c = HeadCache(flags=flags)
+    c = HeadCache(flags=flags, target=target)
     if n_packed:
         c.quantize_prefix(k_raw_bits[:n_packed], v_bits[:n_packed])
     if T > n_packed:
         c.push_residual(k_raw_bits[n_packed:], v_bits[n_packed:])
     return c
+
+
+def build_row_caches(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
+                     target: float = 1.0) -> list:
+    """build_head_cache for every KV head of one sequence, k_raw_bits and
+    v_bits [Hkv][T][128]: the keys of all heads are rotated and scaled
+    together, which the all-heads norm needs, then each head is quantised
+    and filled on its own."""
+    Hkv, T = k_raw_bits.shape[0], k_raw_bits.shape[1]
+    assert n_packed % G == 0 and 0 <= T - n_packed <= R
+    rk = rotate_scale_k(k_raw_bits, flags, target)
+    caches = []
+    for h in range(Hkv):
+        c = HeadCache(flags=flags, target=target)
+        if n_packed:
+            c._pack(rk.k_hat_bf16[h, :n_packed], rk.norm_f16[h, :n_packed], v_bits[h, :n_packed])
+        if T > n_packed:
+            c._push_scaled(RotatedKeys(rk.k_hat[h, n_packed:], rk.k_hat_bf16[h, n_packed:],
+                                       rk.norm[h, n_packed:], rk.norm_f16[h, n_packed:]),
+                           v_bits[h, n_packed:])
+        caches.append(c)
+    return caches
+
+
+def append_row(caches: list, k_raw_bits, v_bits):
+    """One decode token for every KV head of a sequence (k_raw_bits, v_bits
+    [Hkv][128]): rotated and scaled together, then appended head by head
+    (flush-before-append)."""
+    c0 = caches[0]
+    rk = rotate_scale_k(np.asarray(k_raw_bits)[:, None, :], c0.flags, c0.target)
+    for h, c in enumerate(caches):
+        c.append_scaled(rk.k_hat_bf16[h, 0], rk.norm_f16[h, 0], v_bits[h])
