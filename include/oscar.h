@@ -53,8 +53,21 @@ typedef enum {
 } oscar_status;
 
 /* Ablation flags ([notes] III, Ablations: rotation only / scaling only).
- * 0 = the method: rotation then scaling. */
-enum { OSCAR_NO_ROTATE = 1u, OSCAR_NO_SCALE = 2u };
+ * 0 = the method: rotation then scaling, each token-head's key scaled by its
+ * own norm.
+ * OSCAR_NORM_ALL_HEADS: norm-scope variant.  The norm of token i is taken over
+ * the rotated keys of all Hkv heads together ([notes] II, Notation: k_i in
+ * R^{H*d_h} with n_i = ||k_i||; Step Two: "across all heads"), every head's
+ * key is divided by it, and each head stores the same norm.  A head's k_hat
+ * then has norm <= 1 rather than 1. */
+enum { OSCAR_NO_ROTATE = 1u, OSCAR_NO_SCALE = 2u, OSCAR_NORM_ALL_HEADS = 4u };
+
+/* Target norm (the scaling target whose choice [rainbus] 独立分析的弱点 (1)
+ * says an appendix ablates): keys are scaled to norm `target` instead of 1 and
+ * the stored norm is n / target, so dequantisation is unchanged.  0 means 1.
+ * Accepted range [2^-8, 2^8].  A power of two changes no code (the min-max
+ * quantiser is scale-equivariant and such a product is exact); other values
+ * move the bf16 / fp16 roundings. */
 
 #define OSCAR_HEAD_DIM 128
 #define OSCAR_GROUP 32
@@ -103,7 +116,8 @@ typedef struct {
   oscar_f16* k_res_norm;
   int n_packed;      /* quantised tokens per row, multiple of 32 */
   int n_res;         /* residual tokens per row, 0..128 */
-  unsigned flags;    /* OSCAR_NO_ROTATE / OSCAR_NO_SCALE, fixed for the cache's life */
+  unsigned flags;    /* OSCAR_NO_ROTATE / OSCAR_NO_SCALE / OSCAR_NORM_ALL_HEADS, fixed for the cache's life */
+  float norm_target; /* target norm of the scaled keys (0 = 1), fixed for the cache's life */
 } oscar_cache;
 
 /*
@@ -132,6 +146,7 @@ typedef struct {
   oscar_bf16* v_res;        /* [B][Hkv][128][128] */
   oscar_f16* k_res_norm;    /* [B][Hkv][128] */
   unsigned flags;
+  float norm_target;
 } oscar_paged_cache;
 
 /*
@@ -152,6 +167,10 @@ oscar_status oscar_rotate_q(const oscar_bf16* q, float* q_rot, int B, int Hq,
  * [news] 三), norm = ||k|| ([notes] Step Two: divide each token by its own L2
  * norm and keep the norm).  A zero key gives k_hat = 0, norm = 0.
  * OSCAR_NO_ROTATE skips H; OSCAR_NO_SCALE keeps k' and writes norm = 1.
+ * OSCAR_NORM_ALL_HEADS: s sums over the token's keys in all Hkv heads (the
+ * sum is formed from the raw keys, 128 * sum(k^2) = sum(k'^2) by
+ * orthogonality).  norm_target t (0 = 1): k_hat = t * k' * rsqrt(s) and
+ * norm = ||k|| / t.
  *  k        bf16 input,  element (b,h,t,c) at k[((b*Hkv+h)*in_T + t)*128 + c], t < n_tok
  *  k_hat    bf16 output, element at k_hat[((b*Hkv+h)*out_T + out_t0 + t)*128 + c]
  *  norm_out fp16 output, element at norm_out[(b*Hkv+h)*out_T + out_t0 + t]
@@ -159,7 +178,8 @@ oscar_status oscar_rotate_q(const oscar_bf16* q, float* q_rot, int B, int Hq,
  */
 oscar_status oscar_rotate_scale_k(const oscar_bf16* k, int in_T,
                                   oscar_bf16* k_hat, oscar_f16* norm_out, int out_T, int out_t0,
-                                  int B, int Hkv, int n_tok, unsigned flags, void* stream);
+                                  int B, int Hkv, int n_tok, unsigned flags, float norm_target,
+                                  void* stream);
 
 /*
  * Quantisation kernel (2) of [news] 三: keys as block-wise per-channel INT2

@@ -47,7 +47,7 @@ oscar_status check_cache(const oscar_cache* c) {
   if (c->n_packed < 0 || c->n_packed % kG != 0 || c->n_packed > c->T_cap)
     return OSCAR_ERR_INVALID_ARG;
   if (c->n_res < 0 || c->n_res > kR) return OSCAR_ERR_INVALID_ARG;
-  if (c->flags & ~3u) return OSCAR_ERR_INVALID_ARG;
+  if ((c->flags & ~kAllFlags) || !target_ok(c->norm_target)) return OSCAR_ERR_INVALID_ARG;
   return OSCAR_OK;
 }
 
@@ -136,7 +136,7 @@ extern "C" {
 
 oscar_status oscar_rotate_q(const oscar_bf16* q, float* q_rot, int B, int Hq, unsigned flags,
                             void* stream) {
-  if (!q || !q_rot || B <= 0 || Hq <= 0 || (flags & ~3u)) return OSCAR_ERR_INVALID_ARG;
+  if (!q || !q_rot || B <= 0 || Hq <= 0 || (flags & ~kAllFlags)) return OSCAR_ERR_INVALID_ARG;
   if (!al16(q) || !al16(q_rot)) return OSCAR_ERR_ALIGNMENT;
   const long long n = (long long)B * Hq;
   if (n > (1LL << 30)) return OSCAR_ERR_INVALID_ARG;
@@ -147,8 +147,9 @@ oscar_status oscar_rotate_q(const oscar_bf16* q, float* q_rot, int B, int Hq, un
 
 oscar_status oscar_rotate_scale_k(const oscar_bf16* k, int in_T, oscar_bf16* k_hat,
                                   oscar_f16* norm_out, int out_T, int out_t0, int B, int Hkv,
-                                  int n_tok, unsigned flags, void* stream) {
-  if (!k || !k_hat || !norm_out || B <= 0 || Hkv <= 0 || n_tok <= 0 || (flags & ~3u))
+                                  int n_tok, unsigned flags, float norm_target, void* stream) {
+  if (!k || !k_hat || !norm_out || B <= 0 || Hkv <= 0 || n_tok <= 0 || (flags & ~kAllFlags) ||
+      !target_ok(norm_target))
     return OSCAR_ERR_INVALID_ARG;
   if (in_T < n_tok || out_t0 < 0 || out_t0 + (long long)n_tok > out_T)
     return OSCAR_ERR_INVALID_ARG;
@@ -156,8 +157,8 @@ oscar_status oscar_rotate_scale_k(const oscar_bf16* k, int in_T, oscar_bf16* k_h
   const long long rows = (long long)B * Hkv;
   if (rows * n_tok > (1LL << 34)) return OSCAR_ERR_INVALID_ARG;
   cudaError_t e = launch_rotate_scale_k(k, in_T, k_hat, reinterpret_cast<__half*>(norm_out),
-                                        out_T, out_t0, (int)rows, n_tok, nullptr, nullptr, flags,
-                                        as_stream(stream));
+                                        out_T, out_t0, (int)rows, Hkv, n_tok, nullptr, nullptr,
+                                        key_scale(flags, norm_target), as_stream(stream));
   g_launches++;
   return from_cuda(e);
 }
@@ -194,7 +195,8 @@ oscar_status oscar_prefill_kv(oscar_cache* c, const oscar_bf16* k, const oscar_b
   if (c->n_res != 0) return OSCAR_ERR_INVALID_ARG;  // packed tokens must precede residual ones
   if ((long long)c->n_packed + n_tok > c->T_cap) return OSCAR_ERR_CAPACITY;
   cudaError_t e = launch_prefill_kv(k, v, in_T, n_tok, c->B, c->Hkv, c->T_cap, c->n_packed,
-                                    c->flags, c->packed, as_stream(stream));
+                                    key_scale(c->flags, c->norm_target), c->packed,
+                                    as_stream(stream));
   g_launches++;
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   c->n_packed += n_tok;
@@ -231,7 +233,8 @@ oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const osca
     const int m = std::min(n_tok - done, kR - c->n_res);
     cudaError_t e = launch_rotate_scale_k(
         k_new + (size_t)done * kD, n_tok, c->k_res, reinterpret_cast<__half*>(c->k_res_norm), kR,
-        c->n_res, rows, m, v_new + (size_t)done * kD, c->v_res, c->flags, s);
+        c->n_res, rows, c->Hkv, m, v_new + (size_t)done * kD, c->v_res,
+        key_scale(c->flags, c->norm_target), s);
     g_launches++;
     if (e != cudaSuccess) return OSCAR_ERR_CUDA;
     c->n_res += m;
@@ -282,6 +285,7 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   a.num_splits = S;
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
   cudaError_t e = launch_decode_int2(a, as_stream(stream));
   g_launches += 2;
   return from_cuda(e);
@@ -309,7 +313,7 @@ oscar_status check_paged(const oscar_paged_cache* c) {
     if (!p) return OSCAR_ERR_INVALID_ARG;
     if (!al4(p)) return OSCAR_ERR_ALIGNMENT;
   }
-  if (c->flags & ~3u) return OSCAR_ERR_INVALID_ARG;
+  if ((c->flags & ~kAllFlags) || !target_ok(c->norm_target)) return OSCAR_ERR_INVALID_ARG;
   return OSCAR_OK;
 }
 
@@ -327,7 +331,7 @@ PagedArgs paged_args(const oscar_paged_cache* c) {
   p.Hkv = c->Hkv;
   p.max_blocks = c->max_blocks;
   p.n_pages = c->n_pages;
-  p.flags = c->flags;
+  p.ks = key_scale(c->flags, c->norm_target);
   return p;
 }
 
@@ -398,6 +402,7 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
   a.num_splits = S;
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
   a.block_table = c->block_table;
   a.seq_packed = c->n_packed;
   a.seq_res = c->n_res;

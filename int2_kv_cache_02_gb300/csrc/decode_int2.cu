@@ -84,6 +84,37 @@ constexpr uint32_t pow4_inv_h2(int p) {
        : p == 3 ? 0x24002400u : 0x1C001C00u;
 }
 
+// Per-block step scale for caches whose keys are not all of unit norm (the
+// all-heads norm scope: a head's k_hat may be far below 1).  Returns 2^E as
+// fp16x2 with E chosen so that the block's largest key step times 2^E lies in
+// [0.5, 1): the query-step products q' sigma s 4^-p then keep both fp16
+// limbs in the normal range, as they do for unit-norm keys.  The caller
+// divides the Q.K sum by 2^E.  Lane tig holds channels 32 tig .. 32 tig + 31;
+// lanes xor 1, 2 hold the rest.  Steps are >= 0, so the max of their fp16
+// values picks the largest.
+__device__ __forceinline__ int block_step_exp(const uint4* ks4) {
+  __half2 m = u32_as_half2(0u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint4 v = ks4[i];
+    m = __hmax2(m, __hmax2(__hmax2(u32_as_half2(v.x), u32_as_half2(v.y)),
+                           __hmax2(u32_as_half2(v.z), u32_as_half2(v.w))));
+  }
+  uint32_t mb = half2_as_u32(m);
+  mb = max(mb & 0xffffu, mb >> 16);
+  mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+  mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+  return mb == 0 ? 0 : 14 - (int)(mb >> 10);   // mb >> 10: biased exponent
+}
+
+// fp16x2 {2^E 4^-p, ..} for p = 0..4 (exact: powers of two >= 2^-24).
+__device__ __forceinline__ void step_scales(uint32_t (&c)[5], int E) {
+  const float f = __int_as_float((127 + E) << 23);
+  c[0] = half2_as_u32(__floats2half2_rn(f, f));
+#pragma unroll
+  for (int p = 1; p < 5; ++p) c[p] = hmul2_u(c[0], pow4_inv_h2(p));
+}
+
 // Value code pair at slot k as centred fp16 values (c - 1.5) * 2^(2p - 9):
 // the masked pair is the subnormal c * 4^p * 2^-24 (as for the keys), and
 // one exact HFMA2 scales it by 2^15 and subtracts 1.5 * 2^(2p - 9).  p is
@@ -298,7 +329,7 @@ __device__ __forceinline__ float scale_query(float (&qf)[32], const float* qrow,
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
   int e = 0;
   if (amax > 0.0f) frexpf(amax, &e);
-  int sh = (amax > 0.0f) ? (((a.flags & OSCAR_NO_SCALE) ? 1 : 14) - e) : 0;
+  int sh = (amax > 0.0f) ? (a.q_exp - e) : 0;
   sh = max(-100, min(100, sh));
   const float sigma = ldexpf(1.0f, sh);
 #pragma unroll
@@ -313,7 +344,7 @@ __device__ __forceinline__ float scale_query(float (&qf)[32], const float* qrow,
 //  * scores, softmax and outputs: head tig mod GQ (columns 2 tig, 2 tig + 1
 //    are its hi and lo limbs), tokens gid + 8 j, j = 0..3;
 //  * P.V: channels on M as in the row layout, (head, limb of p~) on N.
-template <int GQ, class Ring>
+template <int GQ, bool BSCALE, class Ring>
 __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
                                             MergeSmem<GQ, NW>& E, long long qrow0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -381,6 +412,13 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
         kw[mt][r][0] = v.x; kw[mt][r][1] = v.y;
         kw10[mt][r][0] = v.x >> 10; kw10[mt][r][1] = v.y >> 10;
       }
+    uint32_t cs[5];
+    float qk_blk = qk_scale;
+    if constexpr (BSCALE) {
+      const int E = block_step_exp(ks4);
+      step_scales(cs, E);
+      qk_blk = qk_scale * __int_as_float((127 - E) << 23);
+    }
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
     float acc[2][4];
 #pragma unroll
@@ -392,8 +430,13 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
         constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
         constexpr int P23[4] = {key_pos(1), key_pos(3), key_pos(5), key_pos(7)};
         uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
-        if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
-        if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+        if constexpr (BSCALE) {
+          s01 = hmul2_u(s01, cs[P01[k8 & 3]]);
+          s23 = hmul2_u(s23, cs[P23[k8 & 3]]);
+        } else {
+          if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
+          if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+        }
         const uint32_t r01 =
             hfma2_u(qz[k8][0], s01, hfma2_u(qhm[k8][0], s01, neg2_u(hmul2_u(qhm[k8][0], s01))));
         const uint32_t r23 =
@@ -446,7 +489,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
     for (int j = 0; j < 4; ++j) {
       const int mt = j >> 1, r = j & 1;
       const float qk = r ? acc[mt][2] + acc[mt][3] : acc[mt][0] + acc[mt][1];
-      sc[j] = fmaf(qk, qk_scale, zs) * nf[j];
+      sc[j] = fmaf(qk, qk_blk, zs) * nf[j];
     }
     // Lazy rescaling (see the row layout).  Each lane tests its own scores;
     // only when some lane is past the threshold does the warp form the
@@ -540,7 +583,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
 //    gid; B operand: key codes of token 8 nt + gid, n-tiles nt = 0..3;
 //  * scores and softmax: head gid, tokens 8 nt + 2 tig and + 1;
 //  * P.V: channels on M, the 8 heads on N, one n-tile per limb of p~.
-template <int GQ, class Ring>
+template <int GQ, bool BSCALE, class Ring>
 __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
                                             MergeSmem<GQ, NW>& E, long long qrow0) {
   static_assert(GQ == 8, "the row layout serves groups of 8 query heads");
@@ -616,6 +659,13 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
     }
     // The Q.K accumulators start from zero (not from Z) so their MMA chains
     // do not wait for the Z chain; Z joins each score below.
+    uint32_t cs[5];
+    float qk_blk = qk_scale;
+    if constexpr (BSCALE) {
+      const int E = block_step_exp(ks4);
+      step_scales(cs, E);
+      qk_blk = qk_scale * __int_as_float((127 - E) << 23);
+    }
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
     float acc[4][4];
 #pragma unroll
@@ -629,8 +679,13 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
         constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
         constexpr int P23[4] = {key_pos(1), key_pos(3), key_pos(5), key_pos(7)};
         uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
-        if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
-        if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+        if constexpr (BSCALE) {
+          s01 = hmul2_u(s01, cs[P01[k8 & 3]]);
+          s23 = hmul2_u(s23, cs[P23[k8 & 3]]);
+        } else {
+          if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
+          if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+        }
         uint32_t at[4];
         at[0] = hmul2_u(aq[k8][0], s01);
         at[1] = hfma2_u(aq[k8][1], s01, hfma2_u(aq[k8][0], s01, neg2_u(at[0])));
@@ -665,8 +720,8 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
     float sc[8];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      sc[2 * nt] = fmaf(acc[nt][0] + acc[nt][2], qk_scale, zs) * ne[nt];
-      sc[2 * nt + 1] = fmaf(acc[nt][1] + acc[nt][3], qk_scale, zs) * no[nt];
+      sc[2 * nt] = fmaf(acc[nt][0] + acc[nt][2], qk_blk, zs) * ne[nt];
+      sc[2 * nt + 1] = fmaf(acc[nt][1] + acc[nt][3], qk_blk, zs) * no[nt];
     }
 
     // Online softmax for this thread's head.
@@ -836,7 +891,8 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
 }
 
 // Up to 4 CTAs per SM in the column layout (128 registers), 3 in the row layout.
-template <int GQ, bool PAGED>
+// BSCALE: per-block step scale (caches with the all-heads norm scope).
+template <int GQ, bool PAGED, bool BSCALE>
 __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
@@ -848,9 +904,9 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
   if (split < a.num_splits) {
     const WarpRing<PAGED> R = make_ring<PAGED>(a, smem, b, h, split);
     if constexpr (GQ <= 4) {
-      packed_cols<GQ>(a, R, E, qrow0);
+      packed_cols<GQ, BSCALE>(a, R, E, qrow0);
     } else {
-      packed_rows<GQ>(a, R, E, qrow0);
+      packed_rows<GQ, BSCALE>(a, R, E, qrow0);
     }
   } else {
     residual_split<GQ, PAGED>(a, E, row, qrow0, b);
@@ -862,46 +918,46 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
 
 // Opt in to kSmemBytes of dynamic shared memory (needed above 48 KB), once
 // per instantiation and device.
-template <int GQ, bool PAGED>
+template <int GQ, bool PAGED, bool BSCALE>
 cudaError_t allow_smem() {
   static int done[128] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED>,
+  e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED, BSCALE>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess && dev >= 0 && dev < 128) done[dev] = 1;
   return e;
 }
 
-template <int GQ, bool PAGED>
+template <int GQ, bool PAGED, bool BSCALE>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e0 = allow_smem<GQ, PAGED>();
+  cudaError_t e0 = allow_smem<GQ, PAGED, BSCALE>();
   if (e0 != cudaSuccess) return e0;
   dim3 grid(a.num_splits + 1, a.Hkv, a.B);
-  decode_int2_kernel<GQ, PAGED><<<grid, NW * 32, kSmemBytes, s>>>(a);
+  decode_int2_kernel<GQ, PAGED, BSCALE><<<grid, NW * 32, kSmemBytes, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_combine(a.ws, a.out, a.B * a.Hq, a.num_splits + 1, s);
 }
 
-template <bool PAGED>
+template <bool PAGED, bool BSCALE>
 cudaError_t launch_p(const DecodeArgs& a, cudaStream_t s) {
   switch (a.Hq / a.Hkv) {
-    case 1: return launch_g<1, PAGED>(a, s);
-    case 2: return launch_g<2, PAGED>(a, s);
-    case 4: return launch_g<4, PAGED>(a, s);
-    case 8: return launch_g<8, PAGED>(a, s);
+    case 1: return launch_g<1, PAGED, BSCALE>(a, s);
+    case 2: return launch_g<2, PAGED, BSCALE>(a, s);
+    case 4: return launch_g<4, PAGED, BSCALE>(a, s);
+    case 8: return launch_g<8, PAGED, BSCALE>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <int GQ>
 int occupancy_g() {
-  if (allow_smem<GQ, false>() != cudaSuccess) return 0;
+  if (allow_smem<GQ, false, false>() != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ, false>, NW * 32,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ, false, false>, NW * 32,
                                                     kSmemBytes) != cudaSuccess)
     return 0;
   return n;
@@ -910,7 +966,9 @@ int occupancy_g() {
 }  // namespace
 
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t s) {
-  return a.block_table ? launch_p<true>(a, s) : launch_p<false>(a, s);
+  if (a.flags & OSCAR_NORM_ALL_HEADS)
+    return a.block_table ? launch_p<true, true>(a, s) : launch_p<false, true>(a, s);
+  return a.block_table ? launch_p<true, false>(a, s) : launch_p<false, false>(a, s);
 }
 
 int decode_int2_ctas_per_sm(int g) {

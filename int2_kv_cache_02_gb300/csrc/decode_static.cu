@@ -66,7 +66,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
     if (!aligned16(p)) return OSCAR_ERR_ALIGNMENT;
   }
   if (c->n_packed < 0 || c->n_packed % kG != 0 || c->n_packed > c->T_cap || c->n_res < 0 ||
-      c->n_res > kR || (c->flags & ~3u))
+      c->n_res > kR || (c->flags & ~kAllFlags) || !target_ok(c->norm_target))
     return OSCAR_ERR_INVALID_ARG;
   if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
       !std::isfinite(softmax_scale))
@@ -102,6 +102,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   a.num_splits = S;
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
   cudaError_t e = launch_decode_int2(a, static_cast<cudaStream_t>(stream));
   count_launches(2);
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;

@@ -4,16 +4,48 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
+#include "../../include/oscar.h"
+
 namespace oscar {
+
+// How keys are scaled (Omni-Token Scaling and its variants): the ablation
+// and norm-scope flags of oscar.h and the target norm (1 = unit norm).
+struct KeyScale {
+  unsigned flags;
+  float target;
+};
+
+constexpr unsigned kAllFlags = OSCAR_NO_ROTATE | OSCAR_NO_SCALE | OSCAR_NORM_ALL_HEADS;
+
+// Target norm of the scaled keys as the ABI takes it: 0 means 1; otherwise
+// within [2^-8, 2^8].
+inline bool target_ok(float t) {
+  return t == 0.0f || (t >= 0.00390625f && t <= 256.0f);   // false for NaN
+}
+inline KeyScale key_scale(unsigned flags, float target) {
+  return KeyScale{flags, target == 0.0f ? 1.0f : target};
+}
+// Query exponent of the decode kernel: keys scaled to norm t have elements,
+// hence steps, below t, so the query's largest element goes to about
+// 2^(14 - ceil(log2 t)); unscaled keys are as large as the data (2^1).
+inline int query_exponent(const KeyScale& ks) {
+  if (ks.flags & OSCAR_NO_SCALE) return 1;
+  int e = 0;
+  const float m = frexpf(ks.target, &e);   // t = m * 2^e, m in [0.5, 1)
+  return 14 - (m > 0.5f ? e : e - 1);
+}
 
 cudaError_t launch_rotate_q(const uint16_t* q, float* out, int n_vec, unsigned flags,
                             cudaStream_t s);
 
+// Rows are (b, h) with h fastest over Hkv heads (the all-heads norm reads a
+// token's keys in every head of its sequence).
 cudaError_t launch_rotate_scale_k(const uint16_t* k, int in_T, uint16_t* k_hat, __half* norm,
-                                  int out_T, int out_t0, int n_rows, int n_tok,
-                                  const uint16_t* v_in, uint16_t* v_out, unsigned flags,
+                                  int out_T, int out_t0, int n_rows, int Hkv, int n_tok,
+                                  const uint16_t* v_in, uint16_t* v_out, KeyScale ks,
                                   cudaStream_t s);
 
 // Quantises tokens [0, n_tok) of each source row into the block records of
@@ -34,6 +66,9 @@ struct DecodeArgs {
   int B, Hkv, Hq, T_cap, n_packed, n_res, num_splits;
   unsigned flags;
   float scale_log2;   // softmax_scale * log2(e)
+  // the query is scaled by 2^(q_exp - e), e the exponent of its largest
+  // element, so that q'*step stays in fp16 range for the cache's key scale
+  int q_exp = 14;
   // paged cache (block_table != nullptr): records at packed + (page*Hkv + h)
   // * block bytes, page = block_table[b*max_blocks + block]; per-sequence
   // lengths seq_packed[b], seq_res[b] replace n_packed, n_res; n_packed
@@ -83,7 +118,7 @@ struct PagedArgs {
   __half* k_res_norm;
   unsigned* status;
   int B, Hkv, max_blocks, n_pages;
-  unsigned flags;
+  KeyScale ks;
 };
 cudaError_t launch_paged_prefill(const PagedArgs& p, const uint16_t* k, const uint16_t* v,
                                  int in_T, const int32_t* n_tok, int max_tok, cudaStream_t s);
@@ -92,7 +127,7 @@ cudaError_t launch_paged_append(const PagedArgs& p, const uint16_t* k_new, const
 
 // Fused rotate + scale + quantise of n_tok tokens of raw keys and values.
 cudaError_t launch_prefill_kv(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,
-                              int Hkv, int T_cap, int p0, unsigned flags, uint8_t* packed,
+                              int Hkv, int T_cap, int p0, KeyScale ks, uint8_t* packed,
                               cudaStream_t s);
 
 // One CTA polls an mbarrier nothing arrives at, `iterations` times, then

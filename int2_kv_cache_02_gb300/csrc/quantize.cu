@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
 // the norms in shared memory; the values are staged as in quantize_kv_kernel.
 __global__ void __launch_bounds__(128) prefill_kv_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int in_T, int Hkv,
-    int T_cap, int p0, unsigned flags, uint8_t* __restrict__ packed) {
+    int T_cap, int p0, KeyScale ks, uint8_t* __restrict__ packed) {
   __shared__ __align__(16) uint16_t kt[kG][kD];
   __shared__ __align__(16) uint16_t vt[kG][kD];
   __shared__ __align__(16) uint8_t kc[kG][kD];
@@ -75,12 +75,17 @@ __global__ void __launch_bounds__(128) prefill_kv_kernel(
 #pragma unroll
     for (int i = 0; i < 4; ++i) vd[tid + 128 * i] = vs[tid + 128 * i];
   }
+  // with the all-heads norm, head 0 of this sequence's token src_tok
+  const long long head0_tok = src_tok - (long long)blockIdx.y * in_T;
 #pragma unroll 2
   for (int i = 0; i < 8; ++i) {
     const int t = 8 * warp + i;
+    float s_all = 0.0f;
+    if (ks.flags & OSCAR_NORM_ALL_HEADS)
+      s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, Hkv, lane);
     const uint2 raw = reinterpret_cast<const uint2*>(k + (src_tok + t) * kD)[lane];
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    const float norm = rotate_scale_key(x, lane, flags);
+    const float norm = rotate_scale_key(x, lane, ks, s_all);
     reinterpret_cast<uint2*>(&kt[t][0])[lane] = pack_bf16x4(x);
     if (lane == 0) ns[t] = __float2half_rn(norm);
   }
@@ -133,12 +138,16 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(PagedArgs p,
 #pragma unroll
     for (int i = 0; i < 4; ++i) vd[tid + 128 * i] = vs[tid + 128 * i];
   }
+  const long long head0_tok = src_tok - (long long)h * in_T;
 #pragma unroll 2
   for (int i = 0; i < 8; ++i) {
     const int t = 8 * warp + i;
+    float s_all = 0.0f;
+    if (p.ks.flags & OSCAR_NORM_ALL_HEADS)
+      s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, p.Hkv, lane);
     const uint2 raw = reinterpret_cast<const uint2*>(k + (src_tok + t) * kD)[lane];
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    const float norm = rotate_scale_key(x, lane, p.flags);
+    const float norm = rotate_scale_key(x, lane, p.ks, s_all);
     reinterpret_cast<uint2*>(&kt[t][0])[lane] = pack_bf16x4(x);
     if (lane == 0) ns[t] = __float2half_rn(norm);
   }
@@ -230,10 +239,10 @@ cudaError_t launch_quantize_kv(const uint16_t* k_hat, const __half* k_norm, cons
 }
 
 cudaError_t launch_prefill_kv(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,
-                              int Hkv, int T_cap, int p0, unsigned flags, uint8_t* packed,
+                              int Hkv, int T_cap, int p0, KeyScale ks, uint8_t* packed,
                               cudaStream_t s) {
   dim3 grid(n_tok / kG, Hkv, B);
-  prefill_kv_kernel<<<grid, 128, 0, s>>>(k, v, in_T, Hkv, T_cap, p0, flags, packed);
+  prefill_kv_kernel<<<grid, 128, 0, s>>>(k, v, in_T, Hkv, T_cap, p0, ks, packed);
   return cudaGetLastError();
 }
 

@@ -1,5 +1,5 @@
 // Canalized Rotation (online fast Walsh-Hadamard transform over head_dim)
-// and Omni-Token Scaling.
+// and Omni-Token Scaling, with its norm-scope and target-norm variants.
 //
 // "OScaR: The Occam's Razor for Extreme KV Cache Quantization in LLMs and
 // Beyond" (reading notes), II. Method, Step One (K' = K.H, H orthogonal with
@@ -35,8 +35,8 @@ __global__ void __launch_bounds__(256) rotate_q_kernel(const uint16_t* __restric
 // the same token (the decode append).
 __global__ void __launch_bounds__(256) rotate_scale_k_kernel(
     const uint16_t* __restrict__ k, int in_T, uint16_t* __restrict__ k_hat,
-    __half* __restrict__ norm_out, int out_T, int out_t0, int n_rows, int n_tok,
-    const uint16_t* __restrict__ v_in, uint16_t* __restrict__ v_out, unsigned flags) {
+    __half* __restrict__ norm_out, int out_T, int out_t0, int n_rows, int Hkv, int n_tok,
+    const uint16_t* __restrict__ v_in, uint16_t* __restrict__ v_out, KeyScale ks) {
   const int lane = threadIdx.x & 31;
   const long long v = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (v >= (long long)n_rows * n_tok) return;
@@ -45,9 +45,14 @@ __global__ void __launch_bounds__(256) rotate_scale_k_kernel(
   const long long src = (row * in_T + t) * kD;
   const long long dst_tok = row * out_T + out_t0 + t;
 
+  float s_all = 0.0f;
+  if (ks.flags & OSCAR_NORM_ALL_HEADS) {
+    const long long row0 = row - row % Hkv;   // head 0 of this sequence
+    s_all = all_heads_sq(k + (row0 * in_T + t) * kD, (long long)in_T * kD, Hkv, lane);
+  }
   const uint2 raw = reinterpret_cast<const uint2*>(k + src)[lane];
   float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-  const float norm = rotate_scale_key(x, lane, flags);
+  const float norm = rotate_scale_key(x, lane, ks, s_all);
   reinterpret_cast<uint2*>(k_hat + dst_tok * kD)[lane] = pack_bf16x4(x);
   if (lane == 0) norm_out[dst_tok] = __float2half_rn(norm);
   if (v_in != nullptr) {
@@ -75,9 +80,12 @@ __global__ void __launch_bounds__(256) paged_append_kernel(PagedArgs p,
   }
   const int slot = (r == kR) ? 0 : r;
   const long long dst = row * kR + slot;
+  float s_all = 0.0f;
+  if (p.ks.flags & OSCAR_NORM_ALL_HEADS)
+    s_all = all_heads_sq(k_new + (long long)b * p.Hkv * kD, kD, p.Hkv, lane);
   const uint2 raw = reinterpret_cast<const uint2*>(k_new + row * kD)[lane];
   float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-  const float norm = rotate_scale_key(x, lane, p.flags);
+  const float norm = rotate_scale_key(x, lane, p.ks, s_all);
   reinterpret_cast<uint2*>(p.k_res + dst * kD)[lane] = pack_bf16x4(x);
   if (lane == 0) p.k_res_norm[dst] = __float2half_rn(norm);
   reinterpret_cast<uint2*>(p.v_res + dst * kD)[lane] =
@@ -106,13 +114,13 @@ cudaError_t launch_rotate_q(const uint16_t* q, float* out, int n_vec, unsigned f
 }
 
 cudaError_t launch_rotate_scale_k(const uint16_t* k, int in_T, uint16_t* k_hat, __half* norm,
-                                  int out_T, int out_t0, int n_rows, int n_tok,
-                                  const uint16_t* v_in, uint16_t* v_out, unsigned flags,
+                                  int out_T, int out_t0, int n_rows, int Hkv, int n_tok,
+                                  const uint16_t* v_in, uint16_t* v_out, KeyScale ks,
                                   cudaStream_t s) {
   const long long n = (long long)n_rows * n_tok;
   const long long grid = (n + 7) / 8;
   rotate_scale_k_kernel<<<(unsigned)grid, 256, 0, s>>>(k, in_T, k_hat, norm, out_T, out_t0,
-                                                       n_rows, n_tok, v_in, v_out, flags);
+                                                       n_rows, Hkv, n_tok, v_in, v_out, ks);
   return cudaGetLastError();
 }
 

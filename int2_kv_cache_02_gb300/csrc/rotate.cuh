@@ -6,6 +6,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "launch.h"
 
 namespace oscar {
 
@@ -33,24 +34,45 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Rotates (unless OSCAR_NO_ROTATE) and scales to unit norm (unless
-// OSCAR_NO_SCALE) the key held in x; returns its norm (1 when not scaled,
-// 0 for a zero key, whose k_hat is then 0).
-__device__ __forceinline__ float rotate_scale_key(float (&x)[4], int lane, unsigned flags) {
-  const bool rot = !(flags & OSCAR_NO_ROTATE);
+// Sum of squares of one token's raw keys over all Hkv heads, for the
+// all-heads norm: head h's key (4 elements per lane) at k0 + h * head_stride;
+// each head's sum is a warp sum of the lanes' partials, added in head order,
+// so every kernel that scales keys forms the same value.  By orthogonality of
+// H the rotated keys have 128 times this sum (exact in fp32).
+__device__ __forceinline__ float all_heads_sq(const uint16_t* k0, long long head_stride, int Hkv,
+                                             int lane) {
+  float s = 0.0f;
+  for (int h = 0; h < Hkv; ++h) {
+    const uint2 raw = reinterpret_cast<const uint2*>(k0 + h * head_stride)[lane];
+    const float a = bf16_lo(raw.x), b = bf16_hi(raw.x), c = bf16_lo(raw.y), d = bf16_hi(raw.y);
+    s += warp_sum(fmaf(d, d, fmaf(c, c, fmaf(b, b, a * a))));
+  }
+  return s;
+}
+
+// Rotates (unless OSCAR_NO_ROTATE) and scales (unless OSCAR_NO_SCALE) the key
+// held in x to the norm ks.target; returns the stored norm n / target, with n
+// the key's own norm or, with OSCAR_NORM_ALL_HEADS, the norm of the token's
+// keys over all heads, whose raw sum of squares the caller passes in s_all.
+// Unscaled keys store 1; a zero key (zero norm) keeps k_hat = 0 and stores 0.
+__device__ __forceinline__ float rotate_scale_key(float (&x)[4], int lane, KeyScale ks,
+                                                  float s_all = 0.0f) {
+  const bool rot = !(ks.flags & OSCAR_NO_ROTATE);
   if (rot) fht128(x, lane);
-  if (flags & OSCAR_NO_SCALE) {
+  if (ks.flags & OSCAR_NO_SCALE) {
     const float f = rot ? kInvSqrtD : 1.0f;
 #pragma unroll
     for (int r = 0; r < 4; ++r) x[r] *= f;
     return 1.0f;
   }
-  const float s = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+  const float s = (ks.flags & OSCAR_NORM_ALL_HEADS)
+                      ? (rot ? 128.0f * s_all : s_all)
+                      : warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
   if (s > 0.0f) {
-    const float rs = rsqrtf(s);
+    const float f = rsqrtf(s) * ks.target;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) x[r] *= rs;
-    return sqrtf(s) * (rot ? kInvSqrtD : 1.0f);
+    for (int r = 0; r < 4; ++r) x[r] *= f;
+    return sqrtf(s) * (rot ? kInvSqrtD : 1.0f) / ks.target;
   }
 #pragma unroll
   for (int r = 0; r < 4; ++r) x[r] = 0.0f;

@@ -18,7 +18,7 @@ import torch
 from . import _build
 
 D, G, R = 128, 32, 128
-NO_ROTATE, NO_SCALE = 1, 2
+NO_ROTATE, NO_SCALE, NORM_ALL_HEADS = 1, 2, 4
 
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "ALIGNMENT", 4: "CAPACITY",
            5: "WORKSPACE", 6: "CUDA", 7: "DEVICE_STATUS"}
@@ -35,7 +35,8 @@ class OscarCacheStruct(ctypes.Structure):
     _fields_ = [("B", c_int), ("Hkv", c_int), ("T_cap", c_int),
                 ("packed", c_void_p),
                 ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
-                ("n_packed", c_int), ("n_res", c_int), ("flags", c_uint)]
+                ("n_packed", c_int), ("n_res", c_int), ("flags", c_uint),
+                ("norm_target", c_float)]
 
 
 class OscarPagedCacheStruct(ctypes.Structure):
@@ -43,7 +44,7 @@ class OscarPagedCacheStruct(ctypes.Structure):
                 ("pages", c_void_p), ("block_table", c_void_p),
                 ("n_packed", c_void_p), ("n_res", c_void_p),
                 ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
-                ("flags", c_uint)]
+                ("flags", c_uint), ("norm_target", c_float)]
 
 
 BLOCK_BYTES = 2752
@@ -64,7 +65,7 @@ def _load() -> ctypes.CDLL:
     sig = {
         "oscar_rotate_q": (c_int, [c_void_p, c_void_p, c_int, c_int, c_uint, c_void_p]),
         "oscar_rotate_scale_k": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_int,
-                                         c_int, c_int, c_int, c_uint, c_void_p]),
+                                         c_int, c_int, c_int, c_uint, c_float, c_void_p]),
         "oscar_quantize_kv": (c_int, [P, c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p]),
         "oscar_append_kv": (c_int, [P, c_void_p, c_void_p, c_int, c_void_p]),
         "oscar_prefill_kv": (c_int, [P, c_void_p, c_void_p, c_int, c_int, c_void_p]),
@@ -130,7 +131,8 @@ class KVCache:
     """Caller-owned device buffers of one layer's OScaR cache plus the
     oscar_cache struct that points at them (layouts in include/oscar.h)."""
 
-    def __init__(self, B: int, Hkv: int, T_cap: int, flags: int = 0, device=None):
+    def __init__(self, B: int, Hkv: int, T_cap: int, flags: int = 0, device=None,
+                 norm_target: float = 0.0):
         if T_cap % G:
             raise ValueError("T_cap must be a multiple of 32")
         dev = torch.device(device if device is not None else "cuda")
@@ -143,7 +145,7 @@ class KVCache:
         s.B, s.Hkv, s.T_cap = B, Hkv, T_cap
         for name in ("packed", "k_res", "v_res", "k_res_norm"):
             setattr(s, name, getattr(self, name).data_ptr())
-        s.n_packed, s.n_res, s.flags = 0, 0, flags
+        s.n_packed, s.n_res, s.flags, s.norm_target = 0, 0, flags, norm_target
         self.struct = s
 
     B = property(lambda self: self.struct.B)
@@ -152,6 +154,7 @@ class KVCache:
     n_packed = property(lambda self: self.struct.n_packed)
     n_res = property(lambda self: self.struct.n_res)
     flags = property(lambda self: self.struct.flags)
+    norm_target = property(lambda self: self.struct.norm_target)
 
     def ref(self):
         return ctypes.byref(self.struct)
@@ -196,7 +199,7 @@ class PagedKVCache:
     allocator below; the device kernels only follow the table."""
 
     def __init__(self, B: int, Hkv: int, max_blocks: int, n_pages: int, flags: int = 0,
-                 device=None):
+                 device=None, norm_target: float = 0.0):
         dev = torch.device(device if device is not None else "cuda")
         self.pages = torch.zeros((n_pages, Hkv, BLOCK_BYTES), dtype=torch.uint8, device=dev)
         self.block_table = torch.full((B, max_blocks), -1, dtype=torch.int32, device=dev)
@@ -207,6 +210,7 @@ class PagedKVCache:
         self.k_res_norm = torch.zeros((B, Hkv, R), dtype=torch.float16, device=dev)
         s = OscarPagedCacheStruct()
         s.B, s.Hkv, s.max_blocks, s.n_pages, s.flags = B, Hkv, max_blocks, n_pages, flags
+        s.norm_target = norm_target
         s.pages = self.pages.data_ptr()
         s.block_table = self.block_table.data_ptr()
         s.n_packed = self.n_packed_d.data_ptr()
@@ -265,9 +269,9 @@ def rotate_q(q: torch.Tensor, q_rot: torch.Tensor, flags: int = 0, stream=None):
 
 def rotate_scale_k(k: torch.Tensor, k_hat: torch.Tensor, norm: torch.Tensor, B: int, Hkv: int,
                    n_tok: int, in_T: int, out_T: int, out_t0: int = 0, flags: int = 0,
-                   stream=None):
+                   stream=None, norm_target: float = 0.0):
     _check(_lib.oscar_rotate_scale_k(_ptr(k), in_T, _ptr(k_hat), _ptr(norm), out_T, out_t0,
-                                     B, Hkv, n_tok, flags, _stream(stream)),
+                                     B, Hkv, n_tok, flags, norm_target, _stream(stream)),
            "oscar_rotate_scale_k")
 
 

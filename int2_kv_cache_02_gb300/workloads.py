@@ -137,7 +137,8 @@ def draw_q_cuda(wl: Workload, step: int, device="cuda"):
 
 
 def build_cache_cuda(wl: Workload, K, V, flags: int = 0, T_cap: int | None = None,
-                     chunk: int = 8192, device="cuda", fused: bool = True):
+                     chunk: int = 8192, device="cuda", fused: bool = True,
+                     norm_target: float = 0.0):
     """Prompt of T0 tokens -> OScaR cache: rotate + scale + quantise the first
     n_packed tokens, then append the remaining ones to the residual window.
     fused=True does the first part in one oscar_prefill_kv call; fused=False
@@ -146,7 +147,8 @@ def build_cache_cuda(wl: Workload, K, V, flags: int = 0, T_cap: int | None = Non
     import torch
     from . import oscar
     T_cap = T_cap if T_cap is not None else wl.t_cap()
-    cache = oscar.KVCache(wl.B, wl.Hkv, T_cap, flags=flags, device=device)
+    cache = oscar.KVCache(wl.B, wl.Hkv, T_cap, flags=flags, device=device,
+                          norm_target=norm_target)
     T_stride = K.shape[2]
     if fused:
         if wl.n_packed:
@@ -163,7 +165,8 @@ def build_cache_cuda(wl: Workload, K, V, flags: int = 0, T_cap: int | None = Non
 def prefill_two_call(cache, K, V, n_tok: int, chunk: int = 8192, device="cuda"):
     """Tokens [0, n_tok) of raw K, V [B][Hkv][T][128] into the packed cache
     through the two-call path: oscar_rotate_scale_k into a bf16 staging
-    buffer, then oscar_quantize_kv, in chunks (the cache's flags apply)."""
+    buffer, then oscar_quantize_kv, in chunks (the cache's flags and target
+    norm apply)."""
     import torch
     from . import oscar
     B, Hkv, T_stride = K.shape[0], K.shape[1], K.shape[2]
@@ -174,7 +177,7 @@ def prefill_two_call(cache, K, V, n_tok: int, chunk: int = 8192, device="cuda"):
     for t0 in range(0, n_tok, chunk):
         n = min(chunk, n_tok - t0)
         oscar.rotate_scale_k(_offset(K, t0), stage, norm, B, Hkv, n, in_T=T_stride,
-                             out_T=chunk, flags=cache.flags)
+                             out_T=chunk, flags=cache.flags, norm_target=cache.norm_target)
         vstage[:, :, :n].copy_(V[:, :, t0:t0 + n])
         oscar.quantize_kv(cache, stage, norm, vstage, src_T=chunk, n_tok=n)
 

@@ -43,9 +43,10 @@ def assert_attention_close(gpu, ref, what=""):
     return ma, rl
 
 
-def upload_oracle_cache(cache, heads: dict, flags: int = 0):
+def upload_oracle_cache(cache, heads: dict, flags: int = 0, norm_target: float = 0.0):
     """Writes oracle HeadCaches {(b, h): HeadCache} into a KVCache (same
-    n_packed / n_res for every row), using the oracle's own packing."""
+    n_packed / n_res for every row), using the oracle's own packing; the
+    cache takes the flags and target norm the oracle built them with."""
     P = R = None
     for (b, h), hc in heads.items():
         kq, vq = hc.packed_k(), hc.packed_v()
@@ -71,6 +72,7 @@ def upload_oracle_cache(cache, heads: dict, flags: int = 0):
     cache.struct.n_packed = P or 0
     cache.struct.n_res = R or 0
     cache.struct.flags = flags
+    cache.struct.norm_target = norm_target
     return cache
 
 

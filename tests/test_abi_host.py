@@ -73,6 +73,7 @@ def _cache(**kw):
     for i, name in enumerate(["packed", "k_res", "v_res", "k_res_norm"]):
         setattr(s, name, kw.get(name, FAKE + 0x100000 * i))
     s.n_packed, s.n_res, s.flags = kw.get("n_packed", 0), kw.get("n_res", 0), kw.get("flags", 0)
+    s.norm_target = kw.get("norm_target", 0.0)
     return s
 
 
@@ -83,11 +84,17 @@ def test_rotate_validation():
     P = ctypes.c_void_p
     assert L.oscar_rotate_q(None, P(FAKE), 1, 1, 0, None) == 1
     assert L.oscar_rotate_q(P(FAKE + 8), P(FAKE), 1, 1, 0, None) == 3
-    assert L.oscar_rotate_q(P(FAKE), P(FAKE), 1, 1, 4, None) == 1          # unknown flag
+    assert L.oscar_rotate_q(P(FAKE), P(FAKE), 1, 1, 8, None) == 1          # unknown flag
     assert L.oscar_rotate_q(P(FAKE), P(FAKE), 0, 1, 0, None) == 1
-    assert L.oscar_rotate_scale_k(P(FAKE), 4, P(FAKE), P(FAKE), 8, 6, 1, 1, 4, 0, None) == 1
-    assert L.oscar_rotate_scale_k(P(FAKE), 2, P(FAKE), P(FAKE), 8, 0, 1, 1, 4, 0, None) == 1
-    assert L.oscar_rotate_scale_k(P(FAKE), 4, P(FAKE + 2), P(FAKE), 8, 0, 1, 1, 4, 0, None) == 3
+    assert L.oscar_rotate_scale_k(P(FAKE), 4, P(FAKE), P(FAKE), 8, 6, 1, 1, 4, 0, 0.0, None) == 1
+    assert L.oscar_rotate_scale_k(P(FAKE), 2, P(FAKE), P(FAKE), 8, 0, 1, 1, 4, 0, 0.0, None) == 1
+    assert L.oscar_rotate_scale_k(P(FAKE), 4, P(FAKE + 2), P(FAKE), 8, 0, 1, 1, 4, 0, 0.0,
+                                  None) == 3
+    assert L.oscar_rotate_scale_k(P(FAKE), 4, P(FAKE), P(FAKE), 8, 0, 1, 1, 4, 8, 0.0, None) == 1
+    # target norm outside [2^-8, 2^8], negative or NaN
+    for t in (1e-3, 300.0, -1.0, float("nan"), float("inf")):
+        assert L.oscar_rotate_scale_k(P(FAKE), 4, P(FAKE), P(FAKE), 8, 0, 1, 1, 4, 0, t,
+                                      None) == 1
 
 
 @no_gpu_only
@@ -116,6 +123,14 @@ def test_cache_validation_and_state_untouched():
     assert L.oscar_append_kv(ctypes.byref(st), P(FAKE), P(FAKE), 200, None) == 4
     assert st.n_packed == 128 and st.n_res == 128
     assert c.n_packed == 0 and c.n_res == 0
+    # scaling variants: unknown flag bit, target norm out of range
+    for bad in (_cache(flags=8), _cache(norm_target=512.0), _cache(norm_target=-1.0),
+                _cache(norm_target=float("nan"))):
+        assert L.oscar_prefill_kv(ctypes.byref(bad), P(FAKE), P(FAKE), 64, 64, None) == 1
+        assert L.oscar_append_kv(ctypes.byref(bad), P(FAKE), P(FAKE), 1, None) == 1
+        assert L.oscar_decode_attention_static_ws(ctypes.byref(bad), P(FAKE), 2, 0.1, P(FAKE),
+                                                  1, None) == 1
+        assert bad.n_packed == 0 and bad.n_res == 0
 
 
 @no_gpu_only
@@ -143,6 +158,7 @@ def _paged(**kw):
                               "k_res_norm"]):
         setattr(s, name, kw.get(name, FAKE + 0x100000 * i))
     s.flags = kw.get("flags", 0)
+    s.norm_target = kw.get("norm_target", 0.0)
     return s
 
 
@@ -155,6 +171,8 @@ def test_paged_validation():
     assert L.oscar_paged_append_kv(ctypes.byref(bad), P(FAKE), P(FAKE), None, None) == 1
     mis = _paged(pages=FAKE + 8)
     assert L.oscar_paged_append_kv(ctypes.byref(mis), P(FAKE), P(FAKE), None, None) == 3
+    for bad in (_paged(flags=8), _paged(norm_target=1e-3)):
+        assert L.oscar_paged_append_kv(ctypes.byref(bad), P(FAKE), P(FAKE), None, None) == 1
     c = _paged()
     assert L.oscar_paged_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 64, P(FAKE), 48, None) == 1
     assert L.oscar_paged_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 512, P(FAKE), 512,

@@ -104,7 +104,8 @@ def test_paged_decode_matches_oracle(L, g):
             assert_attention_close(got[b], ref, f"sequence {b}, splits {S}")
 
 
-def test_paged_prefill_and_append_equal_contiguous(L):
+@pytest.mark.parametrize("flags, target", [(0, 0.0), (O.NORM_ALL_HEADS, 0.37)])
+def test_paged_prefill_and_append_equal_contiguous(L, flags, target):
     Hkv = 2
     prompts = [(1024, 40), (640, 0), (0, 0), (96, 130)]   # (prefill tokens, appended tokens)
     steps = 140                                           # decode steps after the prompt
@@ -115,7 +116,8 @@ def test_paged_prefill_and_append_equal_contiguous(L):
     v = synth.gen_bf16(1101, Hkv, range(B), range(Hkv), 0, T_all)
     kd, vd = bits_to_bf16_tensor(k), bits_to_bf16_tensor(v)
     max_blocks = (T_all + 127) // 32 + 8
-    paged = L.PagedKVCache(B, Hkv, max_blocks, n_pages=B * max_blocks)
+    paged = L.PagedKVCache(B, Hkv, max_blocks, n_pages=B * max_blocks, flags=flags,
+                           norm_target=target)
     rng = np.random.default_rng(7)
     paged.map_blocks(0, 0, order=list(rng.permutation(B * max_blocks)))
     for b in range(B):
@@ -125,7 +127,7 @@ def test_paged_prefill_and_append_equal_contiguous(L):
     L.paged_prefill_kv(paged, kd, vd, n_tok, max_tok, in_T=T_all)
     conts = []
     for b, (p, a) in enumerate(prompts):
-        c = L.KVCache(1, Hkv, max_blocks * 32)
+        c = L.KVCache(1, Hkv, max_blocks * 32, flags=flags, norm_target=target)
         if p:
             L.prefill_kv(c, kd[b:b + 1].contiguous(), vd[b:b + 1].contiguous(), n_tok=p, in_T=T_all)
         conts.append(c)
