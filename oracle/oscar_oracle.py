@@ -150,7 +150,8 @@ def rotate_scale_k(k_bits: np.ndarray, flags: int = 0, target: float = 1.0) -> R
 
 # --------------------------------------------------------------------------
 # INT2 quantiser ([rainbus] 前置知识 per-channel quantisation with step Δ and
-# zero z; 方法步骤详情: K per-channel blocks of G=32, V per token)
+# zero z; 方法步骤详情: K per-channel blocks of G=32 tokens (larger groups as
+# an option), V per token)
 # --------------------------------------------------------------------------
 
 def quantize_groups(x: np.ndarray):
@@ -178,8 +179,15 @@ def quantize_groups(x: np.ndarray):
 @dataclass
 class QuantK:
     codes: np.ndarray    # uint8 [n][128]
-    step16: np.ndarray   # float16 [n/32][128]
-    zero16: np.ndarray   # float16 [n/32][128]
+    step16: np.ndarray   # float16 [n/group][128]
+    zero16: np.ndarray   # float16 [n/group][128]
+    group: int = G       # tokens sharing a channel's step and zero
+
+    def block_params(self):
+        """(step16, zero16) per 32-token block, as the cache's records carry
+        them: each group's parameters repeated over its group/32 blocks."""
+        r = self.group // G
+        return np.repeat(self.step16, r, axis=0), np.repeat(self.zero16, r, axis=0)
 
 
 @dataclass
@@ -189,19 +197,21 @@ class QuantV:
     zero16: np.ndarray   # float16 [n]
 
 
-def quantize_k(k_hat_bits: np.ndarray) -> QuantK:
-    """Block-wise per-channel INT2 for keys [n][128], n a multiple of 32.
+def quantize_k(k_hat_bits: np.ndarray, group: int = G) -> QuantK:
+    """Block-wise per-channel INT2 for keys [n][128], n a multiple of group.
 
-    Each channel of each block of G=32 consecutive tokens has its own step
-    and zero ([rainbus] 方法步骤详情 item (2); [notes] Notation).
+    Each channel of each group of ``group`` consecutive tokens has its own
+    step and zero ([rainbus] 方法步骤详情 item (2); [notes] Notation).  The
+    pages use groups of 32; 64 and 128 are the larger groups that [rainbus]
+    局限与改进 (1) lists as not studied.
     """
     n = k_hat_bits.shape[0]
-    assert n % G == 0
+    assert group in (32, 64, 128) and n % group == 0
     x = bf16_to_f64(k_hat_bits).astype(np.float32)          # exact
-    xb = x.reshape(n // G, G, D).transpose(0, 2, 1)          # [blk][ch][tok]
+    xb = x.reshape(n // group, group, D).transpose(0, 2, 1)  # [grp][ch][tok]
     codes, step, zero = quantize_groups(xb)
     return QuantK(codes.transpose(0, 2, 1).reshape(n, D).copy(),
-                  f_to_f16(step), f_to_f16(zero))
+                  f_to_f16(step), f_to_f16(zero), group)
 
 
 def quantize_v(v_bits: np.ndarray) -> QuantV:
@@ -216,8 +226,8 @@ def dequant_k(q: QuantK, norm16: np.ndarray) -> np.ndarray:
     inverse quantisation followed by the inverse token scaling ([notes]
     End-to-End Flow, "dequantized and inverse-scaled")."""
     n = q.codes.shape[0]
-    s = np.repeat(q.step16.astype(np.float64), G, axis=0)
-    z = np.repeat(q.zero16.astype(np.float64), G, axis=0)
+    s = np.repeat(q.step16.astype(np.float64), q.group, axis=0)
+    z = np.repeat(q.zero16.astype(np.float64), q.group, axis=0)
     return (q.codes.astype(np.float64) * s + z) * norm16.astype(np.float64)[:n, None]
 
 
@@ -303,6 +313,7 @@ def bf16_attention(q_bits, k_bits, v_bits, tau: float) -> np.ndarray:
 class HeadCache:
     flags: int = 0
     target: float = 1.0
+    group: int = G       # key group size (tokens sharing step and zero)
     k_codes: list = field(default_factory=list)   # QuantK per quantised chunk
     k_norm16: list = field(default_factory=list)
     v_q: list = field(default_factory=list)
@@ -320,7 +331,7 @@ class HeadCache:
 
     def quantize_prefix(self, k_raw_bits: np.ndarray, v_bits: np.ndarray):
         """Rotate, scale and quantise a block-aligned run of tokens."""
-        assert k_raw_bits.shape[0] % G == 0
+        assert k_raw_bits.shape[0] % self.group == 0
         rk = self._rotate(k_raw_bits)
         self._pack(rk.k_hat_bf16, rk.norm_f16, v_bits)
 
@@ -330,7 +341,7 @@ class HeadCache:
         return rotate_scale_k(k_raw_bits, self.flags, self.target)
 
     def _pack(self, k_hat_bits, norm16, v_bits):
-        self.k_codes.append(quantize_k(k_hat_bits))
+        self.k_codes.append(quantize_k(k_hat_bits, self.group))
         self.k_norm16.append(np.asarray(norm16, dtype=np.float16))
         self.v_q.append(quantize_v(v_bits))
 
@@ -371,10 +382,10 @@ class HeadCache:
     def packed_k(self) -> QuantK:
         if not self.k_codes:
             return QuantK(np.zeros((0, D), np.uint8), np.zeros((0, D), np.float16),
-                          np.zeros((0, D), np.float16))
+                          np.zeros((0, D), np.float16), self.group)
         return QuantK(np.concatenate([q.codes for q in self.k_codes]),
                       np.concatenate([q.step16 for q in self.k_codes]),
-                      np.concatenate([q.zero16 for q in self.k_codes]))
+                      np.concatenate([q.zero16 for q in self.k_codes]), self.group)
 
     def packed_norm16(self) -> np.ndarray:
         if not self.k_norm16:
@@ -407,12 +418,13 @@ class HeadCache:
 
 
 def build_head_cache(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
-                     target: float = 1.0) -> HeadCache:
-    """Prompt of T tokens: the first ``n_packed`` (a multiple of 32) are
-    quantised, the remaining T - n_packed (at most 128) stay in the residual."""
+                     target: float = 1.0, group: int = G) -> HeadCache:
+    """Prompt of T tokens: the first ``n_packed`` (a multiple of the key
+    group) are quantised, the remaining T - n_packed (at most 128) stay in the
+    residual."""
     T = k_raw_bits.shape[0]
-    assert n_packed % G == 0 and 0 <= T - n_packed <= R
-    c = HeadCache(flags=flags, target=target)
+    assert n_packed % group == 0 and 0 <= T - n_packed <= R
+    c = HeadCache(flags=flags, target=target, group=group)
     if n_packed:
         c.quantize_prefix(k_raw_bits[:n_packed], v_bits[:n_packed])
     if T > n_packed:
@@ -421,17 +433,17 @@ def build_head_cache(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
 
 
 def build_row_caches(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
-                     target: float = 1.0) -> list:
+                     target: float = 1.0, group: int = G) -> list:
     """build_head_cache for every KV head of one sequence, k_raw_bits and
     v_bits [Hkv][T][128]: the keys of all heads are rotated and scaled
     together, which the all-heads norm needs, then each head is quantised
     and filled on its own."""
     Hkv, T = k_raw_bits.shape[0], k_raw_bits.shape[1]
-    assert n_packed % G == 0 and 0 <= T - n_packed <= R
+    assert n_packed % group == 0 and 0 <= T - n_packed <= R
     rk = rotate_scale_k(k_raw_bits, flags, target)
     caches = []
     for h in range(Hkv):
-        c = HeadCache(flags=flags, target=target)
+        c = HeadCache(flags=flags, target=target, group=group)
         if n_packed:
             c._pack(rk.k_hat_bf16[h, :n_packed], rk.norm_f16[h, :n_packed], v_bits[h, :n_packed])
         if T > n_packed:
