@@ -114,10 +114,12 @@ typedef struct {
   oscar_bf16* k_res;
   oscar_bf16* v_res;
   oscar_f16* k_res_norm;
-  int n_packed;      /* quantised tokens per row, multiple of 32 */
+  int n_packed;      /* quantised tokens per row, multiple of the key group */
   int n_res;         /* residual tokens per row, 0..128 */
   unsigned flags;    /* OSCAR_NO_ROTATE / OSCAR_NO_SCALE / OSCAR_NORM_ALL_HEADS, fixed for the cache's life */
   float norm_target; /* target norm of the scaled keys (0 = 1), fixed for the cache's life */
+  int key_group;     /* tokens sharing a key channel's step and zero: 32 (0), 64 or 128;
+                        n_packed and every quantised run are multiples of it */
 } oscar_cache;
 
 /*
@@ -130,7 +132,7 @@ typedef struct {
  * caller owns the page pool and the table and must map a block before a
  * call writes it.  Lengths are per sequence and live in device memory, so a
  * step needs no host round trip:
- *  n_packed[b]  quantised tokens of sequence b (multiple of 32)
+ *  n_packed[b]  quantised tokens of sequence b (multiple of the key group)
  *  n_res[b]     its residual tokens, 0..128
  * The residual window stays per (b, h) as in oscar_cache.
  */
@@ -147,6 +149,7 @@ typedef struct {
   oscar_f16* k_res_norm;    /* [B][Hkv][128] */
   unsigned flags;
   float norm_target;
+  int key_group;            /* as in oscar_cache */
 } oscar_paged_cache;
 
 /*
@@ -183,8 +186,11 @@ oscar_status oscar_rotate_scale_k(const oscar_bf16* k, int in_T,
 
 /*
  * Quantisation kernel (2) of [news] 三: keys as block-wise per-channel INT2
- * (each channel's step and zero shared by 32 consecutive tokens), values as
- * per-token INT2 ([rainbus] 方法步骤详情 (2)(3)).  Per group: zero = min,
+ * (each channel's step and zero shared by c->key_group consecutive tokens:
+ * 32, or the larger groups 64 and 128 that [rainbus] 局限与改进 (1) names as
+ * untested; every 32-token record of a group carries the group's step and
+ * zero), values as per-token INT2 ([rainbus] 方法步骤详情 (2)(3)).  Per
+ * group: zero = min,
  * step = (max - min)/3 in fp32, code = round-half-even((x - zero)/step)
  * clamped to [0,3] (0 when max == min); step and zero stored as fp16.
  * Tokens [0, n_tok) of each (b,h) row of the sources are written to packed
@@ -195,7 +201,7 @@ oscar_status oscar_rotate_scale_k(const oscar_bf16* k, int in_T,
  * Flush mode: k_hat == k_norm == v == NULL quantises the full residual window
  * (requires c->n_res == 128, src_T and n_tok ignored) and sets c->n_res = 0
  * ([news] 三: batch quantisation once 128 tokens have accumulated).
- * Requires n_tok % 32 == 0, n_tok >= 32, src_T >= n_tok, c->n_res == 0 in
+ * Requires n_tok a multiple of the key group, src_T >= n_tok, c->n_res == 0 in
  * non-flush mode (packed tokens precede residual ones) and
  * c->n_packed + n_tok <= c->T_cap (else OSCAR_ERR_CAPACITY).
  */
@@ -213,7 +219,7 @@ oscar_status oscar_quantize_kv(oscar_cache* c, const oscar_bf16* k_hat, const os
  * c->n_packed += n_tok; the rotation and scaling flags are c->flags.
  *  k  bf16 [B][Hkv][in_T][128] raw keys (row stride in_T tokens)
  *  v  bf16 [B][Hkv][in_T][128] values
- * Requires n_tok % 32 == 0, n_tok >= 32, in_T >= n_tok, c->n_res == 0 and
+ * Requires n_tok a multiple of the key group, in_T >= n_tok, c->n_res == 0 and
  * c->n_packed + n_tok <= c->T_cap (else OSCAR_ERR_CAPACITY); pointers
  * 16-byte aligned.
  */
@@ -318,7 +324,7 @@ oscar_status oscar_device_status(void* stream);
  * k, v bf16 [B][Hkv][in_T][128]: sequence b's tokens [0, n_tok[b]) are
  * rotated, scaled, quantised and written to its logical blocks
  * n_packed[b]/32 .. onwards; then n_packed[b] += n_tok[b].  n_tok: device
- * int32 [B], each a multiple of 32 and <= max_tok (a host bound sizing the
+ * int32 [B], each a multiple of the key group and <= max_tok (a host bound sizing the
  * launch, <= in_T); requires n_res[b] == 0 for sequences with n_tok[b] > 0.
  *
  * oscar_paged_append_kv: one new token (k_new, v_new bf16 [B][Hkv][128])

@@ -48,6 +48,8 @@ oscar_status check_cache(const oscar_cache* c) {
     return OSCAR_ERR_INVALID_ARG;
   if (c->n_res < 0 || c->n_res > kR) return OSCAR_ERR_INVALID_ARG;
   if ((c->flags & ~kAllFlags) || !target_ok(c->norm_target)) return OSCAR_ERR_INVALID_ARG;
+  if (!key_group_ok(c->key_group) || c->n_packed % key_group(c->key_group) != 0)
+    return OSCAR_ERR_INVALID_ARG;
   return OSCAR_OK;
 }
 
@@ -116,7 +118,7 @@ oscar_status flush_residual(oscar_cache* c, cudaStream_t s) {
   if (c->n_packed + kR > c->T_cap) return OSCAR_ERR_CAPACITY;
   cudaError_t e = launch_quantize_kv(
       c->k_res, reinterpret_cast<const __half*>(c->k_res_norm), c->v_res, kR, kR, c->B, c->Hkv,
-      c->T_cap, c->n_packed, c->packed, s);
+      c->T_cap, c->n_packed, key_group(c->key_group), c->packed, s);
   g_launches++;
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   c->n_packed += kR;
@@ -173,12 +175,13 @@ oscar_status oscar_quantize_kv(oscar_cache* c, const oscar_bf16* k_hat, const os
   }
   if (!k_hat || !k_norm || !v) return OSCAR_ERR_INVALID_ARG;
   if (!al16(k_hat) || !al16(k_norm) || !al16(v)) return OSCAR_ERR_ALIGNMENT;
-  if (n_tok < kG || n_tok % kG != 0 || src_T < n_tok) return OSCAR_ERR_INVALID_ARG;
+  const int G = key_group(c->key_group);
+  if (n_tok < G || n_tok % G != 0 || src_T < n_tok) return OSCAR_ERR_INVALID_ARG;
   if (c->n_res != 0) return OSCAR_ERR_INVALID_ARG;  // packed tokens must precede residual ones
   if ((long long)c->n_packed + n_tok > c->T_cap) return OSCAR_ERR_CAPACITY;
   cudaError_t e = launch_quantize_kv(
       k_hat, reinterpret_cast<const __half*>(k_norm), v, src_T, n_tok, c->B, c->Hkv, c->T_cap,
-      c->n_packed, c->packed, as_stream(stream));
+      c->n_packed, G, c->packed, as_stream(stream));
   g_launches++;
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   c->n_packed += n_tok;
@@ -191,10 +194,11 @@ oscar_status oscar_prefill_kv(oscar_cache* c, const oscar_bf16* k, const oscar_b
   if (st != OSCAR_OK) return st;
   if (!k || !v) return OSCAR_ERR_INVALID_ARG;
   if (!al16(k) || !al16(v)) return OSCAR_ERR_ALIGNMENT;
-  if (n_tok < kG || n_tok % kG != 0 || in_T < n_tok) return OSCAR_ERR_INVALID_ARG;
+  const int G = key_group(c->key_group);
+  if (n_tok < G || n_tok % G != 0 || in_T < n_tok) return OSCAR_ERR_INVALID_ARG;
   if (c->n_res != 0) return OSCAR_ERR_INVALID_ARG;  // packed tokens must precede residual ones
   if ((long long)c->n_packed + n_tok > c->T_cap) return OSCAR_ERR_CAPACITY;
-  cudaError_t e = launch_prefill_kv(k, v, in_T, n_tok, c->B, c->Hkv, c->T_cap, c->n_packed,
+  cudaError_t e = launch_prefill_kv(k, v, in_T, n_tok, c->B, c->Hkv, c->T_cap, c->n_packed, G,
                                     key_scale(c->flags, c->norm_target), c->packed,
                                     as_stream(stream));
   g_launches++;
@@ -313,7 +317,8 @@ oscar_status check_paged(const oscar_paged_cache* c) {
     if (!p) return OSCAR_ERR_INVALID_ARG;
     if (!al4(p)) return OSCAR_ERR_ALIGNMENT;
   }
-  if ((c->flags & ~kAllFlags) || !target_ok(c->norm_target)) return OSCAR_ERR_INVALID_ARG;
+  if ((c->flags & ~kAllFlags) || !target_ok(c->norm_target) || !key_group_ok(c->key_group))
+    return OSCAR_ERR_INVALID_ARG;
   return OSCAR_OK;
 }
 
@@ -332,6 +337,7 @@ PagedArgs paged_args(const oscar_paged_cache* c) {
   p.max_blocks = c->max_blocks;
   p.n_pages = c->n_pages;
   p.ks = key_scale(c->flags, c->norm_target);
+  p.group = key_group(c->key_group);
   return p;
 }
 
@@ -346,7 +352,8 @@ oscar_status oscar_paged_prefill_kv(oscar_paged_cache* c, const oscar_bf16* k,
   if (st != OSCAR_OK) return st;
   if (!k || !v || !n_tok) return OSCAR_ERR_INVALID_ARG;
   if (!al16(k) || !al16(v) || !al4(n_tok)) return OSCAR_ERR_ALIGNMENT;
-  if (max_tok < kG || max_tok % kG != 0 || in_T < max_tok) return OSCAR_ERR_INVALID_ARG;
+  const int G = key_group(c->key_group);
+  if (max_tok < G || max_tok % G != 0 || in_T < max_tok) return OSCAR_ERR_INVALID_ARG;
   if (max_tok / kG > c->max_blocks) return OSCAR_ERR_CAPACITY;
   const PagedArgs p = paged_args(c);
   if (!p.status) return OSCAR_ERR_CUDA;

@@ -66,7 +66,8 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
     if (!aligned16(p)) return OSCAR_ERR_ALIGNMENT;
   }
   if (c->n_packed < 0 || c->n_packed % kG != 0 || c->n_packed > c->T_cap || c->n_res < 0 ||
-      c->n_res > kR || (c->flags & ~kAllFlags) || !target_ok(c->norm_target))
+      c->n_res > kR || (c->flags & ~kAllFlags) || !target_ok(c->norm_target) ||
+      !key_group_ok(c->key_group))
     return OSCAR_ERR_INVALID_ARG;
   if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
       !std::isfinite(softmax_scale))

@@ -25,6 +25,9 @@ constexpr unsigned kAllFlags = OSCAR_NO_ROTATE | OSCAR_NO_SCALE | OSCAR_NORM_ALL
 inline bool target_ok(float t) {
   return t == 0.0f || (t >= 0.00390625f && t <= 256.0f);   // false for NaN
 }
+// Key group size as the ABI takes it: 0 means 32; otherwise 32, 64 or 128.
+inline bool key_group_ok(int g) { return g == 0 || g == 32 || g == 64 || g == 128; }
+inline int key_group(int g) { return g == 0 ? 32 : g; }
 inline KeyScale key_scale(unsigned flags, float target) {
   return KeyScale{flags, target == 0.0f ? 1.0f : target};
 }
@@ -50,8 +53,10 @@ cudaError_t launch_rotate_scale_k(const uint16_t* k, int in_T, uint16_t* k_hat, 
 
 // Quantises tokens [0, n_tok) of each source row into the block records of
 // packed positions [p0, p0 + n_tok).
+// Keys are grouped by `group` tokens (32, 64 or 128; n_tok and p0 multiples
+// of it): every channel of a group shares one step and zero.
 cudaError_t launch_quantize_kv(const uint16_t* k_hat, const __half* k_norm, const uint16_t* v,
-                               int src_T, int n_tok, int B, int Hkv, int T_cap, int p0,
+                               int src_T, int n_tok, int B, int Hkv, int T_cap, int p0, int group,
                                uint8_t* packed, cudaStream_t s);
 
 struct DecodeArgs {
@@ -118,6 +123,7 @@ struct PagedArgs {
   __half* k_res_norm;
   unsigned* status;
   int B, Hkv, max_blocks, n_pages;
+  int group;   // key group size: 32, 64 or 128 tokens
   KeyScale ks;
 };
 cudaError_t launch_paged_prefill(const PagedArgs& p, const uint16_t* k, const uint16_t* v,
@@ -127,7 +133,7 @@ cudaError_t launch_paged_append(const PagedArgs& p, const uint16_t* k_new, const
 
 // Fused rotate + scale + quantise of n_tok tokens of raw keys and values.
 cudaError_t launch_prefill_kv(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,
-                              int Hkv, int T_cap, int p0, KeyScale ks, uint8_t* packed,
+                              int Hkv, int T_cap, int p0, int group, KeyScale ks, uint8_t* packed,
                               cudaStream_t s);
 
 // One CTA polls an mbarrier nothing arrives at, `iterations` times, then

@@ -20,78 +20,107 @@
 
 namespace oscar {
 
+// Shared memory of the group kernels: the GS keys of one group (rotated,
+// scaled, bf16) and their norms stay for the whole group; values and codes
+// are staged one 32-token block at a time.
+template <int GS>
+struct GroupSmem {
+  uint16_t kt[GS][kD];
+  uint16_t vt[kG][kD];
+  uint8_t kc[kG][kD];
+  uint8_t vc[kG][kD];
+  __half ns[GS];
+};
+
+// Copies 32 value rows (bf16, 256 B each) into vt: 16 B per thread per step.
+__device__ __forceinline__ void stage_values(uint16_t (&vt)[kG][kD], const uint16_t* v) {
+  const uint4* vs = reinterpret_cast<const uint4*>(v);
+  uint4* vd = reinterpret_cast<uint4*>(&vt[0][0]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) vd[threadIdx.x + 128 * i] = vs[threadIdx.x + 128 * i];
+}
+
+// The group's GS/32 records, one block at a time, with the group's key
+// parameters.  On entry kt and the norms for GS tokens and the values of
+// block 0 (staged first, so that their loads overlap the key work) are in
+// place and synced.  rec_of(s) gives block s's record; values of block s at
+// v_src + 32 s rows.
+template <int GS, class RecOf>
+__device__ __forceinline__ void quantize_group(GroupSmem<GS>& S, const __half* norms,
+                                               const uint16_t* v_src, RecOf rec_of) {
+  const KeyParams kp = key_params<GS>(S.kt);
+  quantize_block(&S.kt[0], S.vt, S.kc, S.vc, norms, rec_of(0), kp);
+  if constexpr (GS > kG) {
+#pragma unroll 1
+    for (int sb = 1; sb < GS / kG; ++sb) {
+      stage_values(S.vt, v_src + (long long)sb * kG * kD);
+      __syncthreads();   // also: every thread is done packing the previous block
+      quantize_block(&S.kt[kG * sb], S.vt, S.kc, S.vc, norms + kG * sb, rec_of(sb), kp);
+    }
+  }
+}
+
+// Quantises tokens [0, n_tok) of each source row (rotated, scaled keys k_hat
+// with their norms, and values) into the records of packed positions
+// [p0, p0 + n_tok): CTA (j, h, b) handles group j.
+template <int GS>
 __global__ void __launch_bounds__(128) quantize_kv_kernel(
     const uint16_t* __restrict__ k_hat, const __half* __restrict__ k_norm,
     const uint16_t* __restrict__ v, int src_T, int Hkv, int T_cap, int p0,
     uint8_t* __restrict__ packed) {
-  __shared__ __align__(16) uint16_t kt[kG][kD];
-  __shared__ __align__(16) uint16_t vt[kG][kD];
-  __shared__ __align__(16) uint8_t kc[kG][kD];
-  __shared__ __align__(16) uint8_t vc[kG][kD];
-
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  auto& S = *reinterpret_cast<GroupSmem<GS>*>(smem_raw);
   const int tid = threadIdx.x;
-  const int blk = blockIdx.x;
+  const int j = blockIdx.x;
   const long long row = (long long)blockIdx.z * Hkv + blockIdx.y;
-  const long long src_tok = row * src_T + (long long)blk * kG;
-
-  // Stage both tiles: 32 tokens x 256 B each, 16 B per thread per step.
+  const long long src_tok = row * src_T + (long long)j * GS;
+  stage_values(S.vt, v + src_tok * kD);
   {
     const uint4* ks = reinterpret_cast<const uint4*>(k_hat + src_tok * kD);
-    const uint4* vs = reinterpret_cast<const uint4*>(v + src_tok * kD);
-    uint4* kd = reinterpret_cast<uint4*>(&kt[0][0]);
-    uint4* vd = reinterpret_cast<uint4*>(&vt[0][0]);
+    uint4* kd = reinterpret_cast<uint4*>(&S.kt[0][0]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kd[tid + 128 * i] = ks[tid + 128 * i];
-      vd[tid + 128 * i] = vs[tid + 128 * i];
-    }
+    for (int i = 0; i < GS / 8; ++i) kd[tid + 128 * i] = ks[tid + 128 * i];
   }
   __syncthreads();
-
-  const long long pblk = (long long)p0 / kG + blk;   // packed block index in the row
-  quantize_block(kt, vt, kc, vc, k_norm + src_tok, packed + (row * (T_cap / kG) + pblk) * kBlkBytes);
+  uint8_t* row_rec = packed + (row * (T_cap / kG) + p0 / kG + (long long)j * (GS / kG)) * kBlkBytes;
+  quantize_group<GS>(S, k_norm + src_tok, v + src_tok * kD,
+                     [&](int sb) { return row_rec + (long long)sb * kBlkBytes; });
 }
 
-// Fused prefill: raw keys and values of n_tok tokens -> block records.  Warp w
-// rotates and scales tokens 8w..8w+7 of the block (one token per warp step,
-// as rotate_scale_k_kernel does), rounds k_hat to bf16 into the tile, keeps
-// the norms in shared memory; the values are staged as in quantize_kv_kernel.
+// Fused prefill: raw keys and values of n_tok tokens -> block records.  CTA
+// (j, h, b) handles group j: warp w rotates and scales tokens w, w + 4, ...
+// of the group (one token per warp step, as rotate_scale_k_kernel does),
+// rounds k_hat to bf16 into the key tile and keeps the norms in shared
+// memory; then the group's records are quantised block by block.
+template <int GS, bool PLAIN>
 __global__ void __launch_bounds__(128) prefill_kv_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int in_T, int Hkv,
     int T_cap, int p0, KeyScale ks, uint8_t* __restrict__ packed) {
-  __shared__ __align__(16) uint16_t kt[kG][kD];
-  __shared__ __align__(16) uint16_t vt[kG][kD];
-  __shared__ __align__(16) uint8_t kc[kG][kD];
-  __shared__ __align__(16) uint8_t vc[kG][kD];
-  __shared__ __half ns[kG];
-
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  auto& S = *reinterpret_cast<GroupSmem<GS>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int blk = blockIdx.x;
+  const int j = blockIdx.x;
   const long long row = (long long)blockIdx.z * Hkv + blockIdx.y;
-  const long long src_tok = row * in_T + (long long)blk * kG;
-  {
-    const uint4* vs = reinterpret_cast<const uint4*>(v + src_tok * kD);
-    uint4* vd = reinterpret_cast<uint4*>(&vt[0][0]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vd[tid + 128 * i] = vs[tid + 128 * i];
-  }
+  const long long src_tok = row * in_T + (long long)j * GS;
+  stage_values(S.vt, v + src_tok * kD);
   // with the all-heads norm, head 0 of this sequence's token src_tok
   const long long head0_tok = src_tok - (long long)blockIdx.y * in_T;
 #pragma unroll 2
-  for (int i = 0; i < 8; ++i) {
-    const int t = 8 * warp + i;
+  for (int i = 0; i < GS / 4; ++i) {
+    const int t = (GS / 4) * warp + i;
     float s_all = 0.0f;
-    if (ks.flags & OSCAR_NORM_ALL_HEADS)
+    if (!PLAIN && (ks.flags & OSCAR_NORM_ALL_HEADS))
       s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, Hkv, lane);
     const uint2 raw = reinterpret_cast<const uint2*>(k + (src_tok + t) * kD)[lane];
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    const float norm = rotate_scale_key(x, lane, ks, s_all);
-    reinterpret_cast<uint2*>(&kt[t][0])[lane] = pack_bf16x4(x);
-    if (lane == 0) ns[t] = __float2half_rn(norm);
+    const float norm = rotate_scale_key<PLAIN>(x, lane, ks, s_all);
+    reinterpret_cast<uint2*>(&S.kt[t][0])[lane] = pack_bf16x4(x);
+    if (lane == 0) S.ns[t] = __float2half_rn(norm);
   }
   __syncthreads();
-  const long long pblk = (long long)p0 / kG + blk;
-  quantize_block(kt, vt, kc, vc, ns, packed + (row * (T_cap / kG) + pblk) * kBlkBytes);
+  uint8_t* row_rec = packed + (row * (T_cap / kG) + p0 / kG + (long long)j * (GS / kG)) * kBlkBytes;
+  quantize_group<GS>(S, S.ns, v + src_tok * kD,
+                     [&](int sb) { return row_rec + (long long)sb * kBlkBytes; });
 }
 
 // ------------------------------------------------------------------ paged
@@ -104,90 +133,86 @@ __device__ __forceinline__ uint8_t* paged_record(const PagedArgs& p, int b, int 
   return p.pages + ((long long)page * p.Hkv + h) * kBlkBytes;
 }
 
-// Fused prefill into pages: CTA (j, h, b) handles tokens 32j..32j+31 of
-// sequence b when 32j < n_tok[b]; they become logical block
-// seq_packed[b]/32 + j.  Lengths are updated by paged_lengths_kernel after.
+// Fused prefill into pages: CTA (j, h, b) handles group j (tokens
+// GS j .. GS j + GS - 1) of sequence b when GS j < n_tok[b]; its blocks become
+// logical blocks seq_packed[b]/32 + (GS/32) j + s.  Lengths are updated by
+// paged_lengths_kernel after.
+template <int GS, bool PLAIN>
 __global__ void __launch_bounds__(128) paged_prefill_kernel(PagedArgs p,
                                                             const uint16_t* __restrict__ k,
                                                             const uint16_t* __restrict__ v,
                                                             int in_T, const int32_t* n_tok,
                                                             int max_tok) {
-  __shared__ __align__(16) uint16_t kt[kG][kD];
-  __shared__ __align__(16) uint16_t vt[kG][kD];
-  __shared__ __align__(16) uint8_t kc[kG][kD];
-  __shared__ __align__(16) uint8_t vc[kG][kD];
-  __shared__ __half ns[kG];
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  auto& S = *reinterpret_cast<GroupSmem<GS>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int n = n_tok[b], p0 = p.seq_packed[b];
   if (n == 0) return;
-  if (n < 0 || n % kG != 0 || n > max_tok || p0 < 0 || p0 % kG != 0 || p.seq_res[b] != 0) {
+  if (n < 0 || n % GS != 0 || n > max_tok || p0 < 0 || p0 % GS != 0 || p.seq_res[b] != 0) {
     if (j == 0 && h == 0 && tid == 0) record_error(p.status, kDevErrBadPaged);
     return;
   }
-  if (kG * j >= n) return;
-  uint8_t* rec = paged_record(p, b, p0 / kG + j, h);
-  if (rec == nullptr) {
-    if (tid == 0) record_error(p.status, kDevErrBadPaged);
-    return;
+  if (GS * j >= n) return;
+  const int lb0 = p0 / kG + j * (GS / kG);
+  for (int sb = 0; sb < GS / kG; ++sb) {   // every block of the group mapped
+    if (paged_record(p, b, lb0 + sb, h) == nullptr) {
+      if (tid == 0) record_error(p.status, kDevErrBadPaged);
+      return;
+    }
   }
-  const long long src_tok = ((long long)b * p.Hkv + h) * in_T + (long long)j * kG;
-  {
-    const uint4* vs = reinterpret_cast<const uint4*>(v + src_tok * kD);
-    uint4* vd = reinterpret_cast<uint4*>(&vt[0][0]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vd[tid + 128 * i] = vs[tid + 128 * i];
-  }
+  const long long src_tok = ((long long)b * p.Hkv + h) * in_T + (long long)j * GS;
+  stage_values(S.vt, v + src_tok * kD);
   const long long head0_tok = src_tok - (long long)h * in_T;
 #pragma unroll 2
-  for (int i = 0; i < 8; ++i) {
-    const int t = 8 * warp + i;
+  for (int i = 0; i < GS / 4; ++i) {
+    const int t = (GS / 4) * warp + i;
     float s_all = 0.0f;
-    if (p.ks.flags & OSCAR_NORM_ALL_HEADS)
+    if (!PLAIN && (p.ks.flags & OSCAR_NORM_ALL_HEADS))
       s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, p.Hkv, lane);
     const uint2 raw = reinterpret_cast<const uint2*>(k + (src_tok + t) * kD)[lane];
     float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    const float norm = rotate_scale_key(x, lane, p.ks, s_all);
-    reinterpret_cast<uint2*>(&kt[t][0])[lane] = pack_bf16x4(x);
-    if (lane == 0) ns[t] = __float2half_rn(norm);
+    const float norm = rotate_scale_key<PLAIN>(x, lane, p.ks, s_all);
+    reinterpret_cast<uint2*>(&S.kt[t][0])[lane] = pack_bf16x4(x);
+    if (lane == 0) S.ns[t] = __float2half_rn(norm);
   }
   __syncthreads();
-  quantize_block(kt, vt, kc, vc, ns, rec);
+  quantize_group<GS>(S, S.ns, v + src_tok * kD,
+                     [&](int sb) { return paged_record(p, b, lb0 + sb, h); });
 }
 
-// Flush of full residual windows: CTA (j, h, b) quantises residual tokens
-// 32j..32j+31 of (b, h) into logical block seq_packed[b]/32 + j when sequence
-// b is active and its window is full.
+// Flush of full residual windows: CTA (j, h, b) quantises residual group j
+// (tokens GS j .. GS j + GS - 1) of (b, h) into logical blocks
+// seq_packed[b]/32 + (GS/32) j + s when sequence b is active and its window
+// is full.
+template <int GS>
 __global__ void __launch_bounds__(128) paged_flush_kernel(PagedArgs p, const int32_t* active) {
-  __shared__ __align__(16) uint16_t kt[kG][kD];
-  __shared__ __align__(16) uint16_t vt[kG][kD];
-  __shared__ __align__(16) uint8_t kc[kG][kD];
-  __shared__ __align__(16) uint8_t vc[kG][kD];
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  auto& S = *reinterpret_cast<GroupSmem<GS>*>(smem_raw);
   const int tid = threadIdx.x;
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   if (active && active[b] == 0) return;
   if (p.seq_res[b] != kR) return;
   const int p0 = p.seq_packed[b];
-  uint8_t* rec = (p0 >= 0 && p0 % kG == 0) ? paged_record(p, b, p0 / kG + j, h) : nullptr;
-  if (rec == nullptr) {
+  const int lb0 = p0 / kG + j * (GS / kG);
+  bool ok = p0 >= 0 && p0 % GS == 0;
+  for (int sb = 0; ok && sb < GS / kG; ++sb) ok = paged_record(p, b, lb0 + sb, h) != nullptr;
+  if (!ok) {
     if (tid == 0) record_error(p.status, kDevErrBadPaged);
     return;
   }
   const long long row = (long long)b * p.Hkv + h;
-  const long long src_tok = row * kR + (long long)j * kG;
+  const long long src_tok = row * kR + (long long)j * GS;
+  stage_values(S.vt, p.v_res + src_tok * kD);
   {
     const uint4* ks = reinterpret_cast<const uint4*>(p.k_res + src_tok * kD);
-    const uint4* vs = reinterpret_cast<const uint4*>(p.v_res + src_tok * kD);
-    uint4* kd = reinterpret_cast<uint4*>(&kt[0][0]);
-    uint4* vd = reinterpret_cast<uint4*>(&vt[0][0]);
+    uint4* kd = reinterpret_cast<uint4*>(&S.kt[0][0]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kd[tid + 128 * i] = ks[tid + 128 * i];
-      vd[tid + 128 * i] = vs[tid + 128 * i];
-    }
+    for (int i = 0; i < GS / 8; ++i) kd[tid + 128 * i] = ks[tid + 128 * i];
   }
   __syncthreads();
-  quantize_block(kt, vt, kc, vc, p.k_res_norm + src_tok, rec);
+  quantize_group<GS>(S, p.k_res_norm + src_tok, p.v_res + src_tok * kD,
+                     [&](int sb) { return paged_record(p, b, lb0 + sb, h); });
 }
 
 // Length updates after a paged prefill (n_tok != nullptr) or append.
@@ -197,7 +222,7 @@ __global__ void paged_lengths_kernel(PagedArgs p, const int32_t* n_tok, int max_
   if (b >= p.B) return;
   if (n_tok) {
     const int n = n_tok[b];
-    if (n > 0 && n % kG == 0 && n <= max_tok && p.seq_res[b] == 0) p.seq_packed[b] += n;
+    if (n > 0 && n % p.group == 0 && n <= max_tok && p.seq_res[b] == 0) p.seq_packed[b] += n;
     return;
   }
   if (active && active[b] == 0) return;
@@ -209,20 +234,103 @@ __global__ void paged_lengths_kernel(PagedArgs p, const int32_t* n_tok, int max_
   }
 }
 
+// Dynamic shared memory of the group kernels: opted in once per kernel and
+// device when above the 48 KB default (GS = 128).
+template <class K>
+cudaError_t allow_group_smem(K kernel, size_t bytes, int (&done)[128]) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 128) done[dev] = 1;
+  return e;
+}
+
+template <int GS, bool PLAIN>
+cudaError_t paged_prefill_gp(const PagedArgs& p, const uint16_t* k, const uint16_t* v, int in_T,
+                             const int32_t* n_tok, int max_tok, cudaStream_t s) {
+  static int done[128] = {};
+  const size_t bytes = sizeof(GroupSmem<GS>);
+  cudaError_t e = allow_group_smem(paged_prefill_kernel<GS, PLAIN>, bytes, done);
+  if (e != cudaSuccess) return e;
+  dim3 grid(max_tok / GS, p.Hkv, p.B);
+  paged_prefill_kernel<GS, PLAIN><<<grid, 128, bytes, s>>>(p, k, v, in_T, n_tok, max_tok);
+  return cudaGetLastError();
+}
+template <int GS>
+cudaError_t paged_prefill_g(const PagedArgs& p, const uint16_t* k, const uint16_t* v, int in_T,
+                            const int32_t* n_tok, int max_tok, cudaStream_t s) {
+  return plain_scale(p.ks) ? paged_prefill_gp<GS, true>(p, k, v, in_T, n_tok, max_tok, s)
+                           : paged_prefill_gp<GS, false>(p, k, v, in_T, n_tok, max_tok, s);
+}
+
+template <int GS>
+cudaError_t paged_flush_g(const PagedArgs& p, const int32_t* active, cudaStream_t s) {
+  static int done[128] = {};
+  const size_t bytes = sizeof(GroupSmem<GS>);
+  cudaError_t e = allow_group_smem(paged_flush_kernel<GS>, bytes, done);
+  if (e != cudaSuccess) return e;
+  dim3 grid(kR / GS, p.Hkv, p.B);
+  paged_flush_kernel<GS><<<grid, 128, bytes, s>>>(p, active);
+  return cudaGetLastError();
+}
+
+template <int GS>
+cudaError_t quantize_kv_g(const uint16_t* k_hat, const __half* k_norm, const uint16_t* v,
+                          int src_T, int n_tok, int B, int Hkv, int T_cap, int p0,
+                          uint8_t* packed, cudaStream_t s) {
+  static int done[128] = {};
+  const size_t bytes = sizeof(GroupSmem<GS>);
+  cudaError_t e = allow_group_smem(quantize_kv_kernel<GS>, bytes, done);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n_tok / GS, Hkv, B);
+  quantize_kv_kernel<GS><<<grid, 128, bytes, s>>>(k_hat, k_norm, v, src_T, Hkv, T_cap, p0, packed);
+  return cudaGetLastError();
+}
+
+template <int GS, bool PLAIN>
+cudaError_t prefill_kv_gp(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,
+                          int Hkv, int T_cap, int p0, KeyScale ks, uint8_t* packed,
+                          cudaStream_t s) {
+  static int done[128] = {};
+  const size_t bytes = sizeof(GroupSmem<GS>);
+  cudaError_t e = allow_group_smem(prefill_kv_kernel<GS, PLAIN>, bytes, done);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n_tok / GS, Hkv, B);
+  prefill_kv_kernel<GS, PLAIN><<<grid, 128, bytes, s>>>(k, v, in_T, Hkv, T_cap, p0, ks, packed);
+  return cudaGetLastError();
+}
+template <int GS>
+cudaError_t prefill_kv_g(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,
+                         int Hkv, int T_cap, int p0, KeyScale ks, uint8_t* packed,
+                         cudaStream_t s) {
+  return plain_scale(ks) ? prefill_kv_gp<GS, true>(k, v, in_T, n_tok, B, Hkv, T_cap, p0, ks, packed, s)
+                         : prefill_kv_gp<GS, false>(k, v, in_T, n_tok, B, Hkv, T_cap, p0, ks, packed, s);
+}
+
 cudaError_t launch_paged_prefill(const PagedArgs& p, const uint16_t* k, const uint16_t* v,
                                  int in_T, const int32_t* n_tok, int max_tok, cudaStream_t s) {
-  dim3 grid(max_tok / kG, p.Hkv, p.B);
-  paged_prefill_kernel<<<grid, 128, 0, s>>>(p, k, v, in_T, n_tok, max_tok);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  switch (p.group) {
+    case 32: e = paged_prefill_g<32>(p, k, v, in_T, n_tok, max_tok, s); break;
+    case 64: e = paged_prefill_g<64>(p, k, v, in_T, n_tok, max_tok, s); break;
+    case 128: e = paged_prefill_g<128>(p, k, v, in_T, n_tok, max_tok, s); break;
+    default: return cudaErrorInvalidValue;
+  }
   if (e != cudaSuccess) return e;
   paged_lengths_kernel<<<(p.B + 127) / 128, 128, 0, s>>>(p, n_tok, max_tok, nullptr);
   return cudaGetLastError();
 }
 
 cudaError_t launch_paged_flush(const PagedArgs& p, const int32_t* active, cudaStream_t s) {
-  dim3 grid(kR / kG, p.Hkv, p.B);
-  paged_flush_kernel<<<grid, 128, 0, s>>>(p, active);
-  return cudaGetLastError();
+  switch (p.group) {
+    case 32: return paged_flush_g<32>(p, active, s);
+    case 64: return paged_flush_g<64>(p, active, s);
+    case 128: return paged_flush_g<128>(p, active, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_paged_lengths(const PagedArgs& p, const int32_t* active, cudaStream_t s) {
@@ -231,19 +339,26 @@ cudaError_t launch_paged_lengths(const PagedArgs& p, const int32_t* active, cuda
 }
 
 cudaError_t launch_quantize_kv(const uint16_t* k_hat, const __half* k_norm, const uint16_t* v,
-                               int src_T, int n_tok, int B, int Hkv, int T_cap, int p0,
+                               int src_T, int n_tok, int B, int Hkv, int T_cap, int p0, int group,
                                uint8_t* packed, cudaStream_t s) {
-  dim3 grid(n_tok / kG, Hkv, B);
-  quantize_kv_kernel<<<grid, 128, 0, s>>>(k_hat, k_norm, v, src_T, Hkv, T_cap, p0, packed);
-  return cudaGetLastError();
+  switch (group) {
+    case 32: return quantize_kv_g<32>(k_hat, k_norm, v, src_T, n_tok, B, Hkv, T_cap, p0, packed, s);
+    case 64: return quantize_kv_g<64>(k_hat, k_norm, v, src_T, n_tok, B, Hkv, T_cap, p0, packed, s);
+    case 128:
+      return quantize_kv_g<128>(k_hat, k_norm, v, src_T, n_tok, B, Hkv, T_cap, p0, packed, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_prefill_kv(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,
-                              int Hkv, int T_cap, int p0, KeyScale ks, uint8_t* packed,
+                              int Hkv, int T_cap, int p0, int group, KeyScale ks, uint8_t* packed,
                               cudaStream_t s) {
-  dim3 grid(n_tok / kG, Hkv, B);
-  prefill_kv_kernel<<<grid, 128, 0, s>>>(k, v, in_T, Hkv, T_cap, p0, ks, packed);
-  return cudaGetLastError();
+  switch (group) {
+    case 32: return prefill_kv_g<32>(k, v, in_T, n_tok, B, Hkv, T_cap, p0, ks, packed, s);
+    case 64: return prefill_kv_g<64>(k, v, in_T, n_tok, B, Hkv, T_cap, p0, ks, packed, s);
+    case 128: return prefill_kv_g<128>(k, v, in_T, n_tok, B, Hkv, T_cap, p0, ks, packed, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace oscar

@@ -3,7 +3,9 @@
 // news article on arXiv 2605.19660, 三).
 //
 // Keys: block-wise per-channel asymmetric INT2 -- every channel of every
-// block of G = 32 consecutive tokens has its own step and zero; values:
+// group of G consecutive tokens (G = 32 by default; 64 and 128 are the
+// larger groups) has its own step and zero, which every 32-token record of
+// the group carries; values:
 // per-token INT2 ("OScaR：面向大模型及多模态LLM极限KV缓存量化的奥卡姆剃刀",
 // 方法步骤详情 (2)(3); 前置知识, step Δ and zero z per block).  Per group:
 // z = min, Δ = (max - min)/3, code = round-half-even((x - z)/Δ) clamped to
@@ -39,14 +41,40 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
   return __uint_as_float(((uint32_t)u) << 16);
 }
 
+// Step and zero of one key channel over a group of N tokens (thread c =
+// channel c of the rows of kt, rotated and scaled keys as bf16).
+struct KeyParams {
+  float mn, step, rstep;
+  bool live;
+};
+template <int N>
+__device__ __forceinline__ KeyParams key_params(const uint16_t (*kt)[kD]) {
+  const int c = threadIdx.x;
+  float mn = bf16_bits_to_float(kt[0][c]), mx = mn;
+#pragma unroll 8
+  for (int t = 1; t < N; ++t) {
+    const float x = bf16_bits_to_float(kt[t][c]);
+    mn = fminf(mn, x);
+    mx = fmaxf(mx, x);
+  }
+  KeyParams p;
+  p.live = mx > mn;
+  p.mn = mn;
+  p.step = p.live ? __fdiv_rn(__fsub_rn(mx, mn), 3.0f) : 0.0f;
+  p.rstep = p.live ? __frcp_rn(p.step) : 0.0f;
+  return p;
+}
+
 // Called by all 128 threads of the CTA after a __syncthreads that follows
 // the staging of kt (rotated, scaled keys as bf16) and vt (values as bf16)
-// for the 32 tokens of one block; norms: the block's 32 key norms (global or
-// shared memory).  Writes the block record at rec (layout in oscar.h).
-__device__ __forceinline__ void quantize_block(const uint16_t (&kt)[kG][kD],
+// for the 32 tokens of one block; kp: this thread's key channel parameters
+// over the block's group; norms: the block's 32 key norms (global or shared
+// memory).  Writes the block record at rec (layout in oscar.h).
+__device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
                                                const uint16_t (&vt)[kG][kD],
                                                uint8_t (&kc)[kG][kD], uint8_t (&vc)[kG][kD],
-                                               const __half* norms, uint8_t* rec) {
+                                               const __half* norms, uint8_t* rec,
+                                               const KeyParams& kp) {
   const int tid = threadIdx.x;
   uint32_t* k_codes = reinterpret_cast<uint32_t*>(rec + kRecKC);
   uint32_t* v_codes = reinterpret_cast<uint32_t*>(rec + kRecVC);
@@ -56,24 +84,14 @@ __device__ __forceinline__ void quantize_block(const uint16_t (&kt)[kG][kD],
   __half* v_scale = reinterpret_cast<__half*>(rec + kRecVS);
   __half* v_zero = reinterpret_cast<__half*>(rec + kRecVZ);
 
-  // Keys: thread = channel, group = the 32 tokens of the block.
+  // Keys: thread = channel, with its group's parameters.
   {
     const int c = tid;
-    float mn = bf16_bits_to_float(kt[0][c]), mx = mn;
-#pragma unroll 8
-    for (int t = 1; t < kG; ++t) {
-      const float x = bf16_bits_to_float(kt[t][c]);
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
-    }
-    const bool live = mx > mn;
-    const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), 3.0f) : 0.0f;
-    const float rstep = live ? __frcp_rn(step) : 0.0f;
 #pragma unroll 8
     for (int t = 0; t < kG; ++t)
-      kc[t][c] = quant_code_fast(bf16_bits_to_float(kt[t][c]), mn, step, rstep, live);
-    k_scale[c] = __float2half_rn(step);
-    k_zero[c] = __float2half_rn(mn);
+      kc[t][c] = quant_code_fast(bf16_bits_to_float(kt[t][c]), kp.mn, kp.step, kp.rstep, kp.live);
+    k_scale[c] = __float2half_rn(kp.step);
+    k_zero[c] = __float2half_rn(kp.mn);
   }
 
   // Values: warp w handles tokens 8w..8w+7, lane holds channels 4l..4l+3.

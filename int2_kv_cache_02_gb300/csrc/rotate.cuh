@@ -55,8 +55,15 @@ __device__ __forceinline__ float all_heads_sq(const uint16_t* k0, long long head
 // the key's own norm or, with OSCAR_NORM_ALL_HEADS, the norm of the token's
 // keys over all heads, whose raw sum of squares the caller passes in s_all.
 // Unscaled keys store 1; a zero key (zero norm) keeps k_hat = 0 and stores 0.
+// PLAIN: the method itself (no flags, unit target) fixed at compile time, so
+// the per-token tests of the variants fold away.
+template <bool PLAIN = false>
 __device__ __forceinline__ float rotate_scale_key(float (&x)[4], int lane, KeyScale ks,
                                                   float s_all = 0.0f) {
+  if constexpr (PLAIN) {
+    ks.flags = 0u;
+    ks.target = 1.0f;
+  }
   const bool rot = !(ks.flags & OSCAR_NO_ROTATE);
   if (rot) fht128(x, lane);
   if (ks.flags & OSCAR_NO_SCALE) {
@@ -69,10 +76,12 @@ __device__ __forceinline__ float rotate_scale_key(float (&x)[4], int lane, KeySc
                       ? (rot ? 128.0f * s_all : s_all)
                       : warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
   if (s > 0.0f) {
-    const float f = rsqrtf(s) * ks.target;
+    const bool unit = ks.target == 1.0f;   // the method's target: no extra rounding
+    const float f = unit ? rsqrtf(s) : rsqrtf(s) * ks.target;
 #pragma unroll
     for (int r = 0; r < 4; ++r) x[r] *= f;
-    return sqrtf(s) * (rot ? kInvSqrtD : 1.0f) / ks.target;
+    const float n = sqrtf(s) * (rot ? kInvSqrtD : 1.0f);
+    return unit ? n : n / ks.target;
   }
 #pragma unroll
   for (int r = 0; r < 4; ++r) x[r] = 0.0f;
@@ -89,4 +98,10 @@ __device__ __forceinline__ uint2 pack_bf16x4(const float (&x)[4]) {
   return o;
 }
 
+}  // namespace oscar
+
+namespace oscar {
+// The method's own scaling (no ablation or scope flag, unit target): the
+// kernels that scale keys are instantiated for it separately.
+inline bool plain_scale(const KeyScale& ks) { return ks.flags == 0u && ks.target == 1.0f; }
 }  // namespace oscar

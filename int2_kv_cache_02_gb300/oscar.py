@@ -36,7 +36,7 @@ class OscarCacheStruct(ctypes.Structure):
                 ("packed", c_void_p),
                 ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
                 ("n_packed", c_int), ("n_res", c_int), ("flags", c_uint),
-                ("norm_target", c_float)]
+                ("norm_target", c_float), ("key_group", c_int)]
 
 
 class OscarPagedCacheStruct(ctypes.Structure):
@@ -44,7 +44,7 @@ class OscarPagedCacheStruct(ctypes.Structure):
                 ("pages", c_void_p), ("block_table", c_void_p),
                 ("n_packed", c_void_p), ("n_res", c_void_p),
                 ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
-                ("flags", c_uint), ("norm_target", c_float)]
+                ("flags", c_uint), ("norm_target", c_float), ("key_group", c_int)]
 
 
 BLOCK_BYTES = 2752
@@ -132,7 +132,7 @@ class KVCache:
     oscar_cache struct that points at them (layouts in include/oscar.h)."""
 
     def __init__(self, B: int, Hkv: int, T_cap: int, flags: int = 0, device=None,
-                 norm_target: float = 0.0):
+                 norm_target: float = 0.0, key_group: int = 0):
         if T_cap % G:
             raise ValueError("T_cap must be a multiple of 32")
         dev = torch.device(device if device is not None else "cuda")
@@ -146,6 +146,7 @@ class KVCache:
         for name in ("packed", "k_res", "v_res", "k_res_norm"):
             setattr(s, name, getattr(self, name).data_ptr())
         s.n_packed, s.n_res, s.flags, s.norm_target = 0, 0, flags, norm_target
+        s.key_group = key_group
         self.struct = s
 
     B = property(lambda self: self.struct.B)
@@ -155,6 +156,7 @@ class KVCache:
     n_res = property(lambda self: self.struct.n_res)
     flags = property(lambda self: self.struct.flags)
     norm_target = property(lambda self: self.struct.norm_target)
+    key_group = property(lambda self: self.struct.key_group or 32)
 
     def ref(self):
         return ctypes.byref(self.struct)
@@ -199,7 +201,7 @@ class PagedKVCache:
     allocator below; the device kernels only follow the table."""
 
     def __init__(self, B: int, Hkv: int, max_blocks: int, n_pages: int, flags: int = 0,
-                 device=None, norm_target: float = 0.0):
+                 device=None, norm_target: float = 0.0, key_group: int = 0):
         dev = torch.device(device if device is not None else "cuda")
         self.pages = torch.zeros((n_pages, Hkv, BLOCK_BYTES), dtype=torch.uint8, device=dev)
         self.block_table = torch.full((B, max_blocks), -1, dtype=torch.int32, device=dev)
@@ -211,6 +213,7 @@ class PagedKVCache:
         s = OscarPagedCacheStruct()
         s.B, s.Hkv, s.max_blocks, s.n_pages, s.flags = B, Hkv, max_blocks, n_pages, flags
         s.norm_target = norm_target
+        s.key_group = key_group
         s.pages = self.pages.data_ptr()
         s.block_table = self.block_table.data_ptr()
         s.n_packed = self.n_packed_d.data_ptr()

@@ -43,7 +43,8 @@ def assert_attention_close(gpu, ref, what=""):
     return ma, rl
 
 
-def upload_oracle_cache(cache, heads: dict, flags: int = 0, norm_target: float = 0.0):
+def upload_oracle_cache(cache, heads: dict, flags: int = 0, norm_target: float = 0.0,
+                        key_group: int = 0):
     """Writes oracle HeadCaches {(b, h): HeadCache} into a KVCache (same
     n_packed / n_res for every row), using the oracle's own packing; the
     cache takes the flags and target norm the oracle built them with."""
@@ -60,8 +61,9 @@ def upload_oracle_cache(cache, heads: dict, flags: int = 0, norm_target: float =
                 torch.from_numpy(np.ascontiguousarray(arr)))
             put("k_codes", O.pack_k_words(kq.codes).reshape(nb, 256).view(np.int32))
             put("v_codes", O.pack_v_words(vq.codes).view(np.int32))
-            put("k_scale", kq.step16)
-            put("k_zero", kq.zero16)
+            ks16, kz16 = kq.block_params()
+            put("k_scale", ks16)
+            put("k_zero", kz16)
             put("k_norm", hc.packed_norm16().reshape(nb, 4, 8))
             put("v_scale", vq.step16.reshape(nb, 4, 8))
             put("v_zero", vq.zero16.reshape(nb, 4, 8))
@@ -73,6 +75,7 @@ def upload_oracle_cache(cache, heads: dict, flags: int = 0, norm_target: float =
     cache.struct.n_res = R or 0
     cache.struct.flags = flags
     cache.struct.norm_target = norm_target
+    cache.struct.key_group = key_group
     return cache
 
 

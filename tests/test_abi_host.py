@@ -74,6 +74,7 @@ def _cache(**kw):
         setattr(s, name, kw.get(name, FAKE + 0x100000 * i))
     s.n_packed, s.n_res, s.flags = kw.get("n_packed", 0), kw.get("n_res", 0), kw.get("flags", 0)
     s.norm_target = kw.get("norm_target", 0.0)
+    s.key_group = kw.get("key_group", 0)
     return s
 
 
@@ -131,6 +132,13 @@ def test_cache_validation_and_state_untouched():
         assert L.oscar_decode_attention_static_ws(ctypes.byref(bad), P(FAKE), 2, 0.1, P(FAKE),
                                                   1, None) == 1
         assert bad.n_packed == 0 and bad.n_res == 0
+    # key groups: only 32 (0), 64, 128; n_packed and quantised runs multiples of it
+    for bad in (_cache(key_group=48), _cache(key_group=256), _cache(key_group=64, n_packed=32)):
+        assert L.oscar_prefill_kv(ctypes.byref(bad), P(FAKE), P(FAKE), 64, 64, None) == 1
+    g128 = _cache(key_group=128)
+    assert L.oscar_prefill_kv(ctypes.byref(g128), P(FAKE), P(FAKE), 64, 64, None) == 1
+    assert L.oscar_quantize_kv(ctypes.byref(g128), P(FAKE), P(FAKE), P(FAKE), 192, 192, None) == 1
+    assert g128.n_packed == 0
 
 
 @no_gpu_only
@@ -159,6 +167,7 @@ def _paged(**kw):
         setattr(s, name, kw.get(name, FAKE + 0x100000 * i))
     s.flags = kw.get("flags", 0)
     s.norm_target = kw.get("norm_target", 0.0)
+    s.key_group = kw.get("key_group", 0)
     return s
 
 
@@ -171,8 +180,11 @@ def test_paged_validation():
     assert L.oscar_paged_append_kv(ctypes.byref(bad), P(FAKE), P(FAKE), None, None) == 1
     mis = _paged(pages=FAKE + 8)
     assert L.oscar_paged_append_kv(ctypes.byref(mis), P(FAKE), P(FAKE), None, None) == 3
-    for bad in (_paged(flags=8), _paged(norm_target=1e-3)):
+    for bad in (_paged(flags=8), _paged(norm_target=1e-3), _paged(key_group=96)):
         assert L.oscar_paged_append_kv(ctypes.byref(bad), P(FAKE), P(FAKE), None, None) == 1
+    g128 = _paged(key_group=128)
+    assert L.oscar_paged_prefill_kv(ctypes.byref(g128), P(FAKE), P(FAKE), 64, P(FAKE), 64,
+                                    None) == 1          # max_tok not a multiple of the group
     c = _paged()
     assert L.oscar_paged_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 64, P(FAKE), 48, None) == 1
     assert L.oscar_paged_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 512, P(FAKE), 512,

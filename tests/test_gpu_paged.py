@@ -42,9 +42,10 @@ def _per_token(a):
 def _write_record(rec, kq, vq, norm16, j):
     """Block j of an oracle head cache into a 2752-byte record view."""
     t = slice(32 * j, 32 * j + 32)
+    ks16, kz16 = kq.block_params()
     parts = [O.pack_k_words(kq.codes[t]).reshape(-1).view(np.uint8),
              O.pack_v_words(vq.codes[t]).reshape(-1).view(np.uint8),
-             kq.step16[j].view(np.uint8), kq.zero16[j].view(np.uint8),
+             ks16[j].view(np.uint8), kz16[j].view(np.uint8),
              _per_token(norm16[t]).view(np.uint8),
              _per_token(vq.step16[t]).view(np.uint8), _per_token(vq.zero16[t]).view(np.uint8)]
     rec.copy_(torch.from_numpy(np.concatenate(parts)))
