@@ -26,7 +26,8 @@ ones that shape arithmetic here are: Sylvester (natural order) Hadamard of size
 128 with entries +-1/sqrt(128); the norm is per (token, KV head) unless
 NORM_ALL_HEADS asks for the norm over all heads; keys are scaled to a target
 norm (1 unless given) and the stored norm is n / target; asymmetric
-min-max INT2 with step (max-min)/3, zero = min, round half to even, codes from
+min-max INT2 with step (max-min)/3 (INT4, an option: (max-min)/15), zero =
+min, round half to even, codes from
 the fp32 parameters before their fp16 rounding; a constant group stores step 0
 and codes 0; a zero key keeps k_hat = 0 and norm 0; flush-before-append.
 """
@@ -154,23 +155,25 @@ def rotate_scale_k(k_bits: np.ndarray, flags: int = 0, target: float = 1.0) -> R
 # an option), V per token)
 # --------------------------------------------------------------------------
 
-def quantize_groups(x: np.ndarray):
-    """Asymmetric min-max INT2 over the last axis of ``x`` (fp32 values).
+def quantize_groups(x: np.ndarray, bits: int = 2):
+    """Asymmetric min-max quantisation over the last axis of ``x`` (fp32).
 
-    Four levels z + c*Δ, c in {0,1,2,3}: z = min, Δ = (max - min)/3, the code
-    is round-half-even((x - z)/Δ) clamped to [0, 3].  All in fp32, one rounding
+    L = 2^bits - 1 steps (INT2: 3, INT4: 15), levels z + c*Δ with
+    c in {0..L}: z = min, Δ = (max - min)/L, the code is
+    round-half-even((x - z)/Δ) clamped to [0, L].  All in fp32, one rounding
     per operation, in this order.  A constant group gets Δ = 0 and codes 0.
     Returns (codes uint8, step fp32, zero fp32).
     """
+    L = (1 << bits) - 1
     x = np.asarray(x, dtype=np.float32)
     mn = x.min(axis=-1).astype(np.float32)
     mx = x.max(axis=-1).astype(np.float32)
     d = (mx - mn).astype(np.float32)
-    step = (d / np.float32(3.0)).astype(np.float32)
+    step = (d / np.float32(L)).astype(np.float32)
     live = mx > mn
     safe = np.where(live, step, np.float32(1.0)).astype(np.float32)
     t = ((x - mn[..., None]).astype(np.float32) / safe[..., None]).astype(np.float32)
-    codes = np.clip(np.rint(t), 0, 3).astype(np.uint8)
+    codes = np.clip(np.rint(t), 0, L).astype(np.uint8)
     codes = np.where(live[..., None], codes, np.uint8(0)).astype(np.uint8)
     step = np.where(live, step, np.float32(0.0)).astype(np.float32)
     return codes, step, mn
@@ -197,7 +200,7 @@ class QuantV:
     zero16: np.ndarray   # float16 [n]
 
 
-def quantize_k(k_hat_bits: np.ndarray, group: int = G) -> QuantK:
+def quantize_k(k_hat_bits: np.ndarray, group: int = G, bits: int = 2) -> QuantK:
     """Block-wise per-channel INT2 for keys [n][128], n a multiple of group.
 
     Each channel of each group of ``group`` consecutive tokens has its own
@@ -209,15 +212,16 @@ def quantize_k(k_hat_bits: np.ndarray, group: int = G) -> QuantK:
     assert group in (32, 64, 128) and n % group == 0
     x = bf16_to_f64(k_hat_bits).astype(np.float32)          # exact
     xb = x.reshape(n // group, group, D).transpose(0, 2, 1)  # [grp][ch][tok]
-    codes, step, zero = quantize_groups(xb)
+    codes, step, zero = quantize_groups(xb, bits)
     return QuantK(codes.transpose(0, 2, 1).reshape(n, D).copy(),
                   f_to_f16(step), f_to_f16(zero), group)
 
 
-def quantize_v(v_bits: np.ndarray) -> QuantV:
-    """Per-token INT2 for values [n][128] ([rainbus] 方法步骤详情 item (3))."""
+def quantize_v(v_bits: np.ndarray, bits: int = 2) -> QuantV:
+    """Per-token INT2 (or INT4) for values [n][128] ([rainbus] 方法步骤详情
+    item (3))."""
     x = bf16_to_f64(v_bits).astype(np.float32)
-    codes, step, zero = quantize_groups(x)
+    codes, step, zero = quantize_groups(x, bits)
     return QuantV(codes, f_to_f16(step), f_to_f16(zero))
 
 
@@ -282,6 +286,56 @@ def pack_v_words(codes: np.ndarray) -> np.ndarray:
     return out
 
 
+def pack_k_words4(codes: np.ndarray) -> np.ndarray:
+    """INT4 key codes [n][128] -> uint32 [n][16].
+
+    Word w of a token holds channels 8w..8w+7; channel 8w+j sits at bit
+    4*(j//2) + 16*(j%2): even channels in the low half-word, odd channels in
+    the high half-word, in channel order.
+    """
+    n = codes.shape[0]
+    out = np.zeros((n, 16), dtype=np.uint32)
+    for w in range(16):
+        for j in range(8):
+            pos = 4 * (j // 2) + 16 * (j % 2)
+            out[:, w] |= codes[:, 8 * w + j].astype(np.uint32) << np.uint32(pos)
+    return out
+
+
+def pack_v_words4(codes: np.ndarray) -> np.ndarray:
+    """INT4 value codes [n][128] (n a multiple of 32) -> uint32 [n/32][512].
+
+    Per block of 32 tokens, word index = 256*kh + 8*lane + 4*p + hh with
+    kh, p in {0, 1}, hh in {0..3}, lane = 4*g + t (g in 0..7, t in 0..3).
+    The low half-word holds token 16*kh + 2*t + 8*p, the high half-word
+    token + 1; slot k (bits 4k..4k+3 of each half) holds channel
+    g + 8*(4*hh + k).
+    """
+    n = codes.shape[0]
+    assert n % 32 == 0
+    out = np.zeros((n // 32, 512), dtype=np.uint32)
+    for kh in range(2):
+        for lane in range(32):
+            g, t = lane // 4, lane % 4
+            for p in range(2):
+                for hh in range(4):
+                    widx = 256 * kh + 8 * lane + 4 * p + hh
+                    tok = 16 * kh + 2 * t + 8 * p
+                    for k in range(4):
+                        ch = g + 8 * (4 * hh + k)
+                        lo = codes[tok::32, ch].astype(np.uint32) << np.uint32(4 * k)
+                        hi = codes[tok + 1::32, ch].astype(np.uint32) << np.uint32(16 + 4 * k)
+                        out[:, widx] |= lo | hi
+    return out
+
+
+def pack_words(codes: np.ndarray, bits: int, kind: str) -> np.ndarray:
+    """The cache's packed words of key (kind "k") or value ("v") codes."""
+    if bits == 2:
+        return pack_k_words(codes) if kind == "k" else pack_v_words(codes)
+    return pack_k_words4(codes) if kind == "k" else pack_v_words4(codes)
+
+
 # --------------------------------------------------------------------------
 # Attention (fp64)
 # --------------------------------------------------------------------------
@@ -314,6 +368,7 @@ class HeadCache:
     flags: int = 0
     target: float = 1.0
     group: int = G       # key group size (tokens sharing step and zero)
+    bits: int = 2        # code width: 2 (the method) or 4
     k_codes: list = field(default_factory=list)   # QuantK per quantised chunk
     k_norm16: list = field(default_factory=list)
     v_q: list = field(default_factory=list)
@@ -341,9 +396,9 @@ class HeadCache:
         return rotate_scale_k(k_raw_bits, self.flags, self.target)
 
     def _pack(self, k_hat_bits, norm16, v_bits):
-        self.k_codes.append(quantize_k(k_hat_bits, self.group))
+        self.k_codes.append(quantize_k(k_hat_bits, self.group, self.bits))
         self.k_norm16.append(np.asarray(norm16, dtype=np.float16))
-        self.v_q.append(quantize_v(v_bits))
+        self.v_q.append(quantize_v(v_bits, self.bits))
 
     def append(self, k_raw_bits: np.ndarray, v_bits: np.ndarray):
         """One decode token.  Flush-before-append: a full residual (128
@@ -418,13 +473,13 @@ class HeadCache:
 
 
 def build_head_cache(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
-                     target: float = 1.0, group: int = G) -> HeadCache:
+                     target: float = 1.0, group: int = G, bits: int = 2) -> HeadCache:
     """Prompt of T tokens: the first ``n_packed`` (a multiple of the key
     group) are quantised, the remaining T - n_packed (at most 128) stay in the
     residual."""
     T = k_raw_bits.shape[0]
     assert n_packed % group == 0 and 0 <= T - n_packed <= R
-    c = HeadCache(flags=flags, target=target, group=group)
+    c = HeadCache(flags=flags, target=target, group=group, bits=bits)
     if n_packed:
         c.quantize_prefix(k_raw_bits[:n_packed], v_bits[:n_packed])
     if T > n_packed:
@@ -433,7 +488,7 @@ def build_head_cache(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
 
 
 def build_row_caches(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
-                     target: float = 1.0, group: int = G) -> list:
+                     target: float = 1.0, group: int = G, bits: int = 2) -> list:
     """build_head_cache for every KV head of one sequence, k_raw_bits and
     v_bits [Hkv][T][128]: the keys of all heads are rotated and scaled
     together, which the all-heads norm needs, then each head is quantised
@@ -443,7 +498,7 @@ def build_row_caches(k_raw_bits, v_bits, n_packed: int, flags: int = 0,
     rk = rotate_scale_k(k_raw_bits, flags, target)
     caches = []
     for h in range(Hkv):
-        c = HeadCache(flags=flags, target=target, group=group)
+        c = HeadCache(flags=flags, target=target, group=group, bits=bits)
         if n_packed:
             c._pack(rk.k_hat_bf16[h, :n_packed], rk.norm_f16[h, :n_packed], v_bits[h, :n_packed])
         if T > n_packed:
