@@ -305,7 +305,7 @@ def pack_k_words4(codes: np.ndarray) -> np.ndarray:
 def pack_v_words4(codes: np.ndarray) -> np.ndarray:
     """INT4 value codes [n][128] (n a multiple of 32) -> uint32 [n/32][512].
 
-    Per block of 32 tokens, word index = 256*kh + 8*lane + 4*p + hh with
+    Per block of 32 tokens, word index = 256*kh + 128*p + 4*lane + hh with
     kh, p in {0, 1}, hh in {0..3}, lane = 4*g + t (g in 0..7, t in 0..3).
     The low half-word holds token 16*kh + 2*t + 8*p, the high half-word
     token + 1; slot k (bits 4k..4k+3 of each half) holds channel
@@ -319,7 +319,7 @@ def pack_v_words4(codes: np.ndarray) -> np.ndarray:
             g, t = lane // 4, lane % 4
             for p in range(2):
                 for hh in range(4):
-                    widx = 256 * kh + 8 * lane + 4 * p + hh
+                    widx = 256 * kh + 128 * p + 4 * lane + hh
                     tok = 16 * kh + 2 * t + 8 * p
                     for k in range(4):
                         ch = g + 8 * (4 * hh + k)
