@@ -108,9 +108,23 @@ enum { OSCAR_NO_ROTATE = 1u, OSCAR_NO_SCALE = 2u, OSCAR_NORM_ALL_HEADS = 4u };
  */
 #define OSCAR_BLOCK_BYTES 2752
 
+/*
+ * INT4 option (cache field bits = 4; the pages fix only INT2, [rainbus]
+ * 局限与改进 (1) names other widths as unstudied): the same quantiser with
+ * (max - min)/15 as the step and codes 0..15, in a 4800-byte record:
+ *     0  key codes    u32 [32][16]: channel 8w+j at bit 4*(j/2) + 16*(j%2)
+ *  2048  value codes  u32 [512]: word 256*kh + 128p + 4*(4g+t) + hh holds, in
+ *                     its low half, token 16kh + 2t + 8p and in its high half
+ *                     the next token; slot k (bits 4k..4k+3) is channel
+ *                     g + 8*(4hh + k)
+ *  4096  key step, 4352 key zero, 4608 key norms, 4672 value step,
+ *  4736 value zero (as in the INT2 record)
+ */
+#define OSCAR_BLOCK_BYTES_INT4 4800
+
 typedef struct {
   int B, Hkv, T_cap;
-  uint8_t* packed;       /* [B][Hkv][T_cap/32] records of OSCAR_BLOCK_BYTES */
+  uint8_t* packed;       /* [B][Hkv][T_cap/32] records (OSCAR_BLOCK_BYTES, INT4: _INT4) */
   oscar_bf16* k_res;
   oscar_bf16* v_res;
   oscar_f16* k_res_norm;
@@ -120,6 +134,8 @@ typedef struct {
   float norm_target; /* target norm of the scaled keys (0 = 1), fixed for the cache's life */
   int key_group;     /* tokens sharing a key channel's step and zero: 32 (0), 64 or 128;
                         n_packed and every quantised run are multiples of it */
+  int bits;          /* code width: 2 (0, the method) or 4; records of
+                        OSCAR_BLOCK_BYTES or OSCAR_BLOCK_BYTES_INT4 */
 } oscar_cache;
 
 /*
@@ -127,7 +143,7 @@ typedef struct {
  * serving engine's layout; the pages have no counterpart in the method,
  * which is unchanged).  The packed cache lives in pages of 32 tokens: page p
  * holds one record (layout above) per KV head, record h at
- * pages + (p*Hkv + h)*OSCAR_BLOCK_BYTES.  Logical block j of sequence b
+ * pages + (p*Hkv + h)*OSCAR_BLOCK_BYTES (INT4: _INT4).  Logical block j of sequence b
  * (its tokens 32j..32j+31) is page block_table[b*max_blocks + j]; the
  * caller owns the page pool and the table and must map a block before a
  * call writes it.  Lengths are per sequence and live in device memory, so a
@@ -150,6 +166,7 @@ typedef struct {
   unsigned flags;
   float norm_target;
   int key_group;            /* as in oscar_cache */
+  int bits;                 /* as in oscar_cache; a page holds Hkv records of its size */
 } oscar_paged_cache;
 
 /*

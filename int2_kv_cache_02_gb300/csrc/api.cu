@@ -48,7 +48,8 @@ oscar_status check_cache(const oscar_cache* c) {
     return OSCAR_ERR_INVALID_ARG;
   if (c->n_res < 0 || c->n_res > kR) return OSCAR_ERR_INVALID_ARG;
   if ((c->flags & ~kAllFlags) || !target_ok(c->norm_target)) return OSCAR_ERR_INVALID_ARG;
-  if (!key_group_ok(c->key_group) || c->n_packed % key_group(c->key_group) != 0)
+  if (!key_group_ok(c->key_group) || c->n_packed % key_group(c->key_group) != 0 ||
+      !code_bits_ok(c->bits))
     return OSCAR_ERR_INVALID_ARG;
   return OSCAR_OK;
 }
@@ -118,7 +119,7 @@ oscar_status flush_residual(oscar_cache* c, cudaStream_t s) {
   if (c->n_packed + kR > c->T_cap) return OSCAR_ERR_CAPACITY;
   cudaError_t e = launch_quantize_kv(
       c->k_res, reinterpret_cast<const __half*>(c->k_res_norm), c->v_res, kR, kR, c->B, c->Hkv,
-      c->T_cap, c->n_packed, key_group(c->key_group), c->packed, s);
+      c->T_cap, c->n_packed, key_group(c->key_group), code_bits(c->bits), c->packed, s);
   g_launches++;
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   c->n_packed += kR;
@@ -181,7 +182,7 @@ oscar_status oscar_quantize_kv(oscar_cache* c, const oscar_bf16* k_hat, const os
   if ((long long)c->n_packed + n_tok > c->T_cap) return OSCAR_ERR_CAPACITY;
   cudaError_t e = launch_quantize_kv(
       k_hat, reinterpret_cast<const __half*>(k_norm), v, src_T, n_tok, c->B, c->Hkv, c->T_cap,
-      c->n_packed, G, c->packed, as_stream(stream));
+      c->n_packed, G, code_bits(c->bits), c->packed, as_stream(stream));
   g_launches++;
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
   c->n_packed += n_tok;
@@ -199,7 +200,8 @@ oscar_status oscar_prefill_kv(oscar_cache* c, const oscar_bf16* k, const oscar_b
   if (c->n_res != 0) return OSCAR_ERR_INVALID_ARG;  // packed tokens must precede residual ones
   if ((long long)c->n_packed + n_tok > c->T_cap) return OSCAR_ERR_CAPACITY;
   cudaError_t e = launch_prefill_kv(k, v, in_T, n_tok, c->B, c->Hkv, c->T_cap, c->n_packed, G,
-                                    key_scale(c->flags, c->norm_target), c->packed,
+                                    code_bits(c->bits), key_scale(c->flags, c->norm_target),
+                                    c->packed,
                                     as_stream(stream));
   g_launches++;
   if (e != cudaSuccess) return OSCAR_ERR_CUDA;
@@ -290,6 +292,7 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
+  a.bits = code_bits(c->bits);
   cudaError_t e = launch_decode_int2(a, as_stream(stream));
   g_launches += 2;
   return from_cuda(e);
@@ -317,7 +320,8 @@ oscar_status check_paged(const oscar_paged_cache* c) {
     if (!p) return OSCAR_ERR_INVALID_ARG;
     if (!al4(p)) return OSCAR_ERR_ALIGNMENT;
   }
-  if ((c->flags & ~kAllFlags) || !target_ok(c->norm_target) || !key_group_ok(c->key_group))
+  if ((c->flags & ~kAllFlags) || !target_ok(c->norm_target) || !key_group_ok(c->key_group) ||
+      !code_bits_ok(c->bits))
     return OSCAR_ERR_INVALID_ARG;
   return OSCAR_OK;
 }
@@ -338,6 +342,7 @@ PagedArgs paged_args(const oscar_paged_cache* c) {
   p.n_pages = c->n_pages;
   p.ks = key_scale(c->flags, c->norm_target);
   p.group = key_group(c->key_group);
+  p.bits = code_bits(c->bits);
   return p;
 }
 
@@ -410,6 +415,7 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
+  a.bits = code_bits(c->bits);
   a.block_table = c->block_table;
   a.seq_packed = c->n_packed;
   a.seq_res = c->n_res;

@@ -19,6 +19,24 @@ constexpr int kBlkBytes = OSCAR_BLOCK_BYTES;
 constexpr int kRecKC = 0, kRecVC = 1024, kRecKS = 2048, kRecKZ = 2304, kRecKN = 2560,
               kRecVS = 2624, kRecVZ = 2688;
 static_assert(kRecVZ + 64 == kBlkBytes, "record layout");
+// The record of one 32-token block for a code width of BITS (2: the method's
+// INT2 record above; 4: the INT4 option, twice the code bytes, the same side
+// arrays after them).
+template <int BITS>
+struct Rec;
+template <>
+struct Rec<2> {
+  static constexpr int KC = 0, VC = 1024, KS = 2048, KZ = 2304, KN = 2560, VS = 2624, VZ = 2688,
+                       BYTES = 2752;
+};
+template <>
+struct Rec<4> {
+  static constexpr int KC = 0, VC = 2048, KS = 4096, KZ = 4352, KN = 4608, VS = 4672, VZ = 4736,
+                       BYTES = 4800;
+};
+static_assert(Rec<2>::BYTES == kBlkBytes && Rec<4>::BYTES == OSCAR_BLOCK_BYTES_INT4, "records");
+__host__ __device__ constexpr int rec_bytes(int bits) { return bits == 4 ? Rec<4>::BYTES : Rec<2>::BYTES; }
+
 // Position of token t (0..31) of a block in the record's per-token arrays
 // (norms, value step, value zero): tokens i, i+8, i+16, i+24 are adjacent.
 __host__ __device__ constexpr int tok_slot(int t) { return 4 * (t & 7) + (t >> 3); }

@@ -43,12 +43,18 @@ namespace oscar {
 namespace {
 
 constexpr int NW = 4;       // warps per CTA
-constexpr int NSTAGE = 4;   // ring depth per warp (blocks in flight)
-// one 32-token block record: key codes, value codes, key step, key zero,
-// norms, value step, value zero
-constexpr int KC_OFF = kRecKC, VC_OFF = kRecVC, KS_OFF = kRecKS, KZ_OFF = kRecKZ,
-              KN_OFF = kRecKN, VS_OFF = kRecVS, VZ_OFF = kRecVZ;
-constexpr int kSmemBytes = NW * NSTAGE * kBlkBytes + NW * NSTAGE * 8;
+
+// Per code width: the record (key codes, value codes, key step, key zero,
+// norms, value step, value zero; oscar.h) and the ring depth per warp.  The
+// INT4 record is 1.74x the INT2 one, so two of them in flight per warp hold
+// about as many bytes as four INT2 records, and the CTA keeps 4 per SM.
+template <int BITS>
+struct Layout {
+  using RL = Rec<BITS>;
+  static constexpr int NSTAGE = BITS == 2 ? 4 : 2;
+  static constexpr int SMEM = NW * NSTAGE * RL::BYTES + NW * NSTAGE * 8;
+  static constexpr float CENTER = BITS == 2 ? 1.5f : 7.5f;   // mid code (2^BITS - 1) / 2
+};
 
 constexpr float kLazyLog2 = 8.0f;         // lazy softmax rescale threshold (log2 units)
 
@@ -107,12 +113,18 @@ __device__ __forceinline__ int block_step_exp(const uint4* ks4) {
   return mb == 0 ? 0 : 14 - (int)(mb >> 10);   // mb >> 10: biased exponent
 }
 
-// fp16x2 {2^E 4^-p, ..} for p = 0..4 (exact: powers of two >= 2^-24).
+// fp16x2 {2^E 4^-p, ..} for p = 0..4 (INT2) or {2^E 16^-p, ..} for p = 0, 1
+// (INT4) (exact: powers of two >= 2^-24).
+template <int BITS>
 __device__ __forceinline__ void step_scales(uint32_t (&c)[5], int E) {
   const float f = __int_as_float((127 + E) << 23);
   c[0] = half2_as_u32(__floats2half2_rn(f, f));
+  if constexpr (BITS == 2) {
 #pragma unroll
-  for (int p = 1; p < 5; ++p) c[p] = hmul2_u(c[0], pow4_inv_h2(p));
+    for (int p = 1; p < 5; ++p) c[p] = hmul2_u(c[0], pow4_inv_h2(p));
+  } else {
+    c[1] = hmul2_u(c[0], 0x2C002C00u);   // 16^-1
+  }
 }
 
 // Value code pair at slot k as centred fp16 values (c - 1.5) * 2^(2p - 9):
@@ -161,6 +173,46 @@ __device__ __forceinline__ void value_frag(uint32_t (&av)[4], int mt, const uint
   }
 }
 
+// INT4 codes.  A word holds 8 channels (keys) or 4 channels x 2 tokens
+// (values), 4 bits each; nibble positions 0 and 1 of each half-word are exact
+// fp16 subnormals c * 16^p * 2^-24 as they stand, positions 2 and 3 after a
+// shift right by 8 (ws = w >> 8).  Slot K (0..3) of a half-word: position
+// K & 1 of w (K < 2) or of ws.
+template <int K>
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w, uint32_t ws) {
+  return (K < 2 ? w : ws) & (0x000F000Fu << (4 * (K & 1)));
+}
+// fp16x2 {16^-p, 16^-p} for position p = 0, 1
+constexpr uint32_t pow16_inv_h2(int p) { return p == 0 ? 0x3C003C00u : 0x2C002C00u; }
+// Value slot K as (c - 7.5) * 2^(4p - 9), p = K & 1: exact as for INT2.
+template <int K>
+__device__ __forceinline__ uint32_t value_nib(uint32_t w, uint32_t ws) {
+  constexpr uint32_t B = (K & 1) ? 0xB380B380u /* -7.5 * 2^-5 */ : 0xA380A380u /* -7.5 * 2^-9 */;
+  return hfma2_u(nib_pair<K>(w, ws), 0x78007800u /* 2^15 */, B);
+}
+// A operand of P.V m-tile mt from the lane's eight INT4 value words (4 per
+// token pair: slots hold channels g + 8 (4 hh + k)): row gid takes slot
+// 2 (mt % 2) of word hh = mt / 2, row gid + 8 the next slot; words 0..3 are
+// tokens (2 tig, 2 tig + 1), words 4..7 tokens (2 tig + 8, 2 tig + 9).
+__device__ __forceinline__ void value_frag4(uint32_t (&av)[4], int mt, const uint32_t (&wv)[8],
+                                            const uint32_t (&ws)[8]) {
+  const int hh = mt >> 1, p0 = hh, p1 = 4 + hh;
+  if ((mt & 1) == 0) {
+    av[0] = value_nib<0>(wv[p0], ws[p0]); av[1] = value_nib<1>(wv[p0], ws[p0]);
+    av[2] = value_nib<0>(wv[p1], ws[p1]); av[3] = value_nib<1>(wv[p1], ws[p1]);
+  } else {
+    av[0] = value_nib<2>(wv[p0], ws[p0]); av[1] = value_nib<3>(wv[p0], ws[p0]);
+    av[2] = value_nib<2>(wv[p1], ws[p1]); av[3] = value_nib<3>(wv[p1], ws[p1]);
+  }
+}
+// Row factor of P.V m-tile mt, row half r (0: row gid, 1: gid + 8), undone in
+// the epilogue: 2^(9 - 2p) for INT2 (p the code's 2-bit position), 2^(9 - 4p)
+// for INT4 (p = r).
+template <int BITS>
+__host__ __device__ constexpr float row_unscale(int mt, int r) {
+  return BITS == 2 ? value_unscale(2 * (mt & 3) + r) : (r ? 32.0f : 512.0f);
+}
+
 // Four fp16 values (two packed pairs) as floats.
 __device__ __forceinline__ void unpack_h4(float (&f)[4], uint32_t ab, uint32_t cd) {
   const float2 x = __half22float2(u32_as_half2(ab)), y = __half22float2(u32_as_half2(cd));
@@ -176,8 +228,10 @@ __device__ __forceinline__ float warp_allsum(float v) {
 // One warp's contiguous range of a row's 32-token blocks, streamed through
 // the warp's own NSTAGE-deep ring: lane 0 copies block i's record into slot
 // i % NSTAGE with one 1-D bulk copy completing on that slot's mbarrier.
-template <bool PAGED>
+template <bool PAGED, int BITS>
 struct WarpRing {
+  static constexpr int NSTAGE = Layout<BITS>::NSTAGE;
+  static constexpr int RB = Layout<BITS>::RL::BYTES;
   uint8_t* ring;
   uint64_t* bars;
   const uint8_t* src;   // record of the range's first block (contiguous cache)
@@ -202,7 +256,7 @@ struct WarpRing {
       }
       return pages + page * page_bytes;
     } else {
-      return src + (long long)i * kBlkBytes;
+      return src + (long long)i * RB;
     }
   }
 
@@ -219,8 +273,8 @@ struct WarpRing {
     if (lane == 0) {
       uint64_t* bar = &bars[i % NSTAGE];
       const uint8_t* rec = record(i);
-      mbar_arrive_expect_tx(bar, kBlkBytes);
-      bulk_g2s(ring + (i % NSTAGE) * kBlkBytes, rec, kBlkBytes, bar);
+      mbar_arrive_expect_tx(bar, RB);
+      bulk_g2s(ring + (i % NSTAGE) * RB, rec, RB, bar);
     }
   }
   // true on every lane once block i has landed; false if the wait gave up
@@ -229,7 +283,7 @@ struct WarpRing {
                                                      (unsigned)((i / NSTAGE) & 1), kWaitLimit));
   }
   __device__ __forceinline__ const uint8_t* slot(int i) const {
-    return ring + (i % NSTAGE) * kBlkBytes;
+    return ring + (i % NSTAGE) * RB;
   }
   // After consuming block i: refill its slot with block i + NSTAGE.
   __device__ __forceinline__ void release(int i) const {
@@ -266,9 +320,10 @@ __device__ __forceinline__ int row_blocks(const DecodeArgs& a, int b) {
   }
 }
 
-template <bool PAGED>
-__device__ __forceinline__ WarpRing<PAGED> make_ring(const DecodeArgs& a, uint8_t* smem, int b,
-                                                     int h, int split) {
+template <bool PAGED, int BITS>
+__device__ __forceinline__ WarpRing<PAGED, BITS> make_ring(const DecodeArgs& a, uint8_t* smem,
+                                                           int b, int h, int split) {
+  constexpr int NSTAGE = Layout<BITS>::NSTAGE, RB = Layout<BITS>::RL::BYTES;
   const int warp = threadIdx.x >> 5;
   const int nblk = row_blocks<PAGED>(a, b);
   int b0, b1;
@@ -287,15 +342,15 @@ __device__ __forceinline__ WarpRing<PAGED> make_ring(const DecodeArgs& a, uint8_
   const int wb0 = b0 + (int)((long long)(b1 - b0) * warp / NW);
   const int wb1 = b0 + (int)((long long)(b1 - b0) * (warp + 1) / NW);
   const long long row = (long long)b * a.Hkv + h;
-  WarpRing<PAGED> r;
-  r.ring = smem + warp * NSTAGE * kBlkBytes;
-  r.bars = reinterpret_cast<uint64_t*>(smem + NW * NSTAGE * kBlkBytes) + warp * NSTAGE;
-  r.src = a.packed + (row * (long long)(a.T_cap / kG) + wb0) * kBlkBytes;
+  WarpRing<PAGED, BITS> r;
+  r.ring = smem + warp * NSTAGE * RB;
+  r.bars = reinterpret_cast<uint64_t*>(smem + NW * NSTAGE * RB) + warp * NSTAGE;
+  r.src = a.packed + (row * (long long)(a.T_cap / kG) + wb0) * RB;
   r.n = wb1 - wb0;
   r.lane = threadIdx.x & 31;
   r.tab = PAGED ? a.block_table + (long long)b * a.max_blocks + wb0 : nullptr;
-  r.pages = a.packed + (long long)h * kBlkBytes;
-  r.page_bytes = (long long)a.Hkv * kBlkBytes;
+  r.pages = a.packed + (long long)h * RB;
+  r.page_bytes = (long long)a.Hkv * RB;
   r.n_pages = a.n_pages;
   r.status = a.status;
   return r;
@@ -344,7 +399,7 @@ __device__ __forceinline__ float scale_query(float (&qf)[32], const float* qrow,
 //  * scores, softmax and outputs: head tig mod GQ (columns 2 tig, 2 tig + 1
 //    are its hi and lo limbs), tokens gid + 8 j, j = 0..3;
 //  * P.V: channels on M as in the row layout, (head, limb of p~) on N.
-template <int GQ, bool BSCALE, class Ring>
+template <int GQ, bool BSCALE, int BITS, class Ring>
 __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
                                             MergeSmem<GQ, NW>& E, long long qrow0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -352,6 +407,8 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   const int hq = (gid >> 1) % GQ;   // head of this lane's q~ column
   const int limb = gid & 1;         // 0: hi part, 1: lo part
   const int hs = tig % GQ;          // head of this lane's scores and outputs
+  using RL = typename Layout<BITS>::RL;
+  constexpr int LW = BITS == 2 ? 2 : 4;   // key words per token and lane
   R.start();   // the first copies travel while the query is prepared
 
   // This lane's column of q' for channels 32 tig + 4 k8 + {0,1} (pair 0) and
@@ -392,31 +449,40 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   for (; it < R.n; ++it) {
     if (!R.wait(it)) break;
     const uint8_t* st = R.slot(it);
-    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + KC_OFF);
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + VC_OFF);
-    const uint4* ks4 = reinterpret_cast<const uint4*>(st + KS_OFF) + tig * 4;
-    const uint4* kz4 = reinterpret_cast<const uint4*>(st + KZ_OFF) + tig * 4;
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + RL::KC);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + RL::VC);
+    const uint4* ks4 = reinterpret_cast<const uint4*>(st + RL::KS) + tig * 4;
+    const uint4* kz4 = reinterpret_cast<const uint4*>(st + RL::KZ) + tig * 4;
     // norms, value steps and zeros of tokens gid + 8 j, j = 0..3 (adjacent
     // in the record)
-    const uint2 kn4 = *reinterpret_cast<const uint2*>(st + KN_OFF + 8 * gid);
-    const uint2 vs4 = *reinterpret_cast<const uint2*>(st + VS_OFF + 8 * gid);
-    const uint2 vz4 = *reinterpret_cast<const uint2*>(st + VZ_OFF + 8 * gid);
+    const uint2 kn4 = *reinterpret_cast<const uint2*>(st + RL::KN + 8 * gid);
+    const uint2 vs4 = *reinterpret_cast<const uint2*>(st + RL::VS + 8 * gid);
+    const uint2 vz4 = *reinterpret_cast<const uint2*>(st + RL::VZ + 8 * gid);
 
-    // key words 2 tig, 2 tig + 1 of tokens 16 mt + gid + 8 r
-    uint32_t kw[2][2][2], kw10[2][2][2];
+    // key words of tokens 16 mt + gid + 8 r: INT2 words 2 tig, 2 tig + 1
+    // (16 channels each, shifted copies w >> 10), INT4 words 4 tig .. 4 tig + 3
+    // (8 channels each, shifted copies w >> 8)
+    uint32_t kw[2][2][LW], kw10[2][2][LW];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const uint2 v = *reinterpret_cast<const uint2*>(kc + (16 * mt + gid + 8 * r) * 8 + 2 * tig);
-        kw[mt][r][0] = v.x; kw[mt][r][1] = v.y;
-        kw10[mt][r][0] = v.x >> 10; kw10[mt][r][1] = v.y >> 10;
+        if constexpr (BITS == 2) {
+          const uint2 v = *reinterpret_cast<const uint2*>(kc + (16 * mt + gid + 8 * r) * 8 + 2 * tig);
+          kw[mt][r][0] = v.x; kw[mt][r][1] = v.y;
+          kw10[mt][r][0] = v.x >> 10; kw10[mt][r][1] = v.y >> 10;
+        } else {
+          const uint4 v = *reinterpret_cast<const uint4*>(kc + (16 * mt + gid + 8 * r) * 16 + 4 * tig);
+          kw[mt][r][0] = v.x; kw[mt][r][1] = v.y; kw[mt][r][2] = v.z; kw[mt][r][3] = v.w;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) kw10[mt][r][q] = kw[mt][r][q] >> 8;
+        }
       }
     uint32_t cs[5];
     float qk_blk = qk_scale;
     if constexpr (BSCALE) {
       const int E = block_step_exp(ks4);
-      step_scales(cs, E);
+      step_scales<BITS>(cs, E);
       qk_blk = qk_scale * __int_as_float((127 - E) << 23);
     }
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -430,23 +496,42 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
         constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
         constexpr int P23[4] = {key_pos(1), key_pos(3), key_pos(5), key_pos(7)};
         uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
-        if constexpr (BSCALE) {
-          s01 = hmul2_u(s01, cs[P01[k8 & 3]]);
-          s23 = hmul2_u(s23, cs[P23[k8 & 3]]);
+        if constexpr (BITS == 2) {
+          if constexpr (BSCALE) {
+            s01 = hmul2_u(s01, cs[P01[k8 & 3]]);
+            s23 = hmul2_u(s23, cs[P23[k8 & 3]]);
+          } else {
+            if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
+            if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+          }
         } else {
-          if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
-          if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+          // INT4: pair 0 sits at nibble position 0, pair 1 at position 1
+          if constexpr (BSCALE) {
+            s01 = hmul2_u(s01, cs[0]);
+            s23 = hmul2_u(s23, cs[1]);
+          } else {
+            s23 = hmul2_u(s23, pow16_inv_h2(1));
+          }
         }
         const uint32_t r01 =
             hfma2_u(qz[k8][0], s01, hfma2_u(qhm[k8][0], s01, neg2_u(hmul2_u(qhm[k8][0], s01))));
         const uint32_t r23 =
             hfma2_u(qz[k8][1], s23, hfma2_u(qhm[k8][1], s23, neg2_u(hmul2_u(qhm[k8][1], s23))));
-        const int wd = k8 >> 2;
+        const int wd = BITS == 2 ? k8 >> 2 : k8 >> 1;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           const uint32_t wa = kw[mt][0][wd], wa10 = kw10[mt][0][wd];
           const uint32_t wb = kw[mt][1][wd], wb10 = kw10[mt][1][wd];
           uint32_t ak[4];
+          if constexpr (BITS == 4) {
+            if ((k8 & 1) == 0) {
+              ak[0] = nib_pair<0>(wa, wa10); ak[1] = nib_pair<0>(wb, wb10);
+              ak[2] = nib_pair<1>(wa, wa10); ak[3] = nib_pair<1>(wb, wb10);
+            } else {
+              ak[0] = nib_pair<2>(wa, wa10); ak[1] = nib_pair<2>(wb, wb10);
+              ak[2] = nib_pair<3>(wa, wa10); ak[3] = nib_pair<3>(wb, wb10);
+            }
+          } else
           switch (k8 & 3) {
             case 0: ak[0] = key_pair<0>(wa, wa10); ak[1] = key_pair<0>(wb, wb10);
                     ak[2] = key_pair<1>(wa, wa10); ak[3] = key_pair<1>(wb, wb10); break;
@@ -525,7 +610,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
         const float sv = svj[2 * mt + r], zv = zvj[2 * mt + r];
         const float p = fast_exp2(sc[2 * mt + r] - m_run);
         l_run += p;
-        z_run = fmaf(p, fmaf(1.5f, sv, zv), z_run);
+        z_run = fmaf(p, fmaf(Layout<BITS>::CENTER, sv, zv), z_run);
         pt[r] = p * sv;
       }
       const __half2 hh = __floats2half2_rn(pt[0], pt[1]);
@@ -537,16 +622,31 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
 
 #pragma unroll
     for (int kh = 0; kh < 2; ++kh) {
-      const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
-      const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
-      uint32_t w10[4];
+      if constexpr (BITS == 2) {
+        const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
+        const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
+        uint32_t w10[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) w10[q] = wv[q] >> 10;
+        for (int q = 0; q < 4; ++q) w10[q] = wv[q] >> 10;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t av[4];
-        value_frag(av, mt, wv, w10);
-        mma_16816_acc(O[mt], av, bp[kh][0], bp[kh][1]);
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t av[4];
+          value_frag(av, mt, wv, w10);
+          mma_16816_acc(O[mt], av, bp[kh][0], bp[kh][1]);
+        }
+      } else {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(vc + kh * 256 + lane * 4);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(vc + kh * 256 + 128 + lane * 4);
+        const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t ws[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ws[q] = wv[q] >> 8;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t av[4];
+          value_frag4(av, mt, wv, ws);
+          mma_16816_acc(O[mt], av, bp[kh][0], bp[kh][1]);
+        }
       }
     }
     R.release(it);
@@ -571,8 +671,8 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {   // undo the value rows' 2^(2p - 9)
-      E.o[warp][tig][16 * mt + gid] = (O[mt][0] + O[mt][1]) * value_unscale(2 * (mt & 3));
-      E.o[warp][tig][16 * mt + gid + 8] = (O[mt][2] + O[mt][3]) * value_unscale(2 * (mt & 3) + 1);
+      E.o[warp][tig][16 * mt + gid] = (O[mt][0] + O[mt][1]) * row_unscale<BITS>(mt, 0);
+      E.o[warp][tig][16 * mt + gid + 8] = (O[mt][2] + O[mt][3]) * row_unscale<BITS>(mt, 1);
     }
   }
 }
@@ -583,13 +683,15 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
 //    gid; B operand: key codes of token 8 nt + gid, n-tiles nt = 0..3;
 //  * scores and softmax: head gid, tokens 8 nt + 2 tig and + 1;
 //  * P.V: channels on M, the 8 heads on N, one n-tile per limb of p~.
-template <int GQ, bool BSCALE, class Ring>
+template <int GQ, bool BSCALE, int BITS, class Ring>
 __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
                                             MergeSmem<GQ, NW>& E, long long qrow0) {
   static_assert(GQ == 8, "the row layout serves groups of 8 query heads");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int head = gid;
+  using RL = typename Layout<BITS>::RL;
+  constexpr int LW = BITS == 2 ? 2 : 4;   // key words per token and lane
   R.start();   // the first copies travel while the query is prepared
 
   // Query fragments of this thread's head, channels c0 = 32*tig + 4*k8 ..+3,
@@ -630,15 +732,15 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
   for (; it < R.n; ++it) {
     if (!R.wait(it)) break;
     const uint8_t* st = R.slot(it);
-    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + KC_OFF);
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + VC_OFF);
-    const uint4* ks4 = reinterpret_cast<const uint4*>(st + KS_OFF) + tig * 4;
-    const uint4* kz4 = reinterpret_cast<const uint4*>(st + KZ_OFF) + tig * 4;
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + RL::KC);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + RL::VC);
+    const uint4* ks4 = reinterpret_cast<const uint4*>(st + RL::KS) + tig * 4;
+    const uint4* kz4 = reinterpret_cast<const uint4*>(st + RL::KZ) + tig * 4;
     // norms, value steps and zeros: halves 0..3 are tokens 2 tig + 8 nt,
     // halves 4..7 tokens 2 tig + 1 + 8 nt (nt = 0..3)
-    const uint4 kn8 = *reinterpret_cast<const uint4*>(st + KN_OFF + 16 * tig);
-    const uint4 vs8 = *reinterpret_cast<const uint4*>(st + VS_OFF + 16 * tig);
-    const uint4 vz8 = *reinterpret_cast<const uint4*>(st + VZ_OFF + 16 * tig);
+    const uint4 kn8 = *reinterpret_cast<const uint4*>(st + RL::KN + 16 * tig);
+    const uint4 vs8 = *reinterpret_cast<const uint4*>(st + RL::VS + 16 * tig);
+    const uint4 vz8 = *reinterpret_cast<const uint4*>(st + RL::VZ + 16 * tig);
 
     // Z = q'.z of the block: rows g (hi) and g+8 (lo), every column alike.
     float dz[4] = {0.f, 0.f, 0.f, 0.f};
@@ -650,12 +752,19 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
     }
 
     // Q.K^T, k-step outer: q~ fragment for k-step k8, then the 4 n-tiles.
-    uint32_t kw[4][2], kw10[4][2];
+    uint32_t kw[4][LW], kw10[4][LW];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      const uint2 v = *reinterpret_cast<const uint2*>(kc + (8 * nt + gid) * 8 + 2 * tig);
-      kw[nt][0] = v.x; kw[nt][1] = v.y;
-      kw10[nt][0] = v.x >> 10; kw10[nt][1] = v.y >> 10;
+      if constexpr (BITS == 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(kc + (8 * nt + gid) * 8 + 2 * tig);
+        kw[nt][0] = v.x; kw[nt][1] = v.y;
+        kw10[nt][0] = v.x >> 10; kw10[nt][1] = v.y >> 10;
+      } else {
+        const uint4 v = *reinterpret_cast<const uint4*>(kc + (8 * nt + gid) * 16 + 4 * tig);
+        kw[nt][0] = v.x; kw[nt][1] = v.y; kw[nt][2] = v.z; kw[nt][3] = v.w;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) kw10[nt][q] = kw[nt][q] >> 8;
+      }
     }
     // The Q.K accumulators start from zero (not from Z) so their MMA chains
     // do not wait for the Z chain; Z joins each score below.
@@ -663,7 +772,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
     float qk_blk = qk_scale;
     if constexpr (BSCALE) {
       const int E = block_step_exp(ks4);
-      step_scales(cs, E);
+      step_scales<BITS>(cs, E);
       qk_blk = qk_scale * __int_as_float((127 - E) << 23);
     }
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -679,12 +788,22 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
         constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
         constexpr int P23[4] = {key_pos(1), key_pos(3), key_pos(5), key_pos(7)};
         uint32_t s01 = hk ? sv.z : sv.x, s23 = hk ? sv.w : sv.y;
-        if constexpr (BSCALE) {
-          s01 = hmul2_u(s01, cs[P01[k8 & 3]]);
-          s23 = hmul2_u(s23, cs[P23[k8 & 3]]);
+        if constexpr (BITS == 2) {
+          if constexpr (BSCALE) {
+            s01 = hmul2_u(s01, cs[P01[k8 & 3]]);
+            s23 = hmul2_u(s23, cs[P23[k8 & 3]]);
+          } else {
+            if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
+            if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+          }
         } else {
-          if (P01[k8 & 3] != 0) s01 = hmul2_u(s01, pow4_inv_h2(P01[k8 & 3]));
-          if (P23[k8 & 3] != 0) s23 = hmul2_u(s23, pow4_inv_h2(P23[k8 & 3]));
+          // INT4: pair 0 sits at nibble position 0, pair 1 at position 1
+          if constexpr (BSCALE) {
+            s01 = hmul2_u(s01, cs[0]);
+            s23 = hmul2_u(s23, cs[1]);
+          } else {
+            s23 = hmul2_u(s23, pow16_inv_h2(1));
+          }
         }
         uint32_t at[4];
         at[0] = hmul2_u(aq[k8][0], s01);
@@ -693,8 +812,16 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
         at[3] = hfma2_u(aq[k8][3], s23, hfma2_u(aq[k8][2], s23, neg2_u(at[2])));
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-          const uint32_t w = kw[nt][k8 >> 2], w10 = kw10[nt][k8 >> 2];
+          const int wd = BITS == 2 ? k8 >> 2 : k8 >> 1;
+          const uint32_t w = kw[nt][wd], w10 = kw10[nt][wd];
           uint32_t b0v, b1v;
+          if constexpr (BITS == 4) {
+            if ((k8 & 1) == 0) {
+              b0v = nib_pair<0>(w, w10); b1v = nib_pair<1>(w, w10);
+            } else {
+              b0v = nib_pair<2>(w, w10); b1v = nib_pair<3>(w, w10);
+            }
+          } else
           switch (k8 & 3) {
             case 0: b0v = key_pair<0>(w, w10); b1v = key_pair<1>(w, w10); break;
             case 1: b0v = key_pair<2>(w, w10); b1v = key_pair<3>(w, w10); break;
@@ -764,8 +891,8 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
       const float p0 = fast_exp2(sc[2 * nt] - m_run);
       const float p1 = fast_exp2(sc[2 * nt + 1] - m_run);
       l_run += p0 + p1;
-      z_run = fmaf(p0, fmaf(1.5f, se[nt], ze[nt]), z_run);
-      z_run = fmaf(p1, fmaf(1.5f, so[nt], zo[nt]), z_run);
+      z_run = fmaf(p0, fmaf(Layout<BITS>::CENTER, se[nt], ze[nt]), z_run);
+      z_run = fmaf(p1, fmaf(Layout<BITS>::CENTER, so[nt], zo[nt]), z_run);
       pt[2 * nt] = p0 * se[nt];
       pt[2 * nt + 1] = p1 * so[nt];
     }
@@ -786,17 +913,33 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
 
 #pragma unroll
     for (int kh = 0; kh < 2; ++kh) {
-      const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
-      const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
-      uint32_t w10[4];
+      if constexpr (BITS == 2) {
+        const uint4 vw = *reinterpret_cast<const uint4*>(vc + kh * 128 + lane * 4);
+        const uint32_t wv[4] = {vw.x, vw.y, vw.z, vw.w};  // (p,hh) = (0,0) (0,1) (1,0) (1,1)
+        uint32_t w10[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) w10[q] = wv[q] >> 10;
+        for (int q = 0; q < 4; ++q) w10[q] = wv[q] >> 10;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t av[4];
-        value_frag(av, mt, wv, w10);
-        mma_16816_acc(O[0][mt], av, bp[kh][0], bp[kh][1]);
-        mma_16816_acc(O[1][mt], av, bq[kh][0], bq[kh][1]);
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t av[4];
+          value_frag(av, mt, wv, w10);
+          mma_16816_acc(O[0][mt], av, bp[kh][0], bp[kh][1]);
+          mma_16816_acc(O[1][mt], av, bq[kh][0], bq[kh][1]);
+        }
+      } else {
+        const uint4 v0 = *reinterpret_cast<const uint4*>(vc + kh * 256 + lane * 4);
+        const uint4 v1 = *reinterpret_cast<const uint4*>(vc + kh * 256 + 128 + lane * 4);
+        const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t ws[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ws[q] = wv[q] >> 8;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t av[4];
+          value_frag4(av, mt, wv, ws);
+          mma_16816_acc(O[0][mt], av, bp[kh][0], bp[kh][1]);
+          mma_16816_acc(O[1][mt], av, bq[kh][0], bq[kh][1]);
+        }
       }
     }
     R.release(it);
@@ -826,8 +969,8 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
     const int nc = 2 * tig + e;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {   // undo the value rows' 2^(2p - 9)
-      E.o[warp][nc][16 * mt + gid] = O[0][mt][e] * value_unscale(2 * (mt & 3));
-      E.o[warp][nc][16 * mt + gid + 8] = O[0][mt][2 + e] * value_unscale(2 * (mt & 3) + 1);
+      E.o[warp][nc][16 * mt + gid] = O[0][mt][e] * row_unscale<BITS>(mt, 0);
+      E.o[warp][nc][16 * mt + gid + 8] = O[0][mt][2 + e] * row_unscale<BITS>(mt, 1);
     }
   }
 }
@@ -891,22 +1034,24 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
 }
 
 // Up to 4 CTAs per SM in the column layout (128 registers), 3 in the row layout.
-// BSCALE: per-block step scale (caches with the all-heads norm scope).
-template <int GQ, bool PAGED, bool BSCALE>
+// BSCALE: per-block step scale (caches with the all-heads norm scope);
+// BITS: code width of the records (2, or the INT4 option).
+template <int GQ, bool PAGED, bool BSCALE, int BITS>
 __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
-  static_assert(sizeof(MergeSmem<GQ, NW>) <= NW * NSTAGE * kBlkBytes, "merge area");
+  static_assert(sizeof(MergeSmem<GQ, NW>) <= NW * Layout<BITS>::NSTAGE * Layout<BITS>::RL::BYTES,
+                "merge area");
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long long row = (long long)b * a.Hkv + h;
   const long long qrow0 = (long long)b * a.Hq + (long long)h * GQ;  // first query head
 
   if (split < a.num_splits) {
-    const WarpRing<PAGED> R = make_ring<PAGED>(a, smem, b, h, split);
+    const WarpRing<PAGED, BITS> R = make_ring<PAGED, BITS>(a, smem, b, h, split);
     if constexpr (GQ <= 4) {
-      packed_cols<GQ, BSCALE>(a, R, E, qrow0);
+      packed_cols<GQ, BSCALE, BITS>(a, R, E, qrow0);
     } else {
-      packed_rows<GQ, BSCALE>(a, R, E, qrow0);
+      packed_rows<GQ, BSCALE, BITS>(a, R, E, qrow0);
     }
   } else {
     residual_split<GQ, PAGED>(a, E, row, qrow0, b);
@@ -916,49 +1061,56 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
                           (long long)(a.num_splits + 1) * kRecFloats);
 }
 
-// Opt in to kSmemBytes of dynamic shared memory (needed above 48 KB), once
+// Opt in to the kernel's dynamic shared memory (above 48 KB for INT2), once
 // per instantiation and device.
-template <int GQ, bool PAGED, bool BSCALE>
+template <int GQ, bool PAGED, bool BSCALE, int BITS>
 cudaError_t allow_smem() {
   static int done[128] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED, BSCALE>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED, BSCALE, BITS>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BITS>::SMEM);
   if (e == cudaSuccess && dev >= 0 && dev < 128) done[dev] = 1;
   return e;
 }
 
-template <int GQ, bool PAGED, bool BSCALE>
+template <int GQ, bool PAGED, bool BSCALE, int BITS>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e0 = allow_smem<GQ, PAGED, BSCALE>();
+  cudaError_t e0 = allow_smem<GQ, PAGED, BSCALE, BITS>();
   if (e0 != cudaSuccess) return e0;
   dim3 grid(a.num_splits + 1, a.Hkv, a.B);
-  decode_int2_kernel<GQ, PAGED, BSCALE><<<grid, NW * 32, kSmemBytes, s>>>(a);
+  decode_int2_kernel<GQ, PAGED, BSCALE, BITS><<<grid, NW * 32, Layout<BITS>::SMEM, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_combine(a.ws, a.out, a.B * a.Hq, a.num_splits + 1, s);
 }
 
-template <bool PAGED, bool BSCALE>
+template <bool PAGED, bool BSCALE, int BITS>
 cudaError_t launch_p(const DecodeArgs& a, cudaStream_t s) {
   switch (a.Hq / a.Hkv) {
-    case 1: return launch_g<1, PAGED, BSCALE>(a, s);
-    case 2: return launch_g<2, PAGED, BSCALE>(a, s);
-    case 4: return launch_g<4, PAGED, BSCALE>(a, s);
-    case 8: return launch_g<8, PAGED, BSCALE>(a, s);
+    case 1: return launch_g<1, PAGED, BSCALE, BITS>(a, s);
+    case 2: return launch_g<2, PAGED, BSCALE, BITS>(a, s);
+    case 4: return launch_g<4, PAGED, BSCALE, BITS>(a, s);
+    case 8: return launch_g<8, PAGED, BSCALE, BITS>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
+template <int BITS>
+cudaError_t launch_b(const DecodeArgs& a, cudaStream_t s) {
+  if (a.flags & OSCAR_NORM_ALL_HEADS)
+    return a.block_table ? launch_p<true, true, BITS>(a, s) : launch_p<false, true, BITS>(a, s);
+  return a.block_table ? launch_p<true, false, BITS>(a, s) : launch_p<false, false, BITS>(a, s);
+}
+
 template <int GQ>
 int occupancy_g() {
-  if (allow_smem<GQ, false, false>() != cudaSuccess) return 0;
+  if (allow_smem<GQ, false, false, 2>() != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ, false, false>, NW * 32,
-                                                    kSmemBytes) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ, false, false, 2>,
+                                                    NW * 32, Layout<2>::SMEM) != cudaSuccess)
     return 0;
   return n;
 }
@@ -966,9 +1118,11 @@ int occupancy_g() {
 }  // namespace
 
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t s) {
-  if (a.flags & OSCAR_NORM_ALL_HEADS)
-    return a.block_table ? launch_p<true, true>(a, s) : launch_p<false, true>(a, s);
-  return a.block_table ? launch_p<true, false>(a, s) : launch_p<false, false>(a, s);
+  switch (a.bits) {
+    case 2: return launch_b<2>(a, s);
+    case 4: return launch_b<4>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 int decode_int2_ctas_per_sm(int g) {

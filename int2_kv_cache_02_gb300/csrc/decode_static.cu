@@ -67,7 +67,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   }
   if (c->n_packed < 0 || c->n_packed % kG != 0 || c->n_packed > c->T_cap || c->n_res < 0 ||
       c->n_res > kR || (c->flags & ~kAllFlags) || !target_ok(c->norm_target) ||
-      !key_group_ok(c->key_group))
+      !key_group_ok(c->key_group) || !code_bits_ok(c->bits))
     return OSCAR_ERR_INVALID_ARG;
   if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
       !std::isfinite(softmax_scale))
@@ -104,6 +104,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
+  a.bits = code_bits(c->bits);
   cudaError_t e = launch_decode_int2(a, static_cast<cudaStream_t>(stream));
   count_launches(2);
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;

@@ -28,6 +28,9 @@ inline bool target_ok(float t) {
 // Key group size as the ABI takes it: 0 means 32; otherwise 32, 64 or 128.
 inline bool key_group_ok(int g) { return g == 0 || g == 32 || g == 64 || g == 128; }
 inline int key_group(int g) { return g == 0 ? 32 : g; }
+// Code width as the ABI takes it: 0 means 2; otherwise 2 or 4.
+inline bool code_bits_ok(int b) { return b == 0 || b == 2 || b == 4; }
+inline int code_bits(int b) { return b == 0 ? 2 : b; }
 inline KeyScale key_scale(unsigned flags, float target) {
   return KeyScale{flags, target == 0.0f ? 1.0f : target};
 }
@@ -57,7 +60,7 @@ cudaError_t launch_rotate_scale_k(const uint16_t* k, int in_T, uint16_t* k_hat, 
 // of it): every channel of a group shares one step and zero.
 cudaError_t launch_quantize_kv(const uint16_t* k_hat, const __half* k_norm, const uint16_t* v,
                                int src_T, int n_tok, int B, int Hkv, int T_cap, int p0, int group,
-                               uint8_t* packed, cudaStream_t s);
+                               int bits, uint8_t* packed, cudaStream_t s);
 
 struct DecodeArgs {
   const uint8_t* packed;   // block records [B][Hkv][T_cap/32]
@@ -74,6 +77,7 @@ struct DecodeArgs {
   // the query is scaled by 2^(q_exp - e), e the exponent of its largest
   // element, so that q'*step stays in fp16 range for the cache's key scale
   int q_exp = 14;
+  int bits = 2;   // code width of the records (2 or 4)
   // paged cache (block_table != nullptr): records at packed + (page*Hkv + h)
   // * block bytes, page = block_table[b*max_blocks + block]; per-sequence
   // lengths seq_packed[b], seq_res[b] replace n_packed, n_res; n_packed
@@ -124,6 +128,7 @@ struct PagedArgs {
   unsigned* status;
   int B, Hkv, max_blocks, n_pages;
   int group;   // key group size: 32, 64 or 128 tokens
+  int bits;    // code width: 2 or 4
   KeyScale ks;
 };
 cudaError_t launch_paged_prefill(const PagedArgs& p, const uint16_t* k, const uint16_t* v,
@@ -133,8 +138,8 @@ cudaError_t launch_paged_append(const PagedArgs& p, const uint16_t* k_new, const
 
 // Fused rotate + scale + quantise of n_tok tokens of raw keys and values.
 cudaError_t launch_prefill_kv(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,
-                              int Hkv, int T_cap, int p0, int group, KeyScale ks, uint8_t* packed,
-                              cudaStream_t s);
+                              int Hkv, int T_cap, int p0, int group, int bits, KeyScale ks,
+                              uint8_t* packed, cudaStream_t s);
 
 // One CTA polls an mbarrier nothing arrives at, `iterations` times, then
 // records kDevErrWaitTimeout in *status (self-test of the bounded waits).

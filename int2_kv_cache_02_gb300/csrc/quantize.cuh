@@ -1,4 +1,4 @@
-// INT2 quantisation and packing of one 32-token block of keys and values,
+// INT2 (or INT4) quantisation and packing of one 32-token block of keys and values,
 // shared by quantize_kv_kernel and the fused prefill kernel (kernel (2) of the
 // news article on arXiv 2605.19660, 三).
 //
@@ -17,24 +17,31 @@
 
 namespace oscar {
 
+// Largest code of a BITS-bit quantiser (3 for INT2, 15 for INT4).
+template <int BITS>
+constexpr float kMaxCode = (float)((1 << BITS) - 1);
+
+template <int BITS>
 __device__ __forceinline__ uint8_t quant_code(float x, float mn, float step, bool live) {
   if (!live) return 0;
   const float t = __fdiv_rn(__fsub_rn(x, mn), step);
   float r = rintf(t);
-  r = fminf(fmaxf(r, 0.0f), 3.0f);
+  r = fminf(fmaxf(r, 0.0f), kMaxCode<BITS>);
   return (uint8_t)r;
 }
 
 // The same code with the quotient formed as a * (1/step): the correctly
-// rounded reciprocal times a is within ~2^-21 of the rounded quotient for
-// quotients up to 4, so both round to the same integer unless the quotient
-// lies within 1e-5 of a half-integer, where the exact division decides.
+// rounded reciprocal times a is within ~2^-21 (relative) of the rounded
+// quotient, ~2^-19 absolute for quotients up to 16, so both round to the
+// same integer unless the quotient lies within 1e-5 of a half-integer,
+// where the exact division decides.
+template <int BITS>
 __device__ __forceinline__ uint8_t quant_code_fast(float x, float mn, float step, float rstep,
                                                    bool live) {
   if (!live) return 0;
   const float q = __fsub_rn(x, mn) * rstep;
-  if (fabsf(q - floorf(q) - 0.5f) < 1e-5f) return quant_code(x, mn, step, live);
-  return (uint8_t)fminf(fmaxf(rintf(q), 0.0f), 3.0f);
+  if (fabsf(q - floorf(q) - 0.5f) < 1e-5f) return quant_code<BITS>(x, mn, step, live);
+  return (uint8_t)fminf(fmaxf(rintf(q), 0.0f), kMaxCode<BITS>);
 }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
@@ -47,7 +54,7 @@ struct KeyParams {
   float mn, step, rstep;
   bool live;
 };
-template <int N>
+template <int N, int BITS>
 __device__ __forceinline__ KeyParams key_params(const uint16_t (*kt)[kD]) {
   const int c = threadIdx.x;
   float mn = bf16_bits_to_float(kt[0][c]), mx = mn;
@@ -60,7 +67,7 @@ __device__ __forceinline__ KeyParams key_params(const uint16_t (*kt)[kD]) {
   KeyParams p;
   p.live = mx > mn;
   p.mn = mn;
-  p.step = p.live ? __fdiv_rn(__fsub_rn(mx, mn), 3.0f) : 0.0f;
+  p.step = p.live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
   p.rstep = p.live ? __frcp_rn(p.step) : 0.0f;
   return p;
 }
@@ -69,27 +76,30 @@ __device__ __forceinline__ KeyParams key_params(const uint16_t (*kt)[kD]) {
 // the staging of kt (rotated, scaled keys as bf16) and vt (values as bf16)
 // for the 32 tokens of one block; kp: this thread's key channel parameters
 // over the block's group; norms: the block's 32 key norms (global or shared
-// memory).  Writes the block record at rec (layout in oscar.h).
+// memory).  Writes the block record at rec (layout in oscar.h for BITS).
+template <int BITS>
 __device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
                                                const uint16_t (&vt)[kG][kD],
                                                uint8_t (&kc)[kG][kD], uint8_t (&vc)[kG][kD],
                                                const __half* norms, uint8_t* rec,
                                                const KeyParams& kp) {
   const int tid = threadIdx.x;
-  uint32_t* k_codes = reinterpret_cast<uint32_t*>(rec + kRecKC);
-  uint32_t* v_codes = reinterpret_cast<uint32_t*>(rec + kRecVC);
-  __half* k_scale = reinterpret_cast<__half*>(rec + kRecKS);
-  __half* k_zero = reinterpret_cast<__half*>(rec + kRecKZ);
-  __half* k_norm_out = reinterpret_cast<__half*>(rec + kRecKN);
-  __half* v_scale = reinterpret_cast<__half*>(rec + kRecVS);
-  __half* v_zero = reinterpret_cast<__half*>(rec + kRecVZ);
+  using RL = Rec<BITS>;
+  uint32_t* k_codes = reinterpret_cast<uint32_t*>(rec + RL::KC);
+  uint32_t* v_codes = reinterpret_cast<uint32_t*>(rec + RL::VC);
+  __half* k_scale = reinterpret_cast<__half*>(rec + RL::KS);
+  __half* k_zero = reinterpret_cast<__half*>(rec + RL::KZ);
+  __half* k_norm_out = reinterpret_cast<__half*>(rec + RL::KN);
+  __half* v_scale = reinterpret_cast<__half*>(rec + RL::VS);
+  __half* v_zero = reinterpret_cast<__half*>(rec + RL::VZ);
 
   // Keys: thread = channel, with its group's parameters.
   {
     const int c = tid;
 #pragma unroll 8
     for (int t = 0; t < kG; ++t)
-      kc[t][c] = quant_code_fast(bf16_bits_to_float(kt[t][c]), kp.mn, kp.step, kp.rstep, kp.live);
+      kc[t][c] = quant_code_fast<BITS>(bf16_bits_to_float(kt[t][c]), kp.mn, kp.step, kp.rstep,
+                                       kp.live);
     k_scale[c] = __float2half_rn(kp.step);
     k_zero[c] = __float2half_rn(kp.mn);
   }
@@ -111,10 +121,11 @@ __device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
       }
       const bool live = mx > mn;
-      const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), 3.0f) : 0.0f;
+      const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
       const float rstep = live ? __frcp_rn(step) : 0.0f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) vc[t][4 * lane + j] = quant_code_fast(x[j], mn, step, rstep, live);
+      for (int j = 0; j < 4; ++j)
+        vc[t][4 * lane + j] = quant_code_fast<BITS>(x[j], mn, step, rstep, live);
       if (lane == 0) {
         v_scale[tok_slot(t)] = __float2half_rn(step);
         v_zero[tok_slot(t)] = __float2half_rn(mn);
@@ -124,34 +135,68 @@ __device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
   if (tid < kG) k_norm_out[tok_slot(tid)] = norms[tid];
   __syncthreads();
 
-  // Pack keys: word (t, w) = channels 16w..16w+15 of token t; channel 16w+j at
-  // bit 2*(j/2) + 16*(j%2).
+  if constexpr (BITS == 2) {
+    // Pack keys: word (t, w) = channels 16w..16w+15 of token t; channel 16w+j
+    // at bit 2*(j/2) + 16*(j%2).
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int wi = tid + 128 * r;
-    const int t = wi >> 3, w = wi & 7;
-    const uint8_t* src = &kc[t][16 * w];
-    uint32_t word = 0;
+    for (int r = 0; r < 2; ++r) {
+      const int wi = tid + 128 * r;
+      const int t = wi >> 3, w = wi & 7;
+      const uint8_t* src = &kc[t][16 * w];
+      uint32_t word = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) word |= (uint32_t)src[j] << (2 * (j >> 1) + 16 * (j & 1));
-    k_codes[t * 8 + w] = word;
-  }
-  // Pack values: word 128*kh + 4*lane + 2p + hh, lane = 4g + t4; low half token
-  // 16kh + 2*t4 + 8p, high half the next token; slot k = channel g + 8*(8hh+k).
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int wi = tid + 128 * r;
-    const int kh = wi >> 7, lane = (wi >> 2) & 31, p = (wi >> 1) & 1, hh = wi & 1;
-    const int g = lane >> 2, t4 = lane & 3;
-    const int tok = 16 * kh + 2 * t4 + 8 * p;
-    uint32_t word = 0;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int ch = g + 8 * (8 * hh + k);
-      word |= (uint32_t)vc[tok][ch] << (2 * k);
-      word |= (uint32_t)vc[tok + 1][ch] << (16 + 2 * k);
+      for (int j = 0; j < 16; ++j) word |= (uint32_t)src[j] << (2 * (j >> 1) + 16 * (j & 1));
+      k_codes[t * 8 + w] = word;
     }
-    v_codes[wi] = word;
+    // Pack values: word 128*kh + 4*lane + 2p + hh, lane = 4g + t4; low half
+    // token 16kh + 2*t4 + 8p, high half the next token; slot k = channel
+    // g + 8*(8hh+k).
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int wi = tid + 128 * r;
+      const int kh = wi >> 7, lane = (wi >> 2) & 31, p = (wi >> 1) & 1, hh = wi & 1;
+      const int g = lane >> 2, t4 = lane & 3;
+      const int tok = 16 * kh + 2 * t4 + 8 * p;
+      uint32_t word = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int ch = g + 8 * (8 * hh + k);
+        word |= (uint32_t)vc[tok][ch] << (2 * k);
+        word |= (uint32_t)vc[tok + 1][ch] << (16 + 2 * k);
+      }
+      v_codes[wi] = word;
+    }
+  } else {
+    // INT4 keys: word (t, w) = channels 8w..8w+7 of token t; channel 8w+j at
+    // bit 4*(j/2) + 16*(j%2).
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int wi = tid + 128 * r;
+      const int t = wi >> 4, w = wi & 15;
+      const uint8_t* src = &kc[t][8 * w];
+      uint32_t word = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) word |= (uint32_t)src[j] << (4 * (j >> 1) + 16 * (j & 1));
+      k_codes[t * 16 + w] = word;
+    }
+    // INT4 values: word 256*kh + 128p + 4*lane + hh, lane = 4g + t4; low
+    // half token 16kh + 2*t4 + 8p, high half the next token; slot k (4 bits)
+    // = channel g + 8*(4hh+k).
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int wi = tid + 128 * r;
+      const int kh = wi >> 8, p = (wi >> 7) & 1, lane = (wi >> 2) & 31, hh = wi & 3;
+      const int g = lane >> 2, t4 = lane & 3;
+      const int tok = 16 * kh + 2 * t4 + 8 * p;
+      uint32_t word = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int ch = g + 8 * (4 * hh + k);
+        word |= (uint32_t)vc[tok][ch] << (4 * k);
+        word |= (uint32_t)vc[tok + 1][ch] << (16 + 4 * k);
+      }
+      v_codes[wi] = word;
+    }
   }
 }
 

@@ -36,7 +36,7 @@ class OscarCacheStruct(ctypes.Structure):
                 ("packed", c_void_p),
                 ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
                 ("n_packed", c_int), ("n_res", c_int), ("flags", c_uint),
-                ("norm_target", c_float), ("key_group", c_int)]
+                ("norm_target", c_float), ("key_group", c_int), ("bits", c_int)]
 
 
 class OscarPagedCacheStruct(ctypes.Structure):
@@ -44,15 +44,25 @@ class OscarPagedCacheStruct(ctypes.Structure):
                 ("pages", c_void_p), ("block_table", c_void_p),
                 ("n_packed", c_void_p), ("n_res", c_void_p),
                 ("k_res", c_void_p), ("v_res", c_void_p), ("k_res_norm", c_void_p),
-                ("flags", c_uint), ("norm_target", c_float), ("key_group", c_int)]
+                ("flags", c_uint), ("norm_target", c_float), ("key_group", c_int),
+                ("bits", c_int)]
 
 
 BLOCK_BYTES = 2752
+BLOCK_BYTES_INT4 = 4800
 # byte ranges of the fields of one 32-token block record (include/oscar.h)
 RECORD_FIELDS = {"k_codes": (0, 1024), "v_codes": (1024, 2048), "k_scale": (2048, 2304),
                  "k_zero": (2304, 2560), "k_norm": (2560, 2624), "v_scale": (2624, 2688),
                  "v_zero": (2688, 2752)}
+# the INT4 record: twice the code bytes, the same side arrays after them
+RECORD_FIELDS_INT4 = {"k_codes": (0, 2048), "v_codes": (2048, 4096), "k_scale": (4096, 4352),
+                      "k_zero": (4352, 4608), "k_norm": (4608, 4672), "v_scale": (4672, 4736),
+                      "v_zero": (4736, 4800)}
 PER_TOKEN_FIELDS = ("k_norm", "v_scale", "v_zero")
+
+
+def record_bytes(bits: int = 2) -> int:
+    return BLOCK_BYTES_INT4 if bits == 4 else BLOCK_BYTES
 
 
 def _load() -> ctypes.CDLL:
@@ -132,11 +142,11 @@ class KVCache:
     oscar_cache struct that points at them (layouts in include/oscar.h)."""
 
     def __init__(self, B: int, Hkv: int, T_cap: int, flags: int = 0, device=None,
-                 norm_target: float = 0.0, key_group: int = 0):
+                 norm_target: float = 0.0, key_group: int = 0, bits: int = 0):
         if T_cap % G:
             raise ValueError("T_cap must be a multiple of 32")
         dev = torch.device(device if device is not None else "cuda")
-        self.packed = torch.zeros((B, Hkv, T_cap // G, BLOCK_BYTES), dtype=torch.uint8,
+        self.packed = torch.zeros((B, Hkv, T_cap // G, record_bytes(bits)), dtype=torch.uint8,
                                   device=dev)
         self.k_res = torch.zeros((B, Hkv, R, D), dtype=torch.bfloat16, device=dev)
         self.v_res = torch.zeros((B, Hkv, R, D), dtype=torch.bfloat16, device=dev)
@@ -147,6 +157,7 @@ class KVCache:
             setattr(s, name, getattr(self, name).data_ptr())
         s.n_packed, s.n_res, s.flags, s.norm_target = 0, 0, flags, norm_target
         s.key_group = key_group
+        s.bits = bits
         self.struct = s
 
     B = property(lambda self: self.struct.B)
@@ -157,16 +168,17 @@ class KVCache:
     flags = property(lambda self: self.struct.flags)
     norm_target = property(lambda self: self.struct.norm_target)
     key_group = property(lambda self: self.struct.key_group or 32)
+    bits = property(lambda self: self.struct.bits or 2)
 
     def ref(self):
         return ctypes.byref(self.struct)
 
     def field(self, name: str) -> torch.Tensor:
         """Writable view of one record field for every block:
-        [B][Hkv][T_cap/32][n] with n = 256 words (codes) or 128 halves (key
+        [B][Hkv][T_cap/32][n] with n = 256 words (codes; INT4: 512) or 128 halves (key
         step / zero); the per-token arrays (k_norm, v_scale, v_zero) as
         [B][Hkv][T_cap/32][4][8], element [j][i] = token 8j + i of the block."""
-        lo, hi = RECORD_FIELDS[name]
+        lo, hi = (RECORD_FIELDS_INT4 if self.bits == 4 else RECORD_FIELDS)[name]
         raw = self.packed[..., lo:hi]
         if name.endswith("codes"):
             return raw.view(torch.int32)
@@ -177,12 +189,12 @@ class KVCache:
         return f
 
     def tokens(self, name: str) -> torch.Tensor:
-        """A copy of a field in token order: key codes [B][Hkv][T_cap][8];
-        norms and value step / zero [B][Hkv][T_cap]; value codes and key
-        step / zero stay per block ([B][Hkv][T_cap/32][n])."""
+        """A copy of a field in token order: key codes [B][Hkv][T_cap][8]
+        (INT4: [..][16]); norms and value step / zero [B][Hkv][T_cap]; value
+        codes and key step / zero stay per block ([B][Hkv][T_cap/32][n])."""
         f = self.field(name)
         if name == "k_codes":
-            return f.reshape(self.B, self.Hkv, self.T_cap, 8)
+            return f.reshape(self.B, self.Hkv, self.T_cap, 4 * self.bits)
         if name in PER_TOKEN_FIELDS:
             return f.reshape(self.B, self.Hkv, self.T_cap)
         return f.clone()
@@ -201,9 +213,10 @@ class PagedKVCache:
     allocator below; the device kernels only follow the table."""
 
     def __init__(self, B: int, Hkv: int, max_blocks: int, n_pages: int, flags: int = 0,
-                 device=None, norm_target: float = 0.0, key_group: int = 0):
+                 device=None, norm_target: float = 0.0, key_group: int = 0, bits: int = 0):
         dev = torch.device(device if device is not None else "cuda")
-        self.pages = torch.zeros((n_pages, Hkv, BLOCK_BYTES), dtype=torch.uint8, device=dev)
+        self.pages = torch.zeros((n_pages, Hkv, record_bytes(bits)), dtype=torch.uint8,
+                                 device=dev)
         self.block_table = torch.full((B, max_blocks), -1, dtype=torch.int32, device=dev)
         self.n_packed_d = torch.zeros(B, dtype=torch.int32, device=dev)
         self.n_res_d = torch.zeros(B, dtype=torch.int32, device=dev)
@@ -214,6 +227,7 @@ class PagedKVCache:
         s.B, s.Hkv, s.max_blocks, s.n_pages, s.flags = B, Hkv, max_blocks, n_pages, flags
         s.norm_target = norm_target
         s.key_group = key_group
+        s.bits = bits
         s.pages = self.pages.data_ptr()
         s.block_table = self.block_table.data_ptr()
         s.n_packed = self.n_packed_d.data_ptr()

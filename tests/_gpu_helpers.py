@@ -59,8 +59,10 @@ def upload_oracle_cache(cache, heads: dict, flags: int = 0, norm_target: float =
             nb = p // 32
             put = lambda name, arr: cache.field(name)[b, h, :nb].copy_(
                 torch.from_numpy(np.ascontiguousarray(arr)))
-            put("k_codes", O.pack_k_words(kq.codes).reshape(nb, 256).view(np.int32))
-            put("v_codes", O.pack_v_words(vq.codes).view(np.int32))
+            bits = getattr(cache, "bits", 2)
+            put("k_codes", O.pack_words(kq.codes, bits, "k").reshape(nb, 128 * bits)
+                .view(np.int32))
+            put("v_codes", O.pack_words(vq.codes, bits, "v").view(np.int32))
             ks16, kz16 = kq.block_params()
             put("k_scale", ks16)
             put("k_zero", kz16)

@@ -75,6 +75,7 @@ def _cache(**kw):
     s.n_packed, s.n_res, s.flags = kw.get("n_packed", 0), kw.get("n_res", 0), kw.get("flags", 0)
     s.norm_target = kw.get("norm_target", 0.0)
     s.key_group = kw.get("key_group", 0)
+    s.bits = kw.get("bits", 0)
     return s
 
 
@@ -135,6 +136,10 @@ def test_cache_validation_and_state_untouched():
     # key groups: only 32 (0), 64, 128; n_packed and quantised runs multiples of it
     for bad in (_cache(key_group=48), _cache(key_group=256), _cache(key_group=64, n_packed=32)):
         assert L.oscar_prefill_kv(ctypes.byref(bad), P(FAKE), P(FAKE), 64, 64, None) == 1
+    for bad in (_cache(bits=3), _cache(bits=8), _cache(bits=1)):
+        assert L.oscar_prefill_kv(ctypes.byref(bad), P(FAKE), P(FAKE), 64, 64, None) == 1
+        assert L.oscar_decode_attention_static_ws(ctypes.byref(bad), P(FAKE), 2, 0.1, P(FAKE),
+                                                  1, None) == 1
     g128 = _cache(key_group=128)
     assert L.oscar_prefill_kv(ctypes.byref(g128), P(FAKE), P(FAKE), 64, 64, None) == 1
     assert L.oscar_quantize_kv(ctypes.byref(g128), P(FAKE), P(FAKE), P(FAKE), 192, 192, None) == 1
@@ -168,6 +173,7 @@ def _paged(**kw):
     s.flags = kw.get("flags", 0)
     s.norm_target = kw.get("norm_target", 0.0)
     s.key_group = kw.get("key_group", 0)
+    s.bits = kw.get("bits", 0)
     return s
 
 
@@ -180,7 +186,7 @@ def test_paged_validation():
     assert L.oscar_paged_append_kv(ctypes.byref(bad), P(FAKE), P(FAKE), None, None) == 1
     mis = _paged(pages=FAKE + 8)
     assert L.oscar_paged_append_kv(ctypes.byref(mis), P(FAKE), P(FAKE), None, None) == 3
-    for bad in (_paged(flags=8), _paged(norm_target=1e-3), _paged(key_group=96)):
+    for bad in (_paged(flags=8), _paged(norm_target=1e-3), _paged(key_group=96), _paged(bits=3)):
         assert L.oscar_paged_append_kv(ctypes.byref(bad), P(FAKE), P(FAKE), None, None) == 1
     g128 = _paged(key_group=128)
     assert L.oscar_paged_prefill_kv(ctypes.byref(g128), P(FAKE), P(FAKE), 64, P(FAKE), 64,
