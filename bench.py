@@ -51,6 +51,8 @@ def _args():
     p.add_argument("--e2e-steps", type=int, default=256)
     p.add_argument("--no-paged", action="store_true",
                    help="skip the paged-cache decode over a variable-length batch")
+    p.add_argument("--no-int4", action="store_true",
+                   help="skip the INT4-option decode of the same workload")
     p.add_argument("--no-prefill", action="store_true",
                    help="skip the prefill timing (fused vs two-call) of the prompt")
     p.add_argument("--num-splits", type=int, default=0,
@@ -525,6 +527,43 @@ def run_ours(args, world, rank, local):
                          "handed out in a shuffled order"}
         del pc, wsp
         torch.cuda.empty_cache()
+    # ---- INT4 option: the same prompt in 4800-byte records, decode only ----
+    int4 = None
+    if not args.no_int4 and wl.n_packed:
+        c4 = L.KVCache(wl.B, wl.Hkv, wl.n_packed, device=dev, bits=4)
+        L.prefill_kv(c4, K, V, n_tok=wl.n_packed, in_T=wl.T0)
+        if wl.n_res:
+            L.append_kv(c4, K[:, :, wl.n_packed:wl.T0].contiguous(),
+                        V[:, :, wl.n_packed:wl.T0].contiguous(), n_tok=wl.n_res)
+        S4 = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, c4.n_packed)
+        ws4 = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, c4.n_packed, S4),
+                                device=dev)
+        L.rotate_q(Q[0], qr)
+        for _ in range(3):
+            L.decode_attention(c4, qr, wl.Hq, tau, out, ws4, num_splits=S4)
+        torch.cuda.synchronize()
+        reps = 20
+        a = torch.cuda.Event(enable_timing=True)
+        b_ = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            L.decode_attention(c4, qr, wl.Hq, tau, out, ws4, num_splits=S4)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        if L.device_status() != 0:
+            raise RuntimeError("INT4 decode recorded a device error")
+        i_ms = a.elapsed_time(b_) / reps
+        rows = wl.B * wl.Hkv
+        i_bytes = (rows * (c4.n_packed * 150 + c4.n_res * 514)
+                   + 2 * wl.B * wl.Hq * 128 * 4 + 2 * wl.B * wl.Hq * (S4 + 1) * 132 * 4)
+        i_gbs = i_bytes / (i_ms * 1e-3) / 1e9
+        int4 = {"packed_tokens": c4.n_packed, "residual_tokens": c4.n_res, "num_splits": S4,
+                "decode_us": i_ms * 1e3, "GB/s": i_gbs,
+                "frac": i_gbs / (peaks.get("hbm_gbs") or 6800.0),
+                "note": "INT4 option (16 levels, 150 B per packed token-head) over the same "
+                        "prompt; L2 not flushed between the 20 reps (7.5 GB of records)"}
+        del c4, ws4
+        torch.cuda.empty_cache()
     peak = peaks.get("hbm_gbs")
     peak_src = "of measured" if peak else "of fallback"
     peak = peak or 6800.0
@@ -551,6 +590,7 @@ def run_ours(args, world, rank, local):
         "decode_tokens_per_s": world * wl.B / (ms_step * 1e-3),
         "prefill": prefill,
         "paged": paged,
+        "int4": int4,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src, "traffic": traffic,
                      "kernel": "oscar_decode_attention (fused INT2 decode + LSE combine)",
