@@ -106,17 +106,25 @@ __global__ void __launch_bounds__(128) prefill_kv_kernel(
   stage_values(S.vt, v + src_tok * kD);
   // with the all-heads norm, head 0 of this sequence's token src_tok
   const long long head0_tok = src_tok - (long long)blockIdx.y * in_T;
-#pragma unroll 2
-  for (int i = 0; i < GS / 4; ++i) {
-    const int t = (GS / 4) * warp + i;
-    float s_all = 0.0f;
-    if (!PLAIN && (ks.flags & OSCAR_NORM_ALL_HEADS))
-      s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, Hkv, lane);
-    const uint2 raw = reinterpret_cast<const uint2*>(k + (src_tok + t) * kD)[lane];
-    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    const float norm = rotate_scale_key<PLAIN>(x, lane, ks, s_all);
-    reinterpret_cast<uint2*>(&S.kt[t][0])[lane] = pack_bf16x4(x);
-    if (lane == 0) S.ns[t] = __float2half_rn(norm);
+  // 8 tokens' raw keys are loaded before any is transformed, so their loads
+  // overlap one another rather than each FHT waiting on its own
+#pragma unroll 1
+  for (int i0 = 0; i0 < GS / 4; i0 += 8) {
+    uint2 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      raw[i] = reinterpret_cast<const uint2*>(k + (src_tok + (GS / 4) * warp + i0 + i) * kD)[lane];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = (GS / 4) * warp + i0 + i;
+      float s_all = 0.0f;
+      if (!PLAIN && (ks.flags & OSCAR_NORM_ALL_HEADS))
+        s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, Hkv, lane);
+      float x[4] = {bf16_lo(raw[i].x), bf16_hi(raw[i].x), bf16_lo(raw[i].y), bf16_hi(raw[i].y)};
+      const float norm = rotate_scale_key<PLAIN>(x, lane, ks, s_all);
+      reinterpret_cast<uint2*>(&S.kt[t][0])[lane] = pack_bf16x4(x);
+      if (lane == 0) S.ns[t] = __float2half_rn(norm);
+    }
   }
   __syncthreads();
   constexpr int RB = Rec<BITS>::BYTES;
@@ -167,17 +175,23 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(PagedArgs p,
   const long long src_tok = ((long long)b * p.Hkv + h) * in_T + (long long)j * GS;
   stage_values(S.vt, v + src_tok * kD);
   const long long head0_tok = src_tok - (long long)h * in_T;
-#pragma unroll 2
-  for (int i = 0; i < GS / 4; ++i) {
-    const int t = (GS / 4) * warp + i;
-    float s_all = 0.0f;
-    if (!PLAIN && (p.ks.flags & OSCAR_NORM_ALL_HEADS))
-      s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, p.Hkv, lane);
-    const uint2 raw = reinterpret_cast<const uint2*>(k + (src_tok + t) * kD)[lane];
-    float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
-    const float norm = rotate_scale_key<PLAIN>(x, lane, p.ks, s_all);
-    reinterpret_cast<uint2*>(&S.kt[t][0])[lane] = pack_bf16x4(x);
-    if (lane == 0) S.ns[t] = __float2half_rn(norm);
+#pragma unroll 1
+  for (int i0 = 0; i0 < GS / 4; i0 += 8) {
+    uint2 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      raw[i] = reinterpret_cast<const uint2*>(k + (src_tok + (GS / 4) * warp + i0 + i) * kD)[lane];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = (GS / 4) * warp + i0 + i;
+      float s_all = 0.0f;
+      if (!PLAIN && (p.ks.flags & OSCAR_NORM_ALL_HEADS))
+        s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, p.Hkv, lane);
+      float x[4] = {bf16_lo(raw[i].x), bf16_hi(raw[i].x), bf16_lo(raw[i].y), bf16_hi(raw[i].y)};
+      const float norm = rotate_scale_key<PLAIN>(x, lane, p.ks, s_all);
+      reinterpret_cast<uint2*>(&S.kt[t][0])[lane] = pack_bf16x4(x);
+      if (lane == 0) S.ns[t] = __float2half_rn(norm);
+    }
   }
   __syncthreads();
   quantize_group<GS, BITS>(S, S.ns, v + src_tok * kD,

@@ -44,6 +44,25 @@ __device__ __forceinline__ uint8_t quant_code_fast(float x, float mn, float step
   return (uint8_t)fminf(fmaxf(rintf(q), 0.0f), kMaxCode<BITS>);
 }
 
+// The fast code without a branch: c = round-half-even(q), q = (x - mn) /
+// step formed as (x - mn) * (1/step) (0 for a constant group, whose step and
+// reciprocal are 0 and x == mn).  dist keeps the largest |q - c| seen; above
+// kNearHalf, some quotient may lie within 1e-5 of a half-integer (the case
+// quant_code_fast hands to the exact division), and the caller redoes the
+// warp's codes with quant_code_fast, so the codes are always those of
+// quant_code_fast.  (|q - c| is exact and 0.5 - |q - c| equals
+// |q - floor(q) - 0.5| wherever either is below 0.25; the threshold keeps a
+// margin of 1e-5 over that test, so a redo may happen needlessly, never be
+// missed.)
+template <int BITS>
+__device__ __forceinline__ uint8_t quant_code_nb(float x, float mn, float rstep, float& dist) {
+  const float q = __fsub_rn(x, mn) * rstep;
+  const int c = __float2int_rn(q);
+  dist = fmaxf(dist, fabsf(q - (float)c));
+  return (uint8_t)min(c, (1 << BITS) - 1);
+}
+constexpr float kNearHalf = 0.5f - 2e-5f;
+
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
   return __uint_as_float(((uint32_t)u) << 16);
 }
@@ -93,13 +112,19 @@ __device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
   __half* v_scale = reinterpret_cast<__half*>(rec + RL::VS);
   __half* v_zero = reinterpret_cast<__half*>(rec + RL::VZ);
 
-  // Keys: thread = channel, with its group's parameters.
+  // Keys: thread = channel, with its group's parameters.  Codes without a
+  // branch; the rare quotients near a half-integer are redone exactly.
   {
     const int c = tid;
+    float dist = 0.0f;
 #pragma unroll 8
     for (int t = 0; t < kG; ++t)
-      kc[t][c] = quant_code_fast<BITS>(bf16_bits_to_float(kt[t][c]), kp.mn, kp.step, kp.rstep,
-                                       kp.live);
+      kc[t][c] = quant_code_nb<BITS>(bf16_bits_to_float(kt[t][c]), kp.mn, kp.rstep, dist);
+    if (__any_sync(0xffffffffu, dist > kNearHalf)) {
+      for (int t = 0; t < kG; ++t)
+        kc[t][c] = quant_code_fast<BITS>(bf16_bits_to_float(kt[t][c]), kp.mn, kp.step, kp.rstep,
+                                         kp.live);
+    }
     k_scale[c] = __float2half_rn(kp.step);
     k_zero[c] = __float2half_rn(kp.mn);
   }
@@ -123,9 +148,16 @@ __device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
       const bool live = mx > mn;
       const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
       const float rstep = live ? __frcp_rn(step) : 0.0f;
+      float dist = 0.0f;
+      uint8_t cv[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        vc[t][4 * lane + j] = quant_code_fast<BITS>(x[j], mn, step, rstep, live);
+      for (int j = 0; j < 4; ++j) cv[j] = quant_code_nb<BITS>(x[j], mn, rstep, dist);
+      if (__any_sync(0xffffffffu, dist > kNearHalf)) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cv[j] = quant_code_fast<BITS>(x[j], mn, step, rstep, live);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) vc[t][4 * lane + j] = cv[j];
       if (lane == 0) {
         v_scale[tok_slot(t)] = __float2half_rn(step);
         v_zero[tok_slot(t)] = __float2half_rn(mn);

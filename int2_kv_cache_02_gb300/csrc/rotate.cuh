@@ -19,11 +19,13 @@ __device__ __forceinline__ void fht128(float (&x)[4], int lane) {
   x[0] = a + c; x[2] = a - c; x[1] = b + d; x[3] = b - d;
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
-    const bool upper = (lane & m) != 0;
+    // upper lanes take y - x, lower lanes x + y: one fma with a +-1 factor,
+    // the same single rounding as the subtraction or the addition
+    const float sg = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const float y = __shfl_xor_sync(0xffffffffu, x[r], m);
-      x[r] = upper ? (y - x[r]) : (x[r] + y);
+      x[r] = fmaf(sg, x[r], y);
     }
   }
 }

@@ -138,7 +138,7 @@ def draw_q_cuda(wl: Workload, step: int, device="cuda"):
 
 def build_cache_cuda(wl: Workload, K, V, flags: int = 0, T_cap: int | None = None,
                      chunk: int = 8192, device="cuda", fused: bool = True,
-                     norm_target: float = 0.0):
+                     norm_target: float = 0.0, bits: int = 0):
     """Prompt of T0 tokens -> OScaR cache: rotate + scale + quantise the first
     n_packed tokens, then append the remaining ones to the residual window.
     fused=True does the first part in one oscar_prefill_kv call; fused=False
@@ -148,7 +148,7 @@ def build_cache_cuda(wl: Workload, K, V, flags: int = 0, T_cap: int | None = Non
     from . import oscar
     T_cap = T_cap if T_cap is not None else wl.t_cap()
     cache = oscar.KVCache(wl.B, wl.Hkv, T_cap, flags=flags, device=device,
-                          norm_target=norm_target)
+                          norm_target=norm_target, bits=bits)
     T_stride = K.shape[2]
     if fused:
         if wl.n_packed:
