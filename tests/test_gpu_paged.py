@@ -173,3 +173,48 @@ def test_paged_bad_page_is_reported(L):
     L.paged_decode_attention(cache, qr, Hq, TAU, 64, out, ws, num_splits=1)
     assert L.device_status() == DEVICE_STATUS
     assert L.device_status() == 0
+
+
+def test_paged_batch48_variable_lengths_sampled(L):
+    """Full size, as the benchmark's paged measurement runs it: 48 sequences of
+    the batch48_128k prompt cut to lengths drawn in [n/4, n], pages handed
+    out in a shuffled order, one appended token each, the planned split
+    count; sampled (sequence, head) rows against the oracle."""
+    from int2_kv_cache_02_gb300 import workloads as W
+    wl = W.WORKLOADS["batch48_128k"]
+    rng = np.random.default_rng(12345)
+    n_tok = [int(x) // 32 * 32 for x in rng.integers(wl.n_packed // 4, wl.n_packed + 1, size=wl.B)]
+    blocks = [n // 32 + 4 for n in n_tok]
+    pc = L.PagedKVCache(wl.B, wl.Hkv, max(blocks), n_pages=sum(blocks))
+    pc.map_blocks(0, 0, order=list(rng.permutation(sum(blocks))))
+    for b in range(wl.B):
+        pc.map_blocks(b, blocks[b])
+    K, V = W.draw_kv_cuda(wl, 0, wl.T0)
+    L.paged_prefill_kv(pc, K, V, torch.tensor(n_tok, dtype=torch.int32, device="cuda"),
+                       max(n_tok), in_T=wl.T0)
+    del K, V
+    Kn, Vn = W.draw_kv_cuda(wl, wl.T0, 1)
+    L.paged_append_kv(pc, Kn[:, :, 0].contiguous(), Vn[:, :, 0].contiguous())
+    del Kn, Vn
+    q = W.draw_q_cuda(wl, 0)
+    qr = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device="cuda")
+    L.rotate_q(q, qr)
+    maxp = max(n_tok)
+    S = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, maxp)
+    ws = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, maxp, S))
+    out = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device="cuda")
+    L.paged_decode_attention(pc, qr, wl.Hq, TAU, maxp, out, ws, num_splits=S)
+    torch.cuda.synchronize()
+    assert L.device_status() == 0
+    got = out.cpu().numpy()
+    g = wl.g
+    shortest = int(np.argmin(n_tok))
+    for b, h in [(shortest, 1), (11, 6)]:
+        n = n_tok[b]
+        kb = wl.k_bits([b], [h], 0, n)[0, 0]
+        vb = wl.v_bits([b], [h], 0, n)[0, 0]
+        hc = O.build_head_cache(kb, vb, n)
+        hc.append(wl.k_bits([b], [h], wl.T0, 1)[0, 0, 0], wl.v_bits([b], [h], wl.T0, 1)[0, 0, 0])
+        qbits = wl.q_bits([b], range(h * g, (h + 1) * g), 0)[0]
+        ref = hc.decode(O.rotate_q(qbits), TAU)
+        assert_attention_close(got[b, h * g:(h + 1) * g], ref, f"paged row {(b, h)}, n {n}")
