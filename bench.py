@@ -53,6 +53,8 @@ def _args():
                    help="skip the paged-cache decode over a variable-length batch")
     p.add_argument("--no-int4", action="store_true",
                    help="skip the INT4-option decode of the same workload")
+    p.add_argument("--no-ablation", action="store_true",
+                   help="skip the accuracy report of the variants against bf16 attention")
     p.add_argument("--no-prefill", action="store_true",
                    help="skip the prefill timing (fused vs two-call) of the prompt")
     p.add_argument("--num-splits", type=int, default=0,
@@ -564,6 +566,44 @@ def run_ours(args, world, rank, local):
                         "prompt; L2 not flushed between the 20 reps (7.5 GB of records)"}
         del c4, ws4
         torch.cuda.empty_cache()
+    # ---- accuracy of the variants against unquantised bf16 attention ----
+    # (information, not a gate: the pages' ablation of rotation and scaling)
+    ablation = None
+    if not args.no_ablation and wl.n_packed:
+        qb = Q[0]
+        ref = torch.empty_like(out)
+        wsr = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, wl.T0, 64),
+                                device=dev)
+        L.bf16_decode_attention(qb, K, V, wl.B, wl.Hq, wl.Hkv, wl.T0, wl.T0, tau, ref, wsr,
+                                num_splits=64)
+        variants = [("oscar", 0, 2), ("no_rotate", L.NO_ROTATE, 2), ("no_scale", L.NO_SCALE, 2),
+                    ("neither (KIVI-style)", L.NO_ROTATE | L.NO_SCALE, 2),
+                    ("all_heads_norm", L.NORM_ALL_HEADS, 2), ("oscar_int4", 0, 4)]
+        ablation = {"reference": "bf16 split-K decode over the raw bf16 K, V (the same T0 tokens)",
+                    "variants": {}}
+        rn = float(torch.linalg.vector_norm(ref))
+        for name, fl, bits in variants:
+            cv = L.KVCache(wl.B, wl.Hkv, wl.n_packed, flags=fl, device=dev, bits=bits)
+            L.prefill_kv(cv, K, V, n_tok=wl.n_packed, in_T=wl.T0)
+            if wl.n_res:
+                L.append_kv(cv, K[:, :, wl.n_packed:wl.T0].contiguous(),
+                            V[:, :, wl.n_packed:wl.T0].contiguous(), n_tok=wl.n_res)
+            L.rotate_q(qb, qr, flags=fl)
+            Sv = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, cv.n_packed)
+            wsv = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, cv.n_packed, Sv),
+                                    device=dev)
+            ov = torch.empty_like(out)
+            L.decode_attention(cv, qr, wl.Hq, tau, ov, wsv, num_splits=Sv)
+            torch.cuda.synchronize()
+            if L.device_status() != 0:
+                raise RuntimeError(f"ablation variant {name} recorded a device error")
+            d = ov - ref
+            ablation["variants"][name] = {
+                "rel_l2": float(torch.linalg.vector_norm(d)) / rn,
+                "max_abs": float(d.abs().max())}
+            del cv, wsv, ov
+            torch.cuda.empty_cache()
+        del wsr, ref
     peak = peaks.get("hbm_gbs")
     peak_src = "of measured" if peak else "of fallback"
     peak = peak or 6800.0
@@ -591,6 +631,7 @@ def run_ours(args, world, rank, local):
         "prefill": prefill,
         "paged": paged,
         "int4": int4,
+        "ablation": ablation,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src, "traffic": traffic,
                      "kernel": "oscar_decode_attention (fused INT2 decode + LSE combine)",
