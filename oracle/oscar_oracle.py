@@ -21,15 +21,15 @@ Sources (page title and section):
 * [news] news article on arXiv 2605.19660 (animattoys.com): 二 (the two steps),
   三 (three kernels, packed cache + residual cache, rsqrt).
 
-Readings where the pages are silent or ambiguous are listed in the design doc; the
-ones that shape arithmetic here are: Sylvester (natural order) Hadamard of size
-128 with entries +-1/sqrt(128); the norm is per (token, KV head) unless
-NORM_ALL_HEADS asks for the norm over all heads; keys are scaled to a target
-norm (1 unless given) and the stored norm is n / target; asymmetric
-min-max INT2 with step (max-min)/3 (INT4, an option: (max-min)/15), zero =
-min, round half to even, codes from
-the fp32 parameters before their fp16 rounding; a constant group stores step 0
-and codes 0; a zero key keeps k_hat = 0 and norm 0; flush-before-append.
+Where the pages are silent or ambiguous, these readings shape the arithmetic
+here: Sylvester (natural order) Hadamard of size 128 with entries
++-1/sqrt(128); the norm is per (token, KV head) unless NORM_ALL_HEADS asks for
+the norm over all heads; keys are scaled to a target norm (1 unless given)
+and the stored norm is n / target; asymmetric min-max INT2 with step
+(max-min)/3 (INT4, an option: (max-min)/15), zero = min, round half to even,
+codes from the fp32 parameters before their fp16 rounding; key groups of 32
+tokens (64 or 128 as an option); a constant group stores step 0 and codes 0;
+a zero key keeps k_hat = 0 and norm 0; flush-before-append.
 """
 from __future__ import annotations
 
