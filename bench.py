@@ -236,8 +236,9 @@ def run_reference(args, world, rank):
     per = t / max(args.steps, 1)
     scale = total_rows * (wl.n_packed / keep)
     value = per * scale * 1e6
-    sample = (f"1 of {total_rows} rows per step over the first {keep} of {wl.n_packed} packed "
-              f"tokens (+ residual), single thread; extrapolated x{scale:.1f}")
+    sample = (f"1 of {total_rows} rows per step, {keep} packed tokens (+ residual) of the "
+              f"row (the workload's prompt has {wl.n_packed}), single thread; extrapolated "
+              f"x{scale:.1f} (rows x packed-token ratio)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
