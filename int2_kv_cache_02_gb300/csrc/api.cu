@@ -54,33 +54,38 @@ oscar_status check_cache(const oscar_cache* c) {
   return OSCAR_OK;
 }
 
-// Split planning: minimise (waves of CTAs) x (blocks per CTA) + a small
-// per-split cost, so the grid fills the SMs without long tails.
-// Split count for `rows` (sequence, KV head) rows of `nblk` 32-token blocks.
-// A launch runs rows * (s + 1) CTAs (s packed splits and one residual split
-// per row) in waves of sms * ctas_per_sm; a packed CTA costs its blocks plus
-// a fixed start/merge overhead worth kSplitOverheadBlocks blocks.  Each warp
+// Split planning.  A launch runs rows * (s + 1) CTAs (s packed splits and
+// one residual split per row) spread over the SMs; the kernel is bound by
+// instruction issue, so an SM's time is the work of the CTAs it runs:
+// ceil(CTAs / SMs) x (blocks per split + a fixed start/merge overhead worth
+// kSplitOverheadBlocks blocks), slowed in proportion when it holds fewer
+// than kSaturatingWarps warps at once (too few to hide latency).  Each warp
 // keeps at least kMinBlocksPerWarp blocks: shorter ranges measured slower.
-// The cost is waves(s) * (blocks per split + overhead); ties keep fewer
-// splits.
+// Ties keep fewer splits.  (Measured on GB300: the planned counts are the
+// best of a sweep, or within 0.5 % of it, for batch 48 x 128K, batch 8 x
+// 32K, batch 1 x 128K and the g = 8 64K workload.)
 constexpr long long kSplitOverheadBlocks = 32;
 constexpr long long kMinBlocksPerWarp = 16;
+constexpr int kSaturatingWarps = 8;
+constexpr int kWarpsPerCta = 4;
 
 int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
   if (nblk <= 0 || rows <= 0) return 1;
-  const long long slots = (long long)sms * (ctas_per_sm > 0 ? ctas_per_sm : 1);
-  const long long most = std::max<long long>(1, nblk / (4 * kMinBlocksPerWarp));
+  const long long cps = ctas_per_sm > 0 ? ctas_per_sm : 1;
+  const long long most = std::max<long long>(1, nblk / (kWarpsPerCta * kMinBlocksPerWarp));
   const int hi = (int)std::min<long long>(max_splits, most);
   int best = 1;
-  long long best_cost = -1;
+  double best_cost = 1e300;
   for (int s = 1; s <= hi; ++s) {
-    const long long waves = (rows * (s + 1) + slots - 1) / slots;
+    const long long per_sm = (rows * (s + 1) + sms - 1) / sms;   // CTAs of the busiest SM
+    const long long resident = std::min(per_sm, cps);
+    const double rate = std::min(1.0, (double)(resident * kWarpsPerCta) / kSaturatingWarps);
     const long long per = (nblk + s - 1) / s;
-    const long long cost = waves * (per + kSplitOverheadBlocks);
-    if (best_cost < 0 || cost < best_cost) {
+    const double cost = (double)per_sm * (double)(per + kSplitOverheadBlocks) / rate;
+    if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
     }
