@@ -266,6 +266,10 @@ oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const osca
  *                                           k_t = k_hat_t * norm_t       (residual)
  *   out_j   = sum_t softmax(score)_t * v_t, v_t = c*step + zero (packed) or v_res_t
  * over the c->n_packed packed and c->n_res residual tokens of row (b, h).
+ * The records are read as the cache's fields say: INT2 or INT4 codes
+ * (c->bits), each 32-token record with its key group's step and zero
+ * (c->key_group), norms stored as n / target (c->norm_target; the product
+ * with k_hat is the same key), per-head or all-heads norms (c->flags).
  *  q_rot      fp32 [B][Hq][128] rotated queries (oscar_rotate_q)
  *  out        fp32 [B][Hq][128]; an empty cache gives zeros
  *  num_splits packed-token splits per (b,h); 0 = choose for this device
