@@ -218,6 +218,19 @@ def cpu_baseline(wl, budget_s=20.0):
 # reference arm: the oracle as the timed program
 # ---------------------------------------------------------------------------
 
+def kernel_code_sha256() -> str:
+    """sha256 of the decode kernel's source with comments and blank lines
+    removed: the key of the stored traffic record, which a change of code
+    (not of comments) invalidates."""
+    import hashlib
+    import re
+    with open(os.path.join(HERE, "int2_kv_cache_02_gb300", "csrc", "decode_int2.cu")) as f:
+        src = f.read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in src.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def run_reference(args, world, rank):
     from int2_kv_cache_02_gb300 import workloads as W
     if rank != 0:
@@ -610,14 +623,10 @@ def run_ours(args, world, rank, local):
     peak = peak or 6800.0
     traffic = None
     try:
-        import hashlib
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
-        with open(os.path.join(HERE, "int2_kv_cache_02_gb300", "csrc", "decode_int2.cu"),
-                  "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
         # counters taken on another version of the kernel do not describe this one
-        if rec.get("kernel_source_sha256") == sha and wl.name == WORKLOAD:
+        if rec.get("kernel_code_sha256") == kernel_code_sha256() and wl.name == WORKLOAD:
             traffic = rec.get("dram_bytes_per_launch")
     except (OSError, ValueError):
         traffic = None

@@ -32,9 +32,12 @@
 //    operand layout.
 // Each warp streams its own contiguous range of blocks through its own
 // NSTAGE-deep shared-memory ring: one 1-D bulk copy (TMA, cp.async.bulk) of
-// the block's 2752-byte record per block, completing on the warp's mbarrier.  Waits are
-// bounded and record kDevErrWaitTimeout instead of hanging; no CTA-wide
-// barrier runs inside the main loop.
+// the block's record per block (2752 bytes; 4800 for the INT4 option, two in
+// flight), completing on the warp's mbarrier.  Waits are bounded and record
+// kDevErrWaitTimeout instead of hanging; no CTA-wide barrier runs inside the
+// main loop.  Instantiations: query group g, contiguous or paged records
+// (through the block table), a per-block step scale for caches with the
+// all-heads norm, and the code width.
 #include "common.cuh"
 #include "cta_merge.cuh"
 #include "launch.h"
