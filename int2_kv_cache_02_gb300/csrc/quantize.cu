@@ -27,8 +27,8 @@ template <int GS>
 struct GroupSmem {
   uint16_t kt[GS][kD];
   uint16_t vt[kG][kD];
-  uint8_t kc[kG][kD];
-  uint8_t vc[kG][kD];
+  uint8_t kc[kG][kCodeRow];
+  uint8_t vc[kG][kCodeRow];
   __half ns[GS];
 };
 

@@ -67,6 +67,10 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
   return __uint_as_float(((uint32_t)u) << 16);
 }
 
+// Row length of the byte-per-code tiles: 4 bytes of padding put the rows a
+// packing warp reads (4 tokens, 128 bytes apart) on different banks.
+constexpr int kCodeRow = kD + 4;
+
 // Step and zero of one key channel over a group of N tokens (thread c =
 // channel c of the rows of kt, rotated and scaled keys as bf16).
 struct KeyParams {
@@ -99,7 +103,8 @@ __device__ __forceinline__ KeyParams key_params(const uint16_t (*kt)[kD]) {
 template <int BITS>
 __device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
                                                const uint16_t (&vt)[kG][kD],
-                                               uint8_t (&kc)[kG][kD], uint8_t (&vc)[kG][kD],
+                                               uint8_t (&kc)[kG][kCodeRow],
+                                               uint8_t (&vc)[kG][kCodeRow],
                                                const __half* norms, uint8_t* rec,
                                                const KeyParams& kp) {
   const int tid = threadIdx.x;
@@ -135,9 +140,11 @@ __device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
 #pragma unroll 1
     for (int i = 0; i < 8; ++i) {
       const int t = 8 * w + i;
-      float x[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) x[j] = bf16_bits_to_float(vt[t][4 * lane + j]);
+      // the lane's 4 channels in one 8-byte load (the warp reads 256
+      // contiguous bytes)
+      const uint2 raw = reinterpret_cast<const uint2*>(&vt[t][0])[lane];
+      const float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
+                          __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
       float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
       float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
 #pragma unroll
@@ -156,8 +163,10 @@ __device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
 #pragma unroll
         for (int j = 0; j < 4; ++j) cv[j] = quant_code_fast<BITS>(x[j], mn, step, rstep, live);
       }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) vc[t][4 * lane + j] = cv[j];
+      // the lane's 4 codes as one 32-bit store (channels 4 lane .. 4 lane + 3)
+      *reinterpret_cast<uint32_t*>(&vc[t][4 * lane]) =
+          (uint32_t)cv[0] | ((uint32_t)cv[1] << 8) | ((uint32_t)cv[2] << 16) |
+          ((uint32_t)cv[3] << 24);
       if (lane == 0) {
         v_scale[tok_slot(t)] = __float2half_rn(step);
         v_zero[tok_slot(t)] = __float2half_rn(mn);
