@@ -10,10 +10,12 @@
 // constant group; Δ and z stored as fp16 (round to nearest even).
 //
 // One CTA of 128 threads per (b, h, key group): the group's key tile and one
-// 32-token value tile at a time are staged in shared memory, codes computed
-// one byte each, then packed into the block records declared in oscar.h.  The fused
-// prefill kernel rotates and scales the raw keys straight into the key tile
-// (no k_hat round trip through global memory).
+// 32-token value tile at a time are staged in shared memory; the key
+// parameters are formed per channel, then every thread quantises a quarter
+// of one token's keys and values and stores whole words of the block
+// records declared in oscar.h (quantize.cuh).  The fused prefill kernel
+// rotates and scales the raw keys straight into the key tile (no k_hat round
+// trip through global memory).
 #include "launch.h"
 #include "quantize.cuh"
 #include "rotate.cuh"
@@ -21,41 +23,90 @@
 namespace oscar {
 
 // Shared memory of the group kernels: the GS keys of one group (rotated,
-// scaled, bf16) and their norms stay for the whole group; values and codes
-// are staged one 32-token block at a time.
+// scaled, bf16, padded rows), their norms and the group's key parameters
+// stay for the whole group; values are staged one 32-token block at a time,
+// the next block's copies in flight while the current one is worked (two
+// buffers when the group has more than one block).
 template <int GS>
 struct GroupSmem {
-  uint16_t kt[GS][kD];
-  uint16_t vt[kG][kD];
-  uint8_t kc[kG][kCodeRow];
-  uint8_t vc[kG][kCodeRow];
+  static constexpr int NVB = GS > kG ? 2 : 1;
+  alignas(16) uint16_t kt[GS][kTileRow];
+  alignas(16) uint16_t vt[NVB][kG][kTileRow];
+  KeyParamSmem P;
   __half ns[GS];
 };
 
-// Copies 32 value rows (bf16, 256 B each) into vt: 16 B per thread per step.
-__device__ __forceinline__ void stage_values(uint16_t (&vt)[kG][kD], const uint16_t* v) {
-  const uint4* vs = reinterpret_cast<const uint4*>(v);
-  uint4* vd = reinterpret_cast<uint4*>(&vt[0][0]);
+// Rotates and scales the GS raw keys of a group (rows k[t], t < GS) into kt
+// and their norms into ns, in the quarter layout: at step i, warp w and lane
+// l take token 32 i + 8 w + (l & 7).  With the all-heads norm, head0 + t * 128
+// is the token's key of head 0 and head_stride the distance between heads.
+// The next step's raw keys are loaded before the current step is worked.
+template <int GS, bool PLAIN>
+__device__ __forceinline__ void rotate_group(GroupSmem<GS>& S, const uint16_t* k,
+                                             const uint16_t* head0, long long head_stride,
+                                             int Hkv, KeyScale ks) {
+  const int lane = threadIdx.x & 31, Q = lane >> 3;
+  const int tw = 8 * (threadIdx.x >> 5) + (lane & 7);
+  uint4 raw[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) vd[threadIdx.x + 128 * i] = vs[threadIdx.x + 128 * i];
+  for (int j = 0; j < 4; ++j)
+    raw[j] = reinterpret_cast<const uint4*>(k + (long long)tw * kD)[4 * Q + j];
+#pragma unroll 1
+  for (int i = 0; i < GS / kG; ++i) {
+    const int t = kG * i + tw;
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t u[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        x[8 * j + 2 * q] = bf16_lo(u[q]);
+        x[8 * j + 2 * q + 1] = bf16_hi(u[q]);
+      }
+    }
+    if (i + 1 < GS / kG) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        raw[j] = reinterpret_cast<const uint4*>(k + (long long)(t + kG) * kD)[4 * Q + j];
+    }
+    float s_all = 0.0f;
+    if (!PLAIN && (ks.flags & OSCAR_NORM_ALL_HEADS))
+      s_all = all_heads_sq_q(head0 + (long long)t * kD, head_stride, Hkv, lane);
+    const float norm = rotate_scale_key<PLAIN>(x, lane, ks, s_all);
+    uint4* dst = reinterpret_cast<uint4*>(&S.kt[t][32 * Q]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint4 o;
+      o.x = bf16x2_bits(x[8 * j], x[8 * j + 1]);
+      o.y = bf16x2_bits(x[8 * j + 2], x[8 * j + 3]);
+      o.z = bf16x2_bits(x[8 * j + 4], x[8 * j + 5]);
+      o.w = bf16x2_bits(x[8 * j + 6], x[8 * j + 7]);
+      dst[j] = o;
+    }
+    if (Q == 0) S.ns[t] = __float2half_rn(norm);
+  }
 }
 
 // The group's GS/32 records, one block at a time, with the group's key
-// parameters.  On entry kt and the norms for GS tokens and the values of
-// block 0 (staged first, so that their loads overlap the key work) are in
-// place and synced.  rec_of(s) gives block s's record; values of block s at
-// v_src + 32 s rows.
+// parameters.  On entry kt and the norms for GS tokens, the values of block
+// 0 in vt[0] (copied first, so that their loads overlap the key work) and a
+// cleared P.tiny are in place and synced.  rec_of(s) gives block s's record;
+// values of block s at v_src + 32 s rows.
 template <int GS, int BITS, class RecOf>
 __device__ __forceinline__ void quantize_group(GroupSmem<GS>& S, const __half* norms,
                                                const uint16_t* v_src, RecOf rec_of) {
-  const KeyParams kp = key_params<GS, BITS>(S.kt);
-  quantize_block<BITS>(&S.kt[0], S.vt, S.kc, S.vc, norms, rec_of(0), kp);
-  if constexpr (GS > kG) {
+  constexpr int NB = GS / kG;
+  key_params<GS, BITS>(S.kt, S.P, rec_of);
+  __syncthreads();
 #pragma unroll 1
-    for (int sb = 1; sb < GS / kG; ++sb) {
-      stage_values(S.vt, v_src + (long long)sb * kG * kD);
-      __syncthreads();   // also: every thread is done packing the previous block
-      quantize_block<BITS>(&S.kt[kG * sb], S.vt, S.kc, S.vc, norms + kG * sb, rec_of(sb), kp);
+  for (int sb = 0; sb < NB; ++sb) {
+    // the buffer of block sb + 1 was last read by block sb - 1, before the
+    // barrier that ended that block
+    if (sb + 1 < NB) stage_rows<kG>(S.vt[(sb + 1) % S.NVB], v_src + (long long)(sb + 1) * kG * kD);
+    quantize_block<BITS>(&S.kt[kG * sb], S.vt[sb % S.NVB], S.P, norms + kG * sb, rec_of(sb));
+    if (sb + 1 < NB) {
+      async_wait_all();
+      __syncthreads();
     }
   }
 }
@@ -70,17 +121,13 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
     uint8_t* __restrict__ packed) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   auto& S = *reinterpret_cast<GroupSmem<GS>*>(smem_raw);
-  const int tid = threadIdx.x;
   const int j = blockIdx.x;
   const long long row = (long long)blockIdx.z * Hkv + blockIdx.y;
   const long long src_tok = row * src_T + (long long)j * GS;
-  stage_values(S.vt, v + src_tok * kD);
-  {
-    const uint4* ks = reinterpret_cast<const uint4*>(k_hat + src_tok * kD);
-    uint4* kd = reinterpret_cast<uint4*>(&S.kt[0][0]);
-#pragma unroll
-    for (int i = 0; i < GS / 8; ++i) kd[tid + 128 * i] = ks[tid + 128 * i];
-  }
+  stage_rows<kG>(S.vt[0], v + src_tok * kD);
+  stage_rows<GS>(S.kt, k_hat + src_tok * kD);
+  if (threadIdx.x == 0) S.P.tiny = 0;
+  async_wait_all();
   __syncthreads();
   constexpr int RB = Rec<BITS>::BYTES;
   uint8_t* row_rec = packed + (row * (T_cap / kG) + p0 / kG + (long long)j * (GS / kG)) * RB;
@@ -89,43 +136,25 @@ __global__ void __launch_bounds__(128) quantize_kv_kernel(
 }
 
 // Fused prefill: raw keys and values of n_tok tokens -> block records.  CTA
-// (j, h, b) handles group j: warp w rotates and scales tokens w, w + 4, ...
-// of the group (one token per warp step, as rotate_scale_k_kernel does),
-// rounds k_hat to bf16 into the key tile and keeps the norms in shared
-// memory; then the group's records are quantised block by block.
+// (j, h, b) handles group j: the group's keys are rotated and scaled in the
+// quarter layout and rounded to bf16 into the key tile, the norms kept in
+// shared memory; then the group's records are quantised block by block.
 template <int GS, int BITS, bool PLAIN>
 __global__ void __launch_bounds__(128) prefill_kv_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int in_T, int Hkv,
     int T_cap, int p0, KeyScale ks, uint8_t* __restrict__ packed) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   auto& S = *reinterpret_cast<GroupSmem<GS>*>(smem_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = blockIdx.x;
   const long long row = (long long)blockIdx.z * Hkv + blockIdx.y;
   const long long src_tok = row * in_T + (long long)j * GS;
-  stage_values(S.vt, v + src_tok * kD);
+  stage_rows<kG>(S.vt[0], v + src_tok * kD);
+  if (threadIdx.x == 0) S.P.tiny = 0;
   // with the all-heads norm, head 0 of this sequence's token src_tok
   const long long head0_tok = src_tok - (long long)blockIdx.y * in_T;
-  // 8 tokens' raw keys are loaded before any is transformed, so their loads
-  // overlap one another rather than each FHT waiting on its own
-#pragma unroll 1
-  for (int i0 = 0; i0 < GS / 4; i0 += 8) {
-    uint2 raw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      raw[i] = reinterpret_cast<const uint2*>(k + (src_tok + (GS / 4) * warp + i0 + i) * kD)[lane];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = (GS / 4) * warp + i0 + i;
-      float s_all = 0.0f;
-      if (!PLAIN && (ks.flags & OSCAR_NORM_ALL_HEADS))
-        s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, Hkv, lane);
-      float x[4] = {bf16_lo(raw[i].x), bf16_hi(raw[i].x), bf16_lo(raw[i].y), bf16_hi(raw[i].y)};
-      const float norm = rotate_scale_key<PLAIN>(x, lane, ks, s_all);
-      reinterpret_cast<uint2*>(&S.kt[t][0])[lane] = pack_bf16x4(x);
-      if (lane == 0) S.ns[t] = __float2half_rn(norm);
-    }
-  }
+  rotate_group<GS, PLAIN>(S, k + src_tok * kD, k + head0_tok * kD, (long long)in_T * kD, Hkv,
+                          ks);
+  async_wait_all();
   __syncthreads();
   constexpr int RB = Rec<BITS>::BYTES;
   uint8_t* row_rec = packed + (row * (T_cap / kG) + p0 / kG + (long long)j * (GS / kG)) * RB;
@@ -156,7 +185,7 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(PagedArgs p,
                                                             int max_tok) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   auto& S = *reinterpret_cast<GroupSmem<GS>*>(smem_raw);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int n = n_tok[b], p0 = p.seq_packed[b];
   if (n == 0) return;
@@ -173,26 +202,12 @@ __global__ void __launch_bounds__(128) paged_prefill_kernel(PagedArgs p,
     }
   }
   const long long src_tok = ((long long)b * p.Hkv + h) * in_T + (long long)j * GS;
-  stage_values(S.vt, v + src_tok * kD);
+  stage_rows<kG>(S.vt[0], v + src_tok * kD);
+  if (tid == 0) S.P.tiny = 0;
   const long long head0_tok = src_tok - (long long)h * in_T;
-#pragma unroll 1
-  for (int i0 = 0; i0 < GS / 4; i0 += 8) {
-    uint2 raw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      raw[i] = reinterpret_cast<const uint2*>(k + (src_tok + (GS / 4) * warp + i0 + i) * kD)[lane];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = (GS / 4) * warp + i0 + i;
-      float s_all = 0.0f;
-      if (!PLAIN && (p.ks.flags & OSCAR_NORM_ALL_HEADS))
-        s_all = all_heads_sq(k + (head0_tok + t) * kD, (long long)in_T * kD, p.Hkv, lane);
-      float x[4] = {bf16_lo(raw[i].x), bf16_hi(raw[i].x), bf16_lo(raw[i].y), bf16_hi(raw[i].y)};
-      const float norm = rotate_scale_key<PLAIN>(x, lane, p.ks, s_all);
-      reinterpret_cast<uint2*>(&S.kt[t][0])[lane] = pack_bf16x4(x);
-      if (lane == 0) S.ns[t] = __float2half_rn(norm);
-    }
-  }
+  rotate_group<GS, PLAIN>(S, k + src_tok * kD, k + head0_tok * kD, (long long)in_T * kD, p.Hkv,
+                          p.ks);
+  async_wait_all();
   __syncthreads();
   quantize_group<GS, BITS>(S, S.ns, v + src_tok * kD,
                            [&](int sb) { return paged_record<BITS>(p, b, lb0 + sb, h); });
@@ -220,13 +235,10 @@ __global__ void __launch_bounds__(128) paged_flush_kernel(PagedArgs p, const int
   }
   const long long row = (long long)b * p.Hkv + h;
   const long long src_tok = row * kR + (long long)j * GS;
-  stage_values(S.vt, p.v_res + src_tok * kD);
-  {
-    const uint4* ks = reinterpret_cast<const uint4*>(p.k_res + src_tok * kD);
-    uint4* kd = reinterpret_cast<uint4*>(&S.kt[0][0]);
-#pragma unroll
-    for (int i = 0; i < GS / 8; ++i) kd[tid + 128 * i] = ks[tid + 128 * i];
-  }
+  stage_rows<kG>(S.vt[0], p.v_res + src_tok * kD);
+  stage_rows<GS>(S.kt, p.k_res + src_tok * kD);
+  if (tid == 0) S.P.tiny = 0;
+  async_wait_all();
   __syncthreads();
   quantize_group<GS, BITS>(S, p.k_res_norm + src_tok, p.v_res + src_tok * kD,
                            [&](int sb) { return paged_record<BITS>(p, b, lb0 + sb, h); });

@@ -1,6 +1,6 @@
-// INT2 (or INT4) quantisation and packing of one 32-token block of keys and values,
-// shared by quantize_kv_kernel and the fused prefill kernel (kernel (2) of the
-// news article on arXiv 2605.19660, 三).
+// INT2 (or INT4) quantisation and packing of 32-token blocks of keys and
+// values, shared by the group kernels (kernel (2) of the news article on
+// arXiv 2605.19660, 三).
 //
 // Keys: block-wise per-channel asymmetric INT2 -- every channel of every
 // group of G consecutive tokens (G = 32 by default; 64 and 128 are the
@@ -11,6 +11,15 @@
 // z = min, Δ = (max - min)/3, code = round-half-even((x - z)/Δ) clamped to
 // [0, 3], every operation one IEEE fp32 rounding; Δ = 0 and codes 0 for a
 // constant group; Δ and z stored as fp16 (round to nearest even).
+//
+// Thread layout: the CTA's 128 threads work a block as 32 tokens x 4
+// quarters.  Warp w, lane l: token 8w + (l & 7), quarter Q = l >> 3 (the
+// quarter layout of rotate.cuh).  For keys a quarter is channels 32Q..32Q+31,
+// which are exactly the key words 2Q, 2Q+1 (INT2) or 4Q..4Q+3 (INT4) of the
+// token; for values it is the channels 2Q, 2Q+1 + 8m (m = 0..15), which fill
+// whole half-words of the value words.  Each thread forms its words in
+// registers and stores them; the two tokens of a value word swap halves
+// through one shuffle.
 #pragma once
 
 #include "common.cuh"
@@ -21,6 +30,7 @@ namespace oscar {
 template <int BITS>
 constexpr float kMaxCode = (float)((1 << BITS) - 1);
 
+// The code by the exact quotient (the definition).
 template <int BITS>
 __device__ __forceinline__ uint8_t quant_code(float x, float mn, float step, bool live) {
   if (!live) return 0;
@@ -30,213 +40,301 @@ __device__ __forceinline__ uint8_t quant_code(float x, float mn, float step, boo
   return (uint8_t)r;
 }
 
-// The same code with the quotient formed as a * (1/step): the correctly
-// rounded reciprocal times a is within ~2^-21 (relative) of the rounded
-// quotient, ~2^-19 absolute for quotients up to 16, so both round to the
-// same integer unless the quotient lies within 1e-5 of a half-integer,
-// where the exact division decides.
-template <int BITS>
-__device__ __forceinline__ uint8_t quant_code_fast(float x, float mn, float step, float rstep,
-                                                   bool live) {
-  if (!live) return 0;
-  const float q = __fsub_rn(x, mn) * rstep;
-  if (fabsf(q - floorf(q) - 0.5f) < 1e-5f) return quant_code<BITS>(x, mn, step, live);
-  return (uint8_t)fminf(fmaxf(rintf(q), 0.0f), kMaxCode<BITS>);
-}
-
-// The fast code without a branch: c = round-half-even(q), q = (x - mn) /
-// step formed as (x - mn) * (1/step) (0 for a constant group, whose step and
-// reciprocal are 0 and x == mn).  dist keeps the largest |q - c| seen; above
-// kNearHalf, some quotient may lie within 1e-5 of a half-integer (the case
-// quant_code_fast hands to the exact division), and the caller redoes the
-// warp's codes with quant_code_fast, so the codes are always those of
-// quant_code_fast.  (|q - c| is exact and 0.5 - |q - c| equals
-// |q - floor(q) - 0.5| wherever either is below 0.25; the threshold keeps a
-// margin of 1e-5 over that test, so a redo may happen needlessly, never be
-// missed.)
-template <int BITS>
-__device__ __forceinline__ uint8_t quant_code_nb(float x, float mn, float rstep, float& dist) {
-  const float q = __fsub_rn(x, mn) * rstep;
-  const int c = __float2int_rn(q);
-  dist = fmaxf(dist, fabsf(q - (float)c));
-  return (uint8_t)min(c, (1 << BITS) - 1);
-}
+// The code with the quotient formed as q = (x - mn) * (1/step), as an exact
+// small integer in float: q + 1.5 * 2^23 has a unit in the last place of 1
+// for 0 <= q < 2^22, so adding and removing that constant rounds q to the
+// nearest integer, ties to even.  The correctly rounded reciprocal times
+// (x - mn) is within ~2^-21 (relative) of the rounded quotient, ~2^-19
+// absolute for quotients up to 16, so both give the same integer unless the
+// quotient lies within 1e-5 of a half-integer.  d keeps the largest |q - c|
+// of a half-word's codes; above kNearHalf the caller redoes that half-word
+// by the exact quotient (0.5 - |q - c| is the distance to the half-integer;
+// the threshold keeps a margin of 1e-5 over the bound above, so a redo may
+// happen needlessly, never be missed).  With bf16 inputs about one code in
+// a thousand is an exact tie, so redoing only the half-word concerned keeps
+// the redo cheap.  For a constant group step and reciprocal are 0 and x == mn, so
+// q = 0.  q <= (2^BITS - 1)(1 + 2^-22) for every x of the group, so the code
+// needs no clamp.
+constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
 constexpr float kNearHalf = 0.5f - 2e-5f;
-
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t u) {
-  return __uint_as_float(((uint32_t)u) << 16);
+__device__ __forceinline__ float code_rn(float x, float mn, float rs, float& d) {
+  const float q = __fmul_rn(__fsub_rn(x, mn), rs);
+  const float c = __fsub_rn(__fadd_rn(q, kRoundMagic), kRoundMagic);
+  d = fmaxf(d, fabsf(__fsub_rn(q, c)));
+  return c;
+}
+template <int BITS>
+__device__ __forceinline__ float code_exact(float x, float mn, float step) {
+  return (float)quant_code<BITS>(x, mn, step, step > 0.0f);
 }
 
-// Row length of the byte-per-code tiles: 4 bytes of padding put the rows a
-// packing warp reads (4 tokens, 128 bytes apart) on different banks.
-constexpr int kCodeRow = kD + 4;
+// A reciprocal step that overflowed (steps below 2^-128) leaves only the
+// exact quotient.
+__device__ __forceinline__ bool recip_ok(float rs) { return rs <= 3.0e38f; }
 
-// Step and zero of one key channel over a group of N tokens (thread c =
-// channel c of the rows of kt, rotated and scaled keys as bf16).
-struct KeyParams {
-  float mn, step, rstep;
-  bool live;
+// Weight of slot k of a half-word (2 or 4 bits per slot): the half-word is
+// the exact fp32 sum of c * 2^(BITS k), an integer below 2^16.
+template <int BITS>
+__host__ __device__ constexpr float slot_weight(int k) {
+  return (float)(1u << (BITS * k));
+}
+// Half-word value h (an integer below 2^16 held in a float) as bits: the
+// low 16 bits of the result.
+__device__ __forceinline__ uint32_t half_word_bits(float h) {
+  return __float_as_uint(__fadd_rn(h, 8388608.0f));   // 2^23 + h
+}
+
+// Rows of the bf16 tiles: 128 channels + 8 of padding (272 bytes), so that
+// the 16-byte accesses of 8 consecutive rows at one column, and the 4-byte
+// accesses of the value layout, fall on different banks.
+constexpr int kTileRow = kD + 8;
+// Per-channel key parameters in shared memory, 4 floats of padding after
+// every 32 channels: the four quarters' 16-byte reads fall on different banks.
+constexpr int kParamN = kD + 16;
+__host__ __device__ constexpr int param_slot(int c) { return c + 4 * (c >> 5); }
+
+struct KeyParamSmem {
+  alignas(16) float mn[kParamN];
+  alignas(16) float rs[kParamN];
+  alignas(16) float step[kParamN];
+  int tiny;   // some channel's reciprocal step overflowed
 };
-template <int N, int BITS>
-__device__ __forceinline__ KeyParams key_params(const uint16_t (*kt)[kD]) {
+
+// Copies N rows of 128 bf16 (contiguous in global memory, 256 B each) into
+// padded tile rows, 16 B per thread per step, as asynchronous copies that
+// bypass the registers (one commit group); async_wait_all() before the
+// barrier that publishes them.
+template <int N>
+__device__ __forceinline__ void stage_rows(uint16_t (*dst)[kTileRow], const uint16_t* src) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < N / 8; ++i) {
+    const int c = threadIdx.x + 128 * i;   // 16-byte chunk of the source
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(&dst[c >> 4][8 * (c & 15)])),
+                 "l"(s + c)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+
+// Step and zero of every key channel over the N tokens of kt (thread c =
+// channel c): into P and, as fp16, into the records rec_of(0 .. N/32 - 1).
+// P.tiny must have been cleared before the barrier that precedes the call.
+template <int N, int BITS, class RecOf>
+__device__ __forceinline__ void key_params(const uint16_t (*kt)[kTileRow], KeyParamSmem& P,
+                                           RecOf rec_of) {
   const int c = threadIdx.x;
-  float mn = bf16_bits_to_float(kt[0][c]), mx = mn;
+  float mn = __uint_as_float((uint32_t)kt[0][c] << 16), mx = mn;
 #pragma unroll 8
   for (int t = 1; t < N; ++t) {
-    const float x = bf16_bits_to_float(kt[t][c]);
+    const float x = __uint_as_float((uint32_t)kt[t][c] << 16);
     mn = fminf(mn, x);
     mx = fmaxf(mx, x);
   }
-  KeyParams p;
-  p.live = mx > mn;
-  p.mn = mn;
-  p.step = p.live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
-  p.rstep = p.live ? __frcp_rn(p.step) : 0.0f;
-  return p;
+  const bool live = mx > mn;
+  const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
+  const float rs = live ? __frcp_rn(step) : 0.0f;
+  P.mn[param_slot(c)] = mn;
+  P.rs[param_slot(c)] = rs;
+  P.step[param_slot(c)] = step;
+  if (!recip_ok(rs)) P.tiny = 1;
+  const __half hs = __float2half_rn(step), hz = __float2half_rn(mn);
+  using RL = Rec<BITS>;
+#pragma unroll 1
+  for (int sb = 0; sb < N / kG; ++sb) {
+    uint8_t* rec = rec_of(sb);
+    reinterpret_cast<__half*>(rec + RL::KS)[c] = hs;
+    reinterpret_cast<__half*>(rec + RL::KZ)[c] = hz;
+  }
 }
 
-// Called by all 128 threads of the CTA after a __syncthreads that follows
-// the staging of kt (rotated, scaled keys as bf16) and vt (values as bf16)
-// for the 32 tokens of one block; kp: this thread's key channel parameters
-// over the block's group; norms: the block's 32 key norms (global or shared
-// memory).  Writes the block record at rec (layout in oscar.h for BITS).
+// Key words of this thread's token (row of kt) and quarter: INT2 words 2Q,
+// 2Q+1 (16 channels each; channel 16w + j at bit 2(j/2) + 16(j%2)), INT4
+// words 4Q..4Q+3 (8 channels each; channel 8w + j at bit 4(j/2) + 16(j%2)).
 template <int BITS>
-__device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kD],
-                                               const uint16_t (&vt)[kG][kD],
-                                               uint8_t (&kc)[kG][kCodeRow],
-                                               uint8_t (&vc)[kG][kCodeRow],
-                                               const __half* norms, uint8_t* rec,
-                                               const KeyParams& kp) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ void key_words(const uint16_t* row, int Q, const KeyParamSmem& P,
+                                          uint32_t (&w)[BITS == 2 ? 2 : 4]) {
+  constexpr int NW = BITS == 2 ? 2 : 4;   // words of the quarter
+  constexpr int CW = 32 / NW;             // channels per word
+  float x[32];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(row + 32 * Q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 u = src[i];
+      const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[8 * i + 2 * j] = bf16_lo(v[j]);
+        x[8 * i + 2 * j + 1] = bf16_hi(v[j]);
+      }
+    }
+  }
+  const float* mn = P.mn + param_slot(32 * Q);
+  const float* rs = P.rs + param_slot(32 * Q);
+  // half-word h = 2 (e / CW) + (e & 1) holds the codes e of word e / CW with
+  // the parity of h, at slot (e % CW) / 2
+  float hw[2 * NW], d[2 * NW];
+  const float d0 = P.tiny ? 1.0f : 0.0f;
+#pragma unroll
+  for (int i = 0; i < 2 * NW; ++i) {
+    hw[i] = 0.0f;
+    d[i] = d0;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 m = reinterpret_cast<const float4*>(mn)[i];
+    const float4 r = reinterpret_cast<const float4*>(rs)[i];
+    const float mv[4] = {m.x, m.y, m.z, m.w}, rv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * i + j, jw = e % CW, h = 2 * (e / CW) + (jw & 1);
+      hw[h] = fmaf(code_rn(x[e], mv[j], rv[j], d[h]), slot_weight<BITS>(jw >> 1), hw[h]);
+    }
+  }
+  const float* st = P.step + param_slot(32 * Q);
+#pragma unroll
+  for (int h = 0; h < 2 * NW; ++h) {
+    if (d[h] > kNearHalf) {
+      hw[h] = 0.0f;
+#pragma unroll
+      for (int s = 0; s < CW / 2; ++s) {
+        const int e = (h >> 1) * CW + 2 * s + (h & 1);
+        hw[h] = fmaf(code_exact<BITS>(x[e], mn[e], st[e]), slot_weight<BITS>(s), hw[h]);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < NW; ++k)
+    w[k] = __byte_perm(half_word_bits(hw[2 * k]), half_word_bits(hw[2 * k + 1]), 0x5410);
+}
+
+// Value words of this thread's token (row of vt) with the token's step and
+// zero.  The thread quantises channels g + 8m of its token for g = 2Q, 2Q+1
+// (m = 0..15), i.e. whole half-words (g, hh): INT2 slot k = channel
+// g + 8(8hh + k) (hh = 0, 1), INT4 slot k = channel g + 8(4hh + k) (hh =
+// 0..3).  A value word holds one half-word of each token of a pair (t, t+1),
+// t even, in its low and high halves.  The even token stores the words of
+// channel group g = 2Q, the odd token those of g = 2Q + 1; each passes the
+// other group's half-words to its partner (lane ^ 1).  par = t & 1.
+template <int BITS>
+__device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
+                                            uint32_t (&w)[BITS == 2 ? 2 : 4], float& step_out,
+                                            float& mn_out) {
+  constexpr int NH = BITS == 2 ? 2 : 4;   // half-words per channel group g
+  constexpr int PS = 16 / NH;             // slots per half-word
+  float x[2][16];
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(row + 8 * m + 2 * Q);
+    x[0][m] = bf16_lo(u);
+    x[1][m] = bf16_hi(u);
+  }
+  float mn = fminf(x[0][0], x[1][0]), mx = fmaxf(x[0][0], x[1][0]);
+#pragma unroll
+  for (int m = 1; m < 16; ++m) {
+    mn = fminf(mn, fminf(x[0][m], x[1][m]));
+    mx = fmaxf(mx, fmaxf(x[0][m], x[1][m]));
+  }
+#pragma unroll
+  for (int s = 8; s < 32; s <<= 1) {   // the token's other quarters
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, s));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+  }
+  const bool live = mx > mn;
+  const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
+  const float rs = live ? __frcp_rn(step) : 0.0f;
+  float H[2][NH], d[2][NH];
+  const float d0 = recip_ok(rs) ? 0.0f : 1.0f;
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+      H[g][hh] = 0.0f;
+      d[g][hh] = d0;
+    }
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+#pragma unroll
+    for (int m = 0; m < 16; ++m)
+      H[g][m / PS] = fmaf(code_rn(x[g][m], mn, rs, d[g][m / PS]), slot_weight<BITS>(m % PS),
+                          H[g][m / PS]);
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) {
+      if (d[g][hh] > kNearHalf) {
+        H[g][hh] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < PS; ++k)
+          H[g][hh] = fmaf(code_exact<BITS>(x[g][PS * hh + k], mn, step), slot_weight<BITS>(k),
+                          H[g][hh]);
+      }
+    }
+  // keep: this token's half-words of the group it stores; send: the other
+  // group's, two per register (hh 2i low, 2i + 1 high)
+  uint32_t keep[NH], send[NH / 2];
+#pragma unroll
+  for (int hh = 0; hh < NH; ++hh) keep[hh] = half_word_bits(par ? H[1][hh] : H[0][hh]);
+#pragma unroll
+  for (int i = 0; i < NH / 2; ++i)
+    send[i] = __byte_perm(half_word_bits(par ? H[0][2 * i] : H[1][2 * i]),
+                          half_word_bits(par ? H[0][2 * i + 1] : H[1][2 * i + 1]), 0x5410);
+#pragma unroll
+  for (int i = 0; i < NH / 2; ++i) {
+    const uint32_t recv = __shfl_xor_sync(0xffffffffu, send[i], 1);
+    // even token: own half-word low, the partner's high; odd token: reversed
+    w[2 * i] = __byte_perm(keep[2 * i], recv, par ? 0x1054u : 0x5410u);
+    w[2 * i + 1] = __byte_perm(keep[2 * i + 1], recv, par ? 0x1076u : 0x7610u);
+  }
+  step_out = step;
+  mn_out = mn;
+}
+
+// One 32-token block: keys from kt (32 rotated, scaled bf16 rows), values
+// from vt, key parameters in P, norms of the 32 tokens; writes the block's
+// codes, value steps and zeros and norms into the record (layout in oscar.h
+// for BITS; key_params writes the key steps and zeros).  Called by all 128
+// threads after a __syncthreads that follows the staging of kt, vt and P.
+template <int BITS>
+__device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kTileRow],
+                                               const uint16_t (*vt)[kTileRow],
+                                               const KeyParamSmem& P, const __half* norms,
+                                               uint8_t* rec) {
   using RL = Rec<BITS>;
-  uint32_t* k_codes = reinterpret_cast<uint32_t*>(rec + RL::KC);
-  uint32_t* v_codes = reinterpret_cast<uint32_t*>(rec + RL::VC);
-  __half* k_scale = reinterpret_cast<__half*>(rec + RL::KS);
-  __half* k_zero = reinterpret_cast<__half*>(rec + RL::KZ);
-  __half* k_norm_out = reinterpret_cast<__half*>(rec + RL::KN);
-  __half* v_scale = reinterpret_cast<__half*>(rec + RL::VS);
-  __half* v_zero = reinterpret_cast<__half*>(rec + RL::VZ);
-
-  // Keys: thread = channel, with its group's parameters.  Codes without a
-  // branch; the rare quotients near a half-integer are redone exactly.
+  constexpr int NW = BITS == 2 ? 2 : 4;
+  const int lane = threadIdx.x & 31, Q = lane >> 3;
+  const int t = 8 * (threadIdx.x >> 5) + (lane & 7);
   {
-    const int c = tid;
-    float dist = 0.0f;
-#pragma unroll 8
-    for (int t = 0; t < kG; ++t)
-      kc[t][c] = quant_code_nb<BITS>(bf16_bits_to_float(kt[t][c]), kp.mn, kp.rstep, dist);
-    if (__any_sync(0xffffffffu, dist > kNearHalf)) {
-      for (int t = 0; t < kG; ++t)
-        kc[t][c] = quant_code_fast<BITS>(bf16_bits_to_float(kt[t][c]), kp.mn, kp.step, kp.rstep,
-                                         kp.live);
+    uint32_t w[NW];
+    float step, mn;
+    value_words<BITS>(vt[t], Q, t & 1, w, step, mn);
+    // word of (token pair, channel group g, hh = 0): INT2 128 kh + 4 (4g +
+    // t4) + 2p, INT4 256 kh + 128 p + 4 (4g + t4), the pair's first token
+    // being 16 kh + 2 t4 + 8 p
+    const int g = 2 * Q + (t & 1), kh = t >> 4, p = (t >> 3) & 1, t4 = (t >> 1) & 3;
+    uint32_t* vc = reinterpret_cast<uint32_t*>(rec + RL::VC);
+    if constexpr (BITS == 2) {
+      *reinterpret_cast<uint2*>(vc + 128 * kh + 4 * (4 * g + t4) + 2 * p) = make_uint2(w[0], w[1]);
+    } else {
+      *reinterpret_cast<uint4*>(vc + 256 * kh + 128 * p + 4 * (4 * g + t4)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
     }
-    k_scale[c] = __float2half_rn(kp.step);
-    k_zero[c] = __float2half_rn(kp.mn);
+    if (Q == 0) reinterpret_cast<__half*>(rec + RL::VS)[tok_slot(t)] = __float2half_rn(step);
+    if (Q == 1) reinterpret_cast<__half*>(rec + RL::VZ)[tok_slot(t)] = __float2half_rn(mn);
+    if (Q == 2) reinterpret_cast<__half*>(rec + RL::KN)[tok_slot(t)] = norms[t];
   }
-
-  // Values: warp w handles tokens 8w..8w+7, lane holds channels 4l..4l+3.
   {
-    const int w = tid >> 5, lane = tid & 31;
-#pragma unroll 1
-    for (int i = 0; i < 8; ++i) {
-      const int t = 8 * w + i;
-      // the lane's 4 channels in one 8-byte load (the warp reads 256
-      // contiguous bytes)
-      const uint2 raw = reinterpret_cast<const uint2*>(&vt[t][0])[lane];
-      const float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xffff0000u),
-                          __uint_as_float(raw.y << 16), __uint_as_float(raw.y & 0xffff0000u)};
-      float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
-      float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-#pragma unroll
-      for (int m = 16; m > 0; m >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, m));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-      }
-      const bool live = mx > mn;
-      const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
-      const float rstep = live ? __frcp_rn(step) : 0.0f;
-      float dist = 0.0f;
-      uint8_t cv[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) cv[j] = quant_code_nb<BITS>(x[j], mn, rstep, dist);
-      if (__any_sync(0xffffffffu, dist > kNearHalf)) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) cv[j] = quant_code_fast<BITS>(x[j], mn, step, rstep, live);
-      }
-      // the lane's 4 codes as one 32-bit store (channels 4 lane .. 4 lane + 3)
-      *reinterpret_cast<uint32_t*>(&vc[t][4 * lane]) =
-          (uint32_t)cv[0] | ((uint32_t)cv[1] << 8) | ((uint32_t)cv[2] << 16) |
-          ((uint32_t)cv[3] << 24);
-      if (lane == 0) {
-        v_scale[tok_slot(t)] = __float2half_rn(step);
-        v_zero[tok_slot(t)] = __float2half_rn(mn);
-      }
-    }
-  }
-  if (tid < kG) k_norm_out[tok_slot(tid)] = norms[tid];
-  __syncthreads();
-
-  if constexpr (BITS == 2) {
-    // Pack keys: word (t, w) = channels 16w..16w+15 of token t; channel 16w+j
-    // at bit 2*(j/2) + 16*(j%2).
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int wi = tid + 128 * r;
-      const int t = wi >> 3, w = wi & 7;
-      const uint8_t* src = &kc[t][16 * w];
-      uint32_t word = 0;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) word |= (uint32_t)src[j] << (2 * (j >> 1) + 16 * (j & 1));
-      k_codes[t * 8 + w] = word;
-    }
-    // Pack values: word 128*kh + 4*lane + 2p + hh, lane = 4g + t4; low half
-    // token 16kh + 2*t4 + 8p, high half the next token; slot k = channel
-    // g + 8*(8hh+k).
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int wi = tid + 128 * r;
-      const int kh = wi >> 7, lane = (wi >> 2) & 31, p = (wi >> 1) & 1, hh = wi & 1;
-      const int g = lane >> 2, t4 = lane & 3;
-      const int tok = 16 * kh + 2 * t4 + 8 * p;
-      uint32_t word = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int ch = g + 8 * (8 * hh + k);
-        word |= (uint32_t)vc[tok][ch] << (2 * k);
-        word |= (uint32_t)vc[tok + 1][ch] << (16 + 2 * k);
-      }
-      v_codes[wi] = word;
-    }
-  } else {
-    // INT4 keys: word (t, w) = channels 8w..8w+7 of token t; channel 8w+j at
-    // bit 4*(j/2) + 16*(j%2).
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int wi = tid + 128 * r;
-      const int t = wi >> 4, w = wi & 15;
-      const uint8_t* src = &kc[t][8 * w];
-      uint32_t word = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) word |= (uint32_t)src[j] << (4 * (j >> 1) + 16 * (j & 1));
-      k_codes[t * 16 + w] = word;
-    }
-    // INT4 values: word 256*kh + 128p + 4*lane + hh, lane = 4g + t4; low
-    // half token 16kh + 2*t4 + 8p, high half the next token; slot k (4 bits)
-    // = channel g + 8*(4hh+k).
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int wi = tid + 128 * r;
-      const int kh = wi >> 8, p = (wi >> 7) & 1, lane = (wi >> 2) & 31, hh = wi & 3;
-      const int g = lane >> 2, t4 = lane & 3;
-      const int tok = 16 * kh + 2 * t4 + 8 * p;
-      uint32_t word = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int ch = g + 8 * (4 * hh + k);
-        word |= (uint32_t)vc[tok][ch] << (4 * k);
-        word |= (uint32_t)vc[tok + 1][ch] << (16 + 4 * k);
-      }
-      v_codes[wi] = word;
+    uint32_t w[NW];
+    key_words<BITS>(kt[t], Q, P, w);
+    uint32_t* kc = reinterpret_cast<uint32_t*>(rec + RL::KC) + t * 4 * NW + NW * Q;
+    if constexpr (BITS == 2) {
+      *reinterpret_cast<uint2*>(kc) = make_uint2(w[0], w[1]);
+    } else {
+      *reinterpret_cast<uint4*>(kc) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }

@@ -1,8 +1,14 @@
-// Per-token Canalized Rotation and Omni-Token Scaling of one 128-vector held
-// by a warp (lane l: elements 4l..4l+3), shared by the rotate kernels and the
-// fused prefill ("OScaR: The Occam's Razor for Extreme KV Cache Quantization
-// in LLMs and Beyond" reading notes, II. Step One and Step Two; news article
-// on arXiv 2605.19660, 三: FHT and scaling in one kernel, hardware rsqrt).
+// Per-token Canalized Rotation and Omni-Token Scaling of one 128-vector,
+// shared by the rotate kernels and the group kernels ("OScaR: The Occam's
+// Razor for Extreme KV Cache Quantization in LLMs and Beyond" reading notes,
+// II. Step One and Step Two; news article on arXiv 2605.19660, 三: FHT and
+// scaling in one kernel, hardware rsqrt).  Two layouts of the vector:
+//  * one warp per vector, lane l holding elements 4l..4l+3 (float[4]);
+//  * the quarter layout, four lanes per vector (lanes l, l ^ 8, l ^ 16,
+//    l ^ 24), lane l holding elements 32Q..32Q+31 with Q = l >> 3, so a warp
+//    works 8 vectors at once (float[32]).
+// Both apply the same butterflies in the same order and sum the squares in
+// the same order, so they give the same bits.
 #pragma once
 
 #include "common.cuh"
@@ -30,10 +36,62 @@ __device__ __forceinline__ void fht128(float (&x)[4], int lane) {
   }
 }
 
+// The same transform in the quarter layout: index bits 0-4 butterflied in
+// registers (a + b and a - b, the roundings of the lane pairs above), bits 5
+// and 6 across lanes xor 8 and xor 16.
+__device__ __forceinline__ void fht128(float (&x)[32], int lane) {
+#pragma unroll
+  for (int h = 1; h < 32; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (!(e & h)) {
+        const float a = x[e], b = x[e + h];
+        x[e] = a + b;
+        x[e + h] = a - b;
+      }
+#pragma unroll
+  for (int m = 8; m < 32; m <<= 1) {
+    const float sg = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float y = __shfl_xor_sync(0xffffffffu, x[e], m);
+      x[e] = fmaf(sg, x[e], y);
+    }
+  }
+}
+
+// Sum over the warp's lanes, pairing lanes xor 1 first and xor 16 last: every
+// lane ends with the same value, and the quarter layout below forms the same
+// sum with the first three pairings in registers.
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-  for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  for (int m = 1; m < 32; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
   return v;
+}
+
+// Sum of squares of four elements, one rounding order for every kernel.
+__device__ __forceinline__ float sq4(float a, float b, float c, float d) {
+  return fmaf(d, d, fmaf(c, c, fmaf(b, b, a * a)));
+}
+
+// Sum of squares of the vector, in either layout: per group of 4 elements
+// sq4, then the groups paired as warp_sum pairs the lanes of the one-warp
+// layout (groups 8Q..8Q+7 of a quarter in registers, then lanes xor 8, 16).
+__device__ __forceinline__ float sum_sq(const float (&x)[4]) {
+  return warp_sum(sq4(x[0], x[1], x[2], x[3]));
+}
+__device__ __forceinline__ float sum_sq(const float (&x)[32]) {
+  float p[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = sq4(x[4 * i], x[4 * i + 1], x[4 * i + 2], x[4 * i + 3]);
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; i += 2 * h) p[i] += p[i + h];
+  float s = p[0];
+  s += __shfl_xor_sync(0xffffffffu, s, 8);
+  s += __shfl_xor_sync(0xffffffffu, s, 16);
+  return s;
 }
 
 // Sum of squares of one token's raw keys over all Hkv heads, for the
@@ -47,7 +105,29 @@ __device__ __forceinline__ float all_heads_sq(const uint16_t* k0, long long head
   for (int h = 0; h < Hkv; ++h) {
     const uint2 raw = reinterpret_cast<const uint2*>(k0 + h * head_stride)[lane];
     const float a = bf16_lo(raw.x), b = bf16_hi(raw.x), c = bf16_lo(raw.y), d = bf16_hi(raw.y);
-    s += warp_sum(fmaf(d, d, fmaf(c, c, fmaf(b, b, a * a))));
+    s += warp_sum(sq4(a, b, c, d));
+  }
+  return s;
+}
+// The same sum in the quarter layout (lane: 32 elements of its quarter of
+// each head's key).
+__device__ __forceinline__ float all_heads_sq_q(const uint16_t* k0, long long head_stride, int Hkv,
+                                               int lane) {
+  float s = 0.0f;
+  for (int h = 0; h < Hkv; ++h) {
+    const uint4* src = reinterpret_cast<const uint4*>(k0 + h * head_stride) + 4 * (lane >> 3);
+    float x[32];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 u = src[i];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[8 * i + 2 * j] = bf16_lo(w[j]);
+        x[8 * i + 2 * j + 1] = bf16_hi(w[j]);
+      }
+    }
+    s += sum_sq(x);
   }
   return s;
 }
@@ -58,9 +138,10 @@ __device__ __forceinline__ float all_heads_sq(const uint16_t* k0, long long head
 // keys over all heads, whose raw sum of squares the caller passes in s_all.
 // Unscaled keys store 1; a zero key (zero norm) keeps k_hat = 0 and stores 0.
 // PLAIN: the method itself (no flags, unit target) fixed at compile time, so
-// the per-token tests of the variants fold away.
-template <bool PLAIN = false>
-__device__ __forceinline__ float rotate_scale_key(float (&x)[4], int lane, KeyScale ks,
+// the per-token tests of the variants fold away.  N: elements per lane (4:
+// one warp per vector; 32: the quarter layout).
+template <bool PLAIN = false, int N>
+__device__ __forceinline__ float rotate_scale_key(float (&x)[N], int lane, KeyScale ks,
                                                   float s_all = 0.0f) {
   if constexpr (PLAIN) {
     ks.flags = 0u;
@@ -71,33 +152,31 @@ __device__ __forceinline__ float rotate_scale_key(float (&x)[4], int lane, KeySc
   if (ks.flags & OSCAR_NO_SCALE) {
     const float f = rot ? kInvSqrtD : 1.0f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) x[r] *= f;
+    for (int r = 0; r < N; ++r) x[r] *= f;
     return 1.0f;
   }
-  const float s = (ks.flags & OSCAR_NORM_ALL_HEADS)
-                      ? (rot ? 128.0f * s_all : s_all)
-                      : warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+  const float s = (ks.flags & OSCAR_NORM_ALL_HEADS) ? (rot ? 128.0f * s_all : s_all) : sum_sq(x);
   if (s > 0.0f) {
     const bool unit = ks.target == 1.0f;   // the method's target: no extra rounding
     const float f = unit ? rsqrtf(s) : rsqrtf(s) * ks.target;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) x[r] *= f;
+    for (int r = 0; r < N; ++r) x[r] *= f;
     const float n = sqrtf(s) * (rot ? kInvSqrtD : 1.0f);
     return unit ? n : n / ks.target;
   }
 #pragma unroll
-  for (int r = 0; r < 4; ++r) x[r] = 0.0f;
+  for (int r = 0; r < N; ++r) x[r] = 0.0f;
   return 0.0f;
 }
 
-// The warp's vector as 4 bf16 (round to nearest even), packed in a uint2.
+// Two floats as bf16 (round to nearest even), a in the low half.
+__device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+// The warp's vector as 4 bf16, packed in a uint2.
 __device__ __forceinline__ uint2 pack_bf16x4(const float (&x)[4]) {
-  __nv_bfloat162 p0 = __floats2bfloat162_rn(x[0], x[1]);
-  __nv_bfloat162 p1 = __floats2bfloat162_rn(x[2], x[3]);
-  uint2 o;
-  o.x = *reinterpret_cast<uint32_t*>(&p0);
-  o.y = *reinterpret_cast<uint32_t*>(&p1);
-  return o;
+  return make_uint2(bf16x2_bits(x[0], x[1]), bf16x2_bits(x[2], x[3]));
 }
 
 }  // namespace oscar

@@ -57,6 +57,10 @@ def test_quantize_bit_exact(L, g):
     khat[1, 1, 0:g, 9] = O.f64_to_bf16(ties)
     vb[1, 1, 5, :] = O.f64_to_bf16(np.full(128, -0.75))                 # constant value token
     vb[1, 1, 6, :] = O.f64_to_bf16(np.resize(np.arange(31) * 0.5, 128))  # value ties
+    # steps of 2^-133 (the reciprocal overflows fp32): a key channel, a value token
+    tiny = np.resize(np.arange(16.0), 128) * 2.0 ** -133
+    khat[0, 1, 0:g, 17] = O.f64_to_bf16(tiny[:g])
+    vb[0, 1, 9, :] = O.f64_to_bf16(tiny)
     cache = L.KVCache(B, H, T + 128, key_group=g, bits=4)
     L.quantize_kv(cache, bits_to_bf16_tensor(khat), torch.from_numpy(rk.norm_f16).cuda(),
                   bits_to_bf16_tensor(vb), src_T=T, n_tok=g)

@@ -112,6 +112,13 @@ def _special_blocks(k_hat_bits, v_bits):
     kb[64:96, 9] = O.f64_to_bf16(ties)                        # ties 0.5/1.5/2.5 in block 2
     vb[5, :] = O.f64_to_bf16(np.full(128, -0.75))             # constant value token
     vb[6, :] = O.f64_to_bf16(np.resize(ties, 128))            # ties in a value token
+    # steps of 2^-133 (bf16 subnormal levels), whose reciprocal overflows
+    # fp32: a key channel in block 3 and a value token; and a value token
+    # with step 2^-126, the smallest normal one
+    levels = np.array([0.0, 1.0, 2.0, 3.0, 2.0, 1.0, 3.0, 0.0])
+    kb[96:128, 20] = O.f64_to_bf16(np.resize(levels, 32) * 2.0 ** -133)
+    vb[7, :] = O.f64_to_bf16(np.resize(levels, 128) * 2.0 ** -133)
+    vb[8, :] = O.f64_to_bf16(np.resize(levels, 128) * 2.0 ** -126)
     return kb, vb
 
 
