@@ -72,6 +72,37 @@ __device__ __forceinline__ float code_exact(float x, float mn, float step) {
 // exact quotient.
 __device__ __forceinline__ bool recip_ok(float rs) { return rs <= 3.0e38f; }
 
+// INT2 codes by thresholds.  The code of a = fl(x - mn) is
+// rint(fl(a / step)), non-decreasing in a, so it is at least j + 1 exactly
+// when a >= A_j, the smallest fp32 a for which it is.  A_j lies within 3
+// units in the last place of (j + 0.5) step: an a below (j + 0.5) step by
+// more than 2 units has a quotient below j + 0.5, one above by more than 2
+// units a quotient above it.  code_threshold walks there from the rounded
+// product, each step evaluating the definition (one exact division); a code
+// is then three comparisons, exact for every input, with no redo.
+__device__ __forceinline__ bool code_above(float a, float step, int j) {
+  return rintf(__fdiv_rn(a, step)) > (float)j;
+}
+__device__ __noinline__ float code_threshold(float step, int j) {
+  float a = __fmul_rn((float)j + 0.5f, step);   // > 0 for step > 0
+  if (code_above(a, step, j)) {
+    for (int i = 0; i < 8; ++i) {
+      const float below = __uint_as_float(__float_as_uint(a) - 1u);   // a > 0
+      if (!code_above(below, step, j)) break;
+      a = below;
+    }
+  } else {
+    for (int i = 0; i < 8; ++i) {
+      a = __uint_as_float(__float_as_uint(a) + 1u);
+      if (code_above(a, step, j)) break;
+    }
+  }
+  return a;
+}
+__device__ __forceinline__ float code_by_thresholds(float a, float A0, float A1, float A2) {
+  return (a >= A0 ? 1.0f : 0.0f) + (a >= A1 ? 1.0f : 0.0f) + (a >= A2 ? 1.0f : 0.0f);
+}
+
 // Weight of slot k of a half-word (2 or 4 bits per slot): the half-word is
 // the exact fp32 sum of c * 2^(BITS k), an integer below 2^16.
 template <int BITS>
@@ -93,12 +124,37 @@ constexpr int kTileRow = kD + 8;
 constexpr int kParamN = kD + 16;
 __host__ __device__ constexpr int param_slot(int c) { return c + 4 * (c >> 5); }
 
+// Per-channel key parameters: the zero mn and, for INT2, the code thresholds
+// A_0..A_2 of a = x - mn in p; for INT4 the reciprocal step in p[0] and the
+// step in p[1].
 struct KeyParamSmem {
   alignas(16) float mn[kParamN];
-  alignas(16) float rs[kParamN];
-  alignas(16) float step[kParamN];
-  int tiny;   // some channel's reciprocal step overflowed
+  alignas(16) float p[3][kParamN];
+  int tiny;   // INT4: some channel's reciprocal step overflowed
 };
+
+// Exact half-words for the redo of near-half INT4 codes: n codes of x0[2k]
+// (keys: parameters mn0[2k], st0[2k]) or of x0[8k] (values: one mn, step),
+// slot k weighted 16^k.  Kept out of line: it runs for about one half-word
+// in a hundred.
+__device__ __noinline__ float exact_key_half_word4(const uint16_t* x0, const float* mn0,
+                                                   const float* st0, int n) {
+  float h = 0.0f;
+  for (int k = 0; k < n; ++k) {
+    const float x = __uint_as_float((uint32_t)x0[2 * k] << 16);
+    h = fmaf(code_exact<4>(x, mn0[2 * k], st0[2 * k]), slot_weight<4>(k), h);
+  }
+  return h;
+}
+__device__ __noinline__ float exact_value_half_word4(const uint16_t* x0, float mn, float step,
+                                                     int n) {
+  float h = 0.0f;
+  for (int k = 0; k < n; ++k) {
+    const float x = __uint_as_float((uint32_t)x0[8 * k] << 16);
+    h = fmaf(code_exact<4>(x, mn, step), slot_weight<4>(k), h);
+  }
+  return h;
+}
 
 // Copies N rows of 128 bf16 (contiguous in global memory, 256 B each) into
 // padded tile rows, 16 B per thread per step, as asynchronous copies that
@@ -136,11 +192,16 @@ __device__ __forceinline__ void key_params(const uint16_t (*kt)[kTileRow], KeyPa
   }
   const bool live = mx > mn;
   const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
-  const float rs = live ? __frcp_rn(step) : 0.0f;
   P.mn[param_slot(c)] = mn;
-  P.rs[param_slot(c)] = rs;
-  P.step[param_slot(c)] = step;
-  if (!recip_ok(rs)) P.tiny = 1;
+  if constexpr (BITS == 2) {
+#pragma unroll 1
+    for (int j = 0; j < 3; ++j) P.p[j][param_slot(c)] = live ? code_threshold(step, j) : INFINITY;
+  } else {
+    const float rs = live ? __frcp_rn(step) : 0.0f;
+    P.p[0][param_slot(c)] = rs;
+    P.p[1][param_slot(c)] = step;
+    if (!recip_ok(rs)) P.tiny = 1;
+  }
   const __half hs = __float2half_rn(step), hz = __float2half_rn(mn);
   using RL = Rec<BITS>;
 #pragma unroll 1
@@ -154,56 +215,69 @@ __device__ __forceinline__ void key_params(const uint16_t (*kt)[kTileRow], KeyPa
 // Key words of this thread's token (row of kt) and quarter: INT2 words 2Q,
 // 2Q+1 (16 channels each; channel 16w + j at bit 2(j/2) + 16(j%2)), INT4
 // words 4Q..4Q+3 (8 channels each; channel 8w + j at bit 4(j/2) + 16(j%2)).
+// Half-word h = 2 (e / CW) + (e & 1) of the quarter holds its channels e of
+// word e / CW with the parity of h, at slot (e % CW) / 2.
 template <int BITS>
 __device__ __forceinline__ void key_words(const uint16_t* row, int Q, const KeyParamSmem& P,
                                           uint32_t (&w)[BITS == 2 ? 2 : 4]) {
   constexpr int NW = BITS == 2 ? 2 : 4;   // words of the quarter
   constexpr int CW = 32 / NW;             // channels per word
-  float x[32];
+  uint32_t xr[16];                        // the quarter's 32 bf16, packed
   {
     const uint4* src = reinterpret_cast<const uint4*>(row + 32 * Q);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint4 u = src[i];
-      const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+      xr[4 * i] = u.x;
+      xr[4 * i + 1] = u.y;
+      xr[4 * i + 2] = u.z;
+      xr[4 * i + 3] = u.w;
+    }
+  }
+  const int q0 = param_slot(32 * Q);
+  float hw[2 * NW];
+#pragma unroll
+  for (int i = 0; i < 2 * NW; ++i) hw[i] = 0.0f;
+  if constexpr (BITS == 2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 m = reinterpret_cast<const float4*>(P.mn + q0)[i];
+      const float4 t0 = reinterpret_cast<const float4*>(P.p[0] + q0)[i];
+      const float4 t1 = reinterpret_cast<const float4*>(P.p[1] + q0)[i];
+      const float4 t2 = reinterpret_cast<const float4*>(P.p[2] + q0)[i];
+      const float mv[4] = {m.x, m.y, m.z, m.w};
+      const float a0[4] = {t0.x, t0.y, t0.z, t0.w}, a1[4] = {t1.x, t1.y, t1.z, t1.w},
+                  a2[4] = {t2.x, t2.y, t2.z, t2.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        x[8 * i + 2 * j] = bf16_lo(v[j]);
-        x[8 * i + 2 * j + 1] = bf16_hi(v[j]);
+        const int e = 4 * i + j, jw = e % CW, h = 2 * (e / CW) + (jw & 1);
+        const float x = (e & 1) ? bf16_hi(xr[e >> 1]) : bf16_lo(xr[e >> 1]);
+        const float c = code_by_thresholds(__fsub_rn(x, mv[j]), a0[j], a1[j], a2[j]);
+        hw[h] = fmaf(c, slot_weight<BITS>(jw >> 1), hw[h]);
       }
     }
-  }
-  const float* mn = P.mn + param_slot(32 * Q);
-  const float* rs = P.rs + param_slot(32 * Q);
-  // half-word h = 2 (e / CW) + (e & 1) holds the codes e of word e / CW with
-  // the parity of h, at slot (e % CW) / 2
-  float hw[2 * NW], d[2 * NW];
-  const float d0 = P.tiny ? 1.0f : 0.0f;
+  } else {
+    float d[2 * NW];
+    const float d0 = P.tiny ? 1.0f : 0.0f;
 #pragma unroll
-  for (int i = 0; i < 2 * NW; ++i) {
-    hw[i] = 0.0f;
-    d[i] = d0;
-  }
+    for (int i = 0; i < 2 * NW; ++i) d[i] = d0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 m = reinterpret_cast<const float4*>(mn)[i];
-    const float4 r = reinterpret_cast<const float4*>(rs)[i];
-    const float mv[4] = {m.x, m.y, m.z, m.w}, rv[4] = {r.x, r.y, r.z, r.w};
+    for (int i = 0; i < 8; ++i) {
+      const float4 m = reinterpret_cast<const float4*>(P.mn + q0)[i];
+      const float4 r = reinterpret_cast<const float4*>(P.p[0] + q0)[i];
+      const float mv[4] = {m.x, m.y, m.z, m.w}, rv[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int e = 4 * i + j, jw = e % CW, h = 2 * (e / CW) + (jw & 1);
-      hw[h] = fmaf(code_rn(x[e], mv[j], rv[j], d[h]), slot_weight<BITS>(jw >> 1), hw[h]);
+      for (int j = 0; j < 4; ++j) {
+        const int e = 4 * i + j, jw = e % CW, h = 2 * (e / CW) + (jw & 1);
+        const float x = (e & 1) ? bf16_hi(xr[e >> 1]) : bf16_lo(xr[e >> 1]);
+        hw[h] = fmaf(code_rn(x, mv[j], rv[j], d[h]), slot_weight<BITS>(jw >> 1), hw[h]);
+      }
     }
-  }
-  const float* st = P.step + param_slot(32 * Q);
 #pragma unroll
-  for (int h = 0; h < 2 * NW; ++h) {
-    if (d[h] > kNearHalf) {
-      hw[h] = 0.0f;
-#pragma unroll
-      for (int s = 0; s < CW / 2; ++s) {
-        const int e = (h >> 1) * CW + 2 * s + (h & 1);
-        hw[h] = fmaf(code_exact<BITS>(x[e], mn[e], st[e]), slot_weight<BITS>(s), hw[h]);
+    for (int h = 0; h < 2 * NW; ++h) {
+      if (d[h] > kNearHalf) {
+        const int e0 = (h >> 1) * CW + (h & 1);
+        hw[h] = exact_key_half_word4(row + 32 * Q + e0, P.mn + q0 + e0, P.p[1] + q0 + e0, CW / 2);
       }
     }
   }
@@ -226,18 +300,15 @@ __device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
                                             float& mn_out) {
   constexpr int NH = BITS == 2 ? 2 : 4;   // half-words per channel group g
   constexpr int PS = 16 / NH;             // slots per half-word
-  float x[2][16];
+  uint32_t u[16];   // channel pairs (2Q + 8m, 2Q + 1 + 8m), packed bf16
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const uint32_t u = *reinterpret_cast<const uint32_t*>(row + 8 * m + 2 * Q);
-    x[0][m] = bf16_lo(u);
-    x[1][m] = bf16_hi(u);
-  }
-  float mn = fminf(x[0][0], x[1][0]), mx = fmaxf(x[0][0], x[1][0]);
+  for (int m = 0; m < 16; ++m) u[m] = *reinterpret_cast<const uint32_t*>(row + 8 * m + 2 * Q);
+  auto xv = [&](int g, int m) { return g ? bf16_hi(u[m]) : bf16_lo(u[m]); };
+  float mn = fminf(xv(0, 0), xv(1, 0)), mx = fmaxf(xv(0, 0), xv(1, 0));
 #pragma unroll
   for (int m = 1; m < 16; ++m) {
-    mn = fminf(mn, fminf(x[0][m], x[1][m]));
-    mx = fmaxf(mx, fmaxf(x[0][m], x[1][m]));
+    mn = fminf(mn, fminf(xv(0, m), xv(1, m)));
+    mx = fmaxf(mx, fmaxf(xv(0, m), xv(1, m)));
   }
 #pragma unroll
   for (int s = 8; s < 32; s <<= 1) {   // the token's other quarters
@@ -246,34 +317,45 @@ __device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
   }
   const bool live = mx > mn;
   const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
-  const float rs = live ? __frcp_rn(step) : 0.0f;
-  float H[2][NH], d[2][NH];
-  const float d0 = recip_ok(rs) ? 0.0f : 1.0f;
+  float H[2][NH];
 #pragma unroll
   for (int g = 0; g < 2; ++g)
 #pragma unroll
-    for (int hh = 0; hh < NH; ++hh) {
-      H[g][hh] = 0.0f;
-      d[g][hh] = d0;
-    }
+    for (int hh = 0; hh < NH; ++hh) H[g][hh] = 0.0f;
+  if constexpr (BITS == 2) {
+    // the token's thresholds A_0..A_2, one per quarter thread
+    const int lane = threadIdx.x & 31;
+    const float mine = (live && Q < 3) ? code_threshold(step, Q) : INFINITY;
+    const float A0 = __shfl_sync(0xffffffffu, mine, lane & 7);
+    const float A1 = __shfl_sync(0xffffffffu, mine, (lane & 7) + 8);
+    const float A2 = __shfl_sync(0xffffffffu, mine, (lane & 7) + 16);
 #pragma unroll
-  for (int g = 0; g < 2; ++g)
+    for (int g = 0; g < 2; ++g)
 #pragma unroll
-    for (int m = 0; m < 16; ++m)
-      H[g][m / PS] = fmaf(code_rn(x[g][m], mn, rs, d[g][m / PS]), slot_weight<BITS>(m % PS),
-                          H[g][m / PS]);
+      for (int m = 0; m < 16; ++m)
+        H[g][m / PS] = fmaf(code_by_thresholds(__fsub_rn(xv(g, m), mn), A0, A1, A2),
+                            slot_weight<BITS>(m % PS), H[g][m / PS]);
+  } else {
+    const float rs = live ? __frcp_rn(step) : 0.0f;
+    float d[2][NH];
+    const float d0 = recip_ok(rs) ? 0.0f : 1.0f;
 #pragma unroll
-  for (int g = 0; g < 2; ++g)
+    for (int g = 0; g < 2; ++g)
 #pragma unroll
-    for (int hh = 0; hh < NH; ++hh) {
-      if (d[g][hh] > kNearHalf) {
-        H[g][hh] = 0.0f;
+      for (int hh = 0; hh < NH; ++hh) d[g][hh] = d0;
 #pragma unroll
-        for (int k = 0; k < PS; ++k)
-          H[g][hh] = fmaf(code_exact<BITS>(x[g][PS * hh + k], mn, step), slot_weight<BITS>(k),
-                          H[g][hh]);
-      }
-    }
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        H[g][m / PS] = fmaf(code_rn(xv(g, m), mn, rs, d[g][m / PS]), slot_weight<BITS>(m % PS),
+                            H[g][m / PS]);
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh)
+        if (d[g][hh] > kNearHalf)
+          H[g][hh] = exact_value_half_word4(row + 2 * Q + g + 8 * PS * hh, mn, step, PS);
+  }
   // keep: this token's half-words of the group it stores; send: the other
   // group's, two per register (hh 2i low, 2i + 1 high)
   uint32_t keep[NH], send[NH / 2];
