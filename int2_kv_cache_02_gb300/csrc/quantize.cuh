@@ -72,33 +72,32 @@ __device__ __forceinline__ float code_exact(float x, float mn, float step) {
 // exact quotient.
 __device__ __forceinline__ bool recip_ok(float rs) { return rs <= 3.0e38f; }
 
-// INT2 codes by thresholds.  The code of a = fl(x - mn) is
-// rint(fl(a / step)), non-decreasing in a, so it is at least j + 1 exactly
-// when a >= A_j, the smallest fp32 a for which it is.  A_j lies within 3
-// units in the last place of (j + 0.5) step: an a below (j + 0.5) step by
-// more than 2 units has a quotient below j + 0.5, one above by more than 2
-// units a quotient above it.  code_threshold walks there from the rounded
-// product, each step evaluating the definition (one exact division); a code
-// is then three comparisons, exact for every input, with no redo.
-__device__ __forceinline__ bool code_above(float a, float step, int j) {
-  return rintf(__fdiv_rn(a, step)) > (float)j;
+// INT2 codes by thresholds.  The code of a = fl(x - mn) is rint(t) with
+// t = fl(a / step), non-decreasing in a, so it is at least j + 1 exactly
+// when a >= A_j, the smallest fp32 a for which it is; a code is then three
+// comparisons, exact for every input.  A_j follows from the rounding rules:
+// h = j + 1/2 has a last mantissa bit of 0, so under round-half-even the
+// quotients that round to h form [h - u-/2, h + u+/2] with both ends (u-,
+// u+ the fp32 spacings below and above h).  rint(h) = j + 1 when j + 1 is
+// even, so then code >= j + 1 iff a / step >= h - u-/2; otherwise iff
+// a / step > h + u+/2.  The bound m step is exact in fp64 (m has at most 28
+// significant bits, step 24), and A_j is that product rounded up to fp32
+// (for the strict case, the next fp32 when the product is itself an fp32).
+__host__ __device__ constexpr double threshold_factor(int j) {
+  // h = j + 1/2 < 16; fp32 spacing above h is 2^(e - 23), e = floor(log2 h);
+  // below h the same, except at h = 1/2 (a power of two), where it halves
+  return ((j + 1) % 2 == 0)
+             ? (j + 0.5) - 0.5 * (j == 0 ? 0x1p-25 : (j < 2 ? 0x1p-23 : j < 4 ? 0x1p-22 : j < 8 ? 0x1p-21 : 0x1p-20))
+             : (j + 0.5) + 0.5 * (j == 0 ? 0x1p-24 : (j < 2 ? 0x1p-23 : j < 4 ? 0x1p-22 : j < 8 ? 0x1p-21 : 0x1p-20));
 }
-__device__ __noinline__ float code_threshold(float step, int j) {
-  float a = __fmul_rn((float)j + 0.5f, step);   // > 0 for step > 0
-  if (code_above(a, step, j)) {
-    for (int i = 0; i < 8; ++i) {
-      const float below = __uint_as_float(__float_as_uint(a) - 1u);   // a > 0
-      if (!code_above(below, step, j)) break;
-      a = below;
-    }
-  } else {
-    for (int i = 0; i < 8; ++i) {
-      a = __uint_as_float(__float_as_uint(a) + 1u);
-      if (code_above(a, step, j)) break;
-    }
-  }
-  return a;
+__device__ __forceinline__ float code_threshold(float step, int j) {
+  const double b = threshold_factor(j) * (double)step;   // exact
+  const float up = __double2float_ru(b);
+  if ((j + 1) % 2 == 0) return up;
+  return __double2float_rd(b) == up ? __uint_as_float(__float_as_uint(up) + 1u) : up;
 }
+// Number of thresholds at or below a: the code, as a float (three compares
+// that set 1.0 or 0.0, two adds).
 __device__ __forceinline__ float code_by_thresholds(float a, float A0, float A1, float A2) {
   return (a >= A0 ? 1.0f : 0.0f) + (a >= A1 ? 1.0f : 0.0f) + (a >= A2 ? 1.0f : 0.0f);
 }
@@ -176,25 +175,16 @@ __device__ __forceinline__ void async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
-// Step and zero of every key channel over the N tokens of kt (thread c =
-// channel c): into P and, as fp16, into the records rec_of(0 .. N/32 - 1).
-// P.tiny must have been cleared before the barrier that precedes the call.
-template <int N, int BITS, class RecOf>
-__device__ __forceinline__ void key_params(const uint16_t (*kt)[kTileRow], KeyParamSmem& P,
-                                           RecOf rec_of) {
-  const int c = threadIdx.x;
-  float mn = __uint_as_float((uint32_t)kt[0][c] << 16), mx = mn;
-#pragma unroll 8
-  for (int t = 1; t < N; ++t) {
-    const float x = __uint_as_float((uint32_t)kt[t][c] << 16);
-    mn = fminf(mn, x);
-    mx = fmaxf(mx, x);
-  }
+// Step and zero of key channel c from its group's min and max: thresholds
+// (INT2) or reciprocal step and step (INT4) into P; returns the fp16 step
+// and zero the records carry.
+template <int BITS>
+__device__ __forceinline__ __half2 channel_params(int c, float mn, float mx, KeyParamSmem& P) {
   const bool live = mx > mn;
   const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
   P.mn[param_slot(c)] = mn;
   if constexpr (BITS == 2) {
-#pragma unroll 1
+#pragma unroll
     for (int j = 0; j < 3; ++j) P.p[j][param_slot(c)] = live ? code_threshold(step, j) : INFINITY;
   } else {
     const float rs = live ? __frcp_rn(step) : 0.0f;
@@ -202,13 +192,35 @@ __device__ __forceinline__ void key_params(const uint16_t (*kt)[kTileRow], KeyPa
     P.p[1][param_slot(c)] = step;
     if (!recip_ok(rs)) P.tiny = 1;
   }
-  const __half hs = __float2half_rn(step), hz = __float2half_rn(mn);
+  return __halves2half2(__float2half_rn(step), __float2half_rn(mn));
+}
+
+// Step and zero of every key channel over the N tokens of kt: into P and,
+// as fp16, into the records rec_of(0 .. N/32 - 1).  Threads 0..63 take the
+// channel pairs 2t, 2t + 1 (min and max on packed bf16); the others return
+// at once.  P.tiny must have been cleared before the barrier that precedes
+// the call.
+template <int N, int BITS, class RecOf>
+__device__ __forceinline__ void key_params(const uint16_t (*kt)[kTileRow], KeyParamSmem& P,
+                                           RecOf rec_of) {
+  if (threadIdx.x >= kD / 2) return;
+  const int c2 = 2 * threadIdx.x;
+  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&kt[0][c2]), mx2 = mn2;
+#pragma unroll 8
+  for (int t = 1; t < N; ++t) {
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&kt[t][c2]);
+    mn2 = __hmin2(mn2, x);
+    mx2 = __hmax2(mx2, x);
+  }
+  const __half2 p0 = channel_params<BITS>(c2, __low2float(mn2), __low2float(mx2), P);
+  const __half2 p1 = channel_params<BITS>(c2 + 1, __high2float(mn2), __high2float(mx2), P);
+  const __half2 steps = __lows2half2(p0, p1), zeros = __highs2half2(p0, p1);
   using RL = Rec<BITS>;
 #pragma unroll 1
   for (int sb = 0; sb < N / kG; ++sb) {
     uint8_t* rec = rec_of(sb);
-    reinterpret_cast<__half*>(rec + RL::KS)[c] = hs;
-    reinterpret_cast<__half*>(rec + RL::KZ)[c] = hz;
+    reinterpret_cast<__half2*>(rec + RL::KS)[threadIdx.x] = steps;
+    reinterpret_cast<__half2*>(rec + RL::KZ)[threadIdx.x] = zeros;
   }
 }
 
@@ -235,10 +247,10 @@ __device__ __forceinline__ void key_words(const uint16_t* row, int Q, const KeyP
     }
   }
   const int q0 = param_slot(32 * Q);
-  float hw[2 * NW];
-#pragma unroll
-  for (int i = 0; i < 2 * NW; ++i) hw[i] = 0.0f;
   if constexpr (BITS == 2) {
+    float hw[2 * NW];
+#pragma unroll
+    for (int i = 0; i < 2 * NW; ++i) hw[i] = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float4 m = reinterpret_cast<const float4*>(P.mn + q0)[i];
@@ -252,12 +264,17 @@ __device__ __forceinline__ void key_words(const uint16_t* row, int Q, const KeyP
       for (int j = 0; j < 4; ++j) {
         const int e = 4 * i + j, jw = e % CW, h = 2 * (e / CW) + (jw & 1);
         const float x = (e & 1) ? bf16_hi(xr[e >> 1]) : bf16_lo(xr[e >> 1]);
-        const float c = code_by_thresholds(__fsub_rn(x, mv[j]), a0[j], a1[j], a2[j]);
-        hw[h] = fmaf(c, slot_weight<BITS>(jw >> 1), hw[h]);
+        hw[h] = fmaf(code_by_thresholds(__fsub_rn(x, mv[j]), a0[j], a1[j], a2[j]),
+                     slot_weight<BITS>(jw >> 1), hw[h]);
       }
     }
+#pragma unroll
+    for (int k = 0; k < NW; ++k)
+      w[k] = __byte_perm(half_word_bits(hw[2 * k]), half_word_bits(hw[2 * k + 1]), 0x5410);
   } else {
-    float d[2 * NW];
+    float hw[2 * NW], d[2 * NW];
+#pragma unroll
+    for (int i = 0; i < 2 * NW; ++i) hw[i] = 0.0f;
     const float d0 = P.tiny ? 1.0f : 0.0f;
 #pragma unroll
     for (int i = 0; i < 2 * NW; ++i) d[i] = d0;
@@ -280,10 +297,10 @@ __device__ __forceinline__ void key_words(const uint16_t* row, int Q, const KeyP
         hw[h] = exact_key_half_word4(row + 32 * Q + e0, P.mn + q0 + e0, P.p[1] + q0 + e0, CW / 2);
       }
     }
-  }
 #pragma unroll
-  for (int k = 0; k < NW; ++k)
-    w[k] = __byte_perm(half_word_bits(hw[2 * k]), half_word_bits(hw[2 * k + 1]), 0x5410);
+    for (int k = 0; k < NW; ++k)
+      w[k] = __byte_perm(half_word_bits(hw[2 * k]), half_word_bits(hw[2 * k + 1]), 0x5410);
+  }
 }
 
 // Value words of this thread's token (row of vt) with the token's step and
@@ -304,12 +321,15 @@ __device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
 #pragma unroll
   for (int m = 0; m < 16; ++m) u[m] = *reinterpret_cast<const uint32_t*>(row + 8 * m + 2 * Q);
   auto xv = [&](int g, int m) { return g ? bf16_hi(u[m]) : bf16_lo(u[m]); };
-  float mn = fminf(xv(0, 0), xv(1, 0)), mx = fmaxf(xv(0, 0), xv(1, 0));
+  auto b2 = [&](int m) { return *reinterpret_cast<const __nv_bfloat162*>(&u[m]); };
+  __nv_bfloat162 mn2 = b2(0), mx2 = b2(0);
 #pragma unroll
   for (int m = 1; m < 16; ++m) {
-    mn = fminf(mn, fminf(xv(0, m), xv(1, m)));
-    mx = fmaxf(mx, fmaxf(xv(0, m), xv(1, m)));
+    mn2 = __hmin2(mn2, b2(m));
+    mx2 = __hmax2(mx2, b2(m));
   }
+  float mn = fminf(__low2float(mn2), __high2float(mn2));
+  float mx = fmaxf(__low2float(mx2), __high2float(mx2));
 #pragma unroll
   for (int s = 8; s < 32; s <<= 1) {   // the token's other quarters
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, s));
@@ -317,11 +337,7 @@ __device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
   }
   const bool live = mx > mn;
   const float step = live ? __fdiv_rn(__fsub_rn(mx, mn), kMaxCode<BITS>) : 0.0f;
-  float H[2][NH];
-#pragma unroll
-  for (int g = 0; g < 2; ++g)
-#pragma unroll
-    for (int hh = 0; hh < NH; ++hh) H[g][hh] = 0.0f;
+  uint32_t Hb[2][NH];   // half-words as bits
   if constexpr (BITS == 2) {
     // the token's thresholds A_0..A_2, one per quarter thread
     const int lane = threadIdx.x & 31;
@@ -329,20 +345,32 @@ __device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
     const float A0 = __shfl_sync(0xffffffffu, mine, lane & 7);
     const float A1 = __shfl_sync(0xffffffffu, mine, (lane & 7) + 8);
     const float A2 = __shfl_sync(0xffffffffu, mine, (lane & 7) + 16);
+    float H[2][NH];
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) H[g][hh] = 0.0f;
 #pragma unroll
     for (int g = 0; g < 2; ++g)
 #pragma unroll
       for (int m = 0; m < 16; ++m)
         H[g][m / PS] = fmaf(code_by_thresholds(__fsub_rn(xv(g, m), mn), A0, A1, A2),
                             slot_weight<BITS>(m % PS), H[g][m / PS]);
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) Hb[g][hh] = half_word_bits(H[g][hh]);
   } else {
     const float rs = live ? __frcp_rn(step) : 0.0f;
-    float d[2][NH];
+    float H[2][NH], d[2][NH];
     const float d0 = recip_ok(rs) ? 0.0f : 1.0f;
 #pragma unroll
     for (int g = 0; g < 2; ++g)
 #pragma unroll
-      for (int hh = 0; hh < NH; ++hh) d[g][hh] = d0;
+      for (int hh = 0; hh < NH; ++hh) {
+        H[g][hh] = 0.0f;
+        d[g][hh] = d0;
+      }
 #pragma unroll
     for (int g = 0; g < 2; ++g)
 #pragma unroll
@@ -355,16 +383,20 @@ __device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
       for (int hh = 0; hh < NH; ++hh)
         if (d[g][hh] > kNearHalf)
           H[g][hh] = exact_value_half_word4(row + 2 * Q + g + 8 * PS * hh, mn, step, PS);
+#pragma unroll
+    for (int g = 0; g < 2; ++g)
+#pragma unroll
+      for (int hh = 0; hh < NH; ++hh) Hb[g][hh] = half_word_bits(H[g][hh]);
   }
   // keep: this token's half-words of the group it stores; send: the other
   // group's, two per register (hh 2i low, 2i + 1 high)
   uint32_t keep[NH], send[NH / 2];
 #pragma unroll
-  for (int hh = 0; hh < NH; ++hh) keep[hh] = half_word_bits(par ? H[1][hh] : H[0][hh]);
+  for (int hh = 0; hh < NH; ++hh) keep[hh] = par ? Hb[1][hh] : Hb[0][hh];
 #pragma unroll
   for (int i = 0; i < NH / 2; ++i)
-    send[i] = __byte_perm(half_word_bits(par ? H[0][2 * i] : H[1][2 * i]),
-                          half_word_bits(par ? H[0][2 * i + 1] : H[1][2 * i + 1]), 0x5410);
+    send[i] = __byte_perm(par ? Hb[0][2 * i] : Hb[1][2 * i],
+                          par ? Hb[0][2 * i + 1] : Hb[1][2 * i + 1], 0x5410);
 #pragma unroll
   for (int i = 0; i < NH / 2; ++i) {
     const uint32_t recv = __shfl_xor_sync(0xffffffffu, send[i], 1);

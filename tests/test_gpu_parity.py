@@ -162,6 +162,72 @@ def test_quantize_bit_exact(L):
             assert torch.all(cache.packed[b, h, T // 32:] == 0)
 
 
+def _tie_blocks(n_blocks, seed):
+    """Keys and values of one head whose codes sit on exact ties and next to
+    absorbed values: every block mixes (i) levels mn + k s / 2 (k = 0..6,
+    every half level an exact quotient) for a step s that is a power of two,
+    a multiple of 3 or neither, (ii) tiny values beside a large zero, where
+    fl(x - mn) absorbs x, and (iii) random bf16 noise."""
+    rng = np.random.default_rng(seed)
+    T = 32 * n_blocks
+    k = rng.standard_normal((T, 128)) * 0.1
+    v = rng.standard_normal((T, 128))
+    for b in range(n_blocks):
+        r = slice(32 * b, 32 * b + 32)
+        s = [0.25, 0.375, 0.3, 3.0 / 64][b % 4]
+        mn = [-0.5, 0.125, -1.0, 2.0][b % 4]
+        half = mn + np.arange(7) * s / 2
+        k[r, 0:40] = half[rng.integers(0, 7, (32, 40))]
+        k[r, 0:40][0], k[r, 0:40][1] = mn, mn + 3 * s          # every channel spans [mn, mn + 3s]
+        v[32 * b:32 * b + 16, :] = half[rng.integers(0, 7, (16, 128))]
+        v[32 * b:32 * b + 16, 0], v[32 * b:32 * b + 16, 1] = mn, mn + 3 * s
+        # absorption: zero -1000, max 1000, the rest within 1e-3 of 0
+        k[r, 60] = rng.uniform(-1e-3, 1e-3, 32)
+        k[32 * b, 60], k[32 * b + 1, 60] = -1000.0, 1000.0
+        v[32 * b + 20, :] = rng.uniform(-1e-3, 1e-3, 128)
+        v[32 * b + 20, 0], v[32 * b + 20, 1] = -1000.0, 1000.0
+        v[32 * b + 21, :] = rng.choice([-1000.0, 0.0, 1000.0, 5e-4, -5e-4], 128)
+    return O.f64_to_bf16(k), O.f64_to_bf16(v)
+
+
+def _exact_ties(x_bits, bits, keys):
+    """Quotients (x - mn) / step (fp32, as the quantiser forms them) that are
+    exactly k + 1/2."""
+    x = O.bf16_to_f64(x_bits).astype(np.float32)
+    xs = x.reshape(-1, 32, 128) if keys else x[:, None, :]
+    ax = 1 if keys else 2
+    mn, mx = xs.min(ax, keepdims=True), xs.max(ax, keepdims=True)
+    st = ((mx - mn) / np.float32((1 << bits) - 1)).astype(np.float32)
+    t = ((xs - mn) / np.where(mx > mn, st, np.float32(1))).astype(np.float32)
+    return int(((t - np.floor(t)) == 0.5).sum())
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_quantize_ties_and_absorption_bit_exact(L, bits):
+    B, H, nb = 1, 1, 8
+    kb, vb = _tie_blocks(nb, 77 + bits)
+    T = 32 * nb
+    norm = np.ones((B, H, T), np.float16)
+    cache = L.KVCache(B, H, T, bits=bits)
+    L.quantize_kv(cache, bits_to_bf16_tensor(kb[None, None]), torch.from_numpy(norm).cuda(),
+                  bits_to_bf16_tensor(vb[None, None]), src_T=T, n_tok=T)
+    _sync_ok(L)
+    kq, vq = O.quantize_k(kb, bits=bits), O.quantize_v(vb, bits=bits)
+    # the construction does put thousands of quotients exactly on half levels
+    assert _exact_ties(kb, bits, keys=True) > 1000 and _exact_ties(vb, bits, keys=False) > 1000
+    assert int(kq.codes.max()) == (1 << bits) - 1
+    np.testing.assert_array_equal(cache.tokens("k_codes")[0, 0, :T].cpu().numpy().view(np.uint32),
+                                  O.pack_words(kq.codes, bits, "k"))
+    np.testing.assert_array_equal(cache.field("v_codes")[0, 0, :nb].cpu().numpy().view(np.uint32),
+                                  O.pack_words(vq.codes, bits, "v"))
+    for name, want in [("k_scale", kq.step16), ("k_zero", kq.zero16)]:
+        got = cache.field(name)[0, 0, :nb].cpu().numpy()
+        np.testing.assert_array_equal(got.view(np.uint16), want.view(np.uint16))
+    for name, want in [("v_scale", vq.step16), ("v_zero", vq.zero16)]:
+        got = cache.tokens(name)[0, 0, :T].cpu().numpy()
+        np.testing.assert_array_equal(got.view(np.uint16), want.view(np.uint16))
+
+
 # --------------------------------------------------------------------------
 # attention gate on an oracle-built cache
 # --------------------------------------------------------------------------

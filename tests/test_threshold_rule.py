@@ -1,0 +1,94 @@
+"""The rule the INT2 group kernels use to form codes, checked on the host
+against the definition.
+
+The quantiser's code of a = fl(x - mn) (both fp32) is rint(fl(a / step))
+with round-half-even throughout ("OScaR：面向大模型及多模态LLM极限KV缓存量化的
+奥卡姆剃刀", 前置知识: asymmetric quantisation with step Δ and zero z).  The
+kernels count thresholds instead: code >= j + 1 iff a >= A_j, with A_j the
+fp32 rounding upward of m_j * step (exact in fp64), m_j = h - u-/2 when
+j + 1 is even and h + u+/2 (strictly above) when odd, h = j + 1/2 and u-,
+u+ the fp32 spacings below and above h.  This test derives m_j from exact
+rationals and checks, for random steps (normal and subnormal) and for a
+values at, around and far from each threshold, that the threshold count
+equals the definition.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+
+def _spacing(h, below):
+    e = math.floor(math.log2(h))
+    if below and h == Fraction(2) ** e:
+        return Fraction(2) ** (e - 24)
+    return Fraction(2) ** (e - 23)
+
+
+def _factor(j):
+    h = Fraction(2 * j + 1, 2)
+    if (j + 1) % 2 == 0:
+        return h - _spacing(h, True) / 2
+    return h + _spacing(h, False) / 2
+
+
+def _f32_up(x: Fraction) -> np.float32:
+    f = np.float32(float(x))                 # nearest (x is exact in fp64 here)
+    if Fraction(float(f)) < x:
+        f = np.nextafter(f, np.float32(np.inf))
+    return f
+
+
+def _threshold(step: np.float32, j: int) -> np.float32:
+    b = _factor(j) * Fraction(float(step))
+    up = _f32_up(b)
+    if (j + 1) % 2 == 1 and Fraction(float(up)) == b:
+        up = np.nextafter(up, np.float32(np.inf))
+    return up
+
+
+def _code(a: np.float32, step: np.float32, levels: int) -> int:
+    t = np.float32(a) / np.float32(step)     # IEEE fp32 division
+    return int(min(max(np.rint(t), 0), levels))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_threshold_count_equals_definition(bits):
+    levels = (1 << bits) - 1
+    rng = np.random.default_rng(5 + bits)
+    steps = [np.float32(s) for s in
+             list(rng.uniform(1e-3, 10.0, 40)) + [0.25, 1 / 3, 3.0 / 64, 1e-30, 2.0 ** -133,
+                                                   3 * 2.0 ** -140, 1e30]]
+    n_checked = 0
+    with np.errstate(over="ignore"):
+        for s in steps:
+            if not np.isfinite(s) or s == 0:
+                continue
+            A = [_threshold(s, j) for j in range(levels)]
+            assert all(A[i] <= A[i + 1] for i in range(levels - 1))
+            cands = []
+            for Aj in A:
+                f = Aj
+                for _ in range(4):
+                    f = np.nextafter(f, np.float32(0))
+                g = f
+                for _ in range(9):                  # A_j - 4 ulp .. A_j + 4 ulp
+                    cands.append(g)
+                    g = np.nextafter(g, np.float32(np.inf))
+            cands += list((rng.uniform(0, levels, 64) * s).astype(np.float32))
+            for a in cands:
+                if not np.isfinite(a) or a < 0:
+                    continue
+                want = _code(a, s, levels)
+                got = sum(1 for Aj in A if a >= Aj)
+                assert got == want, (float(s), float(a), got, want)
+                n_checked += 1
+    assert n_checked > 1000
+
+
+def test_factors_are_exact_in_fp64():
+    for j in range(15):
+        m = _factor(j)
+        assert Fraction(float(m)) == m              # the kernels hold m as a double
+        assert m.denominator <= 2 ** 26 and m * 2 ** 26 % 1 == 0
