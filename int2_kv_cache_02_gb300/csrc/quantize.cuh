@@ -40,8 +40,8 @@ __device__ __forceinline__ uint8_t quant_code(float x, float mn, float step, boo
   return (uint8_t)r;
 }
 
-// The code with the quotient formed as q = (x - mn) * (1/step), as an exact
-// small integer in float: q + 1.5 * 2^23 has a unit in the last place of 1
+// The INT4 code with the quotient formed as q = (x - mn) * (1/step), as an
+// exact small integer in float: q + 1.5 * 2^23 has a unit in the last place of 1
 // for 0 <= q < 2^22, so adding and removing that constant rounds q to the
 // nearest integer, ties to even.  The correctly rounded reciprocal times
 // (x - mn) is within ~2^-21 (relative) of the rounded quotient, ~2^-19
@@ -52,9 +52,9 @@ __device__ __forceinline__ uint8_t quant_code(float x, float mn, float step, boo
 // the threshold keeps a margin of 1e-5 over the bound above, so a redo may
 // happen needlessly, never be missed).  With bf16 inputs about one code in
 // a thousand is an exact tie, so redoing only the half-word concerned keeps
-// the redo cheap.  For a constant group step and reciprocal are 0 and x == mn, so
-// q = 0.  q <= (2^BITS - 1)(1 + 2^-22) for every x of the group, so the code
-// needs no clamp.
+// the redo cheap.  For a constant group step and reciprocal are 0 and
+// x == mn, so q = 0.  q <= (2^BITS - 1)(1 + 2^-22) for every x of the group,
+// so the code needs no clamp.
 constexpr float kRoundMagic = 12582912.0f;   // 1.5 * 2^23
 constexpr float kNearHalf = 0.5f - 2e-5f;
 __device__ __forceinline__ float code_rn(float x, float mn, float rs, float& d) {
@@ -83,12 +83,18 @@ __device__ __forceinline__ bool recip_ok(float rs) { return rs <= 3.0e38f; }
 // a / step > h + u+/2.  The bound m step is exact in fp64 (m has at most 28
 // significant bits, step 24), and A_j is that product rounded up to fp32
 // (for the strict case, the next fp32 when the product is itself an fp32).
+// fp32 spacing just above (below = false) or just below h = j + 1/2 < 16:
+// 2^(e - 23) with e = floor(log2 h), halved below h = 1/2 (a power of two).
+__host__ __device__ constexpr double fp32_spacing(int j, bool below) {
+  return j == 0 ? (below ? 0x1p-25 : 0x1p-24)
+       : j < 2  ? 0x1p-23
+       : j < 4  ? 0x1p-22
+       : j < 8  ? 0x1p-21
+                : 0x1p-20;
+}
 __host__ __device__ constexpr double threshold_factor(int j) {
-  // h = j + 1/2 < 16; fp32 spacing above h is 2^(e - 23), e = floor(log2 h);
-  // below h the same, except at h = 1/2 (a power of two), where it halves
-  return ((j + 1) % 2 == 0)
-             ? (j + 0.5) - 0.5 * (j == 0 ? 0x1p-25 : (j < 2 ? 0x1p-23 : j < 4 ? 0x1p-22 : j < 8 ? 0x1p-21 : 0x1p-20))
-             : (j + 0.5) + 0.5 * (j == 0 ? 0x1p-24 : (j < 2 ? 0x1p-23 : j < 4 ? 0x1p-22 : j < 8 ? 0x1p-21 : 0x1p-20));
+  return ((j + 1) % 2 == 0) ? (j + 0.5) - 0.5 * fp32_spacing(j, true)
+                            : (j + 0.5) + 0.5 * fp32_spacing(j, false);
 }
 __device__ __forceinline__ float code_threshold(float step, int j) {
   const double b = threshold_factor(j) * (double)step;   // exact
