@@ -5,10 +5,11 @@ CPU-baseline leg of ``bench.py`` may import this module.  It shares no code with
 the CUDA path and imports nothing from the package; it takes plain numpy
 arrays (bf16 values are passed as their uint16 bit patterns).
 
-Precision: fp64 everywhere, except the INT2 quantiser, whose code decision is
-taken in fp32 exactly as the kernel takes it (the pages fix no precision for
-it), and the stored side arrays, which are rounded to fp16 / bf16 as the
-cache format stores them.
+Precision: fp64 everywhere, except the INT2 quantiser, whose parameters and
+code decision are fp32 with one rounding per operation (the quotient
+(x - zero) / step rounded half to even; the pages fix no precision for it),
+and the stored side arrays, which are rounded to fp16 / bf16 as the cache
+format stores them.
 
 Sources (page title and section):
 * [rainbus] "OScaR：面向大模型及多模态LLM极限KV缓存量化的奥卡姆剃刀"
