@@ -10,7 +10,8 @@ j + 1 is even and h + u+/2 (strictly above) when odd, h = j + 1/2 and u-,
 u+ the fp32 spacings below and above h.  This test derives m_j from exact
 rationals and checks, for random steps (normal and subnormal) and for a
 values at, around and far from each threshold, that the threshold count
-equals the definition.
+equals the definition; and, on bf16 key groups and value tokens with ties
+and tiny steps, that it equals the oracle's codes.
 """
 import math
 from fractions import Fraction
@@ -92,3 +93,29 @@ def test_factors_are_exact_in_fp64():
         m = _factor(j)
         assert Fraction(float(m)) == m              # the kernels hold m as a double
         assert m.denominator <= 2 ** 26 and m * 2 ** 26 % 1 == 0
+
+
+def test_threshold_count_equals_oracle_codes():
+    """The rule against the oracle's quantiser on bf16 data: key groups of 32
+    tokens per channel and value tokens, with random, tied and tiny-step
+    groups; the count of thresholds at or below fl(x - zero) is the oracle's
+    code everywhere."""
+    from oracle import oscar_oracle as O
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((64, 128))
+    x[0:32, 0:16] = (rng.integers(0, 7, (32, 16)) * 0.125 - 0.375)     # exact half levels
+    x[32:64, 16] = rng.integers(0, 4, 32) * 2.0 ** -133                # step 2^-133
+    x[5, :] = rng.integers(0, 7, 128) * 0.25 - 0.75                    # a tied value token
+    xb = O.f64_to_bf16(x)
+    xf = O.bf16_to_f64(xb).astype(np.float32)
+    for axis, groups in (("k", xf.reshape(2, 32, 128).transpose(0, 2, 1).reshape(-1, 32)),
+                         ("v", xf)):
+        codes, step, zero = O.quantize_groups(groups)
+        for g in range(groups.shape[0]):
+            if not step[g] > 0:
+                assert np.all(codes[g] == 0)
+                continue
+            A = [_threshold(np.float32(step[g]), j) for j in range(3)]
+            a = (groups[g] - zero[g]).astype(np.float32)
+            got = sum((a >= Aj).astype(np.int64) for Aj in A)
+            np.testing.assert_array_equal(got, codes[g].astype(np.int64), err_msg=f"{axis} {g}")
