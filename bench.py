@@ -1,17 +1,22 @@
 """Benchmark of the OScaR INT2 decode path on GB300.
 
-One step = one decode step of one attention layer for the batch-48, 128K
-context workload (32 query / 8 KV heads, head_dim 128): rotate the queries,
-append the new token's key and value (flushing the full residual window to
-INT2 every 128 steps), then the fused INT2 dequant + inverse scaling +
-split-K attention and the log-sum-exp combine.  The packed cache (~4.35 GB
-read per step) is far larger than L2, so no flush between steps is needed.
+Headline line (the workload the metric is quoted on): one step = one decode
+step of one attention layer for the batch-48, 128K-context workload (32 query
+/ 8 KV heads, head_dim 128): rotate the queries, append the new token's key
+and value (the full residual window is flushed to INT2 every 128 steps, and
+the run is arranged so that at least one flush falls inside the timed
+steps), then the fused INT2 dequant + inverse scaling + split-K attention
+with the log-sum-exp combine in its last CTA per row.  The packed cache
+(about 4.35 GB read per step) is far larger than L2, so no flush of L2 is
+needed between steps.
 
 Prints one JSON line: value = device time per step (us, CUDA events over the
 timed steps, max over ranks); e2e = the same through the C ABI with the step's
 inputs copied from pinned host memory and the output read back every step;
 roofline = the fused decode call against the measured HBM copy bandwidth;
-cpu_baseline = the CPU oracle on a bounded sample, extrapolated.
+configs = the other workloads (decode with L2 flushed before every rep, and
+the streaming ones' whole steps); cpu_baseline = the CPU oracle on a bounded
+sample, single thread and on all cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -19,7 +24,8 @@ from __future__ import annotations
 
 import os
 
-# the CPU oracle leg is timed single-threaded (its BLAS calls must not fan out)
+# the CPU oracle leg is timed per process single-threaded (its BLAS calls must
+# not fan out; the all-core timing runs one process per core)
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -38,6 +44,9 @@ METRIC = "INT2 decode-attn µs/step & HBM GB/s (% of GB300 peak) at 128K ctx, ba
 UNIT = "us/step"
 HERE = os.path.dirname(os.path.abspath(__file__))
 TRAFFIC_FILE = os.path.join(HERE, "profiles", "decode_int2_batch48_128k_traffic.json")
+L2_FLUSH_BYTES = 512 << 20          # written before every flushed rep (L2 is 129 MB)
+CONFIG_WORKLOADS = ("tiny_1k", "qwen3_8b_32k", "long_stream_128k", "omni_tni_64k")
+ABLATION_WORKLOADS = ("tiny_1k", "qwen3_8b_32k", "omni_tni_64k")
 
 
 def _args():
@@ -57,6 +66,8 @@ def _args():
                    help="skip the accuracy report of the variants against bf16 attention")
     p.add_argument("--no-prefill", action="store_true",
                    help="skip the prefill timing (fused vs two-call) of the prompt")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads' decode and stream timings")
     p.add_argument("--num-splits", type=int, default=0,
                    help="split-K count of the INT2 decode (0: the library's planner)")
     p.add_argument("--workload", default=WORKLOAD,
@@ -72,11 +83,27 @@ def _dist_env():
     return world, rank, local
 
 
+def _metric(wl):
+    if wl.name == WORKLOAD:
+        return METRIC
+    return (f"INT2 decode-attn µs/step & HBM GB/s (% of GB300 peak), {wl.name}: batch {wl.B}, "
+            f"{wl.Hq} q / {wl.Hkv} KV heads, {wl.T0} tokens")
+
+
+def _cache_bytes(wl):
+    return wl.B * wl.Hkv * (wl.n_packed * 86 + wl.n_res * 514)
+
+
 def _config(wl, S=None):
+    gb = _cache_bytes(wl) / 1e9
     cfg = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": 128,
            "context": wl.T0, "key_group": 32, "residual_window": 128,
-           "step": "rotate_q + append_kv (flush every 128) + fused INT2 decode + LSE combine",
-           "l2": "inputs larger than L2: ~4.35 GB packed cache read per step vs 129 MB L2",
+           "step": "rotate_q + append_kv (flush every 128) + fused INT2 decode with the "
+                   "LSE combine in its last CTA per row",
+           "l2": (f"inputs larger than L2: ~{gb:.2f} GB packed cache read per step vs 129 MB L2"
+                  if gb > 2 * 0.129 else
+                  f"~{gb * 1e3:.0f} MB packed cache; L2 flushed ({L2_FLUSH_BYTES >> 20} MB "
+                  f"written) before every timed rep"),
            "parallelism": "replicas (one independent layer cache per GPU)"}
     if S is not None:
         cfg["num_splits"] = S
@@ -88,9 +115,9 @@ def _config(wl, S=None):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi polled every 100 ms in a child process; a reader thread
-    collects the lines.  ``start`` returns once the first sample arrived, so
-    the tool's own start-up never overlaps the timed region."""
+    """nvidia-smi polled every 50 ms in a child process; a reader thread
+    collects the lines.  ``wait_first`` returns once the first sample arrived,
+    so the tool's own start-up never overlaps the timed region."""
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -103,7 +130,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100", "-i", str(gpu_index)],
+                 "-lms", "50", "-i", str(gpu_index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -197,7 +224,21 @@ def _oracle_steps(wl, hc, kb, vb, b, h, i0, n):
     return time.perf_counter() - t
 
 
+def _oracle_worker(job):
+    """One process of the all-core oracle timing: builds row (b, h)'s cache and
+    times n decode steps of it (single-threaded).  Module-level so that a
+    spawned pool can run it."""
+    name, b, h, n = job
+    sys.path.insert(0, HERE)
+    from int2_kv_cache_02_gb300 import workloads as W
+    wl = W.WORKLOADS[name]
+    hc, kb, vb = _oracle_row_cache(wl, b, h, wl.T0 + n + 1)
+    return _oracle_steps(wl, hc, kb, vb, b, h, 0, n)
+
+
 def cpu_baseline(wl, budget_s=20.0):
+    """The oracle as it stands, timed on this host's cores: one thread on 2
+    rows, then one process per core on as many rows in parallel."""
     rows = [(0, 0), (wl.B - 1, wl.Hkv - 1)]
     max_steps = 20
     built = [(b, h) + _oracle_row_cache(wl, b, h, wl.T0 + max_steps + 1) for (b, h) in rows]
@@ -209,9 +250,33 @@ def cpu_baseline(wl, budget_s=20.0):
         tot += _oracle_steps(wl, hc, kb, vb, b, h, 1 if k == 0 else 0, n)
     per = tot / (n * len(rows))
     total_rows = wl.B * wl.Hkv
-    return {"value": per * total_rows * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{len(rows)} of {total_rows} (sequence, KV head) rows x {n} decode steps "
-                      f"at full context, single thread; extrapolated x{total_rows} rows"}
+    out = {"value": per * total_rows * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"{len(rows)} of {total_rows} (sequence, KV head) rows x {n} decode steps "
+                     f"at full context, single thread; extrapolated x{total_rows} rows",
+           "host_cores": os.cpu_count()}
+    # all cores: one spawned process per core, one row each (the pool starts
+    # with `spawn`: a forked child of a CUDA process can hang)
+    ncpu = os.cpu_count() or 1
+    rows_all = [(wl.name, r // wl.Hkv % wl.B, r % wl.Hkv, n) for r in range(min(ncpu, total_rows))]
+    try:
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        t0 = time.perf_counter()
+        with ctx.Pool(len(rows_all)) as pool:
+            times = pool.map(_oracle_worker, rows_all)
+        wall = time.perf_counter() - t0
+        # the processes ran their n steps concurrently: the slowest sets the
+        # rate of len(rows_all) rows per n steps
+        per_all = max(times) / n
+        out["all_cores"] = {
+            "value": per_all * total_rows / len(rows_all) * 1e6, "unit": UNIT,
+            "cores": len(rows_all), "kind": "oracle",
+            "sample": f"{len(rows_all)} rows in {len(rows_all)} single-threaded processes, "
+                      f"{n} decode steps each at full context (their cache builds untimed, "
+                      f"{wall:.1f} s in all); extrapolated x{total_rows / len(rows_all):.1f}"}
+    except Exception as e:  # a host without room for the processes keeps the 1-thread figure
+        out["all_cores"] = {"unavailable": f"{type(e).__name__}: {e}"}
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -252,13 +317,13 @@ def run_reference(args, world, rank):
     sample = (f"1 of {total_rows} rows per step, {keep} packed tokens (+ residual) of the "
               f"row (the workload's prompt has {wl.n_packed}), single thread; extrapolated "
               f"x{scale:.1f} (rows x packed-token ratio)")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+    line = {"impl": "reference", "metric": _metric(wl), "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
             "config": _config(wl),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "host_cores": os.cpu_count()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -288,6 +353,177 @@ def _algorithmic_bytes(wl, n_packed, n_res, S):
     return cache + qo + ws
 
 
+def _peaks():
+    try:
+        with open(os.path.join(HERE, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def _median_timed(fn, reps, flushbuf=None):
+    """Median device time (us) of fn() over reps, each bracketed by CUDA
+    events on the current stream; with flushbuf, the buffer is written
+    before every rep, outside the events."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    for a, b in evs:
+        if flushbuf is not None:
+            flushbuf.zero_()
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ts = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    return ts[len(ts) // 2], ts
+
+
+def measure_config(L, W, name, dev, flushbuf, peak, reps=20):
+    """One workload other than the headline one: the fused decode over its
+    prompt (plus one appended token) with L2 flushed before every rep, and
+    for the streaming workloads the whole decode step (rotate_q, append with
+    the flushes every 128 tokens, decode) over the workload's 256 steps, L2
+    flushed before every step."""
+    import torch
+    wl = W.WORKLOADS[name]
+    tau = 1.0 / math.sqrt(128)
+    steps = max(wl.steps, 1)
+    K, V = W.draw_kv_cuda(wl, 0, wl.T0, device=dev)
+    cache = W.build_cache_cuda(wl, K, V, T_cap=wl.t_cap(steps - wl.steps + 1), device=dev)
+    del K, V
+    Kn, Vn = W.draw_kv_cuda(wl, wl.T0, steps + 1, device=dev)
+    Kn = Kn.permute(2, 0, 1, 3).contiguous()
+    Vn = Vn.permute(2, 0, 1, 3).contiguous()
+    Q = torch.stack([W.draw_q_cuda(wl, i, device=dev) for i in range(steps + 1)])
+    qr = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
+    out = torch.empty_like(qr)
+    S_max = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, cache.T_cap)
+    ws = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, cache.T_cap,
+                                                    max(S_max, 64)), device=dev)
+    res = {"B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "context": wl.T0}
+    if wl.n_packed:
+        # decode over the prompt + the first appended token
+        L.append_kv(cache, Kn[0], Vn[0], n_tok=1)
+        L.rotate_q(Q[0], qr)
+        S = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, cache.n_packed)
+        dec = lambda: L.decode_attention(cache, qr, wl.Hq, tau, out, ws, num_splits=S)
+        for _ in range(3):
+            dec()
+        us, _ = _median_timed(dec, reps, flushbuf)
+        nbytes = _algorithmic_bytes(wl, cache.n_packed, cache.n_res, S)
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res.update({"num_splits": S, "packed_tokens": cache.n_packed,
+                    "residual_tokens": cache.n_res, "decode_us": us,
+                    "algorithmic_bytes": nbytes, "GB/s": gbs, "frac": gbs / peak,
+                    "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB written) before each of {reps} reps"})
+    if wl.steps > 1:
+        # the workload's decode steps, one by one, from the next token on
+        n_st = wl.steps - 1
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n_st)]
+        flushes, nbytes = 0, 0
+        for i, (a, b) in enumerate(evs):
+            flushbuf.zero_()
+            if cache.n_res == 128:
+                flushes += 1
+            a.record()
+            L.rotate_q(Q[i + 1], qr)
+            L.append_kv(cache, Kn[i + 1], Vn[i + 1], n_tok=1)
+            L.decode_attention(cache, qr, wl.Hq, tau, out, ws, num_splits=0)
+            b.record()
+            S = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, cache.n_packed)
+            nbytes += _algorithmic_bytes(wl, cache.n_packed, cache.n_res, S)
+        torch.cuda.synchronize()
+        st = [a.elapsed_time(b) * 1e3 for a, b in evs]
+        us = float(np.mean(st))
+        gbs = nbytes / n_st / (us * 1e-6) / 1e9
+        res["stream"] = {"steps": n_st, "flushes": flushes, "us_per_step": us,
+                         "us_per_step_median": float(np.median(st)), "GB/s": gbs,
+                         "frac": gbs / peak,
+                         "note": "whole decode step (rotate_q + append_kv + decode), L2 "
+                                 "flushed before every step; GB/s counts the decode's "
+                                 "algorithmic bytes only"}
+    if L.device_status() != 0:
+        raise RuntimeError(f"{name}: a kernel recorded an error")
+    del cache, ws, Kn, Vn, Q
+    torch.cuda.empty_cache()
+    return res
+
+
+ABLATION_VARIANTS = (("oscar", 0, 2), ("no_rotate (scaling only)", 1, 2),
+                     ("no_scale (rotation only)", 2, 2), ("neither (KIVI-style)", 3, 2),
+                     ("all_heads_norm", 4, 2), ("oscar_int4", 0, 4))
+
+
+def ablation_report(L, W, dev):
+    """Accuracy of the method and its ablations against unquantised bf16
+    attention on needle inputs (a few keys per row point at the row's queries,
+    so attention concentrates and the reference output is far from zero).
+    GPU: every row of the workload, against the bf16 split-K kernel on the
+    same raw keys and values.  Oracle: row (0, 0), its own quantised attention
+    against its own exact bf16 attention.  Information only, not a gate."""
+    import torch
+    from oracle import oscar_oracle as O
+    tau = 1.0 / math.sqrt(128)
+    rep = {"inputs": f"each workload's keys with {W.N_NEEDLES} needle keys per (sequence, KV "
+                     f"head) row: typical key norm, pointing along the mean of the row's "
+                     f"query group (tilted by a seeded tenth), at seeded positions in the "
+                     f"packed prefix; values unchanged; decode step 0",
+           "reference": "bf16 attention over the same raw keys and values",
+           "metric": "relative L2 error of the whole output; per-vector median in 'median'",
+           "workloads": {}}
+    for name in ABLATION_WORKLOADS:
+        wl = W.WORKLOADS[name]
+        K, V = W.draw_kv_cuda(wl, 0, wl.T0, device=dev)
+        W.plant_needles_cuda(wl, K)
+        q = W.draw_q_cuda(wl, 0, device=dev)
+        ref = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
+        wsr = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, wl.T0, 512),
+                                device=dev)
+        L.bf16_decode_attention(q, K, V, wl.B, wl.Hq, wl.Hkv, wl.T0, wl.T0, tau, ref, wsr,
+                                num_splits=0)
+        qr = torch.empty_like(ref)
+        gpu = {}
+        for vname, fl, bits in ABLATION_VARIANTS:
+            cv = L.KVCache(wl.B, wl.Hkv, wl.n_packed, flags=fl, device=dev, bits=bits)
+            L.prefill_kv(cv, K, V, n_tok=wl.n_packed, in_T=wl.T0)
+            if wl.n_res:
+                L.append_kv(cv, K[:, :, wl.n_packed:wl.T0].contiguous(),
+                            V[:, :, wl.n_packed:wl.T0].contiguous(), n_tok=wl.n_res)
+            L.rotate_q(q, qr, flags=fl)
+            wsv = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, cv.n_packed),
+                                    device=dev)
+            ov = torch.empty_like(ref)
+            L.decode_attention(cv, qr, wl.Hq, tau, ov, wsv)
+            torch.cuda.synchronize()
+            if L.device_status() != 0:
+                raise RuntimeError(f"ablation {name} / {vname}: a kernel recorded an error")
+            d = (ov - ref).double()
+            per = torch.linalg.vector_norm(d, dim=-1) / torch.linalg.vector_norm(ref.double(),
+                                                                                 dim=-1)
+            gpu[vname] = {"rel_l2": float(torch.linalg.vector_norm(d)
+                                          / torch.linalg.vector_norm(ref.double())),
+                          "median": float(per.median())}
+            del cv, wsv, ov
+        del K, V, wsr
+        torch.cuda.empty_cache()
+        # the oracle on row (0, 0), per-head norm variants
+        kb = W.plant_needles(wl, wl.k_bits([0], [0], 0, wl.T0)[0, 0], 0, 0)
+        vb = wl.v_bits([0], [0], 0, wl.T0)[0, 0]
+        qb = wl.q_bits([0], range(wl.g), 0)[0]
+        oref = O.bf16_attention(qb, kb, vb, tau)
+        orc = {}
+        for vname, fl, bits in ABLATION_VARIANTS:
+            if fl & O.NORM_ALL_HEADS:
+                continue                         # spans every head of the token: GPU only
+            hc = O.build_head_cache(kb, vb, wl.n_packed, fl, bits=bits)
+            o = hc.decode(O.rotate_q(qb, fl), tau)
+            orc[vname] = float(np.linalg.norm(o - oref) / np.linalg.norm(oref))
+        rep["workloads"][name] = {"gpu": gpu, "oracle_row_0_0": orc}
+    return rep
+
+
 def run_ours(args, world, rank, local):
     import torch
     if world > 1:
@@ -305,8 +541,13 @@ def run_ours(args, world, rank, local):
     tau = 1.0 / math.sqrt(128)
     W_, K_ = args.warmup, args.steps
     E_ = args.e2e_steps
-    total_steps = W_ + K_ + 2 + E_
+    flush_at = min(max(K_ // 2, 0), 64)         # timed step at which a flush falls
+    total_steps = W_ + 128 + K_ + 2 + E_
     T_cap = wl.t_cap(total_steps - wl.steps)
+    peaks = _peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "of measured" if peak else "of fallback"
+    peak = peak or 6800.0
 
     # prompt: raw K, V drawn on the device, cache built through the library
     K, V = W.draw_kv_cuda(wl, 0, wl.T0, device=dev)
@@ -337,14 +578,22 @@ def run_ours(args, world, rank, local):
     vis = [v for v in vis.split(",") if v.strip().isdigit()]
     sampler = ClockSampler(int(vis[local]) if local < len(vis) else local)
     sampler.wait_first()
-    for i in range(W_):
-        step(i)
+    i_step = 0
+    for _ in range(W_):
+        step(i_step)
+        i_step += 1
+    # untimed steps until the residual window fills at timed step flush_at, so
+    # that the timed steps include a flush (one every 128 steps)
+    while (cache.n_res + flush_at) % 128 != 0 and K_ > 0:
+        step(i_step)
+        i_step += 1
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     ctx0 = (cache.n_packed, cache.n_res)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(K_)]
+    st_evs = [torch.cuda.Event(enable_timing=True) for _ in range(K_ + 1)]
     flush_steps = []
     launches0 = L.kernel_launches()
     t_start = torch.cuda.Event(enable_timing=True)
@@ -355,8 +604,12 @@ def run_ours(args, world, rank, local):
     for j in range(K_):
         if cache.n_res == 128:
             flush_steps.append(j)
-        step(W_ + j, evs[j])
+        st_evs[j].record(stream)
+        step(i_step, evs[j])
+        i_step += 1
         bytes_sum += _algorithmic_bytes(wl, cache.n_packed, cache.n_res, S)
+    if K_:
+        st_evs[K_].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -367,15 +620,32 @@ def run_ours(args, world, rank, local):
     if L.device_status() != 0:
         raise RuntimeError("a kernel recorded an error during the benchmark")
 
+    step_us = [st_evs[j].elapsed_time(st_evs[j + 1]) * 1e3 for j in range(K_)]
+    flush_obj = None
+    if flush_steps:
+        plain = [t for j, t in enumerate(step_us) if j not in flush_steps]
+        base_us = float(np.median(plain)) if plain else float("nan")
+        with_f = [step_us[j] for j in flush_steps]
+        rows = wl.B * wl.Hkv
+        fb = rows * 128 * (256 + 2 + 256) + rows * 4 * 2752   # read the window, write 4 records
+        extra = float(np.mean(with_f)) - base_us
+        flush_obj = {"timed_steps_with_flush": flush_steps, "step_us_with_flush": with_f,
+                     "median_step_us_without": base_us, "flush_us": extra,
+                     "flush_GB/s": fb / (extra * 1e-6) / 1e9 if extra > 0 else None,
+                     "algorithmic_bytes": fb,
+                     "note": "a flush quantises the batch's full residual windows (128 tokens "
+                             "per row: rotated keys, norms and values read, 4 records per row "
+                             "written); its cost is the flush step's time minus the median of "
+                             "the other timed steps"}
     ms_total = t_start.elapsed_time(t_end)
     dec_ms = [a.elapsed_time(b) for a, b in evs]
-    ms_step = max_over_ranks(ms_total / K_, world, dev)
-    dec_avg_ms = float(np.mean(dec_ms))
-    achieved = (bytes_sum / K_) / (dec_avg_ms * 1e-3) / 1e9
+    ms_step = max_over_ranks(ms_total / max(K_, 1), world, dev)
+    dec_avg_ms = float(np.mean(dec_ms)) if dec_ms else float("nan")
+    achieved = (bytes_sum / max(K_, 1)) / (dec_avg_ms * 1e-3) / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
     pin = lambda t: t.cpu().pin_memory()
-    base = W_ + K_ + 2
+    base = i_step + 2
     Qh, Kh, Vh = pin(Q[base:base + E_]), pin(Kn[base:base + E_]), pin(Vn[base:base + E_])
     outh = torch.empty((E_,) + tuple(out.shape), dtype=torch.float32).pin_memory()
     # Copies run on their own stream, double-buffered, so that step i + 1's
@@ -426,7 +696,7 @@ def run_ours(args, world, rank, local):
     stream.wait_event(back[(E_ - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_us = e0.elapsed_time(e1) / E_ * 1e3
+    e2e_us = e0.elapsed_time(e1) / max(E_, 1) * 1e3
     h2d = (Qh[0].numel() * Qh.element_size() + Kh[0].numel() * Kh.element_size()
            + Vh[0].numel() * Vh.element_size())
     d2h = out.numel() * out.element_size()
@@ -436,42 +706,35 @@ def run_ours(args, world, rank, local):
     bf16 = None
     if not args.no_bf16:
         qb = Q[0]
-        S16 = 0
         ws16 = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, wl.T0, 512),
                                  device=dev)
         o16 = torch.empty_like(out)
+        run16 = lambda: L.bf16_decode_attention(qb, K, V, wl.B, wl.Hq, wl.Hkv, wl.T0, wl.T0,
+                                                tau, o16, ws16, num_splits=0)
         for _ in range(3):
-            L.bf16_decode_attention(qb, K, V, wl.B, wl.Hq, wl.Hkv, wl.T0, wl.T0, tau, o16, ws16,
-                                    num_splits=S16)
+            run16()
         torch.cuda.synchronize()
         reps = 20
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(reps):
-            L.bf16_decode_attention(qb, K, V, wl.B, wl.Hq, wl.Hkv, wl.T0, wl.T0, tau, o16, ws16,
-                                    num_splits=S16)
+            run16()
         b.record(stream)
         torch.cuda.synchronize()
         bf_ms = a.elapsed_time(b) / reps
         bf_bytes = wl.B * wl.Hkv * wl.T0 * 512
         bf16 = {"us_per_call": bf_ms * 1e3, "GB/s": bf_bytes / (bf_ms * 1e-3) / 1e9,
+                "frac": bf_bytes / (bf_ms * 1e-3) / 1e9 / peak,
                 "int2_decode_speedup": bf_ms / dec_avg_ms,
-                "note": "equal-shape bf16 split-K decode (B48, 32/8, 131072 tokens), "
-                        "25.8 GB of K,V per call"}
-
-    peaks = {}
-    try:
-        with open(os.path.join(HERE, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except OSError:
-        pass
+                "note": f"equal-shape bf16 split-K decode (B{wl.B}, {wl.Hq}/{wl.Hkv}, "
+                        f"{wl.T0} tokens), {bf_bytes / 1e9:.1f} GB of K,V per call"}
+        del ws16
 
     # ---- prefill of the prompt's packed part: fused vs two-call path ----
     prefill = None
     if not args.no_prefill and wl.n_packed:
         def time_build(fused, reps=3):
-            c = None
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             ts = []
@@ -494,7 +757,7 @@ def run_ours(args, world, rank, local):
         f_bytes = th * (256 + 256 + 86)          # read k, v; write the records
         prefill = {"tokens": wl.n_packed, "fused_us": f_ms * 1e3,
                    "fused_GB/s": f_bytes / (f_ms * 1e-3) / 1e9,
-                   "fused_frac": f_bytes / (f_ms * 1e-3) / 1e9 / (peaks.get("hbm_gbs") or 6800.0),
+                   "fused_frac": f_bytes / (f_ms * 1e-3) / 1e9 / peak,
                    "two_call_us": s_ms * 1e3, "speedup": s_ms / f_ms,
                    "note": "rotate + scale + quantise of the prompt's packed tokens; "
                            "algorithmic bytes 598 per token-head (fused)"}
@@ -517,15 +780,17 @@ def run_ours(args, world, rank, local):
         wsp = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, max_tok, Sp),
                                 device=dev)
         L.rotate_q(Q[0], qr)
+        run_p = lambda: L.paged_decode_attention(pc, qr, wl.Hq, tau, max_tok, out, wsp,
+                                                 num_splits=Sp)
         for _ in range(3):
-            L.paged_decode_attention(pc, qr, wl.Hq, tau, max_tok, out, wsp, num_splits=Sp)
+            run_p()
         torch.cuda.synchronize()
         reps = 20
         a = torch.cuda.Event(enable_timing=True)
         b_ = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(reps):
-            L.paged_decode_attention(pc, qr, wl.Hq, tau, max_tok, out, wsp, num_splits=Sp)
+            run_p()
         b_.record(stream)
         torch.cuda.synchronize()
         if L.device_status() != 0:
@@ -537,7 +802,7 @@ def run_ours(args, world, rank, local):
         paged = {"sequences": wl.B, "packed_tokens_min": min(n_tok_h),
                  "packed_tokens_max": max_tok, "packed_tokens_mean": float(np.mean(n_tok_h)),
                  "pages": sum(blocks), "num_splits": Sp, "decode_us": p_ms * 1e3,
-                 "GB/s": p_gbs, "frac": p_gbs / (peaks.get("hbm_gbs") or 6800.0),
+                 "GB/s": p_gbs, "frac": p_gbs / peak,
                  "note": "oscar_paged_decode_attention over per-sequence lengths drawn "
                          "uniformly in [n_packed/4, n_packed] (+1 residual token), pages "
                          "handed out in a shuffled order"}
@@ -555,15 +820,16 @@ def run_ours(args, world, rank, local):
         ws4 = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, c4.n_packed, S4),
                                 device=dev)
         L.rotate_q(Q[0], qr)
+        run4 = lambda: L.decode_attention(c4, qr, wl.Hq, tau, out, ws4, num_splits=S4)
         for _ in range(3):
-            L.decode_attention(c4, qr, wl.Hq, tau, out, ws4, num_splits=S4)
+            run4()
         torch.cuda.synchronize()
         reps = 20
         a = torch.cuda.Event(enable_timing=True)
         b_ = torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(reps):
-            L.decode_attention(c4, qr, wl.Hq, tau, out, ws4, num_splits=S4)
+            run4()
         b_.record(stream)
         torch.cuda.synchronize()
         if L.device_status() != 0:
@@ -574,53 +840,28 @@ def run_ours(args, world, rank, local):
                    + 2 * wl.B * wl.Hq * 128 * 4 + 2 * wl.B * wl.Hq * (S4 + 1) * 132 * 4)
         i_gbs = i_bytes / (i_ms * 1e-3) / 1e9
         int4 = {"packed_tokens": c4.n_packed, "residual_tokens": c4.n_res, "num_splits": S4,
-                "decode_us": i_ms * 1e3, "GB/s": i_gbs,
-                "frac": i_gbs / (peaks.get("hbm_gbs") or 6800.0),
+                "decode_us": i_ms * 1e3, "GB/s": i_gbs, "frac": i_gbs / peak,
                 "note": "INT4 option (16 levels, 150 B per packed token-head) over the same "
                         "prompt; L2 not flushed between the 20 reps (7.5 GB of records)"}
         del c4, ws4
         torch.cuda.empty_cache()
+    # the headline workload's big buffers are not needed any more
+    del K, V, Kn, Vn, cache, ws
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads, each on its own ----
+    configs = None
+    if not args.no_configs and args.workload == WORKLOAD:
+        flushbuf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        configs = {name: measure_config(L, W, name, dev, flushbuf, peak)
+                   for name in CONFIG_WORKLOADS}
+        del flushbuf
+        torch.cuda.empty_cache()
     # ---- accuracy of the variants against unquantised bf16 attention ----
-    # (information, not a gate: the pages' ablation of rotation and scaling)
     ablation = None
-    if not args.no_ablation and wl.n_packed:
-        qb = Q[0]
-        ref = torch.empty_like(out)
-        wsr = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, wl.T0, 64),
-                                device=dev)
-        L.bf16_decode_attention(qb, K, V, wl.B, wl.Hq, wl.Hkv, wl.T0, wl.T0, tau, ref, wsr,
-                                num_splits=64)
-        variants = [("oscar", 0, 2), ("no_rotate", L.NO_ROTATE, 2), ("no_scale", L.NO_SCALE, 2),
-                    ("neither (KIVI-style)", L.NO_ROTATE | L.NO_SCALE, 2),
-                    ("all_heads_norm", L.NORM_ALL_HEADS, 2), ("oscar_int4", 0, 4)]
-        ablation = {"reference": "bf16 split-K decode over the raw bf16 K, V (the same T0 tokens)",
-                    "variants": {}}
-        rn = float(torch.linalg.vector_norm(ref))
-        for name, fl, bits in variants:
-            cv = L.KVCache(wl.B, wl.Hkv, wl.n_packed, flags=fl, device=dev, bits=bits)
-            L.prefill_kv(cv, K, V, n_tok=wl.n_packed, in_T=wl.T0)
-            if wl.n_res:
-                L.append_kv(cv, K[:, :, wl.n_packed:wl.T0].contiguous(),
-                            V[:, :, wl.n_packed:wl.T0].contiguous(), n_tok=wl.n_res)
-            L.rotate_q(qb, qr, flags=fl)
-            Sv = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, cv.n_packed)
-            wsv = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, cv.n_packed, Sv),
-                                    device=dev)
-            ov = torch.empty_like(out)
-            L.decode_attention(cv, qr, wl.Hq, tau, ov, wsv, num_splits=Sv)
-            torch.cuda.synchronize()
-            if L.device_status() != 0:
-                raise RuntimeError(f"ablation variant {name} recorded a device error")
-            d = ov - ref
-            ablation["variants"][name] = {
-                "rel_l2": float(torch.linalg.vector_norm(d)) / rn,
-                "max_abs": float(d.abs().max())}
-            del cv, wsv, ov
-            torch.cuda.empty_cache()
-        del wsr, ref
-    peak = peaks.get("hbm_gbs")
-    peak_src = "of measured" if peak else "of fallback"
-    peak = peak or 6800.0
+    if not args.no_ablation and args.workload == WORKLOAD:
+        ablation = ablation_report(L, W, dev)
+
     traffic = None
     try:
         with open(TRAFFIC_FILE) as f:
@@ -632,28 +873,33 @@ def run_ours(args, world, rank, local):
         traffic = None
 
     line = {
-        "metric": METRIC, "value": ms_step * 1e3, "unit": UNIT, "n_gpus": world,
+        "metric": _metric(wl), "value": ms_step * 1e3, "unit": UNIT, "n_gpus": world,
         "steps": K_, "warmup": W_, "ms_per_step": ms_step, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "int2 codes; f16 tensor-core MMA (hi+lo split), f32 accumulate",
         "data": "synthetic", "config": _config(wl, S),
         "decode_tokens_per_s": world * wl.B / (ms_step * 1e-3),
-        "prefill": prefill,
-        "paged": paged,
-        "int4": int4,
-        "ablation": ablation,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src, "traffic": traffic,
-                     "kernel": "oscar_decode_attention (fused INT2 decode + LSE combine)",
+                     "peak_note": "the measured copy bandwidth (read + write); a read-only "
+                                  "stream can exceed it slightly",
+                     "kernel": "oscar_decode_attention (fused INT2 decode, LSE combine in "
+                               "the last CTA of each row)",
                      "decode_us": dec_avg_ms * 1e3,
-                     "algorithmic_bytes_per_launch": bytes_sum / K_},
+                     "algorithmic_bytes_per_launch": bytes_sum / max(K_, 1)},
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": E_},
         "gpu_launches": int(launches),
         "clocks": _clock_summary(clock_rows, wall0, wall1),
         "context_tokens": {"start": ctx0[0] + ctx0[1],
-                           "end": cache.n_packed + cache.n_res},
+                           "end": ctx0[0] + ctx0[1] + K_},
         "flushes_in_timed_region": len(flush_steps),
+        "flush": flush_obj,
+        "configs": configs,
+        "prefill": prefill,
+        "paged": paged,
+        "int4": int4,
+        "ablation": ablation,
     }
     if bf16 is not None:
         line["bf16_decode"] = bf16

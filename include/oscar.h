@@ -82,8 +82,10 @@ enum { OSCAR_NO_ROTATE = 1u, OSCAR_NO_SCALE = 2u, OSCAR_NORM_ALL_HEADS = 4u };
  * advanced by the calls below (host-side bookkeeping).
  *
  * Packed layout: one record of OSCAR_BLOCK_BYTES per block of 32 tokens,
- * records [B][Hkv][T_cap/32] contiguous (T_cap a multiple of 32).  Byte
- * offsets inside a record:
+ * records [B][Hkv][T_cap/32] contiguous (T_cap a multiple of 32).  The
+ * record takes the place of separate key-code, value-code, step, zero and
+ * norm arrays: one 1-D bulk copy brings a whole block into shared memory.
+ * Byte offsets inside a record:
  *     0  key codes    uint32 [32 tokens][8]: 16 codes per word; word w of a
  *                     token holds channels 16w..16w+15, channel 16w+j at bit
  *                     2*(j/2) + 16*(j%2) (even channels in the low half-word,
@@ -274,8 +276,19 @@ oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const osca
  *  out        fp32 [B][Hq][128]; an empty cache gives zeros
  *  num_splits packed-token splits per (b,h); 0 = choose for this device
  *             (oscar_decode_num_splits); one more split handles the residual.
- *  workspace  device scratch of at least oscar_decode_workspace_bytes(B, Hq,
- *             splits) bytes (16-byte aligned); contents need no initialisation.
+ *  workspace  device scratch of at least oscar_decode_workspace_bytes(B, Hkv,
+ *             Hq, n_packed, splits) bytes (16-byte aligned), caller-owned.  It
+ *             holds the split-K partial records, B*Hq*(splits+1) records of
+ *             528 bytes, then one 32-bit arrival counter per (b, h) row,
+ *             B*Hkv*4 bytes rounded up to 16.  The row's last CTA to finish
+ *             combines the row's partials (no second kernel is launched) and
+ *             sets its counter back to zero.  So the counter area must be
+ *             zero before a workspace's first use (cudaMemset it once after
+ *             allocating); every call leaves it zero.  A CTA that finds its
+ *             row's counter already at or above the row's split count
+ *             records an error in the device status word
+ *             (oscar_device_status).  Calls that use one workspace must not
+ *             overlap on the GPU.
  */
 oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, int Hq,
                                     float softmax_scale, float* out, int num_splits,
@@ -285,8 +298,10 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
  * device (>= 1).  Returns 1 when no device can be queried. */
 int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed);
 
-/* Workspace bytes needed by oscar_decode_attention / oscar_bf16_decode_attention
- * for `num_splits` token splits (0 = the automatic count for n_packed tokens). */
+/* Workspace bytes needed by oscar_decode_attention / oscar_paged_decode_attention
+ * (and enough for oscar_bf16_decode_attention) for `num_splits` token splits
+ * (0 = the automatic count for n_packed tokens): B*Hq*(splits+1)*528 bytes of
+ * partial records plus B*Hkv*4 bytes of row counters, rounded up to 16. */
 size_t oscar_decode_workspace_bytes(int B, int Hkv, int Hq, int n_packed, int num_splits);
 
 /*
@@ -314,19 +329,25 @@ oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* 
  * or a plug-in whose host runtime owns all device memory and lends it no
  * allocator.  The pages have no counterpart: this is an integration aid.
  * Same arguments, results and checks as oscar_decode_attention, except that
- * the split-K partial records live in a 16 MiB array inside the library
+ * the split-K partial records and the row counters (the workspace of
+ * oscar_decode_attention) live in a 16 MiB array inside the library
  * (OSCAR_STATIC_SCRATCH_BYTES), which every GPU that loads the library keeps
  * until the process exits.  The call allocates nothing.
- *  - B * Hq * (splits + 1) * 528 bytes must fit in that array; larger
- *    requests return OSCAR_ERR_WORKSPACE and launch nothing (the automatic
- *    split count of a batch-48, 32-query-head layer needs about 16.2 MB).
+ *  - The workspace, oscar_decode_workspace_bytes(B, Hkv, Hq, n_packed,
+ *    splits), must fit in that array.  With num_splits = 0 the automatic
+ *    split count is lowered to the largest that fits (at least 1); an
+ *    explicit count that does not fit, or a batch whose single split does
+ *    not fit, returns OSCAR_ERR_WORKSPACE and launches nothing.  For
+ *    example a batch-48, 32-query-head, 8-KV-head layer at the 12 splits
+ *    the planner gives a 128K context needs 48*32*13*528 + 48*8*4 bytes,
+ *    about 10.5 MB.
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress); make it before any stream
  *    capture.  A failed lookup returns OSCAR_ERR_CUDA.
  *  - Every call shares the one array and it keeps the last call's contents;
  *    calls whose kernels overlap on the GPU (e.g. on two streams) race on it.
- *    No part of it needs to start at zero: each call writes every record it
- *    reads.
+ *    The row counters must be zero when a call starts: the array starts
+ *    zeroed when the library loads and every call leaves them zero.
  */
 oscar_status oscar_decode_attention_static_ws(const oscar_cache* c, const float* q_rot, int Hq,
                                               float softmax_scale, float* out, int num_splits,

@@ -136,6 +136,7 @@ oscar_status flush_residual(oscar_cache* c, cudaStream_t s) {
 
 namespace oscar {
 // Internal accessors for other translation units of the library.
+oscar_status validate_cache(const oscar_cache* c) { return check_cache(c); }
 unsigned* device_status_word() { return status_ptr(); }
 void count_launches(int n) { g_launches += (unsigned long long)n; }
 }  // namespace oscar
@@ -262,7 +263,7 @@ int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed) {
 size_t oscar_decode_workspace_bytes(int B, int Hkv, int Hq, int n_packed, int num_splits) {
   if (B <= 0 || Hq <= 0) return 0;
   const int s = num_splits > 0 ? num_splits : oscar_decode_num_splits(B, Hkv, Hq, n_packed);
-  return ws_bytes_for(B, Hq, s + 1);
+  return decode_ws_bytes(B, Hkv > 0 ? Hkv : 1, Hq, s + 1);
 }
 
 oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, int Hq,
@@ -276,7 +277,8 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
   if (!al16(q_rot) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
   int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, c->n_packed);
-  if (!workspace || ws_bytes < ws_bytes_for(c->B, Hq, S + 1)) return OSCAR_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < decode_ws_bytes(c->B, c->Hkv, Hq, S + 1))
+    return OSCAR_ERR_WORKSPACE;
   if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;
   DecodeArgs a;
   a.packed = c->packed;
@@ -285,6 +287,7 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
   a.q_rot = q_rot;
   a.ws = static_cast<float*>(workspace);
+  a.row_count = decode_row_counters(a.ws, c->B, Hq, S + 1);
   a.out = out;
   a.status = status_ptr();
   a.B = c->B;
@@ -299,7 +302,7 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
   a.bits = code_bits(c->bits);
   cudaError_t e = launch_decode_int2(a, as_stream(stream));
-  g_launches += 2;
+  g_launches += 1;
   return from_cuda(e);
 }
 
@@ -398,7 +401,8 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
   if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
   if (!al16(q_rot) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
   int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, max_packed);
-  if (!workspace || ws_bytes < ws_bytes_for(c->B, Hq, S + 1)) return OSCAR_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < decode_ws_bytes(c->B, c->Hkv, Hq, S + 1))
+    return OSCAR_ERR_WORKSPACE;
   if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;
   DecodeArgs a;
   a.packed = c->pages;
@@ -407,6 +411,7 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
   a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
   a.q_rot = q_rot;
   a.ws = static_cast<float*>(workspace);
+  a.row_count = decode_row_counters(a.ws, c->B, Hq, S + 1);
   a.out = out;
   a.status = status_ptr();
   if (!a.status) return OSCAR_ERR_CUDA;
@@ -427,7 +432,7 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
   a.max_blocks = c->max_blocks;
   a.n_pages = c->n_pages;
   cudaError_t e = launch_decode_int2(a, as_stream(stream));
-  g_launches += 2;
+  g_launches += 1;
   return from_cuda(e);
 }
 

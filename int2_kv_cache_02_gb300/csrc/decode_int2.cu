@@ -6,8 +6,10 @@
 //
 // Grid (num_splits + 1, Hkv, B): CTA (s, h, b) with s < num_splits streams an
 // equal share of the 32-token blocks of row (b, h); CTA num_splits handles the
-// residual window.  Each CTA writes one log-sum-exp partial per query head;
-// combine_kernel folds them.
+// residual window.  Each CTA writes one log-sum-exp partial per query head
+// and counts itself in the row's arrival counter; the row's last CTA to
+// arrive folds the row's partials into the output (row_combine) and resets
+// the counter, so no second kernel is launched.
 //
 // Packed path, per 32-token block and warp (all on mma.sync m16n8k16 f16):
 //  * no per-element dequantisation: the key step s_c of the block is folded
@@ -273,12 +275,18 @@ struct WarpRing {
     for (int i = 0; i < NSTAGE && i < n; ++i) issue(i);
   }
   __device__ __forceinline__ void issue(int i) const {
-    if (lane == 0) {
-      uint64_t* bar = &bars[i % NSTAGE];
-      const uint8_t* rec = record(i);
-      mbar_arrive_expect_tx(bar, RB);
-      bulk_g2s(ring + (i % NSTAGE) * RB, rec, RB, bar);
-    }
+    // Every lane forms the (warp-uniform) addresses; one lane chosen by
+    // elect.sync arms the slot's mbarrier and issues the copy, so no branch
+    // on the lane index is needed.
+    const uint8_t* rec = record(i);
+    const unsigned bar = smem_u32(&bars[i % NSTAGE]);
+    const unsigned dst = smem_u32(ring + (i % NSTAGE) * RB);
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %2;\n\t"
+        "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%1], [%3], %2, [%0];\n\t}"
+        :: "r"(bar), "r"(dst), "r"(RB), "l"(rec) : "memory");
   }
   // true on every lane once block i has landed; false if the wait gave up
   __device__ __forceinline__ bool wait(int i) const {
@@ -1036,6 +1044,83 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
     for (int i = 0; i < 4; ++i) E.o[warp][j][4 * lane + i] = orr[j][i];
 }
 
+// Log-sum-exp combine of the `parts` partial records of each of the CTA's GQ
+// query heads (flash-decoding): m* = max_s m_s, out = sum_s 2^(m_s - m*) o_s /
+// sum_s 2^(m_s - m*) l_s, scores in the log2 domain.  Partials that saw no
+// token carry m = -inf and drop out; a row with none gives zeros.  Run by
+// the row's last CTA, after every other CTA's records are visible.  Warp w
+// takes head w (and w + 4 for groups of 8); for groups smaller than 4 the
+// warps of a head split its partials and add their sums in shared memory.
+// Lane l holds channels 4 l .. 4 l + 3.  The records were written by other
+// CTAs during this launch, so they are read past L1 (ld.global.cg).
+template <int GQ>
+__device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, NW>& E,
+                                            long long qrow0, int parts) {
+  constexpr int HPW = GQ > NW ? GQ / NW : 1;   // heads per warp
+  constexpr int PG = GQ >= NW ? 1 : NW / GQ;   // warps per head
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int hh = 0; hh < HPW; ++hh) {
+    const int j = GQ >= NW ? warp + NW * hh : warp % GQ;
+    const int pg = GQ >= NW ? 0 : warp / GQ;
+    const float* r0 = a.ws + (qrow0 + j) * parts * kRecFloats;
+    float M = -INFINITY;
+    for (int s = lane; s < parts; s += 32) M = fmaxf(M, __ldcg(r0 + (long long)s * kRecFloats));
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+    // four interleaved sums (partials of rank s mod 4), added pairwise at the
+    // end: short fp32 accumulation chains, as a four-warp split would give
+    float Lp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float4 op[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) op[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+      for (int s0 = pg; s0 < parts; s0 += 4 * PG) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int s = s0 + k * PG;
+          if (s < parts) {
+            const float* r = r0 + (long long)s * kRecFloats;
+            const float ms = __ldcg(r);
+            const float al = ms == -INFINITY ? 0.0f : fast_exp2(ms - M);
+            Lp[k] = fmaf(al, __ldcg(r + 1), Lp[k]);
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(r + 4) + lane);
+            op[k].x = fmaf(al, x.x, op[k].x); op[k].y = fmaf(al, x.y, op[k].y);
+            op[k].z = fmaf(al, x.z, op[k].z); op[k].w = fmaf(al, x.w, op[k].w);
+          }
+        }
+      }
+    }
+    const float L = (Lp[0] + Lp[1]) + (Lp[2] + Lp[3]);
+    const float4 o = make_float4((op[0].x + op[1].x) + (op[2].x + op[3].x),
+                                 (op[0].y + op[1].y) + (op[2].y + op[3].y),
+                                 (op[0].z + op[1].z) + (op[2].z + op[3].z),
+                                 (op[0].w + op[1].w) + (op[2].w + op[3].w));
+    if constexpr (PG == 1) {
+      reinterpret_cast<float4*>(a.out + (qrow0 + j) * kD)[lane] =
+          L > 0.0f ? make_float4(o.x / L, o.y / L, o.z / L, o.w / L)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      if (lane == 0) E.l[warp][0] = L;
+      reinterpret_cast<float4*>(E.o[warp][0])[lane] = o;
+    }
+  }
+  if constexpr (PG > 1) {
+    __syncthreads();
+    const int c = threadIdx.x;   // NW * 32 == kD channels, one per thread
+#pragma unroll
+    for (int j = 0; j < GQ; ++j) {
+      float Lt = 0.0f, oc = 0.0f;
+#pragma unroll
+      for (int g = 0; g < PG; ++g) {
+        Lt += E.l[j + GQ * g][0];
+        oc += E.o[j + GQ * g][0][c];
+      }
+      a.out[(qrow0 + j) * kD + c] = Lt > 0.0f ? oc / Lt : 0.0f;
+    }
+  }
+}
+
 // Up to 4 CTAs per SM in the column layout (128 registers), 3 in the row layout.
 // BSCALE: per-block step scale (caches with the all-heads norm scope);
 // BITS: code width of the records (2, or the INT4 option).
@@ -1060,8 +1145,25 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
     residual_split<GQ, PAGED>(a, E, row, qrow0, b);
   }
   __syncthreads();
-  cta_merge_write<GQ, NW>(E, a.ws + (qrow0 * (a.num_splits + 1) + split) * kRecFloats,
-                          (long long)(a.num_splits + 1) * kRecFloats);
+  const int parts = a.num_splits + 1;
+  cta_merge_write<GQ, NW>(E, a.ws + (qrow0 * parts + split) * kRecFloats,
+                          (long long)parts * kRecFloats);
+  // Arrival: this CTA's records are made visible device-wide first; the
+  // CTA that brings the row's count to `parts` combines the row and leaves
+  // the counter at zero for the next call on this workspace.
+  __shared__ int last_cta;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned prev = atomicAdd(a.row_count + row, 1u);
+    if (prev >= (unsigned)parts) record_error(a.status, kDevErrWorkspace);
+    last_cta = prev == (unsigned)(parts - 1);
+    if (last_cta) a.row_count[row] = 0u;
+  }
+  __syncthreads();
+  if (!last_cta) return;
+  __threadfence();
+  row_combine<GQ>(a, E, qrow0, parts);
 }
 
 // Opt in to the kernel's dynamic shared memory (above 48 KB for INT2), once
@@ -1085,9 +1187,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
   if (e0 != cudaSuccess) return e0;
   dim3 grid(a.num_splits + 1, a.Hkv, a.B);
   decode_int2_kernel<GQ, PAGED, BSCALE, BITS><<<grid, NW * 32, Layout<BITS>::SMEM, s>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_combine(a.ws, a.out, a.B * a.Hq, a.num_splits + 1, s);
+  return cudaGetLastError();
 }
 
 template <bool PAGED, bool BSCALE, int BITS>

@@ -16,9 +16,11 @@
 // with cudaGetSymbolAddress, once per device, on the first call made while
 // that device is current; make that first call before any stream capture.
 // All calls share the one array: calls whose kernels overlap on the GPU (two
-// streams, say) race on it and give wrong results.  Nothing in it has to
-// start at zero: every call writes each partial record before reading it, and
-// the array keeps whatever the last call left there.
+// streams, say) race on it and give wrong results.  The array holds the
+// partial records, which every call writes before it reads them, and after
+// them the rows' arrival counters, which must be zero when a call starts:
+// static device memory starts zeroed, and every call leaves the counters at
+// zero again.  Otherwise the array keeps whatever the last call left there.
 #include <cmath>
 #include <mutex>
 
@@ -29,7 +31,8 @@ namespace {
 
 using namespace oscar;
 
-constexpr size_t kScratchFloats = OSCAR_STATIC_SCRATCH_BYTES / sizeof(float);
+constexpr size_t kScratchBytes = OSCAR_STATIC_SCRATCH_BYTES;
+constexpr size_t kScratchFloats = kScratchBytes / sizeof(float);
 static __device__ __align__(256) float g_decode_scratch[kScratchFloats];
 
 std::mutex g_scratch_mu;
@@ -57,18 +60,8 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
                                                          float softmax_scale, float* out,
                                                          int num_splits, void* stream) {
   // the same argument checks as oscar_decode_attention
-  if (!c) return OSCAR_ERR_INVALID_ARG;
-  if (c->B <= 0 || c->Hkv <= 0 || c->T_cap <= 0 || c->T_cap % kG != 0)
-    return OSCAR_ERR_INVALID_ARG;
-  const void* ptrs[] = {c->packed, c->k_res, c->v_res, c->k_res_norm};
-  for (const void* p : ptrs) {
-    if (!p) return OSCAR_ERR_INVALID_ARG;
-    if (!aligned16(p)) return OSCAR_ERR_ALIGNMENT;
-  }
-  if (c->n_packed < 0 || c->n_packed % kG != 0 || c->n_packed > c->T_cap || c->n_res < 0 ||
-      c->n_res > kR || (c->flags & ~kAllFlags) || !target_ok(c->norm_target) ||
-      !key_group_ok(c->key_group) || !code_bits_ok(c->bits))
-    return OSCAR_ERR_INVALID_ARG;
+  const oscar_status st = validate_cache(c);
+  if (st != OSCAR_OK) return st;
   if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
       !std::isfinite(softmax_scale))
     return OSCAR_ERR_INVALID_ARG;
@@ -76,11 +69,19 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   if (!(g == 1 || g == 2 || g == 4 || g == 8)) return OSCAR_ERR_UNSUPPORTED;
   if (!aligned16(q_rot) || !aligned16(out)) return OSCAR_ERR_ALIGNMENT;
 
-  const int S = num_splits > 0 ? num_splits
-                               : oscar_decode_num_splits(c->B, c->Hkv, Hq, c->n_packed);
-  // the partial records must fit in the static array
-  const size_t need = (size_t)c->B * (size_t)Hq * (size_t)(S + 1) * kRecFloats;
-  if (need > kScratchFloats) return OSCAR_ERR_WORKSPACE;
+  // The partial records and counters must fit in the static array.  An
+  // automatic split count is lowered to the largest that fits; an explicit
+  // one that does not fit is refused.
+  int S = num_splits;
+  if (S == 0) {
+    S = oscar_decode_num_splits(c->B, c->Hkv, Hq, c->n_packed);
+    const size_t cnt = decode_ws_bytes(c->B, c->Hkv, Hq, 0);
+    const size_t per_part = (size_t)c->B * (size_t)Hq * kRecFloats * sizeof(float);
+    const long long parts = cnt < kScratchBytes ? (long long)((kScratchBytes - cnt) / per_part) : 0;
+    if (S + 1 > parts) S = (int)(parts - 1);
+    if (S < 1) return OSCAR_ERR_WORKSPACE;
+  }
+  if (decode_ws_bytes(c->B, c->Hkv, Hq, S + 1) > kScratchBytes) return OSCAR_ERR_WORKSPACE;
 
   float* ws = scratch_address();
   if (!ws) return OSCAR_ERR_CUDA;
@@ -92,6 +93,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
   a.q_rot = q_rot;
   a.ws = ws;
+  a.row_count = decode_row_counters(ws, c->B, Hq, S + 1);
   a.out = out;
   a.status = device_status_word();
   a.B = c->B;
@@ -106,6 +108,6 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
   a.bits = code_bits(c->bits);
   cudaError_t e = launch_decode_int2(a, static_cast<cudaStream_t>(stream));
-  count_launches(2);
+  count_launches(1);
   return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA;
 }

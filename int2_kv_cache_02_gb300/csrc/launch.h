@@ -69,6 +69,7 @@ struct DecodeArgs {
   const __half* k_res_norm;
   const float* q_rot;
   float* ws;          // partial records [B*Hq][num_splits + 1][kRecFloats]
+  unsigned* row_count;  // arrival counters [B*Hkv], zero between calls
   float* out;         // [B][Hq][128]
   unsigned* status;
   int B, Hkv, Hq, T_cap, n_packed, n_res, num_splits;
@@ -91,7 +92,19 @@ struct DecodeArgs {
 // Floats per split-K partial record: m, l, 2 pad, o[128].
 constexpr int kRecFloats = 132;
 
-// Fused INT2 decode attention + combine (two launches).
+// Decode workspace: the partial records [B*Hq][parts][kRecFloats], then the
+// rows' arrival counters [B*Hkv] (u32), rounded up to 16 bytes.
+inline size_t decode_ws_bytes(long long B, long long Hkv, long long Hq, long long parts) {
+  const size_t rec = (size_t)(B * Hq * parts) * kRecFloats * sizeof(float);
+  const size_t cnt = ((size_t)(B * Hkv) * sizeof(unsigned) + 15) / 16 * 16;
+  return rec + cnt;
+}
+inline unsigned* decode_row_counters(float* ws, long long B, long long Hq, long long parts) {
+  return reinterpret_cast<unsigned*>(ws + (size_t)(B * Hq * parts) * kRecFloats);
+}
+
+// Fused INT2 decode attention with the split-K combine in its last CTA per
+// row (one launch).
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t s);
 // Blocks per SM the INT2 decode kernel reaches for query group size g.
 int decode_int2_ctas_per_sm(int g);
@@ -113,6 +126,8 @@ int decode_bf16_ctas_per_sm(int g);
 // and the host launch counter behind oscar_kernel_launches().
 unsigned* device_status_word();
 void count_launches(int n);
+// The argument checks every contiguous-cache call applies to an oscar_cache.
+oscar_status validate_cache(const oscar_cache* c);
 
 // Paged cache: fused prefill of n_tok[b] tokens per sequence (then n_packed
 // += n_tok), flush of full residual windows, residual append of one token,

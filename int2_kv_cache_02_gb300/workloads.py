@@ -199,3 +199,71 @@ class _Offset:
 
 def _offset(t, t0: int):
     return _Offset(t, t0)
+
+
+# ---------------------------------------------------------------------------
+# Needle variant of a workload, for the accuracy report: a few keys per row
+# point at the row's queries, so that attention concentrates on them (in the
+# spirit of the pages' needle-in-a-haystack retrieval runs) and the output of
+# bf16 attention is far from zero.  Input structure only: no step of the
+# method is computed here.
+# ---------------------------------------------------------------------------
+
+N_NEEDLES = 4
+
+
+def needle_keys(wl: Workload, b: int, h: int, step: int = 0):
+    """(positions int [N_NEEDLES], raw bf16 key bits uint16 [N_NEEDLES][128])
+    for row (b, h): each needle key has the norm a typical key of the
+    workload has (the outlier channels included) and points along the mean of
+    the row's query group at decode step `step`, tilted by a seeded random
+    tenth, so that every query head of the group scores it far above the rest
+    of the context.  Positions are seeded, distinct, inside the packed
+    prefix and clear of its first block (the attention sinks)."""
+    g = wl.g
+    q = synth.bf16_bits_to_f32(wl.q_bits([b], range(h * g, (h + 1) * g), step)[0])
+    u = q.astype(np.float64).sum(axis=0)
+    u /= np.linalg.norm(u)
+    cf = wl.chan_factor().astype(np.float64)
+    norm = float(np.sqrt(np.sum(cf * cf)))          # expected norm of a drawn key
+    seed = wl.seed_base + 7
+    row = b * wl.Hkv + h
+    lo, hi = 32, max(33, wl.n_packed - 32)
+    r = synth.splitmix64(seed, np.arange(row * 64, row * 64 + 64)).astype(np.uint64)
+    pos, seen = [], set()
+    for x in r:
+        p = lo + int(x % np.uint64(hi - lo))
+        if p not in seen:
+            seen.add(p)
+            pos.append(p)
+        if len(pos) == N_NEEDLES:
+            break
+    tilt = synth.normal_f32(seed + 1, np.arange(row * N_NEEDLES * 128,
+                                                (row + 1) * N_NEEDLES * 128))
+    tilt = tilt.astype(np.float64).reshape(N_NEEDLES, 128)
+    tilt /= np.linalg.norm(tilt, axis=1, keepdims=True)
+    keys = u[None, :] + 0.1 * tilt
+    keys *= norm / np.linalg.norm(keys, axis=1, keepdims=True)
+    return np.array(pos), synth.f32_to_bf16_bits(keys.astype(np.float32))
+
+
+def plant_needles(wl: Workload, k_bits: np.ndarray, b: int, h: int, t0: int = 0):
+    """Row (b, h)'s raw key bits [n_t][128] for positions t0.. with the needles
+    written in (a copy)."""
+    out = np.array(k_bits, copy=True)
+    pos, keys = needle_keys(wl, b, h)
+    for p, k in zip(pos, keys):
+        if t0 <= p < t0 + out.shape[0]:
+            out[p - t0] = k
+    return out
+
+
+def plant_needles_cuda(wl: Workload, K):
+    """Writes every row's needles into raw keys K [B][Hkv][T][128] on the device."""
+    import torch
+    for b in range(wl.B):
+        for h in range(wl.Hkv):
+            pos, keys = needle_keys(wl, b, h)
+            kt = torch.from_numpy(keys.view(np.int16)).view(torch.bfloat16).to(K.device)
+            K[b, h, torch.from_numpy(pos).to(K.device)] = kt
+    return K

@@ -134,8 +134,14 @@ def test_cache_validation_and_state_untouched():
                                                   1, None) == 1
         assert bad.n_packed == 0 and bad.n_res == 0
     # key groups: only 32 (0), 64, 128; n_packed and quantised runs multiples of it
-    for bad in (_cache(key_group=48), _cache(key_group=256), _cache(key_group=64, n_packed=32)):
+    for bad in (_cache(key_group=48), _cache(key_group=256), _cache(key_group=64, n_packed=32),
+                _cache(key_group=128, n_packed=64)):
         assert L.oscar_prefill_kv(ctypes.byref(bad), P(FAKE), P(FAKE), 64, 64, None) == 1
+        # both decode entry points apply the same cache checks
+        assert L.oscar_decode_attention(ctypes.byref(bad), P(FAKE), 2, 0.1, P(FAKE), 1, P(FAKE),
+                                        1 << 20, None) == 1
+        assert L.oscar_decode_attention_static_ws(ctypes.byref(bad), P(FAKE), 2, 0.1, P(FAKE),
+                                                  1, None) == 1
     for bad in (_cache(bits=3), _cache(bits=8), _cache(bits=1)):
         assert L.oscar_prefill_kv(ctypes.byref(bad), P(FAKE), P(FAKE), 64, 64, None) == 1
         assert L.oscar_decode_attention_static_ws(ctypes.byref(bad), P(FAKE), 2, 0.1, P(FAKE),
@@ -218,7 +224,10 @@ def test_decode_validation():
     assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, P(FAKE), 4, None,
                                     1 << 30, None) == 5
     need = L.oscar_decode_workspace_bytes(2, 2, 8, 0, 4)
-    assert need == 2 * 8 * 5 * 132 * 4
+    # partial records of 132 floats, then one u32 counter per (b, h) row,
+    # rounded up to 16 bytes
+    assert need == 2 * 8 * 5 * 132 * 4 + 16
+    assert L.oscar_decode_workspace_bytes(3, 3, 6, 0, 1) == 3 * 6 * 2 * 528 + 48
     assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, P(FAKE), 4, P(FAKE),
                                     need - 1, None) == 5
     assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, float("nan"), P(FAKE), 4,

@@ -22,7 +22,7 @@ import torch
 from oracle import oscar_oracle as O
 from int2_kv_cache_02_gb300 import synth
 from tests._gpu_helpers import (TAU, assert_attention_close, bits_to_bf16_tensor,
-                                code_mismatches, upload_oracle_cache)
+                                code_mismatches, traced_key_check, upload_oracle_cache)
 
 pytestmark = pytest.mark.gpu
 LEVELS16 = np.arange(16) - 7.5
@@ -186,16 +186,13 @@ def test_pipeline_prefill_append_decode(L):
                 hc.append(kb[b, h, t], vb[b, h, t])
             heads[(b, h)] = hc
     assert (cache.n_packed, cache.n_res) == (heads[(0, 0)].n_packed, heads[(0, 0)].n_res)
-    n_codes = 0
     for (b, h), hc in heads.items():
-        got = cache.tokens("k_codes")[b, h, :cache.n_packed].cpu().numpy().view(np.uint32)
-        n_codes += code_mismatches(got, O.pack_k_words4(hc.packed_k().codes))
+        # every key code traced to its inputs (16 levels)
+        traced_key_check(L, cache, b, h, kb[b, h], vb[b, h], hc, bits=4,
+                         what=f"INT4 row {(b, h)}")
         gotv = cache.field("v_codes")[b, h, :cache.n_packed // 32].cpu().numpy()
         assert np.array_equal(gotv.reshape(-1).view(np.uint32),
                               O.pack_v_words4(hc.packed_v().codes).reshape(-1))
-    # 16 levels: a k_hat 1 ulp off a code boundary flips one code more often
-    # than at 4 levels, still a small count
-    assert n_codes <= 64, n_codes
     qbits = synth.gen_bf16(1412, Hq, range(B), range(Hq), 0, 1)[:, :, 0]
     qrot = O.rotate_q(qbits)
     qr = torch.from_numpy(qrot.astype(np.float32)).cuda()

@@ -81,3 +81,48 @@ def test_static_scratch_rejects_oversized_requests(L):
     assert st == 5                                     # OSCAR_ERR_WORKSPACE
     torch.cuda.synchronize()
     assert torch.all(out == 0)                         # nothing was launched
+
+
+def test_static_scratch_lowers_an_automatic_split_count_that_does_not_fit(L):
+    """With num_splits = 0 the planner's split count is lowered to the largest
+    one whose partial records and row counters fit in the static array; the
+    output then equals the workspace entry's at that count, bit for bit, on
+    two calls in a row.  The shape is chosen so that the planned count does
+    not fit (batch 128 or more, 32 query / 8 KV heads, 32K packed tokens)."""
+    Hkv, Hq, P = 8, 32, 32768
+    limit = 16 << 20
+    for B in (128, 160, 192, 256):
+        S_plan = L.decode_num_splits(B, Hkv, Hq, P)
+        if L.decode_workspace_bytes(B, Hkv, Hq, P, S_plan) > limit:
+            break
+    else:
+        raise AssertionError("no batch up to 256 needs more than the static array")
+    S = max(s for s in range(1, S_plan)
+            if L.decode_workspace_bytes(B, Hkv, Hq, P, s) <= limit)
+    # A cache of random codes with finite, plausible steps, zeros and norms:
+    # both entry points read the same bytes, so no oracle is needed here.
+    g = torch.Generator(device="cuda").manual_seed(930)
+    cache = L.KVCache(B, Hkv, P)
+    cache.packed.copy_(torch.randint(0, 256, cache.packed.shape, dtype=torch.uint8,
+                                     device="cuda", generator=g))
+    for name, lo, hi in (("k_scale", 0.05, 0.4), ("k_zero", -1.0, -0.5), ("k_norm", 8.0, 14.0),
+                         ("v_scale", 0.5, 1.0), ("v_zero", -2.0, -1.5)):
+        cache.field(name).uniform_(lo, hi, generator=g)
+    cache.struct.n_packed = P
+    ws = L.alloc_workspace(L.decode_workspace_bytes(B, Hkv, Hq, P, S))
+    for call, seed in enumerate((931, 932)):
+        qr = _qrot(L, B, Hq, seed)
+        want = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+        L.decode_attention(cache, qr, Hq, TAU, want, ws, num_splits=S)
+        got = torch.full((B, Hq, 128), float("nan"), device="cuda")
+        st = L.library().oscar_decode_attention_static_ws(
+            ctypes.byref(cache.struct), ctypes.c_void_p(qr.data_ptr()), Hq, TAU,
+            ctypes.c_void_p(got.data_ptr()), 0,
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == 0, st
+        torch.cuda.synchronize()
+        assert L.device_status() == 0
+        assert torch.isfinite(want).all()
+        assert torch.equal(got, want), f"call {call}: static entry did not use {S} splits"
+    del cache
+    torch.cuda.empty_cache()
