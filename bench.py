@@ -458,25 +458,35 @@ ABLATION_VARIANTS = (("oscar", 0, 2), ("no_rotate (scaling only)", 1, 2),
 
 def ablation_report(L, W, dev):
     """Accuracy of the method and its ablations against unquantised bf16
-    attention on needle inputs (a few keys per row point at the row's queries,
-    so attention concentrates and the reference output is far from zero).
-    GPU: every row of the workload, against the bf16 split-K kernel on the
-    same raw keys and values.  Oracle: row (0, 0), its own quantised attention
-    against its own exact bf16 attention.  Information only, not a gate."""
+    attention, on inputs whose attention is concentrated so that the
+    reference output is far from zero: tiny_1k and qwen3_8b_32k with needle
+    keys (a few keys per row point at the row's queries with graded score
+    margins), omni_tni_64k as it is (its x30 tokens and x10 segments already
+    draw most of the attention).  GPU: every row of the workload, against the
+    bf16 split-K kernel on the same raw keys and values.  Oracle, row (0, 0):
+    its own quantised attention against its own exact bf16 attention, and the
+    same with quantised keys but exact values (the part rotation and scaling
+    act on).  Information only, not a gate."""
     import torch
     from oracle import oscar_oracle as O
     tau = 1.0 / math.sqrt(128)
-    rep = {"inputs": f"each workload's keys with {W.N_NEEDLES} needle keys per (sequence, KV "
-                     f"head) row: typical key norm, pointing along the mean of the row's "
-                     f"query group (tilted by a seeded tenth), at seeded positions in the "
-                     f"packed prefix; values unchanged; decode step 0",
+    rep = {"inputs": {"tiny_1k": "needles", "qwen3_8b_32k": "needles",
+                      "omni_tni_64k": "the workload's own keys (no needles)"},
+           "needles": f"{W.N_NEEDLES} keys per (sequence, KV head) row at seeded positions in "
+                      f"the packed prefix, along the mean of the row's query group (tilted by a "
+                      f"seeded tenth), scoring ln(context) + {list(W.NEEDLE_MARGINS)} nats; "
+                      f"values unchanged; decode step 0",
            "reference": "bf16 attention over the same raw keys and values",
-           "metric": "relative L2 error of the whole output; per-vector median in 'median'",
+           "metric": "relative L2 error of the whole output ('rel_l2'); median over the "
+                     "(sequence, query head) vectors ('median'); oracle 'keys_only': "
+                     "quantised keys with exact values",
            "workloads": {}}
     for name in ABLATION_WORKLOADS:
         wl = W.WORKLOADS[name]
+        needles = name != "omni_tni_64k"
         K, V = W.draw_kv_cuda(wl, 0, wl.T0, device=dev)
-        W.plant_needles_cuda(wl, K)
+        if needles:
+            W.plant_needles_cuda(wl, K)
         q = W.draw_q_cuda(wl, 0, device=dev)
         ref = torch.empty((wl.B, wl.Hq, 128), dtype=torch.float32, device=dev)
         wsr = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, wl.T0, 512),
@@ -509,17 +519,24 @@ def ablation_report(L, W, dev):
         del K, V, wsr
         torch.cuda.empty_cache()
         # the oracle on row (0, 0), per-head norm variants
-        kb = W.plant_needles(wl, wl.k_bits([0], [0], 0, wl.T0)[0, 0], 0, 0)
+        kb = wl.k_bits([0], [0], 0, wl.T0)[0, 0]
+        if needles:
+            kb = W.plant_needles(wl, kb, 0, 0)
         vb = wl.v_bits([0], [0], 0, wl.T0)[0, 0]
         qb = wl.q_bits([0], range(wl.g), 0)[0]
         oref = O.bf16_attention(qb, kb, vb, tau)
+        vexact = O.bf16_to_f64(vb)
         orc = {}
         for vname, fl, bits in ABLATION_VARIANTS:
             if fl & O.NORM_ALL_HEADS:
                 continue                         # spans every head of the token: GPU only
             hc = O.build_head_cache(kb, vb, wl.n_packed, fl, bits=bits)
-            o = hc.decode(O.rotate_q(qb, fl), tau)
-            orc[vname] = float(np.linalg.norm(o - oref) / np.linalg.norm(oref))
+            qrot = O.rotate_q(qb, fl)
+            o = hc.decode(qrot, tau)
+            keys, _ = hc.keys_values()
+            ok = O.attention(np.atleast_2d(qrot), keys, vexact, tau)
+            orc[vname] = {"rel_l2": float(np.linalg.norm(o - oref) / np.linalg.norm(oref)),
+                          "keys_only": float(np.linalg.norm(ok - oref) / np.linalg.norm(oref))}
         rep["workloads"][name] = {"gpu": gpu, "oracle_row_0_0": orc}
     return rep
 

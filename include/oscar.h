@@ -277,18 +277,19 @@ oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const osca
  *  num_splits packed-token splits per (b,h); 0 = choose for this device
  *             (oscar_decode_num_splits); one more split handles the residual.
  *  workspace  device scratch of at least oscar_decode_workspace_bytes(B, Hkv,
- *             Hq, n_packed, splits) bytes (16-byte aligned), caller-owned.  It
- *             holds the split-K partial records, B*Hq*(splits+1) records of
- *             528 bytes, then one 32-bit arrival counter per (b, h) row,
- *             B*Hkv*4 bytes rounded up to 16.  The row's last CTA to finish
- *             combines the row's partials (no second kernel is launched) and
- *             sets its counter back to zero.  So the counter area must be
- *             zero before a workspace's first use (cudaMemset it once after
- *             allocating); every call leaves it zero.  A CTA that finds its
- *             row's counter already at or above the row's split count
- *             records an error in the device status word
- *             (oscar_device_status).  Calls that use one workspace must not
- *             overlap on the GPU.
+ *             Hq, n_packed, splits) bytes (16-byte aligned), caller-owned.
+ *             Layout: a header of OSCAR_DECODE_WS_HEADER_BYTES (one 32-bit
+ *             arrival counter for each of up to 65536 (b, h) rows), then the
+ *             split-K partial records, B*Hq*(splits+1) records of 528 bytes.
+ *             The row's last CTA to finish combines the row's partials (no
+ *             second kernel is launched) and sets its counter back to zero.
+ *             So the header must be zero before a workspace's first use
+ *             (cudaMemset it once after allocating); every call leaves it
+ *             zero, whatever its shape or split count, and the rest needs no
+ *             initialisation.  A counter found non-zero is reported in the
+ *             device status word (oscar_device_status) and that row's output
+ *             is not written.  B*Hkv must not exceed 65536.  Calls that use
+ *             one workspace must not overlap on the GPU.
  */
 oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, int Hq,
                                     float softmax_scale, float* out, int num_splits,
@@ -300,8 +301,9 @@ int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed);
 
 /* Workspace bytes needed by oscar_decode_attention / oscar_paged_decode_attention
  * (and enough for oscar_bf16_decode_attention) for `num_splits` token splits
- * (0 = the automatic count for n_packed tokens): B*Hq*(splits+1)*528 bytes of
- * partial records plus B*Hkv*4 bytes of row counters, rounded up to 16. */
+ * (0 = the automatic count for n_packed tokens): the counter header plus
+ * B*Hq*(splits+1)*528 bytes of partial records. */
+#define OSCAR_DECODE_WS_HEADER_BYTES (65536u * 4u)
 size_t oscar_decode_workspace_bytes(int B, int Hkv, int Hq, int n_packed, int num_splits);
 
 /*
@@ -339,15 +341,15 @@ oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* 
  *    explicit count that does not fit, or a batch whose single split does
  *    not fit, returns OSCAR_ERR_WORKSPACE and launches nothing.  For
  *    example a batch-48, 32-query-head, 8-KV-head layer at the 12 splits
- *    the planner gives a 128K context needs 48*32*13*528 + 48*8*4 bytes,
- *    about 10.5 MB.
+ *    the planner gives a 128K context needs 256 KiB + 48*32*13*528 bytes,
+ *    about 10.8 MB.
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress); make it before any stream
  *    capture.  A failed lookup returns OSCAR_ERR_CUDA.
  *  - Every call shares the one array and it keeps the last call's contents;
  *    calls whose kernels overlap on the GPU (e.g. on two streams) race on it.
- *    The row counters must be zero when a call starts: the array starts
- *    zeroed when the library loads and every call leaves them zero.
+ *    Its counter header starts zeroed when the library loads and every call
+ *    leaves it zero; each call writes every partial record it reads.
  */
 oscar_status oscar_decode_attention_static_ws(const oscar_cache* c, const float* q_rot, int Hq,
                                               float softmax_scale, float* out, int num_splits,

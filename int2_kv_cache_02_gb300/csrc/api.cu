@@ -137,6 +137,7 @@ oscar_status flush_residual(oscar_cache* c, cudaStream_t s) {
 namespace oscar {
 // Internal accessors for other translation units of the library.
 oscar_status validate_cache(const oscar_cache* c) { return check_cache(c); }
+
 unsigned* device_status_word() { return status_ptr(); }
 void count_launches(int n) { g_launches += (unsigned long long)n; }
 }  // namespace oscar
@@ -275,6 +276,7 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
       !std::isfinite(softmax_scale))
     return OSCAR_ERR_INVALID_ARG;
   if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
+  if ((long long)c->B * c->Hkv > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
   if (!al16(q_rot) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
   int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, c->n_packed);
   if (!workspace || ws_bytes < decode_ws_bytes(c->B, c->Hkv, Hq, S + 1))
@@ -286,8 +288,8 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   a.v_res = c->v_res;
   a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
   a.q_rot = q_rot;
-  a.ws = static_cast<float*>(workspace);
-  a.row_count = decode_row_counters(a.ws, c->B, Hq, S + 1);
+  a.ws = decode_partials(workspace);
+  a.row_count = decode_row_counters(workspace);
   a.out = out;
   a.status = status_ptr();
   a.B = c->B;
@@ -399,6 +401,7 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
       max_packed / kG > c->max_blocks)
     return OSCAR_ERR_INVALID_ARG;
   if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
+  if ((long long)c->B * c->Hkv > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
   if (!al16(q_rot) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
   int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, max_packed);
   if (!workspace || ws_bytes < decode_ws_bytes(c->B, c->Hkv, Hq, S + 1))
@@ -410,8 +413,8 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
   a.v_res = c->v_res;
   a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
   a.q_rot = q_rot;
-  a.ws = static_cast<float*>(workspace);
-  a.row_count = decode_row_counters(a.ws, c->B, Hq, S + 1);
+  a.ws = decode_partials(workspace);
+  a.row_count = decode_row_counters(workspace);
   a.out = out;
   a.status = status_ptr();
   if (!a.status) return OSCAR_ERR_CUDA;

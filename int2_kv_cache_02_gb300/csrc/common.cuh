@@ -46,7 +46,7 @@ enum : unsigned {
   kDevErrWaitTimeout = 1u,   // an mbarrier wait hit its iteration limit
   kDevErrDrainTimeout = 2u,  // copies still in flight after the drain limit
   kDevErrBadPaged = 4u,      // a page id or a per-sequence length out of range
-  kDevErrWorkspace = 8u,     // a decode workspace's arrival counter was not zero
+  kDevErrArrival = 8u,       // a decode row's arrival counter was not zero at the start
 };
 
 // Iteration limits of the bounded spin-waits.  One try_wait may itself

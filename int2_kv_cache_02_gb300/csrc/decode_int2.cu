@@ -1051,8 +1051,12 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
 // the row's last CTA, after every other CTA's records are visible.  Warp w
 // takes head w (and w + 4 for groups of 8); for groups smaller than 4 the
 // warps of a head split its partials and add their sums in shared memory.
-// Lane l holds channels 4 l .. 4 l + 3.  The records were written by other
-// CTAs during this launch, so they are read past L1 (ld.global.cg).
+// Each lane first takes the weight of one partial, then the warp walks the
+// partials with the weights broadcast by shuffles, so the loads of
+// successive partials do not wait on one another; lane l holds channels
+// 4 l .. 4 l + 3, summed in four interleaved fp32 chains.  The records were
+// written by other CTAs during this launch, so they are read past L1
+// (ld.global.cg).
 template <int GQ>
 __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, NW>& E,
                                             long long qrow0, int parts) {
@@ -1068,30 +1072,39 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
     for (int s = lane; s < parts; s += 32) M = fmaxf(M, __ldcg(r0 + (long long)s * kRecFloats));
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-    // four interleaved sums (partials of rank s mod 4), added pairwise at the
-    // end: short fp32 accumulation chains, as a four-warp split would give
-    float Lp[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float L = 0.0f;
     float4 op[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) op[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-      for (int s0 = pg; s0 < parts; s0 += 4 * PG) {
+      const int np = (parts - pg + PG - 1) / PG;   // this warp's partials pg + PG i
+      for (int i0 = 0; i0 < np; i0 += 32) {
+        float w = 0.0f;
+        if (i0 + lane < np) {
+          const float* r = r0 + (long long)(pg + PG * (i0 + lane)) * kRecFloats;
+          const float ms = __ldcg(r);
+          w = ms == -INFINITY ? 0.0f : fast_exp2(ms - M);
+          L = fmaf(w, __ldcg(r + 1), L);
+        }
+        const int cnt = min(32, np - i0);
+#pragma unroll 2
+        for (int q0 = 0; q0 < cnt; q0 += 4) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int s = s0 + k * PG;
-          if (s < parts) {
-            const float* r = r0 + (long long)s * kRecFloats;
-            const float ms = __ldcg(r);
-            const float al = ms == -INFINITY ? 0.0f : fast_exp2(ms - M);
-            Lp[k] = fmaf(al, __ldcg(r + 1), Lp[k]);
-            const float4 x = __ldcg(reinterpret_cast<const float4*>(r + 4) + lane);
-            op[k].x = fmaf(al, x.x, op[k].x); op[k].y = fmaf(al, x.y, op[k].y);
-            op[k].z = fmaf(al, x.z, op[k].z); op[k].w = fmaf(al, x.w, op[k].w);
+          for (int k = 0; k < 4; ++k) {
+            const int q = q0 + k;
+            const float wq = __shfl_sync(0xffffffffu, w, q & 31);
+            if (q < cnt) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(
+                  r0 + (long long)(pg + PG * (i0 + q)) * kRecFloats + 4) + lane);
+              op[k].x = fmaf(wq, x.x, op[k].x); op[k].y = fmaf(wq, x.y, op[k].y);
+              op[k].z = fmaf(wq, x.z, op[k].z); op[k].w = fmaf(wq, x.w, op[k].w);
+            }
           }
         }
       }
     }
-    const float L = (Lp[0] + Lp[1]) + (Lp[2] + Lp[3]);
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) L += __shfl_xor_sync(0xffffffffu, L, m);
     const float4 o = make_float4((op[0].x + op[1].x) + (op[2].x + op[3].x),
                                  (op[0].y + op[1].y) + (op[2].y + op[3].y),
                                  (op[0].z + op[1].z) + (op[2].z + op[3].z),
@@ -1148,21 +1161,27 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
   const int parts = a.num_splits + 1;
   cta_merge_write<GQ, NW>(E, a.ws + (qrow0 * parts + split) * kRecFloats,
                           (long long)parts * kRecFloats);
-  // Arrival: this CTA's records are made visible device-wide first; the
-  // CTA that brings the row's count to `parts` combines the row and leaves
-  // the counter at zero for the next call on this workspace.
+  // Arrival: after the CTA barrier, one thread makes the CTA's records
+  // visible device-wide (fence) and counts the CTA in on the row's counter.
+  // The CTA that brings the count to `parts` combines the row, after a fence
+  // that orders its reads after the other CTAs' records, and sets the
+  // counter back to zero for the next call on this workspace.  A count
+  // already at or above `parts` means the counters were not zero when the
+  // call began: reported, and the row is left uncombined.
   __shared__ int last_cta;
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     const unsigned prev = atomicAdd(a.row_count + row, 1u);
-    if (prev >= (unsigned)parts) record_error(a.status, kDevErrWorkspace);
+    if (prev >= (unsigned)parts) record_error(a.status, kDevErrArrival);
     last_cta = prev == (unsigned)(parts - 1);
-    if (last_cta) a.row_count[row] = 0u;
+    if (last_cta) {
+      a.row_count[row] = 0u;
+      __threadfence();
+    }
   }
   __syncthreads();
   if (!last_cta) return;
-  __threadfence();
   row_combine<GQ>(a, E, qrow0, parts);
 }
 

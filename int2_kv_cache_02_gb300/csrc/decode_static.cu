@@ -16,11 +16,11 @@
 // with cudaGetSymbolAddress, once per device, on the first call made while
 // that device is current; make that first call before any stream capture.
 // All calls share the one array: calls whose kernels overlap on the GPU (two
-// streams, say) race on it and give wrong results.  The array holds the
-// partial records, which every call writes before it reads them, and after
-// them the rows' arrival counters, which must be zero when a call starts:
-// static device memory starts zeroed, and every call leaves the counters at
-// zero again.  Otherwise the array keeps whatever the last call left there.
+// streams, say) race on it and give wrong results.  The array is laid out as
+// a decode workspace: a header of per-row arrival counters, which must be
+// zero when a call starts (static device memory starts zeroed and every call
+// leaves them zero), then the partial records, which every call writes
+// before it reads them.  Otherwise it keeps whatever the last call left.
 #include <cmath>
 #include <mutex>
 
@@ -67,6 +67,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
     return OSCAR_ERR_INVALID_ARG;
   const int g = (Hq % c->Hkv == 0) ? Hq / c->Hkv : 0;
   if (!(g == 1 || g == 2 || g == 4 || g == 8)) return OSCAR_ERR_UNSUPPORTED;
+  if ((long long)c->B * c->Hkv > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
   if (!aligned16(q_rot) || !aligned16(out)) return OSCAR_ERR_ALIGNMENT;
 
   // The partial records and counters must fit in the static array.  An
@@ -75,9 +76,8 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   int S = num_splits;
   if (S == 0) {
     S = oscar_decode_num_splits(c->B, c->Hkv, Hq, c->n_packed);
-    const size_t cnt = decode_ws_bytes(c->B, c->Hkv, Hq, 0);
     const size_t per_part = (size_t)c->B * (size_t)Hq * kRecFloats * sizeof(float);
-    const long long parts = cnt < kScratchBytes ? (long long)((kScratchBytes - cnt) / per_part) : 0;
+    const long long parts = (long long)((kScratchBytes - kDecodeWsHeader) / per_part);
     if (S + 1 > parts) S = (int)(parts - 1);
     if (S < 1) return OSCAR_ERR_WORKSPACE;
   }
@@ -92,8 +92,8 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   a.v_res = c->v_res;
   a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
   a.q_rot = q_rot;
-  a.ws = ws;
-  a.row_count = decode_row_counters(ws, c->B, Hq, S + 1);
+  a.ws = decode_partials(ws);
+  a.row_count = decode_row_counters(ws);
   a.out = out;
   a.status = device_status_word();
   a.B = c->B;

@@ -92,15 +92,19 @@ struct DecodeArgs {
 // Floats per split-K partial record: m, l, 2 pad, o[128].
 constexpr int kRecFloats = 132;
 
-// Decode workspace: the partial records [B*Hq][parts][kRecFloats], then the
-// rows' arrival counters [B*Hkv] (u32), rounded up to 16 bytes.
-inline size_t decode_ws_bytes(long long B, long long Hkv, long long Hq, long long parts) {
-  const size_t rec = (size_t)(B * Hq * parts) * kRecFloats * sizeof(float);
-  const size_t cnt = ((size_t)(B * Hkv) * sizeof(unsigned) + 15) / 16 * 16;
-  return rec + cnt;
+// Decode workspace: a header of kMaxDecodeRows arrival counters (u32, one per
+// (b, h) row, zero between calls), then the partial records
+// [B*Hq][parts][kRecFloats].  The header has the same size and place for
+// every shape and split count, so no call's partials overlap any call's
+// counters.
+constexpr long long kMaxDecodeRows = 1 << 16;
+constexpr size_t kDecodeWsHeader = kMaxDecodeRows * sizeof(unsigned);
+inline size_t decode_ws_bytes(long long B, long long /*Hkv*/, long long Hq, long long parts) {
+  return kDecodeWsHeader + (size_t)(B * Hq * parts) * kRecFloats * sizeof(float);
 }
-inline unsigned* decode_row_counters(float* ws, long long B, long long Hq, long long parts) {
-  return reinterpret_cast<unsigned*>(ws + (size_t)(B * Hq * parts) * kRecFloats);
+inline unsigned* decode_row_counters(void* ws) { return static_cast<unsigned*>(ws); }
+inline float* decode_partials(void* ws) {
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kDecodeWsHeader);
 }
 
 // Fused INT2 decode attention with the split-K combine in its last CTA per

@@ -347,8 +347,8 @@ def decode_workspace_bytes(B: int, Hkv: int, Hq: int, n_packed: int, num_splits:
 
 
 def alloc_workspace(nbytes: int, device=None) -> torch.Tensor:
-    """A decode workspace of at least nbytes, zeroed: its trailing row
-    counters must start at zero, and every decode call leaves them zero."""
+    """A decode workspace of at least nbytes, zeroed: its header of row
+    counters must start at zero, and every decode call leaves it zero."""
     return torch.zeros(max(16, (nbytes + 15) // 16 * 16) // 4, dtype=torch.float32,
                        device=device if device is not None else "cuda")
 

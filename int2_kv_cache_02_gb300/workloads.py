@@ -210,22 +210,24 @@ def _offset(t, t0: int):
 # ---------------------------------------------------------------------------
 
 N_NEEDLES = 4
+NEEDLE_MARGINS = (6.0, 5.0, 4.0, 3.0)   # nats above ln(context) for needles 0..3
 
 
 def needle_keys(wl: Workload, b: int, h: int, step: int = 0):
     """(positions int [N_NEEDLES], raw bf16 key bits uint16 [N_NEEDLES][128])
-    for row (b, h): each needle key has the norm a typical key of the
-    workload has (the outlier channels included) and points along the mean of
-    the row's query group at decode step `step`, tilted by a seeded random
-    tenth, so that every query head of the group scores it far above the rest
-    of the context.  Positions are seeded, distinct, inside the packed
-    prefix and clear of its first block (the attention sinks)."""
+    for row (b, h).  Needle i points along the mean of the row's query group
+    at decode step `step`, tilted by a seeded random tenth, with the length
+    that gives it a softmax score of ln(context) + NEEDLE_MARGINS[i] (nats,
+    averaged over the group's heads): the needles take nearly all of the
+    attention, in graded shares, and the rest of the context keeps a little.
+    Positions are seeded, distinct, inside the packed prefix and clear of its
+    first block (the attention sinks)."""
     g = wl.g
     q = synth.bf16_bits_to_f32(wl.q_bits([b], range(h * g, (h + 1) * g), step)[0])
-    u = q.astype(np.float64).sum(axis=0)
+    q = q.astype(np.float64)
+    u = q.sum(axis=0)
     u /= np.linalg.norm(u)
-    cf = wl.chan_factor().astype(np.float64)
-    norm = float(np.sqrt(np.sum(cf * cf)))          # expected norm of a drawn key
+    tau = 1.0 / np.sqrt(128.0)
     seed = wl.seed_base + 7
     row = b * wl.Hkv + h
     lo, hi = 32, max(33, wl.n_packed - 32)
@@ -242,8 +244,11 @@ def needle_keys(wl: Workload, b: int, h: int, step: int = 0):
                                                 (row + 1) * N_NEEDLES * 128))
     tilt = tilt.astype(np.float64).reshape(N_NEEDLES, 128)
     tilt /= np.linalg.norm(tilt, axis=1, keepdims=True)
-    keys = u[None, :] + 0.1 * tilt
-    keys *= norm / np.linalg.norm(keys, axis=1, keepdims=True)
+    dirs = u[None, :] + 0.1 * tilt
+    dirs /= np.linalg.norm(dirs, axis=1, keepdims=True)
+    target = np.log(wl.T0) + np.asarray(NEEDLE_MARGINS[:N_NEEDLES])
+    per_unit = tau * (dirs @ q.T).mean(axis=1)            # score of a unit-length needle
+    keys = dirs * (target / per_unit)[:, None]
     return np.array(pos), synth.f32_to_bf16_bits(keys.astype(np.float32))
 
 

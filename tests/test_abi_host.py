@@ -224,10 +224,9 @@ def test_decode_validation():
     assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, P(FAKE), 4, None,
                                     1 << 30, None) == 5
     need = L.oscar_decode_workspace_bytes(2, 2, 8, 0, 4)
-    # partial records of 132 floats, then one u32 counter per (b, h) row,
-    # rounded up to 16 bytes
-    assert need == 2 * 8 * 5 * 132 * 4 + 16
-    assert L.oscar_decode_workspace_bytes(3, 3, 6, 0, 1) == 3 * 6 * 2 * 528 + 48
+    # a fixed header of 65536 u32 row counters, then partial records of 132 floats
+    assert need == 65536 * 4 + 2 * 8 * 5 * 132 * 4
+    assert L.oscar_decode_workspace_bytes(3, 3, 6, 0, 1) == 65536 * 4 + 3 * 6 * 2 * 528
     assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, P(FAKE), 4, P(FAKE),
                                     need - 1, None) == 5
     assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, float("nan"), P(FAKE), 4,

@@ -277,6 +277,48 @@ def test_split_invariance(L):
         assert d <= 1e-6
 
 
+def test_workspace_reuse_across_split_counts_and_shapes(L):
+    """The decode workspace is a header of row counters (zero between calls)
+    then the split-K partials.  A zeroed workspace whose partial area holds
+    arbitrary bytes, and one that calls with other split counts and another
+    cache shape used in between, give the same output bit for bit as a fresh
+    one; a non-zero counter is reported in the status word."""
+    B, Hkv, Hq, T, P = 1, 2, 8, 4096 + 128, 4096
+    heads, _, _ = _oracle_heads(330, B, Hkv, T, P)
+    cache = upload_oracle_cache(L.KVCache(B, Hkv, 4096), heads)
+    qbits = synth.gen_bf16(331, Hq, range(B), range(Hq), 0, 1)[:, :, 0]
+    qr = torch.from_numpy(O.rotate_q(qbits).astype(np.float32)).cuda()
+    nbytes = L.decode_workspace_bytes(B, Hkv, Hq, P, 64)
+    header = 65536                                    # u32 counters, in 4-byte words
+    want = {}
+    for S in (13, 2, 7):
+        ws = L.alloc_workspace(nbytes)
+        want[S] = torch.empty((B, Hq, 128), device="cuda")
+        L.decode_attention(cache, qr, Hq, TAU, want[S], ws, num_splits=S)
+    shared = L.alloc_workspace(nbytes)
+    g = torch.Generator(device="cuda").manual_seed(332)
+    part = shared.view(torch.int32)[header:]
+    part.copy_(torch.randint(-2**31, 2**31 - 1, (part.numel(),), dtype=torch.int32,
+                             device="cuda", generator=g))
+    other = upload_oracle_cache(L.KVCache(2, 1, 4096), {(b, 0): heads[(0, b)] for b in range(2)})
+    other_out = torch.empty((2, 4, 128), device="cuda")
+    for S in (13, 2, 7, 13, 2, 7):
+        got = torch.full((B, Hq, 128), float("nan"), device="cuda")
+        L.decode_attention(cache, qr, Hq, TAU, got, shared, num_splits=S)
+        _sync_ok(L)
+        assert torch.equal(got, want[S]), f"splits {S}"
+        # another shape between the calls, on the same workspace
+        L.decode_attention(other, qr.reshape(2, 4, 128).contiguous(), 4, TAU, other_out,
+                           shared, num_splits=5)
+        _sync_ok(L)
+    assert torch.count_nonzero(shared.view(torch.int32)[:header]) == 0
+    # a counter left non-zero (a workspace never zeroed) is reported
+    shared.view(torch.int32)[1] = 3
+    L.decode_attention(cache, qr, Hq, TAU, got, shared, num_splits=2)
+    torch.cuda.synchronize()
+    assert L.device_status() != 0
+
+
 @pytest.mark.parametrize("T,P", [(96, 0), (1024, 1024), (32, 32), (33, 32), (1, 0)])
 def test_decode_edge_sizes(L, T, P):
     B, Hkv, Hq = 1, 2, 8
