@@ -59,11 +59,16 @@ oscar_status check_cache(const oscar_cache* c) {
 // instruction issue, so an SM's time is the work of the CTAs it runs:
 // ceil(CTAs / SMs) x (blocks per split + a fixed start/merge overhead worth
 // kSplitOverheadBlocks blocks), slowed in proportion when it holds fewer
-// than kSaturatingWarps warps at once (too few to hide latency).  Each warp
-// keeps at least kMinBlocksPerWarp blocks: shorter ranges measured slower.
-// Ties keep fewer splits.  (Measured on GB300: the planned counts are the
-// best of a sweep, or within 0.5 % of it, for batch 48 x 128K, batch 8 x
-// 32K, batch 1 x 128K and the g = 8 64K workload.)
+// than kSaturatingWarps warps at once (too few to hide latency).  When the
+// packed CTAs fit in one wave of resident CTAs and only the residual CTAs (a
+// few microseconds each) would spill into a second, those are left out of
+// the count: they finish early and hold no slot for long.  Each warp keeps
+// at least kMinBlocksPerWarp blocks:
+// shorter ranges measured slower.  Ties keep fewer splits.  (Measured on
+// GB300 in a sweep of split counts: batch 1 x 128K plans 37, the best;
+// batch 8 x 32K plans 6, the best; the g = 8 batch-16 64K workload plans 7,
+// the best (152 us against 170 at 6); batch 48 x 128K plans 12, within
+// 1.4 % of the best, 13.)
 constexpr long long kSplitOverheadBlocks = 32;
 constexpr long long kMinBlocksPerWarp = 16;
 constexpr int kSaturatingWarps = 8;
@@ -80,7 +85,9 @@ int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits)
   int best = 1;
   double best_cost = 1e300;
   for (int s = 1; s <= hi; ++s) {
-    const long long per_sm = (rows * (s + 1) + sms - 1) / sms;   // CTAs of the busiest SM
+    const long long packed = rows * s, slots = (long long)sms * cps;
+    const long long ctas = packed <= slots && rows * (s + 1) > slots ? packed : rows * (s + 1);
+    const long long per_sm = (ctas + sms - 1) / sms;              // CTAs of the busiest SM
     const long long resident = std::min(per_sm, cps);
     const double rate = std::min(1.0, (double)(resident * kWarpsPerCta) / kSaturatingWarps);
     const long long per = (nblk + s - 1) / s;
