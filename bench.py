@@ -661,63 +661,65 @@ def run_ours(args, world, rank, local):
     achieved = (bytes_sum / max(K_, 1)) / (dec_avg_ms * 1e-3) / 1e9
 
     # ---- end to end through the C ABI with host buffers ----
-    pin = lambda t: t.cpu().pin_memory()
-    base = i_step + 2
-    Qh, Kh, Vh = pin(Q[base:base + E_]), pin(Kn[base:base + E_]), pin(Vn[base:base + E_])
-    outh = torch.empty((E_,) + tuple(out.shape), dtype=torch.float32).pin_memory()
-    # Copies run on their own stream, double-buffered, so that step i + 1's
-    # inputs travel and step i - 1's output returns while step i computes;
-    # every copy is still inside the timed region.
-    cs = torch.cuda.Stream(device=dev)
-    qd = [torch.empty_like(Q[0]) for _ in range(2)]
-    kd = [torch.empty_like(Kn[0]) for _ in range(2)]
-    vd = [torch.empty_like(Vn[0]) for _ in range(2)]
-    outs = [torch.empty_like(out) for _ in range(2)]
-    filled = [torch.cuda.Event() for _ in range(2)]   # inputs of buffer b on the device
-    used = [torch.cuda.Event() for _ in range(2)]     # step done with buffer b
-    back = [torch.cuda.Event() for _ in range(2)]     # output of buffer b on the host
-    for i in range(2):  # untimed: touch the copy paths
-        qd[i].copy_(Qh[i], non_blocking=True)
-    torch.cuda.synchronize()
+    e2e_us, h2d, d2h = None, 0, 0
+    if E_ > 0:
+        pin = lambda t: t.cpu().pin_memory()
+        base = i_step + 2
+        Qh, Kh, Vh = pin(Q[base:base + E_]), pin(Kn[base:base + E_]), pin(Vn[base:base + E_])
+        outh = torch.empty((E_,) + tuple(out.shape), dtype=torch.float32).pin_memory()
+        # Copies run on their own stream, double-buffered, so that step i + 1's
+        # inputs travel and step i - 1's output returns while step i computes;
+        # every copy is still inside the timed region.
+        cs = torch.cuda.Stream(device=dev)
+        qd = [torch.empty_like(Q[0]) for _ in range(2)]
+        kd = [torch.empty_like(Kn[0]) for _ in range(2)]
+        vd = [torch.empty_like(Vn[0]) for _ in range(2)]
+        outs = [torch.empty_like(out) for _ in range(2)]
+        filled = [torch.cuda.Event() for _ in range(2)]   # inputs of buffer b on the device
+        used = [torch.cuda.Event() for _ in range(2)]     # step done with buffer b
+        back = [torch.cuda.Event() for _ in range(2)]     # output of buffer b on the host
+        for i in range(2):  # untimed: touch the copy paths
+            qd[i].copy_(Qh[i], non_blocking=True)
+        torch.cuda.synchronize()
 
-    def h2d_(i):
-        b = i % 2
-        with torch.cuda.stream(cs):
+        def h2d_(i):
+            b = i % 2
+            with torch.cuda.stream(cs):
+                if i >= 2:
+                    cs.wait_event(used[b])
+                qd[b].copy_(Qh[i], non_blocking=True)
+                kd[b].copy_(Kh[i], non_blocking=True)
+                vd[b].copy_(Vh[i], non_blocking=True)
+                filled[b].record(cs)
+
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        cs.wait_event(e0)
+        h2d_(0)
+        for i in range(E_):
+            b = i % 2
+            if i + 1 < E_:
+                h2d_(i + 1)
+            stream.wait_event(filled[b])
             if i >= 2:
+                stream.wait_event(back[b])
+            L.rotate_q(qd[b], qr)
+            L.append_kv(cache, kd[b], vd[b], n_tok=1)
+            L.decode_attention(cache, qr, wl.Hq, tau, outs[b], ws, num_splits=S)
+            used[b].record(stream)
+            with torch.cuda.stream(cs):
                 cs.wait_event(used[b])
-            qd[b].copy_(Qh[i], non_blocking=True)
-            kd[b].copy_(Kh[i], non_blocking=True)
-            vd[b].copy_(Vh[i], non_blocking=True)
-            filled[b].record(cs)
-
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    cs.wait_event(e0)
-    h2d_(0)
-    for i in range(E_):
-        b = i % 2
-        if i + 1 < E_:
-            h2d_(i + 1)
-        stream.wait_event(filled[b])
-        if i >= 2:
-            stream.wait_event(back[b])
-        L.rotate_q(qd[b], qr)
-        L.append_kv(cache, kd[b], vd[b], n_tok=1)
-        L.decode_attention(cache, qr, wl.Hq, tau, outs[b], ws, num_splits=S)
-        used[b].record(stream)
-        with torch.cuda.stream(cs):
-            cs.wait_event(used[b])
-            outh[i].copy_(outs[b], non_blocking=True)
-            back[b].record(cs)
-    stream.wait_event(back[(E_ - 1) % 2])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_us = e0.elapsed_time(e1) / max(E_, 1) * 1e3
-    h2d = (Qh[0].numel() * Qh.element_size() + Kh[0].numel() * Kh.element_size()
-           + Vh[0].numel() * Vh.element_size())
-    d2h = out.numel() * out.element_size()
-    e2e_us = max_over_ranks(e2e_us, world, dev)
+                outh[i].copy_(outs[b], non_blocking=True)
+                back[b].record(cs)
+        stream.wait_event(back[(E_ - 1) % 2])
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_us = e0.elapsed_time(e1) / max(E_, 1) * 1e3
+        h2d = (Qh[0].numel() * Qh.element_size() + Kh[0].numel() * Kh.element_size()
+               + Vh[0].numel() * Vh.element_size())
+        d2h = out.numel() * out.element_size()
+        e2e_us = max_over_ranks(e2e_us, world, dev)
 
     # ---- bf16 comparison kernel, same shape (context T0) ----
     bf16 = None
@@ -904,8 +906,8 @@ def run_ours(args, world, rank, local):
                                "the last CTA of each row)",
                      "decode_us": dec_avg_ms * 1e3,
                      "algorithmic_bytes_per_launch": bytes_sum / max(K_, 1)},
-        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": E_},
+        "e2e": ({"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h, "steps": E_} if E_ > 0 else None),
         "gpu_launches": int(launches),
         "clocks": _clock_summary(clock_rows, wall0, wall1),
         "context_tokens": {"start": ctx0[0] + ctx0[1],
