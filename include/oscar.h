@@ -380,9 +380,10 @@ oscar_status oscar_device_status(void* stream);
  * oscar_paged_decode_attention: oscar_decode_attention over every
  * sequence's own n_packed[b] + n_res[b] tokens.  max_packed (host) bounds
  * the n_packed[b] and plans the splits (num_splits 0: planned from it):
- * split i covers blocks [i*c, (i+1)*c) of every sequence, c = ceil(max_packed
- * / 32 / splits), so a shorter sequence fills fewer splits (the last split
- * also takes any blocks beyond max_packed).  The workspace is
+ * with c = ceil(max_packed / 32 / splits) blocks, sequence b's n_packed[b]/32
+ * blocks are cut into ceil(n/c) splits of equal length (at most `splits`; a
+ * sequence longer than max_packed spreads over all of them), so a shorter
+ * sequence fills fewer splits.  The workspace is
  * oscar_decode_workspace_bytes(B, Hkv, Hq, max_packed, splits).
  * A sequence with no tokens gives zeros.
  *

@@ -339,13 +339,16 @@ __device__ __forceinline__ WarpRing<PAGED, BITS> make_ring(const DecodeArgs& a, 
   const int nblk = row_blocks<PAGED>(a, b);
   int b0, b1;
   if constexpr (PAGED) {
-    // Equal chunks sized by the batch's longest sequence (n_packed carries
-    // that bound): a short sequence fills fewer splits, each as long as a
-    // long sequence's, so the per-CTA setup is paid per chunk of work and
-    // not per split.  The last split takes whatever is left.
-    const int per = (a.n_packed / kG + a.num_splits - 1) / a.num_splits;
-    b0 = (int)min((long long)nblk, (long long)split * per);
-    b1 = split == a.num_splits - 1 ? nblk : min(nblk, b0 + per);
+    // Chunks of at most c = ceil(longest / splits) blocks, the longest
+    // sequence's split size (n_packed carries that bound): sequence b takes
+    // ceil(n_b / c) splits of equal length, so a short sequence fills fewer
+    // splits, each nearly as long as a long sequence's (no half-empty last
+    // chunk), and the per-CTA setup is paid per chunk of work.  A sequence
+    // longer than the bound spreads over all the splits.
+    const int c = max(1, (a.n_packed / kG + a.num_splits - 1) / a.num_splits);
+    const int sb = max(1, min(a.num_splits, (nblk + c - 1) / c));
+    b0 = split < sb ? (int)((long long)nblk * split / sb) : nblk;
+    b1 = split < sb ? (int)((long long)nblk * (split + 1) / sb) : nblk;
   } else {
     b0 = (int)((long long)nblk * split / a.num_splits);
     b1 = (int)((long long)nblk * (split + 1) / a.num_splits);
