@@ -63,16 +63,26 @@ oscar_status check_cache(const oscar_cache* c) {
 // packed CTAs fit in one wave of resident CTAs and only the residual CTAs (a
 // few microseconds each) would spill into a second, those are left out of
 // the count: they finish early and hold no slot for long.  Each warp keeps
-// at least kMinBlocksPerWarp blocks:
-// shorter ranges measured slower.  Ties keep fewer splits.  (Measured on
-// GB300 in a sweep of split counts: batch 1 x 128K plans 37, the best;
-// batch 8 x 32K plans 6, the best; the g = 8 batch-16 64K workload plans 7,
-// the best (152 us against 170 at 6); batch 48 x 128K plans 12, within
-// 1.4 % of the best, 13.)
+// at least kMinBlocksPerWarp blocks: shorter ranges measured slower.  Ties
+// keep fewer splits.
+//
+// On grids of more than two waves, an even count that wins is then compared
+// with its odd neighbours, and the cheaper of them is taken if its modelled
+// cost is within kEvenSplitPenalty of the winner's: there, on GB300, every
+// even count from 10 to 28 measured 1.2-1.5 % slower than its odd
+// neighbours (batch 48 x 128K: 12 splits 982 us, 11 and 13 splits 969-972
+// us), with the residual CTA placed anywhere in the row, with a padded grid
+// and without the combine; the cause is not known.
+//
+// Measured on GB300 in sweeps of split counts: batch 1 x 128K plans 37, the
+// best; batch 8 x 32K plans 9, the best (59 us against 63.5 at 6); the g = 8
+// batch-16 64K workload plans 7, the best (152 us against 170 at 6); batch
+// 48 x 128K plans 13, the best.
 constexpr long long kSplitOverheadBlocks = 32;
 constexpr long long kMinBlocksPerWarp = 16;
 constexpr int kSaturatingWarps = 8;
 constexpr int kWarpsPerCta = 4;
+constexpr double kEvenSplitPenalty = 1.02;
 
 int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits) {
   int dev = 0, sms = 0;
@@ -80,22 +90,41 @@ int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits)
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
   if (nblk <= 0 || rows <= 0) return 1;
   const long long cps = ctas_per_sm > 0 ? ctas_per_sm : 1;
+  const long long slots = (long long)sms * cps;
   const long long most = std::max<long long>(1, nblk / (kWarpsPerCta * kMinBlocksPerWarp));
   const int hi = (int)std::min<long long>(max_splits, most);
-  int best = 1;
-  double best_cost = 1e300;
-  for (int s = 1; s <= hi; ++s) {
-    const long long packed = rows * s, slots = (long long)sms * cps;
-    const long long ctas = packed <= slots && rows * (s + 1) > slots ? packed : rows * (s + 1);
-    const long long per_sm = (ctas + sms - 1) / sms;              // CTAs of the busiest SM
+  auto ctas_of = [&](int s) {
+    const long long packed = rows * s;
+    return packed <= slots && rows * (s + 1) > slots ? packed : rows * (s + 1);
+  };
+  auto cost_of = [&](int s) {
+    const long long per_sm = (ctas_of(s) + sms - 1) / sms;   // CTAs of the busiest SM
     const long long resident = std::min(per_sm, cps);
     const double rate = std::min(1.0, (double)(resident * kWarpsPerCta) / kSaturatingWarps);
     const long long per = (nblk + s - 1) / s;
-    const double cost = (double)per_sm * (double)(per + kSplitOverheadBlocks) / rate;
+    return (double)per_sm * (double)(per + kSplitOverheadBlocks) / rate;
+  };
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= hi; ++s) {
+    const double cost = cost_of(s);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
     }
+  }
+  if (best % 2 == 0 && ctas_of(best) > 2 * slots) {
+    int odd = 0;
+    double odd_cost = 1e300;
+    for (int s : {best - 1, best + 1}) {
+      if (s < 1 || s > hi) continue;
+      const double c = cost_of(s);
+      if (c < odd_cost - 1e-9) {
+        odd_cost = c;
+        odd = s;
+      }
+    }
+    if (odd > 0 && odd_cost <= best_cost * kEvenSplitPenalty) best = odd;
   }
   return best;
 }

@@ -59,12 +59,18 @@ def test_static_scratch_matches_workspace_entry_on_two_calls(L, splits):
         want = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
         L.decode_attention(cache, qr, Hq, TAU, want, ws, num_splits=splits)
         got = torch.full((B, Hq, 128), float("nan"), device="cuda")
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         st = L.library().oscar_decode_attention_static_ws(
             ctypes.byref(cache.struct), ctypes.c_void_p(qr.data_ptr()), Hq, TAU,
             ctypes.c_void_p(got.data_ptr()), splits,
             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert st == 0, st
         torch.cuda.synchronize()
+        if call > 0:
+            # Once the library's module is loaded (first call), a call takes
+            # no device memory: the driver's free memory is unchanged.
+            assert torch.cuda.mem_get_info()[0] == free0
         assert L.device_status() == 0
         assert_attention_close(got.cpu().numpy(), want.cpu().numpy(), f"call {call}")
 
