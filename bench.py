@@ -44,7 +44,8 @@ METRIC = "INT2 decode-attn µs/step & HBM GB/s (% of GB300 peak) at 128K ctx, ba
 UNIT = "us/step"
 HERE = os.path.dirname(os.path.abspath(__file__))
 TRAFFIC_FILE = os.path.join(HERE, "profiles", "decode_int2_batch48_128k_traffic.json")
-L2_FLUSH_BYTES = 512 << 20          # written before every flushed rep (L2 is 129 MB)
+L2_BYTES = 129 * 10**6             # GB300 L2
+L2_FLUSH_BYTES = 512 << 20          # written before every flushed rep (about 4x L2)
 CONFIG_WORKLOADS = ("tiny_1k", "qwen3_8b_32k", "long_stream_128k", "omni_tni_64k")
 ABLATION_WORKLOADS = ("tiny_1k", "qwen3_8b_32k", "omni_tni_64k")
 
@@ -861,7 +862,11 @@ def run_ours(args, world, rank, local):
         int4 = {"packed_tokens": c4.n_packed, "residual_tokens": c4.n_res, "num_splits": S4,
                 "decode_us": i_ms * 1e3, "GB/s": i_gbs, "frac": i_gbs / peak,
                 "note": "INT4 option (16 levels, 150 B per packed token-head) over the same "
-                        "prompt; L2 not flushed between the 20 reps (7.5 GB of records)"}
+                        "prompt; %.2f GB of records, %s" % (
+                            rows * c4.n_packed * 150 / 1e9,
+                            "L2 not flushed between the 20 reps (records larger than L2)"
+                            if rows * c4.n_packed * 150 > 2 * L2_BYTES else
+                            "L2 not flushed between the 20 reps (records fit in L2: a warm figure)")}
         del c4, ws4
         torch.cuda.empty_cache()
     # the headline workload's big buffers are not needed any more
