@@ -231,8 +231,9 @@ __device__ __forceinline__ float warp_allsum(float v) {
 }
 
 // One warp's contiguous range of a row's 32-token blocks, streamed through
-// the warp's own NSTAGE-deep ring: lane 0 copies block i's record into slot
-// i % NSTAGE with one 1-D bulk copy completing on that slot's mbarrier.
+// the warp's own NSTAGE-deep ring: one elected lane copies block i's record
+// into slot i % NSTAGE with one 1-D bulk copy completing on that slot's
+// mbarrier.
 template <bool PAGED, int BITS>
 struct WarpRing {
   static constexpr int NSTAGE = Layout<BITS>::NSTAGE;
@@ -242,43 +243,43 @@ struct WarpRing {
   const uint8_t* src;   // record of the range's first block (contiguous cache)
   int n;                // blocks in the range
   int lane;
-  // paged cache: the range's block-table entries, the page pool, the row's
-  // KV head, and where to report a page id out of range
+  // paged cache: the range's block-table entries and the row's KV head (the
+  // pool, its size and the status word are read from the launch arguments
+  // where they are used, so they hold no registers through the loop)
   const int32_t* tab;
-  const uint8_t* pages;   // record of head h in page 0
-  long long page_bytes;   // Hkv records
-  int n_pages;
-  unsigned* status;
+  int h;
 
-  // Record of block i of the range.  A page id out of range is reported and
-  // replaced by page 0 (the result is void; nothing outside the pool is read).
-  __device__ __forceinline__ const uint8_t* record(int i) const {
+  // Page id of block i of the range (paged cache; 0 past the range's end or
+  // for a contiguous cache).  Loaded when block i - NSTAGE is taken up, so
+  // the load's latency is hidden by that block's work.
+  __device__ __forceinline__ int page_of(int i) const {
+    if constexpr (PAGED) return i < n ? __ldg(tab + i) : 0;
+    else return 0;
+  }
+  // Record of block i of the range, `page` its page id (paged cache; the
+  // range's ids were checked against the pool when the ring was made).
+  __device__ __forceinline__ const uint8_t* record(int i, int page, const DecodeArgs& a) const {
     if constexpr (PAGED) {
-      int page = __ldg(tab + i);
-      if ((unsigned)page >= (unsigned)n_pages) {
-        record_error(status, kDevErrBadPaged);
-        page = 0;
-      }
-      return pages + page * page_bytes;
+      return a.packed + ((long long)page * a.Hkv + h) * RB;
     } else {
       return src + (long long)i * RB;
     }
   }
 
-  __device__ __forceinline__ void start() const {
+  __device__ __forceinline__ void start(const DecodeArgs& a) const {
     if (lane == 0) {
 #pragma unroll
       for (int s = 0; s < NSTAGE; ++s) mbar_init(&bars[s], 1);
       mbar_fence_init();
     }
     __syncwarp();
-    for (int i = 0; i < NSTAGE && i < n; ++i) issue(i);
+    for (int i = 0; i < NSTAGE && i < n; ++i) issue(i, page_of(i), a);
   }
-  __device__ __forceinline__ void issue(int i) const {
+  __device__ __forceinline__ void issue(int i, int page, const DecodeArgs& a) const {
     // Every lane forms the (warp-uniform) addresses; one lane chosen by
     // elect.sync arms the slot's mbarrier and issues the copy, so no branch
     // on the lane index is needed.
-    const uint8_t* rec = record(i);
+    const uint8_t* rec = record(i, page, a);
     const unsigned bar = smem_u32(&bars[i % NSTAGE]);
     const unsigned dst = smem_u32(ring + (i % NSTAGE) * RB);
     asm volatile(
@@ -296,10 +297,11 @@ struct WarpRing {
   __device__ __forceinline__ const uint8_t* slot(int i) const {
     return ring + (i % NSTAGE) * RB;
   }
-  // After consuming block i: refill its slot with block i + NSTAGE.
-  __device__ __forceinline__ void release(int i) const {
+  // After consuming block i: refill its slot with block i + NSTAGE, whose
+  // page id (paged cache) was loaded by page_of when block i was taken up.
+  __device__ __forceinline__ void release(int i, int page, const DecodeArgs& a) const {
     __syncwarp();
-    if (i + NSTAGE < n) issue(i + NSTAGE);
+    if (i + NSTAGE < n) issue(i + NSTAGE, page, a);
   }
   // The wait for block `it` gave up: record it and wait (bounded) for the
   // copies still in flight, blocks it .. min(it + NSTAGE, n) - 1, so that no
@@ -331,6 +333,18 @@ __device__ __forceinline__ int row_blocks(const DecodeArgs& a, int b) {
   }
 }
 
+// Number of packed splits that sequence b of a paged batch fills: chunks of
+// at most c = ceil(longest / splits) blocks, the longest sequence's split
+// size (n_packed carries that bound), so sequence b takes ceil(n_b / c)
+// splits of equal length; a short sequence fills fewer splits, each nearly
+// as long as a long sequence's (no half-empty last chunk), and the per-CTA
+// setup is paid per chunk of work.  A sequence longer than the bound spreads
+// over all the splits.
+__device__ __forceinline__ int paged_splits_used(const DecodeArgs& a, int nblk) {
+  const int c = max(1, (a.n_packed / kG + a.num_splits - 1) / a.num_splits);
+  return max(1, min(a.num_splits, (nblk + c - 1) / c));
+}
+
 template <bool PAGED, int BITS>
 __device__ __forceinline__ WarpRing<PAGED, BITS> make_ring(const DecodeArgs& a, uint8_t* smem,
                                                            int b, int h, int split) {
@@ -339,14 +353,7 @@ __device__ __forceinline__ WarpRing<PAGED, BITS> make_ring(const DecodeArgs& a, 
   const int nblk = row_blocks<PAGED>(a, b);
   int b0, b1;
   if constexpr (PAGED) {
-    // Chunks of at most c = ceil(longest / splits) blocks, the longest
-    // sequence's split size (n_packed carries that bound): sequence b takes
-    // ceil(n_b / c) splits of equal length, so a short sequence fills fewer
-    // splits, each nearly as long as a long sequence's (no half-empty last
-    // chunk), and the per-CTA setup is paid per chunk of work.  A sequence
-    // longer than the bound spreads over all the splits.
-    const int c = max(1, (a.n_packed / kG + a.num_splits - 1) / a.num_splits);
-    const int sb = max(1, min(a.num_splits, (nblk + c - 1) / c));
+    const int sb = paged_splits_used(a, nblk);
     b0 = split < sb ? (int)((long long)nblk * split / sb) : nblk;
     b1 = split < sb ? (int)((long long)nblk * (split + 1) / sb) : nblk;
   } else {
@@ -363,10 +370,17 @@ __device__ __forceinline__ WarpRing<PAGED, BITS> make_ring(const DecodeArgs& a, 
   r.n = wb1 - wb0;
   r.lane = threadIdx.x & 31;
   r.tab = PAGED ? a.block_table + (long long)b * a.max_blocks + wb0 : nullptr;
-  r.pages = a.packed + (long long)h * RB;
-  r.page_bytes = (long long)a.Hkv * RB;
-  r.n_pages = a.n_pages;
-  r.status = a.status;
+  r.h = h;
+  if constexpr (PAGED) {
+    // Every page id of the range is checked once, before any copy: one out
+    // of range is reported and the warp reads nothing (its result is void).
+    bool bad = false;
+    for (int j = r.lane; j < r.n; j += 32) bad |= (unsigned)__ldg(r.tab + j) >= (unsigned)a.n_pages;
+    if (__any_sync(0xffffffffu, bad)) {
+      if (r.lane == 0) record_error(a.status, kDevErrBadPaged);
+      r.n = 0;
+    }
+  }
   return r;
 }
 
@@ -423,7 +437,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   const int hs = tig % GQ;          // head of this lane's scores and outputs
   using RL = typename Layout<BITS>::RL;
   constexpr int LW = BITS == 2 ? 2 : 4;   // key words per token and lane
-  R.start();   // the first copies travel while the query is prepared
+  R.start(a);   // the first copies travel while the query is prepared
 
   // This lane's column of q' for channels 32 tig + 4 k8 + {0,1} (pair 0) and
   // + {2,3} (pair 1): qz = the column's own limb (the Z operand), qhm = the hi
@@ -462,6 +476,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   int it = 0;
   for (; it < R.n; ++it) {
     if (!R.wait(it)) break;
+    const int page_next = R.page_of(it + Ring::NSTAGE);
     const uint8_t* st = R.slot(it);
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + RL::KC);
     const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + RL::VC);
@@ -663,7 +678,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
         }
       }
     }
-    R.release(it);
+    R.release(it, page_next, a);
   }
   if (it < R.n) {
     R.fail(it, a.status);
@@ -706,7 +721,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
   const int head = gid;
   using RL = typename Layout<BITS>::RL;
   constexpr int LW = BITS == 2 ? 2 : 4;   // key words per token and lane
-  R.start();   // the first copies travel while the query is prepared
+  R.start(a);   // the first copies travel while the query is prepared
 
   // Query fragments of this thread's head, channels c0 = 32*tig + 4*k8 ..+3,
   // as {hi(c0,c0+1), lo(c0,c0+1), hi(c0+2,c0+3), lo(c0+2,c0+3)} (the MMA A
@@ -745,6 +760,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
   int it = 0;
   for (; it < R.n; ++it) {
     if (!R.wait(it)) break;
+    const int page_next = R.page_of(it + Ring::NSTAGE);
     const uint8_t* st = R.slot(it);
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + RL::KC);
     const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + RL::VC);
@@ -956,7 +972,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
         }
       }
     }
-    R.release(it);
+    R.release(it, page_next, a);
   }
   if (it < R.n) {
     R.fail(it, a.status);
@@ -1054,12 +1070,15 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
 // the row's last CTA, after every other CTA's records are visible.  Warp w
 // takes head w (and w + 4 for groups of 8); for groups smaller than 4 the
 // warps of a head split its partials and add their sums in shared memory.
-// Each lane first takes the weight of one partial, then the warp walks the
-// partials with the weights broadcast by shuffles, so the loads of
-// successive partials do not wait on one another; lane l holds channels
-// 4 l .. 4 l + 3, summed in four interleaved fp32 chains.  The records were
-// written by other CTAs during this launch, so they are read past L1
-// (ld.global.cg).
+// The records were written by other CTAs during this launch, so they are
+// read past L1 (ld.global.cg), and the combine sits on the row's critical
+// path, so its loads are issued in few round trips: each lane takes the
+// (m, l) pair of up to two partials in one pass, and the outputs are read
+// kCombineBatch partials at a time, all loads of a batch in flight before
+// the first is used.  Lane l holds channels 4 l .. 4 l + 3, summed in four
+// interleaved fp32 chains (partial q into chain q mod 4, in order of q).
+constexpr int kCombineBatch = 16;
+
 template <int GQ>
 __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, NW>& E,
                                             long long qrow0, int parts) {
@@ -1071,8 +1090,21 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
     const int j = GQ >= NW ? warp + NW * hh : warp % GQ;
     const int pg = GQ >= NW ? 0 : warp / GQ;
     const float* r0 = a.ws + (qrow0 + j) * parts * kRecFloats;
-    float M = -INFINITY;
-    for (int s = lane; s < parts; s += 32) M = fmaxf(M, __ldcg(r0 + (long long)s * kRecFloats));
+    const int np = (parts - pg + PG - 1) / PG;   // this warp's partials pg + PG i
+    auto rec = [&](int i) { return r0 + (long long)(pg + PG * i) * kRecFloats; };
+    // (m, l) of partials lane and lane + 32 in registers; the rest (more than
+    // 64 partials per warp) are read again where needed.
+    float2 ml0 = make_float2(-INFINITY, 0.0f), ml1 = make_float2(-INFINITY, 0.0f);
+    if (lane < np) ml0 = __ldcg(reinterpret_cast<const float2*>(rec(lane)));
+    if (lane + 32 < np) ml1 = __ldcg(reinterpret_cast<const float2*>(rec(lane + 32)));
+    // m* over all the row's partials (for groups smaller than 4 the warps of
+    // a head add their sums unscaled, so they share one m*)
+    float M = fmaxf(ml0.x, ml1.x);
+    if constexpr (PG == 1) {
+      for (int i = lane + 64; i < np; i += 32) M = fmaxf(M, __ldcg(rec(i)));
+    } else {
+      for (int s = lane; s < parts; s += 32) M = fmaxf(M, __ldcg(r0 + (long long)s * kRecFloats));
+    }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
     float L = 0.0f;
@@ -1080,28 +1112,40 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
 #pragma unroll
     for (int k = 0; k < 4; ++k) op[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-      const int np = (parts - pg + PG - 1) / PG;   // this warp's partials pg + PG i
-      for (int i0 = 0; i0 < np; i0 += 32) {
-        float w = 0.0f;
-        if (i0 + lane < np) {
-          const float* r = r0 + (long long)(pg + PG * (i0 + lane)) * kRecFloats;
-          const float ms = __ldcg(r);
-          w = ms == -INFINITY ? 0.0f : fast_exp2(ms - M);
-          L = fmaf(w, __ldcg(r + 1), L);
-        }
-        const int cnt = min(32, np - i0);
-#pragma unroll 2
-        for (int q0 = 0; q0 < cnt; q0 += 4) {
+      const float w0 = ml0.x == -INFINITY ? 0.0f : fast_exp2(ml0.x - M);
+      const float w1 = ml1.x == -INFINITY ? 0.0f : fast_exp2(ml1.x - M);
+      L = fmaf(w0, ml0.y, L);
+      L = fmaf(w1, ml1.y, L);
+      const int nfast = min(np, 64);
+      for (int i0 = 0; i0 < nfast; i0 += kCombineBatch) {
+        float4 x[kCombineBatch];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int q = q0 + k;
-            const float wq = __shfl_sync(0xffffffffu, w, q & 31);
-            if (q < cnt) {
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(
-                  r0 + (long long)(pg + PG * (i0 + q)) * kRecFloats + 4) + lane);
-              op[k].x = fmaf(wq, x.x, op[k].x); op[k].y = fmaf(wq, x.y, op[k].y);
-              op[k].z = fmaf(wq, x.z, op[k].z); op[k].w = fmaf(wq, x.w, op[k].w);
-            }
+        for (int k = 0; k < kCombineBatch; ++k)
+          if (i0 + k < nfast)
+            x[k] = __ldcg(reinterpret_cast<const float4*>(rec(i0 + k) + 4) + lane);
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) {
+          const int q = i0 + k;
+          const float wq = __shfl_sync(0xffffffffu, q < 32 ? w0 : w1, q & 31);
+          if (q < nfast) {
+            op[k & 3].x = fmaf(wq, x[k].x, op[k & 3].x); op[k & 3].y = fmaf(wq, x[k].y, op[k & 3].y);
+            op[k & 3].z = fmaf(wq, x[k].z, op[k & 3].z); op[k & 3].w = fmaf(wq, x[k].w, op[k & 3].w);
+          }
+        }
+      }
+      // partials beyond 64 of this warp (up to 129 splits): four at a time,
+      // each lane adding the l of its own partials
+      for (int i0 = 64; i0 < np; i0 += 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int i = i0 + k;
+          if (i < np) {
+            const float ms = __ldcg(rec(i));
+            const float wq = ms == -INFINITY ? 0.0f : fast_exp2(ms - M);
+            if (((i - lane) & 31) == 0) L = fmaf(wq, __ldcg(rec(i) + 1), L);
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(rec(i) + 4) + lane);
+            op[k].x = fmaf(wq, x.x, op[k].x); op[k].y = fmaf(wq, x.y, op[k].y);
+            op[k].z = fmaf(wq, x.z, op[k].z); op[k].w = fmaf(wq, x.w, op[k].w);
           }
         }
       }
@@ -1151,11 +1195,17 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
   const long long qrow0 = (long long)b * a.Hq + (long long)h * GQ;  // first query head
 
   if (split < a.num_splits) {
-    const WarpRing<PAGED, BITS> R = make_ring<PAGED, BITS>(a, smem, b, h, split);
-    if constexpr (GQ <= 4) {
-      packed_cols<GQ, BSCALE, BITS>(a, R, E, qrow0);
+    if (PAGED && split >= paged_splits_used(a, row_blocks<PAGED>(a, b))) {
+      // A split that a short sequence of a paged batch does not fill skips
+      // the query and writes an empty partial, which the combine ignores.
+      if (threadIdx.x < NW * GQ) E.m[threadIdx.x / GQ][threadIdx.x % GQ] = -INFINITY;
     } else {
-      packed_rows<GQ, BSCALE, BITS>(a, R, E, qrow0);
+      const WarpRing<PAGED, BITS> R = make_ring<PAGED, BITS>(a, smem, b, h, split);
+      if constexpr (GQ <= 4) {
+        packed_cols<GQ, BSCALE, BITS>(a, R, E, qrow0);
+      } else {
+        packed_rows<GQ, BSCALE, BITS>(a, R, E, qrow0);
+      }
     }
   } else {
     residual_split<GQ, PAGED>(a, E, row, qrow0, b);
