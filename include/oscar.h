@@ -299,6 +299,12 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
  * device (>= 1).  Returns 1 when no device can be queried. */
 int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed);
 
+/* The planner behind oscar_decode_num_splits, for a device of `sms`
+ * multiprocessors that hold `ctas_per_sm` decode CTAs each: rows = B*Hkv,
+ * n_blocks = n_packed / 32.  Host arithmetic only (no CUDA call); returns a
+ * count in [1, 512], 1 for non-positive arguments. */
+int oscar_decode_plan_splits(long long rows, long long n_blocks, int ctas_per_sm, int sms);
+
 /* Workspace bytes needed by oscar_decode_attention / oscar_paged_decode_attention
  * (and enough for oscar_bf16_decode_attention) for `num_splits` token splits
  * (0 = the automatic count for n_packed tokens): the counter header plus

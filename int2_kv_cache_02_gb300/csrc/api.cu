@@ -63,7 +63,10 @@ oscar_status check_cache(const oscar_cache* c) {
 // packed CTAs fit in one wave of resident CTAs and only the residual CTAs (a
 // few microseconds each) would spill into a second, those are left out of
 // the count: they finish early and hold no slot for long.  Each warp keeps
-// at least kMinBlocksPerWarp blocks: shorter ranges measured slower.  Ties
+// at least kMinBlocksPerWarp blocks: shorter ranges measured slower.  A grid
+// that fits in one wave may go down to kMinBlocksPerWarpOneWave blocks per
+// warp: there the row is latency-bound and more warps on it shorten it (a
+// 1K-token single-head row: 12.3 us at 3 splits against 14.4 us at 1).  Ties
 // keep fewer splits.
 //
 // On grids of more than two waves, an even count that wins is then compared
@@ -80,19 +83,19 @@ oscar_status check_cache(const oscar_cache* c) {
 // 48 x 128K plans 13, the best.
 constexpr long long kSplitOverheadBlocks = 32;
 constexpr long long kMinBlocksPerWarp = 16;
+constexpr long long kMinBlocksPerWarpOneWave = 2;
 constexpr int kSaturatingWarps = 8;
 constexpr int kWarpsPerCta = 4;
 constexpr double kEvenSplitPenalty = 1.02;
 
-int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits) {
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
-  if (nblk <= 0 || rows <= 0) return 1;
+int plan_splits_for(long long rows, long long nblk, int ctas_per_sm, int sms, int max_splits) {
+  if (nblk <= 0 || rows <= 0 || sms <= 0 || max_splits < 1) return 1;
   const long long cps = ctas_per_sm > 0 ? ctas_per_sm : 1;
   const long long slots = (long long)sms * cps;
   const long long most = std::max<long long>(1, nblk / (kWarpsPerCta * kMinBlocksPerWarp));
+  const long long most1 = std::max<long long>(1, nblk / (kWarpsPerCta * kMinBlocksPerWarpOneWave));
   const int hi = (int)std::min<long long>(max_splits, most);
+  const int hi1 = (int)std::min<long long>(max_splits, most1);
   auto ctas_of = [&](int s) {
     const long long packed = rows * s;
     return packed <= slots && rows * (s + 1) > slots ? packed : rows * (s + 1);
@@ -106,7 +109,8 @@ int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits)
   };
   int best = 1;
   double best_cost = 1e300;
-  for (int s = 1; s <= hi; ++s) {
+  for (int s = 1; s <= hi1; ++s) {
+    if (s > hi && rows * (s + 1) > slots) break;   // beyond one wave: longer ranges only
     const double cost = cost_of(s);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
@@ -127,6 +131,13 @@ int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits)
     if (odd > 0 && odd_cost <= best_cost * kEvenSplitPenalty) best = odd;
   }
   return best;
+}
+
+int plan_splits(long long rows, long long nblk, int ctas_per_sm, int max_splits) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return plan_splits_for(rows, nblk, ctas_per_sm, sms, max_splits);
 }
 
 // Split count of the bf16 comparison kernel (no residual split): waves of
@@ -295,6 +306,10 @@ oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const osca
 int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed) {
   if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || !group_ok(Hq / Hkv)) return 1;
   return plan_splits((long long)B * Hkv, n_packed / kG, decode_int2_ctas_per_sm(Hq / Hkv), 512);
+}
+
+int oscar_decode_plan_splits(long long rows, long long n_blocks, int ctas_per_sm, int sms) {
+  return plan_splits_for(rows, n_blocks, ctas_per_sm, sms, 512);
 }
 
 size_t oscar_decode_workspace_bytes(int B, int Hkv, int Hq, int n_packed, int num_splits) {

@@ -1133,7 +1133,7 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
           }
         }
       }
-      // partials beyond 64 of this warp (up to 129 splits): four at a time,
+      // partials beyond 64 of this warp (more than 64 splits): four at a time,
       // each lane adding the l of its own partials
       for (int i0 = 64; i0 < np; i0 += 4) {
 #pragma unroll

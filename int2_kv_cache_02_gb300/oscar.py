@@ -89,6 +89,7 @@ def _load() -> ctypes.CDLL:
         "oscar_decode_attention_static_ws": (c_int, [P, c_void_p, c_int, c_float, c_void_p,
                                                      c_int, c_void_p]),
         "oscar_decode_num_splits": (c_int, [c_int, c_int, c_int, c_int]),
+        "oscar_decode_plan_splits": (c_int, [ctypes.c_longlong, ctypes.c_longlong, c_int, c_int]),
         "oscar_decode_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
         "oscar_bf16_decode_attention": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int,
                                                 c_int, c_int, c_int, c_float, c_void_p, c_int,
@@ -340,6 +341,10 @@ def append_kv(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, n_tok: i
 
 def decode_num_splits(B: int, Hkv: int, Hq: int, n_packed: int) -> int:
     return int(_lib.oscar_decode_num_splits(B, Hkv, Hq, n_packed))
+
+
+def decode_plan_splits(rows: int, n_blocks: int, ctas_per_sm: int, sms: int) -> int:
+    return int(_lib.oscar_decode_plan_splits(rows, n_blocks, ctas_per_sm, sms))
 
 
 def decode_workspace_bytes(B: int, Hkv: int, Hq: int, n_packed: int, num_splits: int = 0) -> int:
