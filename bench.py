@@ -380,7 +380,27 @@ def _median_timed(fn, reps, flushbuf=None):
     return ts[len(ts) // 2], ts
 
 
-def measure_config(L, W, name, dev, flushbuf, peak, reps=20):
+def _flush_loop_timed(fn, reps, flushbuf):
+    """Device time (us) of fn() with L2 flushed before it: reps of (flush,
+    fn) back to back between two CUDA events, less reps of the flush alone.
+    Event pairs around one short launch read in steps of about 1 us on this
+    GPU, so the loop gives the finer figure."""
+    import torch
+    a, b, c, d = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    a.record()
+    for _ in range(reps):
+        flushbuf.zero_()
+        fn()
+    b.record()
+    c.record()
+    for _ in range(reps):
+        flushbuf.zero_()
+    d.record()
+    torch.cuda.synchronize()
+    return (a.elapsed_time(b) - c.elapsed_time(d)) * 1e3 / reps
+
+
+def measure_config(L, W, name, dev, flushbuf, peak, reps=100):
     """One workload other than the headline one: the fused decode over its
     prompt (plus one appended token) with L2 flushed before every rep, and
     for the streaming workloads the whole decode step (rotate_q, append with
@@ -411,13 +431,18 @@ def measure_config(L, W, name, dev, flushbuf, peak, reps=20):
         dec = lambda: L.decode_attention(cache, qr, wl.Hq, tau, out, ws, num_splits=S)
         for _ in range(3):
             dec()
-        us, _ = _median_timed(dec, reps, flushbuf)
+        us = _flush_loop_timed(dec, reps, flushbuf)
+        us_ev, _ = _median_timed(dec, 20, flushbuf)
         nbytes = _algorithmic_bytes(wl, cache.n_packed, cache.n_res, S)
         gbs = nbytes / (us * 1e-6) / 1e9
         res.update({"num_splits": S, "packed_tokens": cache.n_packed,
                     "residual_tokens": cache.n_res, "decode_us": us,
+                    "decode_us_event_median": us_ev,
                     "algorithmic_bytes": nbytes, "GB/s": gbs, "frac": gbs / peak,
-                    "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB written) before each of {reps} reps"})
+                    "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB written) before each of {reps} "
+                          "back-to-back reps; decode_us = (flush + decode) loop less the "
+                          "flush-only loop, per rep; decode_us_event_median = median of 20 "
+                          "event pairs around single launches (coarser)"})
     if wl.steps > 1:
         # the workload's decode steps, one by one, from the next token on
         n_st = wl.steps - 1

@@ -396,12 +396,16 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
 // a power of two sigma chosen per head so that the fp16 parts stay in range.
 // qf holds channels 32*tig .. 32*tig+31 of the head; the lanes xor 1 and xor 2
 // hold the rest of it.  Returns sigma; qf is scaled in place.
-__device__ __forceinline__ float scale_query(float (&qf)[32], const float* qrow, int tig,
-                                            const DecodeArgs& a) {
+__device__ __forceinline__ void load_query(float4 (&qv)[8], const float* qrow, int tig) {
   const float4* qp = reinterpret_cast<const float4*>(qrow + 32 * tig);
 #pragma unroll
+  for (int i = 0; i < 8; ++i) qv[i] = qp[i];
+}
+__device__ __forceinline__ float scale_query(float (&qf)[32], const float4 (&qv)[8],
+                                            const DecodeArgs& a) {
+#pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float4 v = qp[i];
+    const float4 v = qv[i];
     qf[4 * i] = v.x * a.scale_log2; qf[4 * i + 1] = v.y * a.scale_log2;
     qf[4 * i + 2] = v.z * a.scale_log2; qf[4 * i + 3] = v.w * a.scale_log2;
   }
@@ -437,7 +441,17 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   const int hs = tig % GQ;          // head of this lane's scores and outputs
   using RL = typename Layout<BITS>::RL;
   constexpr int LW = BITS == 2 ? 2 : 4;   // key words per token and lane
-  R.start(a);   // the first copies travel while the query is prepared
+  // The query's loads go out first, then the ring's first copies, which
+  // travel while the query is prepared (INT4: the copies first, which keeps
+  // its instantiations free of spills).
+  float4 qv[8];
+  if constexpr (BITS == 2) {
+    load_query(qv, a.q_rot + (qrow0 + hq) * kD, tig);
+    R.start(a);
+  } else {
+    R.start(a);
+    load_query(qv, a.q_rot + (qrow0 + hq) * kD, tig);
+  }
 
   // This lane's column of q' for channels 32 tig + 4 k8 + {0,1} (pair 0) and
   // + {2,3} (pair 1): qz = the column's own limb (the Z operand), qhm = the hi
@@ -448,7 +462,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   float inv_sigma;
   {
     float qf[32];
-    const float sigma = scale_query(qf, a.q_rot + (qrow0 + hq) * kD, tig, a);
+    const float sigma = scale_query(qf, qv, a);
 #pragma unroll
     for (int k8 = 0; k8 < 8; ++k8)
 #pragma unroll
@@ -721,7 +735,17 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
   const int head = gid;
   using RL = typename Layout<BITS>::RL;
   constexpr int LW = BITS == 2 ? 2 : 4;   // key words per token and lane
-  R.start(a);   // the first copies travel while the query is prepared
+  // The query's loads go out first, then the ring's first copies, which
+  // travel while the query is prepared (INT4: the copies first, which keeps
+  // its instantiations free of spills).
+  float4 qv[8];
+  if constexpr (BITS == 2) {
+    load_query(qv, a.q_rot + (qrow0 + head) * kD, tig);
+    R.start(a);
+  } else {
+    R.start(a);
+    load_query(qv, a.q_rot + (qrow0 + head) * kD, tig);
+  }
 
   // Query fragments of this thread's head, channels c0 = 32*tig + 4*k8 ..+3,
   // as {hi(c0,c0+1), lo(c0,c0+1), hi(c0+2,c0+3), lo(c0+2,c0+3)} (the MMA A
@@ -731,7 +755,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
   float inv_sigma;
   {
     float qf[32];
-    const float sigma = scale_query(qf, a.q_rot + (qrow0 + head) * kD, tig, a);
+    const float sigma = scale_query(qf, qv, a);
     inv_sigma = ldexpf(1.0f, -ilogbf(sigma));
 #pragma unroll
     for (int k8 = 0; k8 < 8; ++k8) {

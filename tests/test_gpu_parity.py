@@ -268,6 +268,16 @@ def test_decode_on_oracle_cache_all_groups(L, g):
     _decode_vs_oracle(L, heads, B, g * Hkv, Hkv, 2112, 310 + g, splits=(1, 2, 7, 0))
 
 
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_decode_with_many_splits(L, g):
+    """More splits than blocks and more than 64 partials per combining warp:
+    splits of one block or none (empty partials), and the combine's path for
+    partials beyond the first 64 of a warp."""
+    B, Hkv, T, P = 1, 2, 4096 + 40, 4096
+    heads, _, _ = _oracle_heads(360 + g, B, Hkv, T, P)
+    _decode_vs_oracle(L, heads, B, g * Hkv, Hkv, 4096, 370 + g, splits=(100, 300))
+
+
 def test_split_invariance(L):
     B, Hkv, Hq, T, P = 1, 2, 8, 4096 + 128, 4096
     heads, _, _ = _oracle_heads(320, B, Hkv, T, P)
