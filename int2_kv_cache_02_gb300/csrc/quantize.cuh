@@ -82,7 +82,8 @@ __device__ __forceinline__ bool recip_ok(float rs) { return rs <= 3.0e38f; }
 // even, so then code >= j + 1 iff a / step >= h - u-/2; otherwise iff
 // a / step > h + u+/2.  The bound m step is exact in fp64 (m has at most 28
 // significant bits, step 24), and A_j is that product rounded up to fp32
-// (for the strict case, the next fp32 when the product is itself an fp32).
+// (for the strict case, the next fp32 when the product is itself an fp32);
+// the kernels form it in fp32 (code_threshold below).
 // fp32 spacing just above (below = false) or just below h = j + 1/2 < 16:
 // 2^(e - 23) with e = floor(log2 h), halved below h = 1/2 (a power of two).
 __host__ __device__ constexpr double fp32_spacing(int j, bool below) {
@@ -96,11 +97,33 @@ __host__ __device__ constexpr double threshold_factor(int j) {
   return ((j + 1) % 2 == 0) ? (j + 0.5) - 0.5 * fp32_spacing(j, true)
                             : (j + 0.5) + 0.5 * fp32_spacing(j, false);
 }
+// In fp32: m_j = h + d with h = j + 1/2 and d = m_j - h = +-2^-k, so
+// m_j step = fma(h, step, d step); d step is exact (a power-of-two scaling
+// of a normal number) and the fused multiply-add forms h step + d step
+// exactly before its one directed rounding, so __fmaf_ru gives the product
+// rounded up and __fmaf_rd rounded down.  A step below 2^-100 is first
+// scaled by 2^64 (exact), so that d step stays normal, and the two results
+// are scaled back with the same directed rounding (a second rounding in the
+// same direction onto a coarser grid changes nothing).  The product of a
+// non-finite step (never formed from finite bf16 data) takes the fp64 form.
 __device__ __forceinline__ float code_threshold(float step, int j) {
-  const double b = threshold_factor(j) * (double)step;   // exact
-  const float up = __double2float_ru(b);
+  if (!(step <= 3.4028234663852886e38f)) {
+    const double b = threshold_factor(j) * (double)step;
+    const float up = __double2float_ru(b);
+    if ((j + 1) % 2 == 0) return up;
+    return __double2float_rd(b) == up ? __uint_as_float(__float_as_uint(up) + 1u) : up;
+  }
+  const float h = (float)j + 0.5f;
+  const float d = (float)(threshold_factor(j) - ((double)j + 0.5));
+  const bool tiny = step < 0x1p-100f;
+  const float s = tiny ? step * 0x1p64f : step;
+  const float c = d * s;
+  float up = __fmaf_ru(h, s, c);
+  if (tiny) up = __fmul_ru(up, 0x1p-64f);
   if ((j + 1) % 2 == 0) return up;
-  return __double2float_rd(b) == up ? __uint_as_float(__float_as_uint(up) + 1u) : up;
+  float dn = __fmaf_rd(h, s, c);
+  if (tiny) dn = __fmul_rd(dn, 0x1p-64f);
+  return dn == up ? __uint_as_float(__float_as_uint(up) + 1u) : up;
 }
 // Number of thresholds at or below a: the code, as a float (three compares
 // that set 1.0 or 0.0, two adds).

@@ -36,6 +36,8 @@ def _factor(j):
 
 def _f32_up(x: Fraction) -> np.float32:
     f = np.float32(float(x))                 # nearest (x is exact in fp64 here)
+    if not np.isfinite(f):                   # beyond the largest fp32: rounds up to inf
+        return f
     if Fraction(float(f)) < x:
         f = np.nextafter(f, np.float32(np.inf))
     return f
@@ -44,7 +46,7 @@ def _f32_up(x: Fraction) -> np.float32:
 def _threshold(step: np.float32, j: int) -> np.float32:
     b = _factor(j) * Fraction(float(step))
     up = _f32_up(b)
-    if (j + 1) % 2 == 1 and Fraction(float(up)) == b:
+    if (j + 1) % 2 == 1 and np.isfinite(up) and Fraction(float(up)) == b:
         up = np.nextafter(up, np.float32(np.inf))
     return up
 
@@ -119,3 +121,53 @@ def test_threshold_count_equals_oracle_codes():
             a = (groups[g] - zero[g]).astype(np.float32)
             got = sum((a >= Aj).astype(np.int64) for Aj in A)
             np.testing.assert_array_equal(got, codes[g].astype(np.int64), err_msg=f"{axis} {g}")
+
+
+def _f32_down(x: Fraction) -> np.float32:
+    f = np.float32(float(x))
+    if not np.isfinite(f):                   # beyond the largest fp32: rounds down to it
+        return np.float32(np.finfo(np.float32).max)
+    if Fraction(float(f)) > x:
+        f = np.nextafter(f, np.float32(-np.inf))
+    return f
+
+
+def _threshold_fp32_form(step: np.float32, j: int) -> np.float32:
+    """The kernels' fp32 form of A_j, step by step: m_j = h + d, h = j + 1/2,
+    d = +-2^-k; c = fl(d * s) in fp32; the fused multiply-add h * s + c
+    rounded up (and down, for the strict case); steps below 2^-100 scaled
+    by 2^64 first and the results scaled back with the same rounding."""
+    h = np.float32(j + 0.5)
+    d = np.float32(float(_factor(j) - Fraction(2 * j + 1, 2)))
+    tiny = step < np.float32(2.0 ** -100)
+    s = np.float32(step * np.float32(2.0 ** 64)) if tiny else step
+    c = np.float32(d * s)                                # fp32 multiply
+    exact = Fraction(float(h)) * Fraction(float(s)) + Fraction(float(c))
+    up, dn = _f32_up(exact), _f32_down(exact)
+    if tiny:
+        up = _f32_up(Fraction(float(up)) * Fraction(1, 2 ** 64))
+        dn = _f32_down(Fraction(float(dn)) * Fraction(1, 2 ** 64))
+    if (j + 1) % 2 == 0:
+        return up
+    return np.nextafter(up, np.float32(np.inf)) if dn == up else up
+
+
+def test_fp32_form_of_the_thresholds_equals_the_rule():
+    """The fp32 fused multiply-add form the kernels use gives the same A_j as
+    the exact rule, for normal, tiny-normal, subnormal and huge steps and the
+    edge of the scaling (2^-100)."""
+    rng = np.random.default_rng(77)
+    bits = np.concatenate([
+        rng.integers(0x00000001, 0x00800000, 300),       # subnormal
+        rng.integers(0x00800000, 0x0d800000, 300),       # normal below 2^-100
+        rng.integers(0x0d000000, 0x0e800000, 300),       # around 2^-100
+        rng.integers(0x0e800000, 0x7f000000, 600),       # normal
+        rng.integers(0x7f000000, 0x7f800000, 100),       # huge (products may overflow)
+        np.array([1, 2, 3, 0x00800000, 0x0d800000, 0x0d7fffff, 0x3eaaaaab, 0x7f7fffff]),
+    ]).astype(np.uint32)
+    with np.errstate(over="ignore"):
+        for b in bits:
+            s = np.array([b], dtype=np.uint32).view(np.float32)[0]
+            for j in range(3):
+                want, got = _threshold(s, j), _threshold_fp32_form(s, j)
+                assert want.view(np.uint32) == got.view(np.uint32), (hex(int(b)), j, want, got)
