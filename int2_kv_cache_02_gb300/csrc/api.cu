@@ -79,7 +79,7 @@ oscar_status check_cache(const oscar_cache* c) {
 //
 // Measured on GB300 in sweeps of split counts: batch 1 x 128K plans 37, the
 // best; batch 8 x 32K plans 9, the best (59 us against 63.5 at 6); the g = 8
-// batch-16 64K workload plans 7, the best (152 us against 170 at 6); batch
+// batch-16 64K workload plans 9, the best (145 us against 160-180 at 6-12); batch
 // 48 x 128K plans 13, the best.
 constexpr long long kSplitOverheadBlocks = 32;
 constexpr long long kMinBlocksPerWarp = 16;

@@ -62,6 +62,13 @@ struct Layout {
 };
 
 constexpr float kLazyLog2 = 8.0f;         // lazy softmax rescale threshold (log2 units)
+constexpr int kQStage = 8 * 32 * 16;   // row layout: staged query fragments (bytes)
+// The kernel's dynamic shared memory (every extern declaration names the
+// same address).
+__device__ __forceinline__ uint8_t* dyn_smem() {
+  extern __shared__ __align__(128) uint8_t dyn_smem_base[];
+  return dyn_smem_base;
+}
 
 __device__ __forceinline__ uint32_t hfma2_u(uint32_t x, uint32_t s, uint32_t b) {
   return half2_as_u32(__hfma2(u32_as_half2(x), u32_as_half2(s), u32_as_half2(b)));
@@ -747,28 +754,33 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
     load_query(qv, a.q_rot + (qrow0 + head) * kD, tig);
   }
 
-  // Query fragments of this thread's head, channels c0 = 32*tig + 4*k8 ..+3,
-  // as {hi(c0,c0+1), lo(c0,c0+1), hi(c0+2,c0+3), lo(c0+2,c0+3)} (the MMA A
-  // layout of rows g and g+8).  The query carries softmax_scale * log2(e)
-  // and a power of two sigma that keeps the fp16 parts in range.
-  uint32_t aq[8][4];
+  // Query fragments of this thread's head, staged by warp 0 in shared memory
+  // after the ring's barriers (all warps of the CTA serve the same 8 heads);
+  // every k-step reads its quad back, which keeps the kernel at 128 registers
+  // and 4 CTAs per SM.
+  uint4* const qs = reinterpret_cast<uint4*>(dyn_smem() + Layout<BITS>::SMEM);
   float inv_sigma;
   {
     float qf[32];
     const float sigma = scale_query(qf, qv, a);
     inv_sigma = ldexpf(1.0f, -ilogbf(sigma));
+    if (warp == 0) {
 #pragma unroll
-    for (int k8 = 0; k8 < 8; ++k8) {
+      for (int k8 = 0; k8 < 8; ++k8) {
+        uint32_t f[4];
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float x0 = qf[4 * k8 + 2 * j], x1 = qf[4 * k8 + 2 * j + 1];
-        const __half2 hh = __floats2half2_rn(x0, x1);
-        const float2 hv = __half22float2(hh);
-        aq[k8][2 * j] = half2_as_u32(hh);
-        aq[k8][2 * j + 1] = half2_as_u32(__floats2half2_rn(x0 - hv.x, x1 - hv.y));
+        for (int j = 0; j < 2; ++j) {
+          const float x0 = qf[4 * k8 + 2 * j], x1 = qf[4 * k8 + 2 * j + 1];
+          const __half2 hh = __floats2half2_rn(x0, x1);
+          const float2 hv = __half22float2(hh);
+          f[2 * j] = half2_as_u32(hh);
+          f[2 * j + 1] = half2_as_u32(__floats2half2_rn(x0 - hv.x, x1 - hv.y));
+        }
+        qs[k8 * 32 + lane] = make_uint4(f[0], f[1], f[2], f[3]);
       }
     }
   }
+  __syncthreads();
   // the Q.K sums carry 2^-24 (subnormal key codes) and sigma
   const float qk_scale = 16777216.0f * inv_sigma;
 
@@ -796,14 +808,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
     const uint4 vs8 = *reinterpret_cast<const uint4*>(st + RL::VS + 16 * tig);
     const uint4 vz8 = *reinterpret_cast<const uint4*>(st + RL::VZ + 16 * tig);
 
-    // Z = q'.z of the block: rows g (hi) and g+8 (lo), every column alike.
     float dz[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint4 zv = kz4[i];
-      mma_16816_acc(dz, aq[2 * i], zv.x, zv.y);
-      mma_16816_acc(dz, aq[2 * i + 1], zv.z, zv.w);
-    }
 
     // Q.K^T, k-step outer: q~ fragment for k-step k8, then the 4 n-tiles.
     uint32_t kw[4][LW], kw10[4][LW];
@@ -834,9 +839,14 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint4 sv = ks4[i];
+      const uint4 zv = kz4[i];
 #pragma unroll
       for (int hk = 0; hk < 2; ++hk) {
         const int k8 = 2 * i + hk;
+        const uint4 q4 = qs[k8 * 32 + lane];
+        const uint32_t aqk[4] = {q4.x, q4.y, q4.z, q4.w};
+        // Z = q'.z of the block: rows g (hi) and g+8 (lo), every column alike.
+        mma_16816_acc(dz, aqk, hk ? zv.z : zv.x, hk ? zv.w : zv.y);
         // key step of the pair's channels times 4^-p of the pair's code
         // position (exact: a power of two)
         constexpr int P01[4] = {key_pos(0), key_pos(2), key_pos(4), key_pos(6)};
@@ -860,10 +870,10 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
           }
         }
         uint32_t at[4];
-        at[0] = hmul2_u(aq[k8][0], s01);
-        at[1] = hfma2_u(aq[k8][1], s01, hfma2_u(aq[k8][0], s01, neg2_u(at[0])));
-        at[2] = hmul2_u(aq[k8][2], s23);
-        at[3] = hfma2_u(aq[k8][3], s23, hfma2_u(aq[k8][2], s23, neg2_u(at[2])));
+        at[0] = hmul2_u(aqk[0], s01);
+        at[1] = hfma2_u(aqk[1], s01, hfma2_u(aqk[0], s01, neg2_u(at[0])));
+        at[2] = hmul2_u(aqk[2], s23);
+        at[3] = hfma2_u(aqk[3], s23, hfma2_u(aqk[2], s23, neg2_u(at[2])));
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
           const int wd = BITS == 2 ? k8 >> 2 : k8 >> 1;
@@ -1205,11 +1215,11 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
   }
 }
 
-// Up to 4 CTAs per SM in the column layout (128 registers), 3 in the row layout.
+// 4 CTAs per SM (128 registers), except the INT4 row layout (3).
 // BSCALE: per-block step scale (caches with the all-heads norm scope);
 // BITS: code width of the records (2, or the INT4 option).
 template <int GQ, bool PAGED, bool BSCALE, int BITS>
-__global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(NW * 32, GQ <= 4 || BITS == 2 ? 4 : 3) decode_int2_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
   static_assert(sizeof(MergeSmem<GQ, NW>) <= NW * Layout<BITS>::NSTAGE * Layout<BITS>::RL::BYTES,
@@ -1264,6 +1274,9 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 ? 4 : 3) decode_int2_kernel(c
 
 // Opt in to the kernel's dynamic shared memory (above 48 KB for INT2), once
 // per instantiation and device.
+template <int GQ, int BITS>
+constexpr int smem_bytes() { return Layout<BITS>::SMEM + (GQ == 8 ? kQStage : 0); }
+
 template <int GQ, bool PAGED, bool BSCALE, int BITS>
 cudaError_t allow_smem() {
   static int done[128] = {};
@@ -1272,7 +1285,7 @@ cudaError_t allow_smem() {
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
   e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED, BSCALE, BITS>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<BITS>::SMEM);
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<GQ, BITS>());
   if (e == cudaSuccess && dev >= 0 && dev < 128) done[dev] = 1;
   return e;
 }
@@ -1282,7 +1295,7 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e0 = allow_smem<GQ, PAGED, BSCALE, BITS>();
   if (e0 != cudaSuccess) return e0;
   dim3 grid(a.num_splits + 1, a.Hkv, a.B);
-  decode_int2_kernel<GQ, PAGED, BSCALE, BITS><<<grid, NW * 32, Layout<BITS>::SMEM, s>>>(a);
+  decode_int2_kernel<GQ, PAGED, BSCALE, BITS><<<grid, NW * 32, smem_bytes<GQ, BITS>(), s>>>(a);
   return cudaGetLastError();
 }
 
@@ -1309,7 +1322,7 @@ int occupancy_g() {
   if (allow_smem<GQ, false, false, 2>() != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ, false, false, 2>,
-                                                    NW * 32, Layout<2>::SMEM) != cudaSuccess)
+                                                    NW * 32, smem_bytes<GQ, 2>()) != cudaSuccess)
     return 0;
   return n;
 }

@@ -1,6 +1,6 @@
 """The split planner (oscar_decode_plan_splits, host arithmetic only) against
 the split counts that sweeps on GB300 (152 SMs, 4 decode CTAs per SM for
-groups up to 4, 3 for groups of 8) measured best, with L2 flushed between
+INT2) measured best, with L2 flushed between
 repetitions.  The counts are the kernel's tuning, not the method's
 arithmetic: a change of the planner's cost model that moves one of them
 must come with a new sweep.
@@ -27,7 +27,7 @@ MEASURED = {
     "batch 48 x 128K after 1280 steps": ((384, 4132, 4), 13),
     "batch 8 x 32K, 32/8 heads": ((64, 1024, 4), 9),       # 3-10 swept
     "batch 1 x 128K, 32/8 heads": ((8, 4096, 4), 37),      # 18-113 swept
-    "batch 16 x 64K, 32/4 heads": ((64, 2048, 3), 7),      # 2-12 swept
+    "batch 16 x 64K, 32/4 heads": ((64, 2048, 4), 9),      # 6-12 swept
     "batch 1 x 1K, 1/1 heads": ((1, 31, 4), 3),            # 1-8 swept (3 and 5 best)
     "batch 1 x 16K, 32/8 heads": ((8, 508, 4), 37),        # 4-50 swept (16 and 37 best)
     "batch 8 x 4K, 32/8 heads": ((64, 124, 4), 3),         # 1-6 swept (3 and 6 best)
