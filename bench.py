@@ -196,11 +196,37 @@ def _clock_summary(rows, t0, t1):
 # CPU oracle (bounded sample)
 # ---------------------------------------------------------------------------
 
-def _oracle_row_cache(wl, b, h, T_hist):
+def _oracle_row_cache(wl, b, h, T_hist, timing=None):
+    """The oracle's cache of row (b, h) over the workload's prompt; with a
+    list `timing`, the seconds of the oracle's prefix build (rotate, scale,
+    quantise) are appended to it."""
     from oracle import oscar_oracle as O
     kb = wl.k_bits([b], [h], 0, T_hist)[0, 0]
     vb = wl.v_bits([b], [h], 0, T_hist)[0, 0]
-    return O.build_head_cache(kb[:wl.T0], vb[:wl.T0], wl.n_packed), kb, vb
+    t = time.perf_counter()
+    hc = O.build_head_cache(kb[:wl.T0], vb[:wl.T0], wl.n_packed)
+    if timing is not None:
+        timing.append(time.perf_counter() - t)
+    return hc, kb, vb
+
+
+def cpu_baseline_configs(names, steps=2):
+    """The oracle, single-threaded, on one row of each other workload: its
+    prefix build (rotate, scale, quantise the prompt) and `steps` decode
+    steps, each extrapolated to all the workload's rows."""
+    from int2_kv_cache_02_gb300 import workloads as W
+    res = {}
+    for name in names:
+        wl = W.WORKLOADS[name]
+        rows = wl.B * wl.Hkv
+        tb = []
+        hc, kb, vb = _oracle_row_cache(wl, 0, 0, wl.T0 + steps + 1, timing=tb)
+        t = _oracle_steps(wl, hc, kb, vb, 0, 0, 0, steps)
+        res[name] = {"decode_us_per_step": t / steps * rows * 1e6,
+                     "prefix_quantize_us": tb[0] * rows * 1e6, "cores": 1, "kind": "oracle",
+                     "sample": f"row (0, 0) of {rows}: its prompt's prefix build and {steps} "
+                               f"decode steps, single thread; extrapolated x{rows} rows"}
+    return res
 
 
 def _truncate_packed(hc, keep):
@@ -242,7 +268,9 @@ def cpu_baseline(wl, budget_s=20.0):
     rows, then one process per core on as many rows in parallel."""
     rows = [(0, 0), (wl.B - 1, wl.Hkv - 1)]
     max_steps = 20
-    built = [(b, h) + _oracle_row_cache(wl, b, h, wl.T0 + max_steps + 1) for (b, h) in rows]
+    tb = []
+    built = [(b, h) + _oracle_row_cache(wl, b, h, wl.T0 + max_steps + 1, timing=tb)
+             for (b, h) in rows]
     b, h, hc, kb, vb = built[0]
     t1 = _oracle_steps(wl, hc, kb, vb, b, h, 0, 1)           # calibration step (untimed)
     n = max(1, min(max_steps, int(budget_s / max(t1, 1e-3) / len(rows))))
@@ -254,7 +282,12 @@ def cpu_baseline(wl, budget_s=20.0):
     out = {"value": per * total_rows * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
            "sample": f"{len(rows)} of {total_rows} (sequence, KV head) rows x {n} decode steps "
                      f"at full context, single thread; extrapolated x{total_rows} rows",
-           "host_cores": os.cpu_count()}
+           "host_cores": os.cpu_count(),
+           "prefix_quantize": {"value": sum(tb) / len(tb) * total_rows * 1e6, "unit": "us",
+                               "cores": 1, "kind": "oracle",
+                               "sample": f"the prompt's prefix build (rotate, scale, quantise "
+                                         f"{wl.n_packed} tokens) of {len(tb)} rows, single "
+                                         f"thread; extrapolated x{total_rows} rows"}}
     # all cores: one spawned process per core, one row each (the pool starts
     # with `spawn`: a forked child of a CUDA process can hang)
     ncpu = os.cpu_count() or 1
@@ -988,6 +1021,8 @@ def run_ours(args, world, rank, local):
         line["bf16_decode"] = bf16
     if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == WORKLOAD:
         line["cpu_baseline"] = cpu_baseline(wl)
+        if not args.no_configs:
+            line["cpu_baseline"]["configs"] = cpu_baseline_configs(CONFIG_WORKLOADS)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
