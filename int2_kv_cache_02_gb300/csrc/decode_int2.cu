@@ -250,11 +250,13 @@ struct WarpRing {
   const uint8_t* src;   // record of the range's first block (contiguous cache)
   int n;                // blocks in the range
   int lane;
-  // paged cache: the range's block-table entries and the row's KV head (the
-  // pool, its size and the status word are read from the launch arguments
-  // where they are used, so they hold no registers through the loop)
+  // paged cache: the range's block-table entries, and the row's record in
+  // page 0 and the page stride, so that a record's address is one 32 x 32
+  // -> 64-bit multiply-add (the pool's size and the status word are read
+  // from the launch arguments where they are used)
   const int32_t* tab;
-  int h;
+  const uint8_t* pages_h;   // record of the row's KV head in page 0
+  unsigned page_stride;     // bytes per page (Hkv records)
 
   // Page id of block i of the range (paged cache; 0 past the range's end or
   // for a contiguous cache).  Loaded when block i - NSTAGE is taken up, so
@@ -267,7 +269,7 @@ struct WarpRing {
   // range's ids were checked against the pool when the ring was made).
   __device__ __forceinline__ const uint8_t* record(int i, int page, const DecodeArgs& a) const {
     if constexpr (PAGED) {
-      return a.packed + ((long long)page * a.Hkv + h) * RB;
+      return pages_h + (unsigned long long)(unsigned)page * page_stride;
     } else {
       return src + (long long)i * RB;
     }
@@ -377,7 +379,8 @@ __device__ __forceinline__ WarpRing<PAGED, BITS> make_ring(const DecodeArgs& a, 
   r.n = wb1 - wb0;
   r.lane = threadIdx.x & 31;
   r.tab = PAGED ? a.block_table + (long long)b * a.max_blocks + wb0 : nullptr;
-  r.h = h;
+  r.pages_h = a.packed + (long long)h * RB;
+  r.page_stride = (unsigned)a.Hkv * (unsigned)RB;
   if constexpr (PAGED) {
     // Every page id of the range is checked once, before any copy: one out
     // of range is reported and the warp reads nothing (its result is void).
