@@ -100,7 +100,8 @@ def _config(wl, S=None):
     cfg = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": 128,
            "context": wl.T0, "key_group": 32, "residual_window": 128,
            "step": "rotate_q + append_kv (flush every 128) + fused INT2 decode with the "
-                   "LSE combine in its last CTA per row",
+                   "LSE combine in its last CTA per row, as three calls (step_compare times "
+                   "the same step as one oscar_decode_step launch)",
            "l2": (f"inputs larger than L2: ~{gb:.2f} GB packed cache read per step vs 129 MB L2"
                   if gb > 2 * 0.129 else
                   f"~{gb * 1e3:.0f} MB packed cache; L2 flushed ({L2_FLUSH_BYTES >> 20} MB "
@@ -456,7 +457,7 @@ def _flush_loop_timed(fn, reps, flushbuf):
 def measure_config(L, W, name, dev, flushbuf, peak, reps=100):
     """One workload other than the headline one: the fused decode over its
     prompt (plus one appended token) with L2 flushed before every rep, and
-    for the streaming workloads the whole decode step (rotate_q, append with
+    for the streaming workloads the whole decode step (oscar_decode_step: rotate_q, append with
     the flushes every 128 tokens, decode) over the workload's 256 steps, L2
     flushed before every step."""
     import torch
@@ -507,9 +508,7 @@ def measure_config(L, W, name, dev, flushbuf, peak, reps=100):
             if cache.n_res == 128:
                 flushes += 1
             a.record()
-            L.rotate_q(Q[i + 1], qr)
-            L.append_kv(cache, Kn[i + 1], Vn[i + 1], n_tok=1)
-            L.decode_attention(cache, qr, wl.Hq, tau, out, ws, num_splits=0)
+            L.decode_step(cache, Q[i + 1], Kn[i + 1], Vn[i + 1], wl.Hq, tau, out, ws)
             b.record()
             S = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, cache.n_packed)
             nbytes += _algorithmic_bytes(wl, cache.n_packed, cache.n_res, S)
@@ -520,9 +519,10 @@ def measure_config(L, W, name, dev, flushbuf, peak, reps=100):
         res["stream"] = {"steps": n_st, "flushes": flushes, "us_per_step": us,
                          "us_per_step_median": float(np.median(st)), "GB/s": gbs,
                          "frac": gbs / peak,
-                         "note": "whole decode step (rotate_q + append_kv + decode), L2 "
-                                 "flushed before every step; GB/s counts the decode's "
-                                 "algorithmic bytes only"}
+                         "note": "whole decode step (oscar_decode_step: rotate_q + append + "
+                                 "decode in one launch, the flush before it when the window "
+                                 "is full), L2 flushed before every step; GB/s counts the "
+                                 "decode's algorithmic bytes only"}
     if L.device_status() != 0:
         raise RuntimeError(f"{name}: a kernel recorded an error")
     del cache, ws, Kn, Vn, Q
@@ -638,7 +638,8 @@ def run_ours(args, world, rank, local):
     W_, K_ = args.warmup, args.steps
     E_ = args.e2e_steps
     flush_at = min(max(K_ // 2, 0), 64)         # timed step at which a flush falls
-    total_steps = W_ + 128 + K_ + 2 + E_
+    N3 = 130   # steps of the three-call comparison leg (one flush among them)
+    total_steps = W_ + 128 + K_ + 2 + E_ + N3
     T_cap = wl.t_cap(total_steps - wl.steps)
     peaks = _peaks()
     peak = peaks.get("hbm_gbs")
@@ -662,6 +663,8 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream()
 
     def step(i, ev=None):
+        # one decode step as three calls: rotate_q, append (with the flush of
+        # a full window), decode; ev brackets the decode
         L.rotate_q(Q[i], qr)
         L.append_kv(cache, Kn[i], Vn[i], n_tok=1)
         if ev is not None:
@@ -669,6 +672,10 @@ def run_ours(args, world, rank, local):
         L.decode_attention(cache, qr, wl.Hq, tau, out, ws, num_splits=S)
         if ev is not None:
             ev[1].record(stream)
+
+    def step_fused(i):
+        # the same step in one call (one launch; two on a flush step)
+        L.decode_step(cache, Q[i], Kn[i], Vn[i], wl.Hq, tau, out, ws, num_splits=S)
 
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     vis = [v for v in vis.split(",") if v.strip().isdigit()]
@@ -725,8 +732,8 @@ def run_ours(args, world, rank, local):
         plain = [t for j, t in enumerate(pre_us) if j not in flush_steps]
         base_us = float(np.median(plain)) if plain else float("nan")
         with_f = [pre_us[j] for j in flush_steps]
-        rows = wl.B * wl.Hkv
-        fb = rows * 128 * (256 + 2 + 256) + rows * 4 * 2752   # read the window, write 4 records
+        rows_ = wl.B * wl.Hkv
+        fb = rows_ * 128 * (256 + 2 + 256) + rows_ * 4 * 2752   # read the window, write 4 records
         extra = float(np.mean(with_f)) - base_us
         flush_obj = {"timed_steps_with_flush": flush_steps,
                      "step_us_with_flush": [step_us[j] for j in flush_steps],
@@ -806,6 +813,33 @@ def run_ours(args, world, rank, local):
                + Vh[0].numel() * Vh.element_size())
         d2h = out.numel() * out.element_size()
         e2e_us = max_over_ranks(e2e_us, world, dev)
+
+    # ---- the fused step (oscar_decode_step) against the three calls ----
+    # alternating on the same cache, so that both see the same context
+    i3 = (i_step + 2 + E_) if E_ > 0 else (i_step + 2)
+    t_fused, t_three = [], []
+    for j in range(N3):
+        a3, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        flush_now = cache.n_res == 128
+        a3.record(stream)
+        if j % 2:
+            step_fused(i3 + j)
+        else:
+            step(i3 + j)
+        b3.record(stream)
+        if not flush_now:
+            (t_fused if j % 2 else t_three).append((a3, b3))
+    torch.cuda.synchronize()
+    if L.device_status() != 0:
+        raise RuntimeError("a kernel recorded an error in the step comparison")
+    step_compare = {"fused_step_us_median": float(np.median([a.elapsed_time(b) * 1e3
+                                                              for a, b in t_fused])),
+                    "three_call_step_us_median": float(np.median([a.elapsed_time(b) * 1e3
+                                                                  for a, b in t_three])),
+                    "steps": N3,
+                    "note": "oscar_decode_step (one launch) against rotate_q + append_kv + "
+                            "decode_attention (three launches), alternating on the same cache "
+                            "(flush steps left out); the timed steps above use the three calls"}
 
     # ---- bf16 comparison kernel, same shape (context T0) ----
     bf16 = None
@@ -1011,6 +1045,7 @@ def run_ours(args, world, rank, local):
                            "end": ctx0[0] + ctx0[1] + K_},
         "flushes_in_timed_region": len(flush_steps),
         "flush": flush_obj,
+        "step_compare": step_compare,
         "configs": configs,
         "prefill": prefill,
         "paged": paged,

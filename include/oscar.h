@@ -295,6 +295,31 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
                                     float softmax_scale, float* out, int num_splits,
                                     void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * Fused decode step: oscar_rotate_q, oscar_append_kv of one token and
+ * oscar_decode_attention in one kernel launch (plus the flush of a full
+ * residual window, before it, as oscar_append_kv does).  The kernel's CTAs
+ * rotate their own query heads, and the residual CTA of each (b, h) row
+ * rotates and scales the new key, writes it and the new value at the next
+ * residual slot, then attends over the window including it; the other CTAs
+ * never read the window.  The rotation and scaling are the same device code
+ * as in the separate calls, so the outputs and the cache equal theirs bit
+ * for bit ([news] 三: kernels ① and ③ around one decode step; [notes] II
+ * End-to-End Flow).
+ *  q          bf16 [B][Hq][128] raw queries
+ *  k_new      bf16 [B][Hkv][128] raw key of the new token
+ *  v_new      bf16 [B][Hkv][128] value of the new token
+ *  out, num_splits, workspace: as for oscar_decode_attention, the split count
+ *             planned for n_packed after the flush (if any).
+ * Contiguous caches only (a paged cache uses the oscar_paged_* calls).  All
+ * checks, including capacity for the flush and the workspace size, happen
+ * before any launch; n_res (and n_packed after a flush) advance on success.
+ * If the flush launched and the decode launch then fails, the flush stays.
+ */
+oscar_status oscar_decode_step(oscar_cache* c, const oscar_bf16* q, const oscar_bf16* k_new,
+                               const oscar_bf16* v_new, int Hq, float softmax_scale, float* out,
+                               int num_splits, void* workspace, size_t ws_bytes, void* stream);
+
 /* Split count oscar_decode_attention uses for num_splits = 0 on the current
  * device (>= 1).  Returns 1 when no device can be queried. */
 int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed);

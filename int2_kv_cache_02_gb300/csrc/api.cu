@@ -359,6 +359,64 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   return from_cuda(e);
 }
 
+oscar_status oscar_decode_step(oscar_cache* c, const oscar_bf16* q, const oscar_bf16* k_new,
+                               const oscar_bf16* v_new, int Hq, float softmax_scale, float* out,
+                               int num_splits, void* workspace, size_t ws_bytes, void* stream) {
+  oscar_status st = check_cache(c);
+  if (st != OSCAR_OK) return st;
+  if (!q || !k_new || !v_new || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
+      !std::isfinite(softmax_scale))
+    return OSCAR_ERR_INVALID_ARG;
+  if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
+  if ((long long)c->B * c->Hkv > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
+  if (!al16(q) || !al16(k_new) || !al16(v_new) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
+  // a full window is flushed first (flush-before-append); everything is
+  // checked before anything is launched
+  const bool flush = c->n_res == kR;
+  const int n_packed = c->n_packed + (flush ? kR : 0);
+  if (n_packed > c->T_cap) return OSCAR_ERR_CAPACITY;
+  const int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, n_packed);
+  if (!workspace || ws_bytes < decode_ws_bytes(c->B, c->Hkv, Hq, S + 1))
+    return OSCAR_ERR_WORKSPACE;
+  if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;
+  const cudaStream_t s = as_stream(stream);
+  if (flush) {
+    st = flush_residual(c, s);
+    if (st != OSCAR_OK) return st;
+  }
+  const KeyScale ks = key_scale(c->flags, c->norm_target);
+  DecodeArgs a;
+  a.packed = c->packed;
+  a.k_res = c->k_res;
+  a.v_res = c->v_res;
+  a.k_res_norm = reinterpret_cast<const __half*>(c->k_res_norm);
+  a.q_rot = nullptr;
+  a.q_raw = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.norm_target = ks.target;
+  a.ws = decode_partials(workspace);
+  a.row_count = decode_row_counters(workspace);
+  a.out = out;
+  a.status = status_ptr();
+  a.B = c->B;
+  a.Hkv = c->Hkv;
+  a.Hq = Hq;
+  a.T_cap = c->T_cap;
+  a.n_packed = c->n_packed;
+  a.n_res = c->n_res + 1;   // the new token, written by the kernel
+  a.num_splits = S;
+  a.flags = c->flags;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.q_exp = query_exponent(ks);
+  a.bits = code_bits(c->bits);
+  cudaError_t e = launch_decode_int2(a, s);
+  g_launches += 1;
+  if (e != cudaSuccess) return OSCAR_ERR_CUDA;
+  c->n_res += 1;
+  return OSCAR_OK;
+}
+
 // ------------------------------------------------------------------ paged
 
 }  // extern "C"

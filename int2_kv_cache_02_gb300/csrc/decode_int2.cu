@@ -43,6 +43,7 @@
 #include "common.cuh"
 #include "cta_merge.cuh"
 #include "launch.h"
+#include "rotate.cuh"
 
 namespace oscar {
 namespace {
@@ -63,6 +64,12 @@ struct Layout {
 
 constexpr float kLazyLog2 = 8.0f;         // lazy softmax rescale threshold (log2 units)
 constexpr int kQStage = 8 * 32 * 16;   // row layout: staged query fragments (bytes)
+constexpr int kQRotStage = 16 * kD * 4;   // fused step: the rotated queries (bytes)
+// Dynamic shared memory of an instantiation: the rings and barriers and the
+// staged query fragments of the row layout; a fused-step launch adds the
+// rotated queries (kQRotStage) after them.
+template <int GQ, int BITS>
+constexpr int smem_bytes() { return Layout<BITS>::SMEM + (GQ == 8 ? kQStage : 0); }
 // The kernel's dynamic shared memory (every extern declaration names the
 // same address).
 __device__ __forceinline__ uint8_t* dyn_smem() {
@@ -411,6 +418,67 @@ __device__ __forceinline__ void load_query(float4 (&qv)[8], const float* qrow, i
 #pragma unroll
   for (int i = 0; i < 8; ++i) qv[i] = qp[i];
 }
+// Fused decode step: the rotated query from its raw bf16 elements 4l .. 4l
+// + 3 (lane l), formed exactly as rotate_q_kernel forms it (same butterflies
+// in the same order), so the fused step and the separate calls agree bit
+// for bit.
+__device__ __forceinline__ float4 rotate_query_raw(const DecodeArgs& a, uint2 raw, int lane) {
+  float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+  if (!(a.flags & OSCAR_NO_ROTATE)) {
+    fht128(x, lane);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) x[r] *= kInvSqrtD;
+  }
+  return make_float4(x[0], x[1], x[2], x[3]);
+}
+__device__ __forceinline__ float4 rotated_query(const DecodeArgs& a, long long v, int lane) {
+  return rotate_query_raw(a, reinterpret_cast<const uint2*>(a.q_raw + v * kD)[lane], lane);
+}
+
+// Fused decode step: the queries, staged as float [heads][128] in shared
+// memory past the end of the non-fused kernel's dynamic shared memory (the
+// fused launch alone enlarges it), in two phases.  load_raw_queries issues
+// the raw loads before the ring's first copies, so that they do not queue
+// behind them; stage_rotated_queries rotates and stores them.  For groups of
+// up to 4 heads every warp rotates all of them into its own area and waits
+// only for itself, so a starting CTA's warps do not wait on one another; for
+// groups of 8 warp w rotates heads w and w + 4 into one area shared by the
+// CTA, behind a barrier.  Both are called by every thread; the result points
+// at the row's first query head.
+template <int GQ>
+struct RawQueries {
+  static constexpr int N = GQ <= NW ? GQ : GQ / NW;   // heads loaded per warp
+  uint2 v[N];
+};
+template <int GQ>
+__device__ __forceinline__ void load_raw_queries(const DecodeArgs& a, long long qrow0,
+                                                 RawQueries<GQ>& raw) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 0; k < RawQueries<GQ>::N; ++k) {
+    const int j = GQ <= NW ? k : warp + NW * k;
+    raw.v[k] = reinterpret_cast<const uint2*>(a.q_raw + (qrow0 + j) * kD)[lane];
+  }
+}
+template <int GQ>
+__device__ __forceinline__ const float* stage_rotated_queries(const DecodeArgs& a,
+                                                              const RawQueries<GQ>& raw,
+                                                              uint8_t* stage) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* qs = reinterpret_cast<float*>(stage) + (GQ <= NW ? warp * GQ * kD : 0);
+#pragma unroll
+  for (int k = 0; k < RawQueries<GQ>::N; ++k) {
+    const int j = GQ <= NW ? k : warp + NW * k;
+    reinterpret_cast<float4*>(qs + j * kD)[lane] = rotate_query_raw(a, raw.v[k], lane);
+  }
+  if constexpr (GQ <= NW) {
+    __syncwarp();
+  } else {
+    __syncthreads();
+  }
+  return qs;
+}
+
 __device__ __forceinline__ float scale_query(float (&qf)[32], const float4 (&qv)[8],
                                             const DecodeArgs& a) {
 #pragma unroll
@@ -455,7 +523,13 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   // travel while the query is prepared (INT4: the copies first, which keeps
   // its instantiations free of spills).
   float4 qv[8];
-  if constexpr (BITS == 2) {
+  if (a.q_raw != nullptr) {   // fused step: rotate the CTA's queries here
+    RawQueries<GQ> raw;
+    load_raw_queries<GQ>(a, qrow0, raw);
+    R.start(a);
+    const float* qs = stage_rotated_queries<GQ>(a, raw, dyn_smem() + smem_bytes<GQ, BITS>());
+    load_query(qv, qs + hq * kD, tig);
+  } else if constexpr (BITS == 2) {
     load_query(qv, a.q_rot + (qrow0 + hq) * kD, tig);
     R.start(a);
   } else {
@@ -749,7 +823,13 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
   // travel while the query is prepared (INT4: the copies first, which keeps
   // its instantiations free of spills).
   float4 qv[8];
-  if constexpr (BITS == 2) {
+  if (a.q_raw != nullptr) {   // fused step: rotate the CTA's queries here
+    RawQueries<GQ> raw;
+    load_raw_queries<GQ>(a, qrow0, raw);
+    R.start(a);
+    const float* qs = stage_rotated_queries<GQ>(a, raw, dyn_smem() + smem_bytes<GQ, BITS>());
+    load_query(qv, qs + head * kD, tig);
+  } else if constexpr (BITS == 2) {
     load_query(qv, a.q_rot + (qrow0 + head) * kD, tig);
     R.start(a);
   } else {
@@ -1055,11 +1135,33 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
       n_res = 0;
     }
   }
+  if (!PAGED && a.k_new != nullptr) {
+    // Fused step: the new token goes to residual slot n_res - 1 first,
+    // rotated and scaled as rotate_scale_k_kernel does it (warp 0) and its
+    // value copied (warp 1); only this CTA reads the row's residual window.
+    const long long tok = row * kR + (n_res - 1);
+    if (warp == 0) {
+      const KeyScale ks{a.flags, a.norm_target};
+      float s_all = 0.0f;
+      if (ks.flags & OSCAR_NORM_ALL_HEADS)
+        s_all = all_heads_sq(a.k_new + (long long)b * a.Hkv * kD, (long long)kD, a.Hkv, lane);
+      const uint2 raw = reinterpret_cast<const uint2*>(a.k_new + row * kD)[lane];
+      float x[4] = {bf16_lo(raw.x), bf16_hi(raw.x), bf16_lo(raw.y), bf16_hi(raw.y)};
+      const float norm = rotate_scale_key(x, lane, ks, s_all);
+      reinterpret_cast<uint2*>(const_cast<uint16_t*>(a.k_res) + tok * kD)[lane] = pack_bf16x4(x);
+      if (lane == 0) const_cast<__half*>(a.k_res_norm)[tok] = __float2half_rn(norm);
+    } else if (warp == 1) {
+      reinterpret_cast<uint2*>(const_cast<uint16_t*>(a.v_res) + tok * kD)[lane] =
+          reinterpret_cast<const uint2*>(a.v_new + row * kD)[lane];
+    }
+    __syncthreads();
+  }
   // Unit-norm bf16 keys times their fp16 norms, bf16 values; CUDA cores.
   float qv[GQ][4], mr[GQ], lr[GQ], orr[GQ][4];
 #pragma unroll
   for (int j = 0; j < GQ; ++j) {
-    const float4 v = reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
+    const float4 v = a.q_raw != nullptr ? rotated_query(a, qrow0 + j, lane)
+                                        : reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
     qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
     mr[j] = -INFINITY; lr[j] = 0.0f;
     orr[j][0] = orr[j][1] = orr[j][2] = orr[j][3] = 0.0f;
@@ -1277,9 +1379,6 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 || BITS == 2 ? 4 : 3) decode_
 
 // Opt in to the kernel's dynamic shared memory (above 48 KB for INT2), once
 // per instantiation and device.
-template <int GQ, int BITS>
-constexpr int smem_bytes() { return Layout<BITS>::SMEM + (GQ == 8 ? kQStage : 0); }
-
 template <int GQ, bool PAGED, bool BSCALE, int BITS>
 cudaError_t allow_smem() {
   static int done[128] = {};
@@ -1288,7 +1387,7 @@ cudaError_t allow_smem() {
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
   e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED, BSCALE, BITS>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<GQ, BITS>());
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<GQ, BITS>() + kQRotStage);
   if (e == cudaSuccess && dev >= 0 && dev < 128) done[dev] = 1;
   return e;
 }
@@ -1298,7 +1397,8 @@ cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e0 = allow_smem<GQ, PAGED, BSCALE, BITS>();
   if (e0 != cudaSuccess) return e0;
   dim3 grid(a.num_splits + 1, a.Hkv, a.B);
-  decode_int2_kernel<GQ, PAGED, BSCALE, BITS><<<grid, NW * 32, smem_bytes<GQ, BITS>(), s>>>(a);
+  const int smem = smem_bytes<GQ, BITS>() + (a.q_raw != nullptr ? kQRotStage : 0);
+  decode_int2_kernel<GQ, PAGED, BSCALE, BITS><<<grid, NW * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 

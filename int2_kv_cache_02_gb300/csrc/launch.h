@@ -87,6 +87,15 @@ struct DecodeArgs {
   const int32_t* seq_packed = nullptr;
   const int32_t* seq_res = nullptr;
   int max_blocks = 0, n_pages = 0;
+  // fused decode step (contiguous cache): q_raw (bf16 [B][Hq][128]) replaces
+  // q_rot and is rotated in the kernel; k_new, v_new (bf16 [B][Hkv][128]) are
+  // the new token, which the residual CTA of each row rotates, scales and
+  // writes at residual slot n_res - 1 before it reads the window (n_res then
+  // counts the new token); norm_target is the cache's key-scaling target
+  const uint16_t* q_raw = nullptr;
+  const uint16_t* k_new = nullptr;
+  const uint16_t* v_new = nullptr;
+  float norm_target = 1.0f;
 };
 
 // Floats per split-K partial record: m, l, 2 pad, o[128].

@@ -88,6 +88,8 @@ def _load() -> ctypes.CDLL:
                                            c_void_p, c_size_t, c_void_p]),
         "oscar_decode_attention_static_ws": (c_int, [P, c_void_p, c_int, c_float, c_void_p,
                                                      c_int, c_void_p]),
+        "oscar_decode_step": (c_int, [P, c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p,
+                                      c_int, c_void_p, c_size_t, c_void_p]),
         "oscar_decode_num_splits": (c_int, [c_int, c_int, c_int, c_int]),
         "oscar_decode_plan_splits": (c_int, [ctypes.c_longlong, ctypes.c_longlong, c_int, c_int]),
         "oscar_decode_workspace_bytes": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
@@ -365,6 +367,19 @@ def decode_attention(cache: KVCache, q_rot: torch.Tensor, Hq: int, softmax_scale
                                        num_splits, _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream)), "oscar_decode_attention")
+
+
+def decode_step(cache: KVCache, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                Hq: int, softmax_scale: float, out: torch.Tensor, workspace: torch.Tensor,
+                num_splits: int = 0, stream=None):
+    """One decode step in one launch: rotate the raw queries q (bf16
+    [B][Hq][128]), append the new token (k_new, v_new bf16 [B][Hkv][128];
+    a full window is flushed first) and attend; equals rotate_q + append_kv +
+    decode_attention bit for bit.  Advances the cache's residual count."""
+    _check(_lib.oscar_decode_step(cache.ref(), _ptr(q), _ptr(k_new), _ptr(v_new), Hq,
+                                  softmax_scale, _ptr(out), num_splits, _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "oscar_decode_step")
 
 
 def decode_attention_static_ws(cache: KVCache, q_rot: torch.Tensor, Hq: int,

@@ -41,7 +41,8 @@ def test_headers_declare_the_documented_calls():
                  "oscar_decode_workspace_bytes", "oscar_decode_num_splits",
                  "oscar_device_status", "oscar_status_string", "oscar_kernel_launches",
                  "oscar_selftest_wait_timeout", "oscar_prefill_kv", "oscar_paged_prefill_kv",
-                 "oscar_paged_append_kv", "oscar_paged_decode_attention"]:
+                 "oscar_paged_append_kv", "oscar_paged_decode_attention", "oscar_decode_step",
+                 "oscar_decode_plan_splits"]:
         assert want in names
     assert _declared("oscar_synth.h") == ["oscar_synth_bf16"]
 
@@ -257,3 +258,37 @@ def test_synth_validation(libs):
     assert f(None, 1, 1, 0, 4, 0, 4, 1, None, None, None) == 1
     assert f(FAKE + 2, 1, 1, 0, 4, 0, 4, 1, None, None, None) == 1
     assert f(FAKE, 1, 1, 0, 2, 0, 4, 1, None, None, None) == 1
+
+
+@no_gpu_only
+def test_decode_step_validation_leaves_the_cache_untouched():
+    """The fused decode step checks everything (arguments, alignment, the
+    flush's capacity, the workspace) before it launches anything, and leaves
+    the cache's counts as they were when a check fails."""
+    from int2_kv_cache_02_gb300 import oscar as O
+    L = O.library()
+    P = ctypes.c_void_p
+    ws = 1 << 30
+
+    def step(c, q=FAKE, k=FAKE, v=FAKE, Hq=4, out=FAKE, splits=1, wsb=ws):
+        return L.oscar_decode_step(ctypes.byref(c), P(q), P(k), P(v), Hq, 0.1, P(out), splits,
+                                   P(FAKE + 0x1000000), wsb, None)
+
+    c = _cache(n_packed=64, n_res=5)
+    assert step(c, q=0) == 1
+    assert step(c, k=0) == 1
+    assert step(c, v=0) == 1
+    assert step(c, out=0) == 1
+    assert step(c, Hq=0) == 1
+    assert step(c, splits=-1) == 1
+    assert step(c, k=FAKE + 8) == 3
+    assert step(c, q=FAKE + 4) == 3
+    assert step(c, Hq=6) == 2                                # group of 3
+    assert step(c, wsb=16) == 5                              # workspace too small
+    assert c.n_packed == 64 and c.n_res == 5
+    full = _cache(n_packed=256, n_res=128)                   # the flush would not fit
+    assert step(full) == 4
+    assert full.n_packed == 256 and full.n_res == 128
+    for bad in (_cache(flags=8), _cache(norm_target=-1.0), _cache(key_group=48)):
+        assert step(bad) == 1
+        assert bad.n_packed == 0 and bad.n_res == 0
