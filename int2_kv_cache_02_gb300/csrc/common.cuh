@@ -122,6 +122,18 @@ __device__ __forceinline__ uint32_t half2_as_u32(__half2 h) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+// Both bf16 of a packed pair as fp32, the low one in x.
+__device__ __forceinline__ float2 bf16_pair(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
+
+// Packed fp32 arithmetic (one instruction for two IEEE operations, each half
+// rounded to nearest even exactly as the scalar operation).  a - b is the
+// fused multiply-add b * -1 + a: one rounding of the exact difference.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;

@@ -33,8 +33,46 @@ struct GroupSmem {
   alignas(16) uint16_t kt[GS][kTileRow];
   alignas(16) uint16_t vt[NVB][kG][kTileRow];
   KeyParamSmem P;
+  KeyMinMax mm[128];
   __half ns[GS];
 };
+
+// Rotates and scales one token's quarter of raw keys (raw: its 32 bf16 as
+// four 16-byte words) into row t of kt and the token's norm into ns, in the
+// quarter layout (lane l holds quarter l >> 3).  With the all-heads norm,
+// head0 is the token's key of head 0 and head_stride the distance between
+// heads.
+template <int GS, bool PLAIN>
+__device__ __forceinline__ void rotate_token(GroupSmem<GS>& S, const uint4 (&raw)[4], int t,
+                                             const uint16_t* head0, long long head_stride,
+                                             int Hkv, KeyScale ks) {
+  const int lane = threadIdx.x & 31, Q = lane >> 3;
+  float x[32];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t u[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      x[8 * j + 2 * q] = bf16_lo(u[q]);
+      x[8 * j + 2 * q + 1] = bf16_hi(u[q]);
+    }
+  }
+  float s_all = 0.0f;
+  if (!PLAIN && (ks.flags & OSCAR_NORM_ALL_HEADS))
+    s_all = all_heads_sq_q(head0, head_stride, Hkv, lane);
+  const float norm = rotate_scale_key<PLAIN>(x, lane, ks, s_all);
+  uint4* dst = reinterpret_cast<uint4*>(&S.kt[t][32 * Q]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint4 o;
+    o.x = bf16x2_bits(x[8 * j], x[8 * j + 1]);
+    o.y = bf16x2_bits(x[8 * j + 2], x[8 * j + 3]);
+    o.z = bf16x2_bits(x[8 * j + 4], x[8 * j + 5]);
+    o.w = bf16x2_bits(x[8 * j + 6], x[8 * j + 7]);
+    dst[j] = o;
+  }
+  if (Q == 0) S.ns[t] = __float2half_rn(norm);
+}
 
 // Rotates and scales the GS raw keys of a group (rows k[t], t < GS) into kt
 // and their norms into ns, in the quarter layout: at step i, warp w and lane
@@ -54,36 +92,15 @@ __device__ __forceinline__ void rotate_group(GroupSmem<GS>& S, const uint16_t* k
 #pragma unroll 1
   for (int i = 0; i < GS / kG; ++i) {
     const int t = kG * i + tw;
-    float x[32];
+    uint4 cur[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t u[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        x[8 * j + 2 * q] = bf16_lo(u[q]);
-        x[8 * j + 2 * q + 1] = bf16_hi(u[q]);
-      }
-    }
+    for (int j = 0; j < 4; ++j) cur[j] = raw[j];
     if (i + 1 < GS / kG) {
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         raw[j] = reinterpret_cast<const uint4*>(k + (long long)(t + kG) * kD)[4 * Q + j];
     }
-    float s_all = 0.0f;
-    if (!PLAIN && (ks.flags & OSCAR_NORM_ALL_HEADS))
-      s_all = all_heads_sq_q(head0 + (long long)t * kD, head_stride, Hkv, lane);
-    const float norm = rotate_scale_key<PLAIN>(x, lane, ks, s_all);
-    uint4* dst = reinterpret_cast<uint4*>(&S.kt[t][32 * Q]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      uint4 o;
-      o.x = bf16x2_bits(x[8 * j], x[8 * j + 1]);
-      o.y = bf16x2_bits(x[8 * j + 2], x[8 * j + 3]);
-      o.z = bf16x2_bits(x[8 * j + 4], x[8 * j + 5]);
-      o.w = bf16x2_bits(x[8 * j + 6], x[8 * j + 7]);
-      dst[j] = o;
-    }
-    if (Q == 0) S.ns[t] = __float2half_rn(norm);
+    rotate_token<GS, PLAIN>(S, cur, t, head0 + (long long)t * kD, head_stride, Hkv, ks);
   }
 }
 
@@ -96,17 +113,23 @@ template <int GS, int BITS, class RecOf>
 __device__ __forceinline__ void quantize_group(GroupSmem<GS>& S, const __half* norms,
                                                const uint16_t* v_src, RecOf rec_of) {
   constexpr int NB = GS / kG;
-  key_params<GS, BITS>(S.kt, S.P, rec_of);
+  // block 0's values need no key parameter: they are worked between the
+  // two halves of the key parameters, so no warp idles at the barriers
+  key_minmax_half<GS>(S.kt, S.mm);
+  value_block<BITS>(S.vt[0], norms, rec_of(0));
+  __syncthreads();
+  key_params<GS, BITS>(S.mm, S.P, rec_of);
   __syncthreads();
 #pragma unroll 1
   for (int sb = 0; sb < NB; ++sb) {
-    // the buffer of block sb + 1 was last read by block sb - 1, before the
-    // barrier that ended that block
+    // the buffer of block sb + 1 was last read by block sb - 1's values,
+    // before the barrier that preceded this block's keys
     if (sb + 1 < NB) stage_rows<kG>(S.vt[(sb + 1) % S.NVB], v_src + (long long)(sb + 1) * kG * kD);
-    quantize_block<BITS>(&S.kt[kG * sb], S.vt[sb % S.NVB], S.P, norms + kG * sb, rec_of(sb));
+    key_block<BITS>(&S.kt[kG * sb], S.P, rec_of(sb));
     if (sb + 1 < NB) {
       async_wait_all();
       __syncthreads();
+      value_block<BITS>(S.vt[(sb + 1) % S.NVB], norms + kG * (sb + 1), rec_of(sb + 1));
     }
   }
 }
@@ -160,6 +183,64 @@ __global__ void __launch_bounds__(128) prefill_kv_kernel(
   uint8_t* row_rec = packed + (row * (T_cap / kG) + p0 / kG + (long long)j * (GS / kG)) * RB;
   quantize_group<GS, BITS>(S, S.ns, v + src_tok * kD,
                            [&](int sb) { return row_rec + (long long)sb * RB; });
+}
+
+// The fused prefill for groups of 32 tokens as a persistent kernel: CTA c
+// works the units c, c + gridDim.x, ... (unit u: group u % n_groups of row
+// u / n_groups, row = b Hkv + h), and the raw keys and values of its next
+// unit are copied into shared memory (cp.async) while the current one is
+// quantised, so a CTA waits for its loads once, not once per group.  Same
+// arithmetic and records as prefill_kv_kernel.
+struct PrefillSmem {
+  GroupSmem<kG> G;
+  alignas(16) uint16_t kraw[kG][kTileRow];   // raw keys of the unit to rotate next
+};
+template <int BITS, bool PLAIN>
+__global__ void __launch_bounds__(128, 7) prefill_kv_persistent(
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int in_T, int Hkv,
+    int n_groups, long long n_units, int T_cap, int p0, KeyScale ks,
+    uint8_t* __restrict__ packed) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  auto& PS = *reinterpret_cast<PrefillSmem*>(smem_raw);
+  auto& S = PS.G;
+  constexpr int RB = Rec<BITS>::BYTES;
+  const int tid = threadIdx.x, lane = tid & 31, Q = lane >> 3;
+  const int tw = 8 * (tid >> 5) + (lane & 7);
+  auto src_tok_of = [&](long long u) {
+    const long long row = u / n_groups;
+    return row * in_T + (u - row * n_groups) * kG;
+  };
+  long long u = blockIdx.x;
+  if (u >= n_units) return;
+  stage_rows<kG>(PS.kraw, k + src_tok_of(u) * kD);
+  stage_rows<kG>(S.vt[0], v + src_tok_of(u) * kD);
+#pragma unroll 1
+  for (; u < n_units; u += gridDim.x) {
+    const long long row = u / n_groups, j = u - row * n_groups;
+    const long long src_tok = row * in_T + j * kG;
+    const long long un = u + gridDim.x;
+    // this unit's raw keys (its values may still be in flight); the
+    // barrier also ends the previous unit's reads of kt, P and ns
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) S.P.tiny = 0;
+    uint4 raw[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) raw[q] = reinterpret_cast<const uint4*>(&PS.kraw[tw][32 * Q])[q];
+    const long long head0_tok = src_tok - (row % Hkv) * (long long)in_T + tw;
+    rotate_token<kG, PLAIN>(S, raw, tw, k + head0_tok * kD, (long long)in_T * kD, Hkv, ks);
+    async_wait_all();
+    __syncthreads();
+    if (un < n_units) stage_rows<kG>(PS.kraw, k + src_tok_of(un) * kD);
+    uint8_t* rec = packed + (row * (T_cap / kG) + p0 / kG + j) * RB;
+    key_minmax_half<kG>(S.kt, S.mm);
+    value_block<BITS>(S.vt[0], S.ns, rec);
+    __syncthreads();
+    key_params<kG, BITS>(S.mm, S.P, [&](int) { return rec; });
+    __syncthreads();
+    if (un < n_units) stage_rows<kG>(S.vt[0], v + src_tok_of(un) * kD);
+    key_block<BITS>(S.kt, S.P, rec);
+  }
 }
 
 // ------------------------------------------------------------------ paged
@@ -325,13 +406,39 @@ cudaError_t prefill_kv_gp(const uint16_t* k, const uint16_t* v, int in_T, int n_
                           int Hkv, int T_cap, int p0, KeyScale ks, uint8_t* packed,
                           cudaStream_t s) {
   static int done[128] = {};
-  const size_t bytes = sizeof(GroupSmem<GS>);
-  cudaError_t e = allow_group_smem(prefill_kv_kernel<GS, BITS, PLAIN>, bytes, done);
-  if (e != cudaSuccess) return e;
-  dim3 grid(n_tok / GS, Hkv, B);
-  prefill_kv_kernel<GS, BITS, PLAIN><<<grid, 128, bytes, s>>>(k, v, in_T, Hkv, T_cap, p0, ks,
-                                                              packed);
-  return cudaGetLastError();
+  if constexpr (GS == kG) {
+    // persistent: as many CTAs as fit on the GPU at once (the count per
+    // device is found once), none more than the units
+    static int ctas[128] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    const size_t bytes = sizeof(PrefillSmem);
+    if (!ctas[dev]) {
+      int per_sm = 0, sms = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_kv_persistent<BITS, PLAIN>,
+                                                        128, bytes);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      ctas[dev] = std::max(1, per_sm) * std::max(1, sms);
+    }
+    const long long units = (long long)(n_tok / kG) * Hkv * B;
+    const int grid = (int)std::min<long long>(units, ctas[dev]);
+    if (grid <= 0) return cudaSuccess;
+    prefill_kv_persistent<BITS, PLAIN><<<grid, 128, bytes, s>>>(k, v, in_T, Hkv, n_tok / kG, units,
+                                                                T_cap, p0, ks, packed);
+    return cudaGetLastError();
+  } else {
+    const size_t bytes = sizeof(GroupSmem<GS>);
+    cudaError_t e = allow_group_smem(prefill_kv_kernel<GS, BITS, PLAIN>, bytes, done);
+    if (e != cudaSuccess) return e;
+    dim3 grid(n_tok / GS, Hkv, B);
+    prefill_kv_kernel<GS, BITS, PLAIN><<<grid, 128, bytes, s>>>(k, v, in_T, Hkv, T_cap, p0, ks,
+                                                                packed);
+    return cudaGetLastError();
+  }
 }
 template <int GS, int BITS>
 cudaError_t prefill_kv_g(const uint16_t* k, const uint16_t* v, int in_T, int n_tok, int B,

@@ -130,6 +130,16 @@ __device__ __forceinline__ float code_threshold(float step, int j) {
 __device__ __forceinline__ float code_by_thresholds(float a, float A0, float A1, float A2) {
   return (a >= A0 ? 1.0f : 0.0f) + (a >= A1 ? 1.0f : 0.0f) + (a >= A2 ? 1.0f : 0.0f);
 }
+// The same for two inputs at once: a = fl(x - mn) for both halves, the
+// flags added as pairs (the same sums in the same order as above).
+__device__ __forceinline__ float2 codes_by_thresholds2(float2 x, float2 mn, float2 A0, float2 A1,
+                                                       float2 A2) {
+  const float2 a = sub2(x, mn);
+  const float2 f0 = make_float2(a.x >= A0.x ? 1.0f : 0.0f, a.y >= A0.y ? 1.0f : 0.0f);
+  const float2 f1 = make_float2(a.x >= A1.x ? 1.0f : 0.0f, a.y >= A1.y ? 1.0f : 0.0f);
+  const float2 f2 = make_float2(a.x >= A2.x ? 1.0f : 0.0f, a.y >= A2.y ? 1.0f : 0.0f);
+  return add2(add2(f0, f1), f2);
+}
 
 // Weight of slot k of a half-word (2 or 4 bits per slot): the half-word is
 // the exact fp32 sum of c * 2^(BITS k), an integer below 2^16.
@@ -224,32 +234,43 @@ __device__ __forceinline__ __half2 channel_params(int c, float mn, float mx, Key
   return __halves2half2(__float2half_rn(step), __float2half_rn(mn));
 }
 
-// Step and zero of every key channel over the N tokens of kt: into P and,
-// as fp16, into the records rec_of(0 .. N/32 - 1).  Threads 0..63 take the
-// channel pairs 2t, 2t + 1 (min and max on packed bf16); the others return
-// at once.  P.tiny must have been cleared before the barrier that precedes
-// the call.
-template <int N, int BITS, class RecOf>
-__device__ __forceinline__ void key_params(const uint16_t (*kt)[kTileRow], KeyParamSmem& P,
-                                           RecOf rec_of) {
-  if (threadIdx.x >= kD / 2) return;
-  const int c2 = 2 * threadIdx.x;
-  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&kt[0][c2]), mx2 = mn2;
+// Per-channel min and max of the N tokens of kt, in two halves: thread t
+// scans rows N/2 (t >> 6) .. N/2 (t >> 6) + N/2 - 1 of channel pair t & 63
+// on packed bf16 and leaves its partial min and max in part[t].
+struct KeyMinMax {
+  __nv_bfloat162 mn, mx;
+};
+template <int N>
+__device__ __forceinline__ void key_minmax_half(const uint16_t (*kt)[kTileRow], KeyMinMax* part) {
+  const int t = threadIdx.x, c2 = 2 * (t & 63), r0 = (N / 2) * (t >> 6);
+  __nv_bfloat162 mn2 = *reinterpret_cast<const __nv_bfloat162*>(&kt[r0][c2]), mx2 = mn2;
 #pragma unroll 8
-  for (int t = 1; t < N; ++t) {
-    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&kt[t][c2]);
+  for (int r = 1; r < N / 2; ++r) {
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&kt[r0 + r][c2]);
     mn2 = __hmin2(mn2, x);
     mx2 = __hmax2(mx2, x);
   }
-  const __half2 p0 = channel_params<BITS>(c2, __low2float(mn2), __low2float(mx2), P);
-  const __half2 p1 = channel_params<BITS>(c2 + 1, __high2float(mn2), __high2float(mx2), P);
-  const __half2 steps = __lows2half2(p0, p1), zeros = __highs2half2(p0, p1);
+  part[t] = KeyMinMax{mn2, mx2};
+}
+
+// Step and zero of key channel 2 (t & 63) + (t >> 6) (one channel per
+// thread) from the two halves' partials of key_minmax_half: its parameters
+// into P and its fp16 step and zero into the records rec_of(0 .. N/32 - 1).
+// P.tiny must have been cleared before the barrier that precedes the call.
+template <int N, int BITS, class RecOf>
+__device__ __forceinline__ void key_params(const KeyMinMax* part, KeyParamSmem& P, RecOf rec_of) {
+  const int t = threadIdx.x, pr = t & 63, hi = t >> 6, c = 2 * pr + hi;
+  const KeyMinMax a = part[pr], b = part[pr + 64];
+  const __nv_bfloat162 mn2 = __hmin2(a.mn, b.mn), mx2 = __hmax2(a.mx, b.mx);
+  const float mn = hi ? __high2float(mn2) : __low2float(mn2);
+  const float mx = hi ? __high2float(mx2) : __low2float(mx2);
+  const __half2 sz = channel_params<BITS>(c, mn, mx, P);
   using RL = Rec<BITS>;
 #pragma unroll 1
   for (int sb = 0; sb < N / kG; ++sb) {
     uint8_t* rec = rec_of(sb);
-    reinterpret_cast<__half2*>(rec + RL::KS)[threadIdx.x] = steps;
-    reinterpret_cast<__half2*>(rec + RL::KZ)[threadIdx.x] = zeros;
+    reinterpret_cast<__half*>(rec + RL::KS)[c] = __low2half(sz);
+    reinterpret_cast<__half*>(rec + RL::KZ)[c] = __high2half(sz);
   }
 }
 
@@ -277,29 +298,33 @@ __device__ __forceinline__ void key_words(const uint16_t* row, int Q, const KeyP
   }
   const int q0 = param_slot(32 * Q);
   if constexpr (BITS == 2) {
-    float hw[2 * NW];
+    // channels e, e + 1 (e even) are one packed bf16 pair and land in the
+    // same slot of half-words 2k, 2k + 1 of word k = e / CW: one packed pair
+    // of accumulators per word
+    float2 hw[NW];
 #pragma unroll
-    for (int i = 0; i < 2 * NW; ++i) hw[i] = 0.0f;
+    for (int k = 0; k < NW; ++k) hw[k] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float4 m = reinterpret_cast<const float4*>(P.mn + q0)[i];
       const float4 t0 = reinterpret_cast<const float4*>(P.p[0] + q0)[i];
       const float4 t1 = reinterpret_cast<const float4*>(P.p[1] + q0)[i];
       const float4 t2 = reinterpret_cast<const float4*>(P.p[2] + q0)[i];
-      const float mv[4] = {m.x, m.y, m.z, m.w};
-      const float a0[4] = {t0.x, t0.y, t0.z, t0.w}, a1[4] = {t1.x, t1.y, t1.z, t1.w},
-                  a2[4] = {t2.x, t2.y, t2.z, t2.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int e = 4 * i + j, jw = e % CW, h = 2 * (e / CW) + (jw & 1);
-        const float x = (e & 1) ? bf16_hi(xr[e >> 1]) : bf16_lo(xr[e >> 1]);
-        hw[h] = fmaf(code_by_thresholds(__fsub_rn(x, mv[j]), a0[j], a1[j], a2[j]),
-                     slot_weight<BITS>(jw >> 1), hw[h]);
+      for (int jj = 0; jj < 2; ++jj) {
+        const int e = 4 * i + 2 * jj, k = e / CW;
+        const float wgt = slot_weight<BITS>((e % CW) >> 1);
+        const float2 mn = jj ? make_float2(m.z, m.w) : make_float2(m.x, m.y);
+        const float2 a0 = jj ? make_float2(t0.z, t0.w) : make_float2(t0.x, t0.y);
+        const float2 a1 = jj ? make_float2(t1.z, t1.w) : make_float2(t1.x, t1.y);
+        const float2 a2 = jj ? make_float2(t2.z, t2.w) : make_float2(t2.x, t2.y);
+        hw[k] = fma2(codes_by_thresholds2(bf16_pair(xr[e >> 1]), mn, a0, a1, a2),
+                     make_float2(wgt, wgt), hw[k]);
       }
     }
 #pragma unroll
     for (int k = 0; k < NW; ++k)
-      w[k] = __byte_perm(half_word_bits(hw[2 * k]), half_word_bits(hw[2 * k + 1]), 0x5410);
+      w[k] = __byte_perm(half_word_bits(hw[k].x), half_word_bits(hw[k].y), 0x5410);
   } else {
     float hw[2 * NW], d[2 * NW];
 #pragma unroll
@@ -374,21 +399,24 @@ __device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
     const float A0 = __shfl_sync(0xffffffffu, mine, lane & 7);
     const float A1 = __shfl_sync(0xffffffffu, mine, (lane & 7) + 8);
     const float A2 = __shfl_sync(0xffffffffu, mine, (lane & 7) + 16);
-    float H[2][NH];
+    // the pair u[m] holds channel 2Q + 8m (group 0) low and 2Q + 1 + 8m
+    // (group 1) high, at the same slot of half-words (0, hh) and (1, hh)
+    float2 H[NH];
 #pragma unroll
-    for (int g = 0; g < 2; ++g)
+    for (int hh = 0; hh < NH; ++hh) H[hh] = make_float2(0.0f, 0.0f);
+    const float2 mn2 = make_float2(mn, mn), A02 = make_float2(A0, A0), A12 = make_float2(A1, A1),
+                 A22 = make_float2(A2, A2);
 #pragma unroll
-      for (int hh = 0; hh < NH; ++hh) H[g][hh] = 0.0f;
+    for (int m = 0; m < 16; ++m) {
+      const float wgt = slot_weight<BITS>(m % PS);
+      H[m / PS] = fma2(codes_by_thresholds2(bf16_pair(u[m]), mn2, A02, A12, A22),
+                       make_float2(wgt, wgt), H[m / PS]);
+    }
 #pragma unroll
-    for (int g = 0; g < 2; ++g)
-#pragma unroll
-      for (int m = 0; m < 16; ++m)
-        H[g][m / PS] = fmaf(code_by_thresholds(__fsub_rn(xv(g, m), mn), A0, A1, A2),
-                            slot_weight<BITS>(m % PS), H[g][m / PS]);
-#pragma unroll
-    for (int g = 0; g < 2; ++g)
-#pragma unroll
-      for (int hh = 0; hh < NH; ++hh) Hb[g][hh] = half_word_bits(H[g][hh]);
+    for (int hh = 0; hh < NH; ++hh) {
+      Hb[0][hh] = half_word_bits(H[hh].x);
+      Hb[1][hh] = half_word_bits(H[hh].y);
+    }
   } else {
     const float rs = live ? __frcp_rn(step) : 0.0f;
     float H[2][NH], d[2][NH];
@@ -437,48 +465,54 @@ __device__ __forceinline__ void value_words(const uint16_t* row, int Q, int par,
   mn_out = mn;
 }
 
-// One 32-token block: keys from kt (32 rotated, scaled bf16 rows), values
-// from vt, key parameters in P, norms of the 32 tokens; writes the block's
-// codes, value steps and zeros and norms into the record (layout in oscar.h
-// for BITS; key_params writes the key steps and zeros).  Called by all 128
-// threads after a __syncthreads that follows the staging of kt, vt and P.
+// One 32-token block of values (vt: 32 rows) and the tokens' norms: its
+// value codes, steps and zeros and its norms into the record (layout in
+// oscar.h for BITS).  Called by all 128 threads once vt and the norms are
+// staged and synced; needs no key parameter.
 template <int BITS>
-__device__ __forceinline__ void quantize_block(const uint16_t (*kt)[kTileRow],
-                                               const uint16_t (*vt)[kTileRow],
-                                               const KeyParamSmem& P, const __half* norms,
-                                               uint8_t* rec) {
+__device__ __forceinline__ void value_block(const uint16_t (*vt)[kTileRow], const __half* norms,
+                                            uint8_t* rec) {
   using RL = Rec<BITS>;
   constexpr int NW = BITS == 2 ? 2 : 4;
   const int lane = threadIdx.x & 31, Q = lane >> 3;
   const int t = 8 * (threadIdx.x >> 5) + (lane & 7);
-  {
-    uint32_t w[NW];
-    float step, mn;
-    value_words<BITS>(vt[t], Q, t & 1, w, step, mn);
-    // word of (token pair, channel group g, hh = 0): INT2 128 kh + 4 (4g +
-    // t4) + 2p, INT4 256 kh + 128 p + 4 (4g + t4), the pair's first token
-    // being 16 kh + 2 t4 + 8 p
-    const int g = 2 * Q + (t & 1), kh = t >> 4, p = (t >> 3) & 1, t4 = (t >> 1) & 3;
-    uint32_t* vc = reinterpret_cast<uint32_t*>(rec + RL::VC);
-    if constexpr (BITS == 2) {
-      *reinterpret_cast<uint2*>(vc + 128 * kh + 4 * (4 * g + t4) + 2 * p) = make_uint2(w[0], w[1]);
-    } else {
-      *reinterpret_cast<uint4*>(vc + 256 * kh + 128 * p + 4 * (4 * g + t4)) =
-          make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    if (Q == 0) reinterpret_cast<__half*>(rec + RL::VS)[tok_slot(t)] = __float2half_rn(step);
-    if (Q == 1) reinterpret_cast<__half*>(rec + RL::VZ)[tok_slot(t)] = __float2half_rn(mn);
-    if (Q == 2) reinterpret_cast<__half*>(rec + RL::KN)[tok_slot(t)] = norms[t];
+  uint32_t w[NW];
+  float step, mn;
+  value_words<BITS>(vt[t], Q, t & 1, w, step, mn);
+  // word of (token pair, channel group g, hh = 0): INT2 128 kh + 4 (4g +
+  // t4) + 2p, INT4 256 kh + 128 p + 4 (4g + t4), the pair's first token
+  // being 16 kh + 2 t4 + 8 p
+  const int g = 2 * Q + (t & 1), kh = t >> 4, p = (t >> 3) & 1, t4 = (t >> 1) & 3;
+  uint32_t* vc = reinterpret_cast<uint32_t*>(rec + RL::VC);
+  if constexpr (BITS == 2) {
+    *reinterpret_cast<uint2*>(vc + 128 * kh + 4 * (4 * g + t4) + 2 * p) = make_uint2(w[0], w[1]);
+  } else {
+    *reinterpret_cast<uint4*>(vc + 256 * kh + 128 * p + 4 * (4 * g + t4)) =
+        make_uint4(w[0], w[1], w[2], w[3]);
   }
-  {
-    uint32_t w[NW];
-    key_words<BITS>(kt[t], Q, P, w);
-    uint32_t* kc = reinterpret_cast<uint32_t*>(rec + RL::KC) + t * 4 * NW + NW * Q;
-    if constexpr (BITS == 2) {
-      *reinterpret_cast<uint2*>(kc) = make_uint2(w[0], w[1]);
-    } else {
-      *reinterpret_cast<uint4*>(kc) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+  if (Q == 0) reinterpret_cast<__half*>(rec + RL::VS)[tok_slot(t)] = __float2half_rn(step);
+  if (Q == 1) reinterpret_cast<__half*>(rec + RL::VZ)[tok_slot(t)] = __float2half_rn(mn);
+  if (Q == 2) reinterpret_cast<__half*>(rec + RL::KN)[tok_slot(t)] = norms[t];
+}
+
+// One 32-token block of keys (kt: 32 rotated, scaled bf16 rows) with the
+// group's key parameters in P: its key codes into the record (key_params
+// writes the key steps and zeros).  Called by all 128 threads once P is
+// formed and synced.
+template <int BITS>
+__device__ __forceinline__ void key_block(const uint16_t (*kt)[kTileRow], const KeyParamSmem& P,
+                                          uint8_t* rec) {
+  using RL = Rec<BITS>;
+  constexpr int NW = BITS == 2 ? 2 : 4;
+  const int lane = threadIdx.x & 31, Q = lane >> 3;
+  const int t = 8 * (threadIdx.x >> 5) + (lane & 7);
+  uint32_t w[NW];
+  key_words<BITS>(kt[t], Q, P, w);
+  uint32_t* kc = reinterpret_cast<uint32_t*>(rec + RL::KC) + t * 4 * NW + NW * Q;
+  if constexpr (BITS == 2) {
+    *reinterpret_cast<uint2*>(kc) = make_uint2(w[0], w[1]);
+  } else {
+    *reinterpret_cast<uint4*>(kc) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 

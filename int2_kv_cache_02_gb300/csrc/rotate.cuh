@@ -38,24 +38,38 @@ __device__ __forceinline__ void fht128(float (&x)[4], int lane) {
 
 // The same transform in the quarter layout: index bits 0-4 butterflied in
 // registers (a + b and a - b, the roundings of the lane pairs above), bits 5
-// and 6 across lanes xor 8 and xor 16.
+// and 6 across lanes xor 8 and xor 16.  Elements 2i, 2i + 1 travel as one
+// packed pair from bit 1 on: a packed operation rounds each half as the
+// scalar one would, so the results are those of the scalar butterflies.
 __device__ __forceinline__ void fht128(float (&x)[32], int lane) {
 #pragma unroll
-  for (int h = 1; h < 32; h <<= 1)
+  for (int e = 0; e < 32; e += 2) {
+    const float a = x[e], b = x[e + 1];
+    x[e] = a + b;
+    x[e + 1] = a - b;
+  }
 #pragma unroll
-    for (int e = 0; e < 32; ++e)
+  for (int h = 2; h < 32; h <<= 1)
+#pragma unroll
+    for (int e = 0; e < 32; e += 2)
       if (!(e & h)) {
-        const float a = x[e], b = x[e + h];
-        x[e] = a + b;
-        x[e + h] = a - b;
+        const float2 a = make_float2(x[e], x[e + 1]), b = make_float2(x[e + h], x[e + h + 1]);
+        const float2 s = add2(a, b), d = sub2(a, b);
+        x[e] = s.x;
+        x[e + 1] = s.y;
+        x[e + h] = d.x;
+        x[e + h + 1] = d.y;
       }
 #pragma unroll
   for (int m = 8; m < 32; m <<= 1) {
     const float sg = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const float y = __shfl_xor_sync(0xffffffffu, x[e], m);
-      x[e] = fmaf(sg, x[e], y);
+    for (int e = 0; e < 32; e += 2) {
+      const float y0 = __shfl_xor_sync(0xffffffffu, x[e], m);
+      const float y1 = __shfl_xor_sync(0xffffffffu, x[e + 1], m);
+      const float2 r = fma2(make_float2(sg, sg), make_float2(x[e], x[e + 1]), make_float2(y0, y1));
+      x[e] = r.x;
+      x[e + 1] = r.y;
     }
   }
 }
@@ -132,6 +146,18 @@ __device__ __forceinline__ float all_heads_sq_q(const uint16_t* k0, long long he
   return s;
 }
 
+// x[r] *= f for every element, two at a time (each product rounded as the
+// scalar one).
+template <int N>
+__device__ __forceinline__ void scale_all(float (&x)[N], float f) {
+#pragma unroll
+  for (int r = 0; r < N; r += 2) {
+    const float2 p = mul2(make_float2(x[r], x[r + 1]), make_float2(f, f));
+    x[r] = p.x;
+    x[r + 1] = p.y;
+  }
+}
+
 // Rotates (unless OSCAR_NO_ROTATE) and scales (unless OSCAR_NO_SCALE) the key
 // held in x to the norm ks.target; returns the stored norm n / target, with n
 // the key's own norm or, with OSCAR_NORM_ALL_HEADS, the norm of the token's
@@ -150,17 +176,13 @@ __device__ __forceinline__ float rotate_scale_key(float (&x)[N], int lane, KeySc
   const bool rot = !(ks.flags & OSCAR_NO_ROTATE);
   if (rot) fht128(x, lane);
   if (ks.flags & OSCAR_NO_SCALE) {
-    const float f = rot ? kInvSqrtD : 1.0f;
-#pragma unroll
-    for (int r = 0; r < N; ++r) x[r] *= f;
+    scale_all(x, rot ? kInvSqrtD : 1.0f);
     return 1.0f;
   }
   const float s = (ks.flags & OSCAR_NORM_ALL_HEADS) ? (rot ? 128.0f * s_all : s_all) : sum_sq(x);
   if (s > 0.0f) {
     const bool unit = ks.target == 1.0f;   // the method's target: no extra rounding
-    const float f = unit ? rsqrtf(s) : rsqrtf(s) * ks.target;
-#pragma unroll
-    for (int r = 0; r < N; ++r) x[r] *= f;
+    scale_all(x, unit ? rsqrtf(s) : rsqrtf(s) * ks.target);
     const float n = sqrtf(s) * (rot ? kInvSqrtD : 1.0f);
     return unit ? n : n / ks.target;
   }
