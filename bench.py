@@ -938,15 +938,46 @@ def run_ours(args, world, rank, local):
         p_bytes = (sum(wl.Hkv * (n * 86 + 1 * 514) for n in n_tok_h)
                    + 2 * wl.B * wl.Hq * 128 * 4 + 2 * wl.B * wl.Hq * (Sp + 1) * 132 * 4)
         p_gbs = p_bytes / (p_ms * 1e-3) / 1e9
+        del pc, wsp
+        torch.cuda.empty_cache()
+        # the contiguous cache at the batch's mean length, timed the same way
+        n_mean = int(round(float(np.mean(n_tok_h)) / 32)) * 32
+        cm = L.KVCache(wl.B, wl.Hkv, n_mean + 128, device=dev)
+        L.prefill_kv(cm, K, V, n_tok=n_mean, in_T=wl.T0)
+        L.append_kv(cm, Kn[0], Vn[0], n_tok=1)
+        Sm = L.decode_num_splits(wl.B, wl.Hkv, wl.Hq, n_mean)
+        wsm = L.alloc_workspace(L.decode_workspace_bytes(wl.B, wl.Hkv, wl.Hq, n_mean, Sm),
+                                device=dev)
+        run_m = lambda: L.decode_attention(cm, qr, wl.Hq, tau, out, wsm, num_splits=Sm)
+        for _ in range(3):
+            run_m()
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(reps):
+            run_m()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        if L.device_status() != 0:
+            raise RuntimeError("contiguous decode recorded a device error")
+        m_ms = a.elapsed_time(b_) / reps
+        m_bytes = (wl.B * wl.Hkv * (n_mean * 86 + 514)
+                   + 2 * wl.B * wl.Hq * 128 * 4 + 2 * wl.B * wl.Hq * (Sm + 1) * 132 * 4)
+        m_gbs = m_bytes / (m_ms * 1e-3) / 1e9
+        del cm, wsm
+        torch.cuda.empty_cache()
         paged = {"sequences": wl.B, "packed_tokens_min": min(n_tok_h),
                  "packed_tokens_max": max_tok, "packed_tokens_mean": float(np.mean(n_tok_h)),
                  "pages": sum(blocks), "num_splits": Sp, "decode_us": p_ms * 1e3,
                  "GB/s": p_gbs, "frac": p_gbs / peak,
+                 "contiguous_at_mean": {"packed_tokens": n_mean, "num_splits": Sm,
+                                        "decode_us": m_ms * 1e3, "GB/s": m_gbs,
+                                        "frac": m_gbs / peak},
+                 "frac_vs_contiguous": p_gbs / m_gbs,
                  "note": "oscar_paged_decode_attention over per-sequence lengths drawn "
                          "uniformly in [n_packed/4, n_packed] (+1 residual token), pages "
-                         "handed out in a shuffled order"}
-        del pc, wsp
-        torch.cuda.empty_cache()
+                         "handed out in a shuffled order; contiguous_at_mean: "
+                         "oscar_decode_attention on a contiguous cache of the same batch with "
+                         "every sequence at the mean length"}
     # ---- INT4 option: the same prompt in 4800-byte records, decode only ----
     int4 = None
     if not args.no_int4 and wl.n_packed:

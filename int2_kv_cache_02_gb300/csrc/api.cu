@@ -54,37 +54,53 @@ oscar_status check_cache(const oscar_cache* c) {
   return OSCAR_OK;
 }
 
-// Split planning.  A launch runs rows * (s + 1) CTAs (s packed splits and
-// one residual split per row) spread over the SMs; the kernel is bound by
-// instruction issue, so an SM's time is the work of the CTAs it runs:
-// ceil(CTAs / SMs) x (blocks per split + a fixed start/merge overhead worth
-// kSplitOverheadBlocks blocks), slowed in proportion when it holds fewer
-// than kSaturatingWarps warps at once (too few to hide latency).  When the
-// packed CTAs fit in one wave of resident CTAs and only the residual CTAs (a
-// few microseconds each) would spill into a second, those are left out of
-// the count: they finish early and hold no slot for long.  Each warp keeps
-// at least kMinBlocksPerWarp blocks: shorter ranges measured slower.  A grid
-// that fits in one wave may go down to kMinBlocksPerWarpOneWave blocks per
-// warp: there the row is latency-bound and more warps on it shorten it (a
-// 1K-token single-head row: 12.3 us at 3 splits against 14.4 us at 1).  Ties
-// keep fewer splits.
+// Split planning.  A launch runs rows * (s + 1) CTAs: s packed splits of
+// about nblk / s blocks per row, whose four warps take a quarter each, and
+// one short residual split per row, in grid order with a row's CTAs
+// adjacent.  The planner models the launch's time for each s and takes the
+// cheapest:
+//  * One wave (rows * s packed CTAs fit in the resident slots): one packed
+//    CTA's time, (kFixedBlocks + blocks per warp) x the time a warp takes
+//    per block when n CTAs share its SM, n the most CTAs any SM gets
+//    (ceil(rows * (s + 1) / SMs): the residual CTAs sit between the packed
+//    ones in grid order, so an SM's share may be all packed).  kBlockUs holds
+//    those per-block times for n = 1..4: the SM's issue slots are shared, so
+//    a warp runs slower as more warps share them, but the SM's throughput
+//    still rises up to four CTAs.  If the residual CTAs spill past the wave,
+//    kLateUs more.
+//  * More waves: the same per-CTA time at four CTAs per SM times the waves
+//    W = rows * s / slots, plus kTailShare of a wave for the unfilled part
+//    of the last one (CTAs of unequal start times fill it partly).
+//  * Plus kCombineUsPerSplit per split for the combine of the row's
+//    partials, which runs after the row's last CTA.
+// Each warp keeps at least kMinBlocksPerWarp blocks when the packed CTAs
+// take more than one wave, and kMinBlocksPerWarpOneWave within one wave.
+// Ties keep fewer splits.
+//
+// The constants are fitted to sweeps of split counts on GB300 (152 SMs,
+// four INT2 decode CTAs per SM; L2 flushed for the shapes that fit in it):
+// 19 shapes from 1 to 384 rows and 128 to 4096 blocks (batch 1-48, 4K-128K
+// tokens, 32/8 and 32/4 heads).  The planned count is within 2.2 % of the
+// fastest swept count on every one (0.3 % on average).  The earlier model,
+// ceil(CTAs / SMs) x (blocks + 32) at full speed from two CTAs per SM on,
+// planned 1 split for batch 48 at 16K-112K tokens, 1.4-1.6 x slower than the
+// best count.
 //
 // On grids of more than two waves, an even count that wins is then compared
 // with its odd neighbours, and the cheaper of them is taken if its modelled
-// cost is within kEvenSplitPenalty of the winner's: there, on GB300, every
-// even count from 10 to 28 measured 1.2-1.5 % slower than its odd
-// neighbours (batch 48 x 128K: 12 splits 982 us, 11 and 13 splits 969-972
-// us), with the residual CTA placed anywhere in the row, with a padded grid
-// and without the combine; the cause is not known.
-//
-// Measured on GB300 in sweeps of split counts: batch 1 x 128K plans 37, the
-// best; batch 8 x 32K plans 9, the best (59 us against 63.5 at 6); the g = 8
-// batch-16 64K workload plans 9, the best (145 us against 160-180 at 6-12); batch
-// 48 x 128K plans 13, the best.
-constexpr long long kSplitOverheadBlocks = 32;
+// cost is within kEvenSplitPenalty of the winner's: there, on GB300, even
+// counts measured 1-3 % slower than their odd neighbours (batch 48 x 128K:
+// 12 splits 982 us, 11 and 13 splits 969-972 us; batch 48 x 80K: 8 and 10
+// splits 632 and 628 us, 9 splits 618 us), with the residual CTA placed
+// anywhere in the row, with a padded grid and without the combine; the
+// cause is not known.
+constexpr double kBlockUs[5] = {0.0, 0.60, 0.80, 1.20, 1.55};
+constexpr double kFixedBlocks = 1.0;
+constexpr double kTailShare = 0.4;
+constexpr double kLateUs = 1.5;
+constexpr double kCombineUsPerSplit = 0.05;
 constexpr long long kMinBlocksPerWarp = 16;
 constexpr long long kMinBlocksPerWarpOneWave = 2;
-constexpr int kSaturatingWarps = 8;
 constexpr int kWarpsPerCta = 4;
 constexpr double kEvenSplitPenalty = 1.02;
 
@@ -96,28 +112,32 @@ int plan_splits_for(long long rows, long long nblk, int ctas_per_sm, int sms, in
   const long long most1 = std::max<long long>(1, nblk / (kWarpsPerCta * kMinBlocksPerWarpOneWave));
   const int hi = (int)std::min<long long>(max_splits, most);
   const int hi1 = (int)std::min<long long>(max_splits, most1);
-  auto ctas_of = [&](int s) {
-    const long long packed = rows * s;
-    return packed <= slots && rows * (s + 1) > slots ? packed : rows * (s + 1);
-  };
+  auto block_us = [&](long long n) { return kBlockUs[std::min<long long>(std::max<long long>(n, 1), 4)]; };
   auto cost_of = [&](int s) {
-    const long long per_sm = (ctas_of(s) + sms - 1) / sms;   // CTAs of the busiest SM
-    const long long resident = std::min(per_sm, cps);
-    const double rate = std::min(1.0, (double)(resident * kWarpsPerCta) / kSaturatingWarps);
-    const long long per = (nblk + s - 1) / s;
-    return (double)per_sm * (double)(per + kSplitOverheadBlocks) / rate;
+    const double per_warp = (double)nblk / s / kWarpsPerCta;
+    const double waves = (double)(rows * s) / (double)slots;
+    double t;
+    if (waves <= 1.0) {
+      const long long n = std::min(cps, (rows * (s + 1) + sms - 1) / sms);
+      t = (kFixedBlocks + per_warp) * block_us(n);
+      if (rows * (s + 1) > slots) t += kLateUs;
+    } else {
+      const double d = (kFixedBlocks + per_warp) * block_us(cps);
+      t = d * (waves + kTailShare * (std::ceil(waves) - waves));
+    }
+    return t + kCombineUsPerSplit * (s + 1);
   };
   int best = 1;
-  double best_cost = 1e300;
-  for (int s = 1; s <= hi1; ++s) {
-    if (s > hi && rows * (s + 1) > slots) break;   // beyond one wave: longer ranges only
+  double best_cost = cost_of(1);
+  for (int s = 2; s <= hi1; ++s) {
+    if (s > hi && rows * s > slots) continue;   // short ranges only within one wave
     const double cost = cost_of(s);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = s;
     }
   }
-  if (best % 2 == 0 && ctas_of(best) > 2 * slots) {
+  if (best % 2 == 0 && rows * (best + 1) > 2 * slots) {
     int odd = 0;
     double odd_cost = 1e300;
     for (int s : {best - 1, best + 1}) {
