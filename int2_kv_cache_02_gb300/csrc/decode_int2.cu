@@ -1166,24 +1166,53 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
     mr[j] = -INFINITY; lr[j] = 0.0f;
     orr[j][0] = orr[j][1] = orr[j][2] = orr[j][3] = 0.0f;
   }
-  for (int t = warp; t < n_res; t += NW) {
-    const long long tok = row * kR + t;
-    const uint2 kr = reinterpret_cast<const uint2*>(a.k_res + tok * kD)[lane];
-    const uint2 vr = reinterpret_cast<const uint2*>(a.v_res + tok * kD)[lane];
-    const float k4[4] = {bf16_lo(kr.x), bf16_hi(kr.x), bf16_lo(kr.y), bf16_hi(kr.y)};
-    const float v4[4] = {bf16_lo(vr.x), bf16_hi(vr.x), bf16_lo(vr.y), bf16_hi(vr.y)};
-    const float nrm = __half2float(a.k_res_norm[tok]);
+  // Warp w takes tokens TU w .. TU w + TU - 1, then TU (w + NW) .., TU at a
+  // time (4, or 2 for groups of 8, which hold twice the query registers):
+  // their TU x GQ dot products reduce across the warp as independent chains,
+  // and the running maximum is raised once per TU tokens.
+  constexpr int TU = GQ >= 8 ? 2 : 4;
+  for (int t0 = TU * warp; t0 < n_res; t0 += TU * NW) {
+    float k4[TU][4], v4[TU][4], nrm[TU];
+#pragma unroll
+    for (int u = 0; u < TU; ++u) {
+      const long long tok = row * kR + min(t0 + u, n_res - 1);
+      const uint2 kr = reinterpret_cast<const uint2*>(a.k_res + tok * kD)[lane];
+      const uint2 vr = reinterpret_cast<const uint2*>(a.v_res + tok * kD)[lane];
+      k4[u][0] = bf16_lo(kr.x); k4[u][1] = bf16_hi(kr.x); k4[u][2] = bf16_lo(kr.y); k4[u][3] = bf16_hi(kr.y);
+      v4[u][0] = bf16_lo(vr.x); v4[u][1] = bf16_hi(vr.x); v4[u][2] = bf16_lo(vr.y); v4[u][3] = bf16_hi(vr.y);
+      nrm[u] = __half2float(a.k_res_norm[tok]);
+    }
+    float d[TU][GQ];
+#pragma unroll
+    for (int u = 0; u < TU; ++u)
+#pragma unroll
+      for (int j = 0; j < GQ; ++j)
+        d[u][j] = qv[j][0] * k4[u][0] + qv[j][1] * k4[u][1] + qv[j][2] * k4[u][2] + qv[j][3] * k4[u][3];
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1)
+#pragma unroll
+      for (int u = 0; u < TU; ++u)
+#pragma unroll
+        for (int j = 0; j < GQ; ++j) d[u][j] += __shfl_xor_sync(0xffffffffu, d[u][j], m);
 #pragma unroll
     for (int j = 0; j < GQ; ++j) {
-      float d = qv[j][0] * k4[0] + qv[j][1] * k4[1] + qv[j][2] * k4[2] + qv[j][3] * k4[3];
-      d = warp_allsum(d);
-      const float s = d * nrm * a.scale_log2;
-      const float m_new = fmaxf(mr[j], s);
-      const float al = fast_exp2(mr[j] - m_new);
-      const float p = fast_exp2(s - m_new);
-      lr[j] = lr[j] * al + p;
+      float sc[TU], m_new = mr[j];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) orr[j][i] = orr[j][i] * al + p * v4[i];
+      for (int u = 0; u < TU; ++u) {
+        sc[u] = t0 + u < n_res ? d[u][j] * nrm[u] * a.scale_log2 : -INFINITY;
+        m_new = fmaxf(m_new, sc[u]);
+      }
+      const float al = fast_exp2(mr[j] - m_new);
+      lr[j] *= al;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) orr[j][i] *= al;
+#pragma unroll
+      for (int u = 0; u < TU; ++u) {
+        const float p = fast_exp2(sc[u] - m_new);
+        lr[j] += p;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) orr[j][i] = fmaf(p, v4[u][i], orr[j][i]);
+      }
       mr[j] = m_new;
     }
   }
@@ -1329,8 +1358,23 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 || BITS == 2 ? 4 : 3) decode_
   auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
   static_assert(sizeof(MergeSmem<GQ, NW>) <= NW * Layout<BITS>::NSTAGE * Layout<BITS>::RL::BYTES,
                 "merge area");
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const long long row = (long long)b * a.Hkv + h;
+  // One-dimensional grid, the residual CTAs first: CTA L < rows is row L's
+  // residual split, and the others take the packed splits row by row.  So
+  // every residual CTA starts in the first wave, where its work (up to a
+  // full 128-token window) runs beside the packed CTAs instead of after
+  // them at the end of a many-wave grid.
+  const long long rows = (long long)a.B * a.Hkv;
+  long long row;
+  int split;
+  if ((long long)blockIdx.x < rows) {
+    row = blockIdx.x;
+    split = a.num_splits;
+  } else {
+    const long long q = (long long)blockIdx.x - rows;
+    row = q / a.num_splits;
+    split = (int)(q - row * a.num_splits);
+  }
+  const int b = (int)(row / a.Hkv), h = (int)(row - (long long)b * a.Hkv);
   const long long qrow0 = (long long)b * a.Hq + (long long)h * GQ;  // first query head
 
   if (split < a.num_splits) {
@@ -1396,7 +1440,9 @@ template <int GQ, bool PAGED, bool BSCALE, int BITS>
 cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t e0 = allow_smem<GQ, PAGED, BSCALE, BITS>();
   if (e0 != cudaSuccess) return e0;
-  dim3 grid(a.num_splits + 1, a.Hkv, a.B);
+  const long long ctas = (long long)a.B * a.Hkv * (a.num_splits + 1);
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const dim3 grid((unsigned)ctas);
   const int smem = smem_bytes<GQ, BITS>() + (a.q_raw != nullptr ? kQRotStage : 0);
   decode_int2_kernel<GQ, PAGED, BSCALE, BITS><<<grid, NW * 32, smem, s>>>(a);
   return cudaGetLastError();
