@@ -1059,7 +1059,7 @@ def run_ours(args, world, rank, local):
                      "frac": achieved / peak, "peak_source": peak_src, "traffic": traffic,
                      "peak_note": "the measured copy bandwidth (read + write); a read-only "
                                   "stream can exceed it slightly (this library's INT4 decode "
-                                  "reads at 1.02-1.03 of it), while torch.sum's read stream "
+                                  "reads at 1.02-1.04 of it), while torch.sum's read stream "
                                   "(read_only_peak) stays just below it",
                      "read_only_peak": {"GB/s": read_peak, "frac": achieved / read_peak,
                                         "how": "torch.sum over 4 GiB of fp32 on this GPU, "
