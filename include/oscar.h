@@ -159,7 +159,7 @@ typedef struct {
   int max_blocks;           /* row length of block_table */
   int n_pages;              /* pages in the pool (page ids 0..n_pages-1) */
   uint8_t* pages;           /* [n_pages][Hkv] records of OSCAR_BLOCK_BYTES */
-  int32_t* block_table;     /* device [B][max_blocks] page ids */
+  int32_t* block_table;     /* device [B][max_blocks] page ids (B * max_blocks < 2^31) */
   int32_t* n_packed;        /* device [B] */
   int32_t* n_res;           /* device [B] */
   oscar_bf16* k_res;        /* [B][Hkv][128][128] */

@@ -449,6 +449,8 @@ oscar_status check_paged(const oscar_paged_cache* c) {
   if (!c) return OSCAR_ERR_INVALID_ARG;
   if (c->B <= 0 || c->Hkv <= 0 || c->max_blocks <= 0 || c->n_pages <= 0)
     return OSCAR_ERR_INVALID_ARG;
+  // the kernels index the block table with 32-bit entry numbers
+  if ((long long)c->B * c->max_blocks > 0x7fffffffLL) return OSCAR_ERR_UNSUPPORTED;
   const void* p16[] = {c->pages, c->k_res, c->v_res, c->k_res_norm};
   for (const void* p : p16) {
     if (!p) return OSCAR_ERR_INVALID_ARG;

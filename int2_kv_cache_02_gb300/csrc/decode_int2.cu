@@ -257,26 +257,26 @@ struct WarpRing {
   const uint8_t* src;   // record of the range's first block (contiguous cache)
   int n;                // blocks in the range
   int lane;
-  // paged cache: the range's block-table entries, and the row's record in
-  // page 0 and the page stride, so that a record's address is one 32 x 32
-  // -> 64-bit multiply-add (the pool's size and the status word are read
-  // from the launch arguments where they are used)
-  const int32_t* tab;
-  const uint8_t* pages_h;   // record of the row's KV head in page 0
-  unsigned page_stride;     // bytes per page (Hkv records)
+  // paged cache: the index of the range's first block-table entry and the
+  // offset of the row's KV head within a page; the table, the pool and the
+  // page stride are read from the launch arguments where they are used, so
+  // the loop keeps two 32-bit values for paging (a record's address is one
+  // 32 x 32 -> 64-bit multiply-add onto the pool)
+  int tab_i;                // the range's first entry in the block table
+  unsigned hoff;            // the row's KV head record within a page (bytes)
 
   // Page id of block i of the range (paged cache; 0 past the range's end or
   // for a contiguous cache).  Loaded when block i - NSTAGE is taken up, so
   // the load's latency is hidden by that block's work.
-  __device__ __forceinline__ int page_of(int i) const {
-    if constexpr (PAGED) return i < n ? __ldg(tab + i) : 0;
+  __device__ __forceinline__ int page_of(int i, const DecodeArgs& a) const {
+    if constexpr (PAGED) return i < n ? __ldg(a.block_table + (tab_i + i)) : 0;
     else return 0;
   }
   // Record of block i of the range, `page` its page id (paged cache; the
   // range's ids were checked against the pool when the ring was made).
   __device__ __forceinline__ const uint8_t* record(int i, int page, const DecodeArgs& a) const {
     if constexpr (PAGED) {
-      return pages_h + (unsigned long long)(unsigned)page * page_stride;
+      return a.packed + ((unsigned long long)(unsigned)page * ((unsigned)a.Hkv * (unsigned)RB) + hoff);
     } else {
       return src + (long long)i * RB;
     }
@@ -289,7 +289,7 @@ struct WarpRing {
       mbar_fence_init();
     }
     __syncwarp();
-    for (int i = 0; i < NSTAGE && i < n; ++i) issue(i, page_of(i), a);
+    for (int i = 0; i < NSTAGE && i < n; ++i) issue(i, page_of(i, a), a);
   }
   __device__ __forceinline__ void issue(int i, int page, const DecodeArgs& a) const {
     // Every lane forms the (warp-uniform) addresses; one lane chosen by
@@ -385,14 +385,13 @@ __device__ __forceinline__ WarpRing<PAGED, BITS> make_ring(const DecodeArgs& a, 
   r.src = a.packed + (row * (long long)(a.T_cap / kG) + wb0) * RB;
   r.n = wb1 - wb0;
   r.lane = threadIdx.x & 31;
-  r.tab = PAGED ? a.block_table + (long long)b * a.max_blocks + wb0 : nullptr;
-  r.pages_h = a.packed + (long long)h * RB;
-  r.page_stride = (unsigned)a.Hkv * (unsigned)RB;
+  r.tab_i = PAGED ? b * a.max_blocks + wb0 : 0;
+  r.hoff = (unsigned)h * (unsigned)RB;
   if constexpr (PAGED) {
     // Every page id of the range is checked once, before any copy: one out
     // of range is reported and the warp reads nothing (its result is void).
     bool bad = false;
-    for (int j = r.lane; j < r.n; j += 32) bad |= (unsigned)__ldg(r.tab + j) >= (unsigned)a.n_pages;
+    for (int j = r.lane; j < r.n; j += 32) bad |= (unsigned)__ldg(a.block_table + (r.tab_i + j)) >= (unsigned)a.n_pages;
     if (__any_sync(0xffffffffu, bad)) {
       if (r.lane == 0) record_error(a.status, kDevErrBadPaged);
       r.n = 0;
@@ -574,7 +573,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   int it = 0;
   for (; it < R.n; ++it) {
     if (!R.wait(it)) break;
-    const int page_next = R.page_of(it + Ring::NSTAGE);
+    const int page_next = R.page_of(it + Ring::NSTAGE, a);
     const uint8_t* st = R.slot(it);
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + RL::KC);
     const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + RL::VC);
@@ -879,7 +878,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
   int it = 0;
   for (; it < R.n; ++it) {
     if (!R.wait(it)) break;
-    const int page_next = R.page_of(it + Ring::NSTAGE);
+    const int page_next = R.page_of(it + Ring::NSTAGE, a);
     const uint8_t* st = R.slot(it);
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + RL::KC);
     const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + RL::VC);

@@ -208,6 +208,11 @@ def test_paged_validation():
                                           P(FAKE), 1 << 20, None) == 1
     assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, 64, P(FAKE), 2,
                                           P(FAKE), 10, None) == 5
+    # a block table of 2^31 entries or more (the kernels index it in 32 bits)
+    big = _paged(B=2, max_blocks=1 << 30)
+    assert L.oscar_paged_append_kv(ctypes.byref(big), P(FAKE), P(FAKE), None, None) == 2
+    assert L.oscar_paged_decode_attention(ctypes.byref(big), P(FAKE), 8, 0.1, 64, P(FAKE), 0,
+                                          P(FAKE), 1 << 20, None) == 2
 
 
 @no_gpu_only
