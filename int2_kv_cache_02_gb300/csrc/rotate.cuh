@@ -26,12 +26,16 @@ __device__ __forceinline__ void fht128(float (&x)[4], int lane) {
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
     // upper lanes take y - x, lower lanes x + y: one fma with a +-1 factor,
-    // the same single rounding as the subtraction or the addition
+    // the same single rounding as the subtraction or the addition (two
+    // elements per packed fma)
     const float sg = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float y = __shfl_xor_sync(0xffffffffu, x[r], m);
-      x[r] = fmaf(sg, x[r], y);
+    for (int r = 0; r < 4; r += 2) {
+      const float y0 = __shfl_xor_sync(0xffffffffu, x[r], m);
+      const float y1 = __shfl_xor_sync(0xffffffffu, x[r + 1], m);
+      const float2 v = fma2(make_float2(sg, sg), make_float2(x[r], x[r + 1]), make_float2(y0, y1));
+      x[r] = v.x;
+      x[r + 1] = v.y;
     }
   }
 }
