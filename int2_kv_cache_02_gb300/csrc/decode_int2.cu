@@ -4,9 +4,10 @@
 // Cache Quantization in LLMs and Beyond", II. End-to-End Flow and III.
 // Efficiency: "Q.K^T and dequantization fused into a single kernel").
 //
-// Grid (num_splits + 1, Hkv, B): CTA (s, h, b) with s < num_splits streams an
-// equal share of the 32-token blocks of row (b, h); CTA num_splits handles the
-// residual window.  Each CTA writes one log-sum-exp partial per query head
+// One-dimensional grid of B * Hkv * (num_splits + 1) CTAs: the first B * Hkv
+// handle the residual windows of rows (b, h), so they all start in the first
+// wave; the others, row by row, each stream an equal share of the 32-token
+// blocks of their row.  Each CTA writes one log-sum-exp partial per query head
 // and counts itself in the row's arrival counter; the row's last CTA to
 // arrive folds the row's partials into the output (row_combine) and resets
 // the counter, so no second kernel is launched.
