@@ -239,12 +239,6 @@ __device__ __forceinline__ void unpack_h4(float (&f)[4], uint32_t ab, uint32_t c
   f[0] = x.x; f[1] = x.y; f[2] = y.x; f[3] = y.y;
 }
 
-__device__ __forceinline__ float warp_allsum(float v) {
-#pragma unroll
-  for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
-  return v;
-}
-
 // One warp's contiguous range of a row's 32-token blocks, streamed through
 // the warp's own NSTAGE-deep ring: one elected lane copies block i's record
 // into slot i % NSTAGE with one 1-D bulk copy completing on that slot's
@@ -1157,63 +1151,140 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
     __syncthreads();
   }
   // Unit-norm bf16 keys times their fp16 norms, bf16 values; CUDA cores.
-  float qv[GQ][4], mr[GQ], lr[GQ], orr[GQ][4];
+  float mr[GQ], lr[GQ], orr[GQ][4];
 #pragma unroll
   for (int j = 0; j < GQ; ++j) {
-    const float4 v = a.q_raw != nullptr ? rotated_query(a, qrow0 + j, lane)
-                                        : reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
-    qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
-    mr[j] = -INFINITY; lr[j] = 0.0f;
+    mr[j] = -INFINITY;
+    lr[j] = 0.0f;
     orr[j][0] = orr[j][1] = orr[j][2] = orr[j][3] = 0.0f;
   }
-  // Warp w takes tokens TU w .. TU w + TU - 1, then TU (w + NW) .., TU at a
-  // time (4, or 2 for groups of 8, which hold twice the query registers):
-  // their TU x GQ dot products reduce across the warp as independent chains,
-  // and the running maximum is raised once per TU tokens.
-  constexpr int TU = GQ >= 8 ? 2 : 4;
-  for (int t0 = TU * warp; t0 < n_res; t0 += TU * NW) {
-    float k4[TU][4], v4[TU][4], nrm[TU];
-#pragma unroll
-    for (int u = 0; u < TU; ++u) {
-      const long long tok = row * kR + min(t0 + u, n_res - 1);
-      const uint2 kr = reinterpret_cast<const uint2*>(a.k_res + tok * kD)[lane];
-      const uint2 vr = reinterpret_cast<const uint2*>(a.v_res + tok * kD)[lane];
-      k4[u][0] = bf16_lo(kr.x); k4[u][1] = bf16_hi(kr.x); k4[u][2] = bf16_lo(kr.y); k4[u][3] = bf16_hi(kr.y);
-      v4[u][0] = bf16_lo(vr.x); v4[u][1] = bf16_hi(vr.x); v4[u][2] = bf16_lo(vr.y); v4[u][3] = bf16_hi(vr.y);
-      nrm[u] = __half2float(a.k_res_norm[tok]);
+  if constexpr (GQ == 8) {
+    // Groups of 8: warp w takes the window's tokens 32 w .. 32 w + 31 (the
+    // window holds at most NW * 32 = R of them), one pass, no cross-lane sums
+    // for the scores (8 heads would need 8 reduction chains per token):
+    //  * Q.K with a token per lane: lane t reads its key row and forms all GQ
+    //    dot products over the 128 channels against the queries, which every
+    //    lane reads from shared memory (the ring area, unused by this CTA);
+    //  * the warp's maximum and sum of each head's weights (five shuffles);
+    //  * P.V with four channels per lane: each token's weights reach the
+    //    lanes by shuffle, its value row is one 8-byte load per lane.
+    static_assert(kR == NW * 32, "one 32-token slice of the window per warp");
+    float* qs = reinterpret_cast<float*>(dyn_smem());   // [GQ][128] fp32
+    for (int i = threadIdx.x; i < GQ * 32; i += NW * 32) {   // every lane of a warp alike
+      const int j = i >> 5;
+      const float4 v = a.q_raw != nullptr ? rotated_query(a, qrow0 + j, lane)
+                                          : reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
+      reinterpret_cast<float4*>(qs)[i] = v;
     }
-    float d[TU][GQ];
+    __syncthreads();
+    const int t0 = 32 * warp, nt = min(32, n_res - t0);   // this warp's tokens (warp-uniform)
+    if (nt > 0) {
+      const bool mine = lane < nt;
+      const long long tok = row * kR + t0 + (mine ? lane : 0);
+      float d[GQ];
 #pragma unroll
-    for (int u = 0; u < TU; ++u)
+      for (int j = 0; j < GQ; ++j) d[j] = 0.0f;
+      const uint4* kr = reinterpret_cast<const uint4*>(a.k_res + tok * kD);
+      const float4* q4 = reinterpret_cast<const float4*>(qs);
+#pragma unroll 4
+      for (int c8 = 0; c8 < kD / 8; ++c8) {
+        const uint4 u = kr[c8];
+        const float k8[8] = {bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y),
+                             bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w)};
 #pragma unroll
-      for (int j = 0; j < GQ; ++j)
-        d[u][j] = qv[j][0] * k4[u][0] + qv[j][1] * k4[u][1] + qv[j][2] * k4[u][2] + qv[j][3] * k4[u][3];
+        for (int j = 0; j < GQ; ++j) {
+          const float4 qa = q4[j * 32 + 2 * c8], qb = q4[j * 32 + 2 * c8 + 1];
+          d[j] = fmaf(k8[0], qa.x, d[j]); d[j] = fmaf(k8[1], qa.y, d[j]);
+          d[j] = fmaf(k8[2], qa.z, d[j]); d[j] = fmaf(k8[3], qa.w, d[j]);
+          d[j] = fmaf(k8[4], qb.x, d[j]); d[j] = fmaf(k8[5], qb.y, d[j]);
+          d[j] = fmaf(k8[6], qb.z, d[j]); d[j] = fmaf(k8[7], qb.w, d[j]);
+        }
+      }
+      const float nrm = __half2float(a.k_res_norm[tok]);
+      float p[GQ];
 #pragma unroll
-    for (int m = 16; m > 0; m >>= 1)
+      for (int j = 0; j < GQ; ++j) {
+        const float sc = mine ? d[j] * nrm * a.scale_log2 : -INFINITY;
+        float m = sc;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        p[j] = fast_exp2(sc - m);
+        float l = p[j];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        mr[j] = m;
+        lr[j] = l;
+      }
+      const uint2* vr = reinterpret_cast<const uint2*>(a.v_res + (row * kR + t0) * kD) + lane;
+#pragma unroll 4
+      for (int u = 0; u < nt; ++u) {
+        const uint2 w = vr[u * (kD / 4)];
+        const float v4[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+#pragma unroll
+        for (int j = 0; j < GQ; ++j) {
+          const float pj = __shfl_sync(0xffffffffu, p[j], u);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) orr[j][i] = fmaf(pj, v4[i], orr[j][i]);
+        }
+      }
+    }
+  } else {
+    // Groups of up to 4: channels 4l .. 4l + 3 per lane, warp w takes tokens
+    // 4 w .. 4 w + 3, then 4 (w + NW) .., four at a time: their 4 x GQ dot
+    // products reduce across the warp as independent chains, and the running
+    // maximum is raised once per four tokens.
+    float qv[GQ][4];
+#pragma unroll
+    for (int j = 0; j < GQ; ++j) {
+      const float4 v = a.q_raw != nullptr ? rotated_query(a, qrow0 + j, lane)
+                                          : reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
+      qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
+    }
+    constexpr int TU = 4;
+    for (int t0 = TU * warp; t0 < n_res; t0 += TU * NW) {
+      float k4[TU][4], v4[TU][4], nrm[TU];
+#pragma unroll
+      for (int u = 0; u < TU; ++u) {
+        const long long tok = row * kR + min(t0 + u, n_res - 1);
+        const uint2 kr = reinterpret_cast<const uint2*>(a.k_res + tok * kD)[lane];
+        const uint2 vr = reinterpret_cast<const uint2*>(a.v_res + tok * kD)[lane];
+        k4[u][0] = bf16_lo(kr.x); k4[u][1] = bf16_hi(kr.x); k4[u][2] = bf16_lo(kr.y); k4[u][3] = bf16_hi(kr.y);
+        v4[u][0] = bf16_lo(vr.x); v4[u][1] = bf16_hi(vr.x); v4[u][2] = bf16_lo(vr.y); v4[u][3] = bf16_hi(vr.y);
+        nrm[u] = __half2float(a.k_res_norm[tok]);
+      }
+      float d[TU][GQ];
 #pragma unroll
       for (int u = 0; u < TU; ++u)
 #pragma unroll
-        for (int j = 0; j < GQ; ++j) d[u][j] += __shfl_xor_sync(0xffffffffu, d[u][j], m);
+        for (int j = 0; j < GQ; ++j)
+          d[u][j] = qv[j][0] * k4[u][0] + qv[j][1] * k4[u][1] + qv[j][2] * k4[u][2] + qv[j][3] * k4[u][3];
 #pragma unroll
-    for (int j = 0; j < GQ; ++j) {
-      float sc[TU], m_new = mr[j];
+      for (int m = 16; m > 0; m >>= 1)
 #pragma unroll
-      for (int u = 0; u < TU; ++u) {
-        sc[u] = t0 + u < n_res ? d[u][j] * nrm[u] * a.scale_log2 : -INFINITY;
-        m_new = fmaxf(m_new, sc[u]);
+        for (int u = 0; u < TU; ++u)
+#pragma unroll
+          for (int j = 0; j < GQ; ++j) d[u][j] += __shfl_xor_sync(0xffffffffu, d[u][j], m);
+#pragma unroll
+      for (int j = 0; j < GQ; ++j) {
+        float sc[TU], m_new = mr[j];
+#pragma unroll
+        for (int u = 0; u < TU; ++u) {
+          sc[u] = t0 + u < n_res ? d[u][j] * nrm[u] * a.scale_log2 : -INFINITY;
+          m_new = fmaxf(m_new, sc[u]);
+        }
+        const float al = fast_exp2(mr[j] - m_new);
+        lr[j] *= al;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) orr[j][i] *= al;
+#pragma unroll
+        for (int u = 0; u < TU; ++u) {
+          const float p = fast_exp2(sc[u] - m_new);
+          lr[j] += p;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) orr[j][i] = fmaf(p, v4[u][i], orr[j][i]);
+        }
+        mr[j] = m_new;
       }
-      const float al = fast_exp2(mr[j] - m_new);
-      lr[j] *= al;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) orr[j][i] *= al;
-#pragma unroll
-      for (int u = 0; u < TU; ++u) {
-        const float p = fast_exp2(sc[u] - m_new);
-        lr[j] += p;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) orr[j][i] = fmaf(p, v4[u][i], orr[j][i]);
-      }
-      mr[j] = m_new;
     }
   }
   __syncthreads();
