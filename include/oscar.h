@@ -371,9 +371,9 @@ oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* 
  *    split count is lowered to the largest that fits (at least 1); an
  *    explicit count that does not fit, or a batch whose single split does
  *    not fit, returns OSCAR_ERR_WORKSPACE and launches nothing.  For
- *    example a batch-48, 32-query-head, 8-KV-head layer at the 12 splits
- *    the planner gives a 128K context needs 256 KiB + 48*32*13*528 bytes,
- *    about 10.8 MB.
+ *    example a batch-48, 32-query-head, 8-KV-head layer at the 11 splits
+ *    the planner gives a 128K context needs 256 KiB + 48*32*12*528 bytes,
+ *    about 10.0 MB.
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress); make it before any stream
  *    capture.  A failed lookup returns OSCAR_ERR_CUDA.

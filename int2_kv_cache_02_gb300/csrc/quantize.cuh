@@ -125,13 +125,9 @@ __device__ __forceinline__ float code_threshold(float step, int j) {
   if (tiny) dn = __fmul_rd(dn, 0x1p-64f);
   return dn == up ? __uint_as_float(__float_as_uint(up) + 1u) : up;
 }
-// Number of thresholds at or below a: the code, as a float (three compares
-// that set 1.0 or 0.0, two adds).
-__device__ __forceinline__ float code_by_thresholds(float a, float A0, float A1, float A2) {
-  return (a >= A0 ? 1.0f : 0.0f) + (a >= A1 ? 1.0f : 0.0f) + (a >= A2 ? 1.0f : 0.0f);
-}
-// The same for two inputs at once: a = fl(x - mn) for both halves, the
-// flags added as pairs (the same sums in the same order as above).
+// Number of thresholds at or below a = fl(x - mn): the code, as a float
+// (three compares that set 1.0 or 0.0, two adds), for two inputs at once
+// (packed fp32: each half rounded as the scalar operation).
 __device__ __forceinline__ float2 codes_by_thresholds2(float2 x, float2 mn, float2 A0, float2 A1,
                                                        float2 A2) {
   const float2 a = sub2(x, mn);

@@ -268,6 +268,17 @@ def test_decode_on_oracle_cache_all_groups(L, g):
     _decode_vs_oracle(L, heads, B, g * Hkv, Hkv, 2112, 310 + g, splits=(1, 2, 7, 0))
 
 
+@pytest.mark.parametrize("g", [1, 4, 8])
+@pytest.mark.parametrize("R", [128, 127, 64, 31])
+def test_decode_residual_window_fills(L, g, R):
+    """The residual CTA over windows of 31 to 128 tokens: each warp's slice
+    of the window full, partial or empty (groups of 8 take a token per lane,
+    smaller groups four tokens per warp step)."""
+    B, Hkv, P = 2, 2, 1024
+    heads, _, _ = _oracle_heads(380 + g + R, B, Hkv, P + R, P)
+    _decode_vs_oracle(L, heads, B, g * Hkv, Hkv, P + 128, 390 + g, splits=(3, 0))
+
+
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
 def test_decode_with_many_splits(L, g):
     """More splits than blocks and more than 64 partials per combining warp:
