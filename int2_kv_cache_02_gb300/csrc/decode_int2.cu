@@ -1336,6 +1336,13 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
     float2 ml0 = make_float2(-INFINITY, 0.0f), ml1 = make_float2(-INFINITY, 0.0f);
     if (lane < np) ml0 = __ldcg(reinterpret_cast<const float2*>(rec(lane)));
     if (lane + 32 < np) ml1 = __ldcg(reinterpret_cast<const float2*>(rec(lane + 32)));
+    // the first batch of outputs is loaded with the (m, l) pairs: its loads
+    // do not wait for m*
+    const int nfast = min(np, 64);
+    float4 x[kCombineBatch];
+#pragma unroll
+    for (int k = 0; k < kCombineBatch; ++k)
+      if (k < nfast) x[k] = __ldcg(reinterpret_cast<const float4*>(rec(k) + 4) + lane);
     // m* over all the row's partials (for groups smaller than 4 the warps of
     // a head add their sums unscaled, so they share one m*)
     float M = fmaxf(ml0.x, ml1.x);
@@ -1355,13 +1362,13 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
       const float w1 = ml1.x == -INFINITY ? 0.0f : fast_exp2(ml1.x - M);
       L = fmaf(w0, ml0.y, L);
       L = fmaf(w1, ml1.y, L);
-      const int nfast = min(np, 64);
       for (int i0 = 0; i0 < nfast; i0 += kCombineBatch) {
-        float4 x[kCombineBatch];
+        if (i0 > 0) {
 #pragma unroll
-        for (int k = 0; k < kCombineBatch; ++k)
-          if (i0 + k < nfast)
-            x[k] = __ldcg(reinterpret_cast<const float4*>(rec(i0 + k) + 4) + lane);
+          for (int k = 0; k < kCombineBatch; ++k)
+            if (i0 + k < nfast)
+              x[k] = __ldcg(reinterpret_cast<const float4*>(rec(i0 + k) + 4) + lane);
+        }
 #pragma unroll
         for (int k = 0; k < kCombineBatch; ++k) {
           const int q = i0 + k;
