@@ -1475,24 +1475,26 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 || BITS == 2 ? 4 : 3) decode_
   const int parts = a.num_splits + 1;
   cta_merge_write<GQ, NW>(E, a.ws + (qrow0 * parts + split) * kRecFloats,
                           (long long)parts * kRecFloats);
-  // Arrival: after the CTA barrier, one thread makes the CTA's records
-  // visible device-wide (fence) and counts the CTA in on the row's counter.
-  // The CTA that brings the count to `parts` combines the row, after a fence
-  // that orders its reads after the other CTAs' records, and sets the
-  // counter back to zero for the next call on this workspace.  A count
+  // Arrival: after the CTA barrier, one thread counts the CTA in on the
+  // row's counter with one acquire-release atomic at GPU scope, which makes
+  // the CTA's records visible with the count.  The CTA that brings the count
+  // to `parts` has acquired the other CTAs' records with it; it combines the
+  // row and sets the counter back to zero for the next call on this
+  // workspace.  A count
   // already at or above `parts` means the counters were not zero when the
   // call began: reported, and the row is left uncombined.
   __shared__ int last_cta;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned prev = atomicAdd(a.row_count + row, 1u);
+    // acquire-release at GPU scope: the CTA's records (ordered before this
+    // thread by the barrier) are released with the count, and the CTA that
+    // completes it acquires every other CTA's records before its reads
+    unsigned prev;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(prev) : "l"(a.row_count + row) : "memory");
     if (prev >= (unsigned)parts) record_error(a.status, kDevErrArrival);
     last_cta = prev == (unsigned)(parts - 1);
-    if (last_cta) {
-      a.row_count[row] = 0u;
-      __threadfence();
-    }
+    if (last_cta) a.row_count[row] = 0u;
   }
   __syncthreads();
   if (!last_cta) return;
