@@ -26,7 +26,11 @@
  *  - bf16 / fp16 values are passed as their 16-bit patterns.
  *  - (b, h) rows are contiguous: "[B][Hkv][X]" means row (b*Hkv + h) of X.
  *  - Query head j reads KV head j / g where g = Hq / Hkv (grouped-query
- *    attention); g must be 1, 2, 4 or 8.
+ *    attention); g is any whole number from 1 to 16 (Hq a multiple of Hkv).
+ *    The decode kernels work 1, 2, 4 or 8 query heads per (b, h) CTA: a
+ *    group of 3 runs as 4 heads with one padding head, groups of 5 to 7 as
+ *    8, and groups of 9 to 16 as two slices of 8 per KV head, each reading
+ *    the KV head's cache (padding heads are computed, never written).
  */
 #ifndef OSCAR_H
 #define OSCAR_H
@@ -44,7 +48,7 @@ typedef uint16_t oscar_f16;
 typedef enum {
   OSCAR_OK = 0,
   OSCAR_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad flag, state violation */
-  OSCAR_ERR_UNSUPPORTED = 2,   /* e.g. Hq/Hkv not in {1,2,4,8} */
+  OSCAR_ERR_UNSUPPORTED = 2,   /* e.g. Hq/Hkv not a whole number in 1..16 */
   OSCAR_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned */
   OSCAR_ERR_CAPACITY = 4,      /* would write past T_cap */
   OSCAR_ERR_WORKSPACE = 5,     /* workspace too small or null */
@@ -288,8 +292,10 @@ oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const osca
  *             zero, whatever its shape or split count, and the rest needs no
  *             initialisation.  A counter found non-zero is reported in the
  *             device status word (oscar_device_status) and that row's output
- *             is not written.  B*Hkv must not exceed 65536.  Calls that use
- *             one workspace must not overlap on the GPU.
+ *             is not written.  B*Hkv must not exceed 65536 (B*Hkv*2 for
+ *             groups of 9 to 16 query heads, which take two rows per KV head;
+ *             else OSCAR_ERR_UNSUPPORTED).  Calls that use one workspace must
+ *             not overlap on the GPU.
  */
 oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, int Hq,
                                     float softmax_scale, float* out, int num_splits,

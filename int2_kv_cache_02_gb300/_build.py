@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 
 LIBS = {
-    "liboscar.so": ["rotate.cu", "quantize.cu", "decode_int2.cu", "decode_bf16.cu",
+    "liboscar.so": ["rotate.cu", "quantize.cu", "decode_int2.cu", "decode_int2_pad.cu", "decode_bf16.cu",
                     "combine.cu", "api.cu", "decode_static.cu"],
     "liboscar_synth.so": ["synth.cu"],
 }

@@ -30,7 +30,6 @@ unsigned* status_ptr() {
 }
 
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline bool group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8; }
 inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 oscar_status from_cuda(cudaError_t e) { return e == cudaSuccess ? OSCAR_OK : OSCAR_ERR_CUDA; }
@@ -324,8 +323,9 @@ oscar_status oscar_append_kv(oscar_cache* c, const oscar_bf16* k_new, const osca
 }
 
 int oscar_decode_num_splits(int B, int Hkv, int Hq, int n_packed) {
-  if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || !group_ok(Hq / Hkv)) return 1;
-  return plan_splits((long long)B * Hkv, n_packed / kG, decode_int2_ctas_per_sm(Hq / Hkv), 512);
+  const long long rows = decode_rows(B, Hkv, Hq);
+  if (rows == 0) return 1;
+  return plan_splits(rows, n_packed / kG, decode_int2_ctas_per_sm(Hq / Hkv), 512);
 }
 
 int oscar_decode_plan_splits(long long rows, long long n_blocks, int ctas_per_sm, int sms) {
@@ -346,8 +346,8 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
       !std::isfinite(softmax_scale))
     return OSCAR_ERR_INVALID_ARG;
-  if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
-  if ((long long)c->B * c->Hkv > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
+  const long long rows = decode_rows(c->B, c->Hkv, Hq);
+  if (rows == 0 || rows > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
   if (!al16(q_rot) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
   int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, c->n_packed);
   if (!workspace || ws_bytes < decode_ws_bytes(c->B, c->Hkv, Hq, S + 1))
@@ -370,6 +370,7 @@ oscar_status oscar_decode_attention(const oscar_cache* c, const float* q_rot, in
   a.n_packed = c->n_packed;
   a.n_res = c->n_res;
   a.num_splits = S;
+  a.slices = decode_slices(Hq / c->Hkv);
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
@@ -387,8 +388,8 @@ oscar_status oscar_decode_step(oscar_cache* c, const oscar_bf16* q, const oscar_
   if (!q || !k_new || !v_new || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
       !std::isfinite(softmax_scale))
     return OSCAR_ERR_INVALID_ARG;
-  if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
-  if ((long long)c->B * c->Hkv > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
+  const long long rows = decode_rows(c->B, c->Hkv, Hq);
+  if (rows == 0 || rows > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
   if (!al16(q) || !al16(k_new) || !al16(v_new) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
   // a full window is flushed first (flush-before-append); everything is
   // checked before anything is launched
@@ -426,6 +427,7 @@ oscar_status oscar_decode_step(oscar_cache* c, const oscar_bf16* q, const oscar_
   a.n_packed = c->n_packed;
   a.n_res = c->n_res + 1;   // the new token, written by the kernel
   a.num_splits = S;
+  a.slices = decode_slices(Hq / c->Hkv);
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.q_exp = query_exponent(ks);
@@ -531,8 +533,8 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
       !std::isfinite(softmax_scale) || max_packed < 0 || max_packed % kG != 0 ||
       max_packed / kG > c->max_blocks)
     return OSCAR_ERR_INVALID_ARG;
-  if (Hq % c->Hkv != 0 || !group_ok(Hq / c->Hkv)) return OSCAR_ERR_UNSUPPORTED;
-  if ((long long)c->B * c->Hkv > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
+  const long long rows = decode_rows(c->B, c->Hkv, Hq);
+  if (rows == 0 || rows > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
   if (!al16(q_rot) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
   int S = num_splits > 0 ? num_splits : oscar_decode_num_splits(c->B, c->Hkv, Hq, max_packed);
   if (!workspace || ws_bytes < decode_ws_bytes(c->B, c->Hkv, Hq, S + 1))
@@ -556,6 +558,7 @@ oscar_status oscar_paged_decode_attention(const oscar_paged_cache* c, const floa
   a.n_packed = max_packed;  // sizes the equal chunks of the splits
   a.n_res = 0;
   a.num_splits = S;
+  a.slices = decode_slices(Hq / c->Hkv);
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));
@@ -578,13 +581,15 @@ oscar_status oscar_bf16_decode_attention(const oscar_bf16* q, const oscar_bf16* 
   if (!q || !K || !V || !out || B <= 0 || Hq <= 0 || Hkv <= 0 || T < 0 || T_stride < T ||
       num_splits < 0 || num_splits > 4096 || !std::isfinite(softmax_scale))
     return OSCAR_ERR_INVALID_ARG;
-  if (Hq % Hkv != 0 || !group_ok(Hq / Hkv)) return OSCAR_ERR_UNSUPPORTED;
+  const long long rows = decode_rows(B, Hkv, Hq);
+  if (rows == 0) return OSCAR_ERR_UNSUPPORTED;
+  // grid (splits, Hkv x slices, B)
+  if (B > 65535 || rows / B > 65535) return OSCAR_ERR_UNSUPPORTED;
   if (!al16(q) || !al16(K) || !al16(V) || !al16(out)) return OSCAR_ERR_ALIGNMENT;
   int S = num_splits;
   if (S == 0) {
     const long long chunk = 16;  // tokens per warp chunk, the unit of work here
-    S = plan_splits_bf16((long long)B * Hkv, (T + chunk - 1) / chunk,
-                         decode_bf16_ctas_per_sm(Hq / Hkv), 512);
+    S = plan_splits_bf16(rows, (T + chunk - 1) / chunk, decode_bf16_ctas_per_sm(Hq / Hkv), 512);
   }
   if (!workspace || ws_bytes < ws_bytes_for(B, Hq, S)) return OSCAR_ERR_WORKSPACE;
   if (!al16(workspace)) return OSCAR_ERR_ALIGNMENT;

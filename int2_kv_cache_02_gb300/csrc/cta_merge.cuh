@@ -19,14 +19,15 @@ struct MergeSmem {
 };
 
 // Called by all NW*32 threads of the CTA (NW*32 >= 128) after a __syncthreads
-// that follows the per-warp writes into `s`.
+// that follows the per-warp writes into `s`; heads 0 .. nh - 1 (nh <= GQ) are
+// written, the rest are padding.
 template <int GQ, int NW>
 __device__ __forceinline__ void cta_merge_write(const MergeSmem<GQ, NW>& s, float* rec_base,
-                                                long long rec_stride) {
+                                                long long rec_stride, int nh = GQ) {
   const int c = threadIdx.x;
   if (c >= kD) return;
 #pragma unroll 1
-  for (int j = 0; j < GQ; ++j) {
+  for (int j = 0; j < nh; ++j) {
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < NW; ++w) M = fmaxf(M, s.m[w][j]);

@@ -28,16 +28,21 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const Bf16DecodeAr
   __shared__ __align__(16) float pbuf[NW][64];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  // blockIdx.y = slice sl of KV head h's query group (heads GQ sl ..), as in
+  // the INT2 kernel: nh of its GQ heads are active, the rest padding
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int slices = decode_slices(a.Hq / a.Hkv);
+  const int h = blockIdx.y / slices, sl = blockIdx.y - h * slices;
+  const int g = a.Hq / a.Hkv, nh = min(GQ, g - GQ * sl);
   const long long row = (long long)b * a.Hkv + h;
-  const long long qrow0 = (long long)b * a.Hq + (long long)h * GQ;
+  const long long qrow0 = (long long)b * a.Hq + (long long)h * g + GQ * sl;
   const int t_begin = (int)((long long)a.T * split / a.num_splits);
   const int t_end = (int)((long long)a.T * (split + 1) / a.num_splits);
 
   float qv[GV][4];
 #pragma unroll
   for (int j = 0; j < GV; ++j) {
-    const uint2 r = reinterpret_cast<const uint2*>(a.q + (qrow0 + j % GQ) * kD)[lane];
+    const uint2 r = reinterpret_cast<const uint2*>(a.q + (qrow0 + min(j % GQ, nh - 1)) * kD)[lane];
     qv[j][0] = bf16_lo(r.x); qv[j][1] = bf16_hi(r.x);
     qv[j][2] = bf16_lo(r.y); qv[j][3] = bf16_hi(r.y);
   }
@@ -154,12 +159,12 @@ __global__ void __launch_bounds__(NW * 32) decode_bf16_kernel(const Bf16DecodeAr
   }
   __syncthreads();
   cta_merge_write<GQ, NW>(E, a.ws + (qrow0 * a.num_splits + split) * kRecFloats,
-                          (long long)a.num_splits * kRecFloats);
+                          (long long)a.num_splits * kRecFloats, nh);
 }
 
 template <int GQ>
 cudaError_t launch_g(const Bf16DecodeArgs& a, cudaStream_t s) {
-  dim3 grid(a.num_splits, a.Hkv, a.B);
+  dim3 grid(a.num_splits, a.Hkv * decode_slices(a.Hq / a.Hkv), a.B);
   decode_bf16_kernel<GQ><<<grid, NW * 32, 0, s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -178,7 +183,7 @@ int occupancy_g() {
 }  // namespace
 
 cudaError_t launch_decode_bf16(const Bf16DecodeArgs& a, cudaStream_t s) {
-  switch (a.Hq / a.Hkv) {
+  switch (decode_group_width(a.Hq / a.Hkv)) {
     case 1: return launch_g<1>(a, s);
     case 2: return launch_g<2>(a, s);
     case 4: return launch_g<4>(a, s);
@@ -188,7 +193,7 @@ cudaError_t launch_decode_bf16(const Bf16DecodeArgs& a, cudaStream_t s) {
 }
 
 int decode_bf16_ctas_per_sm(int g) {
-  switch (g) {
+  switch (decode_group_width(g)) {
     case 1: return occupancy_g<1>();
     case 2: return occupancy_g<2>();
     case 4: return occupancy_g<4>();

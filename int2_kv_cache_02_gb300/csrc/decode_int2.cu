@@ -445,13 +445,13 @@ struct RawQueries {
   uint2 v[N];
 };
 template <int GQ>
-__device__ __forceinline__ void load_raw_queries(const DecodeArgs& a, long long qrow0,
+__device__ __forceinline__ void load_raw_queries(const DecodeArgs& a, long long qrow0, int nh,
                                                  RawQueries<GQ>& raw) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int k = 0; k < RawQueries<GQ>::N; ++k) {
     const int j = GQ <= NW ? k : warp + NW * k;
-    raw.v[k] = reinterpret_cast<const uint2*>(a.q_raw + (qrow0 + j) * kD)[lane];
+    raw.v[k] = reinterpret_cast<const uint2*>(a.q_raw + (qrow0 + min(j, nh - 1)) * kD)[lane];
   }
 }
 template <int GQ>
@@ -505,10 +505,12 @@ __device__ __forceinline__ float scale_query(float (&qf)[32], const float4 (&qv)
 //  * P.V: channels on M as in the row layout, (head, limb of p~) on N.
 template <int GQ, bool BSCALE, int BITS, class Ring>
 __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
-                                            MergeSmem<GQ, NW>& E, long long qrow0) {
+                                            MergeSmem<GQ, NW>& E, long long qrow0, int nh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int hq = (gid >> 1) % GQ;   // head of this lane's q~ column
+  // head of this lane's q~ column (a padding head of a partial group works
+  // on the last active head's query; its results are not merged)
+  const int hq = min((gid >> 1) % GQ, nh - 1);
   const int limb = gid & 1;         // 0: hi part, 1: lo part
   const int hs = tig % GQ;          // head of this lane's scores and outputs
   using RL = typename Layout<BITS>::RL;
@@ -519,7 +521,7 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
   float4 qv[8];
   if (a.q_raw != nullptr) {   // fused step: rotate the CTA's queries here
     RawQueries<GQ> raw;
-    load_raw_queries<GQ>(a, qrow0, raw);
+    load_raw_queries<GQ>(a, qrow0, nh, raw);
     R.start(a);
     const float* qs = stage_rotated_queries<GQ>(a, raw, dyn_smem() + smem_bytes<GQ, BITS>());
     load_query(qv, qs + hq * kD, tig);
@@ -806,11 +808,12 @@ __device__ __forceinline__ void packed_cols(const DecodeArgs& a, const Ring& R,
 //  * P.V: channels on M, the 8 heads on N, one n-tile per limb of p~.
 template <int GQ, bool BSCALE, int BITS, class Ring>
 __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
-                                            MergeSmem<GQ, NW>& E, long long qrow0) {
+                                            MergeSmem<GQ, NW>& E, long long qrow0, int nh) {
   static_assert(GQ == 8, "the row layout serves groups of 8 query heads");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int head = gid;
+  // this thread's head (a padding head works on the last active head's query)
+  const int head = min(gid, nh - 1);
   using RL = typename Layout<BITS>::RL;
   constexpr int LW = BITS == 2 ? 2 : 4;   // key words per token and lane
   // The query's loads go out first, then the ring's first copies, which
@@ -819,7 +822,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
   float4 qv[8];
   if (a.q_raw != nullptr) {   // fused step: rotate the CTA's queries here
     RawQueries<GQ> raw;
-    load_raw_queries<GQ>(a, qrow0, raw);
+    load_raw_queries<GQ>(a, qrow0, nh, raw);
     R.start(a);
     const float* qs = stage_rotated_queries<GQ>(a, raw, dyn_smem() + smem_bytes<GQ, BITS>());
     load_query(qv, qs + head * kD, tig);
@@ -1119,7 +1122,7 @@ __device__ __forceinline__ void packed_rows(const DecodeArgs& a, const Ring& R,
 // --------------------------------------------------------------- residual
 template <int GQ, bool PAGED>
 __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ, NW>& E,
-                                               long long row, long long qrow0, int b) {
+                                               long long row, long long qrow0, int nh, int b) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int n_res = a.n_res;
   if constexpr (PAGED) {
@@ -1171,7 +1174,7 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
     static_assert(kR == NW * 32, "one 32-token slice of the window per warp");
     float* qs = reinterpret_cast<float*>(dyn_smem());   // [GQ][128] fp32
     for (int i = threadIdx.x; i < GQ * 32; i += NW * 32) {   // every lane of a warp alike
-      const int j = i >> 5;
+      const int j = min(i >> 5, nh - 1);
       const float4 v = a.q_raw != nullptr ? rotated_query(a, qrow0 + j, lane)
                                           : reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
       reinterpret_cast<float4*>(qs)[i] = v;
@@ -1236,8 +1239,9 @@ __device__ __forceinline__ void residual_split(const DecodeArgs& a, MergeSmem<GQ
     float qv[GQ][4];
 #pragma unroll
     for (int j = 0; j < GQ; ++j) {
-      const float4 v = a.q_raw != nullptr ? rotated_query(a, qrow0 + j, lane)
-                                          : reinterpret_cast<const float4*>(a.q_rot + (qrow0 + j) * kD)[lane];
+      const long long qj = qrow0 + min(j, nh - 1);
+      const float4 v = a.q_raw != nullptr ? rotated_query(a, qj, lane)
+                                          : reinterpret_cast<const float4*>(a.q_rot + qj * kD)[lane];
       qv[j][0] = v.x; qv[j][1] = v.y; qv[j][2] = v.z; qv[j][3] = v.w;
     }
     constexpr int TU = 4;
@@ -1320,7 +1324,7 @@ constexpr int kCombineBatch = 16;
 
 template <int GQ>
 __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, NW>& E,
-                                            long long qrow0, int parts) {
+                                            long long qrow0, int nh, int parts) {
   constexpr int HPW = GQ > NW ? GQ / NW : 1;   // heads per warp
   constexpr int PG = GQ >= NW ? 1 : NW / GQ;   // warps per head
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1328,6 +1332,7 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
   for (int hh = 0; hh < HPW; ++hh) {
     const int j = GQ >= NW ? warp + NW * hh : warp % GQ;
     const int pg = GQ >= NW ? 0 : warp / GQ;
+    if (j >= nh) continue;   // a padding head (warp-uniform): no partials, no output
     const float* r0 = a.ws + (qrow0 + j) * parts * kRecFloats;
     const int np = (parts - pg + PG - 1) / PG;   // this warp's partials pg + PG i
     auto rec = [&](int i) { return r0 + (long long)(pg + PG * i) * kRecFloats; };
@@ -1416,6 +1421,7 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
     const int c = threadIdx.x;   // NW * 32 == kD channels, one per thread
 #pragma unroll
     for (int j = 0; j < GQ; ++j) {
+      if (j >= nh) break;
       float Lt = 0.0f, oc = 0.0f;
 #pragma unroll
       for (int g = 0; g < PG; ++g) {
@@ -1429,8 +1435,10 @@ __device__ __forceinline__ void row_combine(const DecodeArgs& a, MergeSmem<GQ, N
 
 // 4 CTAs per SM (128 registers), except the INT4 row layout (3).
 // BSCALE: per-block step scale (caches with the all-heads norm scope);
-// BITS: code width of the records (2, or the INT4 option).
-template <int GQ, bool PAGED, bool BSCALE, int BITS>
+// BITS: code width of the records (2, or the INT4 option); PAD: query groups
+// of another size than GQ (padding heads, or slices of a group above 8), so
+// that the kernels of whole groups keep their code.
+template <int GQ, bool PAGED, bool BSCALE, int BITS, bool PAD>
 __global__ void __launch_bounds__(NW * 32, GQ <= 4 || BITS == 2 ? 4 : 3) decode_int2_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   auto& E = *reinterpret_cast<MergeSmem<GQ, NW>*>(smem);
@@ -1440,20 +1448,35 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 || BITS == 2 ? 4 : 3) decode_
   // residual split, and the others take the packed splits row by row.  So
   // every residual CTA starts in the first wave, where its work (up to a
   // full 128-token window) runs beside the packed CTAs instead of after
-  // them at the end of a many-wave grid.
-  const long long rows = (long long)a.B * a.Hkv;
-  long long row;
+  // them at the end of a many-wave grid.  A row is one slice of up to GQ of
+  // the g query heads that share KV head h of sequence b (slices = ceil(g /
+  // GQ)); the last slice of a group that GQ does not divide, or a group
+  // smaller than GQ, has padding heads, which the CTA works but neither
+  // merges nor outputs.
+  const long long rows = (long long)a.B * a.Hkv * (PAD ? a.slices : 1);
+  long long vrow;
   int split;
   if ((long long)blockIdx.x < rows) {
-    row = blockIdx.x;
+    vrow = blockIdx.x;
     split = a.num_splits;
   } else {
     const long long q = (long long)blockIdx.x - rows;
-    row = q / a.num_splits;
-    split = (int)(q - row * a.num_splits);
+    vrow = q / a.num_splits;
+    split = (int)(q - vrow * a.num_splits);
+  }
+  long long row = vrow;   // the cache row (b, h)
+  int sl = 0;
+  if (PAD && a.slices > 1) {
+    row = vrow / a.slices;
+    sl = (int)(vrow - row * a.slices);
   }
   const int b = (int)(row / a.Hkv), h = (int)(row - (long long)b * a.Hkv);
-  const long long qrow0 = (long long)b * a.Hq + (long long)h * GQ;  // first query head
+  const int g = PAD ? a.Hq / a.Hkv : GQ;
+  const int nh = PAD ? min(GQ, g - GQ * sl) : GQ;   // active heads of the slice
+  const long long qrow0 = (long long)b * a.Hq + (long long)h * g + GQ * sl;  // first query head
+  // (padded groups) kept in shared memory through the block loop
+  __shared__ int s_nh;
+  if (PAD && threadIdx.x == 0) s_nh = nh;
 
   if (split < a.num_splits) {
     if (PAGED && split >= paged_splits_used(a, row_blocks<PAGED>(a, b))) {
@@ -1463,18 +1486,19 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 || BITS == 2 ? 4 : 3) decode_
     } else {
       const WarpRing<PAGED, BITS> R = make_ring<PAGED, BITS>(a, smem, b, h, split);
       if constexpr (GQ <= 4) {
-        packed_cols<GQ, BSCALE, BITS>(a, R, E, qrow0);
+        packed_cols<GQ, BSCALE, BITS>(a, R, E, qrow0, nh);
       } else {
-        packed_rows<GQ, BSCALE, BITS>(a, R, E, qrow0);
+        packed_rows<GQ, BSCALE, BITS>(a, R, E, qrow0, nh);
       }
     }
   } else {
-    residual_split<GQ, PAGED>(a, E, row, qrow0, b);
+    residual_split<GQ, PAGED>(a, E, row, qrow0, nh, b);
   }
   __syncthreads();
   const int parts = a.num_splits + 1;
+  const int nh_e = PAD ? s_nh : GQ;
   cta_merge_write<GQ, NW>(E, a.ws + (qrow0 * parts + split) * kRecFloats,
-                          (long long)parts * kRecFloats);
+                          (long long)parts * kRecFloats, nh_e);
   // Arrival: after the CTA barrier, one thread counts the CTA in on the
   // row's counter with one acquire-release atomic at GPU scope, which makes
   // the CTA's records visible with the count.  The CTA that brings the count
@@ -1491,51 +1515,70 @@ __global__ void __launch_bounds__(NW * 32, GQ <= 4 || BITS == 2 ? 4 : 3) decode_
     // completes it acquires every other CTA's records before its reads
     unsigned prev;
     asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                 : "=r"(prev) : "l"(a.row_count + row) : "memory");
+                 : "=r"(prev) : "l"(a.row_count + vrow) : "memory");
     if (prev >= (unsigned)parts) record_error(a.status, kDevErrArrival);
     last_cta = prev == (unsigned)(parts - 1);
-    if (last_cta) a.row_count[row] = 0u;
+    if (last_cta) a.row_count[vrow] = 0u;
   }
   __syncthreads();
   if (!last_cta) return;
-  row_combine<GQ>(a, E, qrow0, parts);
+  row_combine<GQ>(a, E, qrow0, nh_e, parts);
 }
 
 // Opt in to the kernel's dynamic shared memory (above 48 KB for INT2), once
 // per instantiation and device.
-template <int GQ, bool PAGED, bool BSCALE, int BITS>
+template <int GQ, bool PAGED, bool BSCALE, int BITS, bool PAD>
 cudaError_t allow_smem() {
   static int done[128] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 128 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED, BSCALE, BITS>,
+  e = cudaFuncSetAttribute(decode_int2_kernel<GQ, PAGED, BSCALE, BITS, PAD>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<GQ, BITS>() + kQRotStage);
   if (e == cudaSuccess && dev >= 0 && dev < 128) done[dev] = 1;
   return e;
 }
 
-template <int GQ, bool PAGED, bool BSCALE, int BITS>
-cudaError_t launch_g(const DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e0 = allow_smem<GQ, PAGED, BSCALE, BITS>();
+template <int GQ, bool PAGED, bool BSCALE, int BITS, bool PAD>
+cudaError_t launch_k(const DecodeArgs& a, cudaStream_t s) {
+  cudaError_t e0 = allow_smem<GQ, PAGED, BSCALE, BITS, PAD>();
   if (e0 != cudaSuccess) return e0;
-  const long long ctas = (long long)a.B * a.Hkv * (a.num_splits + 1);
+  const long long ctas = (long long)a.B * a.Hkv * a.slices * (a.num_splits + 1);
   if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   const dim3 grid((unsigned)ctas);
   const int smem = smem_bytes<GQ, BITS>() + (a.q_raw != nullptr ? kQRotStage : 0);
-  decode_int2_kernel<GQ, PAGED, BSCALE, BITS><<<grid, NW * 32, smem, s>>>(a);
+  decode_int2_kernel<GQ, PAGED, BSCALE, BITS, PAD><<<grid, NW * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
+// This translation unit builds the kernels of whole groups (g = 1, 2, 4, 8);
+// decode_int2_pad.cu includes this file with OSCAR_DECODE_PAD_TU defined and
+// builds the padded ones (groups of 4 or 8 heads per CTA for the other g),
+// so the two compile in parallel.
+#ifdef OSCAR_DECODE_PAD_TU
+constexpr bool kPadTU = true;
+#else
+constexpr bool kPadTU = false;
+#endif
+
 template <bool PAGED, bool BSCALE, int BITS>
 cudaError_t launch_p(const DecodeArgs& a, cudaStream_t s) {
-  switch (a.Hq / a.Hkv) {
-    case 1: return launch_g<1, PAGED, BSCALE, BITS>(a, s);
-    case 2: return launch_g<2, PAGED, BSCALE, BITS>(a, s);
-    case 4: return launch_g<4, PAGED, BSCALE, BITS>(a, s);
-    case 8: return launch_g<8, PAGED, BSCALE, BITS>(a, s);
-    default: return cudaErrorInvalidValue;
+  if (a.slices != decode_slices(a.Hq / a.Hkv)) return cudaErrorInvalidValue;
+  if constexpr (kPadTU) {
+    switch (decode_group_width(a.Hq / a.Hkv)) {
+      case 4: return launch_k<4, PAGED, BSCALE, BITS, true>(a, s);
+      case 8: return launch_k<8, PAGED, BSCALE, BITS, true>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    switch (a.Hq / a.Hkv) {
+      case 1: return launch_k<1, PAGED, BSCALE, BITS, false>(a, s);
+      case 2: return launch_k<2, PAGED, BSCALE, BITS, false>(a, s);
+      case 4: return launch_k<4, PAGED, BSCALE, BITS, false>(a, s);
+      case 8: return launch_k<8, PAGED, BSCALE, BITS, false>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
   }
 }
 
@@ -1546,19 +1589,34 @@ cudaError_t launch_b(const DecodeArgs& a, cudaStream_t s) {
   return a.block_table ? launch_p<true, false, BITS>(a, s) : launch_p<false, false, BITS>(a, s);
 }
 
+#ifndef OSCAR_DECODE_PAD_TU
 template <int GQ>
 int occupancy_g() {
-  if (allow_smem<GQ, false, false, 2>() != cudaSuccess) return 0;
+  if (allow_smem<GQ, false, false, 2, false>() != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ, false, false, 2>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_int2_kernel<GQ, false, false, 2, false>,
                                                     NW * 32, smem_bytes<GQ, 2>()) != cudaSuccess)
     return 0;
   return n;
 }
 
+#endif
+
 }  // namespace
 
+#ifdef OSCAR_DECODE_PAD_TU
+cudaError_t launch_decode_int2_padded(const DecodeArgs& a, cudaStream_t s) {
+  switch (a.bits) {
+    case 2: return launch_b<2>(a, s);
+    case 4: return launch_b<4>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+#else
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t s) {
+  if (a.Hkv <= 0 || a.Hq % a.Hkv != 0) return cudaErrorInvalidValue;
+  const int g = a.Hq / a.Hkv;
+  if (g != decode_group_width(g)) return launch_decode_int2_padded(a, s);
   switch (a.bits) {
     case 2: return launch_b<2>(a, s);
     case 4: return launch_b<4>(a, s);
@@ -1567,7 +1625,7 @@ cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t s) {
 }
 
 int decode_int2_ctas_per_sm(int g) {
-  switch (g) {
+  switch (decode_group_width(g)) {
     case 1: return occupancy_g<1>();
     case 2: return occupancy_g<2>();
     case 4: return occupancy_g<4>();
@@ -1575,5 +1633,6 @@ int decode_int2_ctas_per_sm(int g) {
     default: return 0;
   }
 }
+#endif
 
 }  // namespace oscar

@@ -65,9 +65,8 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   if (!q_rot || !out || Hq <= 0 || num_splits < 0 || num_splits > 4096 ||
       !std::isfinite(softmax_scale))
     return OSCAR_ERR_INVALID_ARG;
-  const int g = (Hq % c->Hkv == 0) ? Hq / c->Hkv : 0;
-  if (!(g == 1 || g == 2 || g == 4 || g == 8)) return OSCAR_ERR_UNSUPPORTED;
-  if ((long long)c->B * c->Hkv > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
+  const long long rows = decode_rows(c->B, c->Hkv, Hq);
+  if (rows == 0 || rows > kMaxDecodeRows) return OSCAR_ERR_UNSUPPORTED;
   if (!aligned16(q_rot) || !aligned16(out)) return OSCAR_ERR_ALIGNMENT;
 
   // The partial records and counters must fit in the static array.  An
@@ -103,6 +102,7 @@ extern "C" oscar_status oscar_decode_attention_static_ws(const oscar_cache* c,
   a.n_packed = c->n_packed;
   a.n_res = c->n_res;
   a.num_splits = S;
+  a.slices = decode_slices(Hq / c->Hkv);
   a.flags = c->flags;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.q_exp = query_exponent(key_scale(c->flags, c->norm_target));

@@ -73,6 +73,8 @@ struct DecodeArgs {
   float* out;         // [B][Hq][128]
   unsigned* status;
   int B, Hkv, Hq, T_cap, n_packed, n_res, num_splits;
+  // slices of each query group: decode_slices(Hq / Hkv)
+  int slices = 1;
   unsigned flags;
   float scale_log2;   // softmax_scale * log2(e)
   // the query is scaled by 2^(q_exp - e), e the exponent of its largest
@@ -116,9 +118,32 @@ inline float* decode_partials(void* ws) {
   return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kDecodeWsHeader);
 }
 
+// Query heads per KV head, g = Hq / Hkv, from 1 to kMaxGroup.  The decode
+// kernels are instantiated for groups of 1, 2, 4 and 8 heads per CTA
+// (decode_group_width); a group of another size takes the next width, with
+// padding heads that are worked but neither merged nor written, and a group
+// above 8 is cut into slices of 8 (decode_slices), each of which reads the
+// KV head's cache on its own.
+constexpr int kMaxGroup = 16;
+__host__ __device__ constexpr int decode_group_width(int g) {
+  return g <= 1 ? 1 : g == 2 ? 2 : g <= 4 ? 4 : 8;
+}
+__host__ __device__ constexpr int decode_slices(int g) {
+  return (g + decode_group_width(g) - 1) / decode_group_width(g);
+}
+// Rows of a decode launch, one per (sequence, KV head, slice), or 0 when Hq
+// is not a multiple of Hkv with a group of 1..kMaxGroup heads.
+inline long long decode_rows(long long B, int Hkv, int Hq) {
+  if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || Hq / Hkv > kMaxGroup) return 0;
+  return B * Hkv * decode_slices(Hq / Hkv);
+}
+
 // Fused INT2 decode attention with the split-K combine in its last CTA per
 // row (one launch).
 cudaError_t launch_decode_int2(const DecodeArgs& a, cudaStream_t s);
+// The same for query groups that are not a whole kernel group (1, 2, 4, 8
+// heads): decode_int2_pad.cu.
+cudaError_t launch_decode_int2_padded(const DecodeArgs& a, cudaStream_t s);
 // Blocks per SM the INT2 decode kernel reaches for query group size g.
 int decode_int2_ctas_per_sm(int g);
 

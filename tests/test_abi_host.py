@@ -202,8 +202,10 @@ def test_paged_validation():
     assert L.oscar_paged_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 64, P(FAKE), 48, None) == 1
     assert L.oscar_paged_prefill_kv(ctypes.byref(c), P(FAKE), P(FAKE), 512, P(FAKE), 512,
                                     None) == 4          # more blocks than a table row
-    assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 6, 0.1, 64, P(FAKE), 0,
-                                          P(FAKE), 1 << 20, None) == 2
+    assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 34, 0.1, 64, P(FAKE), 0,
+                                          P(FAKE), 1 << 20, None) == 2      # group of 17
+    assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 5, 0.1, 64, P(FAKE), 0,
+                                          P(FAKE), 1 << 20, None) == 2      # not a multiple
     assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, 33, P(FAKE), 0,
                                           P(FAKE), 1 << 20, None) == 1
     assert L.oscar_paged_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, 64, P(FAKE), 2,
@@ -221,11 +223,18 @@ def test_decode_validation():
     L = O.library()
     P = ctypes.c_void_p
     c = _cache(Hkv=2)
-    # query group of 3 is not supported
-    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 6, 0.1, P(FAKE), 0, P(FAKE),
+    # a query group above 16 heads, or Hq not a multiple of Hkv, is not supported
+    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 34, 0.1, P(FAKE), 0, P(FAKE),
                                     1 << 30, None) == 2
-    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 32, 0.1, P(FAKE), 0, P(FAKE),
+    assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 7, 0.1, P(FAKE), 0, P(FAKE),
                                     1 << 30, None) == 2
+    # groups of 9..16 take two rows per KV head: 32769 KV heads of 12 query
+    # heads are over the 65536 row counters, 32769 of 8 are not
+    big = _cache(B=1, Hkv=32769)
+    assert L.oscar_decode_attention(ctypes.byref(big), P(FAKE), 12 * 32769, 0.1, P(FAKE), 1,
+                                    P(FAKE), 1 << 40, None) == 2
+    assert L.oscar_decode_attention(ctypes.byref(big), P(FAKE), 8 * 32769, 0.1, P(FAKE), 1,
+                                    P(FAKE), 4, None) == 5
     # workspace missing / too small
     assert L.oscar_decode_attention(ctypes.byref(c), P(FAKE), 8, 0.1, P(FAKE), 4, None,
                                     1 << 30, None) == 5
@@ -288,7 +297,8 @@ def test_decode_step_validation_leaves_the_cache_untouched():
     assert step(c, splits=-1) == 1
     assert step(c, k=FAKE + 8) == 3
     assert step(c, q=FAKE + 4) == 3
-    assert step(c, Hq=6) == 2                                # group of 3
+    assert step(c, Hq=34) == 2                               # group of 17
+    assert step(c, Hq=5) == 2                                # not a multiple of Hkv
     assert step(c, wsb=16) == 5                              # workspace too small
     assert c.n_packed == 64 and c.n_res == 5
     full = _cache(n_packed=256, n_res=128)                   # the flush would not fit

@@ -51,7 +51,7 @@ def _write_record(rec, kq, vq, norm16, j):
     rec.copy_(torch.from_numpy(np.concatenate(parts)))
 
 
-@pytest.mark.parametrize("g", [1, 4, 8])
+@pytest.mark.parametrize("g", [1, 3, 4, 8, 16])
 def test_paged_decode_matches_oracle(L, g):
     Hkv = 2
     Hq = Hkv * g

@@ -261,14 +261,16 @@ def _decode_vs_oracle(L, heads, B, Hq, Hkv, T_cap, seed_q, flags=0, splits=(0,))
     return outs, ref
 
 
-@pytest.mark.parametrize("g", [1, 2, 4, 8])
+# groups of 1, 2, 4 and 8 heads run whole; 3 takes the 4-head form with one
+# padding head, 5..7 the 8-head form, 12 and 16 two slices of 8 per KV head
+@pytest.mark.parametrize("g", [1, 2, 3, 4, 5, 6, 7, 8, 12, 16])
 def test_decode_on_oracle_cache_all_groups(L, g):
     B, Hkv, T, P = 2, 2, 2048 + 77, 2048
     heads, _, _ = _oracle_heads(300 + g, B, Hkv, T, P)
     _decode_vs_oracle(L, heads, B, g * Hkv, Hkv, 2112, 310 + g, splits=(1, 2, 7, 0))
 
 
-@pytest.mark.parametrize("g", [1, 4, 8])
+@pytest.mark.parametrize("g", [1, 3, 4, 6, 8, 16])
 @pytest.mark.parametrize("R", [128, 127, 64, 31])
 def test_decode_residual_window_fills(L, g, R):
     """The residual CTA over windows of 31 to 128 tokens: each warp's slice
@@ -279,7 +281,7 @@ def test_decode_residual_window_fills(L, g, R):
     _decode_vs_oracle(L, heads, B, g * Hkv, Hkv, P + 128, 390 + g, splits=(3, 0))
 
 
-@pytest.mark.parametrize("g", [1, 2, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 5, 8, 16])
 def test_decode_with_many_splits(L, g):
     """More splits than blocks and more than 64 partials per combining warp:
     splits of one block or none (empty partials), and the combine's path for
@@ -500,7 +502,8 @@ def test_streaming_flush_equals_one_shot_on_gpu(L):
 # --------------------------------------------------------------------------
 
 @pytest.mark.parametrize("g,T,S", [(1, 1000, 0), (4, 4097, 0), (4, 4097, 3), (8, 777, 2),
-                                   (2, 64, 1), (4, 1, 1)])
+                                   (2, 64, 1), (4, 1, 1), (3, 1000, 0), (6, 500, 2),
+                                   (12, 300, 3), (16, 777, 0)])
 def test_bf16_decode_parity(L, g, T, S):
     B, Hkv = 2, 2
     Hq = g * Hkv

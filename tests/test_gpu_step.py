@@ -41,6 +41,10 @@ CASES = [  # (group size g, code bits, flags, norm target, key group)
     (8, 0, 4, 0.0, 64),
     (4, 0, 1 | 2, 0.0, 0),       # neither rotation nor scaling
     (4, 0, 1, 3.0, 0),           # scaling only, target norm 3
+    (3, 0, 0, 0.0, 0),           # a padding head in the 4-head form
+    (6, 0, 0, 0.0, 0),           # two padding heads in the 8-head form
+    (16, 0, 0, 0.0, 0),          # two slices of 8 heads per KV head
+    (12, 4, 0, 0.0, 0),
 ]
 
 
