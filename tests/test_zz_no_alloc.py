@@ -49,9 +49,10 @@ def _qrot(L, B, Hq, seed):
     return qr
 
 
+@pytest.mark.parametrize("Hq", [8, 24])          # groups of 4, and of 12 (two slices)
 @pytest.mark.parametrize("splits", [0, 5])
-def test_static_scratch_matches_workspace_entry_on_two_calls(L, splits):
-    B, Hkv, Hq = 2, 2, 8
+def test_static_scratch_matches_workspace_entry_on_two_calls(L, splits, Hq):
+    B, Hkv = 2, 2
     cache = _cache(L)
     ws = L.alloc_workspace(L.decode_workspace_bytes(B, Hkv, Hq, cache.n_packed, splits))
     for call, seed in enumerate((910, 911)):          # two calls in a row, new queries
