@@ -40,7 +40,8 @@
 // kDevErrWaitTimeout instead of hanging; no CTA-wide barrier runs inside the
 // main loop.  Instantiations: query group g, contiguous or paged records
 // (through the block table), a per-block step scale for caches with the
-// all-heads norm, and the code width.
+// all-heads norm, the code width, and whether the CTA's group is padded (a
+// group of another size than 1, 2, 4 or 8, or one slice of a group above 8).
 #include "common.cuh"
 #include "cta_merge.cuh"
 #include "launch.h"
