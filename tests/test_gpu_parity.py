@@ -349,6 +349,47 @@ def test_decode_edge_sizes(L, T, P):
     _decode_vs_oracle(L, heads, B, Hq, Hkv, max(32, P), 331, splits=(0, 3))
 
 
+@pytest.mark.parametrize("Hq", [32, 96])   # groups of 4, and of 12 (two rows per KV head)
+def test_decode_at_the_row_limit(L, Hq):
+    """As many rows as the workspace has arrival counters (65536): every
+    row's counter is taken and left at zero (a second call at the same split
+    count is bit-identical, with a clean status word), the split counts agree
+    on every row, and sampled rows match the oracle."""
+    Hkv, P, R = 8, 32, 8
+    g = Hq // Hkv
+    B = 65536 // (Hkv * (2 if g > 8 else 1))
+    T = P + R
+    k = torch.empty((B, Hkv, T, 128), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    synth.gen_bf16_cuda(k, 600, Hkv, 0, 0, T)
+    synth.gen_bf16_cuda(v, 601, Hkv, 0, 0, T)
+    cache = L.KVCache(B, Hkv, P)
+    L.prefill_kv(cache, k, v, n_tok=P)
+    L.append_kv(cache, k[:, :, P:].contiguous(), v[:, :, P:].contiguous(), n_tok=R)
+    del k, v
+    qb = torch.empty((B, Hq, 1, 128), dtype=torch.bfloat16, device="cuda")
+    synth.gen_bf16_cuda(qb, 602, Hq, 0, 0, 1)
+    qr = torch.empty((B, Hq, 128), dtype=torch.float32, device="cuda")
+    L.rotate_q(qb[:, :, 0].contiguous(), qr)
+    ws = L.alloc_workspace(L.decode_workspace_bytes(B, Hkv, Hq, P, 2))
+    outs = []
+    for S in (1, 2, 1):
+        out = torch.full((B, Hq, 128), float("nan"), device="cuda")
+        L.decode_attention(cache, qr, Hq, TAU, out, ws, num_splits=S)
+        _sync_ok(L)
+        outs.append(out)
+    assert torch.equal(outs[0], outs[2])
+    d = (torch.linalg.vector_norm(outs[1] - outs[0]) / torch.linalg.vector_norm(outs[0])).item()
+    assert d <= 1e-6, d
+    for b, h in [(0, 0), (B // 2 + 1, 3), (B - 1, Hkv - 1)]:
+        kb = synth.gen_bf16(600, Hkv, [b], [h], 0, T)[0, 0]
+        vb = synth.gen_bf16(601, Hkv, [b], [h], 0, T)[0, 0]
+        qbits = synth.gen_bf16(602, Hq, [b], range(h * g, (h + 1) * g), 0, 1)[0, :, 0]
+        ref = O.build_head_cache(kb, vb, P).decode(O.rotate_q(qbits), TAU)
+        got = outs[0][b, h * g:(h + 1) * g].cpu().numpy()
+        assert_attention_close(got[None], ref[None], f"row ({b}, {h})")
+
+
 def test_decode_empty_cache_gives_zeros(L):
     cache = L.KVCache(1, 2, 64)
     qr = torch.randn((1, 8, 128), device="cuda")
